@@ -1,0 +1,302 @@
+/*
+ * fp64 CPU oracle for long-context single-token decode attention in Embla 1.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg call this code.  It shares nothing with the CUDA library:
+ * no headers, no helpers, no tables.  Inputs arrive as doubles (the bf16
+ * values the GPU reads, widened exactly); every sum is a plain loop in fp64
+ * in the order the definition states, with no blocking or reordering.
+ *
+ * Source: "The Architecture of Embla 1" (Sevren blog), sections
+ *   "Three kinds of attention"                     (window, full, sparse layers)
+ *   "Sevren Sparse Attention learns to be sparse"  (ReLU^2 weights over RMS-normalised q, k)
+ *   "Skipping V"                                   (a value is needed when any head of the group weighs its key)
+ *
+ * Readings of points the page leaves open (its display equation was lost):
+ *   - score  s_hj = alpha * (q_h / rms(q_h)) . (k_j / rms(k_j)),
+ *            rms(x) = sqrt(mean(x^2) + eps); alpha and eps are arguments;
+ *   - weight w_hj = max(s_hj, 0)^2;
+ *   - output out_h = sum_j w_hj v_j / (c + sum_j w_hj), c an argument;
+ *            0 when c + sum_j w_hj == 0;
+ *   - selection score sigma_j = max over the group's heads of s_hj, rounded to
+ *     fp32: survival (sigma_j > 0) and the top-k order are decided on that
+ *     fp32 value, the precision the CUDA kernels decide in;
+ *   - selection = the topk largest sigma_j among j < n - recent (ties to the
+ *     smaller j) plus the `recent` newest keys; every key when n <= topk+recent;
+ *   - sparse layer: softmax of tau * q'_h . k_j over the selected keys;
+ *   - window layer: RoPE on q at position pos (pairs (2i, 2i+1) rotated by
+ *     pos * base^(-2i/D)), keys stored already rotated, softmax of
+ *     tau * q_rot . k over the valid ring slots.
+ *
+ * Build: gcc -O2 -fPIC -shared -fopenmp -ffp-contract=off oracle.c -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* 1 / sqrt(mean(x^2) + eps) */
+static double rms_inverse(const double *x, int D, double eps) {
+  double ss = 0.0;
+  for (int d = 0; d < D; ++d) ss += x[d] * x[d];
+  return 1.0 / sqrt(ss / (double)D + eps);
+}
+
+static double dot(const double *a, const double *b, int D) {
+  double s = 0.0;
+  for (int d = 0; d < D; ++d) s += a[d] * b[d];
+  return s;
+}
+
+/*
+ * Full-layer scores of one (batch, KV-head) unit: s[h*n + j] = alpha * qhat_h . khat_j.
+ * q: G x D; K: n rows with stride ldk.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_full_scores(int G, int D, int64_t n, const double *q, const double *K, int64_t ldk,
+                       double alpha, double eps, double *s) {
+  if (G < 1 || D < 1 || n < 0 || ldk < D || !(eps >= 0.0)) return -1;
+  double *qhat = (double *)malloc(sizeof(double) * (size_t)G * (size_t)D);
+  double *khat = (double *)malloc(sizeof(double) * (size_t)D);
+  if (!qhat || !khat) { free(qhat); free(khat); return -1; }
+  for (int h = 0; h < G; ++h) {
+    double r = rms_inverse(q + (size_t)h * D, D, eps);
+    for (int d = 0; d < D; ++d) qhat[h * D + d] = q[(size_t)h * D + d] * r;
+  }
+  for (int64_t j = 0; j < n; ++j) {
+    const double *k = K + j * ldk;
+    double r = rms_inverse(k, D, eps);
+    for (int d = 0; d < D; ++d) khat[d] = k[d] * r;
+    for (int h = 0; h < G; ++h) s[(int64_t)h * n + j] = alpha * dot(qhat + h * D, khat, D);
+  }
+  free(qhat);
+  free(khat);
+  return 0;
+}
+
+/*
+ * Full (ReLU^2) layer decode for one unit.
+ *   out     : G x D
+ *   sigma32 : n selection scores (fp32), may be NULL
+ *   n_surv  : keys with sigma32 > 0 (their V rows are the only ones needed)
+ *   n_zero  : per head, keys with exactly zero weight (s_hj <= 0), may be NULL
+ */
+int oracle_full_decode(int G, int D, int64_t n, const double *q, const double *K, int64_t ldk,
+                       const double *V, int64_t ldv, double alpha, double c, double eps,
+                       double *out, float *sigma32, int64_t *n_surv, int64_t *n_zero) {
+  if (ldv < D) return -1;
+  double *s = (double *)malloc(sizeof(double) * (size_t)G * (size_t)(n > 0 ? n : 1));
+  double *num = (double *)calloc((size_t)G * (size_t)D, sizeof(double));
+  double *den = (double *)calloc((size_t)G, sizeof(double));
+  if (!s || !num || !den) { free(s); free(num); free(den); return -1; }
+  if (oracle_full_scores(G, D, n, q, K, ldk, alpha, eps, s) != 0) {
+    free(s); free(num); free(den);
+    return -1;
+  }
+  int64_t surv = 0;
+  if (n_zero) for (int h = 0; h < G; ++h) n_zero[h] = 0;
+  for (int64_t j = 0; j < n; ++j) {
+    double sigma = -INFINITY;
+    for (int h = 0; h < G; ++h) {
+      double shj = s[(int64_t)h * n + j];
+      if (shj > sigma) sigma = shj;
+      double w = shj > 0.0 ? shj * shj : 0.0;
+      if (w == 0.0) {
+        if (n_zero) n_zero[h] += 1;
+        continue;
+      }
+      const double *v = V + j * ldv;
+      for (int d = 0; d < D; ++d) num[h * D + d] += w * v[d];
+      den[h] += w;
+    }
+    float sig32 = (float)sigma;
+    if (sigma32) sigma32[j] = sig32;
+    if (sig32 > 0.0f) ++surv;
+  }
+  for (int h = 0; h < G; ++h) {
+    double z = c + den[h];
+    for (int d = 0; d < D; ++d) out[h * D + d] = (z != 0.0) ? num[h * D + d] / z : 0.0;
+  }
+  *n_surv = surv;
+  free(s); free(num); free(den);
+  return 0;
+}
+
+typedef struct { float s; int32_t j; } cand;
+
+/* higher score first; equal scores: smaller index first */
+static int cand_order(const void *a, const void *b) {
+  const cand *x = (const cand *)a, *y = (const cand *)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->j < y->j) ? -1 : (x->j > y->j);
+}
+
+/*
+ * Sparse-layer selection for one unit: the topk highest sigma32 among the
+ * candidates j < n - recent, plus the `recent` newest keys, ascending.
+ * idx needs min(n, topk + recent) entries.
+ */
+int oracle_select_topk(int64_t n, const float *sigma32, int64_t topk, int64_t recent, int32_t *idx,
+                       int64_t *count) {
+  if (n < 0 || topk < 0 || recent < 0 || n > INT32_MAX) return -1;
+  if (n <= topk + recent) {
+    for (int64_t j = 0; j < n; ++j) idx[j] = (int32_t)j;
+    *count = n;
+    return 0;
+  }
+  int64_t n_cand = n - recent;
+  cand *cs = (cand *)malloc(sizeof(cand) * (size_t)n_cand);
+  unsigned char *mark = (unsigned char *)calloc((size_t)n, 1);
+  if (!cs || !mark) { free(cs); free(mark); return -1; }
+  for (int64_t j = 0; j < n_cand; ++j) { cs[j].s = sigma32[j]; cs[j].j = (int32_t)j; }
+  qsort(cs, (size_t)n_cand, sizeof(cand), cand_order);
+  for (int64_t i = 0; i < topk; ++i) mark[cs[i].j] = 1;
+  for (int64_t j = n_cand; j < n; ++j) mark[j] = 1;
+  int64_t m = 0;
+  for (int64_t j = 0; j < n; ++j)
+    if (mark[j]) idx[m++] = (int32_t)j;
+  *count = m;
+  free(cs);
+  free(mark);
+  return 0;
+}
+
+/*
+ * Sparse-layer decode for one unit: softmax of tau * q'_h . k_j over the m
+ * selected keys idx[0..m), output G x D.
+ */
+int oracle_sparse_decode(int G, int D, int64_t m, const double *q, const double *K, int64_t ldk,
+                         const double *V, int64_t ldv, const int32_t *idx, double tau,
+                         double *out) {
+  if (G < 1 || D < 1 || m < 0 || ldk < D || ldv < D) return -1;
+  double *z = (double *)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+  if (!z) return -1;
+  for (int h = 0; h < G; ++h) {
+    const double *qh = q + (size_t)h * D;
+    double zmax = -INFINITY;
+    for (int64_t i = 0; i < m; ++i) {
+      z[i] = tau * dot(qh, K + (int64_t)idx[i] * ldk, D);
+      if (z[i] > zmax) zmax = z[i];
+    }
+    double denom = 0.0;
+    for (int64_t i = 0; i < m; ++i) { z[i] = exp(z[i] - zmax); denom += z[i]; }
+    for (int d = 0; d < D; ++d) out[(size_t)h * D + d] = 0.0;
+    for (int64_t i = 0; i < m; ++i) {
+      double p = z[i] / denom;
+      const double *v = V + (int64_t)idx[i] * ldv;
+      for (int d = 0; d < D; ++d) out[(size_t)h * D + d] += p * v[d];
+    }
+  }
+  free(z);
+  return 0;
+}
+
+/*
+ * Window-layer decode for one unit.  Kw, Vw: W ring slots (slot = position
+ * mod W), keys already rotated at their own positions.  The valid positions
+ * are max(0, pos-W+1) .. pos.  q is rotated at pos, then softmax attention.
+ */
+int oracle_window_decode(int G, int D, int64_t W, int64_t pos, const double *q, const double *Kw,
+                         const double *Vw, double base, double tau, double *out) {
+  if (G < 1 || D < 2 || (D & 1) || W < 1 || pos < 0) return -1;
+  double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+  double *z = (double *)malloc(sizeof(double) * (size_t)W);
+  int64_t *slot = (int64_t *)malloc(sizeof(int64_t) * (size_t)W);
+  if (!qr || !z || !slot) { free(qr); free(z); free(slot); return -1; }
+  int64_t first = pos - W + 1 > 0 ? pos - W + 1 : 0;
+  int64_t nv = 0;
+  for (int64_t p = first; p <= pos; ++p) slot[nv++] = p % W;
+  for (int h = 0; h < G; ++h) {
+    const double *qh = q + (size_t)h * D;
+    for (int i = 0; i < D / 2; ++i) {
+      double theta = (double)pos * pow(base, -2.0 * (double)i / (double)D);
+      double cs = cos(theta), sn = sin(theta);
+      qr[2 * i] = qh[2 * i] * cs - qh[2 * i + 1] * sn;
+      qr[2 * i + 1] = qh[2 * i] * sn + qh[2 * i + 1] * cs;
+    }
+    double zmax = -INFINITY;
+    for (int64_t i = 0; i < nv; ++i) {
+      z[i] = tau * dot(qr, Kw + slot[i] * D, D);
+      if (z[i] > zmax) zmax = z[i];
+    }
+    double denom = 0.0;
+    for (int64_t i = 0; i < nv; ++i) { z[i] = exp(z[i] - zmax); denom += z[i]; }
+    for (int d = 0; d < D; ++d) out[(size_t)h * D + d] = 0.0;
+    for (int64_t i = 0; i < nv; ++i) {
+      double p = z[i] / denom;
+      const double *v = Vw + slot[i] * D;
+      for (int d = 0; d < D; ++d) out[(size_t)h * D + d] += p * v[d];
+    }
+  }
+  free(qr); free(z); free(slot);
+  return 0;
+}
+
+/* ----------------------------------------------------------------------------
+ * Batched forms: every (b, g) unit of a batch, units spread over OpenMP
+ * threads.  Query head h belongs to KV head h / G with G = Hq / Hkv, so the
+ * G query rows of unit (b, g) are rows g*G .. g*G+G-1 of q[b].
+ * ------------------------------------------------------------------------- */
+
+int oracle_full_decode_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t ncap,
+                             const double *q, const double *K, const double *V, double alpha,
+                             double c, double eps, double *out, float *sigma32, int64_t *n_surv) {
+  if (B < 0 || Hkv < 1 || Hq % Hkv || ncap < n) return -1;
+  int G = Hq / Hkv;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+    int64_t b = u / Hkv, g = u % Hkv;
+    const double *qu = q + ((size_t)b * Hq + (size_t)g * G) * D;
+    const double *Ku = K + (size_t)u * ncap * D;
+    const double *Vu = V + (size_t)u * ncap * D;
+    double *ou = out + ((size_t)b * Hq + (size_t)g * G) * D;
+    float *su = sigma32 ? sigma32 + (size_t)u * ncap : NULL;
+    err |= oracle_full_decode(G, D, n, qu, Ku, D, Vu, D, alpha, c, eps, ou, su, n_surv + u, NULL) != 0;
+  }
+  return err ? -1 : 0;
+}
+
+int oracle_select_topk_batch(int B, int Hkv, int64_t n, int64_t ncap, const float *sigma32,
+                             int64_t topk, int64_t recent, int32_t *idx, int64_t idx_stride,
+                             int64_t *count) {
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u)
+    err |= oracle_select_topk(n, sigma32 + (size_t)u * ncap, topk, recent, idx + u * idx_stride,
+                              count + u) != 0;
+  return err ? -1 : 0;
+}
+
+int oracle_sparse_decode_batch(int B, int Hq, int Hkv, int D, int64_t ncap, const double *q,
+                               const double *K, const double *V, const int32_t *idx,
+                               int64_t idx_stride, const int64_t *count, double tau, double *out) {
+  if (B < 0 || Hkv < 1 || Hq % Hkv) return -1;
+  int G = Hq / Hkv;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+    int64_t b = u / Hkv, g = u % Hkv;
+    err |= oracle_sparse_decode(G, D, count[u], q + ((size_t)b * Hq + (size_t)g * G) * D,
+                                K + (size_t)u * ncap * D, D, V + (size_t)u * ncap * D, D,
+                                idx + u * idx_stride, tau,
+                                out + ((size_t)b * Hq + (size_t)g * G) * D) != 0;
+  }
+  return err ? -1 : 0;
+}
+
+int oracle_window_decode_batch(int B, int Hq, int Hkv, int D, int64_t W, int64_t pos,
+                               const double *q, const double *Kw, const double *Vw, double base,
+                               double tau, double *out) {
+  if (B < 0 || Hkv < 1 || Hq % Hkv) return -1;
+  int G = Hq / Hkv;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+    int64_t b = u / Hkv, g = u % Hkv;
+    err |= oracle_window_decode(G, D, W, pos, q + ((size_t)b * Hq + (size_t)g * G) * D,
+                                Kw + (size_t)u * W * D, Vw + (size_t)u * W * D, base, tau,
+                                out + ((size_t)b * Hq + (size_t)g * G) * D) != 0;
+  }
+  return err ? -1 : 0;
+}
