@@ -1,0 +1,176 @@
+/*
+ * embla_attn.h — C ABI for long-context single-token decode attention of the
+ * Embla 1 layer types, on one NVIDIA GB300 (sm_103a) GPU.
+ *
+ * The operations follow "The Architecture of Embla 1" (Sevren blog):
+ *   - full layer   : section "Sevren Sparse Attention learns to be sparse" and
+ *                    "Skipping V" — ReLU^2 weights over RMS-normalised query and
+ *                    key, value rows read only for keys some head of the KV
+ *                    group weighs above zero;
+ *   - selection    : section "Three kinds of attention" (Sparse) — the 1,024
+ *                    keys the full layer scored highest plus the 128 newest;
+ *   - sparse layer : same section — softmax over the selected rows of the full
+ *                    layer's cache, no position encoding;
+ *   - window layer : same section (Sliding window) — softmax over the newest
+ *                    128 keys with rotary position embedding.
+ *
+ * The page's display equation for the full layer was lost in extraction, so
+ * its score scale (alpha), the constant added to the normaliser (c) and the
+ * RMS epsilon (eps) are arguments.  With s = alpha * qhat . khat and
+ * w = max(s, 0)^2, the full layer returns sum_j w_j v_j / (c + sum_j w_j), and
+ * 0 where c + sum_j w_j == 0.
+ *
+ * Conventions shared by every call
+ *   - Layouts are dense row-major.  q: [B, Hq, D] bf16.  Caches: [B, Hkv,
+ *     cache_stride, D] bf16 (row j of unit (b, g) at ((b*Hkv + g)*cache_stride
+ *     + j)*D).  Query head h reads KV head h / G, G = Hq / Hkv.
+ *   - Every pointer argument except `shape` and `workspace_bytes`-sized host
+ *     values is a DEVICE pointer owned by the caller.  The library never
+ *     allocates, frees or synchronises; work is enqueued on `stream` (a
+ *     cudaStream_t; NULL means the legacy default stream).
+ *   - Arguments are validated on the host before any launch; a failed check
+ *     returns a status and enqueues nothing.  A launch failure returns
+ *     EMBLA_ERR_CUDA.  No call throws, traps or aborts.
+ *   - Device pointers must be 16-byte aligned.  head_dim must be 128;
+ *     G must be 4 or 8.
+ *   - `workspace` is caller-provided device scratch of at least the size the
+ *     matching *_workspace_size call returns for the same shape on the
+ *     current device.  Its contents need not be initialised and are not
+ *     meaningful after the call.  Calls that share a workspace must be
+ *     ordered on one stream.
+ */
+#ifndef EMBLA_ATTN_H
+#define EMBLA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EMBLA_OK = 0,
+  EMBLA_ERR_INVALID_ARG = 1,   /* a null pointer, bad size, misaligned pointer, bad scalar */
+  EMBLA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim != 128, G not in {4, 8} */
+  EMBLA_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_size result */
+  EMBLA_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+  EMBLA_ERR_DEVICE_CHECK = 5   /* a kernel recorded a failed device-side check */
+} embla_status;
+
+typedef struct {
+  int32_t batch;         /* B >= 0 */
+  int32_t n_q_heads;     /* Hq >= 1 */
+  int32_t n_kv_heads;    /* Hkv >= 1, Hq % Hkv == 0 */
+  int32_t head_dim;      /* D; 128 */
+  int64_t ctx_len;       /* n: keys in the cache, the current token is key n-1; 0 <= n < 2^31 */
+  int64_t cache_stride;  /* rows between consecutive (b, g) planes of K and V; >= n */
+} embla_shape;
+
+/* Text for a status code (static storage, never NULL). */
+const char *embla_status_string(embla_status status);
+
+/* Number of streaming multiprocessors the launches size their grids for (current device). */
+int embla_device_sm_count(void);
+
+/*
+ * Full (ReLU^2) layer decode — "Sevren Sparse Attention learns to be sparse",
+ * "Skipping V".
+ *   q          bf16 [B, Hq, D]              raw query (normalised inside)
+ *   k_cache    bf16 [B, Hkv, cache_stride, D]
+ *   v_cache    bf16 [B, Hkv, cache_stride, D]; only rows of surviving keys are read
+ *   alpha      score scale, finite and > 0
+ *   c          normaliser constant, finite and >= 0
+ *   eps        RMS epsilon, finite and >= 0 (eps == 0 with an all-zero row gives NaN)
+ *   out        fp32 [B, Hq, D]
+ *   n_surv     int32 [B, Hkv]: keys j < n with max over the group of s_hj > 0
+ *   sel_scores fp32 [B, Hkv, cache_stride] or NULL: sigma_j = max over the
+ *              group's heads of s_hj for j < n (the selection score); rows
+ *              >= n are not written
+ *   sel_hist   uint32 [B, Hkv, 2048], required iff sel_scores != NULL:
+ *              per unit, how many keys j < n fall in each of 2048 bins of the
+ *              order-preserving 32-bit form of sigma_j (its top 11 bits).
+ *              Zeroed and filled by this call; embla_select_topk reads it.
+ */
+size_t embla_full_decode_workspace_size(const embla_shape *shape);
+embla_status embla_full_decode(const embla_shape *shape, const void *q, const void *k_cache,
+                               const void *v_cache, float alpha, float c, float eps, float *out,
+                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Sparse-layer selection — "Three kinds of attention" (Sparse): the `topk`
+ * keys with the highest sel_scores among j < n - recent (equal scores: the
+ * smaller index first) together with the `recent` newest keys n-recent..n-1;
+ * every key when n <= topk + recent.
+ *   sel_scores, sel_hist  as written by embla_full_decode for the same shape
+ *   topk, recent          >= 0 (1024 and 128 in Embla 1)
+ *   idx        int32 [B, Hkv, idx_stride], idx_stride >= topk + recent:
+ *              selected key indices in ascending order; entries at and past
+ *              count[b, g] are not written
+ *   count      int32 [B, Hkv] = min(n, topk + recent)
+ */
+size_t embla_select_topk_workspace_size(const embla_shape *shape, int32_t topk, int32_t recent);
+embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores,
+                               const uint32_t *sel_hist, int32_t topk, int32_t recent,
+                               int32_t *idx, int32_t idx_stride, int32_t *count, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * Sparse-layer decode — "Three kinds of attention" (Sparse): for every query
+ * head, softmax of tau * q_h . k_j over the selected keys of its KV head
+ * (no normalisation, no position), then the weighted sum of their values.
+ *   q          bf16 [B, Hq, D]   this sparse layer's own query
+ *   k_cache, v_cache   the full layer's caches, as for embla_full_decode
+ *   idx        int32 [B, Hkv, idx_stride]; the first count[b, g] entries are
+ *              read and must lie in [0, n); an entry outside is skipped and
+ *              recorded (see embla_device_check)
+ *   count      int32 [B, Hkv], each in [0, idx_stride]; a unit with count 0
+ *              gets a zero output
+ *   tau        softmax scale, finite
+ *   out        fp32 [B, Hq, D]
+ */
+size_t embla_sparse_decode_workspace_size(const embla_shape *shape, int32_t idx_stride);
+embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *idx, int32_t idx_stride,
+                                 const int32_t *count, float tau, float *out, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Window-layer decode — "Three kinds of attention" (Sliding window).
+ *   q          bf16 [B, Hq, D]   raw query; rotated here at position pos:
+ *              pair (2i, 2i+1) turned by pos * rope_base^(-2i/D)
+ *   k_win      bf16 [B, Hkv, window, D] ring: position p lives in slot
+ *              p % window and was rotated at p when it was written
+ *   v_win      bf16 [B, Hkv, window, D] ring, same slots
+ *   window     ring size, 1..1024 (128 in Embla 1)
+ *   pos        position of the current token (>= 0); the valid positions are
+ *              max(0, pos-window+1) .. pos
+ *   rope_base  > 0 (10000 in the workloads here)
+ *   tau        softmax scale, finite
+ *   out        fp32 [B, Hq, D]
+ * shape->ctx_len and shape->cache_stride are not used by this call.
+ */
+size_t embla_window_decode_workspace_size(const embla_shape *shape, int32_t window);
+embla_status embla_window_decode(const embla_shape *shape, const void *q, const void *k_win,
+                                 const void *v_win, int32_t window, int64_t pos, float rope_base,
+                                 float tau, float *out, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/*
+ * Device-side check word.  Kernels record failed checks (an index outside
+ * [0, n) handed to embla_sparse_decode, a pipeline wait that exceeded its
+ * time limit) by OR-ing flag bits into a word in device memory instead of
+ * trapping.  This call synchronises `stream`, copies the word to *flags and,
+ * if `clear` is non-zero, resets it.  Returns EMBLA_ERR_DEVICE_CHECK when any
+ * flag was set, EMBLA_OK otherwise.
+ *   bit 0  index out of range (sparse decode)
+ *   bit 1  pipeline wait timed out (full decode)
+ */
+embla_status embla_device_check(uint32_t *flags, int clear, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EMBLA_ATTN_H */

@@ -1,0 +1,230 @@
+"""Python binding of libembla_attn.so: decode attention for the Embla 1 layer types
+on one GB300 (sm_103a).
+
+Argument marshalling only.  Every function here checks tensor dtypes, devices and
+contiguity, then calls the C entry point of the same name with raw device pointers and
+the current CUDA stream; all arithmetic runs in the library's CUDA kernels.  There is
+no CPU path: if the library was not built, importing the binding's functions raises.
+
+Tensors (torch, on the current CUDA device, C-contiguous):
+  q              bf16  [B, Hq, D]
+  k_cache/v_cache bf16 [B, Hkv, cache_stride, D]
+  out            fp32  [B, Hq, D]
+  n_surv, count  int32 [B, Hkv]
+  sel_scores     fp32  [B, Hkv, cache_stride]
+  sel_hist       int32 [B, Hkv, 2048]  (holds uint32 counts)
+  idx            int32 [B, Hkv, idx_stride]
+  workspace      uint8 (any shape), at least the *_workspace_size result
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libembla_attn.so")
+HIST_BINS = 2048
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
+          4: "CUDA error", 5: "device-side check failed"}
+
+
+class EmblaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("ctx_len", ctypes.c_int64), ("cache_stride", ctypes.c_int64)]
+
+
+@dataclass(frozen=True)
+class Shape:
+    batch: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ctx_len: int
+    cache_stride: int
+
+    def c(self) -> _Shape:
+        return _Shape(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim, self.ctx_len,
+                      self.cache_stride)
+
+    @property
+    def units(self) -> int:
+        return self.batch * self.n_kv_heads
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load libembla_attn.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run relu_sparse_kv_gb300.build.build() "
+                               "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz, vp = (ctypes.POINTER(_Shape), ctypes.c_int32, ctypes.c_int64,
+                                    ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p)
+        sigs = {
+            "embla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "embla_device_sm_count": (ctypes.c_int, []),
+            "embla_full_decode_workspace_size": (sz, [P]),
+            "embla_full_decode": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32, vp, vp, vp, vp, vp,
+                                                 sz, vp]),
+            "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
+            "embla_select_topk": (ctypes.c_int, [P, vp, vp, i32, i32, vp, i32, vp, vp, sz, vp]),
+            "embla_sparse_decode_workspace_size": (sz, [P, i32]),
+            "embla_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, vp, i32, vp, f32, vp, vp, sz,
+                                                   vp]),
+            "embla_window_decode_workspace_size": (sz, [P, i32]),
+            "embla_window_decode": (ctypes.c_int, [P, vp, vp, vp, i32, i64, f32, f32, vp, vp, sz,
+                                                   vp]),
+            "embla_device_check": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
+                                                  vp]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(t, dtype, shape, name, allow_none=False):
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _call(name, *args):
+    st = getattr(library(), name)(*args)
+    if st != 0:
+        raise EmblaError(name, st)
+
+
+def _workspace(nbytes: int, workspace, device):
+    if workspace is None:
+        return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise EmblaError("workspace", 3)
+    return workspace
+
+
+# ----------------------------------------------------------------------------- sizes
+
+def embla_full_decode_workspace_size(shape: Shape) -> int:
+    return library().embla_full_decode_workspace_size(ctypes.byref(shape.c()))
+
+
+def embla_select_topk_workspace_size(shape: Shape, topk: int = 1024, recent: int = 128) -> int:
+    return library().embla_select_topk_workspace_size(ctypes.byref(shape.c()), topk, recent)
+
+
+def embla_sparse_decode_workspace_size(shape: Shape, idx_stride: int) -> int:
+    return library().embla_sparse_decode_workspace_size(ctypes.byref(shape.c()), idx_stride)
+
+
+def embla_device_sm_count() -> int:
+    return library().embla_device_sm_count()
+
+
+# ----------------------------------------------------------------------------- calls
+
+def embla_full_decode(shape: Shape, q, k_cache, v_cache, out, n_surv, sel_scores=None,
+                      sel_hist=None, alpha: float = 1.0, c: float = 1.0, eps: float = 1e-6,
+                      workspace=None, stream=None):
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    _check(n_surv, torch.int32, (B, Hkv), "n_surv")
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores", allow_none=True)
+    _check(sel_hist, torch.int32, (B, Hkv, HIST_BINS), "sel_hist", allow_none=True)
+    ws = _workspace(embla_full_decode_workspace_size(shape), workspace, q.device)
+    _call("embla_full_decode", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          alpha, c, eps, _ptr(out), _ptr(n_surv), _ptr(sel_scores), _ptr(sel_hist), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_select_topk(shape: Shape, sel_scores, sel_hist, idx, count, topk: int = 1024,
+                      recent: int = 128, workspace=None, stream=None):
+    B, Hkv, ncap = shape.batch, shape.n_kv_heads, shape.cache_stride
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores")
+    _check(sel_hist, torch.int32, (B, Hkv, HIST_BINS), "sel_hist")
+    _check(idx, torch.int32, None, "idx")
+    if idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hkv):
+        raise ValueError("idx must be [B, Hkv, idx_stride]")
+    _check(count, torch.int32, (B, Hkv), "count")
+    ws = _workspace(embla_select_topk_workspace_size(shape, topk, recent), workspace,
+                    sel_scores.device)
+    _call("embla_select_topk", ctypes.byref(shape.c()), _ptr(sel_scores), _ptr(sel_hist), topk,
+          recent, _ptr(idx), idx.shape[2], _ptr(count), _ptr(ws), ws.numel() * ws.element_size(),
+          _stream(stream))
+
+
+def embla_sparse_decode(shape: Shape, q, k_cache, v_cache, idx, count, out, tau: float | None = None,
+                        workspace=None, stream=None):
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(idx, torch.int32, None, "idx")
+    if idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hkv):
+        raise ValueError("idx must be [B, Hkv, idx_stride]")
+    _check(count, torch.int32, (B, Hkv), "count")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    tau = D ** -0.5 if tau is None else tau
+    ws = _workspace(embla_sparse_decode_workspace_size(shape, idx.shape[2]), workspace, q.device)
+    _call("embla_sparse_decode", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          _ptr(idx), idx.shape[2], _ptr(count), tau, _ptr(out), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_window_decode(shape: Shape, q, k_win, v_win, pos: int, out, window: int = 128,
+                        rope_base: float = 10000.0, tau: float | None = None, stream=None):
+    B, Hq, Hkv, D = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_win, torch.bfloat16, (B, Hkv, window, D), "k_win")
+    _check(v_win, torch.bfloat16, (B, Hkv, window, D), "v_win")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    tau = D ** -0.5 if tau is None else tau
+    _call("embla_window_decode", ctypes.byref(shape.c()), _ptr(q), _ptr(k_win), _ptr(v_win),
+          window, pos, rope_base, tau, _ptr(out), None, 0, _stream(stream))
+
+
+def embla_device_check(clear: bool = True, stream=None) -> int:
+    """Synchronise and return the device-side check flags (bit 0: index range, bit 1: wait timeout)."""
+    flags = ctypes.c_uint32(0)
+    library().embla_device_check(ctypes.byref(flags), 1 if clear else 0, _stream(stream))
+    return flags.value

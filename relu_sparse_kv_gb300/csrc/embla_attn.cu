@@ -1,0 +1,282 @@
+// C ABI of the library: host-side argument checks, workspace sizing, TMA descriptor
+// encoding and the launches of the kernels in this directory.  Declarations and the
+// meaning of every argument are in include/embla_attn.h.
+#include <cstring>
+#include <mutex>
+
+#include "embla_attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+using namespace embla;
+
+namespace {
+
+// Device-side check word (flag bits, see embla_device_check).
+__device__ uint32_t g_check_flags;
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+int sm_count_of(int dev) {
+  static int cache[kMaxDevices] = {0};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+uint32_t *flags_ptr() {
+  static uint32_t *cache[kMaxDevices] = {nullptr};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cache[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_check_flags) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t *>(p);
+  }
+  return cache[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, 128] with 256-byte rows, boxes of {64 columns, box_rows}, 128B swizzle.
+bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows,
+                 CUtensorMapL2promotion promo) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite(float x) { return x == x && x - x == 0.0f; }
+
+// Common shape checks; sets *G.  ctx_checks: also validate ctx_len / cache_stride.
+embla_status check_shape(const embla_shape *s, int *G, bool ctx_checks) {
+  if (!s) return EMBLA_ERR_INVALID_ARG;
+  if (s->batch < 0 || s->n_q_heads < 1 || s->n_kv_heads < 1) return EMBLA_ERR_INVALID_ARG;
+  if (s->n_q_heads % s->n_kv_heads) return EMBLA_ERR_INVALID_ARG;
+  if (s->head_dim < 1) return EMBLA_ERR_INVALID_ARG;
+  if (ctx_checks) {
+    if (s->ctx_len < 0 || s->ctx_len > INT32_MAX) return EMBLA_ERR_INVALID_ARG;
+    if (s->cache_stride < s->ctx_len) return EMBLA_ERR_INVALID_ARG;
+  }
+  *G = s->n_q_heads / s->n_kv_heads;
+  if (s->head_dim != kHeadDim) return EMBLA_ERR_UNSUPPORTED;
+  if (*G != 4 && *G != 8) return EMBLA_ERR_UNSUPPORTED;
+  return EMBLA_OK;
+}
+
+embla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EMBLA_OK : EMBLA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *embla_status_string(embla_status status) {
+  switch (status) {
+    case EMBLA_OK: return "ok";
+    case EMBLA_ERR_INVALID_ARG: return "invalid argument";
+    case EMBLA_ERR_UNSUPPORTED: return "unsupported shape (head_dim must be 128, G in {4, 8})";
+    case EMBLA_ERR_WORKSPACE: return "workspace too small";
+    case EMBLA_ERR_CUDA: return "CUDA error";
+    case EMBLA_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+int embla_device_sm_count(void) { return sm_count_of(current_device()); }
+
+size_t embla_full_decode_workspace_size(const embla_shape *shape) {
+  int G = 0;
+  if (check_shape(shape, &G, true) != EMBLA_OK) return 0;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return 0;
+  return full_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_kv_heads, G, sms);
+}
+
+embla_status embla_full_decode(const embla_shape *shape, const void *q, const void *k_cache,
+                               const void *v_cache, float alpha, float c, float eps, float *out,
+                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  if (!(finite(alpha) && alpha > 0.0f) || !(finite(c) && c >= 0.0f) ||
+      !(finite(eps) && eps >= 0.0f))
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!q || !k_cache || !v_cache || !out || !n_surv || !workspace) return EMBLA_ERR_INVALID_ARG;
+  if ((sel_scores == nullptr) != (sel_hist == nullptr)) return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace) || (sel_scores && (!aligned16(sel_scores) || !aligned16(sel_hist))))
+    return EMBLA_ERR_INVALID_ARG;
+  // TMA row coordinates are 32-bit
+  if (units * shape->cache_stride + kTileKeys > INT32_MAX) return EMBLA_ERR_UNSUPPORTED;
+  const int dev = current_device();
+  const int sms = sm_count_of(dev);
+  if (sms <= 0) return EMBLA_ERR_CUDA;
+  if (workspace_bytes < full_workspace_bytes(units, G, sms)) return EMBLA_ERR_WORKSPACE;
+  uint32_t *flags = flags_ptr();
+  if (!flags) return EMBLA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const FullSplit sp = full_split(units, shape->ctx_len, sms);
+  if (sel_scores) {
+    st = cuda_status(cudaMemsetAsync(sel_hist, 0, static_cast<size_t>(units) * kHistBins * 4, s));
+    if (st != EMBLA_OK) return st;
+  }
+  if (sp.tiles > 0) {
+    CUtensorMap tm_k, tm_q;
+    if (!encode_rows(&tm_k, k_cache, static_cast<uint64_t>(units * shape->cache_stride),
+                     kTileKeys, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+        !encode_rows(&tm_q, q, static_cast<uint64_t>(shape->batch) * shape->n_q_heads,
+                     static_cast<uint32_t>(G), CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      return EMBLA_ERR_CUDA;
+    st = cuda_status(launch_full_decode(G, tm_k, tm_q, v_cache, sel_scores, sel_hist,
+                                        static_cast<float *>(workspace), flags, sp,
+                                        shape->ctx_len, shape->cache_stride, shape->n_q_heads,
+                                        shape->n_kv_heads, alpha, eps, s));
+    if (st != EMBLA_OK) return st;
+  }
+  return cuda_status(launch_full_combine(G, static_cast<const float *>(workspace), sp, c, out,
+                                         n_surv, s));
+}
+
+size_t embla_select_topk_workspace_size(const embla_shape *shape, int32_t topk, int32_t recent) {
+  int G = 0;
+  if (check_shape(shape, &G, true) != EMBLA_OK || topk < 0 || recent < 0) return 0;
+  return select_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_kv_heads,
+                                shape->ctx_len);
+}
+
+embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores,
+                               const uint32_t *sel_hist, int32_t topk, int32_t recent,
+                               int32_t *idx, int32_t idx_stride, int32_t *count, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  if (topk < 0 || recent < 0 || static_cast<int64_t>(topk) + recent > INT32_MAX ||
+      idx_stride < topk + recent)
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!sel_scores || !sel_hist || !idx || !count || !workspace) return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(sel_scores) || !aligned16(sel_hist) || !aligned16(idx) || !aligned16(count) ||
+      !aligned16(workspace))
+    return EMBLA_ERR_INVALID_ARG;
+  if (workspace_bytes < select_workspace_bytes(units, shape->ctx_len)) return EMBLA_ERR_WORKSPACE;
+  return cuda_status(launch_select(sel_scores, sel_hist, units, shape->ctx_len,
+                                   shape->cache_stride, topk, recent, idx, idx_stride, count,
+                                   workspace, static_cast<cudaStream_t>(stream)));
+}
+
+size_t embla_sparse_decode_workspace_size(const embla_shape *shape, int32_t idx_stride) {
+  int G = 0;
+  if (check_shape(shape, &G, true) != EMBLA_OK || idx_stride < 0) return 0;
+  return sparse_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_kv_heads, G,
+                                idx_stride);
+}
+
+embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *idx, int32_t idx_stride,
+                                 const int32_t *count, float tau, float *out, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  if (!finite(tau) || idx_stride < 0) return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!q || !k_cache || !v_cache || !idx || !count || !out || !workspace)
+    return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace) || !aligned16(idx) || !aligned16(count))
+    return EMBLA_ERR_INVALID_ARG;
+  if (workspace_bytes < sparse_workspace_bytes(units, G, idx_stride)) return EMBLA_ERR_WORKSPACE;
+  uint32_t *flags = flags_ptr();
+  if (!flags) return EMBLA_ERR_CUDA;
+  return cuda_status(launch_sparse_decode(G, q, k_cache, v_cache, idx, idx_stride, count, units,
+                                          shape->n_kv_heads, shape->ctx_len, shape->cache_stride,
+                                          tau, out, workspace, flags,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t embla_window_decode_workspace_size(const embla_shape *shape, int32_t window) {
+  (void)shape;
+  (void)window;
+  return 0;
+}
+
+embla_status embla_window_decode(const embla_shape *shape, const void *q, const void *k_win,
+                                 const void *v_win, int32_t window, int64_t pos, float rope_base,
+                                 float tau, float *out, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  int G = 0;
+  embla_status st = check_shape(shape, &G, false);
+  if (st != EMBLA_OK) return st;
+  if (window < 1 || window > 1024 || pos < 0 || !(finite(rope_base) && rope_base > 0.0f) ||
+      !finite(tau))
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!q || !k_win || !v_win || !out) return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_win) || !aligned16(v_win) || !aligned16(out))
+    return EMBLA_ERR_INVALID_ARG;
+  return cuda_status(launch_window_decode(G, q, k_win, v_win, units, window, pos, rope_base, tau,
+                                          out, static_cast<cudaStream_t>(stream)));
+}
+
+embla_status embla_device_check(uint32_t *flags, int clear, void *stream) {
+  uint32_t *d = flags_ptr();
+  if (!d || !flags) return d ? EMBLA_ERR_INVALID_ARG : EMBLA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, d, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return EMBLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return EMBLA_ERR_CUDA;
+  if (clear && v) {
+    if (cudaMemsetAsync(d, 0, sizeof(uint32_t), s) != cudaSuccess) return EMBLA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return EMBLA_ERR_CUDA;
+  }
+  *flags = v;
+  return v ? EMBLA_ERR_DEVICE_CHECK : EMBLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Launchers shared between the translation units of the library (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace embla {
+
+constexpr int kHeadDim = 128;
+constexpr int kTileKeys = 128;     // keys per full-decode tile (the MMA's M)
+constexpr int kHistBins = 2048;    // selection histogram: top 11 bits of the order key
+
+// Work split of the full-layer decode: T tiles (TU per unit) over P persistent CTAs,
+// CTA c owning tiles [floor(c*T/P), floor((c+1)*T/P)).  The partial record of the
+// stretch of unit u that CTA c handles lives in slot c + u.
+struct FullSplit {
+  int64_t units;      // B * Hkv
+  int64_t tiles_per_unit;
+  int64_t tiles;      // units * tiles_per_unit
+  int32_t ctas;       // P
+};
+
+__host__ __device__ inline int64_t split_first_tile(int64_t c, int64_t T, int64_t P) {
+  return (c * T) / P;
+}
+// The CTA whose range holds tile t.
+__host__ __device__ inline int64_t split_cta_of_tile(int64_t t, int64_t T, int64_t P) {
+  return ((t + 1) * P - 1) / T;
+}
+
+FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count);
+int full_record_floats(int G);
+size_t full_workspace_bytes(int64_t units, int G, int sm_count);
+
+cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
+                               const void *v_cache, float *sel_scores, uint32_t *sel_hist,
+                               float *records, uint32_t *flags, const FullSplit &sp, int64_t n,
+                               int64_t ncap, int Hq, int Hkv, float alpha, float eps,
+                               cudaStream_t stream);
+cudaError_t launch_full_combine(int G, const float *records, const FullSplit &sp, float c,
+                                float *out, int32_t *n_surv, cudaStream_t stream);
+
+size_t select_workspace_bytes(int64_t units, int64_t ctx_len);
+cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int64_t units,
+                          int64_t n, int64_t ncap, int topk, int recent, int32_t *idx,
+                          int idx_stride, int32_t *count, void *workspace, cudaStream_t stream);
+
+size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride);
+cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *idx, int idx_stride, const int32_t *count,
+                                 int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
+                                 float *out, void *workspace, uint32_t *flags, cudaStream_t stream);
+
+cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const void *v_win,
+                                 int64_t units, int window, int64_t pos, float rope_base,
+                                 float tau, float *out, cudaStream_t stream);
+
+}  // namespace embla

@@ -1,0 +1,153 @@
+"""CPU-side checks of the C ABI: the library loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments before touching the device.  Also the host-side
+work split of the full-layer decode, compiled from its header with g++."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import relu_sparse_kv_gb300 as E
+from relu_sparse_kv_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "embla_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return E.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(embla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    out = subprocess.run(["nm", "-D", "--defined-only", E.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (embla_[a-z0-9_]+)", out))
+    assert set(names) <= exported, set(names) - exported
+    for n in names:
+        getattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.embla_status_string(code)
+    assert lib.embla_status_string(99) == b"unknown status"
+
+
+def _shape(**kw):
+    d = dict(batch=1, n_q_heads=16, n_kv_heads=4, head_dim=128, ctx_len=4096, cache_stride=4096)
+    d.update(kw)
+    return E._Shape(**d)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), 2),              # unsupported head_dim
+    (dict(n_q_heads=12, n_kv_heads=4), 2),  # G = 3
+    (dict(n_q_heads=16, n_kv_heads=3), 1),  # Hq % Hkv != 0
+    (dict(cache_stride=100), 1),         # stride < n
+    (dict(ctx_len=-1), 1),
+    (dict(batch=-1), 1),
+])
+def test_shape_validation_without_gpu(lib, kw, status):
+    s = _shape(**kw)
+    st = lib.embla_full_decode(ctypes.byref(s), None, None, None, 1.0, 1.0, 1e-6, None, None,
+                               None, None, None, 0, None)
+    assert st == status
+
+
+def test_scalar_and_pointer_validation_without_gpu(lib):
+    s = _shape()
+    f = lib.embla_full_decode
+    assert f(None, None, None, None, 1.0, 1.0, 1e-6, None, None, None, None, None, 0, None) == 1
+    assert f(ctypes.byref(s), None, None, None, -1.0, 1.0, 1e-6, None, None, None, None, None, 0, None) == 1
+    assert f(ctypes.byref(s), None, None, None, 1.0, -1.0, 1e-6, None, None, None, None, None, 0, None) == 1
+    assert f(ctypes.byref(s), None, None, None, 1.0, 1.0, float("nan"), None, None, None, None, None, 0, None) == 1
+    assert f(ctypes.byref(s), None, None, None, 1.0, 1.0, 1e-6, None, None, None, None, None, 0, None) == 1
+    sel = lib.embla_select_topk
+    assert sel(ctypes.byref(s), None, None, 1024, 128, None, 1000, None, None, 0, None) == 1  # stride
+    assert sel(ctypes.byref(s), None, None, -1, 128, None, 1152, None, None, 0, None) == 1
+    sp = lib.embla_sparse_decode
+    assert sp(ctypes.byref(s), None, None, None, None, 1152, None, float("inf"), None, None, 0, None) == 1
+    w = lib.embla_window_decode
+    assert w(ctypes.byref(s), None, None, None, 0, 5, 10000.0, 0.1, None, None, 0, None) == 1
+    assert w(ctypes.byref(s), None, None, None, 128, -1, 10000.0, 0.1, None, None, 0, None) == 1
+    assert w(ctypes.byref(s), None, None, None, 128, 5, 0.0, 0.1, None, None, 0, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    s = _shape(batch=0)
+    assert lib.embla_full_decode(ctypes.byref(s), None, None, None, 1.0, 1.0, 1e-6, None, None,
+                                 None, None, None, 0, None) == 0
+    assert lib.embla_sparse_decode(ctypes.byref(s), None, None, None, None, 1152, None, 0.1,
+                                   None, None, 0, None) == 0
+
+
+HARNESS = r"""
+#include <cstdio>
+#include "internal.h"
+using namespace embla;
+int main() {
+  // every tile belongs to exactly one CTA; the stretch of unit u held by CTA c uses
+  // slot c+u, which no other (CTA, unit) pair uses; the combine's [c0, c1] range
+  // lists exactly the CTAs that touched u
+  for (int sms = 1; sms <= 20; ++sms)
+    for (long units = 1; units <= 9; ++units)
+      for (long n = 0; n <= 1300; n += 97) {
+        FullSplit sp = full_split(units, n, sms);
+        long T = sp.tiles, P = sp.ctas;
+        if (T == 0) { if (P != 0) return 1; continue; }
+        if (P < 1 || P > T || P > sms) return 2;
+        static int owner[100000];
+        static int slot_user[200];
+        for (int i = 0; i < 200; ++i) slot_user[i] = -1;
+        for (long c = 0; c < P; ++c) {
+          long b = split_first_tile(c, T, P), e = split_first_tile(c + 1, T, P);
+          if (e <= b) return 3;
+          for (long t = b; t < e; ++t) {
+            owner[t] = (int)c;
+            if (split_cta_of_tile(t, T, P) != c) return 4;
+            long u = t / sp.tiles_per_unit, slot = c + u;
+            if (slot >= P + units) return 5;
+            if (slot_user[slot] != -1 && slot_user[slot] != (int)(c * 1000 + u)) return 6;
+            slot_user[slot] = (int)(c * 1000 + u);
+          }
+        }
+        if (split_first_tile(P, T, P) != T) return 7;
+        for (long u = 0; u < units; ++u) {
+          long c0 = split_cta_of_tile(u * sp.tiles_per_unit, T, P);
+          long c1 = split_cta_of_tile(u * sp.tiles_per_unit + sp.tiles_per_unit - 1, T, P);
+          for (long c = 0; c < P; ++c) {
+            long b = split_first_tile(c, T, P), e = split_first_tile(c + 1, T, P);
+            bool touches = b < (u + 1) * sp.tiles_per_unit && e > u * sp.tiles_per_unit;
+            if (touches != (c >= c0 && c <= c1)) return 8;
+          }
+        }
+      }
+  std::puts("ok");
+  return 0;
+}
+"""
+
+
+def test_full_decode_work_split_host_logic(tmp_path):
+    src = tmp_path / "split.cpp"
+    src.write_text(HARNESS)
+    exe = tmp_path / "split"
+    cuda_inc = "/usr/local/cuda/include"
+    r = subprocess.run(["g++", "-std=c++17", "-O1", "-I" + B.CSRC, "-I" + cuda_inc, str(src),
+                        os.path.join(B.BUILD, "full_decode.o"), "-o", str(exe),
+                        "-L/usr/local/cuda/lib64", "-lcudart_static", "-ldl", "-lpthread",
+                        "-lrt"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout)

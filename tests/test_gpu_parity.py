@@ -1,0 +1,187 @@
+"""GPU parity against the fp64 oracle, through the C ABI.
+
+Bars: surviving-key counts and selected index sets bit-exact; outputs within
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle| (bf16 inputs, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import relu_sparse_kv_gb300 as E
+from helpers import FullRun, assert_close, order_key_np, to_dev
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def _layer(B, Hq, Hkv, n, pattern="subset", frac=0.05, n_cap=None, seed=1, sparse=(1,)):
+    return gen.make_full_layer(seed=seed, layer=0, B=B, Hq=Hq, Hkv=Hkv, D=D, n=n,
+                               pattern=pattern, frac=frac, n_cap=n_cap, sparse_layers=sparse)
+
+
+def _check_full(fl, run, alpha=1.0, c=1.0, eps=1e-6):
+    ref_out, ref_sig, ref_ns = oracle.full_decode_batch(fl.q, fl.K, fl.V, fl.n, alpha=alpha, c=c,
+                                                        eps=eps)
+    ns = run.n_surv.cpu().numpy()
+    assert np.array_equal(ns, ref_ns), (ns, ref_ns)
+    assert np.array_equal(ns, fl.n_pos)
+    assert_close(run.out.cpu().numpy(), ref_out)
+    sel = run.sel.cpu().numpy()[:, :, :fl.n]
+    assert_close(sel, ref_sig[:, :, :fl.n], atol=1e-4 * max(alpha, 1e-3), rtol=1e-5, what="sigma")
+    assert np.array_equal(sel > 0, ref_sig[:, :, :fl.n] > 0)
+    # histogram: counts of the top 11 bits of the GPU's own scores
+    hist = run.hist.cpu().numpy().view(np.uint32)
+    for b in range(sel.shape[0]):
+        for g in range(sel.shape[1]):
+            expect = np.bincount(order_key_np(sel[b, g]) >> 21, minlength=E.HIST_BINS)
+            assert np.array_equal(hist[b, g], expect)
+    return ref_sig
+
+
+@pytest.mark.parametrize("n", [1, 7, 127, 128, 129, 1000, 1152, 1153, 2048, 4099])
+def test_full_and_select_small_contexts(n):
+    fl = _layer(2, 16, 4, n, pattern="bernoulli", frac=0.3)
+    run = FullRun(fl)
+    ref_sig = _check_full(fl, run)
+    ref_idx, ref_cnt = oracle.select_topk_batch(ref_sig, fl.n)
+    cnt = run.count.cpu().numpy()
+    assert np.array_equal(cnt, ref_cnt)
+    idx = run.idx.cpu().numpy()
+    for b in range(2):
+        for g in range(4):
+            assert np.array_equal(idx[b, g, :cnt[b, g]], ref_idx[b, g, :ref_cnt[b, g]])
+    ref_sp = oracle.sparse_decode_batch(fl.sparse_q[0], fl.K, fl.V, ref_idx, ref_cnt)
+    assert_close(run.sparse(fl.sparse_q[0]), ref_sp)
+
+
+@pytest.mark.parametrize("G", [4, 8])
+@pytest.mark.parametrize("alpha,c", [(1.0, 1.0), (1.0, 0.0), (1.0 / 128, 1.0), (1.0 / 128, 0.0)])
+def test_full_scalars_and_group_sizes(G, alpha, c):
+    Hkv = 2 if G == 8 else 4
+    fl = _layer(3, G * Hkv, Hkv, 3000, pattern="subset", frac=0.2, seed=5)
+    run = FullRun(fl, alpha=alpha, c=c)
+    _check_full(fl, run, alpha=alpha, c=c)
+
+
+def test_padding_rows_past_context_are_never_read():
+    # rows n..n_cap-1 of K and V hold NaN; none may reach any output
+    fl = _layer(2, 16, 4, 2500, pattern="subset", frac=0.1, n_cap=2700, seed=7)
+    run = FullRun(fl)
+    ref_sig = _check_full(fl, run)
+    assert np.isfinite(run.out.cpu().numpy()).all()
+    ref_idx, ref_cnt = oracle.select_topk_batch(ref_sig, fl.n)
+    assert np.array_equal(run.idx.cpu().numpy(), ref_idx)
+
+
+@pytest.mark.parametrize("B,n", [(1, 64 * 128), (5, 3 * 128 + 5), (40, 300)])
+def test_full_many_units_and_split_boundaries(B, n):
+    # shapes whose tiles split across CTAs at unit boundaries in different ways
+    fl = _layer(B, 16, 4, n, pattern="runs" if n > 2000 else "subset", frac=0.05, seed=B)
+    run = FullRun(fl)
+    _check_full(fl, run)
+
+
+def test_zero_context_gives_zero_output():
+    B, Hq, Hkv = 2, 16, 4
+    shape = E.Shape(B, Hq, Hkv, D, 0, 16)
+    q = torch.randn(B, Hq, D, device="cuda").to(torch.bfloat16)
+    K = torch.zeros(B, Hkv, 16, D, device="cuda", dtype=torch.bfloat16)
+    out = torch.full((B, Hq, D), 7.0, device="cuda")
+    ns = torch.full((B, Hkv), 9, dtype=torch.int32, device="cuda")
+    E.embla_full_decode(shape, q, K, K, out, ns)
+    torch.cuda.synchronize()
+    assert (out == 0).all() and (ns == 0).all()
+
+
+def test_spill_below_zero_and_dense_selection():
+    # per-sequence positive fractions 0.5 / 0.2 / 0.05 / 0.01: more and fewer than 1,024
+    # survivors; the selection then takes keys scored just below zero
+    fl = _layer(4, 16, 4, 16384, pattern="subset", frac=[0.5, 0.2, 0.05, 0.01], seed=11)
+    run = FullRun(fl)
+    ref_sig = _check_full(fl, run)
+    ref_idx, ref_cnt = oracle.select_topk_batch(ref_sig, fl.n)
+    assert np.array_equal(run.count.cpu().numpy(), ref_cnt)
+    assert np.array_equal(run.idx.cpu().numpy(), ref_idx)
+    assert_close(run.sparse(fl.sparse_q[0]),
+                 oracle.sparse_decode_batch(fl.sparse_q[0], fl.K, fl.V, ref_idx, ref_cnt))
+
+
+def test_select_handles_a_crowded_boundary_bin():
+    # all candidate scores equal except a few: the boundary bin holds thousands of keys,
+    # which exercises the radix passes before the shared-memory sort
+    B, Hkv, n = 1, 4, 20000
+    shape = E.Shape(B, 16, Hkv, D, n, n)
+    rng = np.random.default_rng(3)
+    sig = np.full((B, Hkv, n), 0.75, dtype=np.float32)
+    sig[0, 1, rng.choice(n, 50, replace=False)] = 2.0
+    sig[0, 2] = rng.integers(0, 3, n).astype(np.float32) * 0.5
+    sel = torch.from_numpy(sig).cuda()
+    hist = np.stack([[np.bincount(order_key_np(sig[0, g]) >> 21, minlength=E.HIST_BINS)
+                      for g in range(Hkv)]]).astype(np.int32)
+    hist_t = torch.from_numpy(hist).cuda()
+    idx = torch.full((B, Hkv, 1152), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(B, Hkv, dtype=torch.int32, device="cuda")
+    E.embla_select_topk(shape, sel, hist_t, idx, cnt)
+    torch.cuda.synchronize()
+    ref_idx, ref_cnt = oracle.select_topk_batch(sig, n)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
+@pytest.mark.parametrize("pos", [0, 5, 126, 127, 128, 1000, 65535])
+@pytest.mark.parametrize("G", [4, 8])
+def test_window_decode(pos, G):
+    Hkv = 4 if G == 4 else 2
+    wl = gen.make_window_layer(seed=2, layer=3, B=3, Hq=G * Hkv, Hkv=Hkv, D=D, W=128, pos=pos)
+    shape = E.Shape(3, G * Hkv, Hkv, D, 0, 0)
+    out = torch.full((3, G * Hkv, D), float("nan"), device="cuda")
+    E.embla_window_decode(shape, to_dev(wl.q), to_dev(wl.K), to_dev(wl.V), pos, out)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), oracle.window_decode_batch(wl.q, wl.K, wl.V, pos))
+
+
+def test_sparse_decode_with_arbitrary_indices_and_counts():
+    B, Hq, Hkv, n = 2, 16, 4, 5000
+    rng = np.random.default_rng(9)
+    q = gen.normal_bf16(11, (B, Hq, D))
+    K = gen.normal_bf16(12, (B, Hkv, n, D))
+    V = gen.normal_bf16(13, (B, Hkv, n, D))
+    stride = 1152
+    idx = np.zeros((B, Hkv, stride), dtype=np.int32)
+    cnt = np.array([[0, 1, 500, 1152], [37, 129, 1000, 1151]], dtype=np.int64)
+    for b in range(B):
+        for g in range(Hkv):
+            idx[b, g, :cnt[b, g]] = np.sort(rng.choice(n, cnt[b, g], replace=False))
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    E.embla_sparse_decode(shape, to_dev(q), to_dev(K), to_dev(V), torch.from_numpy(idx).cuda(),
+                          torch.from_numpy(cnt.astype(np.int32)).cuda(), out, tau=0.1)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    ref = oracle.sparse_decode_batch(q, K, V, idx, cnt, tau=0.1)
+    got = out.cpu().numpy()
+    assert np.all(got[0, 0:4] == 0.0)  # count 0: zero output
+    assert_close(got, ref)
+
+
+def test_out_of_range_index_is_skipped_and_flagged():
+    B, Hq, Hkv, n = 1, 16, 4, 300
+    q = gen.normal_bf16(21, (B, Hq, D))
+    K = gen.normal_bf16(22, (B, Hkv, n, D))
+    V = gen.normal_bf16(23, (B, Hkv, n, D))
+    idx = np.tile(np.arange(8, dtype=np.int32), (B, Hkv, 1))
+    idx[0, 2, 3] = n + 5
+    cnt = np.full((B, Hkv), 8, dtype=np.int32)
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    out = torch.empty((B, Hq, D), device="cuda")
+    E.embla_device_check(clear=True)
+    E.embla_sparse_decode(shape, to_dev(q), to_dev(K), to_dev(V), torch.from_numpy(idx).cuda(),
+                          torch.from_numpy(cnt).cuda(), out)
+    assert E.embla_device_check(clear=True) & 1
+    assert E.embla_device_check(clear=True) == 0
+    good = np.array([0, 1, 2, 4, 5, 6, 7], dtype=np.int32)
+    ref = oracle.sparse_decode(q[0, 8:12], K[0, 2], V[0, 2], good)
+    assert_close(out.cpu().numpy()[0, 8:12], ref)
