@@ -1,0 +1,506 @@
+"""Decode-attention benchmark for the Embla 1 layer types on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+One step is one decode token for every sequence of the batch through the whole hot
+path of the workload: the full (ReLU^2) layer, its top-1024 + recent-128 selection
+and the sparse layers that reuse it (and, for the whole-model workload, every window
+layer).  Default workload: batch 8, context 32,768, 16 query / 4 KV heads, head_dim
+128, 5% of keys scoring above zero, three sparse layers.
+
+The timed steps replay CUDA graphs of the library's C-ABI calls on device-resident
+inputs.  Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attention tokens/s and needed-byte HBM GB/s (% of roofline) at 32k–128k"
+ROW_BYTES = 128 * 2          # one bf16 key or value row (head_dim 128)
+TOPK, RECENT = 1024, 128
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def state_bytes(c: int, batch: int, bytes_per_elem: int, d_kv: int, tokens: int, layers: int) -> int:
+    """Cache state M_state = c * B * b * d_kv * L_kv * n_ret (c = 2 for separate K and V)."""
+    return c * batch * bytes_per_elem * d_kv * tokens * layers
+
+
+def full_layer_needed_bytes(units: int, n: int, total_survivors: int) -> int:
+    """Bytes a full layer must read: every K row, and the V rows of surviving keys only."""
+    return units * n * ROW_BYTES + total_survivors * ROW_BYTES
+
+
+def sparse_layer_needed_bytes(total_selected: int) -> int:
+    """Bytes a sparse layer must read: the selected K and V rows."""
+    return 2 * total_selected * ROW_BYTES
+
+
+def window_layer_needed_bytes(units: int, valid_rows: int) -> int:
+    return 2 * units * valid_rows * ROW_BYTES
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _traffic_from_profile(workload_key: str, src_digest: str):
+    """DRAM bytes per launch of the full-layer kernel from a committed ncu summary, if the
+    summary was taken on the current kernel source (same digest) and workload."""
+    path = os.path.join(ROOT, "profiles", "full_decode_traffic.md")
+    try:
+        for line in open(path):
+            if line.startswith("traffic:"):
+                kv = dict(tok.split("=", 1) for tok in line.split()[1:])
+                if kv.get("workload") == workload_key and kv.get("src") == src_digest:
+                    return float(kv["bytes_per_launch"])
+    except OSError:
+        pass
+    return None
+
+
+def _kernel_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("full_decode.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "relu_sparse_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(device_index)], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        window = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in window),
+                "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
+                "samples": len(window)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def load_workload(cfg: int, seed: int = 0, batch=None, ctx=None):
+    import gen
+    fls = list(gen.config_full_layers(cfg, seed=seed, B=batch, n=ctx))
+    wls = list(gen.config_window_layers(cfg, seed=seed, B=batch, n=ctx))
+    return fls, wls
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The fp64 CPU oracle on a bounded sample: every layer of the step for a few sequences."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import gen
+    import oracle
+
+    cfg = gen.CONFIGS[args.config]
+    sample_b = 1
+    fls = list(gen.config_full_layers(args.config, seed=0, B=sample_b))
+    wls = list(gen.config_window_layers(args.config, seed=0, B=sample_b))
+    # widen to fp64 once, outside the timed region
+    prep = []
+    for fl in fls:
+        prep.append((oracle.f64(fl.q), oracle.f64(fl.K), oracle.f64(fl.V),
+                     [oracle.f64(qs) for qs in fl.sparse_q], fl.n))
+    wprep = [(oracle.f64(w.q), oracle.f64(w.K), oracle.f64(w.V), w.pos) for w in wls]
+
+    def step():
+        for q, K, V, qss, n in prep:
+            _, sig, _ = oracle.full_decode_batch(q, K, V, n)
+            if qss:
+                idx, cnt = oracle.select_topk_batch(sig, n)
+                for qs in qss:
+                    oracle.sparse_decode_batch(qs, K, V, idx, cnt)
+        for q, K, V, pos in wprep:
+            oracle.window_decode_batch(q, K, V, pos)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = sample_b * args.steps / dt
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["name"], "batch": cfg["B"], "ctx_len": cfg["n"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample_b} of {cfg['B']} sequences, every layer of the step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(cfg_id: int, budget_s: float = 12.0):
+    """The oracle as it stands, on this host's cores, over the whole batch of one full layer
+    step (full + selection + its sparse layers), repeated until ~budget_s of work."""
+    import gen
+    import oracle
+
+    cfg = gen.CONFIGS[cfg_id]
+    B = cfg["B"] if cfg_id != 5 else 1
+    fl = next(gen.config_full_layers(cfg_id, seed=0, B=B))
+    q, K, V = oracle.f64(fl.q), oracle.f64(fl.K), oracle.f64(fl.V)
+    qss = [oracle.f64(x) for x in fl.sparse_q]
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        _, sig, _ = oracle.full_decode_batch(q, K, V, fl.n)
+        idx, cnt = oracle.select_topk_batch(sig, fl.n)
+        for qs in qss:
+            oracle.sparse_decode_batch(qs, K, V, idx, cnt)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = (f"{reps} pass(es) over {B} sequence(s): full layer + selection + "
+              f"{len(qss)} sparse layer(s)" + (" (one of the five full-layer blocks)" if cfg_id == 5 else ""))
+    return {"value": B * reps / dt, "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling)")
+    ap.add_argument("--ctx", type=int, default=None, help="override the workload's context (profiling)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import gen
+    import relu_sparse_kv_gb300 as E
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = gen.CONFIGS[args.config]
+    fls, wls = load_workload(args.config, seed=rank, batch=args.batch, ctx=args.ctx)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    layers = []
+    for fl in fls:
+        B, Hq, D = fl.q.shape
+        Hkv, ncap = fl.K.shape[1], fl.K.shape[2]
+        shape = E.Shape(B, Hq, Hkv, D, fl.n, ncap)
+        L = dict(fl=fl, shape=shape, q=to_dev(fl.q), K=to_dev(fl.K), V=to_dev(fl.V),
+                 qs=[to_dev(x) for x in fl.sparse_q])
+        L["out"] = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+        L["n_surv"] = torch.empty(B, Hkv, dtype=torch.int32, device=dev)
+        need_sel = len(fl.sparse_q) > 0
+        L["sel"] = torch.empty(B, Hkv, ncap, dtype=torch.float32, device=dev) if need_sel else None
+        L["hist"] = torch.empty(B, Hkv, E.HIST_BINS, dtype=torch.int32, device=dev) if need_sel else None
+        L["idx"] = torch.empty(B, Hkv, TOPK + RECENT, dtype=torch.int32, device=dev)
+        L["count"] = torch.empty(B, Hkv, dtype=torch.int32, device=dev)
+        L["souts"] = [torch.empty(B, Hq, D, dtype=torch.float32, device=dev) for _ in fl.sparse_q]
+        L["ws_full"] = torch.empty(E.embla_full_decode_workspace_size(shape), dtype=torch.uint8, device=dev)
+        L["ws_sel"] = torch.empty(max(16, E.embla_select_topk_workspace_size(shape)), dtype=torch.uint8, device=dev)
+        L["ws_sp"] = torch.empty(max(16, E.embla_sparse_decode_workspace_size(shape, TOPK + RECENT)),
+                                 dtype=torch.uint8, device=dev)
+        layers.append(L)
+    wins = []
+    for wl in wls:
+        B, Hq, D = wl.q.shape
+        Hkv, W = wl.K.shape[1], wl.K.shape[2]
+        wins.append(dict(wl=wl, shape=E.Shape(B, Hq, Hkv, D, 0, 0), q=to_dev(wl.q), K=to_dev(wl.K),
+                         V=to_dev(wl.V), out=torch.empty(B, Hq, D, dtype=torch.float32, device=dev)))
+
+    def full_call(L):
+        E.embla_full_decode(L["shape"], L["q"], L["K"], L["V"], L["out"], L["n_surv"], L["sel"],
+                            L["hist"], alpha=1.0, c=1.0, eps=1e-6, workspace=L["ws_full"])
+
+    def rest_calls(L):
+        if not L["qs"]:
+            return
+        E.embla_select_topk(L["shape"], L["sel"], L["hist"], L["idx"], L["count"], TOPK, RECENT,
+                            workspace=L["ws_sel"])
+        for qs, so in zip(L["qs"], L["souts"]):
+            E.embla_sparse_decode(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"], so,
+                                  workspace=L["ws_sp"])
+
+    def window_calls():
+        for w in wins:
+            E.embla_window_decode(w["shape"], w["q"], w["K"], w["V"], w["wl"].pos, w["out"])
+
+    # eager pass: sets kernel attributes and fills the library's per-device caches
+    for L in layers:
+        full_call(L)
+        rest_calls(L)
+    window_calls()
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+
+    # graphs: one per full-layer call (timed alone for the roofline) and one for the rest
+    stream = torch.cuda.Stream(device=dev)
+    g_full, g_rest = [], []
+    with torch.cuda.stream(stream):
+        for L in layers:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                full_call(L)
+            g_full.append(g)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                rest_calls(L)
+            g_rest.append(g)
+        g_win = None
+        if wins:
+            g_win = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_win, stream=stream):
+                window_calls()
+    torch.cuda.synchronize()
+
+    # accounting from this rank's own results
+    n_surv_tot = [int(L["n_surv"].sum().item()) for L in layers]
+    sel_tot = [int(L["count"].sum().item()) if L["qs"] else 0 for L in layers]
+    full_bytes = [full_layer_needed_bytes(L["shape"].units, L["fl"].n, s) for L, s in zip(layers, n_surv_tot)]
+    sparse_bytes = sum(len(L["qs"]) * sparse_layer_needed_bytes(s) for L, s in zip(layers, sel_tot))
+    win_bytes = sum(window_layer_needed_bytes(w["shape"].units, min(w["wl"].pos + 1, w["wl"].K.shape[2]))
+                    for w in wins)
+    needed = sum(full_bytes) + sparse_bytes + win_bytes
+    keys_total = sum(L["shape"].units * L["fl"].n for L in layers)
+    skipped_v = 1.0 - sum(n_surv_tot) / max(1, keys_total)
+    batch = layers[0]["shape"].batch
+    launches_per_step = 0
+    for L in layers:
+        launches_per_step += 2
+        if L["qs"]:
+            launches_per_step += (2 if L["fl"].n > TOPK + RECENT else 1) + 2 * len(L["qs"])
+    launches_per_step += len(wins)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * len(layers))]
+
+    def step(timed_i=None):
+        for li, (gf, gr) in enumerate(zip(g_full, g_rest)):
+            if timed_i is not None:
+                ev[timed_i * len(layers) + li][0].record(stream)
+            gf.replay()
+            if timed_i is not None:
+                ev[timed_i * len(layers) + li][1].record(stream)
+            gr.replay()
+        if g_win is not None:
+            g_win.replay()
+
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop(t_wall0, t_wall1)
+    ms = start.elapsed_time(end)
+    full_ms = [statistics.mean(ev[i * len(layers) + li][0].elapsed_time(ev[i * len(layers) + li][1])
+                               for i in range(args.steps)) for li in range(len(layers))]
+    assert E.embla_device_check() == 0
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * batch / (ms_per_step * 1e-3)
+
+    # end to end through the public Python API, host buffers, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        L0 = layers[0]
+        pin = lambda t: t.cpu().pin_memory()
+        h_q = [pin(L["q"]) for L in layers]
+        h_qs = [[pin(x) for x in L["qs"]] for L in layers]
+        n = L0["fl"].n
+        h_krow = [pin(L["K"][:, :, n - 1, :].contiguous()) for L in layers]
+        h_vrow = [pin(L["V"][:, :, n - 1, :].contiguous()) for L in layers]
+        h_wq = [pin(w["q"]) for w in wins]
+        h_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in layers]
+        h_sout = [[torch.empty_like(x, device="cpu").pin_memory() for x in L["souts"]] for L in layers]
+        h_ns = [torch.empty_like(L["n_surv"], device="cpu").pin_memory() for L in layers]
+        h_wout = [torch.empty_like(w["out"], device="cpu").pin_memory() for w in wins]
+        h2d = sum(x.numel() * x.element_size() for x in h_q + h_krow + h_vrow + h_wq) + \
+            sum(x.numel() * x.element_size() for xs in h_qs for x in xs)
+        d2h = sum(x.numel() * x.element_size() for x in h_out + h_ns + h_wout) + \
+            sum(x.numel() * x.element_size() for xs in h_sout for x in xs)
+
+        def e2e_step():
+            for li, L in enumerate(layers):
+                L["q"].copy_(h_q[li], non_blocking=True)
+                for x, hx in zip(L["qs"], h_qs[li]):
+                    x.copy_(hx, non_blocking=True)
+                L["K"][:, :, n - 1, :].copy_(h_krow[li], non_blocking=True)
+                L["V"][:, :, n - 1, :].copy_(h_vrow[li], non_blocking=True)
+                full_call(L)
+                rest_calls(L)
+            for wi, w in enumerate(wins):
+                w["q"].copy_(h_wq[wi], non_blocking=True)
+            window_calls()
+            for li, L in enumerate(layers):
+                h_out[li].copy_(L["out"], non_blocking=True)
+                h_ns[li].copy_(L["n_surv"], non_blocking=True)
+                for hx, x in zip(h_sout[li], L["souts"]):
+                    hx.copy_(x, non_blocking=True)
+            for wi, w in enumerate(wins):
+                h_wout[wi].copy_(w["out"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        dt = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([dt], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * batch * args.e2e_steps / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps,
+               "inputs": "per-step queries and the appended token's K/V rows from pinned host "
+                         "memory; the KV caches stay resident in HBM"}
+
+    peak, peak_src = _peaks()
+    wl_key = f"cfg{args.config}"
+    achieved = [fb / (fm * 1e-3) / 1e9 for fb, fm in zip(full_bytes, full_ms)]
+    ach = statistics.mean(achieved)
+    roofline = {"bound": "hbm", "kernel": "embla_full_decode (histogram reset + score/skip kernel + combine)",
+                "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+                "traffic": _traffic_from_profile(wl_key, _kernel_digest()),
+                "algorithmic_bytes_per_launch": full_bytes[0],
+                "launch_ms": round(statistics.mean(full_ms), 5)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.config)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"] + ("" if args.batch is None and args.ctx is None else
+                                              f" (overridden: batch {args.batch}, ctx {args.ctx})"),
+                   "batch": batch, "ctx_len": layers[0]["fl"].n,
+                   "q_heads": 16, "kv_heads": 4, "head_dim": 128,
+                   "full_layers": len(layers), "sparse_layers": sum(len(L["qs"]) for L in layers),
+                   "window_layers": len(wins), "accumulate": "f32",
+                   "l2": "not flushed: inputs larger than L2 (each full layer's K cache is "
+                         f"{keys_total * ROW_BYTES // len(layers) / 1e6:.0f} MB)",
+                   "needed_bytes_per_step": needed,
+                   "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),
+                   "needed_frac_of_peak": round(needed / (ms_per_step * 1e-3) / 1e9 / peak, 4),
+                   "skipped_v_fraction": round(skipped_v, 5)},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

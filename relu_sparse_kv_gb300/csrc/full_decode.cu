@@ -25,39 +25,57 @@
 namespace embla {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kVSlots = 4;
-constexpr int kVRows = 32;                         // V rows per batch
+#ifndef EMBLA_K_STAGES
+#define EMBLA_K_STAGES 4
+#endif
+#ifndef EMBLA_W_SLOTS
+#define EMBLA_W_SLOTS 8
+#endif
+#ifndef EMBLA_V_RING_ROWS
+#define EMBLA_V_RING_ROWS 128
+#endif
+constexpr int kStages = EMBLA_K_STAGES;            // K tiles in flight
+constexpr int kWSlots = EMBLA_W_SLOTS;             // per-tile survivor lists in flight
+constexpr int kRing = EMBLA_V_RING_ROWS;           // V rows in flight
+constexpr int kGroups = 2;                         // epilogue warpgroups, alternating tiles
+constexpr int kAccBufs = 2 * kGroups;              // tensor-memory accumulators
 constexpr int kRowBytes = kHeadDim * 2;            // 256
 constexpr int kTileBytes = kTileKeys * kRowBytes;  // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;         // 128 rows x 64 dims
 constexpr int kQBufBytes = 4096;                   // 16 rows x 128 dims (MMA N = 16)
 constexpr int kQHalfBytes = kQBufBytes / 2;
-constexpr int kThreads = 320;
 constexpr int kMmaN = 16;
+constexpr int kTmemCols = kAccBufs * kMmaN;        // 64
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN);
-constexpr int kFlagFlush = 1, kFlagDone = 2;
-constexpr int kEpiBarrier = 1;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
+constexpr int kWarpIssuer = kWarpEpi + 4 * kGroups;
+constexpr int kWarpAcc = kWarpIssuer + 1;
+constexpr int kThreads = (kWarpAcc + 4) * 32;      // 480
+constexpr uint16_t kNoBin = 0xFFFF;
+static_assert(kRing >= kTileKeys, "a whole tile of survivors must fit the V ring");
 
+// One tile's survivors, compacted per TMEM quarter (ascending key order within a quarter).
 template <int G>
-struct VMeta {
-  int32_t cnt, flags, unit, rec;
-  int32_t seg_surv, pad0, pad1, pad2;
-  int32_t key[kVRows];
-  float w[kVRows][G];
+struct WSlot {
+  int32_t cnt[4];             // survivors per quarter
+  int32_t row0;               // first V-ring row of this tile (written by the issuer)
+  int32_t pad[3];
+  uint16_t bin[kTileKeys];    // selection-histogram bin per key (kNoBin: no key there)
+  int32_t key[4][32];         // key index within the unit
+  float w[4][32][G];          // ReLU^2 weights per head
 };
 
 template <int G>
 struct Smem {
   static constexpr int k_off = 0;
   static constexpr int q_off = k_off + kStages * kTileBytes;
-  static constexpr int v_off = q_off + 2 * kQBufBytes;
-  static constexpr int meta_off = v_off + kVSlots * kVRows * kRowBytes;
-  static constexpr int hist_off = meta_off + kVSlots * static_cast<int>(sizeof(VMeta<G>));
-  static constexpr int aq_off = hist_off + kHistBins * 4;
-  static constexpr int misc_off = aq_off + 2 * 16 * 4;
-  static constexpr int bar_off = misc_off + 64;
-  static constexpr int n_bars = 2 * kStages + 8 + 2 * kVSlots;
+  static constexpr int ring_off = q_off + 2 * kQBufBytes;
+  static constexpr int wslot_off = ring_off + kRing * kRowBytes;
+  static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G>));
+  static constexpr int misc_off = hist_off + kHistBins * 4;
+  static constexpr int end_off = misc_off + 64;                 // int64 per W slot
+  static constexpr int bar_off = end_off + kWSlots * 8;
+  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 4 + 3 * kWSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
 };
@@ -73,35 +91,41 @@ struct FullParams {
   float alpha, eps;
 };
 
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
+__device__ __forceinline__ float sumsq8(const uint4 &v) {
+  float a = bf16lo(v.x) * bf16lo(v.x);
+  float b = bf16hi(v.x) * bf16hi(v.x);
+  a = fmaf(bf16lo(v.y), bf16lo(v.y), a);
+  b = fmaf(bf16hi(v.y), bf16hi(v.y), b);
+  a = fmaf(bf16lo(v.z), bf16lo(v.z), a);
+  b = fmaf(bf16hi(v.z), bf16hi(v.z), b);
+  a = fmaf(bf16lo(v.w), bf16lo(v.w), a);
+  b = fmaf(bf16hi(v.w), bf16hi(v.w), b);
+  return a + b;
 }
 
-__device__ __forceinline__ float sumsq8(const uint4 &v) {
-  float s = 0.0f;
-  s = fmaf(bf16lo(v.x), bf16lo(v.x), s);
-  s = fmaf(bf16hi(v.x), bf16hi(v.x), s);
-  s = fmaf(bf16lo(v.y), bf16lo(v.y), s);
-  s = fmaf(bf16hi(v.y), bf16hi(v.y), s);
-  s = fmaf(bf16lo(v.z), bf16lo(v.z), s);
-  s = fmaf(bf16hi(v.z), bf16hi(v.z), s);
-  s = fmaf(bf16lo(v.w), bf16lo(v.w), s);
-  s = fmaf(bf16hi(v.w), bf16hi(v.w), s);
-  return s;
+// acc[0..3] += squares of the 8 bf16 values, spread over four independent chains
+__device__ __forceinline__ void sumsq8_acc(const uint4 &v, float (&acc)[4]) {
+  acc[0] = fmaf(bf16lo(v.x), bf16lo(v.x), acc[0]);
+  acc[1] = fmaf(bf16hi(v.x), bf16hi(v.x), acc[1]);
+  acc[2] = fmaf(bf16lo(v.y), bf16lo(v.y), acc[2]);
+  acc[3] = fmaf(bf16hi(v.y), bf16hi(v.y), acc[3]);
+  acc[0] = fmaf(bf16lo(v.z), bf16lo(v.z), acc[0]);
+  acc[1] = fmaf(bf16hi(v.z), bf16hi(v.z), acc[1]);
+  acc[2] = fmaf(bf16lo(v.w), bf16lo(v.w), acc[2]);
+  acc[3] = fmaf(bf16hi(v.w), bf16hi(v.w), acc[3]);
 }
 
 __device__ __forceinline__ void set_abort(volatile int *abort_flag, uint32_t *flags) {
   *abort_flag = 1;
   atomicOr(flags, kFlagWaitTimeout);
+}
+
+// Advance (tile-in-unit, unit) to the next tile of the flattened sequence.
+__device__ __forceinline__ void next_tile(int64_t &tl, int64_t &u, int64_t TU) {
+  if (++tl == TU) {
+    tl = 0;
+    ++u;
+  }
 }
 
 template <int G>
@@ -114,52 +138,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sK = smem + L::k_off;
   uint8_t *sQ = smem + L::q_off;
-  uint8_t *sV = smem + L::v_off;
-  VMeta<G> *meta = reinterpret_cast<VMeta<G> *>(smem + L::meta_off);
+  uint8_t *sRing = smem + L::ring_off;
+  WSlot<G> *wslots = reinterpret_cast<WSlot<G> *>(smem + L::wslot_off);
   uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem + L::hist_off);
-  float *s_aq = reinterpret_cast<float *>(smem + L::aq_off);
   int *misc = reinterpret_cast<int *>(smem + L::misc_off);
-  int *s_wcnt = misc;                                   // [4] survivors per TMEM quarter
-  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc + 4);
-  volatile int *s_abort = misc + 5;
-  volatile int *s_k_issued = misc + 6;
-  volatile int *s_vb_total = misc + 7;
-  volatile int *s_q_issued = misc + 8;
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
+  volatile int *s_abort = misc + 1;
+  volatile int *s_k_issued = misc + 2;
+  volatile int *s_q_issued = misc + 3;
+  volatile int *s_v_issued = misc + 4;
+  int64_t *s_end = reinterpret_cast<int64_t *>(smem + L::end_off);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
-  uint64_t *full = bars;
-  uint64_t *empty = full + kStages;
-  uint64_t *accf = empty + kStages;
-  uint64_t *acce = accf + 2;
-  uint64_t *qfull = acce + 2;
-  uint64_t *qempty = qfull + 2;
-  uint64_t *vfull = qempty + 2;
-  uint64_t *vempty = vfull + kVSlots;
+  uint64_t *full = bars;                 // K tile landed
+  uint64_t *empty = full + kStages;      // K tile consumed (MMA and sum of squares)
+  uint64_t *accf = empty + kStages;      // accumulator written
+  uint64_t *acce = accf + kAccBufs;      // accumulator read
+  uint64_t *qfull = acce + kAccBufs;     // query rows landed
+  uint64_t *qempty = qfull + 2;          // query rows no longer needed
+  uint64_t *wfull = qempty + 2;          // survivor list written
+  uint64_t *wempty = wfull + kWSlots;    // survivor list and its V rows consumed
+  uint64_t *vfull = wempty + kWSlots;    // V rows of a tile landed
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
   const int64_t tb = split_first_tile(cta, p.T, p.P);
   const int64_t te = split_first_tile(cta + 1, p.T, p.P);
+  const int64_t u0 = tb / p.TU, tl0 = tb - u0 * p.TU;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&accf[a], 1);
-      mbar_init(&acce[a], 4);
-      mbar_init(&qfull[a], 1);
-      mbar_init(&qempty[a], 2);
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
     }
-    for (int v = 0; v < kVSlots; ++v) {
-      mbar_init(&vfull[v], 1);
-      mbar_init(&vempty[v], 4);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], 1 + 4 * kGroups);
+    }
+    for (int w = 0; w < kWSlots; ++w) {
+      mbar_init(&wfull[w], 4);
+      mbar_init(&wempty[w], 4);
+      mbar_init(&vfull[w], 1);
     }
     *s_abort = 0;
     *s_k_issued = 0;
-    *s_vb_total = 0;
     *s_q_issued = 0;
+    *s_v_issued = 0;
     fence_barrier_init();
   }
   // Rows G..15 of the query operand feed only MMA columns that are never read; zero
@@ -168,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0u;
   fence_proxy_async_smem();
-  if (warp == 1) {
-    tmem_alloc(s_tmem, 32);
+  if (warp == kWarpMma) {
+    tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -177,21 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
 
-  if (warp == 0) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_q);
       const uint64_t policy = policy_evict_first();
-      int64_t cur_u = -1;
+      int64_t u = u0, tl = tl0;
       int seg = -1;
       int64_t i = 0;
-      for (int64_t t = tb; t < te; ++t, ++i) {
+      for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
         if (*s_abort) break;
-        const int64_t u = t / p.TU;
-        const int64_t tl = t - u * p.TU;
-        if (u != cur_u) {
-          cur_u = u;
+        if (i == 0 || tl == 0) {
           ++seg;
           const int qb = seg & 1;
           if (seg >= 2 && !mbar_wait(&qempty[qb], ((seg >> 1) - 1) & 1)) {
@@ -217,17 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int64_t cur_u = -1;
+      int64_t u = u0, tl = tl0;
       int seg = -1, qb = 0;
       int64_t i = 0, issued = 0;
-      for (int64_t t = tb; t < te; ++t, ++i) {
+      for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
         if (*s_abort) break;
-        const int64_t u = t / p.TU;
-        if (u != cur_u) {
-          cur_u = u;
+        if (i == 0 || tl == 0) {
           ++seg;
           qb = seg & 1;
           if (!mbar_wait(&qfull[qb], (seg >> 1) & 1)) {
@@ -236,9 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int s = static_cast<int>(i % kStages);
-        const int a = static_cast<int>(i & 1);
+        const int b = static_cast<int>(i % kAccBufs);
         if (!mbar_wait(&full[s], (i / kStages) & 1) ||
-            (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) - 1) & 1))) {
+            (i >= kAccBufs && !mbar_wait(&acce[b], ((i / kAccBufs) - 1) & 1))) {
           set_abort(s_abort, p.flags);
           break;
         }
@@ -249,73 +272,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint64_t adesc = smem_desc_sw128(kaddr + (kk >> 2) * kHalfBytes + (kk & 3) * 32);
           const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * kQHalfBytes + (kk & 3) * 32);
-          tc_mma_bf16(tmem + a * kMmaN, adesc, bdesc, kIdesc, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + b * kMmaN, adesc, bdesc, kIdesc, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&accf[a]);
+        tc_commit(&accf[b]);
         issued = i + 1;
-        const bool seg_end = (t + 1 == te) || ((t + 1) / p.TU != u);
-        if (seg_end) tc_commit(&qempty[qb]);
+        if (t + 1 == te || tl + 1 == p.TU) tc_commit(&qempty[qb]);
       }
-      // the accumulator must be idle before the tensor memory is released
-      if (issued > 0) mbar_wait(&accf[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+      // the accumulators must be idle before the tensor memory is released
+      if (issued > 0)
+        mbar_wait(&accf[(issued - 1) % kAccBufs], ((issued - 1) / kAccBufs) & 1);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ------------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;  // 0..127
-    const int ew = warp - 2;          // epilogue warp 0..3
-    const int quarter = warp & 3;     // TMEM lanes this warp may read
+  } else if (warp < kWarpIssuer) {
+    // ------------------------------------------------------------------ epilogue groups
+    const int group = (warp - kWarpEpi) >> 2;
+    const int quarter = warp & 3;     // the TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
     const uint32_t lanemask_lt = (1u << lane) - 1u;
     float aq[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) aq[h] = 0.0f;
-    int64_t cur_u = -1;
+    int64_t u = u0, tl = tl0;
     int seg = -1;
-    int64_t i = 0, vb = 0;
-    int seg_surv = 0;
-    for (int64_t t = tb; t < te; ++t, ++i) {
-      const int64_t u = t / p.TU;
-      const int64_t tl = t - u * p.TU;
-      if (u != cur_u) {
-        cur_u = u;
+    int64_t i = 0;
+    for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+      if (__any_sync(0xffffffffu, *s_abort)) break;
+      if (i == 0 || tl == 0) {
+        // every epilogue warp takes the new unit's query norms, whichever tiles it owns
         ++seg;
-        seg_surv = 0;
         const int qb = seg & 1;
-        bool ok = mbar_wait(&qfull[qb], (seg >> 1) & 1);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          for (int h = ew; h < G; h += 4) {
-            float ss = 0.0f;
-            if (lane < 16) {
-              const uint4 v = *reinterpret_cast<const uint4 *>(
-                  sQ + qb * kQBufBytes + (lane >> 3) * kQHalfBytes + h * 128 + (lane & 7) * 16);
-              ss = sumsq8(v);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (lane == 0) s_aq[qb * 16 + h] = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-          }
-        }
-        if (bar_red_or(kEpiBarrier, 128, !ok || *s_abort)) {
-          if (!ok) set_abort(s_abort, p.flags);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&qfull[qb], (seg >> 1) & 1));
+        if (!ok) {
+          set_abort(s_abort, p.flags);
           break;
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) aq[h] = s_aq[qb * 16 + h];
-        if (et == 0) mbar_arrive(&qempty[qb]);
-      }
-      const int s = static_cast<int>(i % kStages);
-      const int a = static_cast<int>(i & 1);
-      bool ok = mbar_wait(&accf[a], (i >> 1) & 1) && mbar_wait(&full[s], (i / kStages) & 1);
-      ok = __all_sync(0xffffffffu, ok);
-      float dot[G];
-      float ss = 0.0f;
+        for (int h = 0; h < G; ++h) {
+          float ss = 0.0f;
+          if (lane < 16)
+            ss = sumsq8(*reinterpret_cast<const uint4 *>(sQ + qb * kQBufBytes +
+                                                         (lane >> 3) * kQHalfBytes + h * 128 +
+                                                         (lane & 7) * 16));
 #pragma unroll
-      for (int h = 0; h < G; ++h) dot[h] = 0.0f;
-      if (ok) {
-        tc_fence_after_sync();
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kMmaN;
+          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          aq[h] = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[qb]);
+      }
+      if (static_cast<int>(i % kGroups) != group) continue;
+      const int b = static_cast<int>(i % kAccBufs);
+      const int s = static_cast<int>(i % kStages);
+      const int slot = static_cast<int>(i % kWSlots);
+      bool ok = mbar_wait(&accf[b], (i / kAccBufs) & 1) && mbar_wait(&full[s], (i / kStages) & 1) &&
+                (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        set_abort(s_abort, p.flags);
+        break;
+      }
+      float dot[G];
+      tc_fence_after_sync();
+      {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * kMmaN;
         if constexpr (G == 4) {
           uint32_t r[4];
           tmem_load_x4(taddr, r);
@@ -329,25 +348,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 8; ++h) dot[h] = __uint_as_float(r[h]);
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[a]);
-        // this key's sum of squares; chunk order rotated by row so 8 neighbouring
-        // rows hit 8 different bank groups (the swizzle permutes chunks within a row)
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);
+      // this key's sum of squares; chunk order rotated by row so 8 neighbouring rows hit 8
+      // different bank groups (the swizzle permutes chunks within a row)
+      float ss;
+      {
         const uint8_t *rowp = sK + s * kTileBytes + row * 128;
-        float ss0 = 0.0f, ss1 = 0.0f;
+        float a0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int pc = (c ^ (row & 7)) * 16;
-          ss0 += sumsq8(*reinterpret_cast<const uint4 *>(rowp + pc));
-          ss1 += sumsq8(*reinterpret_cast<const uint4 *>(rowp + kHalfBytes + pc));
+          sumsq8_acc(*reinterpret_cast<const uint4 *>(rowp + pc), a0);
+          sumsq8_acc(*reinterpret_cast<const uint4 *>(rowp + kHalfBytes + pc), a1);
         }
-        ss = ss0 + ss1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        ss = ((a0[0] + a0[1]) + (a0[2] + a0[3])) + ((a1[0] + a1[1]) + (a1[2] + a1[3]));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+
       const int64_t j = tl * kTileKeys + row;
-      const bool valid = ok && j < p.n;
+      const bool valid = j < p.n;
       const float rk = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
       float sc[G];
       float sigma = -INFINITY;
@@ -356,85 +379,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc[h] = dot[h] * aq[h] * rk;
         sigma = fmaxf(sigma, sc[h]);
       }
-      if (valid && p.sel != nullptr) {
-        p.sel[u * p.ncap + j] = sigma;
-        atomicAdd(&s_hist[order_key(sigma) >> 21], 1u);
+      WSlot<G> &ws = wslots[slot];
+      if (p.sel != nullptr) {
+        if (valid) p.sel[u * p.ncap + j] = sigma;
+        ws.bin[row] = valid ? static_cast<uint16_t>(order_key(sigma) >> 21) : kNoBin;
       }
       const bool surv = valid && sigma > 0.0f;
       const uint32_t bal = __ballot_sync(0xffffffffu, surv);
-      if (lane == 0) s_wcnt[quarter] = __popc(bal);
-      if (bar_red_or(kEpiBarrier, 128, !ok || *s_abort)) {
-        if (!ok) set_abort(s_abort, p.flags);
+      if (surv) {
+        const int r = __popc(bal & lanemask_lt);
+        ws.key[quarter][r] = static_cast<int32_t>(j);
+#pragma unroll
+        for (int h = 0; h < G; ++h) ws.w[quarter][r][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
+      }
+      if (lane == 0) ws.cnt[quarter] = __popc(bal);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wfull[slot]);
+    }
+    __syncwarp();
+  } else if (warp == kWarpIssuer) {
+    // ------------------------------------------------------------------ V issuer
+    // Reads each tile's survivor list in order, keeps the selection histogram, and
+    // bulk-copies the surviving keys' V rows into a ring of kRing rows.
+    int64_t u = u0, tl = tl0;
+    int64_t i = 0, rows_issued = 0, rows_freed = 0, oldest = 0;
+    for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+      if (__any_sync(0xffffffffu, *s_abort)) break;
+      const int slot = static_cast<int>(i % kWSlots);
+      // the epilogue refilled this slot, so tile i - kWSlots and older are consumed
+      while (oldest <= i - kWSlots) {
+        rows_freed = s_end[oldest % kWSlots];
+        ++oldest;
+      }
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&wfull[slot], (i / kWSlots) & 1));
+      if (!ok) {
+        set_abort(s_abort, p.flags);
         break;
       }
-      int off = 0, m = 0;
+      WSlot<G> &ws = wslots[slot];
+      const int c0 = ws.cnt[0], c1 = ws.cnt[1], c2 = ws.cnt[2], c3 = ws.cnt[3];
+      const int m = c0 + c1 + c2 + c3;
+      if (p.sel != nullptr) {
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int cq = s_wcnt[q4];
-        off += (q4 < quarter) ? cq : 0;
-        m += cq;
+        for (int r = lane; r < kTileKeys; r += 32) {
+          const uint16_t bn = ws.bin[r];
+          if (bn != kNoBin) atomicAdd(&s_hist[bn], 1u);
+        }
       }
-      seg_surv += m;
-      const bool seg_end = (t + 1 == te) || ((t + 1) / p.TU != u);
-      const bool last = (t + 1 == te);
-      int nb = (m + kVRows - 1) / kVRows;
-      if (seg_end && nb == 0) nb = 1;
-      bool ok2 = true;
-      for (int k = 0; k < nb; ++k) {
-        const int64_t vbk = vb + k;
-        if (vbk >= kVSlots)
-          ok2 = ok2 && mbar_wait(&vempty[vbk % kVSlots], ((vbk / kVSlots) - 1) & 1);
+      while (ok && rows_issued + m - rows_freed > kRing) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&wempty[oldest % kWSlots], (oldest / kWSlots) & 1));
+        rows_freed = s_end[oldest % kWSlots];
+        ++oldest;
       }
-      if (ok2 && surv) {
-        const int pos = off + __popc(bal & lanemask_lt);
-        VMeta<G> &mt = meta[(vb + pos / kVRows) % kVSlots];
-        const int e = pos % kVRows;
-        mt.key[e] = static_cast<int32_t>(j);
-#pragma unroll
-        for (int h = 0; h < G; ++h) mt.w[e][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
-      }
-      if (bar_red_or(kEpiBarrier, 128, !ok2 || *s_abort)) {
-        if (!ok2) set_abort(s_abort, p.flags);
+      if (!ok) {
+        set_abort(s_abort, p.flags);
         break;
       }
-      if (ew < nb) {
-        const int slot = static_cast<int>((vb + ew) % kVSlots);
-        VMeta<G> &mt = meta[slot];
-        const int cnt = min(kVRows, max(0, m - ew * kVRows));
-        if (lane == 0) {
-          mt.cnt = cnt;
-          mt.flags = (ew == nb - 1) ? ((seg_end ? kFlagFlush : 0) | (last ? kFlagDone : 0)) : 0;
-          mt.unit = static_cast<int32_t>(u);
-          mt.rec = static_cast<int32_t>(cta + u);
-          mt.seg_surv = seg_surv;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], cnt * kRowBytes);
-        __syncwarp();
-        if (lane < cnt) {
-          const int64_t jj = mt.key[lane];
-          bulk_load(sV + slot * (kVRows * kRowBytes) + lane * kRowBytes,
-                    p.v + (u * p.ncap + jj) * kRowBytes, kRowBytes, &vfull[slot]);
-        }
+      if (lane == 0) {
+        ws.row0 = static_cast<int32_t>(rows_issued % kRing);
+        s_end[slot] = rows_issued + m;
       }
-      vb += nb;
-      if (et == 0) *s_vb_total = static_cast<int>(vb);
-      if (seg_end && p.sel != nullptr) {
-        for (int bin = et; bin < kHistBins; bin += 128) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(m * kRowBytes));
+      __syncwarp();
+      for (int e = lane; e < m; e += 32) {
+        int q = 0, k = e;
+        if (k >= c0) { k -= c0; q = 1;
+          if (k >= c1) { k -= c1; q = 2;
+            if (k >= c2) { k -= c2; q = 3; } } }
+        const int64_t key = ws.key[q][k];
+        const int dst = static_cast<int>((rows_issued + e) % kRing);
+        bulk_load(sRing + dst * kRowBytes, p.v + (u * p.ncap + key) * kRowBytes, kRowBytes,
+                  &vfull[slot]);
+      }
+      rows_issued += m;
+      if (lane == 0) *s_v_issued = static_cast<int>(i + 1);
+      if (p.sel != nullptr && (t + 1 == te || tl + 1 == p.TU)) {
+        __syncwarp();
+        for (int bin = lane; bin < kHistBins; bin += 32) {
           const uint32_t cnt = s_hist[bin];
           if (cnt) {
             atomicAdd(&p.hist[u * kHistBins + bin], cnt);
             s_hist[bin] = 0u;
           }
         }
-        named_bar_sync(kEpiBarrier, 128);
+        __syncwarp();
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ V accumulators
     constexpr int HPW = G / 4;  // heads per warp
-    const int vw = warp - 6;
+    const int aw = warp - kWarpAcc;
     const int d0 = lane * 4;
     float acc[HPW][4];
     float den[HPW];
@@ -444,47 +481,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int d = 0; d < 4; ++d) acc[hh][d] = 0.0f;
     }
-    for (int64_t vb = 0;; ++vb) {
-      const int slot = static_cast<int>(vb % kVSlots);
-      bool ok = !*s_abort && mbar_wait(&vfull[slot], (vb / kVSlots) & 1);
-      ok = __all_sync(0xffffffffu, ok);
+    int seg_surv = 0;
+    int64_t u = u0, tl = tl0;
+    int64_t i = 0;
+    for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+      if (__any_sync(0xffffffffu, *s_abort)) break;
+      const int slot = static_cast<int>(i % kWSlots);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&vfull[slot], (i / kWSlots) & 1));
       if (!ok) {
         set_abort(s_abort, p.flags);
         break;
       }
-      const VMeta<G> &mt = meta[slot];
-      const int cnt = mt.cnt, flags = mt.flags, rec = mt.rec, seg_surv = mt.seg_surv;
-      const uint8_t *vd = sV + slot * (kVRows * kRowBytes) + lane * 8;
-      for (int e = 0; e < cnt; ++e) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(vd + e * kRowBytes);
-        const float v0 = bf16lo(raw.x), v1 = bf16hi(raw.x), v2 = bf16lo(raw.y),
-                    v3 = bf16hi(raw.y);
+      const WSlot<G> &ws = wslots[slot];
+      int e = ws.row0;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int cq = ws.cnt[q];
+        for (int k = 0; k < cq; ++k, ++e) {
+          const uint2 raw = *reinterpret_cast<const uint2 *>(sRing + (e % kRing) * kRowBytes + lane * 8);
+          const float v0 = bf16lo(raw.x), v1 = bf16hi(raw.x), v2 = bf16lo(raw.y),
+                      v3 = bf16hi(raw.y);
 #pragma unroll
-        for (int hh = 0; hh < HPW; ++hh) {
-          const float w = mt.w[e][vw + 4 * hh];
-          acc[hh][0] = fmaf(w, v0, acc[hh][0]);
-          acc[hh][1] = fmaf(w, v1, acc[hh][1]);
-          acc[hh][2] = fmaf(w, v2, acc[hh][2]);
-          acc[hh][3] = fmaf(w, v3, acc[hh][3]);
-          den[hh] += w;
+          for (int hh = 0; hh < HPW; ++hh) {
+            const float w = ws.w[q][k][aw + 4 * hh];
+            acc[hh][0] = fmaf(w, v0, acc[hh][0]);
+            acc[hh][1] = fmaf(w, v1, acc[hh][1]);
+            acc[hh][2] = fmaf(w, v2, acc[hh][2]);
+            acc[hh][3] = fmaf(w, v3, acc[hh][3]);
+            den[hh] += w;
+          }
         }
       }
+      seg_surv += e - ws.row0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&vempty[slot]);
-      if (flags & kFlagFlush) {
-        float *r = p.rec + static_cast<int64_t>(rec) * p.rec_stride;
+      if (lane == 0) mbar_arrive(&wempty[slot]);
+      if (t + 1 == te || tl + 1 == p.TU) {
+        float *r = p.rec + (cta + u) * p.rec_stride;
 #pragma unroll
         for (int hh = 0; hh < HPW; ++hh) {
-          const int h = vw + 4 * hh;
+          const int h = aw + 4 * hh;
           *reinterpret_cast<float4 *>(r + h * kHeadDim + d0) =
               make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
           if (lane == 0) r[G * kHeadDim + h] = den[hh];
           den[hh] = 0.0f;
           acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.0f;
         }
-        if (vw == 0 && lane == 0) reinterpret_cast<int32_t *>(r)[G * kHeadDim + G] = seg_surv;
+        if (aw == 0 && lane == 0) reinterpret_cast<int32_t *>(r)[G * kHeadDim + G] = seg_surv;
+        seg_surv = 0;
       }
-      if (flags & kFlagDone) break;
     }
     __syncwarp();
   }
@@ -493,23 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     // No copy may still be landing in shared memory when the CTA leaves: wait (bounded)
     // for the last armed phase of every barrier that a copy completes.
-    const int k_issued = *s_k_issued, vb_total = *s_vb_total, q_issued = *s_q_issued;
+    const int k_issued = *s_k_issued, q_issued = *s_q_issued, v_issued = *s_v_issued;
     for (int s = 0; s < kStages; ++s) {
       const int uses = k_issued > s ? (k_issued - 1 - s) / kStages + 1 : 0;
       if (uses) mbar_wait(&full[s], (uses - 1) & 1);
     }
-    for (int v = 0; v < kVSlots; ++v) {
-      const int uses = vb_total > v ? (vb_total - 1 - v) / kVSlots + 1 : 0;
-      if (uses) mbar_wait(&vfull[v], (uses - 1) & 1);
+    for (int w = 0; w < kWSlots; ++w) {
+      const int uses = v_issued > w ? (v_issued - 1 - w) / kWSlots + 1 : 0;
+      if (uses) mbar_wait(&vfull[w], (uses - 1) & 1);
     }
     for (int q = 0; q < 2; ++q) {
       const int uses = q_issued > q ? (q_issued - 1 - q) / 2 + 1 : 0;
       if (uses) mbar_wait(&qfull[q], (uses - 1) & 1);
     }
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 32);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
