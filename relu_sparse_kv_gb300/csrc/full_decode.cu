@@ -51,18 +51,20 @@ constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
 constexpr int kWarpIssuer = kWarpEpi + 4 * kGroups;
 constexpr int kWarpAcc = kWarpIssuer + 1;
 constexpr int kThreads = (kWarpAcc + 4) * 32;      // 480
-constexpr uint16_t kNoBin = 0xFFFF;
 static_assert(kRing >= kTileKeys, "a whole tile of survivors must fit the V ring");
+static_assert((kRing & (kRing - 1)) == 0, "the V ring size is a power of two");
 
-// One tile's survivors, compacted per TMEM quarter (ascending key order within a quarter).
+// One tile's survivors.  The epilogue warps fill one 32-entry list per TMEM quarter; the
+// issuer then rewrites the entries in place as one flat list (quarter-major, so ascending
+// key order) before fetching their V rows.
 template <int G>
 struct WSlot {
   int32_t cnt[4];             // survivors per quarter
   int32_t row0;               // first V-ring row of this tile (written by the issuer)
-  int32_t pad[3];
-  uint16_t bin[kTileKeys];    // selection-histogram bin per key (kNoBin: no key there)
-  int32_t key[4][32];         // key index within the unit
-  float w[4][32][G];          // ReLU^2 weights per head
+  int32_t m;                  // survivors in the tile (written by the issuer)
+  int32_t pad[2];
+  int32_t key[4 * 32];        // key index within the unit: [quarter][32], then flat [m]
+  float w[4 * 32][G];         // ReLU^2 weights per head, same two layouts
 };
 
 template <int G>
@@ -72,10 +74,10 @@ struct Smem {
   static constexpr int ring_off = q_off + 2 * kQBufBytes;
   static constexpr int wslot_off = ring_off + kRing * kRowBytes;
   static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G>));
-  static constexpr int misc_off = hist_off + kHistBins * 4;
+  static constexpr int misc_off = hist_off + 2 * kHistBins * 4;   // one histogram per segment parity
   static constexpr int end_off = misc_off + 64;                 // int64 per W slot
   static constexpr int bar_off = end_off + kWSlots * 8;
-  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 4 + 3 * kWSlots;
+  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 6 + 3 * kWSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
 };
@@ -131,11 +133,12 @@ __device__ __forceinline__ void next_tile(int64_t &tl, int64_t &u, int64_t TU) {
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     full_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_q, const FullParams p) {
+                       const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_v, const FullParams p) {
   using L = Smem<G>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // offset arithmetic on the shared array keeps every access in the shared state space
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *sK = smem + L::k_off;
   uint8_t *sQ = smem + L::q_off;
   uint8_t *sRing = smem + L::ring_off;
@@ -158,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *wfull = qempty + 2;          // survivor list written
   uint64_t *wempty = wfull + kWSlots;    // survivor list and its V rows consumed
   uint64_t *vfull = wempty + kWSlots;    // V rows of a tile landed
+  uint64_t *hfree = vfull + kWSlots;     // histogram of a segment parity flushed and cleared
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -184,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&wempty[w], 4);
       mbar_init(&vfull[w], 1);
     }
+    mbar_init(&hfree[0], 1);
+    mbar_init(&hfree[1], 1);
     *s_abort = 0;
     *s_k_issued = 0;
     *s_q_issued = 0;
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // them anyway so no stale bits reach the tensor core.
   for (int i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0u;
+  for (int i = threadIdx.x; i < 2 * kHistBins; i += kThreads) s_hist[i] = 0u;
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
     tmem_alloc(s_tmem, kTmemCols);
@@ -210,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_v);
       const uint64_t policy = policy_evict_first();
       int64_t u = u0, tl = tl0;
       int seg = -1;
@@ -301,7 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every epilogue warp takes the new unit's query norms, whichever tiles it owns
         ++seg;
         const int qb = seg & 1;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&qfull[qb], (seg >> 1) & 1));
+        const bool ok = __all_sync(
+            0xffffffffu, mbar_wait(&qfull[qb], (seg >> 1) & 1) &&
+                             (seg < 2 || p.sel == nullptr ||
+                              mbar_wait(&hfree[qb], ((seg >> 1) - 1) & 1)));
         if (!ok) {
           set_abort(s_abort, p.flags);
           break;
@@ -381,16 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       WSlot<G> &ws = wslots[slot];
       if (p.sel != nullptr) {
-        if (valid) p.sel[u * p.ncap + j] = sigma;
-        ws.bin[row] = valid ? static_cast<uint16_t>(order_key(sigma) >> 21) : kNoBin;
+        // one shared-memory atomic per distinct bin in the warp
+        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+          p.sel[u * p.ncap + j] = sigma;
+          const uint32_t bin = order_key(sigma) >> 21;
+          const uint32_t peers = __match_any_sync(vmask, bin);
+          if (lane == __ffs(peers) - 1)
+            atomicAdd(&s_hist[(seg & 1) * kHistBins + bin], static_cast<uint32_t>(__popc(peers)));
+        }
       }
       const bool surv = valid && sigma > 0.0f;
       const uint32_t bal = __ballot_sync(0xffffffffu, surv);
       if (surv) {
-        const int r = __popc(bal & lanemask_lt);
-        ws.key[quarter][r] = static_cast<int32_t>(j);
+        const int r = quarter * 32 + __popc(bal & lanemask_lt);
+        ws.key[r] = static_cast<int32_t>(j);
 #pragma unroll
-        for (int h = 0; h < G; ++h) ws.w[quarter][r][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
+        for (int h = 0; h < G; ++h) ws.w[r][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
       }
       if (lane == 0) ws.cnt[quarter] = __popc(bal);
       __syncwarp();
@@ -403,8 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bulk-copies the surviving keys' V rows into a ring of kRing rows.
     int64_t u = u0, tl = tl0;
     int64_t i = 0, rows_issued = 0, rows_freed = 0, oldest = 0;
+    int seg = -1;
     for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
       if (__any_sync(0xffffffffu, *s_abort)) break;
+      if (i == 0 || tl == 0) ++seg;
       const int slot = static_cast<int>(i % kWSlots);
       // the epilogue refilled this slot, so tile i - kWSlots and older are consumed
       while (oldest <= i - kWSlots) {
@@ -419,14 +438,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       WSlot<G> &ws = wslots[slot];
       const int c0 = ws.cnt[0], c1 = ws.cnt[1], c2 = ws.cnt[2], c3 = ws.cnt[3];
       const int m = c0 + c1 + c2 + c3;
-      if (p.sel != nullptr) {
+      const int m4 = (m + 3) & ~3;  // ring rows taken: whole groups of four
+      // flatten the four quarter lists in place (each lane moves at most four entries)
+      {
+        int32_t kk[4];
+        float ww[4][G];
 #pragma unroll
-        for (int r = lane; r < kTileKeys; r += 32) {
-          const uint16_t bn = ws.bin[r];
-          if (bn != kNoBin) atomicAdd(&s_hist[bn], 1u);
+        for (int r = 0; r < 4; ++r) {
+          const int e = lane + 32 * r;
+          if (e < m) {
+            const int q = (e >= c0) + (e >= c0 + c1) + (e >= c0 + c1 + c2);
+            const int src = 32 * q + e - (q == 0 ? 0 : q == 1 ? c0 : q == 2 ? c0 + c1 : c0 + c1 + c2);
+            kk[r] = ws.key[src];
+#pragma unroll
+            for (int h = 0; h < G; ++h) ww[r][h] = ws.w[src][h];
+          }
         }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int e = lane + 32 * r;
+          if (e < m) {
+            ws.key[e] = kk[r];
+#pragma unroll
+            for (int h = 0; h < G; ++h) ws.w[e][h] = ww[r][h];
+          }
+        }
+        __syncwarp();
       }
-      while (ok && rows_issued + m - rows_freed > kRing) {
+      while (ok && rows_issued + m4 - rows_freed > kRing) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&wempty[oldest % kWSlots], (oldest / kWSlots) & 1));
         rows_freed = s_end[oldest % kWSlots];
@@ -438,33 +478,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         ws.row0 = static_cast<int32_t>(rows_issued % kRing);
-        s_end[slot] = rows_issued + m;
+        ws.m = m;
+        s_end[slot] = rows_issued + m4;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(m * kRowBytes));
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(m4 * kRowBytes));
       __syncwarp();
-      for (int e = lane; e < m; e += 32) {
-        int q = 0, k = e;
-        if (k >= c0) { k -= c0; q = 1;
-          if (k >= c1) { k -= c1; q = 2;
-            if (k >= c2) { k -= c2; q = 3; } } }
-        const int64_t key = ws.key[q][k];
+      if (4 * lane < m) {
+        // one gather of four V rows per lane; a short last group repeats its last row
+        const int e = 4 * lane;
+        const int32_t base = static_cast<int32_t>(u * p.ncap);
+        const int32_t y0 = base + ws.key[e];
+        const int32_t y1 = base + ws.key[min(e + 1, m - 1)];
+        const int32_t y2 = base + ws.key[min(e + 2, m - 1)];
+        const int32_t y3 = base + ws.key[min(e + 3, m - 1)];
         const int dst = static_cast<int>((rows_issued + e) % kRing);
-        bulk_load(sRing + dst * kRowBytes, p.v + (u * p.ncap + key) * kRowBytes, kRowBytes,
-                  &vfull[slot]);
+        tma_gather4(sRing + dst * kRowBytes, &tm_v, &vfull[slot], 0, y0, y1, y2, y3);
       }
-      rows_issued += m;
+      rows_issued += m4;
       if (lane == 0) *s_v_issued = static_cast<int>(i + 1);
       if (p.sel != nullptr && (t + 1 == te || tl + 1 == p.TU)) {
-        __syncwarp();
+        // every tile of this unit has been scored (their lists were waited for in order):
+        // move the segment's histogram to global memory and hand the buffer back
+        uint32_t *h = s_hist + (seg & 1) * kHistBins;
         for (int bin = lane; bin < kHistBins; bin += 32) {
-          const uint32_t cnt = s_hist[bin];
+          const uint32_t cnt = h[bin];
           if (cnt) {
             atomicAdd(&p.hist[u * kHistBins + bin], cnt);
-            s_hist[bin] = 0u;
+            h[bin] = 0u;
           }
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(&hfree[seg & 1]);
       }
     }
     __syncwarp();
@@ -493,17 +538,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const WSlot<G> &ws = wslots[slot];
-      int e = ws.row0;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const int cq = ws.cnt[q];
-        for (int k = 0; k < cq; ++k, ++e) {
-          const uint2 raw = *reinterpret_cast<const uint2 *>(sRing + (e % kRing) * kRowBytes + lane * 8);
-          const float v0 = bf16lo(raw.x), v1 = bf16hi(raw.x), v2 = bf16lo(raw.y),
-                      v3 = bf16hi(raw.y);
+      const int row0 = ws.row0, m = ws.m;
+      for (int e0 = 0; e0 < m; e0 += 4) {
+        uint2 raw[4];
+        float wv[4][HPW];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          // rows past m belong to the tile's last gather group: read them, weigh them 0
+          const int e = e0 + r;
+          raw[r] = *reinterpret_cast<const uint2 *>(sRing + ((row0 + e) & (kRing - 1)) * kRowBytes + lane * 8);
+#pragma unroll
+          for (int hh = 0; hh < HPW; ++hh) wv[r][hh] = e < m ? ws.w[e][aw + 4 * hh] : 0.0f;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float v0 = bf16lo(raw[r].x), v1 = bf16hi(raw[r].x), v2 = bf16lo(raw[r].y),
+                      v3 = bf16hi(raw[r].y);
 #pragma unroll
           for (int hh = 0; hh < HPW; ++hh) {
-            const float w = ws.w[q][k][aw + 4 * hh];
+            const float w = wv[r][hh];
             acc[hh][0] = fmaf(w, v0, acc[hh][0]);
             acc[hh][1] = fmaf(w, v1, acc[hh][1]);
             acc[hh][2] = fmaf(w, v2, acc[hh][2]);
@@ -512,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      seg_surv += e - ws.row0;
+      seg_surv += m;
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[slot]);
       if (t + 1 == te || tl + 1 == p.TU) {
@@ -591,12 +644,13 @@ __global__ void __launch_bounds__(256)
 
 template <int G>
 cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                                 const FullParams &p, cudaStream_t stream) {
+                                 const CUtensorMap &tm_v, const FullParams &p,
+                                 cudaStream_t stream) {
   const int smem = Smem<G>::alloc;
   cudaError_t e = cudaFuncSetAttribute(full_decode_kernel<G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  full_decode_kernel<G><<<p.P, kThreads, smem, stream>>>(tm_k, tm_q, p);
+  full_decode_kernel<G><<<p.P, kThreads, smem, stream>>>(tm_k, tm_q, tm_v, p);
   return cudaGetLastError();
 }
 
@@ -621,7 +675,7 @@ size_t full_workspace_bytes(int64_t units, int G, int sm_count) {
 }
 
 cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                               const void *v_cache, float *sel_scores, uint32_t *sel_hist,
+                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores, uint32_t *sel_hist,
                                float *records, uint32_t *flags, const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
                                cudaStream_t stream) {
@@ -642,8 +696,8 @@ cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap
   p.rec_stride = full_record_floats(G);
   p.alpha = alpha;
   p.eps = eps;
-  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, p, stream);
-  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, p, stream);
+  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, tm_v, p, stream);
+  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, tm_v, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -35,7 +35,7 @@ int full_record_floats(int G);
 size_t full_workspace_bytes(int64_t units, int G, int sm_count);
 
 cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                               const void *v_cache, float *sel_scores, uint32_t *sel_hist,
+                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores, uint32_t *sel_hist,
                                float *records, uint32_t *flags, const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
                                cudaStream_t stream);
