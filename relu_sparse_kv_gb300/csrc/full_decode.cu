@@ -5,20 +5,26 @@
 // divided by a constant plus the sum of weights) and "Skipping V" (a value row is
 // read only when some query head of the KV group gives its key a weight above zero).
 //
-// One persistent CTA per SM walks a contiguous run of 128-key tiles of the
-// flattened (unit, tile) sequence, unit = (batch, KV head).  Warp roles:
-//   warp 0   TMA producer: 32 KB K tiles (two 64-column boxes, 128-byte swizzle)
-//            into a 4-stage ring; the unit's G query rows when the unit changes.
-//   warp 1   tcgen05 issuer: D[128 keys x 16] = K_tile . Q^T (raw bf16 operands,
-//            fp32 accumulation in tensor memory, double-buffered columns).
-//   warps 2-5  epilogue, one thread per key: reads its G dot products from tensor
-//            memory and its key row from shared memory (sum of squares), forms
-//            s_h = dot_h * alpha*rq_h * rk, sigma = max_h s_h, writes sigma and the
-//            2048-bin histogram of its order key, compacts the keys with sigma > 0
-//            and fetches only their V rows with bulk copies.
-//   warps 6-9  V accumulators: num_h += w_h v, den_h += w_h over the fetched rows;
-//            at the end of each stretch of a unit they write a partial record.
-// A second kernel sums the partial records of each unit and divides.
+// One persistent CTA per SM walks a contiguous run of 128-key tiles of the flattened
+// (unit, tile) sequence, unit = (batch, KV head).  Warp roles:
+//   warp 0     TMA producer: 32 KB K tiles (two 64-column boxes, 128-byte swizzle) into
+//              a 4-stage ring; the unit's G query rows when the unit changes.
+//   warps 1, 19  tcgen05 issuers taking alternate tiles: D[128 keys x 16] = K . Q^T
+//              (raw bf16 operands, fp32 in tensor memory), one independent MMA per
+//              16-dim k-step; four tiles in flight use all 512 columns.
+//   warps 15-18  key norms, one thread per key as soon as a tile lands:
+//              rk = 1/sqrt(mean(k^2) + eps), handed to the epilogue through a small
+//              shared-memory ring; the K stage is free once these and the MMAs are done.
+//   warps 2-9  two epilogue warpgroups taking alternate tiles, one thread per key:
+//              s_h = dot_h * alpha*rq_h * rk, sigma = max_h s_h; writes sigma and its
+//              histogram bin, and lists the keys with sigma > 0 with their ReLU^2
+//              weights (one list per warp, no cross-warp synchronisation).
+//   warp 10    V issuer: flattens each tile's lists in tile order and fetches only the
+//              listed V rows, four per TMA gather, into a 128-row ring; flushes the
+//              histogram of a unit when its last tile has been listed.
+//   warps 11-14  V accumulators (heads split over warps): num_h += w_h v, den_h += w_h
+//              in tile order; at the end of each stretch of a unit they write a partial
+//              record.  A second kernel sums the records of each unit and divides.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -39,18 +45,26 @@ constexpr int kWSlots = EMBLA_W_SLOTS;             // per-tile survivor lists in
 constexpr int kRing = EMBLA_V_RING_ROWS;           // V rows in flight
 constexpr int kGroups = 2;                         // epilogue warpgroups, alternating tiles
 constexpr int kAccBufs = 2 * kGroups;              // tensor-memory accumulators
+constexpr int kNormSlots = 8;                      // per-tile key-norm arrays in flight
 constexpr int kRowBytes = kHeadDim * 2;            // 256
 constexpr int kTileBytes = kTileKeys * kRowBytes;  // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;         // 128 rows x 64 dims
 constexpr int kQBufBytes = 4096;                   // 16 rows x 128 dims (MMA N = 16)
 constexpr int kQHalfBytes = kQBufBytes / 2;
-constexpr int kMmaN = 16;
-constexpr int kTmemCols = kAccBufs * kMmaN;        // 64
+constexpr int kMmaN = 16;                          // scores: 128 keys x 16 query rows
+constexpr int kKSteps = kHeadDim / 16;             // MMA k-steps per tile
+// Each k-step writes its own accumulator, so a tile's eight MMAs do not wait on each
+// other; the epilogue adds the eight partial dot products.
+constexpr int kAccCols = kKSteps * kMmaN;          // 128 columns per tile
+constexpr int kTmemCols = kAccBufs * kAccCols;     // 512
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN);
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
 constexpr int kWarpIssuer = kWarpEpi + 4 * kGroups;
 constexpr int kWarpAcc = kWarpIssuer + 1;
-constexpr int kThreads = (kWarpAcc + 4) * 32;      // 480
+constexpr int kWarpNorm = kWarpAcc + 4;
+constexpr int kWarpMma2 = kWarpNorm + 4;           // second MMA issuer (odd tiles)
+constexpr int kMmaWarps = 2;
+constexpr int kThreads = (kWarpMma2 + 1) * 32;     // 640
 static_assert(kRing >= kTileKeys, "a whole tile of survivors must fit the V ring");
 static_assert((kRing & (kRing - 1)) == 0, "the V ring size is a power of two");
 
@@ -74,10 +88,11 @@ struct Smem {
   static constexpr int ring_off = q_off + 2 * kQBufBytes;
   static constexpr int wslot_off = ring_off + kRing * kRowBytes;
   static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G>));
-  static constexpr int misc_off = hist_off + 2 * kHistBins * 4;   // one histogram per segment parity
+  static constexpr int rk_off = hist_off + 2 * kHistBins * 4;     // one histogram per segment parity
+  static constexpr int misc_off = rk_off + kNormSlots * kTileKeys * 4;
   static constexpr int end_off = misc_off + 64;                 // int64 per W slot
   static constexpr int bar_off = end_off + kWSlots * 8;
-  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 6 + 3 * kWSlots;
+  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 6 + 3 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
 };
@@ -105,25 +120,13 @@ __device__ __forceinline__ float sumsq8(const uint4 &v) {
   return a + b;
 }
 
-// acc[0..3] += squares of the 8 bf16 values, spread over four independent chains
-__device__ __forceinline__ void sumsq8_acc(const uint4 &v, float (&acc)[4]) {
-  acc[0] = fmaf(bf16lo(v.x), bf16lo(v.x), acc[0]);
-  acc[1] = fmaf(bf16hi(v.x), bf16hi(v.x), acc[1]);
-  acc[2] = fmaf(bf16lo(v.y), bf16lo(v.y), acc[2]);
-  acc[3] = fmaf(bf16hi(v.y), bf16hi(v.y), acc[3]);
-  acc[0] = fmaf(bf16lo(v.z), bf16lo(v.z), acc[0]);
-  acc[1] = fmaf(bf16hi(v.z), bf16hi(v.z), acc[1]);
-  acc[2] = fmaf(bf16lo(v.w), bf16lo(v.w), acc[2]);
-  acc[3] = fmaf(bf16hi(v.w), bf16hi(v.w), acc[3]);
-}
-
 __device__ __forceinline__ void set_abort(volatile int *abort_flag, uint32_t *flags) {
   *abort_flag = 1;
   atomicOr(flags, kFlagWaitTimeout);
 }
 
 // Advance (tile-in-unit, unit) to the next tile of the flattened sequence.
-__device__ __forceinline__ void next_tile(int64_t &tl, int64_t &u, int64_t TU) {
+__device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
   if (++tl == TU) {
     tl = 0;
     ++u;
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sRing = smem + L::ring_off;
   WSlot<G> *wslots = reinterpret_cast<WSlot<G> *>(smem + L::wslot_off);
   uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem + L::hist_off);
+  float *s_rk = reinterpret_cast<float *>(smem + L::rk_off);
   int *misc = reinterpret_cast<int *>(smem + L::misc_off);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
   volatile int *s_abort = misc + 1;
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t *s_end = reinterpret_cast<int64_t *>(smem + L::end_off);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
   uint64_t *full = bars;                 // K tile landed
-  uint64_t *empty = full + kStages;      // K tile consumed (MMA and sum of squares)
+  uint64_t *empty = full + kStages;      // K tile consumed (MMA and key norms)
   uint64_t *accf = empty + kStages;      // accumulator written
   uint64_t *acce = accf + kAccBufs;      // accumulator read
   uint64_t *qfull = acce + kAccBufs;     // query rows landed
@@ -162,18 +166,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *wempty = wfull + kWSlots;    // survivor list and its V rows consumed
   uint64_t *vfull = wempty + kWSlots;    // V rows of a tile landed
   uint64_t *hfree = vfull + kWSlots;     // histogram of a segment parity flushed and cleared
+  uint64_t *rkfull = hfree + 2;          // key norms of a tile written
+  uint64_t *rkempty = rkfull + kNormSlots;  // key norms of a tile read
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
   const int64_t tb = split_first_tile(cta, p.T, p.P);
   const int64_t te = split_first_tile(cta + 1, p.T, p.P);
-  const int64_t u0 = tb / p.TU, tl0 = tb - u0 * p.TU;
+  // tile counts fit 32 bits: the host limits units * cache_stride to 2^31 rows
+  const int ntiles = static_cast<int>(te - tb);
+  const int TU = static_cast<int>(p.TU);
+  const int u0 = static_cast<int>(tb / p.TU), tl0 = static_cast<int>(tb - tb / p.TU * p.TU);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
+      mbar_init(&empty[s], 5);  // MMA commit + the four norm warps
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&accf[b], 1);
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&qfull[q], 1);
-      mbar_init(&qempty[q], 1 + 4 * kGroups);
+      mbar_init(&qempty[q], kMmaWarps + 4 * kGroups);
     }
     for (int w = 0; w < kWSlots; ++w) {
       mbar_init(&wfull[w], 4);
@@ -190,6 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&hfree[0], 1);
     mbar_init(&hfree[1], 1);
+    for (int r = 0; r < kNormSlots; ++r) {
+      mbar_init(&rkfull[r], 4);
+      mbar_init(&rkempty[r], 4);
+    }
     *s_abort = 0;
     *s_k_issued = 0;
     *s_q_issued = 0;
@@ -218,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_v);
       const uint64_t policy = policy_evict_first();
-      int64_t u = u0, tl = tl0;
+      int u = u0, tl = tl0;
       int seg = -1;
-      int64_t i = 0;
-      for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+      int s = 0, sphase = 0;
+      for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
         if (*s_abort) break;
         if (i == 0 || tl == 0) {
           ++seg;
@@ -236,56 +249,88 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sQ + qb * kQBufBytes + kQHalfBytes, &tm_q, &qfull[qb], 64, qrow);
           *s_q_issued = seg + 1;
         }
-        const int s = static_cast<int>(i % kStages);
-        if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1)) {
+        if (i >= kStages && !mbar_wait(&empty[s], sphase ^ 1)) {
           set_abort(s_abort, p.flags);
           break;
         }
         mbar_arrive_expect_tx(&full[s], kTileBytes);
-        const int32_t row = static_cast<int32_t>(u * p.ncap + tl * kTileKeys);
+        const int32_t row = static_cast<int32_t>(static_cast<int64_t>(u) * p.ncap) + tl * kTileKeys;
         tma_load_2d_hint(sK + s * kTileBytes, &tm_k, &full[s], 0, row, policy);
         tma_load_2d_hint(sK + s * kTileBytes + kHalfBytes, &tm_k, &full[s], 64, row, policy);
-        *s_k_issued = static_cast<int>(i + 1);
+        *s_k_issued = i + 1;
+        if (++s == kStages) {
+          s = 0;
+          sphase ^= 1;
+        }
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMma || warp == kWarpMma2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Two issuing threads take alternate tiles: every tcgen05 instruction and barrier
+    // check costs a single thread a long latency, so one thread alone cannot keep up.
+    const int mw = warp == kWarpMma ? 0 : 1;
     if (lane == 0) {
-      int64_t u = u0, tl = tl0;
-      int seg = -1, qb = 0;
-      int64_t i = 0, issued = 0;
-      for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+      // descriptors are built once; per k-step only their start-address field moves
+      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(sK));
+      const uint64_t qdesc0 = smem_desc_sw128(smem_u32(sQ));
+      uint64_t qdesc = qdesc0;
+      int tl = tl0, seg = -1, qb = 0, issued = 0;
+      int s = 0, sphase = 0, b = 0, bphase = 0;
+      for (int i = 0; i < ntiles; ++i) {
         if (*s_abort) break;
         if (i == 0 || tl == 0) {
           ++seg;
           qb = seg & 1;
+          qdesc = qdesc0 + static_cast<uint64_t>((qb * kQBufBytes) >> 4);
           if (!mbar_wait(&qfull[qb], (seg >> 1) & 1)) {
             set_abort(s_abort, p.flags);
             break;
           }
         }
-        const int s = static_cast<int>(i % kStages);
-        const int b = static_cast<int>(i % kAccBufs);
-        if (!mbar_wait(&full[s], (i / kStages) & 1) ||
-            (i >= kAccBufs && !mbar_wait(&acce[b], ((i / kAccBufs) - 1) & 1))) {
+        if ((i & 1) != mw) {
+          // not this issuer's tile; it still hands back the query buffer at a unit's end
+          if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qempty[qb]);
+          if (++tl == TU) tl = 0;
+          if (++s == kStages) {
+            s = 0;
+            sphase ^= 1;
+          }
+          if (++b == kAccBufs) {
+            b = 0;
+            bphase ^= 1;
+          }
+          continue;
+        }
+        if (!mbar_wait(&full[s], sphase) || (i >= kAccBufs && !mbar_wait(&acce[b], bphase ^ 1))) {
           set_abort(s_abort, p.flags);
           break;
         }
         tc_fence_after_sync();
-        const uint32_t kaddr = smem_u32(sK + s * kTileBytes);
-        const uint32_t qaddr = smem_u32(sQ + qb * kQBufBytes);
+        const uint64_t adesc = kdesc0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
+        const uint32_t dcol = tmem + b * kAccCols;
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(kaddr + (kk >> 2) * kHalfBytes + (kk & 3) * 32);
-          const uint64_t bdesc = smem_desc_sw128(qaddr + (kk >> 2) * kQHalfBytes + (kk & 3) * 32);
-          tc_mma_bf16(tmem + b * kMmaN, adesc, bdesc, kIdesc, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kKSteps; ++kk) {
+          // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is 32
+          // bytes into a 128-byte row, the second half of the dims starts a new box
+          tc_mma_bf16(dcol + kk * kMmaN, adesc + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4),
+                      qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), kIdesc, 0u);
         }
         tc_commit(&accf[b]);
+        tc_commit(&empty[s]);
         issued = i + 1;
-        if (t + 1 == te || tl + 1 == p.TU) tc_commit(&qempty[qb]);
+        if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qempty[qb]);
+        if (++tl == TU) tl = 0;
+        if (++s == kStages) {
+          s = 0;
+          sphase ^= 1;
+        }
+        if (++b == kAccBufs) {
+          b = 0;
+          bphase ^= 1;
+        }
       }
-      // the accumulators must be idle before the tensor memory is released
+      // this issuer's accumulators must be idle before the tensor memory is released
       if (issued > 0)
         mbar_wait(&accf[(issued - 1) % kAccBufs], ((issued - 1) / kAccBufs) & 1);
     }
@@ -299,10 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float aq[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) aq[h] = 0.0f;
-    int64_t u = u0, tl = tl0;
+    int u = u0, tl = tl0;
     int seg = -1;
-    int64_t i = 0;
-    for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
       if (__any_sync(0xffffffffu, *s_abort)) break;
       if (i == 0 || tl == 0) {
         // every epilogue warp takes the new unit's query norms, whichever tiles it owns
@@ -332,9 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (static_cast<int>(i % kGroups) != group) continue;
       const int b = static_cast<int>(i % kAccBufs);
-      const int s = static_cast<int>(i % kStages);
       const int slot = static_cast<int>(i % kWSlots);
-      bool ok = mbar_wait(&accf[b], (i / kAccBufs) & 1) && mbar_wait(&full[s], (i / kStages) & 1) &&
+      const int ns = static_cast<int>(i % kNormSlots);
+      bool ok = mbar_wait(&accf[b], (i / kAccBufs) & 1) &&
+                mbar_wait(&rkfull[ns], (i / kNormSlots) & 1) &&
                 (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -344,44 +389,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       float dot[G];
       tc_fence_after_sync();
       {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * kMmaN;
-        if constexpr (G == 4) {
-          uint32_t r[4];
-          tmem_load_x4(taddr, r);
-          tmem_wait_ld(r);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * kAccCols;
+        uint32_t r[kKSteps * G];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) dot[h] = __uint_as_float(r[h]);
-        } else {
-          uint32_t r[8];
-          tmem_load_x8(taddr, r);
-          tmem_wait_ld(r);
+        for (int kk = 0; kk < kKSteps; ++kk) {
+          if constexpr (G == 4)
+            tmem_load_x4(taddr + kk * kMmaN, *reinterpret_cast<uint32_t(*)[4]>(&r[kk * G]));
+          else
+            tmem_load_x8(taddr + kk * kMmaN, *reinterpret_cast<uint32_t(*)[8]>(&r[kk * G]));
+        }
+        tmem_wait_ld(r);
 #pragma unroll
-          for (int h = 0; h < 8; ++h) dot[h] = __uint_as_float(r[h]);
+        for (int h = 0; h < G; ++h) {
+          const float p0 = __uint_as_float(r[0 * G + h]) + __uint_as_float(r[1 * G + h]);
+          const float p1 = __uint_as_float(r[2 * G + h]) + __uint_as_float(r[3 * G + h]);
+          const float p2 = __uint_as_float(r[4 * G + h]) + __uint_as_float(r[5 * G + h]);
+          const float p3 = __uint_as_float(r[6 * G + h]) + __uint_as_float(r[7 * G + h]);
+          dot[h] = (p0 + p1) + (p2 + p3);
         }
       }
       tc_fence_before_sync();
+      const float rk = s_rk[ns * kTileKeys + row];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[b]);
-      // this key's sum of squares; chunk order rotated by row so 8 neighbouring rows hit 8
-      // different bank groups (the swizzle permutes chunks within a row)
-      float ss;
-      {
-        const uint8_t *rowp = sK + s * kTileBytes + row * 128;
-        float a0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int pc = (c ^ (row & 7)) * 16;
-          sumsq8_acc(*reinterpret_cast<const uint4 *>(rowp + pc), a0);
-          sumsq8_acc(*reinterpret_cast<const uint4 *>(rowp + kHalfBytes + pc), a1);
-        }
-        ss = ((a0[0] + a0[1]) + (a0[2] + a0[3])) + ((a1[0] + a1[1]) + (a1[2] + a1[3]));
+      if (lane == 0) {
+        mbar_arrive(&acce[b]);
+        mbar_arrive(&rkempty[ns]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
 
-      const int64_t j = tl * kTileKeys + row;
+      const int j = tl * kTileKeys + row;
       const bool valid = j < p.n;
-      const float rk = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
       float sc[G];
       float sigma = -INFINITY;
 #pragma unroll
@@ -394,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one shared-memory atomic per distinct bin in the warp
         const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
         if (valid) {
-          p.sel[u * p.ncap + j] = sigma;
+          p.sel[static_cast<int64_t>(u) * p.ncap + j] = sigma;
           const uint32_t bin = order_key(sigma) >> 21;
           const uint32_t peers = __match_any_sync(vmask, bin);
           if (lane == __ffs(peers) - 1)
@@ -418,10 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ V issuer
     // Reads each tile's survivor list in order, keeps the selection histogram, and
     // bulk-copies the surviving keys' V rows into a ring of kRing rows.
-    int64_t u = u0, tl = tl0;
-    int64_t i = 0, rows_issued = 0, rows_freed = 0, oldest = 0;
+    int u = u0, tl = tl0;
+    int64_t rows_issued = 0, rows_freed = 0;
+    int oldest = 0;
     int seg = -1;
-    for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
       if (__any_sync(0xffffffffu, *s_abort)) break;
       if (i == 0 || tl == 0) ++seg;
       const int slot = static_cast<int>(i % kWSlots);
@@ -487,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (4 * lane < m) {
         // one gather of four V rows per lane; a short last group repeats its last row
         const int e = 4 * lane;
-        const int32_t base = static_cast<int32_t>(u * p.ncap);
+        const int32_t base = static_cast<int32_t>(static_cast<int64_t>(u) * p.ncap);
         const int32_t y0 = base + ws.key[e];
         const int32_t y1 = base + ws.key[min(e + 1, m - 1)];
         const int32_t y2 = base + ws.key[min(e + 2, m - 1)];
@@ -496,21 +533,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_gather4(sRing + dst * kRowBytes, &tm_v, &vfull[slot], 0, y0, y1, y2, y3);
       }
       rows_issued += m4;
-      if (lane == 0) *s_v_issued = static_cast<int>(i + 1);
-      if (p.sel != nullptr && (t + 1 == te || tl + 1 == p.TU)) {
+      if (lane == 0) *s_v_issued = i + 1;
+      if (p.sel != nullptr && (i + 1 == ntiles || tl + 1 == TU)) {
         // every tile of this unit has been scored (their lists were waited for in order):
         // move the segment's histogram to global memory and hand the buffer back
         uint32_t *h = s_hist + (seg & 1) * kHistBins;
         for (int bin = lane; bin < kHistBins; bin += 32) {
           const uint32_t cnt = h[bin];
           if (cnt) {
-            atomicAdd(&p.hist[u * kHistBins + bin], cnt);
+            atomicAdd(&p.hist[static_cast<int64_t>(u) * kHistBins + bin], cnt);
             h[bin] = 0u;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&hfree[seg & 1]);
       }
+    }
+    __syncwarp();
+  } else if (warp >= kWarpNorm) {
+    // ------------------------------------------------------------------ key norms
+    // One thread per key of each landed tile: 1 / sqrt(mean(k^2) + eps).  The stage is
+    // released as soon as these four warps and the tile's MMAs are done with it.
+    const int row = (warp - kWarpNorm) * 32 + lane;
+    for (int i = 0; i < ntiles; ++i) {
+      if (__any_sync(0xffffffffu, *s_abort)) break;
+      const int s = static_cast<int>(i % kStages);
+      const int ns = static_cast<int>(i % kNormSlots);
+      const bool ok = __all_sync(0xffffffffu,
+                                 mbar_wait(&full[s], (i / kStages) & 1) &&
+                                     (i < kNormSlots ||
+                                      mbar_wait(&rkempty[ns], ((i / kNormSlots) - 1) & 1)));
+      if (!ok) {
+        set_abort(s_abort, p.flags);
+        break;
+      }
+      // chunk order rotated by row so 8 neighbouring rows hit 8 different bank groups
+      // (the swizzle permutes 16-byte chunks within a row; the order does not matter)
+      const uint8_t *rowp = sK + s * kTileBytes + row * 128;
+      float a[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) a[c] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int pc = (c ^ (row & 7)) * 16;
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(rowp + pc);
+        const uint4 x1 = *reinterpret_cast<const uint4 *>(rowp + kHalfBytes + pc);
+        sq_acc_bf16x2(x0.x, a[0], a[1]);
+        sq_acc_bf16x2(x0.y, a[2], a[3]);
+        sq_acc_bf16x2(x0.z, a[4], a[5]);
+        sq_acc_bf16x2(x0.w, a[6], a[7]);
+        sq_acc_bf16x2(x1.x, a[0], a[1]);
+        sq_acc_bf16x2(x1.y, a[2], a[3]);
+        sq_acc_bf16x2(x1.z, a[4], a[5]);
+        sq_acc_bf16x2(x1.w, a[6], a[7]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+      s_rk[ns * kTileKeys + row] = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rkfull[ns]);
     }
     __syncwarp();
   } else {
@@ -527,9 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 0; d < 4; ++d) acc[hh][d] = 0.0f;
     }
     int seg_surv = 0;
-    int64_t u = u0, tl = tl0;
-    int64_t i = 0;
-    for (int64_t t = tb; t < te; ++t, ++i, next_tile(tl, u, p.TU)) {
+    int u = u0, tl = tl0;
+    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
       if (__any_sync(0xffffffffu, *s_abort)) break;
       const int slot = static_cast<int>(i % kWSlots);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&vfull[slot], (i / kWSlots) & 1));
@@ -568,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       seg_surv += m;
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[slot]);
-      if (t + 1 == te || tl + 1 == p.TU) {
+      if (i + 1 == ntiles || tl + 1 == TU) {
         float *r = p.rec + (cta + u) * p.rec_stride;
 #pragma unroll
         for (int hh = 0; hh < HPW; ++hh) {

@@ -219,6 +219,20 @@ __device__ __forceinline__ void tmem_load_x8(uint32_t taddr, uint32_t (&r)[8]) {
                : "r"(taddr));
 }
 
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_load_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
 // Wait for this thread's tcgen05.ld results; the registers are passed through so the
 // compiler cannot read them before the wait.
 template <int N>
@@ -233,6 +247,17 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[N]) {
 // bf16 pair in a 32-bit word -> two floats (exact).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// a += lo(w)^2, b += hi(w)^2 for the two bf16 values packed in w: bf16 products are exact
+// in fp32, the additions round in fp32 (the same result as widening first).
+__device__ __forceinline__ void sq_acc_bf16x2(uint32_t w, float &a, float &b) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, lo, lo, %0;\n\t"
+      "fma.rn.f32.bf16 %1, hi, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(w));
+}
 
 // Order-preserving 32-bit key of a float (-0 folded onto +0): larger float, larger key.
 __device__ __forceinline__ uint32_t order_key(float s) {
