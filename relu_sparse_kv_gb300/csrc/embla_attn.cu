@@ -172,22 +172,27 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
     st = cuda_status(cudaMemsetAsync(sel_hist, 0, static_cast<size_t>(units) * kHistBins * 4, s));
     if (st != EMBLA_OK) return st;
   }
-  if (sp.tiles > 0) {
-    CUtensorMap tm_k, tm_q, tm_v;
-    if (!encode_rows(&tm_k, k_cache, static_cast<uint64_t>(units * shape->cache_stride),
-                     kTileKeys, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-        !encode_rows(&tm_q, q, static_cast<uint64_t>(shape->batch) * shape->n_q_heads,
-                     static_cast<uint32_t>(G), CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-        !encode_row_gather(&tm_v, v_cache, static_cast<uint64_t>(units * shape->cache_stride)))
-      return EMBLA_ERR_CUDA;
-    st = cuda_status(launch_full_decode(G, tm_k, tm_q, tm_v, v_cache, sel_scores, sel_hist,
-                                        static_cast<float *>(workspace), flags, sp,
-                                        shape->ctx_len, shape->cache_stride, shape->n_q_heads,
-                                        shape->n_kv_heads, alpha, eps, s));
-    if (st != EMBLA_OK) return st;
+  if (sp.tiles == 0) {
+    // no keys: every output is 0 and nothing survives
+    st = cuda_status(cudaMemsetAsync(out, 0, static_cast<size_t>(units) * G * kHeadDim * 4, s));
+    if (st == EMBLA_OK) st = cuda_status(cudaMemsetAsync(n_surv, 0, static_cast<size_t>(units) * 4, s));
+    return st;
   }
-  return cuda_status(launch_full_combine(G, static_cast<const float *>(workspace), sp, c, out,
-                                         n_surv, s));
+  int32_t *arrivals = full_arrivals(workspace, units, G, sms);
+  st = cuda_status(cudaMemsetAsync(arrivals, 0, static_cast<size_t>(units) * 4 * sizeof(int32_t), s));
+  if (st != EMBLA_OK) return st;
+  CUtensorMap tm_k, tm_q, tm_v;
+  if (!encode_rows(&tm_k, k_cache, static_cast<uint64_t>(units * shape->cache_stride), kTileKeys,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_rows(&tm_q, q, static_cast<uint64_t>(shape->batch) * shape->n_q_heads,
+                   static_cast<uint32_t>(G), CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !encode_row_gather(&tm_v, v_cache, static_cast<uint64_t>(units * shape->cache_stride)))
+    return EMBLA_ERR_CUDA;
+  return cuda_status(launch_full_decode(G, tm_k, tm_q, tm_v, v_cache, sel_scores, sel_hist,
+                                        workspace, arrivals, out, n_surv, c, flags, sp,
+                                        shape->ctx_len,
+                                        shape->cache_stride, shape->n_q_heads, shape->n_kv_heads,
+                                        alpha, eps, s));
 }
 
 size_t embla_select_topk_workspace_size(const embla_shape *shape, int32_t topk, int32_t recent) {

@@ -24,7 +24,8 @@
 //              histogram of a unit when its last tile has been listed.
 //   warps 11-14  V accumulators (heads split over warps): num_h += w_h v, den_h += w_h
 //              in tile order; at the end of each stretch of a unit they write a partial
-//              record.  A second kernel sums the records of each unit and divides.
+//              record, and the last warp to publish a unit's record sums its records and
+//              writes out = num / (c + den) and the survivor count.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -102,6 +103,10 @@ struct FullParams {
   float *sel;        // selection scores or null
   uint32_t *hist;    // selection histogram or null
   float *rec;        // partial records
+  int32_t *arrivals; // per unit and accumulator warp: record parts published so far (zeroed by the host call)
+  float *out;        // [units][G][D]
+  int32_t *n_surv;   // [units]
+  float c;           // normaliser constant
   uint32_t *flags;
   int64_t T, TU, n, ncap;
   int32_t P, Hq, Hkv, rec_stride;
@@ -662,6 +667,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (aw == 0 && lane == 0) reinterpret_cast<int32_t *>(r)[G * kHeadDim + G] = seg_surv;
         seg_surv = 0;
+        // Every CTA that worked on unit u publishes its part of the record; for each
+        // accumulator warp (head group) the last CTA to count itself in sums that head
+        // group over the unit's records, in CTA order, and writes its outputs.
+        const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
+        const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
+        const int parts = static_cast<int>(c1 - c0 + 1);
+        __threadfence();  // each lane's part of the record is visible before the count
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4 + aw], 1) == parts - 1;
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();
+          float *o = p.out + static_cast<int64_t>(u) * G * kHeadDim;
+#pragma unroll
+          for (int hh = 0; hh < HPW; ++hh) {
+            const int h = aw + 4 * hh;
+            float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float dsum = 0.0f;
+            for (int64_t cc = c0; cc <= c1; ++cc) {
+              const float *rr = p.rec + (cc + u) * p.rec_stride;  // written by other SMs: read L2
+              const float4 x = __ldcg(reinterpret_cast<const float4 *>(rr + h * kHeadDim + d0));
+              num.x += x.x;
+              num.y += x.y;
+              num.z += x.z;
+              num.w += x.w;
+              dsum += __ldcg(rr + G * kHeadDim + h);
+            }
+            const float z = p.c + dsum;
+            *reinterpret_cast<float4 *>(o + h * kHeadDim + d0) =
+                z != 0.0f ? make_float4(num.x / z, num.y / z, num.z / z, num.w / z)
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          }
+          if (aw == 0 && lane == 0) {
+            int32_t tot = 0;
+            for (int64_t cc = c0; cc <= c1; ++cc)
+              tot += __ldcg(reinterpret_cast<const int32_t *>(p.rec + (cc + u) * p.rec_stride) +
+                            G * kHeadDim + G);
+            p.n_surv[u] = tot;
+          }
+        }
       }
     }
     __syncwarp();
@@ -688,38 +733,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-template <int G>
-__global__ void __launch_bounds__(256)
-    full_combine_kernel(const float *__restrict__ rec, int rec_stride, int64_t T, int32_t P,
-                        int64_t TU, float c, float *__restrict__ out, int32_t *__restrict__ n_surv) {
-  const int64_t u = blockIdx.x;
-  float *o = out + u * G * kHeadDim;
-  if (TU == 0) {
-    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) o[i] = 0.0f;
-    if (threadIdx.x == 0) n_surv[u] = 0;
-    return;
-  }
-  const int64_t c0 = split_cta_of_tile(u * TU, T, P);
-  const int64_t c1 = split_cta_of_tile(u * TU + TU - 1, T, P);
-  for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
-    const int h = i / kHeadDim;
-    float num = 0.0f, den = 0.0f;
-    for (int64_t cc = c0; cc <= c1; ++cc) {
-      const float *r = rec + (cc + u) * rec_stride;
-      num += r[i];
-      den += r[G * kHeadDim + h];
-    }
-    const float z = c + den;
-    o[i] = (z != 0.0f) ? num / z : 0.0f;
-  }
-  if (threadIdx.x == 0) {
-    int32_t s = 0;
-    for (int64_t cc = c0; cc <= c1; ++cc)
-      s += reinterpret_cast<const int32_t *>(rec + (cc + u) * rec_stride)[G * kHeadDim + G];
-    n_surv[u] = s;
   }
 }
 
@@ -751,13 +764,25 @@ int full_record_floats(int G) {
   return (f + 3) & ~3;
 }
 
+static size_t full_records_bytes(int64_t units, int G, int sm_count) {
+  return (static_cast<size_t>(units + sm_count) * full_record_floats(G) * sizeof(float) + 255) &
+         ~static_cast<size_t>(255);
+}
+
 size_t full_workspace_bytes(int64_t units, int G, int sm_count) {
-  return static_cast<size_t>(units + sm_count) * full_record_floats(G) * sizeof(float);
+  return full_records_bytes(units, G, sm_count) + static_cast<size_t>(units) * 4 * sizeof(int32_t);
+}
+
+int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count) {
+  return reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                     full_records_bytes(units, G, sm_count));
 }
 
 cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores, uint32_t *sel_hist,
-                               float *records, uint32_t *flags, const FullSplit &sp, int64_t n,
+                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores,
+                               uint32_t *sel_hist, void *workspace, int32_t *arrivals,
+                               float *out, int32_t *n_surv, float c, uint32_t *flags,
+                               const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
                                cudaStream_t stream) {
   if (sp.tiles == 0) return cudaSuccess;
@@ -765,7 +790,11 @@ cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap
   p.v = static_cast<const uint8_t *>(v_cache);
   p.sel = sel_scores;
   p.hist = sel_hist;
-  p.rec = records;
+  p.rec = static_cast<float *>(workspace);
+  p.arrivals = arrivals;
+  p.out = out;
+  p.n_surv = n_surv;
+  p.c = c;
   p.flags = flags;
   p.T = sp.tiles;
   p.TU = sp.tiles_per_unit;
@@ -780,22 +809,6 @@ cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap
   if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, tm_v, p, stream);
   if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, tm_v, p, stream);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_full_combine(int G, const float *records, const FullSplit &sp, float c,
-                                float *out, int32_t *n_surv, cudaStream_t stream) {
-  if (sp.units == 0) return cudaSuccess;
-  const int stride = full_record_floats(G);
-  const dim3 grid(static_cast<unsigned>(sp.units));
-  if (G == 4)
-    full_combine_kernel<4><<<grid, 256, 0, stream>>>(records, stride, sp.tiles, sp.ctas,
-                                                     sp.tiles_per_unit, c, out, n_surv);
-  else if (G == 8)
-    full_combine_kernel<8><<<grid, 256, 0, stream>>>(records, stride, sp.tiles, sp.ctas,
-                                                     sp.tiles_per_unit, c, out, n_surv);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
 }
 
 }  // namespace embla

@@ -34,13 +34,16 @@ FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count);
 int full_record_floats(int G);
 size_t full_workspace_bytes(int64_t units, int G, int sm_count);
 
+// The arrival counters (4 per unit) at the end of the full-decode workspace (zeroed per call).
+int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count);
+
 cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores, uint32_t *sel_hist,
-                               float *records, uint32_t *flags, const FullSplit &sp, int64_t n,
+                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores,
+                               uint32_t *sel_hist, void *workspace, int32_t *arrivals,
+                               float *out, int32_t *n_surv, float c, uint32_t *flags,
+                               const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
                                cudaStream_t stream);
-cudaError_t launch_full_combine(int G, const float *records, const FullSplit &sp, float c,
-                                float *out, int32_t *n_surv, cudaStream_t stream);
 
 size_t select_workspace_bytes(int64_t units, int64_t ctx_len);
 cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int64_t units,
