@@ -99,6 +99,40 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Full (ReLU^2) layer decode on library-owned scratch.  The Embla pages have
+ * no counterpart to this call: it computes exactly what embla_full_decode
+ * computes, with the same arguments and results, but takes no workspace.  It
+ * is meant for callers that cannot hand the library device memory for
+ * scratch: an engine that lays out all of its device memory once at start-up
+ * and must not allocate while it decodes (a cudaMalloc can stall the whole
+ * device and breaks up a pooled allocator), or a C program with no device
+ * allocator of its own.  Nothing is allocated, here or inside: the scratch is
+ * one fixed array of EMBLA_FULL_DECODE_SCRATCH_BYTES (4 MiB) in the library's
+ * device memory, one per device.
+ *   Limit: when embla_full_decode_workspace_size(shape) exceeds
+ *     EMBLA_FULL_DECODE_SCRATCH_BYTES the call returns EMBLA_ERR_WORKSPACE and
+ *     launches nothing.  On a 152-SM device that is above about 1850 (b, g)
+ *     units at G = 4 and about 850 at G = 8.
+ *   Set-up: the first call on a device, made with that device current, looks
+ *     up the array's device address and keeps it for later calls (a failed
+ *     look-up returns EMBLA_ERR_CUDA).  Make that first call before beginning
+ *     any stream capture.
+ *   Zeroing: the per-unit arrival counters in the scratch must start at zero;
+ *     every call zeroes them on `stream` before its kernel.  The rest of the
+ *     scratch is written before it is read and needs no initial value.
+ *   Concurrency: all calls on one device share the one array.  Two calls that
+ *     may run at the same time on the device (different streams or host
+ *     threads with no ordering between them) race on it and give wrong
+ *     results; calls ordered on one stream are safe.
+ */
+#define EMBLA_FULL_DECODE_SCRATCH_BYTES ((size_t)4 << 20)
+embla_status embla_full_decode_static_scratch(const embla_shape *shape, const void *q,
+                                              const void *k_cache, const void *v_cache,
+                                              float alpha, float c, float eps, float *out,
+                                              int32_t *n_surv, float *sel_scores,
+                                              uint32_t *sel_hist, void *stream);
+
+/*
  * Sparse-layer selection — "Three kinds of attention" (Sparse): the `topk`
  * keys with the highest sel_scores among j < n - recent (equal scores: the
  * smaller index first) together with the `recent` newest keys n-recent..n-1;

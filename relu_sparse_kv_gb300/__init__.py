@@ -27,6 +27,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libembla_attn.so")
 HIST_BINS = 2048
+FULL_DECODE_SCRATCH_BYTES = 4 << 20  # EMBLA_FULL_DECODE_SCRATCH_BYTES in the C header
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
           4: "CUDA error", 5: "device-side check failed"}
@@ -81,6 +82,8 @@ def library() -> ctypes.CDLL:
             "embla_full_decode_workspace_size": (sz, [P]),
             "embla_full_decode": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32, vp, vp, vp, vp, vp,
                                                  sz, vp]),
+            "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
+                                                                vp, vp, vp, vp, vp]),
             "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
             "embla_select_topk": (ctypes.c_int, [P, vp, vp, i32, i32, vp, i32, vp, vp, sz, vp]),
             "embla_sparse_decode_workspace_size": (sz, [P, i32]),
@@ -174,6 +177,27 @@ def embla_full_decode(shape: Shape, q, k_cache, v_cache, out, n_surv, sel_scores
     _call("embla_full_decode", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache),
           alpha, c, eps, _ptr(out), _ptr(n_surv), _ptr(sel_scores), _ptr(sel_hist), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_full_decode_static_scratch(shape: Shape, q, k_cache, v_cache, out, n_surv,
+                                     sel_scores=None, sel_hist=None, alpha: float = 1.0,
+                                     c: float = 1.0, eps: float = 1e-6, stream=None):
+    """embla_full_decode on the library's fixed per-device scratch: for callers that may not
+    allocate device memory while decoding.  Neither this wrapper nor the library allocates;
+    shapes needing more than FULL_DECODE_SCRATCH_BYTES of scratch raise EmblaError
+    (workspace too small).  Calls that can overlap on one device share the scratch and race."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    _check(n_surv, torch.int32, (B, Hkv), "n_surv")
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores", allow_none=True)
+    _check(sel_hist, torch.int32, (B, Hkv, HIST_BINS), "sel_hist", allow_none=True)
+    _call("embla_full_decode_static_scratch", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache),
+          _ptr(v_cache), alpha, c, eps, _ptr(out), _ptr(n_surv), _ptr(sel_scores),
+          _ptr(sel_hist), _stream(stream))
 
 
 def embla_select_topk(shape: Shape, sel_scores, sel_hist, idx, count, topk: int = 1024,

@@ -10,6 +10,10 @@
 
 using namespace embla;
 
+// Scratch of embla_full_decode_static_scratch: one fixed array per device, so that
+// call needs no workspace from its caller and allocates nothing itself.
+static __device__ __align__(256) unsigned char g_full_scratch[EMBLA_FULL_DECODE_SCRATCH_BYTES];
+
 namespace {
 
 // Device-side check word (flag bits, see embla_device_check).
@@ -42,6 +46,22 @@ uint32_t *flags_ptr() {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_check_flags) != cudaSuccess) return nullptr;
     cache[dev] = static_cast<uint32_t *>(p);
+  }
+  return cache[dev];
+}
+
+// Device address of g_full_scratch on the current device, looked up on the first
+// call for that device and kept; nullptr if the look-up fails.
+void *full_scratch_ptr() {
+  static std::mutex mu;
+  static void *cache[kMaxDevices] = {nullptr};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_full_scratch) != cudaSuccess) return nullptr;
+    cache[dev] = p;
   }
   return cache[dev];
 }
@@ -193,6 +213,26 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
                                         shape->ctx_len,
                                         shape->cache_stride, shape->n_q_heads, shape->n_kv_heads,
                                         alpha, eps, s));
+}
+
+embla_status embla_full_decode_static_scratch(const embla_shape *shape, const void *q,
+                                              const void *k_cache, const void *v_cache,
+                                              float alpha, float c, float eps, float *out,
+                                              int32_t *n_surv, float *sel_scores,
+                                              uint32_t *sel_hist, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return EMBLA_ERR_CUDA;
+  const size_t need = full_workspace_bytes(units, G, sms);
+  if (need > EMBLA_FULL_DECODE_SCRATCH_BYTES) return EMBLA_ERR_WORKSPACE;
+  void *scratch = full_scratch_ptr();
+  if (!scratch) return EMBLA_ERR_CUDA;
+  // The workspace call zeroes the arrival counters inside the scratch on `stream`.
+  return embla_full_decode(shape, q, k_cache, v_cache, alpha, c, eps, out, n_surv, sel_scores,
+                           sel_hist, scratch, need, stream);
 }
 
 size_t embla_select_topk_workspace_size(const embla_shape *shape, int32_t topk, int32_t recent) {

@@ -151,3 +151,10 @@ def test_full_decode_work_split_host_logic(tmp_path):
     assert r.returncode == 0, r.stderr[-2000:]
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout)
+
+
+def test_static_scratch_size_matches_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define EMBLA_FULL_DECODE_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m, "scratch size define not found"
+    assert int(m.group(1)) << int(m.group(2)) == E.FULL_DECODE_SCRATCH_BYTES
