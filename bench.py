@@ -142,6 +142,40 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workload
 
+def workload_name(cfg, batch=None, ctx=None) -> str:
+    if batch is None and ctx is None:
+        return cfg["name"]
+    return cfg["name"] + f" (overridden: batch {batch}, ctx {ctx})"
+
+
+def static_config(cfg_id: int, batch=None, ctx=None) -> dict:
+    """The workload's description, the same on both arms."""
+    import gen
+    cfg = gen.CONFIGS[cfg_id]
+    if cfg_id == 5:
+        fulls = [len(gen.EMBLA_SPARSE_OF[layer]) for layer in gen.EMBLA_FULL_LAYERS]
+        wins = list(gen.EMBLA_WINDOW_LAYERS)
+    else:
+        fulls, wins = [len(cfg["sparse"])], []
+    return {"workload": workload_name(cfg, batch, ctx),
+            "batch": cfg["B"] if batch is None else batch,
+            "ctx_len": cfg["n"] if ctx is None else ctx,
+            "q_heads": gen.HQ, "kv_heads": gen.HKV, "head_dim": gen.HEAD_DIM,
+            "full_layers": len(fulls), "sparse_layers": sum(fulls),
+            "window_layers": len(wins), "accumulate": "f32"}
+
+
+def omp_threads() -> int:
+    """Threads the oracle's OpenMP loops use on this host."""
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.split(",")[0].strip().isdigit():
+        return int(env.split(",")[0])
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def load_workload(cfg: int, seed: int = 0, batch=None, ctx=None):
     import gen
     fls = list(gen.config_full_layers(cfg, seed=seed, B=batch, n=ctx))
@@ -154,6 +188,24 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (x itself on one rank).  The timed regions of all ranks
+    are bracketed by barriers, so the slowest rank's time is the job's time."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, batch: int, seconds_per_step: float) -> float:
+    """Weak scaling: every rank decodes its own batch of `batch` sequences per step, so the
+    job's tokens/s is world * batch over the slowest rank's step time."""
+    return world * batch / seconds_per_step
 
 
 def run_reference(args):
@@ -193,13 +245,13 @@ def run_reference(args):
         step()
     dt = time.perf_counter() - t0
     value = sample_b * args.steps / dt
-    cores = os.cpu_count()
+    cores = omp_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg["name"], "batch": cfg["B"], "ctx_len": cfg["n"]},
+        "config": static_config(args.config),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{sample_b} of {cfg['B']} sequences, every layer of the step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -233,7 +285,7 @@ def cpu_baseline(cfg_id: int, budget_s: float = 12.0):
     dt = time.perf_counter() - t0
     sample = (f"{reps} pass(es) over {B} sequence(s): full layer + selection + "
               f"{len(qss)} sparse layer(s)" + (" (one of the five full-layer blocks)" if cfg_id == 5 else ""))
-    return {"value": B * reps / dt, "unit": "tokens/s", "cores": os.cpu_count(),
+    return {"value": B * reps / dt, "unit": "tokens/s", "cores": omp_threads(),
             "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
 
 
@@ -353,11 +405,14 @@ def main():
     keys_total = sum(L["shape"].units * L["fl"].n for L in layers)
     skipped_v = 1.0 - sum(n_surv_tot) / max(1, keys_total)
     batch = layers[0]["shape"].batch
+    # kernels of this library per step: one full-decode kernel per full layer (its two
+    # memsets are not kernels), one selection kernel and one kernel per sparse layer, one
+    # window kernel per window layer
     launches_per_step = 0
     for L in layers:
-        launches_per_step += 2
+        launches_per_step += 1
         if L["qs"]:
-            launches_per_step += (2 if L["fl"].n > TOPK + RECENT else 1) + 2 * len(L["qs"])
+            launches_per_step += 1 + len(L["qs"])
     launches_per_step += len(wins)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -396,12 +451,9 @@ def main():
     full_ms = [statistics.mean(ev[i * len(layers) + li][0].elapsed_time(ev[i * len(layers) + li][1])
                                for i in range(args.steps)) for li in range(len(layers))]
     assert E.embla_device_check() == 0
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
-    value = world * batch / (ms_per_step * 1e-3)
+    value = job_throughput(world, batch, ms_per_step * 1e-3)
 
     # end to end through the public Python API, host buffers, copies inside the timed region
     e2e = None
@@ -452,21 +504,18 @@ def main():
         for _ in range(args.e2e_steps):
             e2e_step()
         dt = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([dt], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * batch * args.e2e_steps / dt, "unit": "tokens/s",
+        dt = max_over_ranks(dt, world, dev)
+        e2e = {"value": job_throughput(world, batch, dt / args.e2e_steps), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps,
                "inputs": "per-step queries and the appended token's K/V rows from pinned host "
                          "memory; the KV caches stay resident in HBM"}
 
     peak, peak_src = _peaks()
-    wl_key = f"cfg{args.config}"
+    wl_key = workload_name(cfg, args.batch, args.ctx).replace(" ", "_")
     achieved = [fb / (fm * 1e-3) / 1e9 for fb, fm in zip(full_bytes, full_ms)]
     ach = statistics.mean(achieved)
-    roofline = {"bound": "hbm", "kernel": "embla_full_decode (histogram reset + score/skip kernel + combine)",
+    roofline = {"bound": "hbm", "kernel": "full_decode_kernel (one embla_full_decode call: 2 memsets + 1 kernel)",
                 "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                 "traffic": _traffic_from_profile(wl_key, _kernel_digest()),
@@ -480,12 +529,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": cfg["name"] + ("" if args.batch is None and args.ctx is None else
-                                              f" (overridden: batch {args.batch}, ctx {args.ctx})"),
-                   "batch": batch, "ctx_len": layers[0]["fl"].n,
-                   "q_heads": 16, "kv_heads": 4, "head_dim": 128,
-                   "full_layers": len(layers), "sparse_layers": sum(len(L["qs"]) for L in layers),
-                   "window_layers": len(wins), "accumulate": "f32",
+        "config": {**static_config(args.config, args.batch, args.ctx),
                    "l2": "not flushed: inputs larger than L2 (each full layer's K cache is "
                          f"{keys_total * ROW_BYTES // len(layers) / 1e6:.0f} MB)",
                    "needed_bytes_per_step": needed,
