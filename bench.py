@@ -405,12 +405,12 @@ def main():
     keys_total = sum(L["shape"].units * L["fl"].n for L in layers)
     skipped_v = 1.0 - sum(n_surv_tot) / max(1, keys_total)
     batch = layers[0]["shape"].batch
-    # kernels of this library per step: one full-decode kernel per full layer (its two
-    # memsets are not kernels), one selection kernel and one kernel per sparse layer, one
-    # window kernel per window layer
+    # kernels of this library per step: per full layer a zeroing kernel and the decode
+    # kernel, one selection kernel and one kernel per sparse layer, one window kernel per
+    # window layer
     launches_per_step = 0
     for L in layers:
-        launches_per_step += 1
+        launches_per_step += 2
         if L["qs"]:
             launches_per_step += 1 + len(L["qs"])
     launches_per_step += len(wins)
@@ -515,7 +515,7 @@ def main():
     wl_key = workload_name(cfg, args.batch, args.ctx).replace(" ", "_")
     achieved = [fb / (fm * 1e-3) / 1e9 for fb, fm in zip(full_bytes, full_ms)]
     ach = statistics.mean(achieved)
-    roofline = {"bound": "hbm", "kernel": "full_decode_kernel (one embla_full_decode call: 2 memsets + 1 kernel)",
+    roofline = {"bound": "hbm", "kernel": "full_decode_kernel (one embla_full_decode call: zeroing kernel + decode kernel)",
                 "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                 "traffic": _traffic_from_profile(wl_key, _kernel_digest()),

@@ -118,7 +118,7 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
  *     look-up returns EMBLA_ERR_CUDA).  Make that first call before beginning
  *     any stream capture.
  *   Zeroing: the per-unit arrival counters in the scratch must start at zero;
- *     every call zeroes them on `stream` before its kernel.  The rest of the
+ *     every call zeroes them on `stream` before its decode kernel uses them.  The rest of the
  *     scratch is written before it is read and needs no initial value.
  *   Concurrency: all calls on one device share the one array.  Two calls that
  *     may run at the same time on the device (different streams or host

@@ -188,19 +188,17 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   const FullSplit sp = full_split(units, shape->ctx_len, sms);
-  if (sel_scores) {
-    st = cuda_status(cudaMemsetAsync(sel_hist, 0, static_cast<size_t>(units) * kHistBins * 4, s));
-    if (st != EMBLA_OK) return st;
-  }
   if (sp.tiles == 0) {
-    // no keys: every output is 0 and nothing survives
-    st = cuda_status(cudaMemsetAsync(out, 0, static_cast<size_t>(units) * G * kHeadDim * 4, s));
+    // no keys: every output is 0, nothing survives, the histogram is empty
+    if (sel_scores)
+      st = cuda_status(cudaMemsetAsync(sel_hist, 0, static_cast<size_t>(units) * kHistBins * 4, s));
+    if (st == EMBLA_OK)
+      st = cuda_status(cudaMemsetAsync(out, 0, static_cast<size_t>(units) * G * kHeadDim * 4, s));
     if (st == EMBLA_OK) st = cuda_status(cudaMemsetAsync(n_surv, 0, static_cast<size_t>(units) * 4, s));
     return st;
   }
+  // the launch zeroes the histogram and the arrival counters itself
   int32_t *arrivals = full_arrivals(workspace, units, G, sms);
-  st = cuda_status(cudaMemsetAsync(arrivals, 0, static_cast<size_t>(units) * 4 * sizeof(int32_t), s));
-  if (st != EMBLA_OK) return st;
   CUtensorMap tm_k, tm_q, tm_v;
   if (!encode_rows(&tm_k, k_cache, static_cast<uint64_t>(units * shape->cache_stride), kTileKeys,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
@@ -230,7 +228,8 @@ embla_status embla_full_decode_static_scratch(const embla_shape *shape, const vo
   if (need > EMBLA_FULL_DECODE_SCRATCH_BYTES) return EMBLA_ERR_WORKSPACE;
   void *scratch = full_scratch_ptr();
   if (!scratch) return EMBLA_ERR_CUDA;
-  // The workspace call zeroes the arrival counters inside the scratch on `stream`.
+  // The workspace call zeroes the arrival counters inside the scratch on `stream`
+  // before its decode kernel uses them.
   return embla_full_decode(shape, q, k_cache, v_cache, alpha, c, eps, out, n_surv, sel_scores,
                            sel_hist, scratch, need, stream);
 }

@@ -543,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every tile of this unit has been scored (their lists were waited for in order):
         // move the segment's histogram to global memory and hand the buffer back
         uint32_t *h = s_hist + (seg & 1) * kHistBins;
+        pdl_wait_primary();  // the global histogram has been zeroed
         for (int bin = lane; bin < kHistBins; bin += 32) {
           const uint32_t cnt = h[bin];
           if (cnt) {
@@ -675,36 +676,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int parts = static_cast<int>(c1 - c0 + 1);
         __threadfence();  // each lane's part of the record is visible before the count
         __syncwarp();
+        pdl_wait_primary();  // the arrival counters have been zeroed
         int last = 0;
         if (lane == 0) last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4 + aw], 1) == parts - 1;
         if (__shfl_sync(0xffffffffu, last, 0)) {
           __threadfence();
+          // records of CTAs c0..c1 (other SMs wrote them: read through L2), loaded eight
+          // at a time so the loads overlap, summed in CTA order
+          const float *rr = p.rec + (c0 + u) * p.rec_stride;
           float *o = p.out + static_cast<int64_t>(u) * G * kHeadDim;
 #pragma unroll
           for (int hh = 0; hh < HPW; ++hh) {
             const int h = aw + 4 * hh;
             float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             float dsum = 0.0f;
-            for (int64_t cc = c0; cc <= c1; ++cc) {
-              const float *rr = p.rec + (cc + u) * p.rec_stride;  // written by other SMs: read L2
-              const float4 x = __ldcg(reinterpret_cast<const float4 *>(rr + h * kHeadDim + d0));
-              num.x += x.x;
-              num.y += x.y;
-              num.z += x.z;
-              num.w += x.w;
-              dsum += __ldcg(rr + G * kHeadDim + h);
+            for (int k0 = 0; k0 < parts; k0 += 8) {
+              float4 x[8];
+              float dd[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                x[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                dd[k] = 0.0f;
+                if (k0 + k < parts) {
+                  const float *r = rr + static_cast<int64_t>(k0 + k) * p.rec_stride;
+                  x[k] = __ldcg(reinterpret_cast<const float4 *>(r + h * kHeadDim + d0));
+                  dd[k] = __ldcg(r + G * kHeadDim + h);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                num.x += x[k].x;
+                num.y += x[k].y;
+                num.z += x[k].z;
+                num.w += x[k].w;
+                dsum += dd[k];
+              }
             }
             const float z = p.c + dsum;
             *reinterpret_cast<float4 *>(o + h * kHeadDim + d0) =
                 z != 0.0f ? make_float4(num.x / z, num.y / z, num.z / z, num.w / z)
                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           }
-          if (aw == 0 && lane == 0) {
+          if (aw == 0) {
             int32_t tot = 0;
-            for (int64_t cc = c0; cc <= c1; ++cc)
-              tot += __ldcg(reinterpret_cast<const int32_t *>(p.rec + (cc + u) * p.rec_stride) +
+            for (int k = lane; k < parts; k += 32)
+              tot += __ldcg(reinterpret_cast<const int32_t *>(rr + static_cast<int64_t>(k) * p.rec_stride) +
                             G * kHeadDim + G);
-            p.n_surv[u] = tot;
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o2);
+            if (lane == 0) p.n_surv[u] = tot;
           }
         }
       }
@@ -736,16 +756,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Zeroes what the decode accumulates into with atomics: the selection histogram (if any)
+// and the per-unit arrival counters.  It lets the decode kernel launch at once; the decode
+// waits for it only before its first histogram flush and its first arrival.
+__global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t hist_vecs,
+                                                        int32_t *arrivals, int64_t n_arrivals) {
+  pdl_launch_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = t; i < hist_vecs; i += stride) hist[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = t; i < n_arrivals; i += stride) arrivals[i] = 0;
+}
+
 template <int G>
 cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                                 const CUtensorMap &tm_v, const FullParams &p,
+                                 const CUtensorMap &tm_v, const FullParams &p, int64_t units,
                                  cudaStream_t stream) {
   const int smem = Smem<G>::alloc;
   cudaError_t e = cudaFuncSetAttribute(full_decode_kernel<G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  full_decode_kernel<G><<<p.P, kThreads, smem, stream>>>(tm_k, tm_q, tm_v, p);
-  return cudaGetLastError();
+  const int64_t hist_vecs = p.hist ? units * kHistBins / 4 : 0;
+  const int64_t work = hist_vecs > 4 * units ? hist_vecs : 4 * units;
+  const int64_t zblocks = (work + 255) / 256;
+  full_zero_kernel<<<static_cast<unsigned>(zblocks < 1024 ? zblocks : 1024), 256, 0, stream>>>(
+      reinterpret_cast<uint4 *>(p.hist), hist_vecs, p.arrivals, 4 * units);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.P));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, full_decode_kernel<G>, tm_k, tm_q, tm_v, p);
 }
 
 }  // namespace
@@ -806,8 +854,8 @@ cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap
   p.rec_stride = full_record_floats(G);
   p.alpha = alpha;
   p.eps = eps;
-  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, tm_v, p, stream);
-  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, tm_v, p, stream);
+  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, tm_v, p, sp.units, stream);
+  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, tm_v, p, sp.units, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -119,6 +119,16 @@ __device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start launching, and
+// wait until the kernel this one was launched behind has finished and its writes are
+// visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
