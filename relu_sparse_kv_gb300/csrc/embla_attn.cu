@@ -99,19 +99,6 @@ bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 tensor [rows, 128] read one whole 256-byte row per box (row gathers), no swizzle.
-bool encode_row_gather(CUtensorMap *map, const void *base, uint64_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), rows};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), 1u};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool finite(float x) { return x == x && x - x == 0.0f; }
@@ -199,14 +186,13 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
   }
   // the launch zeroes the histogram and the arrival counters itself
   int32_t *arrivals = full_arrivals(workspace, units, G, sms);
-  CUtensorMap tm_k, tm_q, tm_v;
+  CUtensorMap tm_k, tm_q;
   if (!encode_rows(&tm_k, k_cache, static_cast<uint64_t>(units * shape->cache_stride), kTileKeys,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_rows(&tm_q, q, static_cast<uint64_t>(shape->batch) * shape->n_q_heads,
-                   static_cast<uint32_t>(G), CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-      !encode_row_gather(&tm_v, v_cache, static_cast<uint64_t>(units * shape->cache_stride)))
+                   static_cast<uint32_t>(G), CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return EMBLA_ERR_CUDA;
-  return cuda_status(launch_full_decode(G, tm_k, tm_q, tm_v, v_cache, sel_scores, sel_hist,
+  return cuda_status(launch_full_decode(G, tm_k, tm_q, v_cache, sel_scores, sel_hist,
                                         workspace, arrivals, out, n_surv, c, flags, sp,
                                         shape->ctx_len,
                                         shape->cache_stride, shape->n_q_heads, shape->n_kv_heads,

@@ -9,20 +9,21 @@
 // (unit, tile) sequence, unit = (batch, KV head).  Warp roles:
 //   warp 0     TMA producer: 32 KB K tiles (two 64-column boxes, 128-byte swizzle) into
 //              a 4-stage ring; the unit's G query rows when the unit changes.
-//   warps 1, 19  tcgen05 issuers taking alternate tiles: D[128 keys x 16] = K . Q^T
+//   warps 1, 18  tcgen05 issuers taking alternate tiles: D[128 keys x 16] = K . Q^T
 //              (raw bf16 operands, fp32 in tensor memory), one independent MMA per
 //              16-dim k-step; four tiles in flight use all 512 columns.
-//   warps 15-18  key norms, one thread per key as soon as a tile lands:
+//   warps 14-17  key norms, one thread per key as soon as a tile lands:
 //              rk = 1/sqrt(mean(k^2) + eps), handed to the epilogue through a small
 //              shared-memory ring; the K stage is free once these and the MMAs are done.
 //   warps 2-9  two epilogue warpgroups taking alternate tiles, one thread per key:
-//              s_h = dot_h * alpha*rq_h * rk, sigma = max_h s_h; writes sigma and its
-//              histogram bin, and lists the keys with sigma > 0 with their ReLU^2
-//              weights (one list per warp, no cross-warp synchronisation).
-//   warp 10    V issuer: flattens each tile's lists in tile order and fetches only the
-//              listed V rows, four per TMA gather, into a 128-row ring; flushes the
-//              histogram of a unit when its last tile has been listed.
-//   warps 11-14  V accumulators (heads split over warps): num_h += w_h v, den_h += w_h
+//              s_h = dot_h * alpha*rq_h * rk, sigma = max_h s_h; lists the keys with
+//              sigma > 0 with their ReLU^2 weights in key order; a leader reserves that
+//              many rows of a 128-row V ring (in tile order), and every surviving key's
+//              thread copies its own 256-byte V row into the ring.
+//   warp 19    selection scores (when requested): writes each tile's sigma to global
+//              memory and counts it into a shared histogram, flushed when a unit's
+//              stretch ends.
+//   warps 10-13  V accumulators (heads split over warps): num_h += w_h v, den_h += w_h
 //              in tile order; at the end of each stretch of a unit they write a partial
 //              record, and the last warp to publish a unit's record sums its records and
 //              writes out = num / (c + den) and the survivor count.
@@ -60,26 +61,26 @@ constexpr int kAccCols = kKSteps * kMmaN;          // 128 columns per tile
 constexpr int kTmemCols = kAccBufs * kAccCols;     // 512
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN);
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
-constexpr int kWarpIssuer = kWarpEpi + 4 * kGroups;
-constexpr int kWarpAcc = kWarpIssuer + 1;
+constexpr int kWarpAcc = kWarpEpi + 4 * kGroups;
 constexpr int kWarpNorm = kWarpAcc + 4;
 constexpr int kWarpMma2 = kWarpNorm + 4;           // second MMA issuer (odd tiles)
+constexpr int kWarpHist = kWarpMma2 + 1;           // selection scores and histogram
 constexpr int kMmaWarps = 2;
-constexpr int kThreads = (kWarpMma2 + 1) * 32;     // 640
+constexpr int kThreads = (kWarpHist + 1) * 32;     // 640
 static_assert(kRing >= kTileKeys, "a whole tile of survivors must fit the V ring");
 static_assert((kRing & (kRing - 1)) == 0, "the V ring size is a power of two");
 
-// One tile's survivors.  The epilogue warps fill one 32-entry list per TMEM quarter; the
-// issuer then rewrites the entries in place as one flat list (quarter-major, so ascending
-// key order) before fetching their V rows.
+// One tile's survivors in ascending key order: entry e has its V row in ring row
+// (row0 + e) mod kRing.  Also the tile's selection scores, for the histogram warp.
 template <int G>
 struct WSlot {
-  int32_t cnt[4];             // survivors per quarter
-  int32_t row0;               // first V-ring row of this tile (written by the issuer)
-  int32_t m;                  // survivors in the tile (written by the issuer)
+  int32_t cnt[4];             // survivors per TMEM quarter (32 keys each)
+  int32_t row0;               // first V-ring row of this tile
+  int32_t m;                  // survivors in the tile
   int32_t pad[2];
-  int32_t key[4 * 32];        // key index within the unit: [quarter][32], then flat [m]
-  float w[4 * 32][G];         // ReLU^2 weights per head, same two layouts
+  int32_t key[kTileKeys];     // key index within the unit
+  float w[kTileKeys][G];      // ReLU^2 weights per head
+  float sig[kTileKeys];       // sigma of every key of the tile
 };
 
 template <int G>
@@ -89,11 +90,11 @@ struct Smem {
   static constexpr int ring_off = q_off + 2 * kQBufBytes;
   static constexpr int wslot_off = ring_off + kRing * kRowBytes;
   static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G>));
-  static constexpr int rk_off = hist_off + 2 * kHistBins * 4;     // one histogram per segment parity
+  static constexpr int rk_off = hist_off + kHistBins * 4;
   static constexpr int misc_off = rk_off + kNormSlots * kTileKeys * 4;
-  static constexpr int end_off = misc_off + 64;                 // int64 per W slot
-  static constexpr int bar_off = end_off + kWSlots * 8;
-  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 6 + 3 * kWSlots + 2 * kNormSlots;
+  static constexpr int end_off = misc_off + 64;                 // int64 per W slot, + 2 ring counters
+  static constexpr int bar_off = end_off + (kWSlots + 2) * 8;
+  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 4 + 4 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
 };
@@ -141,8 +142,7 @@ __device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     full_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_v, const FullParams p) {
+                       const __grid_constant__ CUtensorMap tm_q, const FullParams p) {
   using L = Smem<G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // offset arithmetic on the shared array keeps every access in the shared state space
@@ -159,7 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_k_issued = misc + 2;
   volatile int *s_q_issued = misc + 3;
   volatile int *s_v_issued = misc + 4;
-  int64_t *s_end = reinterpret_cast<int64_t *>(smem + L::end_off);
+  int *s_ring_oldest = misc + 5;         // oldest tile whose ring rows are not known free
+  volatile int *s_lead_ok = misc + 6;    // [group]: the leader's waits succeeded
+  int64_t *s_end = reinterpret_cast<int64_t *>(smem + L::end_off);  // ring row end per W slot
+  int64_t *s_ring_issued = s_end + kWSlots;  // ring rows reserved so far
+  int64_t *s_ring_freed = s_end + kWSlots + 1;  // ring rows known consumed
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
   uint64_t *full = bars;                 // K tile landed
   uint64_t *empty = full + kStages;      // K tile consumed (MMA and key norms)
@@ -167,11 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acce = accf + kAccBufs;      // accumulator read
   uint64_t *qfull = acce + kAccBufs;     // query rows landed
   uint64_t *qempty = qfull + 2;          // query rows no longer needed
-  uint64_t *wfull = qempty + 2;          // survivor list written
-  uint64_t *wempty = wfull + kWSlots;    // survivor list and its V rows consumed
-  uint64_t *vfull = wempty + kWSlots;    // V rows of a tile landed
-  uint64_t *hfree = vfull + kWSlots;     // histogram of a segment parity flushed and cleared
-  uint64_t *rkfull = hfree + 2;          // key norms of a tile written
+  uint64_t *adone = qempty + 2;          // ring rows of a tile reserved (orders the groups)
+  uint64_t *wempty = adone + kWSlots;    // survivor list and its V rows consumed
+  uint64_t *vfull = wempty + kWSlots;    // survivor list written and its V rows landed
+  uint64_t *sfull = vfull + kWSlots;     // selection scores of a tile written
+  uint64_t *rkfull = sfull + kWSlots;    // key norms of a tile written
   uint64_t *rkempty = rkfull + kNormSlots;  // key norms of a tile read
 
   const int warp = threadIdx.x >> 5;
@@ -198,12 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qempty[q], kMmaWarps + 4 * kGroups);
     }
     for (int w = 0; w < kWSlots; ++w) {
-      mbar_init(&wfull[w], 4);
-      mbar_init(&wempty[w], 4);
-      mbar_init(&vfull[w], 1);
+      mbar_init(&adone[w], 1);
+      mbar_init(&wempty[w], p.sel != nullptr ? 5 : 4);  // accumulators (+ histogram warp)
+      mbar_init(&vfull[w], 4);
+      mbar_init(&sfull[w], 4);
     }
-    mbar_init(&hfree[0], 1);
-    mbar_init(&hfree[1], 1);
     for (int r = 0; r < kNormSlots; ++r) {
       mbar_init(&rkfull[r], 4);
       mbar_init(&rkempty[r], 4);
@@ -212,13 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_k_issued = 0;
     *s_q_issued = 0;
     *s_v_issued = 0;
+    *s_ring_oldest = 0;
+    *s_ring_issued = 0;
+    *s_ring_freed = 0;
     fence_barrier_init();
   }
   // Rows G..15 of the query operand feed only MMA columns that are never read; zero
   // them anyway so no stale bits reach the tensor core.
   for (int i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = threadIdx.x; i < 2 * kHistBins; i += kThreads) s_hist[i] = 0u;
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0u;
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
     tmem_alloc(s_tmem, kTmemCols);
@@ -234,7 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_v);
       const uint64_t policy = policy_evict_first();
       int u = u0, tl = tl0;
       int seg = -1;
@@ -340,9 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&accf[(issued - 1) % kAccBufs], ((issued - 1) / kAccBufs) & 1);
     }
     __syncwarp();
-  } else if (warp < kWarpIssuer) {
+  } else if (warp < kWarpAcc) {
     // ------------------------------------------------------------------ epilogue groups
+    // Every decision to stop is taken by the whole group (named_bar_and), so no warp is
+    // left waiting at a group barrier that the others have abandoned.
     const int group = (warp - kWarpEpi) >> 2;
+    const uint32_t gbar = 1u + static_cast<uint32_t>(group);
+    const bool leader = ((warp - kWarpEpi) & 3) == 0 && lane == 0;
     const int quarter = warp & 3;     // the TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
     const uint32_t lanemask_lt = (1u << lane) - 1u;
@@ -352,16 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int u = u0, tl = tl0;
     int seg = -1;
     for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-      if (__any_sync(0xffffffffu, *s_abort)) break;
       if (i == 0 || tl == 0) {
         // every epilogue warp takes the new unit's query norms, whichever tiles it owns
         ++seg;
         const int qb = seg & 1;
-        const bool ok = __all_sync(
-            0xffffffffu, mbar_wait(&qfull[qb], (seg >> 1) & 1) &&
-                             (seg < 2 || p.sel == nullptr ||
-                              mbar_wait(&hfree[qb], ((seg >> 1) - 1) & 1)));
-        if (!ok) {
+        const bool ok = !*s_abort && mbar_wait(&qfull[qb], (seg >> 1) & 1);
+        if (!named_bar_and(gbar, 128, ok)) {
           set_abort(s_abort, p.flags);
           break;
         }
@@ -383,11 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = static_cast<int>(i % kAccBufs);
       const int slot = static_cast<int>(i % kWSlots);
       const int ns = static_cast<int>(i % kNormSlots);
-      bool ok = mbar_wait(&accf[b], (i / kAccBufs) & 1) &&
-                mbar_wait(&rkfull[ns], (i / kNormSlots) & 1) &&
-                (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
+      const bool ok = !*s_abort && mbar_wait(&accf[b], (i / kAccBufs) & 1) &&
+                      mbar_wait(&rkfull[ns], (i / kNormSlots) & 1) &&
+                      (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
+      if (!named_bar_and(gbar, 128, ok)) {
         set_abort(s_abort, p.flags);
         break;
       }
@@ -432,127 +436,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       WSlot<G> &ws = wslots[slot];
       if (p.sel != nullptr) {
-        // one shared-memory atomic per distinct bin in the warp
-        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-        if (valid) {
-          p.sel[static_cast<int64_t>(u) * p.ncap + j] = sigma;
-          const uint32_t bin = order_key(sigma) >> 21;
-          const uint32_t peers = __match_any_sync(vmask, bin);
-          if (lane == __ffs(peers) - 1)
-            atomicAdd(&s_hist[(seg & 1) * kHistBins + bin], static_cast<uint32_t>(__popc(peers)));
-        }
+        ws.sig[row] = sigma;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[slot]);
       }
       const bool surv = valid && sigma > 0.0f;
       const uint32_t bal = __ballot_sync(0xffffffffu, surv);
-      if (surv) {
-        const int r = quarter * 32 + __popc(bal & lanemask_lt);
-        ws.key[r] = static_cast<int32_t>(j);
-#pragma unroll
-        for (int h = 0; h < G; ++h) ws.w[r][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
-      }
       if (lane == 0) ws.cnt[quarter] = __popc(bal);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&wfull[slot]);
+      named_bar_sync(gbar, 128);  // the four counts are in
+      int off = 0, m = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = ws.cnt[q];
+        m += c;
+        off += q < quarter ? c : 0;
+      }
+      const int e = off + __popc(bal & lanemask_lt);  // this key's place in the tile's list
+      if (surv) {
+        ws.key[e] = j;
+#pragma unroll
+        for (int h = 0; h < G; ++h) ws.w[e][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
+      }
+      if (leader) {
+        // Reserve m ring rows in tile order: after the previous tile's reservation, and
+        // once the accumulators have freed enough of the ring.
+        bool lok = i == 0 || mbar_wait(&adone[(i - 1) % kWSlots], ((i - 1) / kWSlots) & 1);
+        const int64_t issued = *s_ring_issued;
+        int64_t freed = *s_ring_freed;
+        int oldest = *s_ring_oldest;
+        // this group waited for tile i - kWSlots to be consumed before reusing its slot, so
+        // it and every older tile are done (their slots' row ends are not yet overwritten)
+        while (oldest <= i - kWSlots) {
+          freed = s_end[oldest % kWSlots];
+          ++oldest;
+        }
+        while (lok && issued + m - freed > kRing) {
+          lok = mbar_wait(&wempty[oldest % kWSlots], (oldest / kWSlots) & 1);
+          freed = s_end[oldest % kWSlots];
+          ++oldest;
+        }
+        ws.row0 = static_cast<int32_t>(issued % kRing);
+        ws.m = m;
+        s_end[slot] = issued + m;
+        *s_ring_issued = issued + m;
+        *s_ring_freed = freed;
+        *s_ring_oldest = oldest;
+        s_lead_ok[group] = lok;
+        if (lok) {
+          *s_v_issued = i + 1;
+          mbar_arrive(&adone[slot]);  // the next tile may reserve
+        }
+      }
+      __syncwarp();
+      named_bar_sync(gbar, 128);  // the reservation is published
+      if (!s_lead_ok[group]) {
+        set_abort(s_abort, p.flags);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(__popc(bal) * kRowBytes));
+      __syncwarp();
+      if (surv)
+        bulk_load(sRing + ((ws.row0 + e) & (kRing - 1)) * kRowBytes,
+                  p.v + (static_cast<int64_t>(u) * p.ncap + j) * kRowBytes, kRowBytes, &vfull[slot]);
     }
     __syncwarp();
-  } else if (warp == kWarpIssuer) {
-    // ------------------------------------------------------------------ V issuer
-    // Reads each tile's survivor list in order, keeps the selection histogram, and
-    // bulk-copies the surviving keys' V rows into a ring of kRing rows.
-    int u = u0, tl = tl0;
-    int64_t rows_issued = 0, rows_freed = 0;
-    int oldest = 0;
-    int seg = -1;
-    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-      if (__any_sync(0xffffffffu, *s_abort)) break;
-      if (i == 0 || tl == 0) ++seg;
-      const int slot = static_cast<int>(i % kWSlots);
-      // the epilogue refilled this slot, so tile i - kWSlots and older are consumed
-      while (oldest <= i - kWSlots) {
-        rows_freed = s_end[oldest % kWSlots];
-        ++oldest;
-      }
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&wfull[slot], (i / kWSlots) & 1));
-      if (!ok) {
-        set_abort(s_abort, p.flags);
-        break;
-      }
-      WSlot<G> &ws = wslots[slot];
-      const int c0 = ws.cnt[0], c1 = ws.cnt[1], c2 = ws.cnt[2], c3 = ws.cnt[3];
-      const int m = c0 + c1 + c2 + c3;
-      const int m4 = (m + 3) & ~3;  // ring rows taken: whole groups of four
-      // flatten the four quarter lists in place (each lane moves at most four entries)
-      {
-        int32_t kk[4];
-        float ww[4][G];
+  } else if (warp == kWarpHist) {
+    // ------------------------------------------------------------------ selection scores
+    // Tile by tile in order: sigma of the keys j < n to global memory, and counted into
+    // the histogram of the order key's top 11 bits; at the end of each stretch of a unit
+    // the histogram is added to the unit's global one and cleared.
+    if (p.sel != nullptr) {
+      int u = u0, tl = tl0;
+      for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
+        const int slot = static_cast<int>(i % kWSlots);
+        const bool ok = __all_sync(0xffffffffu, !*s_abort && mbar_wait(&sfull[slot], (i / kWSlots) & 1));
+        if (!ok) {
+          set_abort(s_abort, p.flags);
+          break;
+        }
+        const WSlot<G> &ws = wslots[slot];
+        float sg[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sg[r] = ws.sig[lane + 32 * r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[slot]);
+        float *dst = p.sel + static_cast<int64_t>(u) * p.ncap + tl * kTileKeys;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int e = lane + 32 * r;
-          if (e < m) {
-            const int q = (e >= c0) + (e >= c0 + c1) + (e >= c0 + c1 + c2);
-            const int src = 32 * q + e - (q == 0 ? 0 : q == 1 ? c0 : q == 2 ? c0 + c1 : c0 + c1 + c2);
-            kk[r] = ws.key[src];
-#pragma unroll
-            for (int h = 0; h < G; ++h) ww[r][h] = ws.w[src][h];
+          const int row = lane + 32 * r;
+          if (tl * kTileKeys + row < p.n) {
+            dst[row] = sg[r];
+            atomicAdd(&s_hist[order_key(sg[r]) >> 21], 1u);
           }
         }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int e = lane + 32 * r;
-          if (e < m) {
-            ws.key[e] = kk[r];
-#pragma unroll
-            for (int h = 0; h < G; ++h) ws.w[e][h] = ww[r][h];
+        if (i + 1 == ntiles || tl + 1 == TU) {
+          __syncwarp();
+          pdl_wait_primary();  // the global histogram has been zeroed
+          for (int bin = lane; bin < kHistBins; bin += 32) {
+            const uint32_t cnt = s_hist[bin];
+            if (cnt) {
+              atomicAdd(&p.hist[static_cast<int64_t>(u) * kHistBins + bin], cnt);
+              s_hist[bin] = 0u;
+            }
           }
+          __syncwarp();
         }
-        __syncwarp();
-      }
-      while (ok && rows_issued + m4 - rows_freed > kRing) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&wempty[oldest % kWSlots], (oldest / kWSlots) & 1));
-        rows_freed = s_end[oldest % kWSlots];
-        ++oldest;
-      }
-      if (!ok) {
-        set_abort(s_abort, p.flags);
-        break;
-      }
-      if (lane == 0) {
-        ws.row0 = static_cast<int32_t>(rows_issued % kRing);
-        ws.m = m;
-        s_end[slot] = rows_issued + m4;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(m4 * kRowBytes));
-      __syncwarp();
-      if (4 * lane < m) {
-        // one gather of four V rows per lane; a short last group repeats its last row
-        const int e = 4 * lane;
-        const int32_t base = static_cast<int32_t>(static_cast<int64_t>(u) * p.ncap);
-        const int32_t y0 = base + ws.key[e];
-        const int32_t y1 = base + ws.key[min(e + 1, m - 1)];
-        const int32_t y2 = base + ws.key[min(e + 2, m - 1)];
-        const int32_t y3 = base + ws.key[min(e + 3, m - 1)];
-        const int dst = static_cast<int>((rows_issued + e) % kRing);
-        tma_gather4(sRing + dst * kRowBytes, &tm_v, &vfull[slot], 0, y0, y1, y2, y3);
-      }
-      rows_issued += m4;
-      if (lane == 0) *s_v_issued = i + 1;
-      if (p.sel != nullptr && (i + 1 == ntiles || tl + 1 == TU)) {
-        // every tile of this unit has been scored (their lists were waited for in order):
-        // move the segment's histogram to global memory and hand the buffer back
-        uint32_t *h = s_hist + (seg & 1) * kHistBins;
-        pdl_wait_primary();  // the global histogram has been zeroed
-        for (int bin = lane; bin < kHistBins; bin += 32) {
-          const uint32_t cnt = h[bin];
-          if (cnt) {
-            atomicAdd(&p.hist[static_cast<int64_t>(u) * kHistBins + bin], cnt);
-            h[bin] = 0u;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&hfree[seg & 1]);
       }
     }
     __syncwarp();
@@ -631,9 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float wv[4][HPW];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          // rows past m belong to the tile's last gather group: read them, weigh them 0
+          // rows past m are not this tile's: skip them (weight 0, value 0)
           const int e = e0 + r;
-          raw[r] = *reinterpret_cast<const uint2 *>(sRing + ((row0 + e) & (kRing - 1)) * kRowBytes + lane * 8);
+          raw[r] = e < m ? *reinterpret_cast<const uint2 *>(sRing + ((row0 + e) & (kRing - 1)) * kRowBytes + lane * 8)
+                         : make_uint2(0u, 0u);
 #pragma unroll
           for (int hh = 0; hh < HPW; ++hh) wv[r][hh] = e < m ? ws.w[e][aw + 4 * hh] : 0.0f;
         }
@@ -770,8 +760,7 @@ __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t his
 
 template <int G>
 cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                                 const CUtensorMap &tm_v, const FullParams &p, int64_t units,
-                                 cudaStream_t stream) {
+                                 const FullParams &p, int64_t units, cudaStream_t stream) {
   const int smem = Smem<G>::alloc;
   cudaError_t e = cudaFuncSetAttribute(full_decode_kernel<G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -793,7 +782,7 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, full_decode_kernel<G>, tm_k, tm_q, tm_v, p);
+  return cudaLaunchKernelEx(&cfg, full_decode_kernel<G>, tm_k, tm_q, p);
 }
 
 }  // namespace
@@ -827,7 +816,7 @@ int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count) {
 }
 
 cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores,
+                               const void *v_cache, float *sel_scores,
                                uint32_t *sel_hist, void *workspace, int32_t *arrivals,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
@@ -854,8 +843,8 @@ cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap
   p.rec_stride = full_record_floats(G);
   p.alpha = alpha;
   p.eps = eps;
-  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, tm_v, p, sp.units, stream);
-  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, tm_v, p, sp.units, stream);
+  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, p, sp.units, stream);
+  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, p, sp.units, stream);
   return cudaErrorInvalidValue;
 }
 

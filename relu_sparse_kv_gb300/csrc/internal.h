@@ -38,7 +38,7 @@ size_t full_workspace_bytes(int64_t units, int G, int sm_count);
 int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count);
 
 cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_v, const void *v_cache, float *sel_scores,
+                               const void *v_cache, float *sel_scores,
                                uint32_t *sel_hist, void *workspace, int32_t *arrivals,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
