@@ -7,11 +7,14 @@
 //   Sliding window — the newest 128 keys, ordinary softmax, rotary position
 //             embedding (the query is rotated here; keys were rotated when written).
 //
-// Each warp folds chunks of 8 rows; a row is read by 16 lanes (8 dims each, one
+// Each warp first copies all of its rows (K and V, 256 bytes each) into its own part of
+// shared memory with one bulk copy per row, so every row of the warp is in flight at
+// once, then folds them in chunks of 8 rows; a row is read by 16 lanes (8 dims each, one
 // 16-byte load of K and of V), so a warp's two lane groups take 4 rows each.  The
 // group's 4 x G partial dot products are summed by a reduce-scatter over its 16 lanes
 // and gathered back, then every lane updates its group's running max m, sum l and its
-// 8-dim slice of the unnormalised output, rescaling once per chunk.  Warps merge in shared memory by rescaling with exp(m_w - M).
+// 8-dim slice of the unnormalised output, rescaling once per chunk.  Warps merge in
+// shared memory (reusing the rows' space) by rescaling with exp(m_w - M).
 // A sparse layer spreads each (batch, KV-head) unit over a cluster of 8 CTAs that merge
 // through distributed shared memory; a window layer uses one CTA per unit.
 #include <cooperative_groups.h>
@@ -29,7 +32,8 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCluster = 8;        // CTAs per sparse unit
-constexpr int kIdxChunk = 512;     // selected rows a sparse CTA stages at a time
+constexpr int kWarpRows = 20;      // rows a warp stages per pass
+constexpr int kStageBytes = kWarps * kWarpRows * 2 * kHeadDim * 2;  // 80 KB: K and V rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRowBytes = kHeadDim * 2;
 
@@ -58,22 +62,52 @@ struct Chunk {
   uint32_t present;  // bit r: row r of this lane's group exists
 };
 
-// rows[r]: row index of K/V for this lane's group's row r, or -1
-__device__ __forceinline__ void load_chunk(Chunk &c, const uint8_t *K, const uint8_t *V,
-                                           const int32_t (&rows)[4], int sl) {
-  c.present = 0;
+// Chunk rows from a warp's staged rows: present[r] says whether the group's row r holds
+// a row; sK/sV point at the group's row 0 (rows 256 bytes apart).
+__device__ __forceinline__ void load_chunk(Chunk &c, const uint8_t *sK, const uint8_t *sV,
+                                           uint32_t present, int sl) {
+  c.present = present;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    if (rows[r] >= 0) {
-      const int64_t off = static_cast<int64_t>(rows[r]) * kRowBytes;
-      c.k[r] = __ldg(reinterpret_cast<const uint4 *>(K + off) + sl);
-      c.v[r] = __ldg(reinterpret_cast<const uint4 *>(V + off) + sl);
-      c.present |= 1u << r;
+    if ((present >> r) & 1u) {
+      c.k[r] = *reinterpret_cast<const uint4 *>(sK + r * kRowBytes + sl * 16);
+      c.v[r] = *reinterpret_cast<const uint4 *>(sV + r * kRowBytes + sl * 16);
     } else {
       c.k[r] = make_uint4(0u, 0u, 0u, 0u);
       c.v[r] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+}
+
+// The rows of one warp in shared memory: K rows then V rows, kWarpRows each.
+struct WarpStage {
+  uint8_t *k, *v;
+  __device__ WarpStage(uint8_t *stage, int warp)
+      : k(stage + warp * kWarpRows * 2 * kRowBytes), v(k + kWarpRows * kRowBytes) {}
+};
+
+// Copy up to kWarpRows rows (row indices from `row_of(i)` for i < nrows, negative =
+// absent) of K and V into the warp's stage: the two lane groups take alternate rows, each
+// lane one 16-byte piece of the row's K and of its V, all in flight together.  Returns
+// the mask of rows present (bit i).
+template <class RowOf>
+__device__ __forceinline__ uint32_t stage_rows(const WarpStage &ws, const uint8_t *K,
+                                               const uint8_t *V, int nrows, RowOf row_of,
+                                               int lane) {
+  const int64_t mine = lane < nrows ? row_of(lane) : -1;
+  const uint32_t present = __ballot_sync(0xffffffffu, mine >= 0);
+  const int grp = lane >> 4, sl = lane & 15;
+  for (int r2 = 0; r2 < (nrows + 1) / 2; ++r2) {
+    const int r = 2 * r2 + grp;
+    const int64_t row = __shfl_sync(0xffffffffu, mine, r < 32 ? r : 31);
+    if (r < nrows && row >= 0) {
+      cp_async16(ws.k + r * kRowBytes + sl * 16, K + row * kRowBytes + sl * 16);
+      cp_async16(ws.v + r * kRowBytes + sl * 16, V + row * kRowBytes + sl * 16);
+    }
+  }
+  cp_async_wait_all();
+  __syncwarp();
+  return present;
 }
 
 // acc += a . b over the 8 bf16 pairs of two uint4 (bf16 products are exact in fp32)
@@ -270,6 +304,29 @@ struct DotsF32 {
 
 
 // ----------------------------------------------------------------------------- sparse
+//
+// Tensor-core path.  A warp takes blocks of 16 selected rows.  It copies their K and V
+// rows into shared memory (16-byte pieces permuted within each row by row % 8, so that
+// the 8 rows an ldmatrix reads fall in different banks), then
+//   S  = Q . K^T  as m16n8k16 MMAs: M = query heads (G of 16 used), N = 8 rows, K = dims;
+//   P  = exp2(tau2 * S - m) with a running max m and sum l per head (the accumulator of
+//        S holds, per lane, head lane/4 and rows 2(lane%4), +1 of each 8-row tile, which
+//        is exactly the B operand layout the next product needs);
+//   O^T += V^T . P^T  as MMAs with M = dims (8 tiles of 16), N = heads, K = the 16 rows.
+// P is rounded to bf16 for the second product; l sums the unrounded fp32 values.
+
+constexpr int kSpWarps = 9;                 // 9 x 16 = 144 rows: a cluster of 8 covers 1152
+constexpr int kSpThreads = kSpWarps * 32;
+constexpr int kSpBlock = 16;                // rows per warp step
+constexpr int kSpStage = 2 * kSpBlock * kRowBytes;  // K and V rows of one step: 8 KB
+
+template <int G>
+struct SpMerge {
+  float m[kSpWarps][G], l[kSpWarps][G];
+  float acc[kSpWarps][G][kHeadDim];
+  float cm[G], cl[G];
+  float ca[G][kHeadDim];
+};
 
 struct SparseParams {
   const uint16_t *q;
@@ -282,73 +339,194 @@ struct SparseParams {
   float tau;
 };
 
+// byte offset of 16-byte piece c of staged row r
+__device__ __forceinline__ uint32_t sp_piece(int r, int c) {
+  return static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
+}
+
 template <int G>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2)
     sparse_decode_kernel(const SparseParams p) {
-  __shared__ Merge<G> mg;
+  extern __shared__ __align__(128) uint8_t smem[];  // staged rows, then the merge state
+  SpMerge<G> &mg = *reinterpret_cast<SpMerge<G> *>(smem);
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int64_t u = blockIdx.x / kCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
   int cnt = p.count[u];
   cnt = cnt < 0 ? 0 : (cnt > p.idx_stride ? p.idx_stride : cnt);
-  const int grp = lane >> 4, sl = lane & 15;
-  DotsBf16<G> dots;
-  dots.load(p.q + u * G * kHeadDim, sl);
-  Soft<G> st;
-  st.init();
   const int32_t *idx = p.idx + u * p.idx_stride;
   const uint8_t *Ku = p.K + u * p.ncap * kRowBytes;
   const uint8_t *Vu = p.V + u * p.ncap * kRowBytes;
-  __shared__ int32_t s_rows[kIdxChunk];
   const float tau2 = p.tau * kLog2e;
+  uint8_t *sK = smem + warp * kSpStage;
+  uint8_t *sV = sK + kSpBlock * kRowBytes;
+  const uint32_t sK_u = smem_u32(sK), sV_u = smem_u32(sV);
+
+  // query as the A operand of S = Q . K^T: row g (head g), dims 16ks + 2t, +1 and +8, +9
+  uint32_t qa0[8], qa2[8];
+  {
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (u * G + (g < G ? g : 0)) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa0[ks] = g < G ? qrow[8 * ks + t] : 0u;
+      qa2[ks] = g < G ? qrow[8 * ks + 4 + t] : 0u;
+    }
+  }
+  float m = -INFINITY, l = 0.0f;  // head g's running max (base 2) and sum
+  float o[8][4];                  // O^T tile i: dims 16i + g (+8), heads 2t, 2t + 1
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+
   const int r0 = rank * p.rows_per_cta;
   const int r1 = min(cnt, r0 + p.rows_per_cta);
-  for (int c0 = r0; c0 < r1; c0 += kIdxChunk) {
-    const int c1 = min(r1, c0 + kIdxChunk);
-    // one round trip for the chunk's indices; out-of-range entries are skipped and flagged
-    for (int r = c0 + threadIdx.x; r < c1; r += kThreads) {
-      const int32_t j = idx[r];
-      const bool bad = j < 0 || static_cast<int64_t>(j) >= p.n;
-      if (bad) atomicOr(p.flags, kFlagIndexRange);
-      s_rows[r - c0] = bad ? -1 : j;
+  for (int b0 = r0 + warp * kSpBlock; b0 < r1; b0 += kSpWarps * kSpBlock) {
+    // stage: lane r < 16 looks up row r (absent past the count, or for an index outside
+    // [0, n), which is flagged); then each copy instruction moves two whole rows, lanes
+    // 0-15 the 16 pieces of one and lanes 16-31 those of the next; absent rows are zeros
+    int64_t j = -1;
+    if (lane < kSpBlock && b0 + lane < r1) {
+      const int32_t jj = idx[b0 + lane];
+      if (jj < 0 || static_cast<int64_t>(jj) >= p.n)
+        atomicOr(p.flags, kFlagIndexRange);
+      else
+        j = jj;
     }
-    __syncthreads();
-    for (int cb = c0 + warp * kChunk; cb < c1; cb += kWarps * kChunk) {
-      int32_t rows[4];
+    const uint32_t present = __ballot_sync(0xffffffffu, j >= 0);  // bit r: row r
+    const int piece = lane & 15;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = cb + grp * 4 + r;
-        rows[r] = i < c1 ? s_rows[i - c0] : -1;
-      }
-      Chunk ch;
-      load_chunk(ch, Ku, Vu, rows, sl);
-      fold_chunk<G>(st, dots, tau2, ch, sl);
+    for (int k = 0; k < kSpBlock / 2; ++k) {
+      const int r = 2 * k + (lane >> 4);
+      const int64_t jr = __shfl_sync(0xffffffffu, j, r);
+      const uint32_t nbytes = jr >= 0 ? 16u : 0u;
+      const int64_t off = (jr >= 0 ? jr : 0) * kRowBytes + piece * 16;
+      cp_async16_zfill(sK + sp_piece(r, piece), Ku + off, nbytes);
+      cp_async16_zfill(sV + sp_piece(r, piece), Vu + off, nbytes);
     }
-    __syncthreads();
+    cp_async_wait_all();
+    __syncwarp();
+
+    // S = Q . K^T for rows 0-7 (s0) and 8-15 (s1)
+    float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    {
+      const int mat = lane >> 3, mr = lane & 7;
+      const int row = (mat >> 1) * 8 + mr;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t bk[4];
+        ldmatrix_x4(bk, sK_u + sp_piece(row, 2 * ks + (mat & 1)));
+        mma_16816_bf16(s0, qa0[ks], 0u, qa2[ks], 0u, bk[0], bk[1]);
+        mma_16816_bf16(s1, qa0[ks], 0u, qa2[ks], 0u, bk[2], bk[3]);
+      }
+    }
+    // online softmax for head g over rows 2t, 2t+1 (s0) and 8+2t, 9+2t (s1)
+    float z[4];
+    z[0] = (present >> (2 * t)) & 1u ? tau2 * s0[0] : -INFINITY;
+    z[1] = (present >> (2 * t + 1)) & 1u ? tau2 * s0[1] : -INFINITY;
+    z[2] = (present >> (8 + 2 * t)) & 1u ? tau2 * s1[0] : -INFINITY;
+    z[3] = (present >> (9 + 2 * t)) & 1u ? tau2 * s1[1] : -INFINITY;
+    float mx = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    float sc = 1.0f, pz[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (mn != -INFINITY) {
+      sc = exp2f(m - mn);  // 0 while nothing had been seen
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pz[k] = exp2f(z[k] - mn);
+    }
+    float ps = (pz[0] + pz[1]) + (pz[2] + pz[3]);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+    m = mn;
+    l = fmaf(l, sc, ps);
+    // rescale O^T: this lane holds heads 2t and 2t + 1, whose factors live in lanes 8t, 8t + 4
+    const float sc_a = __shfl_sync(0xffffffffu, sc, 8 * t);
+    const float sc_b = __shfl_sync(0xffffffffu, sc, 8 * t + 4);
+    const uint32_t pb0 = pack_bf16x2(pz[0], pz[1]), pb1 = pack_bf16x2(pz[2], pz[3]);
+    {
+      const int mat = lane >> 3, mr = lane & 7;
+      const int row = (mat >> 1) * 8 + mr;  // matrices: rows 0-7 / 8-15 x dims +0 / +8
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t av[4];
+        ldmatrix_x4_trans(av, sV_u + sp_piece(row, 2 * i + (mat & 1)));
+        o[i][0] *= sc_a;
+        o[i][1] *= sc_b;
+        o[i][2] *= sc_a;
+        o[i][3] *= sc_b;
+        // A = V^T tile: a0 rows(dims) g / k rows 0-7, a1 dims g+8 / rows 0-7,
+        // a2 dims g / rows 8-15, a3 dims g+8 / rows 8-15
+        mma_16816_bf16(o[i], av[0], av[1], av[2], av[3], pb0, pb1);
+      }
+    }
+    __syncwarp();  // the stage is read before the next block's copies land in it
   }
-  merge_warps<G>(mg, st, warp, lane);
+
+  // this warp's state into shared memory (reusing the stages: wait for every warp)
+  __syncthreads();
+  if (t == 0 && g < G) {
+    mg.m[warp][g] = m;
+    mg.l[warp][g] = l;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (2 * t < G) {
+      mg.acc[warp][2 * t][16 * i + g] = o[i][0];
+      mg.acc[warp][2 * t][16 * i + g + 8] = o[i][2];
+    }
+    if (2 * t + 1 < G) {
+      mg.acc[warp][2 * t + 1][16 * i + g] = o[i][1];
+      mg.acc[warp][2 * t + 1][16 * i + g + 8] = o[i][3];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kSpThreads) {
+    const int h = i / kHeadDim, d = i % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kSpWarps; ++w) M = fmaxf(M, mg.m[w][h]);
+    float L = 0.0f, A = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kSpWarps; ++w) {
+        const float f = exp2f(mg.m[w][h] - M);
+        L = fmaf(mg.l[w][h], f, L);
+        A = fmaf(mg.acc[w][h][d], f, A);
+      }
+    }
+    mg.ca[h][d] = A;
+    if (d == 0) {
+      mg.cm[h] = M;
+      mg.cl[h] = L;
+    }
+  }
+  // the cluster's CTAs each finish an eighth of the outputs from all eight states
   cluster.sync();
-  if (rank == 0) {
-    for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) {
-      const int h = i / kHeadDim, d = i % kHeadDim;
-      float M = -INFINITY;
+  constexpr int kPer = G * kHeadDim / kCluster;
+  for (int i = rank * kPer + threadIdx.x; i < (rank + 1) * kPer; i += kSpThreads) {
+    const int h = i / kHeadDim, d = i % kHeadDim;
+    float cmv[kCluster];
+    float M = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kCluster; ++c) M = fmaxf(M, cluster.map_shared_rank(&mg, c)->cm[h]);
-      float L = 0.0f, A = 0.0f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int c = 0; c < kCluster; ++c) {
-          const Merge<G> *o = cluster.map_shared_rank(&mg, c);
-          const float sc = exp2f(o->cm[h] - M);
-          L = fmaf(o->cl[h], sc, L);
-          A = fmaf(o->ca[h][d], sc, A);
-        }
-      }
-      p.out[u * G * kHeadDim + i] = L > 0.0f ? A / L : 0.0f;
+    for (int c = 0; c < kCluster; ++c) {
+      cmv[c] = cluster.map_shared_rank(&mg, c)->cm[h];
+      M = fmaxf(M, cmv[c]);
     }
+    float L = 0.0f, A = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int c = 0; c < kCluster; ++c) {
+        const SpMerge<G> *o2 = cluster.map_shared_rank(&mg, c);
+        const float f = exp2f(cmv[c] - M);
+        L = fmaf(o2->cl[h], f, L);
+        A = fmaf(o2->ca[h][d], f, A);
+      }
+    }
+    p.out[u * G * kHeadDim + i] = L > 0.0f ? A / L : 0.0f;
   }
-  cluster.sync();  // the other CTAs' shared memory stays alive until the leader is done
+  cluster.sync();  // the other CTAs' shared memory stays alive until every CTA is done
 }
 
 // ----------------------------------------------------------------------------- window
@@ -363,8 +541,9 @@ struct WindowParams {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 2) window_decode_kernel(const WindowParams p) {
-  __shared__ Merge<G> mg;
+__global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1) window_decode_kernel(const WindowParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];  // staged rows, then the merge state
+  Merge<G> &mg = *reinterpret_cast<Merge<G> *>(smem);
   const int64_t u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 4, sl = lane & 15;
@@ -396,22 +575,51 @@ __global__ void __launch_bounds__(kThreads, 2) window_decode_kernel(const Window
   const uint8_t *Ku = p.K + u * p.window * kRowBytes;
   const uint8_t *Vu = p.V + u * p.window * kRowBytes;
   const float tau2 = p.tau * kLog2e;
-  for (int cb = warp * kChunk; cb < nv; cb += kWarps * kChunk) {
-    int32_t rows[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = cb + grp * 4 + r;
-      rows[r] = i < nv ? static_cast<int32_t>((first + i) % p.window) : -1;
+  // the valid positions, split into contiguous runs per warp
+  const int per_warp = (nv + kWarps - 1) / kWarps;
+  const int w0 = warp * per_warp;
+  const int w1 = min(nv, w0 + per_warp);
+  const WarpStage ws(smem, warp);
+  for (int b0 = w0; b0 < w1; b0 += kWarpRows) {
+    const int nrows = min(kWarpRows, w1 - b0);
+    const uint32_t present = stage_rows(
+        ws, Ku, Vu, nrows,
+        [&](int i) -> int64_t { return (first + b0 + i) % p.window; }, lane);
+    for (int c = 0; c < nrows; c += kChunk) {
+      const int f = c + grp * 4;
+      const uint32_t pm = f < 32 ? (present >> f) & 0xFu : 0u;
+      Chunk ch;
+      load_chunk(ch, ws.k + f * kRowBytes, ws.v + f * kRowBytes, pm, sl);
+      fold_chunk<G>(st, dots, tau2, ch, sl);
     }
-    Chunk ch;
-    load_chunk(ch, Ku, Vu, rows, sl);
-    fold_chunk<G>(st, dots, tau2, ch, sl);
+    __syncwarp();
   }
+  __syncthreads();  // every warp is done with its rows before the merge state reuses them
   merge_warps<G>(mg, st, warp, lane);
   for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) {
     const int h = i / kHeadDim;
     p.out[u * G * kHeadDim + i] = mg.cl[h] > 0.0f ? mg.ca[h][i % kHeadDim] / mg.cl[h] : 0.0f;
   }
+}
+
+// Both kernels stage rows in dynamic shared memory that the merge state reuses.
+template <class Params>
+cudaError_t launch_staged(void (*kernel)(Params), dim3 grid, const Params &p, cudaStream_t stream) {
+  static_assert(sizeof(Merge<8>) <= kStageBytes, "the merge state fits the staging space");
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, kStageBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const SparseParams &p,
+                            cudaStream_t stream) {
+  constexpr int bytes = kSpWarps * kSpStage;
+  static_assert(sizeof(SpMerge<8>) <= bytes, "the merge state fits the staging space");
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kSpThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -442,16 +650,12 @@ cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, cons
   p.n = n;
   p.ncap = ncap;
   p.idx_stride = idx_stride;
-  p.rows_per_cta = (idx_stride + kCluster - 1) / kCluster;
+  p.rows_per_cta = ((idx_stride + kCluster - 1) / kCluster + kSpBlock - 1) / kSpBlock * kSpBlock;
   p.tau = tau;
   const dim3 grid(static_cast<unsigned>(units * kCluster));
-  if (G == 4)
-    sparse_decode_kernel<4><<<grid, kThreads, 0, stream>>>(p);
-  else if (G == 8)
-    sparse_decode_kernel<8><<<grid, kThreads, 0, stream>>>(p);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (G == 4) return launch_sparse_t(sparse_decode_kernel<4>, grid, p, stream);
+  if (G == 8) return launch_sparse_t(sparse_decode_kernel<8>, grid, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const void *v_win,
@@ -467,13 +671,10 @@ cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const 
   p.window = window;
   p.rope_base = rope_base;
   p.tau = tau;
-  if (G == 4)
-    window_decode_kernel<4><<<static_cast<unsigned>(units), kThreads, 0, stream>>>(p);
-  else if (G == 8)
-    window_decode_kernel<8><<<static_cast<unsigned>(units), kThreads, 0, stream>>>(p);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(units));
+  if (G == 4) return launch_staged(window_decode_kernel<4>, grid, p, stream);
+  if (G == 8) return launch_staged(window_decode_kernel<8>, grid, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace embla
