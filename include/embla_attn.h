@@ -35,7 +35,7 @@
  *     G must be 4 or 8.
  *   - `workspace` is caller-provided device scratch of at least the size the
  *     matching *_workspace_size call returns for the same shape on the
- *     current device.  Its contents need not be initialised and are not
+ *     current device (NULL when that size is 0).  Its contents need not be initialised and are not
  *     meaningful after the call.  Calls that share a workspace must be
  *     ordered on one stream.
  */
@@ -199,7 +199,7 @@ embla_status embla_window_decode(const embla_shape *shape, const void *q, const 
  * if `clear` is non-zero, resets it.  Returns EMBLA_ERR_DEVICE_CHECK when any
  * flag was set, EMBLA_OK otherwise.
  *   bit 0  index out of range (sparse decode)
- *   bit 1  pipeline wait timed out (full decode)
+ *   bit 1  a wait for data in flight timed out (full decode, selection)
  */
 embla_status embla_device_check(uint32_t *flags, int clear, void *stream);
 

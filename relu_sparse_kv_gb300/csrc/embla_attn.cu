@@ -239,14 +239,18 @@ embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores
     return EMBLA_ERR_INVALID_ARG;
   const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
   if (units == 0) return EMBLA_OK;
-  if (!sel_scores || !sel_hist || !idx || !count || !workspace) return EMBLA_ERR_INVALID_ARG;
-  if (!aligned16(sel_scores) || !aligned16(sel_hist) || !aligned16(idx) || !aligned16(count) ||
-      !aligned16(workspace))
+  const size_t ws_need = select_workspace_bytes(units, shape->ctx_len);
+  if (!sel_scores || !sel_hist || !idx || !count || (ws_need && !workspace))
     return EMBLA_ERR_INVALID_ARG;
-  if (workspace_bytes < select_workspace_bytes(units, shape->ctx_len)) return EMBLA_ERR_WORKSPACE;
+  if (!aligned16(sel_scores) || !aligned16(sel_hist) || !aligned16(idx) || !aligned16(count) ||
+      (workspace && !aligned16(workspace)))
+    return EMBLA_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_need) return EMBLA_ERR_WORKSPACE;
+  uint32_t *flags = flags_ptr();
+  if (!flags) return EMBLA_ERR_CUDA;
   return cuda_status(launch_select(sel_scores, sel_hist, units, shape->ctx_len,
                                    shape->cache_stride, topk, recent, idx, idx_stride, count,
-                                   workspace, static_cast<cudaStream_t>(stream)));
+                                   workspace, flags, static_cast<cudaStream_t>(stream)));
 }
 
 size_t embla_sparse_decode_workspace_size(const embla_shape *shape, int32_t idx_stride) {

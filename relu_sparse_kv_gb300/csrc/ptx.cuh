@@ -170,6 +170,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Cluster barrier in two halves: arrive once this CTA no longer needs the others' shared
+// memory, wait before leaving so no CTA's shared memory goes away while it is read.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start launching, and
 // wait until the kernel this one was launched behind has finished and its writes are
 // visible (returns at once when there is no such dependency).

@@ -131,6 +131,35 @@ def test_select_handles_a_crowded_boundary_bin():
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
 
 
+def _select_case(sig, n, ncap):
+    """Run the selection on given scores (rows of ncap, the first n used) and compare."""
+    B, Hkv = sig.shape[:2]
+    shape = E.Shape(B, 16, Hkv, D, n, ncap)
+    hist = np.stack([[np.bincount(order_key_np(sig[b, g, :n]) >> 21, minlength=E.HIST_BINS)
+                      for g in range(Hkv)] for b in range(B)]).astype(np.int32)
+    idx = torch.full((B, Hkv, 1152), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(B, Hkv, dtype=torch.int32, device="cuda")
+    E.embla_select_topk(shape, torch.from_numpy(sig).cuda(), torch.from_numpy(hist).cuda(), idx, cnt)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    ref_idx, ref_cnt = oracle.select_topk_batch(sig, n)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
+@pytest.mark.parametrize("n,ncap", [(262144, 262144), (300000, 300000), (50001, 50003),
+                                    (4097, 4098), (1153, 1157)])
+def test_select_long_and_unaligned_rows(n, ncap):
+    # the largest context one cluster holds in shared memory, one past it (the streaming
+    # kernel), and row strides that start every unit's scores at a different 4-byte phase
+    rng = np.random.default_rng(n)
+    B, Hkv = 2, 4
+    sig = rng.standard_normal((B, Hkv, ncap)).astype(np.float32)
+    sig[:, :, n:] = np.nan
+    sig[0, 3, :n] = np.round(sig[0, 3, :n] * 4) / 4  # many exact ties
+    _select_case(sig, n, ncap)
+
+
 @pytest.mark.parametrize("pos", [0, 5, 126, 127, 128, 1000, 65535])
 @pytest.mark.parametrize("G", [4, 8])
 def test_window_decode(pos, G):
