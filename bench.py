@@ -190,6 +190,26 @@ def _dist():
     return world, rank, local
 
 
+def _graph_events_work(torch, stream) -> bool:
+    """Whether timing events can be recorded inside a captured CUDA graph (PyTorch's
+    external events) and read back after a replay."""
+    try:
+        a = torch.cuda.Event(enable_timing=True, external=True)
+        b = torch.cuda.Event(enable_timing=True, external=True)
+        x = torch.zeros(1024, device=stream.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                a.record(stream)
+                x.add_(1.0)
+                b.record(stream)
+            g.replay()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) >= 0.0
+    except Exception:
+        return False
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest of every rank's x (x itself on one rank).  The timed regions of all ranks
     are bracketed by barriers, so the slowest rank's time is the job's time."""
@@ -374,24 +394,66 @@ def main():
     torch.cuda.synchronize()
     assert E.embla_device_check() == 0
 
-    # graphs: one per full-layer call (timed alone for the roofline) and one for the rest
     stream = torch.cuda.Stream(device=dev)
-    g_full, g_rest = [], []
-    with torch.cuda.stream(stream):
-        for L in layers:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                full_call(L)
-            g_full.append(g)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                rest_calls(L)
-            g_rest.append(g)
-        g_win = None
-        if wins:
-            g_win = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_win, stream=stream):
+    nl = len(layers)
+    in_graph_events = _graph_events_work(torch, stream)
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        return g
+
+    if in_graph_events:
+        # one graph per timed step (a decode step is one graph launch), with the events
+        # around each full-layer call recorded inside it
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(args.steps * nl)]
+
+        side = torch.cuda.Stream(device=dev)
+
+        def step_body(i):
+            # the event after a full-layer call is recorded on a side branch of the graph,
+            # so the call's kernel and the next one stay directly chained
+            def body():
+                for li, L in enumerate(layers):
+                    if i is not None:
+                        ev[i * nl + li][0].record(stream)
+                    full_call(L)
+                    if i is not None:
+                        side.wait_stream(stream)
+                        ev[i * nl + li][1].record(side)
+                    rest_calls(L)
                 window_calls()
+                if i is not None:
+                    stream.wait_stream(side)
+            return body
+
+        with torch.cuda.stream(stream):
+            g_warm = capture(step_body(None))
+            g_steps = [capture(step_body(i)) for i in range(args.steps)]
+
+        def step(timed_i=None):
+            (g_warm if timed_i is None else g_steps[timed_i]).replay()
+    else:
+        # graphs: one per full-layer call (timed alone for the roofline) and one for the rest
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps * nl)]
+        with torch.cuda.stream(stream):
+            g_full = [capture(lambda L=L: full_call(L)) for L in layers]
+            g_rest = [capture(lambda L=L: rest_calls(L)) for L in layers]
+            g_win = capture(window_calls) if wins else None
+
+        def step(timed_i=None):
+            for li, (gf, gr) in enumerate(zip(g_full, g_rest)):
+                if timed_i is not None:
+                    ev[timed_i * nl + li][0].record(stream)
+                gf.replay()
+                if timed_i is not None:
+                    ev[timed_i * nl + li][1].record(stream)
+                gr.replay()
+            if g_win is not None:
+                g_win.replay()
     torch.cuda.synchronize()
 
     # accounting from this rank's own results
@@ -415,20 +477,6 @@ def main():
             launches_per_step += 1 + len(L["qs"])
     launches_per_step += len(wins)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps * len(layers))]
-
-    def step(timed_i=None):
-        for li, (gf, gr) in enumerate(zip(g_full, g_rest)):
-            if timed_i is not None:
-                ev[timed_i * len(layers) + li][0].record(stream)
-            gf.replay()
-            if timed_i is not None:
-                ev[timed_i * len(layers) + li][1].record(stream)
-            gr.replay()
-        if g_win is not None:
-            g_win.replay()
-
     clocks = ClockSampler(local)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -448,8 +496,8 @@ def main():
         torch.distributed.barrier()
     clk = clocks.stop(t_wall0, t_wall1)
     ms = start.elapsed_time(end)
-    full_ms = [statistics.mean(ev[i * len(layers) + li][0].elapsed_time(ev[i * len(layers) + li][1])
-                               for i in range(args.steps)) for li in range(len(layers))]
+    full_ms = [statistics.mean(ev[i * nl + li][0].elapsed_time(ev[i * nl + li][1])
+                               for i in range(args.steps)) for li in range(nl)]
     assert E.embla_device_check() == 0
     ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
@@ -530,6 +578,10 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {**static_config(args.config, args.batch, args.ctx),
+                   "launch": ("one CUDA graph per step; events inside it around each full-layer call "
+                              "(the closing one on a side branch)"
+                              if in_graph_events else
+                              "two CUDA graphs per full layer (its call, then the rest); events between them"),
                    "l2": "not flushed: inputs larger than L2 (each full layer's K cache is "
                          f"{keys_total * ROW_BYTES // len(layers) / 1e6:.0f} MB)",
                    "needed_bytes_per_step": needed,

@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *rkfull = sfull + kWSlots;    // key norms of a tile written
   uint64_t *rkempty = rkfull + kNormSlots;  // key norms of a tile read
 
+  // the zeroing kernel before this one waited for everything earlier, so the selection
+  // kernel after this one may launch now (it waits for this kernel to finish)
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
@@ -747,10 +750,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Zeroes what the decode accumulates into with atomics: the selection histogram (if any)
-// and the per-unit arrival counters.  It lets the decode kernel launch at once; the decode
-// waits for it only before its first histogram flush and its first arrival.
+// and the per-unit arrival counters.  Once the kernel before it has finished it lets the
+// decode kernel launch; the decode waits for the zeroing only before its first histogram
+// flush and its first arrival.
 __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t hist_vecs,
                                                         int32_t *arrivals, int64_t n_arrivals) {
+  pdl_wait_primary();
   pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -768,21 +773,12 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
   const int64_t hist_vecs = p.hist ? units * kHistBins / 4 : 0;
   const int64_t work = hist_vecs > 4 * units ? hist_vecs : 4 * units;
   const int64_t zblocks = (work + 255) / 256;
-  full_zero_kernel<<<static_cast<unsigned>(zblocks < 1024 ? zblocks : 1024), 256, 0, stream>>>(
-      reinterpret_cast<uint4 *>(p.hist), hist_vecs, p.arrivals, 4 * units);
-  e = cudaGetLastError();
+  e = launch_pdl(full_zero_kernel, dim3(static_cast<unsigned>(zblocks < 1024 ? zblocks : 1024)),
+                 dim3(256), 0, stream, 0u, reinterpret_cast<uint4 *>(p.hist), hist_vecs,
+                 p.arrivals, 4 * units);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.P));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, full_decode_kernel<G>, tm_k, tm_q, p);
+  return launch_pdl(full_decode_kernel<G>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
+                    static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, p);
 }
 
 }  // namespace

@@ -5,8 +5,40 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace embla {
+
+// Launch a kernel of this library so that it may be scheduled while the kernel before it
+// in the stream is still running (programmatic dependent launch).  Every such kernel
+// waits for its predecessor to finish (griddepcontrol.wait) before it reads an input or
+// writes an output, and only then lets its own successor launch, so stream order holds
+// for data; what overlaps is the launch itself.  `cluster` > 0 sets the cluster size of
+// kernels that do not fix it at compile time.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = static_cast<unsigned>(na);
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kHeadDim = 128;
 constexpr int kTileKeys = 128;     // keys per full-decode tile (the MMA's M)

@@ -165,6 +165,8 @@ __device__ void bitonic_desc(uint64_t *keys, int m) {
 
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads)
     select_kernel(const SelParams p) {
+  pdl_wait_primary();  // the scores and histogram are complete
+  pdl_launch_dependents();
   __shared__ Shared sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -562,6 +564,8 @@ __device__ __forceinline__ int fast_scan(int v, int *total, int32_t *warp_sum) {
 }
 
 __global__ void __launch_bounds__(kFThreads, 1) select_fast_kernel(const FastParams p) {
+  pdl_wait_primary();  // the scores and histogram are complete
+  pdl_launch_dependents();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   FastShared &sh = *reinterpret_cast<FastShared *>(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
@@ -886,19 +890,8 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
     cudaError_t e = cudaFuncSetAttribute(select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sizeof(FastShared) + (kFKeys + 4) * sizeof(uint32_t)));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(units * f.cl));
-    cfg.blockDim = dim3(kFThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(bytes);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(f.cl);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, select_fast_kernel, f);
+    return launch_pdl(select_fast_kernel, dim3(static_cast<unsigned>(units * f.cl)), dim3(kFThreads),
+                      static_cast<size_t>(bytes), stream, static_cast<unsigned>(f.cl), f);
   }
   const SelLayout L = sel_layout(units, n);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -918,8 +911,8 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
   p.idx = idx;
   p.idx_stride = idx_stride;
   p.count = count;
-  select_kernel<<<static_cast<unsigned>(units * kCl), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(static_cast<unsigned>(units * kCl)), dim3(kThreads), 0,
+                    stream, 0u, p);
 }
 
 }  // namespace embla

@@ -110,23 +110,6 @@ __device__ __forceinline__ uint32_t stage_rows(const WarpStage &ws, const uint8_
   return present;
 }
 
-// acc += a . b over the 8 bf16 pairs of two uint4 (bf16 products are exact in fp32)
-__device__ __forceinline__ float dot8_bf16(const uint4 &a, const uint4 &b) {
-  float s0 = 0.0f, s1 = 0.0f;
-  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-      "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %6;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t"
-      "mov.b32 {al, ah}, %3;\n\tmov.b32 {bl, bh}, %7;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t"
-      "mov.b32 {al, ah}, %4;\n\tmov.b32 {bl, bh}, %8;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t"
-      "mov.b32 {al, ah}, %5;\n\tmov.b32 {bl, bh}, %9;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
-      : "+f"(s0), "+f"(s1)
-      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
-  return s0 + s1;
-}
-
 // Fold one chunk into the group's running softmax state.  Scores are kept in base 2:
 // tau2 = tau * log2(e), so exp(tau * s - m) = exp2(tau2 * s - m2).
 template <int G, class Dots>
@@ -266,20 +249,6 @@ __device__ void merge_warps(Merge<G> &mg, Soft<G> &st, int warp, int lane) {
 }
 
 // Partial dot products of this lane's 8 dims of a key row with every head's query.
-// Sparse layers use the raw bf16 query (exact bf16 products, fp32 sums).
-template <int G>
-struct DotsBf16 {
-  uint4 q[G];
-  __device__ void load(const uint16_t *qrow, int sl) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) q[h] = *reinterpret_cast<const uint4 *>(qrow + h * kHeadDim + sl * 8);
-  }
-  __device__ __forceinline__ void operator()(const uint4 &k, float (&d)[G]) const {
-#pragma unroll
-    for (int h = 0; h < G; ++h) d[h] = dot8_bf16(q[h], k);
-  }
-};
-
 // Window layers use the rotated query, kept in fp32.
 template <int G>
 struct DotsF32 {
@@ -347,6 +316,8 @@ __device__ __forceinline__ uint32_t sp_piece(int r, int c) {
 template <int G>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2)
     sparse_decode_kernel(const SparseParams p) {
+  pdl_wait_primary();  // the selection and the query are complete
+  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];  // staged rows, then the merge state
   SpMerge<G> &mg = *reinterpret_cast<SpMerge<G> *>(smem);
   cg::cluster_group cluster = cg::this_cluster();
@@ -505,7 +476,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2
   // the cluster's CTAs each finish an eighth of the outputs from all eight states
   cluster.sync();
   constexpr int kPer = G * kHeadDim / kCluster;
-  for (int i = rank * kPer + threadIdx.x; i < (rank + 1) * kPer; i += kSpThreads) {
+  static_assert(kPer <= kSpThreads, "one output per thread");
+  const int i = rank * kPer + threadIdx.x;
+  float res = 0.0f;
+  if (threadIdx.x < kPer) {
     const int h = i / kHeadDim, d = i % kHeadDim;
     float cmv[kCluster];
     float M = -INFINITY;
@@ -524,9 +498,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2
         A = fmaf(o2->ca[h][d], f, A);
       }
     }
-    p.out[u * G * kHeadDim + i] = L > 0.0f ? A / L : 0.0f;
+    res = L > 0.0f ? A / L : 0.0f;
   }
-  cluster.sync();  // the other CTAs' shared memory stays alive until every CTA is done
+  cluster_arrive();  // done reading the other CTAs' shared memory
+  if (threadIdx.x < kPer) p.out[u * G * kHeadDim + i] = res;
+  cluster_wait();  // and they are done reading this one's
 }
 
 // ----------------------------------------------------------------------------- window
@@ -542,6 +518,8 @@ struct WindowParams {
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1) window_decode_kernel(const WindowParams p) {
+  pdl_wait_primary();  // the query and the ring are complete
+  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];  // staged rows, then the merge state
   Merge<G> &mg = *reinterpret_cast<Merge<G> *>(smem);
   const int64_t u = blockIdx.x;
@@ -608,8 +586,7 @@ cudaError_t launch_staged(void (*kernel)(Params), dim3 grid, const Params &p, cu
   static_assert(sizeof(Merge<8>) <= kStageBytes, "the merge state fits the staging space");
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, kStageBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, dim3(kThreads), kStageBytes, stream, 0u, p);
 }
 
 cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const SparseParams &p,
@@ -618,8 +595,7 @@ cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const Spars
   static_assert(sizeof(SpMerge<8>) <= bytes, "the merge state fits the staging space");
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kSpThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, dim3(kSpThreads), bytes, stream, 0u, p);
 }
 
 }  // namespace
