@@ -248,9 +248,11 @@ embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores
   if (workspace_bytes < ws_need) return EMBLA_ERR_WORKSPACE;
   uint32_t *flags = flags_ptr();
   if (!flags) return EMBLA_ERR_CUDA;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return EMBLA_ERR_CUDA;
   return cuda_status(launch_select(sel_scores, sel_hist, units, shape->ctx_len,
                                    shape->cache_stride, topk, recent, idx, idx_stride, count,
-                                   workspace, flags, static_cast<cudaStream_t>(stream)));
+                                   workspace, flags, sms, static_cast<cudaStream_t>(stream)));
 }
 
 size_t embla_sparse_decode_workspace_size(const embla_shape *shape, int32_t idx_stride) {

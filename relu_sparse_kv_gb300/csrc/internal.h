@@ -81,7 +81,7 @@ size_t select_workspace_bytes(int64_t units, int64_t ctx_len);
 cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int64_t units,
                           int64_t n, int64_t ncap, int topk, int recent, int32_t *idx,
                           int idx_stride, int32_t *count, void *workspace, uint32_t *flags,
-                          cudaStream_t stream);
+                          int sm_count, cudaStream_t stream);
 
 size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride);
 cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,

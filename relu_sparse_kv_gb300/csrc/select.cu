@@ -868,10 +868,16 @@ size_t select_workspace_bytes(int64_t units, int64_t ctx_len) {
 cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int64_t units,
                           int64_t n, int64_t ncap, int topk, int recent, int32_t *idx,
                           int idx_stride, int32_t *count, void *workspace, uint32_t *flags,
-                          cudaStream_t stream) {
+                          int sm_count, cudaStream_t stream) {
   if (units == 0) return cudaSuccess;
   if (n <= static_cast<int64_t>(kMaxCluster) * kFKeys) {
+    // about kFChunk keys per CTA, but no more CTAs than two per SM over all units (one
+    // wave), and never more than kFKeys keys in one CTA
     int64_t cl = (n + kFChunk - 1) / kFChunk;
+    const int64_t wave = units > 0 ? (2 * static_cast<int64_t>(sm_count)) / units : 1;
+    if (cl > wave) cl = wave;
+    const int64_t least = (n + kFKeys - 1) / kFKeys;
+    if (cl < least) cl = least;
     cl = cl < 1 ? 1 : (cl > kMaxCluster ? kMaxCluster : cl);
     FastParams f;
     f.sel = sel_scores;

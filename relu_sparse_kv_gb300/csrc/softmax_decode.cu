@@ -513,7 +513,8 @@ struct WindowParams {
   float *out;
   int64_t pos;
   int window;
-  float rope_base, tau;
+  float tau;
+  float cs[kHeadDim / 2], sn[kHeadDim / 2];  // cos, sin of the rotation of pair i at pos
 };
 
 template <int G>
@@ -526,17 +527,14 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1) window_decode_kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 4, sl = lane & 15;
   DotsF32<G> dots;
-  // this lane's dims 8sl..8sl+7 are rotary pairs 4sl..4sl+3; pair i turns by
-  // pos * base^(-2i/D), the angle formed in double so large positions keep their phase
+  // this lane's dims 8sl..8sl+7 are rotary pairs 4sl..4sl+3; the launch supplies each
+  // pair's cos and sin at pos
   {
     const uint16_t *qrow = p.q + u * G * kHeadDim + sl * 8;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int i = 4 * sl + k;
-      const double inv = pow(static_cast<double>(p.rope_base), -2.0 * i / kHeadDim);
-      double sn, cs;
-      sincos(static_cast<double>(p.pos) * inv, &sn, &cs);
-      const float c = static_cast<float>(cs), s = static_cast<float>(sn);
+      const float c = p.cs[i], s = p.sn[i];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const uint32_t w = *reinterpret_cast<const uint32_t *>(qrow + h * kHeadDim + 2 * k);
@@ -645,8 +643,16 @@ cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const 
   p.out = out;
   p.pos = pos;
   p.window = window;
-  p.rope_base = rope_base;
   p.tau = tau;
+  // pair i turns by pos * base^(-2i/D): the angle in double, reduced to [-pi, pi] before
+  // its cosine and sine, so large positions keep their phase
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < kHeadDim / 2; ++i) {
+    const double ang = static_cast<double>(pos) * std::pow(static_cast<double>(rope_base), -2.0 * i / kHeadDim);
+    const double red = ang - two_pi * std::nearbyint(ang / two_pi);
+    p.cs[i] = static_cast<float>(std::cos(red));
+    p.sn[i] = static_cast<float>(std::sin(red));
+  }
   const dim3 grid(static_cast<unsigned>(units));
   if (G == 4) return launch_staged(window_decode_kernel<4>, grid, p, stream);
   if (G == 8) return launch_staged(window_decode_kernel<8>, grid, p, stream);
