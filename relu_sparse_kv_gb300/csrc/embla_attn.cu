@@ -280,9 +280,11 @@ embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const 
   if (workspace_bytes < sparse_workspace_bytes(units, G, idx_stride)) return EMBLA_ERR_WORKSPACE;
   uint32_t *flags = flags_ptr();
   if (!flags) return EMBLA_ERR_CUDA;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return EMBLA_ERR_CUDA;
   return cuda_status(launch_sparse_decode(G, q, k_cache, v_cache, idx, idx_stride, count, units,
                                           shape->n_kv_heads, shape->ctx_len, shape->cache_stride,
-                                          tau, out, workspace, flags,
+                                          tau, out, workspace, flags, sms,
                                           static_cast<cudaStream_t>(stream)));
 }
 

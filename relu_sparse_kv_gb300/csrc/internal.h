@@ -87,7 +87,8 @@ size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride);
 cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
                                  const int32_t *idx, int idx_stride, const int32_t *count,
                                  int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
-                                 float *out, void *workspace, uint32_t *flags, cudaStream_t stream);
+                                 float *out, void *workspace, uint32_t *flags, int sm_count,
+                                 cudaStream_t stream);
 
 cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const void *v_win,
                                  int64_t units, int window, int64_t pos, float rope_base,

@@ -15,7 +15,7 @@
 // and gathered back, then every lane updates its group's running max m, sum l and its
 // 8-dim slice of the unnormalised output, rescaling once per chunk.  Warps merge in
 // shared memory (reusing the rows' space) by rescaling with exp(m_w - M).
-// A sparse layer spreads each (batch, KV-head) unit over a cluster of 8 CTAs that merge
+// A sparse layer spreads each (batch, KV-head) unit over a cluster of up to 8 CTAs that merge
 // through distributed shared memory; a window layer uses one CTA per unit.
 #include <cooperative_groups.h>
 
@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kCluster = 8;        // CTAs per sparse unit
+constexpr int kMaxCluster = 8;     // CTAs per sparse unit, at most
 constexpr int kWarpRows = 20;      // rows a warp stages per pass
 constexpr int kStageBytes = kWarps * kWarpRows * 2 * kHeadDim * 2;  // 80 KB: K and V rows
 constexpr float kLog2e = 1.4426950408889634f;
@@ -305,6 +305,7 @@ struct SparseParams {
   uint32_t *flags;
   int64_t n, ncap;
   int idx_stride, rows_per_cta;
+  int cl;  // CTAs per unit (the cluster size): 1, 2, 4 or 8
   float tau;
 };
 
@@ -313,8 +314,8 @@ __device__ __forceinline__ uint32_t sp_piece(int r, int c) {
   return static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
 }
 
-template <int G>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2)
+template <int G, int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
     sparse_decode_kernel(const SparseParams p) {
   pdl_wait_primary();  // the selection and the query are complete
   pdl_launch_dependents();
@@ -322,7 +323,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2
   SpMerge<G> &mg = *reinterpret_cast<SpMerge<G> *>(smem);
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
-  const int64_t u = blockIdx.x / kCluster;
+  const int64_t u = blockIdx.x / CL;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   int cnt = p.count[u];
@@ -473,35 +474,44 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kSpThreads, 2
       mg.cl[h] = L;
     }
   }
-  // the cluster's CTAs each finish an eighth of the outputs from all eight states
+  // the cluster's CTAs each finish their share of the outputs from all the CTAs' states
   cluster.sync();
-  constexpr int kPer = G * kHeadDim / kCluster;
-  static_assert(kPer <= kSpThreads, "one output per thread");
-  const int i = rank * kPer + threadIdx.x;
-  float res = 0.0f;
-  if (threadIdx.x < kPer) {
-    const int h = i / kHeadDim, d = i % kHeadDim;
-    float cmv[kCluster];
-    float M = -INFINITY;
+  constexpr int per = G * kHeadDim / CL;  // outputs of this CTA (at most 4 per thread)
+  static_assert(per <= 4 * kSpThreads, "at most 4 outputs per thread");
+  float res[4];
 #pragma unroll
-    for (int c = 0; c < kCluster; ++c) {
-      cmv[c] = cluster.map_shared_rank(&mg, c)->cm[h];
-      M = fmaxf(M, cmv[c]);
-    }
-    float L = 0.0f, A = 0.0f;
-    if (M != -INFINITY) {
+  for (int k = 0; k < 4; ++k) {
+    res[k] = 0.0f;
+    const int li = threadIdx.x + k * kSpThreads;
+    if (li < per) {
+      const int i = rank * per + li;
+      const int h = i / kHeadDim, d = i % kHeadDim;
+      float cmv[CL];
+      float M = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kCluster; ++c) {
-        const SpMerge<G> *o2 = cluster.map_shared_rank(&mg, c);
-        const float f = exp2f(cmv[c] - M);
-        L = fmaf(o2->cl[h], f, L);
-        A = fmaf(o2->ca[h][d], f, A);
+      for (int c = 0; c < CL; ++c) {
+        cmv[c] = cluster.map_shared_rank(&mg, c)->cm[h];
+        M = fmaxf(M, cmv[c]);
       }
+      float L = 0.0f, A = 0.0f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+          const SpMerge<G> *o2 = cluster.map_shared_rank(&mg, c);
+          const float f = exp2f(cmv[c] - M);
+          L = fmaf(o2->cl[h], f, L);
+          A = fmaf(o2->ca[h][d], f, A);
+        }
+      }
+      res[k] = L > 0.0f ? A / L : 0.0f;
     }
-    res = L > 0.0f ? A / L : 0.0f;
   }
   cluster_arrive();  // done reading the other CTAs' shared memory
-  if (threadIdx.x < kPer) p.out[u * G * kHeadDim + i] = res;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int li = threadIdx.x + k * kSpThreads;
+    if (li < per) p.out[u * G * kHeadDim + rank * per + li] = res[k];
+  }
   cluster_wait();  // and they are done reading this one's
 }
 
@@ -596,6 +606,16 @@ cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const Spars
   return launch_pdl(kernel, grid, dim3(kSpThreads), bytes, stream, 0u, p);
 }
 
+template <int G>
+cudaError_t launch_sparse_g(dim3 grid, const SparseParams &p, cudaStream_t stream) {
+  switch (p.cl) {
+    case 8: return launch_sparse_t(sparse_decode_kernel<G, 8>, grid, p, stream);
+    case 4: return launch_sparse_t(sparse_decode_kernel<G, 4>, grid, p, stream);
+    case 2: return launch_sparse_t(sparse_decode_kernel<G, 2>, grid, p, stream);
+    default: return launch_sparse_t(sparse_decode_kernel<G, 1>, grid, p, stream);
+  }
+}
+
 }  // namespace
 
 size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride) {
@@ -608,7 +628,7 @@ size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride) {
 cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
                                  const int32_t *idx, int idx_stride, const int32_t *count,
                                  int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
-                                 float *out, void *workspace, uint32_t *flags,
+                                 float *out, void *workspace, uint32_t *flags, int sm_count,
                                  cudaStream_t stream) {
   (void)Hkv;
   (void)workspace;
@@ -624,11 +644,15 @@ cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, cons
   p.n = n;
   p.ncap = ncap;
   p.idx_stride = idx_stride;
-  p.rows_per_cta = ((idx_stride + kCluster - 1) / kCluster + kSpBlock - 1) / kSpBlock * kSpBlock;
+  // 8 CTAs per unit, fewer when that would take more than one wave (two CTAs per SM)
+  int cl = kMaxCluster;
+  while (cl > 1 && units * cl > 2 * static_cast<int64_t>(sm_count)) cl >>= 1;
+  p.cl = cl;
+  p.rows_per_cta = ((idx_stride + cl - 1) / cl + kSpBlock - 1) / kSpBlock * kSpBlock;
   p.tau = tau;
-  const dim3 grid(static_cast<unsigned>(units * kCluster));
-  if (G == 4) return launch_sparse_t(sparse_decode_kernel<4>, grid, p, stream);
-  if (G == 8) return launch_sparse_t(sparse_decode_kernel<8>, grid, p, stream);
+  const dim3 grid(static_cast<unsigned>(units * cl));
+  if (G == 4) return launch_sparse_g<4>(grid, p, stream);
+  if (G == 8) return launch_sparse_g<8>(grid, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -196,6 +196,29 @@ def test_sparse_decode_with_arbitrary_indices_and_counts():
     assert_close(got, ref)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv", [(10, 16, 4), (20, 16, 4), (40, 16, 4), (80, 16, 4),
+                                      (40, 16, 2), (90, 16, 2)])
+def test_sparse_decode_cluster_sizes(B, Hq, Hkv):
+    # 40 .. 320 units: the launch spreads a unit over 8, 4, 2 or 1 CTAs to stay one wave
+    n, stride = 1400, 1152
+    rng = np.random.default_rng(B * 7 + Hkv)
+    q = gen.normal_bf16(21, (B, Hq, D))
+    K = gen.normal_bf16(22, (B, Hkv, n, D))
+    V = gen.normal_bf16(23, (B, Hkv, n, D))
+    cnt = rng.integers(0, stride + 1, size=(B, Hkv)).astype(np.int64)
+    idx = np.zeros((B, Hkv, stride), dtype=np.int32)
+    for b in range(B):
+        for g in range(Hkv):
+            idx[b, g, :cnt[b, g]] = np.sort(rng.choice(n, cnt[b, g], replace=False))
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    E.embla_sparse_decode(shape, to_dev(q), to_dev(K), to_dev(V), torch.from_numpy(idx).cuda(),
+                          torch.from_numpy(cnt.astype(np.int32)).cuda(), out)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    assert_close(out.cpu().numpy(), oracle.sparse_decode_batch(q, K, V, idx, cnt))
+
+
 def test_out_of_range_index_is_skipped_and_flagged():
     B, Hq, Hkv, n = 1, 16, 4, 300
     q = gen.normal_bf16(21, (B, Hq, D))
