@@ -8,7 +8,7 @@
 // One persistent CTA per SM walks a contiguous run of 128-key tiles of the flattened
 // (unit, tile) sequence, unit = (batch, KV head).  Warp roles:
 //   warp 0     TMA producer: 32 KB K tiles (two 64-column boxes, 128-byte swizzle) into
-//              a 4-stage ring; the unit's G query rows when the unit changes.
+//              a 3-stage ring; the unit's G query rows when the unit changes.
 //   warps 1, 18  tcgen05 issuers taking alternate tiles: D[128 keys x 16] = K . Q^T
 //              (raw bf16 operands, fp32 in tensor memory), one independent MMA per
 //              16-dim k-step; four tiles in flight use all 512 columns.
@@ -18,7 +18,7 @@
 //   warps 2-9  two epilogue warpgroups taking alternate tiles, one thread per key:
 //              s_h = dot_h * alpha*rq_h * rk, sigma = max_h s_h; lists the keys with
 //              sigma > 0 with their ReLU^2 weights in key order; a leader reserves that
-//              many rows of a 128-row V ring (in tile order), and every surviving key's
+//              many rows of a 256-row V ring (in tile order), and every surviving key's
 //              thread copies its own 256-byte V row into the ring.
 //   warp 19    selection scores (when requested): writes each tile's sigma to global
 //              memory and counts it into a shared histogram, flushed when a unit's
@@ -34,15 +34,21 @@ namespace embla {
 namespace {
 
 #ifndef EMBLA_K_STAGES
-#define EMBLA_K_STAGES 4
+#define EMBLA_K_STAGES 3
 #endif
 #ifndef EMBLA_W_SLOTS
 #define EMBLA_W_SLOTS 8
 #endif
 #ifndef EMBLA_V_RING_ROWS
-#define EMBLA_V_RING_ROWS 128
+#define EMBLA_V_RING_ROWS 256
 #endif
 constexpr int kStages = EMBLA_K_STAGES;            // K tiles in flight
+// Tile i lands on barrier full[(i % kStages) * 2 + (i & 1)]: one barrier per stage and MMA
+// issuer, so the uses of each barrier are consumed in order by one issuer (with an odd
+// stage count a stage's consecutive tiles belong to different issuers, and a parity test
+// by one issuer could be answered by the other's phase).  Barrier uses repeat every
+// kFullPeriod tiles.
+constexpr int kFullPeriod = kStages % 2 == 0 ? kStages : 2 * kStages;
 constexpr int kWSlots = EMBLA_W_SLOTS;             // per-tile survivor lists in flight
 constexpr int kRing = EMBLA_V_RING_ROWS;           // V rows in flight
 constexpr int kGroups = 2;                         // epilogue warpgroups, alternating tiles
@@ -94,7 +100,7 @@ struct Smem {
   static constexpr int misc_off = rk_off + kNormSlots * kTileKeys * 4;
   static constexpr int end_off = misc_off + 64;                 // int64 per W slot, + 2 ring counters
   static constexpr int bar_off = end_off + (kWSlots + 2) * 8;
-  static constexpr int n_bars = 2 * kStages + 2 * kAccBufs + 4 + 4 * kWSlots + 2 * kNormSlots;
+  static constexpr int n_bars = 3 * kStages + 2 * kAccBufs + 4 + 4 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
 };
@@ -165,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t *s_ring_issued = s_end + kWSlots;  // ring rows reserved so far
   int64_t *s_ring_freed = s_end + kWSlots + 1;  // ring rows known consumed
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
-  uint64_t *full = bars;                 // K tile landed
-  uint64_t *empty = full + kStages;      // K tile consumed (MMA and key norms)
+  uint64_t *full = bars;                 // K tile landed: [stage][tile parity]
+  uint64_t *empty = full + 2 * kStages;  // K tile consumed (MMA and key norms)
   uint64_t *accf = empty + kStages;      // accumulator written
   uint64_t *acce = accf + kAccBufs;      // accumulator read
   uint64_t *qfull = acce + kAccBufs;     // query rows landed
@@ -193,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[2 * s], 1);
+      mbar_init(&full[2 * s + 1], 1);
       mbar_init(&empty[s], 5);  // MMA commit + the four norm warps
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -266,10 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           set_abort(s_abort, p.flags);
           break;
         }
-        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        uint64_t *fb = &full[2 * s + (i & 1)];
+        mbar_arrive_expect_tx(fb, kTileBytes);
         const int32_t row = static_cast<int32_t>(static_cast<int64_t>(u) * p.ncap) + tl * kTileKeys;
-        tma_load_2d_hint(sK + s * kTileBytes, &tm_k, &full[s], 0, row, policy);
-        tma_load_2d_hint(sK + s * kTileBytes + kHalfBytes, &tm_k, &full[s], 64, row, policy);
+        tma_load_2d_hint(sK + s * kTileBytes, &tm_k, fb, 0, row, policy);
+        tma_load_2d_hint(sK + s * kTileBytes + kHalfBytes, &tm_k, fb, 64, row, policy);
         *s_k_issued = i + 1;
         if (++s == kStages) {
           s = 0;
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qdesc0 = smem_desc_sw128(smem_u32(sQ));
       uint64_t qdesc = qdesc0;
       int tl = tl0, seg = -1, qb = 0, issued = 0;
-      int s = 0, sphase = 0, b = 0, bphase = 0;
+      int s = 0, b = 0, bphase = 0;
       for (int i = 0; i < ntiles; ++i) {
         if (*s_abort) break;
         if (i == 0 || tl == 0) {
@@ -305,17 +313,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // not this issuer's tile; it still hands back the query buffer at a unit's end
           if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qempty[qb]);
           if (++tl == TU) tl = 0;
-          if (++s == kStages) {
-            s = 0;
-            sphase ^= 1;
-          }
+          if (++s == kStages) s = 0;
           if (++b == kAccBufs) {
             b = 0;
             bphase ^= 1;
           }
           continue;
         }
-        if (!mbar_wait(&full[s], sphase) || (i >= kAccBufs && !mbar_wait(&acce[b], bphase ^ 1))) {
+        if (!mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) ||
+            (i >= kAccBufs && !mbar_wait(&acce[b], bphase ^ 1))) {
           set_abort(s_abort, p.flags);
           break;
         }
@@ -334,10 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = i + 1;
         if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qempty[qb]);
         if (++tl == TU) tl = 0;
-        if (++s == kStages) {
-          s = 0;
-          sphase ^= 1;
-        }
+        if (++s == kStages) s = 0;
         if (++b == kAccBufs) {
           b = 0;
           bphase ^= 1;
@@ -422,10 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before_sync();
       const float rk = s_rk[ns * kTileKeys + row];
+      const float rk_used = __shfl_sync(0xffffffffu, rk, 31);  // every lane's read is back
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&acce[b]);
-        mbar_arrive(&rkempty[ns]);
+        mbar_arrive_after(&rkempty[ns], rk_used);
       }
 
       const int j = tl * kTileKeys + row;
@@ -522,8 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sg[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) sg[r] = ws.sig[lane + 32 * r];
+        float used = (sg[0] + sg[1]) + (sg[2] + sg[3]);
+        used = __shfl_sync(0xffffffffu, used, 31) + used;  // the whole warp takes part
         __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty[slot]);
+        if (lane == 0) mbar_arrive_after(&wempty[slot], used);
         float *dst = p.sel + static_cast<int64_t>(u) * p.ncap + tl * kTileKeys;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -558,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = static_cast<int>(i % kStages);
       const int ns = static_cast<int>(i % kNormSlots);
       const bool ok = __all_sync(0xffffffffu,
-                                 mbar_wait(&full[s], (i / kStages) & 1) &&
+                                 mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) &&
                                      (i < kNormSlots ||
                                       mbar_wait(&rkempty[ns], ((i / kNormSlots) - 1) & 1)));
       if (!ok) {
@@ -585,9 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq_acc_bf16x2(x1.z, a[4], a[5]);
         sq_acc_bf16x2(x1.w, a[6], a[7]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // every lane's sum depends on all of its reads of the stage
       const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+      const float done = __shfl_sync(0xffffffffu, ss, 0) + __shfl_sync(0xffffffffu, ss, 31);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_after(&empty[s], done);
       s_rk[ns * kTileKeys + row] = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
       __syncwarp();
       if (lane == 0) mbar_arrive(&rkfull[ns]);
@@ -646,8 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       seg_surv += m;
+      // the running sums depend on every ring row and weight this lane read
+      float used = 0.0f;
+#pragma unroll
+      for (int hh = 0; hh < HPW; ++hh)
+        used += den[hh] + ((acc[hh][0] + acc[hh][1]) + (acc[hh][2] + acc[hh][3]));
+      used = __shfl_sync(0xffffffffu, used, 31) + used;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&wempty[slot]);
+      if (lane == 0) mbar_arrive_after(&wempty[slot], used);
       if (i + 1 == ntiles || tl + 1 == TU) {
         float *r = p.rec + (cta + u) * p.rec_stride;
 #pragma unroll
@@ -730,9 +744,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // No copy may still be landing in shared memory when the CTA leaves: wait (bounded)
     // for the last armed phase of every barrier that a copy completes.
     const int k_issued = *s_k_issued, q_issued = *s_q_issued, v_issued = *s_v_issued;
-    for (int s = 0; s < kStages; ++s) {
-      const int uses = k_issued > s ? (k_issued - 1 - s) / kStages + 1 : 0;
-      if (uses) mbar_wait(&full[s], (uses - 1) & 1);
+    for (int f = 0; f < 2 * kStages; ++f) {
+      // tiles i < k_issued with i % kStages == f / 2 and i % 2 == f % 2
+      int uses = 0;
+      for (int i = 0; i < k_issued && i < kFullPeriod; ++i)
+        if (i % kStages == f / 2 && (i & 1) == (f & 1))
+          uses += (k_issued - 1 - i) / kFullPeriod + 1;
+      if (uses) mbar_wait(&full[f], (uses - 1) & 1);
     }
     for (int w = 0; w < kWSlots; ++w) {
       const int uses = v_issued > w ? (v_issued - 1 - w) / kWSlots + 1 : 0;

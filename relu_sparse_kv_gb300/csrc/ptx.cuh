@@ -49,6 +49,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
       : "memory");
 }
 
+// Arrive once `used` has been computed: a warp that read a shared buffer into registers
+// passes a value derived from everything it read, so the buffer is handed back only
+// after those reads have returned (and a refill cannot overwrite them in flight).
+__device__ __forceinline__ void mbar_arrive_after(uint64_t *bar, float used) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar)), "f"(used)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
