@@ -466,6 +466,17 @@ def main():
     needed = sum(full_bytes) + sparse_bytes + win_bytes
     keys_total = sum(L["shape"].units * L["fl"].n for L in layers)
     skipped_v = 1.0 - sum(n_surv_tot) / max(1, keys_total)
+    # the same V reads counted at the page's granularity (8-key chunks)
+    chunk_rows = 0
+    for L in layers:
+        if L["sel"] is None:
+            chunk_rows += L["shape"].units * L["fl"].n
+            continue
+        kn = torch.empty(L["shape"].batch, L["shape"].n_kv_heads, dtype=torch.int32, device=dev)
+        cn = torch.empty_like(kn)
+        E.embla_skip_stats(L["shape"], L["sel"], kn, cn, chunk=8)
+        chunk_rows += min(int(cn.sum().item()) * 8, L["shape"].units * L["fl"].n)
+    skipped_v_chunk8 = 1.0 - chunk_rows / max(1, keys_total)
     batch = layers[0]["shape"].batch
     # kernels of this library per step: per full layer a zeroing kernel and the decode
     # kernel, one selection kernel and one kernel per sparse layer, one window kernel per
@@ -587,7 +598,8 @@ def main():
                    "needed_bytes_per_step": needed,
                    "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),
                    "needed_frac_of_peak": round(needed / (ms_per_step * 1e-3) / 1e9 / peak, 4),
-                   "skipped_v_fraction": round(skipped_v, 5)},
+                   "skipped_v_fraction": round(skipped_v, 5),
+                   "skipped_v_fraction_8key_chunks": round(skipped_v_chunk8, 5)},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clk,
     }

@@ -192,6 +192,22 @@ embla_status embla_window_decode(const embla_shape *shape, const void *q, const 
                                  void *stream);
 
 /*
+ * V-read accounting — "The Architecture of Embla 1", "Skipping V": a value row
+ * is read only when some query head of the group gives its key a weight above
+ * zero, i.e. when sigma_j > 0; the page's own kernel decides this for groups of
+ * keys (8 at a time).  From the selection scores of embla_full_decode:
+ *   sel_scores     fp32 [B, Hkv, cache_stride], as embla_full_decode wrote them
+ *   chunk          a power of two, 1..1024 (8 on the page)
+ *   keys_needed    int32 [B, Hkv]: keys j < n with sigma_j > 0 (equals n_surv)
+ *   chunks_needed  int32 [B, Hkv]: chunks [c*chunk, (c+1)*chunk) of [0, n)
+ *                  holding at least one such key
+ * Reading V chunk by chunk reads (chunks_needed * chunk) rows, the last chunk
+ * cut at n; per-key compaction (embla_full_decode) reads keys_needed rows.
+ */
+embla_status embla_skip_stats(const embla_shape *shape, const float *sel_scores, int32_t chunk,
+                              int32_t *keys_needed, int32_t *chunks_needed, void *stream);
+
+/*
  * Device-side check word.  Kernels record failed checks (an index outside
  * [0, n) handed to embla_sparse_decode, a pipeline wait that exceeded its
  * time limit) by OR-ing flag bits into a word in device memory instead of

@@ -55,6 +55,8 @@ def _load():
             "oracle_select_topk_batch": [i, i, i64, i64, vp, i64, i64, vp, i64, vp],
             "oracle_sparse_decode_batch": [i, i, i, i, i64, vp, vp, vp, vp, i64, vp, d, vp],
             "oracle_window_decode_batch": [i, i, i, i, i64, i64, vp, vp, vp, d, d, vp],
+            "oracle_skip_stats": [i64, vp, i64, vp, vp],
+            "oracle_skip_stats_batch": [i, i, i64, i64, vp, i64, vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -166,6 +168,18 @@ def select_topk_batch(sigma32, n, topk=1024, recent=128):
     _ok(_load().oracle_select_topk_batch(B, Hkv, n, ncap, _p(s), topk, recent, _p(idx), stride,
                                          _p(cnt)), "select_topk_batch")
     return idx, cnt
+
+
+def skip_stats_batch(sigma32, n, chunk=8):
+    """All units: (keys_needed [B, Hkv], chunks_needed [B, Hkv]) -- keys j < n with
+    sigma > 0, and chunks of `chunk` keys holding at least one of them."""
+    s = np.ascontiguousarray(sigma32, dtype=np.float32)
+    B, Hkv, ncap = s.shape
+    keys = np.zeros((B, Hkv), dtype=np.int64)
+    chunks = np.zeros((B, Hkv), dtype=np.int64)
+    _ok(_load().oracle_skip_stats_batch(B, Hkv, n, ncap, _p(s), chunk, _p(keys), _p(chunks)),
+        "skip_stats_batch")
+    return keys, chunks
 
 
 def sparse_decode_batch(q, K, V, idx, count, tau=None):

@@ -257,6 +257,41 @@ int oracle_full_decode_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t n
   return err ? -1 : 0;
 }
 
+/*
+ * V-read accounting of one unit ("The Architecture of Embla 1", section "Skipping V": a
+ * value row is needed only when some head of the group gives its key a weight above zero,
+ * i.e. sigma_j > 0; the page's kernel checks keys in groups of 8).
+ *   keys_needed   : keys j < n with sigma32[j] > 0
+ *   chunks_needed : chunks [c*chunk, min(n, (c+1)*chunk)) holding at least one such key
+ */
+int oracle_skip_stats(int64_t n, const float *sigma32, int64_t chunk, int64_t *keys_needed,
+                      int64_t *chunks_needed) {
+  if (n < 0 || chunk < 1 || !keys_needed || !chunks_needed) return -1;
+  int64_t keys = 0, chunks = 0;
+  for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+    int any = 0;
+    for (int64_t j = c0; j < n && j < c0 + chunk; ++j) {
+      if (sigma32[j] > 0.0f) {
+        ++keys;
+        any = 1;
+      }
+    }
+    chunks += any;
+  }
+  *keys_needed = keys;
+  *chunks_needed = chunks;
+  return 0;
+}
+
+int oracle_skip_stats_batch(int B, int Hkv, int64_t n, int64_t ncap, const float *sigma32,
+                            int64_t chunk, int64_t *keys_needed, int64_t *chunks_needed) {
+  int err = 0;
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u)
+    err |= oracle_skip_stats(n, sigma32 + (size_t)u * ncap, chunk, keys_needed + u,
+                             chunks_needed + u) != 0;
+  return err ? -1 : 0;
+}
+
 int oracle_select_topk_batch(int B, int Hkv, int64_t n, int64_t ncap, const float *sigma32,
                              int64_t topk, int64_t recent, int32_t *idx, int64_t idx_stride,
                              int64_t *count) {

@@ -92,6 +92,7 @@ def library() -> ctypes.CDLL:
             "embla_window_decode_workspace_size": (sz, [P, i32]),
             "embla_window_decode": (ctypes.c_int, [P, vp, vp, vp, i32, i64, f32, f32, vp, vp, sz,
                                                    vp]),
+            "embla_skip_stats": (ctypes.c_int, [P, vp, i32, vp, vp, vp]),
             "embla_device_check": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
                                                   vp]),
         }
@@ -245,6 +246,18 @@ def embla_window_decode(shape: Shape, q, k_win, v_win, pos: int, out, window: in
     tau = D ** -0.5 if tau is None else tau
     _call("embla_window_decode", ctypes.byref(shape.c()), _ptr(q), _ptr(k_win), _ptr(v_win),
           window, pos, rope_base, tau, _ptr(out), None, 0, _stream(stream))
+
+
+def embla_skip_stats(shape: Shape, sel_scores, keys_needed, chunks_needed, chunk: int = 8,
+                     stream=None):
+    """Per unit: keys whose V row is needed (sigma > 0) and chunks of `chunk` keys that
+    hold at least one of them."""
+    B, Hkv, ncap = shape.batch, shape.n_kv_heads, shape.cache_stride
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores")
+    _check(keys_needed, torch.int32, (B, Hkv), "keys_needed")
+    _check(chunks_needed, torch.int32, (B, Hkv), "chunks_needed")
+    _call("embla_skip_stats", ctypes.byref(shape.c()), _ptr(sel_scores), chunk, _ptr(keys_needed),
+          _ptr(chunks_needed), _stream(stream))
 
 
 def embla_device_check(clear: bool = True, stream=None) -> int:

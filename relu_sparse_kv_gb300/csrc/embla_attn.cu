@@ -315,6 +315,22 @@ embla_status embla_window_decode(const embla_shape *shape, const void *q, const 
                                           out, static_cast<cudaStream_t>(stream)));
 }
 
+embla_status embla_skip_stats(const embla_shape *shape, const float *sel_scores, int32_t chunk,
+                              int32_t *keys_needed, int32_t *chunks_needed, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  if (chunk < 1 || chunk > 1024 || (chunk & (chunk - 1)) != 0) return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!sel_scores || !keys_needed || !chunks_needed) return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(sel_scores) || !aligned16(keys_needed) || !aligned16(chunks_needed))
+    return EMBLA_ERR_INVALID_ARG;
+  return cuda_status(launch_skip_stats(sel_scores, units, shape->ctx_len, shape->cache_stride,
+                                       chunk, keys_needed, chunks_needed,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 embla_status embla_device_check(uint32_t *flags, int clear, void *stream) {
   uint32_t *d = flags_ptr();
   if (!d || !flags) return d ? EMBLA_ERR_INVALID_ARG : EMBLA_ERR_CUDA;

@@ -90,6 +90,10 @@ cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, cons
                                  float *out, void *workspace, uint32_t *flags, int sm_count,
                                  cudaStream_t stream);
 
+cudaError_t launch_skip_stats(const float *sel_scores, int64_t units, int64_t n, int64_t ncap,
+                              int chunk, int32_t *keys_needed, int32_t *chunks_needed,
+                              cudaStream_t stream);
+
 cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const void *v_win,
                                  int64_t units, int window, int64_t pos, float rope_base,
                                  float tau, float *out, cudaStream_t stream);

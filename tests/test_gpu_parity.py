@@ -184,6 +184,37 @@ def test_select_long_and_unaligned_rows(n, ncap):
     _select_case(sig, n, ncap)
 
 
+@pytest.mark.parametrize("chunk", [1, 2, 8, 32, 64, 1024])
+@pytest.mark.parametrize("n,ncap", [(5000, 5000), (4099, 4103), (33, 40), (1, 1)])
+def test_skip_stats(chunk, n, ncap):
+    rng = np.random.default_rng(n + chunk)
+    B, Hkv = 3, 4
+    sig = rng.standard_normal((B, Hkv, ncap)).astype(np.float32)
+    sig[0, 0] = -1.0                                      # nothing needed
+    sig[1, 1] = np.where(rng.random(ncap) < 0.01, 1.0, -1.0)
+    sig[2, 3, n:] = 5.0                                    # past the context: not counted
+    shape = E.Shape(B, 16, Hkv, D, n, ncap)
+    keys = torch.full((B, Hkv), -1, dtype=torch.int32, device="cuda")
+    chunks = torch.full((B, Hkv), -1, dtype=torch.int32, device="cuda")
+    E.embla_skip_stats(shape, torch.from_numpy(sig).cuda(), keys, chunks, chunk=chunk)
+    torch.cuda.synchronize()
+    rk, rc = oracle.skip_stats_batch(sig, n, chunk)
+    assert np.array_equal(keys.cpu().numpy(), rk)
+    assert np.array_equal(chunks.cpu().numpy(), rc)
+
+
+def test_skip_stats_of_a_full_layer_match_its_survivors():
+    fl = _layer(2, 16, 4, 20000, pattern="runs", frac=0.05, seed=19, sparse=())
+    run = FullRun(fl, with_select=False)
+    keys = torch.empty(2, 4, dtype=torch.int32, device="cuda")
+    chunks = torch.empty(2, 4, dtype=torch.int32, device="cuda")
+    E.embla_skip_stats(run.shape, run.sel, keys, chunks, chunk=8)
+    torch.cuda.synchronize()
+    assert np.array_equal(keys.cpu().numpy(), fl.n_pos)
+    _, rc = oracle.skip_stats_batch(run.sel.cpu().numpy(), fl.n, 8)
+    assert np.array_equal(chunks.cpu().numpy(), rc)
+
+
 @pytest.mark.parametrize("pos", [0, 5, 126, 127, 128, 1000, 65535])
 @pytest.mark.parametrize("G", [4, 8])
 def test_window_decode(pos, G):

@@ -466,3 +466,57 @@ def test_window_rotation_frequencies_closed_form():
     for h, z in enumerate((z0, z1)):
         p = np.exp(z - z.max())
         np.testing.assert_allclose(out[h], p / p.sum(), rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------- V-read accounting
+# "Skipping V": a value row is needed exactly when sigma_j > 0; the page's kernel decides it
+# for groups of 8 keys.  The accounting counts needed keys and needed chunks.
+
+def test_skip_stats_degenerate_chunk_sizes():
+    rng = np.random.default_rng(40)
+    sig = rng.standard_normal((2, 3, 1000)).astype(np.float32)
+    keys1, chunks1 = oracle.skip_stats_batch(sig, 1000, 1)
+    assert np.array_equal(keys1, chunks1)                       # a chunk of one key is the key
+    assert np.array_equal(keys1, (sig > 0).sum(-1))
+    keysn, chunksn = oracle.skip_stats_batch(sig, 1000, 4096)  # one chunk holds everything
+    assert np.array_equal(chunksn, (keysn > 0).astype(np.int64))
+    zero = np.full((1, 1, 64), -1.0, dtype=np.float32)
+    assert oracle.skip_stats_batch(zero, 64, 8) == (np.zeros((1, 1)), np.zeros((1, 1)))
+
+
+@pytest.mark.parametrize("p,chunk", [(8, 8), (16, 8), (40, 8), (2, 8), (4, 16), (1, 8)])
+def test_skip_stats_periodic_survivors(p, chunk):
+    # survivors at every p-th key: when p >= chunk each one has a chunk of its own; when p
+    # divides the chunk every chunk holds chunk / p of them
+    n = 4096
+    sig = np.where(np.arange(n) % p == 0, 1.0, -1.0).astype(np.float32)[None, None]
+    keys, chunks = oracle.skip_stats_batch(sig, n, chunk)
+    multiples = (n + p - 1) // p
+    assert keys[0, 0] == multiples
+    if p >= chunk:
+        assert chunks[0, 0] == multiples
+    else:
+        assert chunk % p == 0 and chunks[0, 0] == n // chunk
+
+
+@pytest.mark.parametrize("f", [0.01, 0.05, 0.2])
+def test_skip_stats_independent_survivors_binomial(f):
+    # keys survive independently with probability f: a chunk of 8 is needed with
+    # probability 1 - (1 - f)^8, independently of the others
+    n, units = 1 << 16, 8
+    rng = np.random.default_rng(int(f * 1000))
+    sig = np.where(rng.random((1, units, n)) < f, 1.0, -1.0).astype(np.float32)
+    _, chunks = oracle.skip_stats_batch(sig, n, 8)
+    m = units * n // 8
+    pr = 1.0 - (1.0 - f) ** 8
+    mean, sd = m * pr, math.sqrt(m * pr * (1 - pr))
+    assert abs(chunks.sum() - mean) < 5 * sd
+
+
+def test_skip_stats_keys_needed_equals_survivor_count():
+    fl = gen.make_full_layer(seed=41, layer=0, B=2, Hq=16, Hkv=4, D=128, n=3000,
+                             pattern="subset", frac=0.1)
+    _, sig, n_surv = oracle.full_decode_batch(fl.q, fl.K, fl.V, fl.n)
+    keys, chunks = oracle.skip_stats_batch(sig, fl.n, 8)
+    assert np.array_equal(keys, n_surv)
+    assert (chunks * 8 >= keys).all() and (chunks <= keys).all()
