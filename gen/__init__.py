@@ -59,6 +59,14 @@ def _load():
         lib.gen_signed_keys.restype = i64
         lib.gen_signed_keys.argtypes = [u64, ctypes.c_int, ctypes.c_int, i64, vp, vp, i64, i64,
                                         ctypes.c_double, ctypes.c_double, ctypes.c_int, i64, vp]
+        lib.gen_signed_keys_e4m3.restype = i64
+        lib.gen_signed_keys_e4m3.argtypes = [u64, ctypes.c_int, ctypes.c_int, i64, vp, vp, i64,
+                                             i64, ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                                             i64, vp, vp]
+        lib.gen_normal_e4m3.restype = None
+        lib.gen_normal_e4m3.argtypes = [u64, i64, ctypes.c_int, vp, vp]
+        lib.gen_e4m3_encode.restype = None
+        lib.gen_e4m3_encode.argtypes = [vp, i64, vp]
         _lib = lib
     return _lib
 
@@ -113,6 +121,40 @@ def signed_keys(strm: int, q_group: np.ndarray, t: np.ndarray, n_cand: int, topk
     return K
 
 
+def signed_keys_e4m3(strm: int, q_group: np.ndarray, t: np.ndarray, n_cand: int,
+                     topk: int = 1024, margin: float = 2e-3, gap: float = 2e-3,
+                     max_attempts: int = 64, max_gap_iters: int = 100000):
+    """signed_keys stored as 8-bit E4M3 codes with one float32 scale per key: (K8, Ks).
+    The signs, margins and the top-k gap hold for the decoded keys scale * code."""
+    q_group = np.ascontiguousarray(q_group, dtype=np.uint16)
+    G, D = q_group.shape
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    n = t.shape[0]
+    K8 = np.empty((n, D), dtype=np.uint8)
+    Ks = np.empty(n, dtype=np.float32)
+    r = _load().gen_signed_keys_e4m3(strm, G, D, n, _ptr(q_group), _ptr(t), n_cand, topk, margin,
+                                     gap, max_attempts, max_gap_iters, _ptr(K8), _ptr(Ks))
+    if r < 0:
+        raise RuntimeError(f"gen_signed_keys_e4m3 failed with code {r}")
+    return K8, Ks
+
+
+def normal_e4m3(strm: int, rows: int, D: int):
+    """rows x D standard normals in 8-bit E4M3 codes with one scale per row: (codes, scales)."""
+    out = np.empty((rows, D), dtype=np.uint8)
+    sc = np.empty(rows, dtype=np.float32)
+    _load().gen_normal_e4m3(strm, rows, D, _ptr(out), _ptr(sc))
+    return out, sc
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round to 8-bit E4M3 codes (nearest, ties to even; saturating at 448)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().gen_e4m3_encode(_ptr(x), x.size, _ptr(out))
+    return out
+
+
 def bf16_to_f32(a: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32."""
     return (a.astype(np.uint32) << 16).view(np.float32)
@@ -140,6 +182,9 @@ class FullLayer:
     n: int
     sparse_q: list = field(default_factory=list)   # per sparse layer: [B, Hq, D] bf16 bits
     sparse_layers: list = field(default_factory=list)
+    kv: str = "bf16"       # "e4m3": K and V hold 8-bit codes, Ks and Vs their scales
+    Ks: np.ndarray | None = None  # [B, Hkv, n_cap] float32
+    Vs: np.ndarray | None = None
 
     @property
     def n_pos(self) -> np.ndarray:
@@ -158,17 +203,25 @@ class WindowLayer:
 def make_full_layer(seed: int, layer: int, B: int, Hq: int, Hkv: int, D: int, n: int,
                     pattern: str, frac, run_len: int = 64, n_cap: int | None = None,
                     topk: int = 1024, recent: int = 128, margin: float = 2e-3,
-                    gap: float = 2e-3, sparse_layers=()) -> FullLayer:
+                    gap: float = 2e-3, sparse_layers=(), kv: str = "bf16") -> FullLayer:
     """One full layer's query and sign-controlled cache (plus sparse-layer queries).
 
-    frac may be a scalar or a per-sequence list (cycled over the batch).
+    frac may be a scalar or a per-sequence list (cycled over the batch).  kv "e4m3"
+    stores K and V as 8-bit codes with a float32 scale per (token, KV head).
     """
     n_cap = n if n_cap is None else n_cap
-    assert n_cap >= n and Hq % Hkv == 0
+    assert n_cap >= n and Hq % Hkv == 0 and kv in ("bf16", "e4m3")
     G = Hq // Hkv
     q = normal_bf16(stream(seed, ROLE_Q_FULL, layer), (B, Hq, D))
-    K = np.full((B, Hkv, n_cap, D), BF16_NAN, dtype=np.uint16)
-    V = np.full((B, Hkv, n_cap, D), BF16_NAN, dtype=np.uint16)
+    if kv == "e4m3":
+        K = np.full((B, Hkv, n_cap, D), 0x7F, dtype=np.uint8)
+        V = np.full((B, Hkv, n_cap, D), 0x7F, dtype=np.uint8)
+        Ks = np.full((B, Hkv, n_cap), np.nan, dtype=np.float32)
+        Vs = np.full((B, Hkv, n_cap), np.nan, dtype=np.float32)
+    else:
+        K = np.full((B, Hkv, n_cap, D), BF16_NAN, dtype=np.uint16)
+        V = np.full((B, Hkv, n_cap, D), BF16_NAN, dtype=np.uint16)
+        Ks = Vs = None
     T = np.empty((B, Hkv, n), dtype=np.int8)
     fr = list(frac) if isinstance(frac, (list, tuple)) else [frac]
     n_cand = n - recent if n > topk + recent else 0
@@ -176,10 +229,17 @@ def make_full_layer(seed: int, layer: int, B: int, Hq: int, Hkv: int, D: int, n:
         f_b = fr[b % len(fr)]
         for g in range(Hkv):
             T[b, g] = targets(stream(seed, ROLE_T, layer, b, g), n, pattern, f_b, run_len)
-            K[b, g, :n] = signed_keys(stream(seed, ROLE_K, layer, b, g), q[b, g * G:(g + 1) * G],
-                                      T[b, g], n_cand, topk, margin, gap)
-            V[b, g, :n] = normal_bf16(stream(seed, ROLE_V, layer, b, g), (n, D))
-    fl = FullLayer(layer=layer, q=q, K=K, V=V, targets=T, n=n)
+            if kv == "e4m3":
+                K[b, g, :n], Ks[b, g, :n] = signed_keys_e4m3(
+                    stream(seed, ROLE_K, layer, b, g), q[b, g * G:(g + 1) * G], T[b, g], n_cand,
+                    topk, margin, gap)
+                V[b, g, :n], Vs[b, g, :n] = normal_e4m3(stream(seed, ROLE_V, layer, b, g), n, D)
+            else:
+                K[b, g, :n] = signed_keys(stream(seed, ROLE_K, layer, b, g),
+                                          q[b, g * G:(g + 1) * G], T[b, g], n_cand, topk,
+                                          margin, gap)
+                V[b, g, :n] = normal_bf16(stream(seed, ROLE_V, layer, b, g), (n, D))
+    fl = FullLayer(layer=layer, q=q, K=K, V=V, targets=T, n=n, kv=kv, Ks=Ks, Vs=Vs)
     for sl in sparse_layers:
         fl.sparse_layers.append(sl)
         fl.sparse_q.append(normal_bf16(stream(seed, ROLE_Q_SPARSE, sl), (B, Hq, D)))
@@ -218,6 +278,9 @@ CONFIGS = {
             frac=[0.5, 0.2, 0.05, 0.01], sparse=(1,)),
     5: dict(name="embla-attention-step-b16-n64k", B=16, n=65536, pattern="subset", frac=0.05,
             sparse=None),
+    # Embla 1's own head shape: 8 query heads per KV head, K and V in 8 bits
+    6: dict(name="gqa8-e4m3-full+select+3sparse-b8-n32k-f0.05", B=8, n=32768, pattern="subset",
+            frac=0.05, sparse=(1, 2, 3), Hq=16, Hkv=2, kv="e4m3"),
 }
 HQ, HKV, HEAD_DIM, WINDOW, ROPE_BASE = 16, 4, 128, 128, 10000.0
 
@@ -233,8 +296,9 @@ def config_full_layers(cfg: int, seed: int = 0, B: int | None = None, n: int | N
             yield make_full_layer(seed, layer, B, HQ, HKV, HEAD_DIM, n, c["pattern"], c["frac"],
                                   n_cap=n_cap, sparse_layers=EMBLA_SPARSE_OF[layer])
     else:
-        yield make_full_layer(seed, 0, B, HQ, HKV, HEAD_DIM, n, c["pattern"], c["frac"],
-                              n_cap=n_cap, sparse_layers=c["sparse"])
+        yield make_full_layer(seed, 0, B, c.get("Hq", HQ), c.get("Hkv", HKV), HEAD_DIM, n,
+                              c["pattern"], c["frac"], n_cap=n_cap, sparse_layers=c["sparse"],
+                              kv=c.get("kv", "bf16"))
 
 
 def config_window_layers(cfg: int, seed: int = 0, B: int | None = None, n: int | None = None):

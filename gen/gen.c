@@ -88,6 +88,62 @@ void gen_normal_bf16(uint64_t stream, int64_t start, int64_t count, uint16_t *ou
     out[i] = f32_to_bf16((float)normal_at(stream, (uint64_t)(start + i)));
 }
 
+/* 8-bit floats, E4M3 without infinities: sign, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent field 0 is subnormal (m * 2^-9); S.1111.111 is NaN; the largest finite
+ * magnitude is 448.  Rounding to nearest, ties to even; magnitudes past 448 saturate. */
+static uint8_t f64_to_e4m3(double x) {
+  const uint8_t sign = x < 0.0 ? 0x80 : 0x00;
+  const double a = fabs(x);
+  if (a != a) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    const double m = nearbyint(a * 512.0); /* units of 2^-9; 8 carries into the first normal */
+    return sign | (uint8_t)m;
+  }
+  int e;
+  frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int E = e - 1 + 7;
+  double r = nearbyint((a / ldexp(1.0, e - 1) - 1.0) * 8.0);
+  if (r >= 8.0) { r = 0.0; E += 1; }
+  if (E > 15 || (E == 15 && r > 6.0)) return sign | 0x7E;
+  return sign | (uint8_t)(E << 3) | (uint8_t)r;
+}
+
+static double e4m3_to_f64(uint8_t b) {
+  const int E = (b >> 3) & 15, m = b & 7;
+  if (E == 15 && m == 7) return NAN;
+  const double v = E == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, E - 7);
+  return (b & 0x80) ? -v : v;
+}
+
+/* One row to 8 bits with its own scale (the largest magnitude maps to 448); deq, when
+ * given, receives scale * value as the reader will see it. */
+static void quantize_row_e4m3(const double *v, int D, uint8_t *out, float *scale, double *deq) {
+  double amax = 0.0;
+  for (int d = 0; d < D; ++d) if (fabs(v[d]) > amax) amax = fabs(v[d]);
+  const float sc = amax > 0.0 ? (float)(amax / 448.0) : 1.0f;
+  for (int d = 0; d < D; ++d) {
+    out[d] = f64_to_e4m3(v[d] / (double)sc);
+    if (deq) deq[d] = (double)sc * e4m3_to_f64(out[d]);
+  }
+  *scale = sc;
+}
+
+/* Rows of standard normals (row r uses draws r*D .. r*D+D-1 of the stream) in 8 bits. */
+void gen_normal_e4m3(uint64_t stream, int64_t rows, int D, uint8_t *out, float *scale) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    double v[1024];
+    for (int d = 0; d < D && d < 1024; ++d) v[d] = normal_at(stream, (uint64_t)(r * D + d));
+    quantize_row_e4m3(v, D, out + r * D, scale + r, NULL);
+  }
+}
+
+/* Element codes to values (for tests of the encoder). */
+void gen_e4m3_encode(const double *x, int64_t n, uint8_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f64_to_e4m3(x[i]);
+}
+
 /*
  * Target signs for n keys (t[j] = +1 means every head of the group scores
  * key j above zero).  kind 0: independent, P(+1) = frac.  kind 1: exactly
@@ -177,13 +233,36 @@ typedef struct {
   double minv[MAXG * MAXG];
   double margin;
   uint64_t stream;
+  int e4m3;        /* keys stored in 8 bits with a scale per row, else bf16 */
+  uint16_t *Kb;    /* bf16 keys (row stride D) */
+  uint8_t *K8;     /* 8-bit keys (row stride D) */
+  float *Ks;       /* their scales */
 } signer;
 
-/* max_h D*cos(q_h, k) over the group, in double, from the bf16 key. */
-static double proxy_max(const signer *s, const uint16_t *kb) {
+/* Key j as the reader sees it (decoded), into kd. */
+static void key_values(const signer *s, int64_t j, double *kd) {
+  if (s->e4m3) {
+    for (int d = 0; d < s->D; ++d) kd[d] = (double)s->Ks[j] * e4m3_to_f64(s->K8[j * s->D + d]);
+  } else {
+    for (int d = 0; d < s->D; ++d) kd[d] = bf16_to_f64(s->Kb[j * s->D + d]);
+  }
+}
+
+/* Store key j from its exact values. */
+static void store_key(const signer *s, int64_t j, const double *v) {
+  if (s->e4m3) {
+    quantize_row_e4m3(v, s->D, s->K8 + j * s->D, s->Ks + j, NULL);
+  } else {
+    for (int d = 0; d < s->D; ++d) s->Kb[j * s->D + d] = f32_to_bf16((float)v[d]);
+  }
+}
+
+/* max_h D*cos(q_h, k) over the group, in double, from key j as stored. */
+static double proxy_max(const signer *s, int64_t j) {
   double kk = 0.0;
   double kd[MAXD];
-  for (int d = 0; d < s->D; ++d) { kd[d] = bf16_to_f64(kb[d]); kk += kd[d] * kd[d]; }
+  key_values(s, j, kd);
+  for (int d = 0; d < s->D; ++d) kk += kd[d] * kd[d];
   double kn = sqrt(kk), best = -INFINITY;
   for (int h = 0; h < s->G; ++h) {
     double dot = 0.0;
@@ -195,7 +274,7 @@ static double proxy_max(const signer *s, const uint16_t *kb) {
 }
 
 /* Draw key j (attempt a) with target sign t; returns 1 when it meets the margin. */
-static int draw_key(const signer *s, int64_t j, int64_t a, int t, uint16_t *kb) {
+static int draw_key(const signer *s, int64_t j, int64_t a, int t) {
   const int G = s->G, D = s->D;
   uint64_t st = gen_substream(s->stream, (uint64_t)j, (uint64_t)a);
   double z[MAXD], c[MAXG], want[MAXG], delta[MAXG];
@@ -215,14 +294,16 @@ static int draw_key(const signer *s, int64_t j, int64_t a, int t, uint16_t *kb) 
     for (int i = 0; i < G; ++i) acc += s->minv[h * G + i] * want[i];
     delta[h] = acc;
   }
+  double v[MAXD];
   for (int d = 0; d < D; ++d) {
-    double v = z[d];
-    for (int h = 0; h < G; ++h) v += delta[h] * s->q[h * D + d];
-    kb[d] = f32_to_bf16((float)v);
+    v[d] = z[d];
+    for (int h = 0; h < G; ++h) v[d] += delta[h] * s->q[h * D + d];
   }
-  /* check every head's sign and margin on the rounded key */
+  store_key(s, j, v);
+  /* check every head's sign and margin on the stored (rounded) key */
   double kd[MAXD], kk = 0.0;
-  for (int d = 0; d < D; ++d) { kd[d] = bf16_to_f64(kb[d]); kk += kd[d] * kd[d]; }
+  key_values(s, j, kd);
+  for (int d = 0; d < D; ++d) kk += kd[d] * kd[d];
   double kn = sqrt(kk);
   if (!(kn > 0.0)) return 0;
   for (int h = 0; h < G; ++h) {
@@ -268,13 +349,15 @@ static void select_desc(double *v, int64_t *id, int64_t n, int64_t k) {
  *   -1 bad arguments, -2 singular query group, -3 margin not met after
  *   max_attempts draws, -4 gap not met after max_gap_iters redraws.
  */
-int64_t gen_signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t *q,
-                        const int8_t *t, int64_t n_cand, int64_t topk, double margin,
-                        double gap, int max_attempts, int64_t max_gap_iters, uint16_t *K) {
+static int64_t signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t *q,
+                           const int8_t *t, int64_t n_cand, int64_t topk, double margin,
+                           double gap, int max_attempts, int64_t max_gap_iters, uint16_t *Kb,
+                           uint8_t *K8, float *Ks) {
   if (G < 1 || G > MAXG || D < 1 || D > MAXD || n < 0 || n_cand > n) return -1;
   signer *s = (signer *)malloc(sizeof(signer));
   if (!s) return -1;
   s->G = G; s->D = D; s->margin = margin; s->stream = stream;
+  s->e4m3 = K8 != NULL; s->Kb = Kb; s->K8 = K8; s->Ks = Ks;
   for (int i = 0; i < G * D; ++i) s->q[i] = bf16_to_f64(q[i]);
   double m[MAXG * MAXG];
   for (int h = 0; h < G; ++h) {
@@ -295,7 +378,7 @@ int64_t gen_signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t
 #pragma omp parallel for schedule(dynamic, 256) reduction(+ : redraws) reduction(| : failed)
   for (int64_t j = 0; j < n; ++j) {
     int64_t a = 0;
-    while (!draw_key(s, j, a, t[j] > 0 ? 1 : -1, K + j * D)) {
+    while (!draw_key(s, j, a, t[j] > 0 ? 1 : -1)) {
       if (++a >= max_attempts) { failed = 1; break; }
     }
     attempt[j] = a;
@@ -308,7 +391,7 @@ int64_t gen_signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t
     double *w = (double *)malloc(sizeof(double) * (size_t)n_cand);
     int64_t *id = (int64_t *)malloc(sizeof(int64_t) * (size_t)n_cand);
 #pragma omp parallel for schedule(static)
-    for (int64_t j = 0; j < n_cand; ++j) v[j] = proxy_max(s, K + j * D);
+    for (int64_t j = 0; j < n_cand; ++j) v[j] = proxy_max(s, j);
     int64_t iters = 0;
     for (;;) {
       for (int64_t j = 0; j < n_cand; ++j) { w[j] = v[j]; id[j] = j; }
@@ -322,11 +405,11 @@ int64_t gen_signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t
       int64_t a = attempt[j];
       do {
         if (++a >= attempt[j] + max_attempts) { failed = 1; break; }
-      } while (!draw_key(s, j, a, t[j] > 0 ? 1 : -1, K + j * D));
+      } while (!draw_key(s, j, a, t[j] > 0 ? 1 : -1));
       if (failed) break;
       redraws += a - attempt[j];
       attempt[j] = a;
-      v[j] = proxy_max(s, K + j * D);
+      v[j] = proxy_max(s, j);
     }
     free(v); free(w); free(id);
     if (failed) { free(attempt); free(s); return -4; }
@@ -334,4 +417,21 @@ int64_t gen_signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t
   free(attempt);
   free(s);
   return redraws;
+}
+
+int64_t gen_signed_keys(uint64_t stream, int G, int D, int64_t n, const uint16_t *q,
+                        const int8_t *t, int64_t n_cand, int64_t topk, double margin,
+                        double gap, int max_attempts, int64_t max_gap_iters, uint16_t *K) {
+  return signed_keys(stream, G, D, n, q, t, n_cand, topk, margin, gap, max_attempts,
+                     max_gap_iters, K, NULL, NULL);
+}
+
+/* The same keys stored in 8 bits (E4M3) with one scale per key; signs, margins and the
+ * top-k gap hold for the decoded keys. */
+int64_t gen_signed_keys_e4m3(uint64_t stream, int G, int D, int64_t n, const uint16_t *q,
+                             const int8_t *t, int64_t n_cand, int64_t topk, double margin,
+                             double gap, int max_attempts, int64_t max_gap_iters, uint8_t *K8,
+                             float *Ks) {
+  return signed_keys(stream, G, D, n, q, t, n_cand, topk, margin, gap, max_attempts,
+                     max_gap_iters, NULL, K8, Ks);
 }

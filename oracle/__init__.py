@@ -170,6 +170,28 @@ def select_topk_batch(sigma32, n, topk=1024, recent=128):
     return idx, cnt
 
 
+def e4m3_table() -> np.ndarray:
+    """The 256 values of an 8-bit E4M3 code (no infinities): sign, 4 exponent bits with bias
+    7, 3 mantissa bits; exponent field 0 is subnormal, m * 2^-9; S.1111.111 is NaN."""
+    v = np.empty(256, dtype=np.float64)
+    for b in range(256):
+        e, m = (b >> 3) & 15, b & 7
+        if e == 15 and m == 7:
+            x = np.nan
+        elif e == 0:
+            x = m * 2.0 ** -9
+        else:
+            x = (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        v[b] = -x if b & 0x80 else x
+    return v
+
+
+def dequant_e4m3(codes, scales) -> np.ndarray:
+    """float64 values scale * code of an 8-bit cache [..., n, D] with scales [..., n]."""
+    t = e4m3_table()
+    return t[np.asarray(codes, dtype=np.uint8)] * np.asarray(scales, dtype=np.float64)[..., None]
+
+
 def skip_stats_batch(sigma32, n, chunk=8):
     """All units: (keys_needed [B, Hkv], chunks_needed [B, Hkv]) -- keys j < n with
     sigma > 0, and chunks of `chunk` keys holding at least one of them."""

@@ -520,3 +520,54 @@ def test_skip_stats_keys_needed_equals_survivor_count():
     keys, chunks = oracle.skip_stats_batch(sig, fl.n, 8)
     assert np.array_equal(keys, n_surv)
     assert (chunks * 8 >= keys).all() and (chunks <= keys).all()
+
+
+# ----------------------------------------------------------------------------- 8-bit caches
+# E4M3 as the OCP 8-bit float format defines it: largest finite 448 (S.1111.110), smallest
+# normal 2^-6, smallest subnormal 2^-9, no infinities, S.1111.111 NaN.
+
+def test_e4m3_table_fixed_points():
+    t = oracle.e4m3_table()
+    assert t[0x7E] == 448.0 and t[0xFE] == -448.0
+    assert t[0x08] == 2.0 ** -6 and t[0x01] == 2.0 ** -9 and t[0x07] == 7 * 2.0 ** -9
+    assert t[0x38] == 1.0 and t[0xB8] == -1.0 and t[0x00] == 0.0 and t[0x80] == 0.0
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    pos = t[:0x7F]
+    assert (np.diff(pos) > 0).all()                      # codes 0..126 increase strictly
+    assert np.array_equal(t[0x80:0xFF], -pos)            # negatives mirror the positives
+
+
+def test_e4m3_encoder_rounds_to_nearest_even():
+    # the generator's encoder against this decoder: the nearest code, ties to the even one
+    t = oracle.e4m3_table()
+    grid = t[:0x7F]
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(4000) * 10, (grid[1:] + grid[:-1]) / 2,
+                        rng.uniform(0, 2.0 ** -6, 500)])
+    codes = gen.e4m3_encode(x)
+    dec = t[codes]
+    a = np.minimum(np.abs(x), 448.0)
+    # distance to the chosen code is the smallest distance to any code
+    best = np.abs(grid[None, :] - a[:, None]).min(axis=1)
+    assert np.allclose(np.abs(np.abs(dec) - a), best, atol=0, rtol=0)
+    ties = np.isclose(np.abs(grid[None, :] - a[:, None]), best[:, None], rtol=0, atol=0).sum(1) == 2
+    assert (codes[ties] % 2 == 0).all()                  # ties go to the even mantissa
+    assert (gen.e4m3_encode(np.array([1e9, -1e9])) == [0x7E, 0xFE]).all()
+
+
+def test_e4m3_full_layer_matches_bf16_path_on_the_decoded_cache():
+    # the full layer reads the decoded cache: same survivors as the construction targets,
+    # and the oracle on decoded values is the oracle of the bf16 path on those values
+    fl = gen.make_full_layer(seed=42, layer=0, B=1, Hq=16, Hkv=2, D=128, n=2000,
+                             pattern="subset", frac=0.1, kv="e4m3")
+    Kd = oracle.dequant_e4m3(fl.K, fl.Ks)
+    Vd = oracle.dequant_e4m3(fl.V, fl.Vs)
+    out, sig, ns = oracle.full_decode_batch(fl.q, Kd, Vd, fl.n)
+    assert np.array_equal(ns, fl.n_pos)
+    assert np.isfinite(out).all()
+    # scaling a key row (its scale) does not change the normalised score
+    Ks2 = fl.Ks.copy(); Ks2[0, 0, :fl.n] *= 3.0
+    _, sig2, _ = oracle.full_decode_batch(fl.q, oracle.dequant_e4m3(fl.K, Ks2), Vd, fl.n,
+                                          eps=0.0)
+    _, sig0, _ = oracle.full_decode_batch(fl.q, Kd, Vd, fl.n, eps=0.0)
+    assert np.allclose(sig2[0, 0, :fl.n], sig0[0, 0, :fl.n], rtol=1e-6, atol=1e-6)
