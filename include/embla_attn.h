@@ -99,6 +99,31 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Full (ReLU^2) layer decode over 8-bit caches — the same operation as
+ * embla_full_decode, on K and V kept in 8-bit precision ("KV bridge, KV reuse,
+ * and prefill": the full caches grow by 2.6 KB per token at 8 bits).  The page
+ * does not name the 8-bit format; this call takes OCP FP8 E4M3 codes (bias 7,
+ * no infinities, S.1111.111 is NaN, largest finite 448) with one fp32 scale per
+ * (token, KV head): row j of unit u stands for scale[u][j] * decode(code[u][j][:]).
+ * Results are those of embla_full_decode on those decoded rows.
+ *   k_codes, v_codes   uint8 [B, Hkv, cache_stride, D] E4M3 codes
+ *   k_scales, v_scales fp32 [B, Hkv, cache_stride]; cache_stride % 4 == 0
+ *   every other argument, the workspace size (embla_full_decode_workspace_size)
+ *   and every result as for embla_full_decode.
+ * The query enters the tensor cores as three E4M3 terms per element (q = 2^e
+ * (t1 + t2/16 + t3/256), 2^e a power of two per head); the sum reproduces every
+ * query element of magnitude at least 2^-14 times its head's largest exactly,
+ * and every other one to within 2^-25 times that largest.  Rows j >= n are read (they share 128-key tiles with
+ * rows < n) but nothing they hold reaches a result.
+ */
+embla_status embla_full_decode_e4m3(const embla_shape *shape, const void *q,
+                                    const uint8_t *k_codes, const float *k_scales,
+                                    const uint8_t *v_codes, const float *v_scales, float alpha,
+                                    float c, float eps, float *out, int32_t *n_surv,
+                                    float *sel_scores, uint32_t *sel_hist, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
  * Full (ReLU^2) layer decode on library-owned scratch.  The Embla pages have
  * no counterpart to this call: it computes exactly what embla_full_decode
  * computes, with the same arguments and results, but takes no workspace.  It
@@ -169,6 +194,24 @@ embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const 
                                  const void *v_cache, const int32_t *idx, int32_t idx_stride,
                                  const int32_t *count, float tau, float *out, void *workspace,
                                  size_t workspace_bytes, void *stream);
+
+/*
+ * Sparse-layer decode over the full layer's 8-bit caches (the format of
+ * embla_full_decode_e4m3): the same operation as embla_sparse_decode on the
+ * decoded rows scale * decode(codes).
+ *   k_codes, v_codes, k_scales, v_scales   as for embla_full_decode_e4m3
+ *   every other argument, the workspace size and the result as for
+ *   embla_sparse_decode.
+ * The query enters the tensor cores in f16 after division by a power of two per
+ * head (exact for every element at least 2^-24 times its head's largest); the
+ * value sums run in fp32.
+ */
+embla_status embla_sparse_decode_e4m3(const embla_shape *shape, const void *q,
+                                      const uint8_t *k_codes, const float *k_scales,
+                                      const uint8_t *v_codes, const float *v_scales,
+                                      const int32_t *idx, int32_t idx_stride,
+                                      const int32_t *count, float tau, float *out,
+                                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Window-layer decode — "Three kinds of attention" (Sliding window).

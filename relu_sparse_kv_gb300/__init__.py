@@ -9,6 +9,8 @@ no CPU path: if the library was not built, importing the binding's functions rai
 Tensors (torch, on the current CUDA device, C-contiguous):
   q              bf16  [B, Hq, D]
   k_cache/v_cache bf16 [B, Hkv, cache_stride, D]
+  k_codes/v_codes uint8 [B, Hkv, cache_stride, D]  (E4M3 codes, *_e4m3 calls)
+  k_scales/v_scales fp32 [B, Hkv, cache_stride]    (one scale per token and KV head)
   out            fp32  [B, Hq, D]
   n_surv, count  int32 [B, Hkv]
   sel_scores     fp32  [B, Hkv, cache_stride]
@@ -82,6 +84,10 @@ def library() -> ctypes.CDLL:
             "embla_full_decode_workspace_size": (sz, [P]),
             "embla_full_decode": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32, vp, vp, vp, vp, vp,
                                                  sz, vp]),
+            "embla_full_decode_e4m3": (ctypes.c_int, [P, vp, vp, vp, vp, vp, f32, f32, f32, vp,
+                                                       vp, vp, vp, vp, sz, vp]),
+            "embla_sparse_decode_e4m3": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, i32, vp,
+                                                         f32, vp, vp, sz, vp]),
             "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
                                                                 vp, vp, vp, vp, vp]),
             "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
@@ -180,6 +186,30 @@ def embla_full_decode(shape: Shape, q, k_cache, v_cache, out, n_surv, sel_scores
           ws.numel() * ws.element_size(), _stream(stream))
 
 
+def embla_full_decode_e4m3(shape: Shape, q, k_codes, k_scales, v_codes, v_scales, out, n_surv,
+                           sel_scores=None, sel_hist=None, alpha: float = 1.0, c: float = 1.0,
+                           eps: float = 1e-6, workspace=None, stream=None):
+    """embla_full_decode over 8-bit caches: E4M3 codes (uint8 [B, Hkv, cache_stride, D]) with
+    one fp32 scale per (token, KV head) (float32 [B, Hkv, cache_stride]); row j stands for
+    scale * decode(codes).  cache_stride must be a multiple of 4."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_codes, torch.uint8, (B, Hkv, ncap, D), "k_codes")
+    _check(k_scales, torch.float32, (B, Hkv, ncap), "k_scales")
+    _check(v_codes, torch.uint8, (B, Hkv, ncap, D), "v_codes")
+    _check(v_scales, torch.float32, (B, Hkv, ncap), "v_scales")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    _check(n_surv, torch.int32, (B, Hkv), "n_surv")
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores", allow_none=True)
+    _check(sel_hist, torch.int32, (B, Hkv, HIST_BINS), "sel_hist", allow_none=True)
+    ws = _workspace(embla_full_decode_workspace_size(shape), workspace, q.device)
+    _call("embla_full_decode_e4m3", ctypes.byref(shape.c()), _ptr(q), _ptr(k_codes),
+          _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), alpha, c, eps, _ptr(out), _ptr(n_surv),
+          _ptr(sel_scores), _ptr(sel_hist), _ptr(ws), ws.numel() * ws.element_size(),
+          _stream(stream))
+
+
 def embla_full_decode_static_scratch(shape: Shape, q, k_cache, v_cache, out, n_surv,
                                      sel_scores=None, sel_hist=None, alpha: float = 1.0,
                                      c: float = 1.0, eps: float = 1e-6, stream=None):
@@ -234,6 +264,28 @@ def embla_sparse_decode(shape: Shape, q, k_cache, v_cache, idx, count, out, tau:
     _call("embla_sparse_decode", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache),
           _ptr(idx), idx.shape[2], _ptr(count), tau, _ptr(out), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_sparse_decode_e4m3(shape: Shape, q, k_codes, k_scales, v_codes, v_scales, idx, count,
+                             out, tau: float | None = None, workspace=None, stream=None):
+    """embla_sparse_decode over the full layer's 8-bit caches (as for embla_full_decode_e4m3)."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_codes, torch.uint8, (B, Hkv, ncap, D), "k_codes")
+    _check(k_scales, torch.float32, (B, Hkv, ncap), "k_scales")
+    _check(v_codes, torch.uint8, (B, Hkv, ncap, D), "v_codes")
+    _check(v_scales, torch.float32, (B, Hkv, ncap), "v_scales")
+    _check(idx, torch.int32, None, "idx")
+    if idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hkv):
+        raise ValueError("idx must be [B, Hkv, idx_stride]")
+    _check(count, torch.int32, (B, Hkv), "count")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    tau = D ** -0.5 if tau is None else tau
+    ws = _workspace(embla_sparse_decode_workspace_size(shape, idx.shape[2]), workspace, q.device)
+    _call("embla_sparse_decode_e4m3", ctypes.byref(shape.c()), _ptr(q), _ptr(k_codes),
+          _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(idx), idx.shape[2], _ptr(count),
+          tau, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
 def embla_window_decode(shape: Shape, q, k_win, v_win, pos: int, out, window: int = 128,

@@ -99,6 +99,34 @@ bool encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D uint8 tensor [rows, 128] of E4M3 codes (128-byte rows), boxes of {128 columns,
+// box_rows}, 128B swizzle.
+bool encode_rows_e4m3(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D fp32 tensor [units, ncap] of per-token scales, boxes of {128 tokens, 1 unit}; tokens
+// past ncap read as 0.
+bool encode_scales(CUtensorMap *map, const float *base, uint64_t units, uint64_t ncap) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {ncap, units};
+  const cuuint64_t strides[1] = {ncap * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKeys), 1u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool finite(float x) { return x == x && x - x == 0.0f; }
@@ -147,19 +175,30 @@ size_t embla_full_decode_workspace_size(const embla_shape *shape) {
   return full_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_kv_heads, G, sms);
 }
 
-embla_status embla_full_decode(const embla_shape *shape, const void *q, const void *k_cache,
-                               const void *v_cache, float alpha, float c, float eps, float *out,
-                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
-                               void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// The full-layer decode for bf16 caches (k_scales and v_scales null) or 8-bit E4M3 caches
+// with per-token scales.
+embla_status full_decode_impl(const embla_shape *shape, const void *q, const void *k_cache,
+                              const float *k_scales, const void *v_cache, const float *v_scales,
+                              bool kv8, float alpha, float c, float eps, float *out,
+                              int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
+                              void *workspace, size_t workspace_bytes, void *stream) {
   int G = 0;
   embla_status st = check_shape(shape, &G, true);
   if (st != EMBLA_OK) return st;
   if (!(finite(alpha) && alpha > 0.0f) || !(finite(c) && c >= 0.0f) ||
       !(finite(eps) && eps >= 0.0f))
     return EMBLA_ERR_INVALID_ARG;
+  // the scale arrays are read as [units, cache_stride] with 16-byte aligned rows
+  if (kv8 && shape->cache_stride % 4 != 0) return EMBLA_ERR_INVALID_ARG;
   const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
   if (units == 0) return EMBLA_OK;
   if (!q || !k_cache || !v_cache || !out || !n_surv || !workspace) return EMBLA_ERR_INVALID_ARG;
+  if (kv8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
+    return EMBLA_ERR_INVALID_ARG;
   if ((sel_scores == nullptr) != (sel_hist == nullptr)) return EMBLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(workspace) || (sel_scores && (!aligned16(sel_scores) || !aligned16(sel_hist))))
@@ -186,17 +225,48 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
   }
   // the launch zeroes the histogram and the arrival counters itself
   int32_t *arrivals = full_arrivals(workspace, units, G, sms);
-  CUtensorMap tm_k, tm_q;
-  if (!encode_rows(&tm_k, k_cache, static_cast<uint64_t>(units * shape->cache_stride), kTileKeys,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+  const uint64_t rows = static_cast<uint64_t>(units * shape->cache_stride);
+  CUtensorMap tm_k, tm_q, tm_ks, tm_vs;
+  const bool kmap = kv8 ? encode_rows_e4m3(&tm_k, k_cache, rows, kTileKeys)
+                        : encode_rows(&tm_k, k_cache, rows, kTileKeys,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (!kmap ||
       !encode_rows(&tm_q, q, static_cast<uint64_t>(shape->batch) * shape->n_q_heads,
                    static_cast<uint32_t>(G), CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return EMBLA_ERR_CUDA;
-  return cuda_status(launch_full_decode(G, tm_k, tm_q, v_cache, sel_scores, sel_hist,
+  if (kv8 && (!encode_scales(&tm_ks, k_scales, static_cast<uint64_t>(units),
+                             static_cast<uint64_t>(shape->cache_stride)) ||
+              !encode_scales(&tm_vs, v_scales, static_cast<uint64_t>(units),
+                             static_cast<uint64_t>(shape->cache_stride))))
+    return EMBLA_ERR_CUDA;
+  return cuda_status(launch_full_decode(G, kv8, tm_k, tm_q, kv8 ? &tm_ks : nullptr,
+                                        kv8 ? &tm_vs : nullptr, v_cache, sel_scores, sel_hist,
                                         workspace, arrivals, out, n_surv, c, flags, sp,
                                         shape->ctx_len,
                                         shape->cache_stride, shape->n_q_heads, shape->n_kv_heads,
                                         alpha, eps, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+embla_status embla_full_decode(const embla_shape *shape, const void *q, const void *k_cache,
+                               const void *v_cache, float alpha, float c, float eps, float *out,
+                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  return full_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, alpha, c, eps,
+                          out, n_surv, sel_scores, sel_hist, workspace, workspace_bytes, stream);
+}
+
+embla_status embla_full_decode_e4m3(const embla_shape *shape, const void *q,
+                                    const uint8_t *k_codes, const float *k_scales,
+                                    const uint8_t *v_codes, const float *v_scales, float alpha,
+                                    float c, float eps, float *out, int32_t *n_surv,
+                                    float *sel_scores, uint32_t *sel_hist, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  return full_decode_impl(shape, q, k_codes, k_scales, v_codes, v_scales, true, alpha, c, eps,
+                          out, n_surv, sel_scores, sel_hist, workspace, workspace_bytes, stream);
 }
 
 embla_status embla_full_decode_static_scratch(const embla_shape *shape, const void *q,
@@ -262,10 +332,15 @@ size_t embla_sparse_decode_workspace_size(const embla_shape *shape, int32_t idx_
                                 idx_stride);
 }
 
-embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const void *k_cache,
-                                 const void *v_cache, const int32_t *idx, int32_t idx_stride,
-                                 const int32_t *count, float tau, float *out, void *workspace,
-                                 size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+embla_status sparse_decode_impl(const embla_shape *shape, const void *q, const void *k_cache,
+                                const float *k_scales, const void *v_cache,
+                                const float *v_scales, bool kv8, const int32_t *idx,
+                                int32_t idx_stride, const int32_t *count, float tau, float *out,
+                                void *workspace, size_t workspace_bytes, void *stream) {
   int G = 0;
   embla_status st = check_shape(shape, &G, true);
   if (st != EMBLA_OK) return st;
@@ -273,6 +348,8 @@ embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const 
   const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
   if (units == 0) return EMBLA_OK;
   if (!q || !k_cache || !v_cache || !idx || !count || !out || !workspace)
+    return EMBLA_ERR_INVALID_ARG;
+  if (kv8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
     return EMBLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(workspace) || !aligned16(idx) || !aligned16(count))
@@ -282,10 +359,33 @@ embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const 
   if (!flags) return EMBLA_ERR_CUDA;
   const int sms = sm_count_of(current_device());
   if (sms <= 0) return EMBLA_ERR_CUDA;
-  return cuda_status(launch_sparse_decode(G, q, k_cache, v_cache, idx, idx_stride, count, units,
-                                          shape->n_kv_heads, shape->ctx_len, shape->cache_stride,
-                                          tau, out, workspace, flags, sms,
+  return cuda_status(launch_sparse_decode(G, q, k_cache, v_cache, kv8 ? k_scales : nullptr,
+                                          kv8 ? v_scales : nullptr, idx, idx_stride, count,
+                                          units, shape->n_kv_heads, shape->ctx_len,
+                                          shape->cache_stride, tau, out, workspace, flags, sms,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *idx, int32_t idx_stride,
+                                 const int32_t *count, float tau, float *out, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+  return sparse_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, idx, idx_stride,
+                            count, tau, out, workspace, workspace_bytes, stream);
+}
+
+embla_status embla_sparse_decode_e4m3(const embla_shape *shape, const void *q,
+                                      const uint8_t *k_codes, const float *k_scales,
+                                      const uint8_t *v_codes, const float *v_scales,
+                                      const int32_t *idx, int32_t idx_stride,
+                                      const int32_t *count, float tau, float *out,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+  return sparse_decode_impl(shape, q, k_codes, k_scales, v_codes, v_scales, true, idx,
+                            idx_stride, count, tau, out, workspace, workspace_bytes, stream);
 }
 
 size_t embla_window_decode_workspace_size(const embla_shape *shape, int32_t window) {

@@ -27,6 +27,19 @@
 //              in tile order; at the end of each stretch of a unit they write a partial
 //              record, and the last warp to publish a unit's record sums its records and
 //              writes out = num / (c + den) and the survivor count.
+//
+// 8-bit caches (E4M3 codes with one fp32 scale per token and KV head; same roles):
+//   - a stage is the 16 KB code tile (one 128-column box, 128-byte swizzle) plus the
+//     tile's 512-byte K-scale and V-scale runs; 6 stages.
+//   - the key-norm warps also build, once per unit, the query as three E4M3 terms with
+//     t1 + t2 / 16 + t3 / 256 = q / 2^e (2^e a power of two per head, so |q / 2^e| < 256),
+//     laid out as MMA rows term * G + h; the sum is within 2^-25 of the head's largest
+//     |q| of every element, and exact for every element at least 2^-14 of it.
+//   - the tensor cores take the codes and the terms directly (kind::f8f6f4, K = 32), one
+//     accumulator per k-step; the epilogue sums the terms and k-steps in fp32 and folds
+//     2^e into the query factor, and the key scale into rk:
+//     rk = ks / sqrt(ks^2 * mean(code^2) + eps).
+//   - 128-byte V rows; the accumulators decode the codes and weight them by w * vs.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -36,36 +49,23 @@ namespace {
 #ifndef EMBLA_K_STAGES
 #define EMBLA_K_STAGES 3
 #endif
+#ifndef EMBLA_K8_STAGES
+#define EMBLA_K8_STAGES 6
+#endif
 #ifndef EMBLA_W_SLOTS
 #define EMBLA_W_SLOTS 8
 #endif
 #ifndef EMBLA_V_RING_ROWS
 #define EMBLA_V_RING_ROWS 256
 #endif
-constexpr int kStages = EMBLA_K_STAGES;            // K tiles in flight
-// Tile i lands on barrier full[(i % kStages) * 2 + (i & 1)]: one barrier per stage and MMA
-// issuer, so the uses of each barrier are consumed in order by one issuer (with an odd
-// stage count a stage's consecutive tiles belong to different issuers, and a parity test
-// by one issuer could be answered by the other's phase).  Barrier uses repeat every
-// kFullPeriod tiles.
-constexpr int kFullPeriod = kStages % 2 == 0 ? kStages : 2 * kStages;
 constexpr int kWSlots = EMBLA_W_SLOTS;             // per-tile survivor lists in flight
 constexpr int kRing = EMBLA_V_RING_ROWS;           // V rows in flight
 constexpr int kGroups = 2;                         // epilogue warpgroups, alternating tiles
 constexpr int kAccBufs = 2 * kGroups;              // tensor-memory accumulators
 constexpr int kNormSlots = 8;                      // per-tile key-norm arrays in flight
-constexpr int kRowBytes = kHeadDim * 2;            // 256
-constexpr int kTileBytes = kTileKeys * kRowBytes;  // 32 KB
-constexpr int kHalfBytes = kTileBytes / 2;         // 128 rows x 64 dims
-constexpr int kQBufBytes = 4096;                   // 16 rows x 128 dims (MMA N = 16)
+constexpr int kQBufBytes = 4096;                   // 16 rows x 128 dims of bf16 (MMA N = 16)
 constexpr int kQHalfBytes = kQBufBytes / 2;
-constexpr int kMmaN = 16;                          // scores: 128 keys x 16 query rows
-constexpr int kKSteps = kHeadDim / 16;             // MMA k-steps per tile
-// Each k-step writes its own accumulator, so a tile's eight MMAs do not wait on each
-// other; the epilogue adds the eight partial dot products.
-constexpr int kAccCols = kKSteps * kMmaN;          // 128 columns per tile
-constexpr int kTmemCols = kAccBufs * kAccCols;     // 512
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN);
+constexpr int kQ8BufBytes = 4096;                  // up to 32 rows x 128 dims of E4M3
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
 constexpr int kWarpAcc = kWarpEpi + 4 * kGroups;
 constexpr int kWarpNorm = kWarpAcc + 4;
@@ -76,9 +76,39 @@ constexpr int kThreads = (kWarpHist + 1) * 32;     // 640
 static_assert(kRing >= kTileKeys, "a whole tile of survivors must fit the V ring");
 static_assert((kRing & (kRing - 1)) == 0, "the V ring size is a power of two");
 
+// What differs between bf16 caches (KV8 false) and 8-bit E4M3 caches with per-token
+// scales (KV8 true).
+template <int G, bool KV8>
+struct Cfg {
+  static constexpr int stages = KV8 ? EMBLA_K8_STAGES : EMBLA_K_STAGES;  // K tiles in flight
+  // Tile i lands on barrier full[(i % stages) * 2 + (i & 1)]: one barrier per stage and MMA
+  // issuer, so the uses of each barrier are consumed in order by one issuer (with an odd
+  // stage count a stage's consecutive tiles belong to different issuers, and a parity
+  // test by one issuer could be answered by the other's phase).  Barrier uses repeat
+  // every full_period tiles.
+  static constexpr int full_period = stages % 2 == 0 ? stages : 2 * stages;
+  static constexpr int row_bytes = KV8 ? kHeadDim : 2 * kHeadDim;  // one cached K or V row
+  static constexpr int tile_bytes = kTileKeys * row_bytes;           // 32 KB / 16 KB
+  static constexpr int half_bytes = kTileKeys * 128;                 // one 128-byte-wide box
+  static constexpr int scale_bytes = KV8 ? kTileKeys * 4 : 0;        // K (then V) scales
+  static constexpr int stage_bytes = tile_bytes + 2 * scale_bytes;
+  // scores: 128 keys x mma_n query rows (bf16: G heads; E4M3: 3 terms x G heads)
+  static constexpr int mma_n = KV8 ? (3 * G <= 16 ? 16 : 32) : 16;
+  static constexpr int kstep_dims = KV8 ? 32 : 16;
+  static constexpr int ksteps = kHeadDim / kstep_dims;
+  // Each k-step writes its own accumulator, so a tile's MMAs do not wait on each other
+  // (and no long sum is kept inside the tensor core); the epilogue adds the partials.
+  static constexpr int acc_cols = ksteps * mma_n;                    // 128 / 64 / 128
+  static constexpr int tmem_cols = kAccBufs * acc_cols;              // 512 / 256 / 512
+  static constexpr uint32_t idesc = KV8 ? idesc_e4m3_f32(128, mma_n) : idesc_bf16_f32(128, 16);
+  static_assert(stage_bytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+  static_assert(tile_bytes == (KV8 ? 1 : 2) * half_bytes, "a tile is one or two boxes");
+  static_assert(tmem_cols == 256 || tmem_cols == 512, "tensor-memory allocation size");
+};
+
 // One tile's survivors in ascending key order: entry e has its V row in ring row
 // (row0 + e) mod kRing.  Also the tile's selection scores, for the histogram warp.
-template <int G>
+template <int G, bool KV8>
 struct WSlot {
   int32_t cnt[4];             // survivors per TMEM quarter (32 keys each)
   int32_t row0;               // first V-ring row of this tile
@@ -87,26 +117,31 @@ struct WSlot {
   int32_t key[kTileKeys];     // key index within the unit
   float w[kTileKeys][G];      // ReLU^2 weights per head
   float sig[kTileKeys];       // sigma of every key of the tile
+  float vs[KV8 ? kTileKeys : 1];  // V scale of each survivor (8-bit caches)
 };
 
-template <int G>
+template <int G, bool KV8>
 struct Smem {
+  using C = Cfg<G, KV8>;
   static constexpr int k_off = 0;
-  static constexpr int q_off = k_off + kStages * kTileBytes;
-  static constexpr int ring_off = q_off + 2 * kQBufBytes;
-  static constexpr int wslot_off = ring_off + kRing * kRowBytes;
-  static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G>));
+  static constexpr int q_off = k_off + C::stages * C::stage_bytes;
+  static constexpr int q8_off = q_off + 2 * kQBufBytes;
+  static constexpr int ring_off = q8_off + (KV8 ? 2 * kQ8BufBytes : 0);
+  static constexpr int wslot_off = ring_off + kRing * C::row_bytes;
+  static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G, KV8>));
   static constexpr int rk_off = hist_off + kHistBins * 4;
-  static constexpr int misc_off = rk_off + kNormSlots * kTileKeys * 4;
+  static constexpr int vs_off = rk_off + kNormSlots * kTileKeys * 4;  // V scales beside rk
+  static constexpr int misc_off = vs_off + (KV8 ? kNormSlots * kTileKeys * 4 : 0);
   static constexpr int end_off = misc_off + 64;                 // int64 per W slot, + 2 ring counters
   static constexpr int bar_off = end_off + (kWSlots + 2) * 8;
-  static constexpr int n_bars = 3 * kStages + 2 * kAccBufs + 4 + 4 * kWSlots + 2 * kNormSlots;
+  static constexpr int n_bars = 3 * C::stages + 2 * kAccBufs + 8 + 4 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
+  static_assert(alloc <= 227 * 1024, "shared memory per CTA");
 };
 
 struct FullParams {
-  const uint8_t *v;  // V cache
+  const uint8_t *v;  // V cache (bf16 rows or E4M3 codes)
   float *sel;        // selection scores or null
   uint32_t *hist;    // selection histogram or null
   float *rec;        // partial records
@@ -120,6 +155,15 @@ struct FullParams {
   float alpha, eps;
 };
 
+// Power-of-two exponent e with |q| / 2^e < 256 for the head's largest |q| element (the
+// E4M3 query terms); kept within [-120, 127] so 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int q8_exponent(float maxabs) {
+  const int be = static_cast<int>((__float_as_uint(maxabs) >> 23) & 0xFFu);  // biased
+  const int e = be - 127 - 7;
+  return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
 __device__ __forceinline__ float sumsq8(const uint4 &v) {
   float a = bf16lo(v.x) * bf16lo(v.x);
   float b = bf16hi(v.x) * bf16hi(v.x);
@@ -130,6 +174,74 @@ __device__ __forceinline__ float sumsq8(const uint4 &v) {
   a = fmaf(bf16lo(v.w), bf16lo(v.w), a);
   b = fmaf(bf16hi(v.w), bf16hi(v.w), b);
   return a + b;
+}
+
+// Largest |x| of the eight bf16 values in v.
+__device__ __forceinline__ float maxabs8(const uint4 &v) {
+  const float a = fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
+                        fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))));
+  const float b = fmaxf(fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))),
+                        fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w))));
+  return fmaxf(a, b);
+}
+
+// The unit's query rows (bf16, two 64-dim boxes of 128-byte swizzled rows) as three E4M3
+// terms per head: x = q / 2^e, t1 = rn(x), t2 = rn(16 (x - t1)), t3 = rn(16 (16 (x - t1) -
+// t2)), so q = 2^e (t1 + t2 / 16 + t3 / 256) up to 2^-25 of the head's largest |q| (every
+// remainder is at most 8 in magnitude, so no term saturates; the scaling by 16 keeps the
+// later terms clear of the E4M3 subnormal range).  Written as rows t * G + h of a
+// 128-byte swizzled operand.  Thread t of the 128 takes head
+// t / 8 and dims 16 (t % 8) .. 16 (t % 8) + 15; all 32 lanes of a warp must call it.
+template <int G>
+__device__ __forceinline__ void build_q8_terms(const uint8_t *qsrc, uint8_t *qdst, int t) {
+  const int h = t >> 3, c = t & 7;
+  float x[16];
+  float mx = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) x[k] = 0.0f;
+  if (h < G) {
+    // dims 16c.. are 16-byte chunks 2c and 2c+1 of the row, in box c / 4
+    const uint8_t *qr = qsrc + (c >> 2) * kQHalfBytes + h * 128;
+    const uint4 a = *reinterpret_cast<const uint4 *>(qr + ((((2 * c) & 7) ^ (h & 7)) * 16));
+    const uint4 b = *reinterpret_cast<const uint4 *>(qr + ((((2 * c + 1) & 7) ^ (h & 7)) * 16));
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      x[2 * k] = bf16lo(w[k]);
+      x[2 * k + 1] = bf16hi(w[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(x[k]));
+  }
+  // the head's 8 threads are 8 neighbouring lanes
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (h < G) {
+    const float inv = pow2f(-q8_exponent(mx));
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] *= inv;
+#pragma unroll
+    for (int term = 0; term < 3; ++term) {
+      uint32_t cw[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) cw[g] = f32x4_to_e4m3x4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+      const int r = term * G + h;
+      *reinterpret_cast<uint4 *>(qdst + r * 128 + ((c ^ (r & 7)) * 16)) =
+          make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      if (term < 2) {
+        // the remainder (exact in fp32, at most 8 in magnitude) times 16 for the next term
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float d0, d1, d2, d3;
+          e4m3x4_to_f32(cw[g], d0, d1, d2, d3);
+          x[4 * g] = (x[4 * g] - d0) * 16.0f;
+          x[4 * g + 1] = (x[4 * g + 1] - d1) * 16.0f;
+          x[4 * g + 2] = (x[4 * g + 2] - d2) * 16.0f;
+          x[4 * g + 3] = (x[4 * g + 3] - d3) * 16.0f;
+        }
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ void set_abort(volatile int *abort_flag, uint32_t *flags) {
@@ -145,20 +257,28 @@ __device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
   }
 }
 
-template <int G>
+template <int G, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     full_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_q, const FullParams p) {
-  using L = Smem<G>;
+                       const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_ks,
+                       const __grid_constant__ CUtensorMap tm_vs, const FullParams p) {
+  using L = Smem<G, KV8>;
+  using C = Cfg<G, KV8>;
+  constexpr int kStages = C::stages;
+  constexpr int kFullPeriod = C::full_period;
+  constexpr int kRowBytes = C::row_bytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // offset arithmetic on the shared array keeps every access in the shared state space
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *sK = smem + L::k_off;
   uint8_t *sQ = smem + L::q_off;
+  uint8_t *sQ8 = smem + L::q8_off;  // E4M3 query terms (8-bit caches)
   uint8_t *sRing = smem + L::ring_off;
-  WSlot<G> *wslots = reinterpret_cast<WSlot<G> *>(smem + L::wslot_off);
+  WSlot<G, KV8> *wslots = reinterpret_cast<WSlot<G, KV8> *>(smem + L::wslot_off);
   uint32_t *s_hist = reinterpret_cast<uint32_t *>(smem + L::hist_off);
   float *s_rk = reinterpret_cast<float *>(smem + L::rk_off);
+  float *s_vs = reinterpret_cast<float *>(smem + L::vs_off);
   int *misc = reinterpret_cast<int *>(smem + L::misc_off);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
   volatile int *s_abort = misc + 1;
@@ -183,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *sfull = vfull + kWSlots;     // selection scores of a tile written
   uint64_t *rkfull = sfull + kWSlots;    // key norms of a tile written
   uint64_t *rkempty = rkfull + kNormSlots;  // key norms of a tile read
+  uint64_t *q8full = rkempty + kNormSlots;  // E4M3 query terms written
+  uint64_t *q8empty = q8full + 2;           // E4M3 query terms no longer needed
 
   // the zeroing kernel before this one waited for everything earlier, so the selection
   // kernel after this one may launch now (it waits for this kernel to finish)
@@ -209,7 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&qfull[q], 1);
-      mbar_init(&qempty[q], kMmaWarps + 4 * kGroups);
+      // readers of the bf16 query rows: the epilogue warps, and the MMA issuers (bf16
+      // caches) or the norm warps building the E4M3 terms (8-bit caches)
+      mbar_init(&qempty[q], 4 * kGroups + (KV8 ? 4 : kMmaWarps));
+      mbar_init(&q8full[q], 4);
+      mbar_init(&q8empty[q], kMmaWarps);
     }
     for (int w = 0; w < kWSlots; ++w) {
       mbar_init(&adone[w], 1);
@@ -234,10 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // them anyway so no stale bits reach the tensor core.
   for (int i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (KV8)
+    for (int i = threadIdx.x; i < 2 * kQ8BufBytes / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(sQ8)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0u;
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
-    tmem_alloc(s_tmem, kTmemCols);
+    tmem_alloc(s_tmem, C::tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -250,6 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_q);
+      if constexpr (KV8) {
+        tma_prefetch_desc(&tm_ks);
+        tma_prefetch_desc(&tm_vs);
+      }
       const uint64_t policy = policy_evict_first();
       int u = u0, tl = tl0;
       int seg = -1;
@@ -274,10 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint64_t *fb = &full[2 * s + (i & 1)];
-        mbar_arrive_expect_tx(fb, kTileBytes);
+        mbar_arrive_expect_tx(fb, C::stage_bytes);
         const int32_t row = static_cast<int32_t>(static_cast<int64_t>(u) * p.ncap) + tl * kTileKeys;
-        tma_load_2d_hint(sK + s * kTileBytes, &tm_k, fb, 0, row, policy);
-        tma_load_2d_hint(sK + s * kTileBytes + kHalfBytes, &tm_k, fb, 64, row, policy);
+        uint8_t *st = sK + s * C::stage_bytes;
+        tma_load_2d_hint(st, &tm_k, fb, 0, row, policy);
+        if constexpr (KV8) {
+          // the tile's K and V scales: 128 floats each from row u of the [units, ncap] arrays
+          tma_load_2d_hint(st + C::tile_bytes, &tm_ks, fb, tl * kTileKeys, u, policy);
+          tma_load_2d_hint(st + C::tile_bytes + C::scale_bytes, &tm_vs, fb, tl * kTileKeys, u,
+                           policy);
+        } else {
+          tma_load_2d_hint(st + C::half_bytes, &tm_k, fb, 64, row, policy);
+        }
         *s_k_issued = i + 1;
         if (++s == kStages) {
           s = 0;
@@ -293,8 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mw = warp == kWarpMma ? 0 : 1;
     if (lane == 0) {
       // descriptors are built once; per k-step only their start-address field moves
+      // (8-bit caches: the MMA's query operand is the E4M3 terms, which the norm warps
+      // write; the bf16 rows are handed back by those warps instead)
+      constexpr int qbuf_bytes = KV8 ? kQ8BufBytes : kQBufBytes;
+      uint64_t *qf = KV8 ? q8full : qfull;
+      uint64_t *qe = KV8 ? q8empty : qempty;
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(sK));
-      const uint64_t qdesc0 = smem_desc_sw128(smem_u32(sQ));
+      const uint64_t qdesc0 = smem_desc_sw128(smem_u32(KV8 ? sQ8 : sQ));
       uint64_t qdesc = qdesc0;
       int tl = tl0, seg = -1, qb = 0, issued = 0;
       int s = 0, b = 0, bphase = 0;
@@ -303,15 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i == 0 || tl == 0) {
           ++seg;
           qb = seg & 1;
-          qdesc = qdesc0 + static_cast<uint64_t>((qb * kQBufBytes) >> 4);
-          if (!mbar_wait(&qfull[qb], (seg >> 1) & 1)) {
+          qdesc = qdesc0 + static_cast<uint64_t>((qb * qbuf_bytes) >> 4);
+          if (!mbar_wait(&qf[qb], (seg >> 1) & 1)) {
             set_abort(s_abort, p.flags);
             break;
           }
         }
         if ((i & 1) != mw) {
           // not this issuer's tile; it still hands back the query buffer at a unit's end
-          if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qempty[qb]);
+          if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qe[qb]);
           if (++tl == TU) tl = 0;
           if (++s == kStages) s = 0;
           if (++b == kAccBufs) {
@@ -326,19 +472,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint64_t adesc = kdesc0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
-        const uint32_t dcol = tmem + b * kAccCols;
+        const uint64_t adesc = kdesc0 + static_cast<uint64_t>((s * C::stage_bytes) >> 4);
+        const uint32_t dcol = tmem + b * C::acc_cols;
 #pragma unroll
-        for (int kk = 0; kk < kKSteps; ++kk) {
-          // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is 32
-          // bytes into a 128-byte row, the second half of the dims starts a new box
-          tc_mma_bf16(dcol + kk * kMmaN, adesc + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4),
-                      qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), kIdesc, 0u);
+        for (int kk = 0; kk < C::ksteps; ++kk) {
+          if constexpr (KV8) {
+            // partial scores over dims 32kk..32kk+31: D_kk[key][t*G + h] = code . t_th;
+            // k-step kk is 32 bytes into the 128-byte rows of codes and of terms
+            tc_mma_e4m3(dcol + kk * C::mma_n, adesc + ((kk * 32) >> 4), qdesc + ((kk * 32) >> 4),
+                        C::idesc, 0u);
+          } else {
+            // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is
+            // 32 bytes into a 128-byte row, the second half of the dims starts a new box
+            tc_mma_bf16(dcol + kk * C::mma_n,
+                        adesc + (((kk >> 2) * C::half_bytes + (kk & 3) * 32) >> 4),
+                        qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), C::idesc, 0u);
+          }
         }
         tc_commit(&accf[b]);
         tc_commit(&empty[s]);
         issued = i + 1;
-        if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qempty[qb]);
+        if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qe[qb]);
         if (++tl == TU) tl = 0;
         if (++s == kStages) s = 0;
         if (++b == kAccBufs) {
@@ -378,14 +532,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float ss = 0.0f;
-          if (lane < 16)
-            ss = sumsq8(*reinterpret_cast<const uint4 *>(sQ + qb * kQBufBytes +
-                                                         (lane >> 3) * kQHalfBytes + h * 128 +
-                                                         (lane & 7) * 16));
+          float ss = 0.0f, mx = 0.0f;
+          if (lane < 16) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(sQ + qb * kQBufBytes +
+                                                             (lane >> 3) * kQHalfBytes + h * 128 +
+                                                             (lane & 7) * 16);
+            ss = sumsq8(x);
+            if constexpr (KV8) mx = maxabs8(x);
+          }
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          for (int o = 16; o > 0; o >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if constexpr (KV8) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
           aq[h] = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+          // the E4M3 terms hold q / 2^e: put the 2^e back here
+          if constexpr (KV8) aq[h] *= pow2f(q8_exponent(mx));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[qb]);
@@ -403,15 +565,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float dot[G];
       tc_fence_after_sync();
-      {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * kAccCols;
-        uint32_t r[kKSteps * G];
+      if constexpr (KV8) {
+        // k-steps two at a time: columns t*G + h of each k-step's accumulator
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
 #pragma unroll
-        for (int kk = 0; kk < kKSteps; ++kk) {
+        for (int h = 0; h < G; ++h) dot[h] = 0.0f;
+#pragma unroll
+        for (int k2 = 0; k2 < C::ksteps; k2 += 2) {
+          uint32_t r[2 * 3 * G];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t a = taddr + (k2 + k) * C::mma_n;
+            if constexpr (G == 4) {
+              tmem_load_x8(a, *reinterpret_cast<uint32_t(*)[8]>(&r[k * 12]));
+              tmem_load_x4(a + 8, *reinterpret_cast<uint32_t(*)[4]>(&r[k * 12 + 8]));
+            } else {
+              tmem_load_x16(a, *reinterpret_cast<uint32_t(*)[16]>(&r[k * 24]));
+              tmem_load_x8(a + 16, *reinterpret_cast<uint32_t(*)[8]>(&r[k * 24 + 16]));
+            }
+          }
+          tmem_wait_ld(r);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t *rk3 = &r[k * 3 * G];
+              // t1 + t2 / 16 + t3 / 256 (the scalings are exact)
+              dot[h] += (__uint_as_float(rk3[2 * G + h]) * 0.0625f + __uint_as_float(rk3[G + h])) *
+                            0.0625f +
+                        __uint_as_float(rk3[h]);
+            }
+          }
+        }
+      } else {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
+        uint32_t r[C::ksteps * G];
+#pragma unroll
+        for (int kk = 0; kk < C::ksteps; ++kk) {
           if constexpr (G == 4)
-            tmem_load_x4(taddr + kk * kMmaN, *reinterpret_cast<uint32_t(*)[4]>(&r[kk * G]));
+            tmem_load_x4(taddr + kk * C::mma_n, *reinterpret_cast<uint32_t(*)[4]>(&r[kk * G]));
           else
-            tmem_load_x8(taddr + kk * kMmaN, *reinterpret_cast<uint32_t(*)[8]>(&r[kk * G]));
+            tmem_load_x8(taddr + kk * C::mma_n, *reinterpret_cast<uint32_t(*)[8]>(&r[kk * G]));
         }
         tmem_wait_ld(r);
 #pragma unroll
@@ -425,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before_sync();
       const float rk = s_rk[ns * kTileKeys + row];
-      const float rk_used = __shfl_sync(0xffffffffu, rk, 31);  // every lane's read is back
+      const float vsc = KV8 ? s_vs[ns * kTileKeys + row] : 0.0f;
+      // every lane's reads are back
+      const float rk_used = __shfl_sync(0xffffffffu, KV8 ? rk + vsc : rk, 31);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&acce[b]);
@@ -441,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc[h] = dot[h] * aq[h] * rk;
         sigma = fmaxf(sigma, sc[h]);
       }
-      WSlot<G> &ws = wslots[slot];
+      WSlot<G, KV8> &ws = wslots[slot];
       if (p.sel != nullptr) {
         ws.sig[row] = sigma;
         __syncwarp();
@@ -464,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ws.key[e] = j;
 #pragma unroll
         for (int h = 0; h < G; ++h) ws.w[e][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
+        if constexpr (KV8) ws.vs[e] = vsc;
       }
       if (leader) {
         // Reserve m ring rows in tile order: after the previous tile's reservation, and
@@ -522,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           set_abort(s_abort, p.flags);
           break;
         }
-        const WSlot<G> &ws = wslots[slot];
+        const WSlot<G, KV8> &ws = wslots[slot];
         float sg[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) sg[r] = ws.sig[lane + 32 * r];
@@ -556,11 +753,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kWarpNorm) {
     // ------------------------------------------------------------------ key norms
-    // One thread per key of each landed tile: 1 / sqrt(mean(k^2) + eps).  The stage is
-    // released as soon as these four warps and the tile's MMAs are done with it.
+    // One thread per key of each landed tile: 1 / sqrt(mean(k^2) + eps) (8-bit caches:
+    // ks / sqrt(ks^2 mean(code^2) + eps), with the key's V scale passed along).  The stage
+    // is released as soon as these four warps and the tile's MMAs are done with it.
     const int row = (warp - kWarpNorm) * 32 + lane;
-    for (int i = 0; i < ntiles; ++i) {
+    int u = u0, tl = tl0, seg = -1;
+    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
       if (__any_sync(0xffffffffu, *s_abort)) break;
+      if constexpr (KV8) {
+        if (i == 0 || tl == 0) {
+          // the unit's query as E4M3 terms for the tensor cores
+          ++seg;
+          const int qb = seg & 1;
+          const bool qok = __all_sync(0xffffffffu,
+                                      mbar_wait(&qfull[qb], (seg >> 1) & 1) &&
+                                          (seg < 2 || mbar_wait(&q8empty[qb], ((seg >> 1) - 1) & 1)));
+          if (!qok) {
+            set_abort(s_abort, p.flags);
+            break;
+          }
+          build_q8_terms<G>(sQ + qb * kQBufBytes, sQ8 + qb * kQ8BufBytes, row);
+          fence_proxy_async_smem();  // the terms are read by the tensor cores
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&q8full[qb]);
+            mbar_arrive(&qempty[qb]);
+          }
+        }
+      }
       const int s = static_cast<int>(i % kStages);
       const int ns = static_cast<int>(i % kNormSlots);
       const bool ok = __all_sync(0xffffffffu,
@@ -573,30 +793,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // chunk order rotated by row so 8 neighbouring rows hit 8 different bank groups
       // (the swizzle permutes 16-byte chunks within a row; the order does not matter)
-      const uint8_t *rowp = sK + s * kTileBytes + row * 128;
-      float a[8];
+      const uint8_t *st = sK + s * C::stage_bytes;
+      const uint8_t *rowp = st + row * 128;
+      float rk, vsc = 0.0f, done;
+      if constexpr (KV8) {
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) a[c] = 0.0f;
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(rowp + (c ^ (row & 7)) * 16);
+          sq_acc_e4m3x4(x.x, a[0], a[1]);
+          sq_acc_e4m3x4(x.y, a[2], a[3]);
+          sq_acc_e4m3x4(x.z, a[0], a[1]);
+          sq_acc_e4m3x4(x.w, a[2], a[3]);
+        }
+        const float ks = reinterpret_cast<const float *>(st + C::tile_bytes)[row];
+        vsc = reinterpret_cast<const float *>(st + C::tile_bytes + C::scale_bytes)[row];
+        const float ss = (a[0] + a[1]) + (a[2] + a[3]);
+        const float dep = ss + ks + vsc;  // every lane's value depends on all of its reads
+        done = __shfl_sync(0xffffffffu, dep, 0) + __shfl_sync(0xffffffffu, dep, 31);
+        rk = ks * rsqrtf(ks * ks * (ss * (1.0f / kHeadDim)) + p.eps);
+      } else {
+        float a[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int pc = (c ^ (row & 7)) * 16;
-        const uint4 x0 = *reinterpret_cast<const uint4 *>(rowp + pc);
-        const uint4 x1 = *reinterpret_cast<const uint4 *>(rowp + kHalfBytes + pc);
-        sq_acc_bf16x2(x0.x, a[0], a[1]);
-        sq_acc_bf16x2(x0.y, a[2], a[3]);
-        sq_acc_bf16x2(x0.z, a[4], a[5]);
-        sq_acc_bf16x2(x0.w, a[6], a[7]);
-        sq_acc_bf16x2(x1.x, a[0], a[1]);
-        sq_acc_bf16x2(x1.y, a[2], a[3]);
-        sq_acc_bf16x2(x1.z, a[4], a[5]);
-        sq_acc_bf16x2(x1.w, a[6], a[7]);
+        for (int c = 0; c < 8; ++c) a[c] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int pc = (c ^ (row & 7)) * 16;
+          const uint4 x0 = *reinterpret_cast<const uint4 *>(rowp + pc);
+          const uint4 x1 = *reinterpret_cast<const uint4 *>(rowp + C::half_bytes + pc);
+          sq_acc_bf16x2(x0.x, a[0], a[1]);
+          sq_acc_bf16x2(x0.y, a[2], a[3]);
+          sq_acc_bf16x2(x0.z, a[4], a[5]);
+          sq_acc_bf16x2(x0.w, a[6], a[7]);
+          sq_acc_bf16x2(x1.x, a[0], a[1]);
+          sq_acc_bf16x2(x1.y, a[2], a[3]);
+          sq_acc_bf16x2(x1.z, a[4], a[5]);
+          sq_acc_bf16x2(x1.w, a[6], a[7]);
+        }
+        // every lane's sum depends on all of its reads of the stage
+        const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+        done = __shfl_sync(0xffffffffu, ss, 0) + __shfl_sync(0xffffffffu, ss, 31);
+        rk = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
       }
-      // every lane's sum depends on all of its reads of the stage
-      const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-      const float done = __shfl_sync(0xffffffffu, ss, 0) + __shfl_sync(0xffffffffu, ss, 31);
       __syncwarp();
       if (lane == 0) mbar_arrive_after(&empty[s], done);
-      s_rk[ns * kTileKeys + row] = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+      s_rk[ns * kTileKeys + row] = rk;
+      if constexpr (KV8) s_vs[ns * kTileKeys + row] = vsc;
       __syncwarp();
       if (lane == 0) mbar_arrive(&rkfull[ns]);
     }
@@ -624,31 +866,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_abort(s_abort, p.flags);
         break;
       }
-      const WSlot<G> &ws = wslots[slot];
+      const WSlot<G, KV8> &ws = wslots[slot];
       const int row0 = ws.row0, m = ws.m;
       for (int e0 = 0; e0 < m; e0 += 4) {
         uint2 raw[4];
         float wv[4][HPW];
+        float vsr[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           // rows past m are not this tile's: skip them (weight 0, value 0)
           const int e = e0 + r;
-          raw[r] = e < m ? *reinterpret_cast<const uint2 *>(sRing + ((row0 + e) & (kRing - 1)) * kRowBytes + lane * 8)
-                         : make_uint2(0u, 0u);
+          const uint8_t *vr = sRing + ((row0 + e) & (kRing - 1)) * kRowBytes;
+          if constexpr (KV8) {
+            raw[r] = make_uint2(e < m ? *reinterpret_cast<const uint32_t *>(vr + lane * 4) : 0u, 0u);
+            vsr[r] = e < m ? ws.vs[e] : 0.0f;
+          } else {
+            raw[r] = e < m ? *reinterpret_cast<const uint2 *>(vr + lane * 8) : make_uint2(0u, 0u);
+          }
 #pragma unroll
           for (int hh = 0; hh < HPW; ++hh) wv[r][hh] = e < m ? ws.w[e][aw + 4 * hh] : 0.0f;
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const float v0 = bf16lo(raw[r].x), v1 = bf16hi(raw[r].x), v2 = bf16lo(raw[r].y),
-                      v3 = bf16hi(raw[r].y);
+          float v0, v1, v2, v3;
+          if constexpr (KV8) {
+            e4m3x4_to_f32(raw[r].x, v0, v1, v2, v3);
+          } else {
+            v0 = bf16lo(raw[r].x);
+            v1 = bf16hi(raw[r].x);
+            v2 = bf16lo(raw[r].y);
+            v3 = bf16hi(raw[r].y);
+          }
 #pragma unroll
           for (int hh = 0; hh < HPW; ++hh) {
             const float w = wv[r][hh];
-            acc[hh][0] = fmaf(w, v0, acc[hh][0]);
-            acc[hh][1] = fmaf(w, v1, acc[hh][1]);
-            acc[hh][2] = fmaf(w, v2, acc[hh][2]);
-            acc[hh][3] = fmaf(w, v3, acc[hh][3]);
+            const float wq = KV8 ? w * vsr[r] : w;  // the weight of the decoded codes
+            acc[hh][0] = fmaf(wq, v0, acc[hh][0]);
+            acc[hh][1] = fmaf(wq, v1, acc[hh][1]);
+            acc[hh][2] = fmaf(wq, v2, acc[hh][2]);
+            acc[hh][3] = fmaf(wq, v3, acc[hh][3]);
             den[hh] += w;
           }
         }
@@ -763,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kWarpMma) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::tmem_cols);
   }
 }
 
@@ -781,11 +1037,12 @@ __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t his
   for (int64_t i = t; i < n_arrivals; i += stride) arrivals[i] = 0;
 }
 
-template <int G>
+template <int G, bool KV8>
 cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_q,
+                                 const CUtensorMap &tm_ks, const CUtensorMap &tm_vs,
                                  const FullParams &p, int64_t units, cudaStream_t stream) {
-  const int smem = Smem<G>::alloc;
-  cudaError_t e = cudaFuncSetAttribute(full_decode_kernel<G>,
+  const int smem = Smem<G, KV8>::alloc;
+  cudaError_t e = cudaFuncSetAttribute(full_decode_kernel<G, KV8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t hist_vecs = p.hist ? units * kHistBins / 4 : 0;
@@ -795,8 +1052,8 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
                  dim3(256), 0, stream, 0u, reinterpret_cast<uint4 *>(p.hist), hist_vecs,
                  p.arrivals, 4 * units);
   if (e != cudaSuccess) return e;
-  return launch_pdl(full_decode_kernel<G>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
-                    static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, p);
+  return launch_pdl(full_decode_kernel<G, KV8>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
+                    static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, tm_ks, tm_vs, p);
 }
 
 }  // namespace
@@ -829,7 +1086,8 @@ int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count) {
                                      full_records_bytes(units, G, sm_count));
 }
 
-cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
+cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
+                               const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
                                const void *v_cache, float *sel_scores,
                                uint32_t *sel_hist, void *workspace, int32_t *arrivals,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
@@ -857,8 +1115,15 @@ cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap
   p.rec_stride = full_record_floats(G);
   p.alpha = alpha;
   p.eps = eps;
-  if (G == 4) return launch_full_decode_t<4>(tm_k, tm_q, p, sp.units, stream);
-  if (G == 8) return launch_full_decode_t<8>(tm_k, tm_q, p, sp.units, stream);
+  if (kv8) {
+    if (!tm_ks || !tm_vs) return cudaErrorInvalidValue;
+    if (G == 4) return launch_full_decode_t<4, true>(tm_k, tm_q, *tm_ks, *tm_vs, p, sp.units, stream);
+    if (G == 8) return launch_full_decode_t<8, true>(tm_k, tm_q, *tm_ks, *tm_vs, p, sp.units, stream);
+    return cudaErrorInvalidValue;
+  }
+  // the bf16 kernel does not read the scale maps
+  if (G == 4) return launch_full_decode_t<4, false>(tm_k, tm_q, tm_k, tm_k, p, sp.units, stream);
+  if (G == 8) return launch_full_decode_t<8, false>(tm_k, tm_q, tm_k, tm_k, p, sp.units, stream);
   return cudaErrorInvalidValue;
 }
 

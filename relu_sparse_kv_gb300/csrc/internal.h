@@ -69,7 +69,9 @@ size_t full_workspace_bytes(int64_t units, int G, int sm_count);
 // The arrival counters (4 per unit) at the end of the full-decode workspace (zeroed per call).
 int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count);
 
-cudaError_t launch_full_decode(int G, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
+// kv8: 8-bit E4M3 caches; tm_ks / tm_vs then map the K and V scales as [units, ncap] fp32.
+cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
+                               const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
                                const void *v_cache, float *sel_scores,
                                uint32_t *sel_hist, void *workspace, int32_t *arrivals,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
@@ -84,8 +86,9 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
                           int sm_count, cudaStream_t stream);
 
 size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride);
+// k_scales / v_scales: per-token scales of 8-bit E4M3 caches, or both null for bf16 caches.
 cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
-                                 const int32_t *idx, int idx_stride, const int32_t *count,
+                                 const float *k_scales, const float *v_scales, const int32_t *idx, int idx_stride, const int32_t *count,
                                  int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
                                  float *out, void *workspace, uint32_t *flags, int sm_count,
                                  cudaStream_t stream);

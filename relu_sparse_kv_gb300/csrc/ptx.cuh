@@ -161,6 +161,16 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint3
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// The same with f16 operands.
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 // Four 8x8 b16 matrices from shared memory; lane l gives the address of row l % 8 of
 // matrix l / 8.
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
@@ -177,6 +187,20 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t sad
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two floats as f16x2 (round to nearest even), first in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes (low byte first) as f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t c) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
   return r;
 }
 
@@ -256,6 +280,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit E4M3 A and B and fp32 accumulation
+// (kind::f8f6f4; K = 32 per instruction).
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile(
@@ -285,6 +321,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor for kind::f8f6f4: E4M3 A and B (format code 0, K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)            // D format: f32
+         | (0u << 7)          // A format: E4M3
+         | (0u << 10)         // B format: E4M3
+         | ((N >> 3) << 17)   // N / 8
+         | ((M >> 4) << 24);  // M / 16
+}
+
 // 32 lanes x 4 consecutive 32-bit columns (one TMEM lane per thread).
 __device__ __forceinline__ void tmem_load_x4(uint32_t taddr, uint32_t (&r)[4]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
@@ -297,6 +342,16 @@ __device__ __forceinline__ void tmem_load_x8(uint32_t taddr, uint32_t (&r)[8]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_load_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns.
@@ -337,6 +392,55 @@ __device__ __forceinline__ void sq_acc_bf16x2(uint32_t w, float &a, float &b) {
       "fma.rn.f32.bf16 %1, hi, hi, %1;\n\t}"
       : "+f"(a), "+f"(b)
       : "r"(w));
+}
+
+// 8-bit E4M3 codes (OCP FP8: bias 7, no infinities, S.1111.111 NaN).  Every E4M3 value is
+// exact in f16, and so are the squares and products formed below in fp32.
+
+// a += c0^2 + c2^2, b += c1^2 + c3^2 for the four codes c0..c3 (lowest byte first) of w.
+__device__ __forceinline__ void sq_acc_e4m3x4(uint32_t w, float &a, float &b) {
+  asm("{\n\t.reg .b16 p0, p1, l0, h0, l1, h1;\n\t.reg .b32 f0, f1;\n\t"
+      "mov.b32 {p0, p1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 f0, p0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 f1, p1;\n\t"
+      "mov.b32 {l0, h0}, f0;\n\t"
+      "mov.b32 {l1, h1}, f1;\n\t"
+      "fma.rn.f32.f16 %0, l0, l0, %0;\n\t"
+      "fma.rn.f32.f16 %1, h0, h0, %1;\n\t"
+      "fma.rn.f32.f16 %0, l1, l1, %0;\n\t"
+      "fma.rn.f32.f16 %1, h1, h1, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(w));
+}
+
+// The four codes of w (lowest byte first) as floats.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float &v0, float &v1, float &v2,
+                                              float &v3) {
+  asm("{\n\t.reg .b16 p0, p1, l0, h0, l1, h1;\n\t.reg .b32 f0, f1;\n\t"
+      "mov.b32 {p0, p1}, %4;\n\t"
+      "cvt.rn.f16x2.e4m3x2 f0, p0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 f1, p1;\n\t"
+      "mov.b32 {l0, h0}, f0;\n\t"
+      "mov.b32 {l1, h1}, f1;\n\t"
+      "cvt.f32.f16 %0, l0;\n\t"
+      "cvt.f32.f16 %1, h0;\n\t"
+      "cvt.f32.f16 %2, l1;\n\t"
+      "cvt.f32.f16 %3, h1;\n\t}"
+      : "=f"(v0), "=f"(v1), "=f"(v2), "=f"(v3)
+      : "r"(w));
+}
+
+// Round four floats to E4M3 (nearest, ties to even, saturating at +-448); x0 lands in the
+// lowest byte.
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(w)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return w;
 }
 
 // Order-preserving 32-bit key of a float (-0 folded onto +0): larger float, larger key.

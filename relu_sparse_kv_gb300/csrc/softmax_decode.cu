@@ -300,6 +300,7 @@ struct SpMerge {
 struct SparseParams {
   const uint16_t *q;
   const uint8_t *K, *V;
+  const float *ks, *vs;  // per-token scales of 8-bit caches (else null)
   const int32_t *idx, *count;
   float *out;
   uint32_t *flags;
@@ -312,6 +313,74 @@ struct SparseParams {
 // byte offset of 16-byte piece c of staged row r
 __device__ __forceinline__ uint32_t sp_piece(int r, int c) {
   return static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
+}
+
+// After every warp has written its running max, sum and unnormalised output into mg:
+// combine the warps, then the cluster's CTAs (through distributed shared memory), and
+// write this CTA's share of the unit's G x 128 outputs.
+template <int G, int CL>
+__device__ __forceinline__ void sp_combine(SpMerge<G> &mg, int rank, int64_t u, float *out_base) {
+  cg::cluster_group cluster = cg::this_cluster();
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kSpThreads) {
+    const int h = i / kHeadDim, d = i % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kSpWarps; ++w) M = fmaxf(M, mg.m[w][h]);
+    float L = 0.0f, A = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kSpWarps; ++w) {
+        const float f = exp2f(mg.m[w][h] - M);
+        L = fmaf(mg.l[w][h], f, L);
+        A = fmaf(mg.acc[w][h][d], f, A);
+      }
+    }
+    mg.ca[h][d] = A;
+    if (d == 0) {
+      mg.cm[h] = M;
+      mg.cl[h] = L;
+    }
+  }
+  // the cluster's CTAs each finish their share of the outputs from all the CTAs' states
+  cluster.sync();
+  constexpr int per = G * kHeadDim / CL;  // outputs of this CTA (at most 4 per thread)
+  static_assert(per <= 4 * kSpThreads, "at most 4 outputs per thread");
+  float res[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    res[k] = 0.0f;
+    const int li = threadIdx.x + k * kSpThreads;
+    if (li < per) {
+      const int i = rank * per + li;
+      const int h = i / kHeadDim, d = i % kHeadDim;
+      float cmv[CL];
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+        cmv[c] = cluster.map_shared_rank(&mg, c)->cm[h];
+        M = fmaxf(M, cmv[c]);
+      }
+      float L = 0.0f, A = 0.0f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+          const SpMerge<G> *o2 = cluster.map_shared_rank(&mg, c);
+          const float f = exp2f(cmv[c] - M);
+          L = fmaf(o2->cl[h], f, L);
+          A = fmaf(o2->ca[h][d], f, A);
+        }
+      }
+      res[k] = L > 0.0f ? A / L : 0.0f;
+    }
+  }
+  cluster_arrive();  // done reading the other CTAs' shared memory
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int li = threadIdx.x + k * kSpThreads;
+    if (li < per) out_base[u * G * kHeadDim + rank * per + li] = res[k];
+  }
+  cluster_wait();  // and they are done reading this one's
 }
 
 template <int G, int CL>
@@ -453,66 +522,205 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
       mg.acc[warp][2 * t + 1][16 * i + g + 8] = o[i][3];
     }
   }
+  sp_combine<G, CL>(mg, rank, u, p.out);
+}
+
+// 8-bit caches: E4M3 codes (128-byte rows) with one fp32 scale per token.  Per block of 16
+// selected rows a warp stages the K and V code rows (16-byte pieces permuted by row % 8)
+// and looks up their scales, then
+//   S = (Q / 2^e) . codes^T as f16 m16n8k16 MMAs (2^e a power of two per head with
+//       |q / 2^e| < 256, so the f16 query is the bf16 query exactly for every element
+//       at least 2^-24 of its head's largest; each lane widens its own pairs of codes to
+//       f16, exactly);
+//   z = tau2 * 2^e * ks_j * S, the same online softmax as above;
+//   O += (p_j * vs_j) * codes_j on the CUDA cores in fp32 (lane: dims 4 lane .. +3 of
+//       every head), l sums p_j.
+constexpr int kSp8Row = kHeadDim;                              // bytes per 8-bit row
+constexpr int kSp8Stage = 2 * kSpBlock * kSp8Row + kSpBlock * 8 * 4;  // K, V, weights[16][8]
+
+__device__ __forceinline__ uint32_t sp8_piece(int r, int c) {
+  return static_cast<uint32_t>(r * kSp8Row + ((c ^ (r & 7)) << 4));
+}
+
+template <int G, int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
+    sparse_decode_e4m3_kernel(const SparseParams p) {
+  pdl_wait_primary();  // the selection and the query are complete
+  pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t smem[];  // staged rows, then the merge state
+  SpMerge<G> &mg = *reinterpret_cast<SpMerge<G> *>(smem);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int64_t u = blockIdx.x / CL;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  int cnt = p.count[u];
+  cnt = cnt < 0 ? 0 : (cnt > p.idx_stride ? p.idx_stride : cnt);
+  const int32_t *idx = p.idx + u * p.idx_stride;
+  const uint8_t *Ku = p.K + u * p.ncap * kSp8Row;
+  const uint8_t *Vu = p.V + u * p.ncap * kSp8Row;
+  const float *ksu = p.ks + u * p.ncap;
+  const float *vsu = p.vs + u * p.ncap;
+  uint8_t *sK = smem + warp * kSp8Stage;
+  uint8_t *sV = sK + kSpBlock * kSp8Row;
+  float *sW = reinterpret_cast<float *>(sV + kSpBlock * kSp8Row);  // [16 rows][8 heads]
+
+  // query of head g as the f16 A operand of S: dims 16ks + 2t, +1 (qa0) and +8, +9 (qa2),
+  // divided by 2^e; the head's 4 lanes together hold all 128 dims
+  uint32_t qa0[8], qa2[8];
+  float escale;
+  {
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (u * G + (g < G ? g : 0)) * kHeadDim);
+    uint32_t w0[8], w2[8];
+    float mx = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      w0[ks] = g < G ? qrow[8 * ks + t] : 0u;
+      w2[ks] = g < G ? qrow[8 * ks + 4 + t] : 0u;
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(w0[ks])), fabsf(bf16hi(w0[ks]))),
+                           fmaxf(fabsf(bf16lo(w2[ks])), fabsf(bf16hi(w2[ks])))));
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 7;
+    e = e < -120 ? -120 : (e > 120 ? 120 : e);
+    escale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa0[ks] = pack_f16x2(bf16lo(w0[ks]) * inv, bf16hi(w0[ks]) * inv);
+      qa2[ks] = pack_f16x2(bf16lo(w2[ks]) * inv, bf16hi(w2[ks]) * inv);
+    }
+  }
+  const float zs = p.tau * kLog2e * escale;
+  float m = -INFINITY, l = 0.0f;  // head g's running max (base 2) and sum
+  float acc[G][4];                // dims 4 lane .. 4 lane + 3 of every head
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
+
+  const int r0 = rank * p.rows_per_cta;
+  const int r1 = min(cnt, r0 + p.rows_per_cta);
+  for (int b0 = r0 + warp * kSpBlock; b0 < r1; b0 += kSpWarps * kSpBlock) {
+    // lane r < 16 looks up row r and its two scales (absent past the count, or for an
+    // index outside [0, n), which is flagged)
+    int64_t j = -1;
+    float ksr = 0.0f, vsr = 0.0f;
+    if (lane < kSpBlock && b0 + lane < r1) {
+      const int32_t jj = idx[b0 + lane];
+      if (jj < 0 || static_cast<int64_t>(jj) >= p.n) {
+        atomicOr(p.flags, kFlagIndexRange);
+      } else {
+        j = jj;
+        ksr = ksu[j];
+        vsr = vsu[j];
+      }
+    }
+    const uint32_t present = __ballot_sync(0xffffffffu, j >= 0);  // bit r: row r
+    // each copy instruction moves four whole rows: lanes 8k .. 8k + 7 the 8 pieces of one
+    const int piece = lane & 7;
+#pragma unroll
+    for (int k = 0; k < kSpBlock / 4; ++k) {
+      const int r = 4 * k + (lane >> 3);
+      const int64_t jr = __shfl_sync(0xffffffffu, j, r);
+      const uint32_t nbytes = jr >= 0 ? 16u : 0u;
+      const int64_t off = (jr >= 0 ? jr : 0) * kSp8Row + piece * 16;
+      cp_async16_zfill(sK + sp8_piece(r, piece), Ku + off, nbytes);
+      cp_async16_zfill(sV + sp8_piece(r, piece), Vu + off, nbytes);
+    }
+    cp_async_wait_all();
+    __syncwarp();
+
+    // S for rows 0-7 (s0) and 8-15 (s1): B operand = codes of row g (8 + g), dims
+    // 16ks + 2t, +1 and 16ks + 2t + 8, +9
+    float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint8_t *ra = sK + sp8_piece(g, ks) + 2 * t;
+      const uint8_t *rb = sK + sp8_piece(8 + g, ks) + 2 * t;
+      const uint32_t a0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ra));
+      const uint32_t a1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ra + 8));
+      const uint32_t b0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(rb));
+      const uint32_t b1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(rb + 8));
+      mma_16816_f16(s0, qa0[ks], 0u, qa2[ks], 0u, a0, a1);
+      mma_16816_f16(s1, qa0[ks], 0u, qa2[ks], 0u, b0, b1);
+    }
+    // online softmax for head g over rows 2t, 2t+1 (s0) and 8+2t, 9+2t (s1)
+    const int rr[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    const float sv[4] = {s0[0], s0[1], s1[0], s1[1]};
+    float z[4], vrow[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float kr = __shfl_sync(0xffffffffu, ksr, rr[k]);
+      vrow[k] = __shfl_sync(0xffffffffu, vsr, rr[k]);
+      z[k] = (present >> rr[k]) & 1u ? zs * kr * sv[k] : -INFINITY;
+    }
+    float mx = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    float sc = 1.0f, pz[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (mn != -INFINITY) {
+      sc = exp2f(m - mn);  // 0 while nothing had been seen
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pz[k] = exp2f(z[k] - mn);
+    }
+    float ps = (pz[0] + pz[1]) + (pz[2] + pz[3]);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+    m = mn;
+    l = fmaf(l, sc, ps);
+    // the rows' weights times their V scales, for every lane
+    if (g < G) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sW[rr[k] * 8 + g] = pz[k] * vrow[k];
+    }
+    float sch[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) sch[h] = __shfl_sync(0xffffffffu, sc, 4 * h);
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      acc[h][0] *= sch[h];
+      acc[h][1] *= sch[h];
+      acc[h][2] *= sch[h];
+      acc[h][3] *= sch[h];
+    }
+    const int last = 32 - __clz(present);  // rows past the last present one weigh 0
+    for (int r = 0; r < last; ++r) {
+      float v0, v1, v2, v3;
+      e4m3x4_to_f32(*reinterpret_cast<const uint32_t *>(sV + sp8_piece(r, lane >> 2) + (lane & 3) * 4),
+                    v0, v1, v2, v3);
+      const float4 wa = *reinterpret_cast<const float4 *>(sW + r * 8);
+      float wr[8] = {wa.x, wa.y, wa.z, wa.w, 0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (G == 8) {
+        const float4 wb = *reinterpret_cast<const float4 *>(sW + r * 8 + 4);
+        wr[4] = wb.x;
+        wr[5] = wb.y;
+        wr[6] = wb.z;
+        wr[7] = wb.w;
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        acc[h][0] = fmaf(wr[h], v0, acc[h][0]);
+        acc[h][1] = fmaf(wr[h], v1, acc[h][1]);
+        acc[h][2] = fmaf(wr[h], v2, acc[h][2]);
+        acc[h][3] = fmaf(wr[h], v3, acc[h][3]);
+      }
+    }
+    __syncwarp();  // the stage is read before the next block's copies land in it
+  }
+
+  // this warp's state into shared memory (reusing the stages: wait for every warp)
   __syncthreads();
-  for (int i = threadIdx.x; i < G * kHeadDim; i += kSpThreads) {
-    const int h = i / kHeadDim, d = i % kHeadDim;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kSpWarps; ++w) M = fmaxf(M, mg.m[w][h]);
-    float L = 0.0f, A = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kSpWarps; ++w) {
-        const float f = exp2f(mg.m[w][h] - M);
-        L = fmaf(mg.l[w][h], f, L);
-        A = fmaf(mg.acc[w][h][d], f, A);
-      }
-    }
-    mg.ca[h][d] = A;
-    if (d == 0) {
-      mg.cm[h] = M;
-      mg.cl[h] = L;
-    }
+  if (t == 0 && g < G) {
+    mg.m[warp][g] = m;
+    mg.l[warp][g] = l;
   }
-  // the cluster's CTAs each finish their share of the outputs from all the CTAs' states
-  cluster.sync();
-  constexpr int per = G * kHeadDim / CL;  // outputs of this CTA (at most 4 per thread)
-  static_assert(per <= 4 * kSpThreads, "at most 4 outputs per thread");
-  float res[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    res[k] = 0.0f;
-    const int li = threadIdx.x + k * kSpThreads;
-    if (li < per) {
-      const int i = rank * per + li;
-      const int h = i / kHeadDim, d = i % kHeadDim;
-      float cmv[CL];
-      float M = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < CL; ++c) {
-        cmv[c] = cluster.map_shared_rank(&mg, c)->cm[h];
-        M = fmaxf(M, cmv[c]);
-      }
-      float L = 0.0f, A = 0.0f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int c = 0; c < CL; ++c) {
-          const SpMerge<G> *o2 = cluster.map_shared_rank(&mg, c);
-          const float f = exp2f(cmv[c] - M);
-          L = fmaf(o2->cl[h], f, L);
-          A = fmaf(o2->ca[h][d], f, A);
-        }
-      }
-      res[k] = L > 0.0f ? A / L : 0.0f;
-    }
-  }
-  cluster_arrive();  // done reading the other CTAs' shared memory
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int li = threadIdx.x + k * kSpThreads;
-    if (li < per) p.out[u * G * kHeadDim + rank * per + li] = res[k];
-  }
-  cluster_wait();  // and they are done reading this one's
+  for (int h = 0; h < G; ++h)
+    *reinterpret_cast<float4 *>(&mg.acc[warp][h][4 * lane]) =
+        make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+  sp_combine<G, CL>(mg, rank, u, p.out);
 }
 
 // ----------------------------------------------------------------------------- window
@@ -597,10 +805,11 @@ cudaError_t launch_staged(void (*kernel)(Params), dim3 grid, const Params &p, cu
   return launch_pdl(kernel, grid, dim3(kThreads), kStageBytes, stream, 0u, p);
 }
 
+template <bool KV8>
 cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const SparseParams &p,
                             cudaStream_t stream) {
-  constexpr int bytes = kSpWarps * kSpStage;
-  static_assert(sizeof(SpMerge<8>) <= bytes, "the merge state fits the staging space");
+  constexpr int stage = kSpWarps * (KV8 ? kSp8Stage : kSpStage);
+  constexpr int bytes = stage > static_cast<int>(sizeof(SpMerge<8>)) ? stage : static_cast<int>(sizeof(SpMerge<8>));
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, grid, dim3(kSpThreads), bytes, stream, 0u, p);
@@ -608,11 +817,19 @@ cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const Spars
 
 template <int G>
 cudaError_t launch_sparse_g(dim3 grid, const SparseParams &p, cudaStream_t stream) {
+  if (p.ks != nullptr) {
+    switch (p.cl) {
+      case 8: return launch_sparse_t<true>(sparse_decode_e4m3_kernel<G, 8>, grid, p, stream);
+      case 4: return launch_sparse_t<true>(sparse_decode_e4m3_kernel<G, 4>, grid, p, stream);
+      case 2: return launch_sparse_t<true>(sparse_decode_e4m3_kernel<G, 2>, grid, p, stream);
+      default: return launch_sparse_t<true>(sparse_decode_e4m3_kernel<G, 1>, grid, p, stream);
+    }
+  }
   switch (p.cl) {
-    case 8: return launch_sparse_t(sparse_decode_kernel<G, 8>, grid, p, stream);
-    case 4: return launch_sparse_t(sparse_decode_kernel<G, 4>, grid, p, stream);
-    case 2: return launch_sparse_t(sparse_decode_kernel<G, 2>, grid, p, stream);
-    default: return launch_sparse_t(sparse_decode_kernel<G, 1>, grid, p, stream);
+    case 8: return launch_sparse_t<false>(sparse_decode_kernel<G, 8>, grid, p, stream);
+    case 4: return launch_sparse_t<false>(sparse_decode_kernel<G, 4>, grid, p, stream);
+    case 2: return launch_sparse_t<false>(sparse_decode_kernel<G, 2>, grid, p, stream);
+    default: return launch_sparse_t<false>(sparse_decode_kernel<G, 1>, grid, p, stream);
   }
 }
 
@@ -626,7 +843,7 @@ size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride) {
 }
 
 cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
-                                 const int32_t *idx, int idx_stride, const int32_t *count,
+                                 const float *k_scales, const float *v_scales, const int32_t *idx, int idx_stride, const int32_t *count,
                                  int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
                                  float *out, void *workspace, uint32_t *flags, int sm_count,
                                  cudaStream_t stream) {
@@ -637,6 +854,8 @@ cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, cons
   p.q = static_cast<const uint16_t *>(q);
   p.K = static_cast<const uint8_t *>(k_cache);
   p.V = static_cast<const uint8_t *>(v_cache);
+  p.ks = k_scales;
+  p.vs = v_scales;
   p.idx = idx;
   p.count = count;
   p.out = out;
