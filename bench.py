@@ -30,7 +30,22 @@ if ROOT not in sys.path:
 
 METRIC = "decode attention tokens/s and needed-byte HBM GB/s (% of roofline) at 32k–128k"
 ROW_BYTES = 128 * 2          # one bf16 key or value row (head_dim 128)
+ROW_BYTES_E4M3 = 128 + 4     # one 8-bit row (E4M3 codes) and its fp32 scale
 TOPK, RECENT = 1024, 128
+L2_BYTES = 129 * 10**6       # GB300 L2
+
+
+def replicas_for(step_bytes: int) -> int:
+    """Copies of the caches that the timed steps rotate through, so a step's cache rows
+    were last touched at least 1.5 L2 sizes of other reads ago (1 when a step alone
+    reads that much)."""
+    if step_bytes >= 1.5 * L2_BYTES:
+        return 1
+    return 1 + -(-int(1.5 * L2_BYTES) // max(1, step_bytes))
+
+
+def row_bytes(kv: str) -> int:
+    return ROW_BYTES_E4M3 if kv == "e4m3" else ROW_BYTES
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -40,14 +55,15 @@ def state_bytes(c: int, batch: int, bytes_per_elem: int, d_kv: int, tokens: int,
     return c * batch * bytes_per_elem * d_kv * tokens * layers
 
 
-def full_layer_needed_bytes(units: int, n: int, total_survivors: int) -> int:
-    """Bytes a full layer must read: every K row, and the V rows of surviving keys only."""
-    return units * n * ROW_BYTES + total_survivors * ROW_BYTES
+def full_layer_needed_bytes(units: int, n: int, total_survivors: int, kv: str = "bf16") -> int:
+    """Bytes a full layer must read: every K row, and the V rows of surviving keys only
+    (8-bit caches: each row's scale with it)."""
+    return units * n * row_bytes(kv) + total_survivors * row_bytes(kv)
 
 
-def sparse_layer_needed_bytes(total_selected: int) -> int:
+def sparse_layer_needed_bytes(total_selected: int, kv: str = "bf16") -> int:
     """Bytes a sparse layer must read: the selected K and V rows."""
-    return 2 * total_selected * ROW_BYTES
+    return 2 * total_selected * row_bytes(kv)
 
 
 def window_layer_needed_bytes(units: int, valid_rows: int) -> int:
@@ -160,7 +176,8 @@ def static_config(cfg_id: int, batch=None, ctx=None) -> dict:
     return {"workload": workload_name(cfg, batch, ctx),
             "batch": cfg["B"] if batch is None else batch,
             "ctx_len": cfg["n"] if ctx is None else ctx,
-            "q_heads": gen.HQ, "kv_heads": gen.HKV, "head_dim": gen.HEAD_DIM,
+            "q_heads": cfg.get("Hq", gen.HQ), "kv_heads": cfg.get("Hkv", gen.HKV),
+            "head_dim": gen.HEAD_DIM, "kv_cache": cfg.get("kv", "bf16"),
             "full_layers": len(fulls), "sparse_layers": sum(fulls),
             "window_layers": len(wins), "accumulate": "f32"}
 
@@ -228,6 +245,13 @@ def job_throughput(world: int, batch: int, seconds_per_step: float) -> float:
     return world * batch / seconds_per_step
 
 
+def _oracle_kv(oracle, fl):
+    """The layer's caches as float64 for the oracle (8-bit caches decoded: scale * code)."""
+    if fl.kv == "e4m3":
+        return oracle.dequant_e4m3(fl.K, fl.Ks), oracle.dequant_e4m3(fl.V, fl.Vs)
+    return oracle.f64(fl.K), oracle.f64(fl.V)
+
+
 def run_reference(args):
     """The fp64 CPU oracle on a bounded sample: every layer of the step for a few sequences."""
     world, rank, _ = _dist()
@@ -244,8 +268,8 @@ def run_reference(args):
     # widen to fp64 once, outside the timed region
     prep = []
     for fl in fls:
-        prep.append((oracle.f64(fl.q), oracle.f64(fl.K), oracle.f64(fl.V),
-                     [oracle.f64(qs) for qs in fl.sparse_q], fl.n))
+        K, V = _oracle_kv(oracle, fl)
+        prep.append((oracle.f64(fl.q), K, V, [oracle.f64(qs) for qs in fl.sparse_q], fl.n))
     wprep = [(oracle.f64(w.q), oracle.f64(w.K), oracle.f64(w.V), w.pos) for w in wls]
 
     def step():
@@ -290,7 +314,8 @@ def cpu_baseline(cfg_id: int, budget_s: float = 12.0):
     cfg = gen.CONFIGS[cfg_id]
     B = cfg["B"] if cfg_id != 5 else 1
     fl = next(gen.config_full_layers(cfg_id, seed=0, B=B))
-    q, K, V = oracle.f64(fl.q), oracle.f64(fl.K), oracle.f64(fl.V)
+    q = oracle.f64(fl.q)
+    K, V = _oracle_kv(oracle, fl)
     qss = [oracle.f64(x) for x in fl.sparse_q]
     reps = 0
     t0 = time.perf_counter()
@@ -342,13 +367,20 @@ def main():
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
+    def to_dev_raw(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
     layers = []
     for fl in fls:
         B, Hq, D = fl.q.shape
         Hkv, ncap = fl.K.shape[1], fl.K.shape[2]
         shape = E.Shape(B, Hq, Hkv, D, fl.n, ncap)
-        L = dict(fl=fl, shape=shape, q=to_dev(fl.q), K=to_dev(fl.K), V=to_dev(fl.V),
-                 qs=[to_dev(x) for x in fl.sparse_q])
+        if fl.kv == "e4m3":
+            L = dict(fl=fl, shape=shape, q=to_dev(fl.q), K=to_dev_raw(fl.K), V=to_dev_raw(fl.V),
+                     Ks=to_dev_raw(fl.Ks), Vs=to_dev_raw(fl.Vs), qs=[to_dev(x) for x in fl.sparse_q])
+        else:
+            L = dict(fl=fl, shape=shape, q=to_dev(fl.q), K=to_dev(fl.K), V=to_dev(fl.V),
+                     qs=[to_dev(x) for x in fl.sparse_q])
         L["out"] = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
         L["n_surv"] = torch.empty(B, Hkv, dtype=torch.int32, device=dev)
         need_sel = len(fl.sparse_q) > 0
@@ -370,6 +402,11 @@ def main():
                          V=to_dev(wl.V), out=torch.empty(B, Hq, D, dtype=torch.float32, device=dev)))
 
     def full_call(L):
+        if "Ks" in L:
+            E.embla_full_decode_e4m3(L["shape"], L["q"], L["K"], L["Ks"], L["V"], L["Vs"], L["out"],
+                                     L["n_surv"], L["sel"], L["hist"], alpha=1.0, c=1.0, eps=1e-6,
+                                     workspace=L["ws_full"])
+            return
         E.embla_full_decode(L["shape"], L["q"], L["K"], L["V"], L["out"], L["n_surv"], L["sel"],
                             L["hist"], alpha=1.0, c=1.0, eps=1e-6, workspace=L["ws_full"])
 
@@ -379,8 +416,12 @@ def main():
         E.embla_select_topk(L["shape"], L["sel"], L["hist"], L["idx"], L["count"], TOPK, RECENT,
                             workspace=L["ws_sel"])
         for qs, so in zip(L["qs"], L["souts"]):
-            E.embla_sparse_decode(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"], so,
-                                  workspace=L["ws_sp"])
+            if "Ks" in L:
+                E.embla_sparse_decode_e4m3(L["shape"], qs, L["K"], L["Ks"], L["V"], L["Vs"],
+                                           L["idx"], L["count"], so, workspace=L["ws_sp"])
+            else:
+                E.embla_sparse_decode(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"], so,
+                                      workspace=L["ws_sp"])
 
     def window_calls():
         for w in wins:
@@ -393,6 +434,26 @@ def main():
     window_calls()
     torch.cuda.synchronize()
     assert E.embla_device_check() == 0
+
+    # caches smaller than L2: the steps rotate through copies of them (identical contents)
+    step_read = sum(full_layer_needed_bytes(L["shape"].units, L["fl"].n, 0, L["fl"].kv) *
+                    (1 + 2 * len(L["qs"]) * TOPK // max(1, L["fl"].n)) for L in layers)
+    n_rep = replicas_for(step_read)
+    reps = [layers]
+    for _ in range(n_rep - 1):
+        copies = []
+        for L in layers:
+            Lr = dict(L)
+            for key in ("K", "V", "Ks", "Vs"):
+                if key in L:
+                    Lr[key] = L[key].clone()
+            copies.append(Lr)
+        reps.append(copies)
+    for copies in reps[1:]:
+        for L in copies:
+            full_call(L)
+            rest_calls(L)
+    torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
     nl = len(layers)
@@ -416,7 +477,7 @@ def main():
             # the event after a full-layer call is recorded on a side branch of the graph,
             # so the call's kernel and the next one stay directly chained
             def body():
-                for li, L in enumerate(layers):
+                for li, L in enumerate(reps[(i or 0) % n_rep]):
                     if i is not None:
                         ev[i * nl + li][0].record(stream)
                     full_call(L)
@@ -440,12 +501,13 @@ def main():
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps * nl)]
         with torch.cuda.stream(stream):
-            g_full = [capture(lambda L=L: full_call(L)) for L in layers]
-            g_rest = [capture(lambda L=L: rest_calls(L)) for L in layers]
+            g_full = [[capture(lambda L=L: full_call(L)) for L in Ls] for Ls in reps]
+            g_rest = [[capture(lambda L=L: rest_calls(L)) for L in Ls] for Ls in reps]
             g_win = capture(window_calls) if wins else None
 
         def step(timed_i=None):
-            for li, (gf, gr) in enumerate(zip(g_full, g_rest)):
+            r = (timed_i or 0) % n_rep
+            for li, (gf, gr) in enumerate(zip(g_full[r], g_rest[r])):
                 if timed_i is not None:
                     ev[timed_i * nl + li][0].record(stream)
                 gf.replay()
@@ -459,8 +521,10 @@ def main():
     # accounting from this rank's own results
     n_surv_tot = [int(L["n_surv"].sum().item()) for L in layers]
     sel_tot = [int(L["count"].sum().item()) if L["qs"] else 0 for L in layers]
-    full_bytes = [full_layer_needed_bytes(L["shape"].units, L["fl"].n, s) for L, s in zip(layers, n_surv_tot)]
-    sparse_bytes = sum(len(L["qs"]) * sparse_layer_needed_bytes(s) for L, s in zip(layers, sel_tot))
+    full_bytes = [full_layer_needed_bytes(L["shape"].units, L["fl"].n, s, L["fl"].kv)
+                  for L, s in zip(layers, n_surv_tot)]
+    sparse_bytes = sum(len(L["qs"]) * sparse_layer_needed_bytes(s, L["fl"].kv)
+                       for L, s in zip(layers, sel_tot))
     win_bytes = sum(window_layer_needed_bytes(w["shape"].units, min(w["wl"].pos + 1, w["wl"].K.shape[2]))
                     for w in wins)
     needed = sum(full_bytes) + sparse_bytes + win_bytes
@@ -524,23 +588,29 @@ def main():
         n = L0["fl"].n
         h_krow = [pin(L["K"][:, :, n - 1, :].contiguous()) for L in layers]
         h_vrow = [pin(L["V"][:, :, n - 1, :].contiguous()) for L in layers]
+        # 8-bit caches: the appended row's two scales as well
+        h_scales = [(pin(L["Ks"][:, :, n - 1].contiguous()), pin(L["Vs"][:, :, n - 1].contiguous()))
+                    if "Ks" in L else () for L in layers]
         h_wq = [pin(w["q"]) for w in wins]
         h_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in layers]
         h_sout = [[torch.empty_like(x, device="cpu").pin_memory() for x in L["souts"]] for L in layers]
         h_ns = [torch.empty_like(L["n_surv"], device="cpu").pin_memory() for L in layers]
         h_wout = [torch.empty_like(w["out"], device="cpu").pin_memory() for w in wins]
         h2d = sum(x.numel() * x.element_size() for x in h_q + h_krow + h_vrow + h_wq) + \
-            sum(x.numel() * x.element_size() for xs in h_qs for x in xs)
+            sum(x.numel() * x.element_size() for xs in h_qs + h_scales for x in xs)
         d2h = sum(x.numel() * x.element_size() for x in h_out + h_ns + h_wout) + \
             sum(x.numel() * x.element_size() for xs in h_sout for x in xs)
 
-        def e2e_step():
-            for li, L in enumerate(layers):
+        def e2e_step(k):
+            for li, L in enumerate(reps[k % n_rep]):
                 L["q"].copy_(h_q[li], non_blocking=True)
                 for x, hx in zip(L["qs"], h_qs[li]):
                     x.copy_(hx, non_blocking=True)
                 L["K"][:, :, n - 1, :].copy_(h_krow[li], non_blocking=True)
                 L["V"][:, :, n - 1, :].copy_(h_vrow[li], non_blocking=True)
+                if h_scales[li]:
+                    L["Ks"][:, :, n - 1].copy_(h_scales[li][0], non_blocking=True)
+                    L["Vs"][:, :, n - 1].copy_(h_scales[li][1], non_blocking=True)
                 full_call(L)
                 rest_calls(L)
             for wi, w in enumerate(wins):
@@ -555,13 +625,13 @@ def main():
                 h_wout[wi].copy_(w["out"], non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
-        for _ in range(3):
-            e2e_step()
+        for k in range(3):
+            e2e_step(k)
         if world > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        for k in range(args.e2e_steps):
+            e2e_step(k)
         dt = time.perf_counter() - t0
         dt = max_over_ranks(dt, world, dev)
         e2e = {"value": job_throughput(world, batch, dt / args.e2e_steps), "unit": "tokens/s",
@@ -586,15 +656,21 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if layers[0]["fl"].kv == "e4m3" else "bf16",
         "data": "synthetic",
         "config": {**static_config(args.config, args.batch, args.ctx),
                    "launch": ("one CUDA graph per step; events inside it around each full-layer call "
                               "(the closing one on a side branch)"
                               if in_graph_events else
                               "two CUDA graphs per full layer (its call, then the rest); events between them"),
-                   "l2": "not flushed: inputs larger than L2 (each full layer's K cache is "
-                         f"{keys_total * ROW_BYTES // len(layers) / 1e6:.0f} MB)",
+                   "l2": ("not flushed: inputs larger than L2 (each full layer's K cache is "
+                          f"{keys_total * row_bytes(layers[0]['fl'].kv) // len(layers) / 1e6:.0f} MB)"
+                          if n_rep == 1 else
+                          f"not flushed: the steps rotate through {n_rep} copies of the caches "
+                          f"({step_read / 1e6:.0f} MB read per step, smaller than L2), so each "
+                          f"step's rows were last read {(n_rep - 1) * step_read / 1e6:.0f} MB of "
+                          "other reads earlier"),
                    "needed_bytes_per_step": needed,
                    "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),
                    "needed_frac_of_peak": round(needed / (ms_per_step * 1e-3) / 1e9 / peak, 4),

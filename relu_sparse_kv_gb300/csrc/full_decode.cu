@@ -17,9 +17,10 @@
 //              shared-memory ring; the K stage is free once these and the MMAs are done.
 //   warps 2-9  two epilogue warpgroups taking alternate tiles, one thread per key:
 //              s_h = dot_h * alpha*rq_h * rk, sigma = max_h s_h; lists the keys with
-//              sigma > 0 with their ReLU^2 weights in key order; a leader reserves that
-//              many rows of a 256-row V ring (in tile order), and every surviving key's
-//              thread copies its own 256-byte V row into the ring.
+//              sigma > 0 with their ReLU^2 weights in key order; each group takes that
+//              many rows of its own 128-row V ring (in its tile order; every warp of
+//              the group tracks the ring itself, so neither group waits for the other),
+//              and every surviving key's thread copies its own 256-byte V row there.
 //   warp 19    selection scores (when requested): writes each tile's sigma to global
 //              memory and counts it into a shared histogram, flushed when a unit's
 //              stretch ends.
@@ -73,8 +74,11 @@ constexpr int kWarpMma2 = kWarpNorm + 4;           // second MMA issuer (odd til
 constexpr int kWarpHist = kWarpMma2 + 1;           // selection scores and histogram
 constexpr int kMmaWarps = 2;
 constexpr int kThreads = (kWarpHist + 1) * 32;     // 640
-static_assert(kRing >= kTileKeys, "a whole tile of survivors must fit the V ring");
-static_assert((kRing & (kRing - 1)) == 0, "the V ring size is a power of two");
+constexpr int kGroupRing = kRing / kGroups;        // each epilogue group's own V ring
+static_assert(kGroupRing >= kTileKeys, "a whole tile of survivors must fit a group's V ring");
+static_assert((kGroupRing & (kGroupRing - 1)) == 0, "the V ring size is a power of two");
+static_assert(kWSlots % kGroups == 0 && kWSlots >= 4 * kGroups,
+              "a W slot stays with one group; a group's last three tiles keep their slots");
 
 // What differs between bf16 caches (KV8 false) and 8-bit E4M3 caches with per-token
 // scales (KV8 true).
@@ -106,8 +110,9 @@ struct Cfg {
   static_assert(tmem_cols == 256 || tmem_cols == 512, "tensor-memory allocation size");
 };
 
-// One tile's survivors in ascending key order: entry e has its V row in ring row
-// (row0 + e) mod kRing.  Also the tile's selection scores, for the histogram warp.
+// One tile's survivors in ascending key order: entry e has its V row in row
+// (row0 + e) mod kGroupRing of the V ring of the tile's epilogue group.  Also the tile's
+// selection scores, for the histogram warp.
 template <int G, bool KV8>
 struct WSlot {
   int32_t cnt[4];             // survivors per TMEM quarter (32 keys each)
@@ -132,9 +137,8 @@ struct Smem {
   static constexpr int rk_off = hist_off + kHistBins * 4;
   static constexpr int vs_off = rk_off + kNormSlots * kTileKeys * 4;  // V scales beside rk
   static constexpr int misc_off = vs_off + (KV8 ? kNormSlots * kTileKeys * 4 : 0);
-  static constexpr int end_off = misc_off + 64;                 // int64 per W slot, + 2 ring counters
-  static constexpr int bar_off = end_off + (kWSlots + 2) * 8;
-  static constexpr int n_bars = 3 * C::stages + 2 * kAccBufs + 8 + 4 * kWSlots + 2 * kNormSlots;
+  static constexpr int bar_off = misc_off + 64;
+  static constexpr int n_bars = 3 * C::stages + 2 * kAccBufs + 8 + 3 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
   static_assert(alloc <= 227 * 1024, "shared memory per CTA");
@@ -284,12 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_abort = misc + 1;
   volatile int *s_k_issued = misc + 2;
   volatile int *s_q_issued = misc + 3;
-  volatile int *s_v_issued = misc + 4;
-  int *s_ring_oldest = misc + 5;         // oldest tile whose ring rows are not known free
-  volatile int *s_lead_ok = misc + 6;    // [group]: the leader's waits succeeded
-  int64_t *s_end = reinterpret_cast<int64_t *>(smem + L::end_off);  // ring row end per W slot
-  int64_t *s_ring_issued = s_end + kWSlots;  // ring rows reserved so far
-  int64_t *s_ring_freed = s_end + kWSlots + 1;  // ring rows known consumed
+  volatile int *s_varm = misc + 4;       // [W slot]: V-copy phases armed on its barrier
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
   uint64_t *full = bars;                 // K tile landed: [stage][tile parity]
   uint64_t *empty = full + 2 * kStages;  // K tile consumed (MMA and key norms)
@@ -297,8 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acce = accf + kAccBufs;      // accumulator read
   uint64_t *qfull = acce + kAccBufs;     // query rows landed
   uint64_t *qempty = qfull + 2;          // query rows no longer needed
-  uint64_t *adone = qempty + 2;          // ring rows of a tile reserved (orders the groups)
-  uint64_t *wempty = adone + kWSlots;    // survivor list and its V rows consumed
+  uint64_t *wempty = qempty + 2;         // survivor list and its V rows consumed
   uint64_t *vfull = wempty + kWSlots;    // survivor list written and its V rows landed
   uint64_t *sfull = vfull + kWSlots;     // selection scores of a tile written
   uint64_t *rkfull = sfull + kWSlots;    // key norms of a tile written
@@ -338,7 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q8empty[q], kMmaWarps);
     }
     for (int w = 0; w < kWSlots; ++w) {
-      mbar_init(&adone[w], 1);
       mbar_init(&wempty[w], p.sel != nullptr ? 5 : 4);  // accumulators (+ histogram warp)
       mbar_init(&vfull[w], 4);
       mbar_init(&sfull[w], 4);
@@ -350,10 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0;
     *s_k_issued = 0;
     *s_q_issued = 0;
-    *s_v_issued = 0;
-    *s_ring_oldest = 0;
-    *s_ring_issued = 0;
-    *s_ring_freed = 0;
+    for (int w = 0; w < kWSlots; ++w) s_varm[w] = 0;
     fence_barrier_init();
   }
   // Rows G..15 of the query operand feed only MMA columns that are never read; zero
@@ -511,13 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // left waiting at a group barrier that the others have abandoned.
     const int group = (warp - kWarpEpi) >> 2;
     const uint32_t gbar = 1u + static_cast<uint32_t>(group);
-    const bool leader = ((warp - kWarpEpi) & 3) == 0 && lane == 0;
     const int quarter = warp & 3;     // the TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
     const uint32_t lanemask_lt = (1u << lane) - 1u;
     float aq[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) aq[h] = 0.0f;
+    // The group's own V ring: rows reserved so far, and the survivor counts of its last
+    // three tiles (i - 2, i - 4, i - 6), whose rows may still be in use.  Every warp of the
+    // group keeps the same copy (they all see every count), so no warp waits for another.
+    uint8_t *gring = sRing + group * kGroupRing * kRowBytes;
+    int issued = 0, m1 = 0, m2 = 0, m3 = 0;
     int u = u0, tl = tl0;
     int seg = -1;
     for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
@@ -662,46 +660,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < G; ++h) ws.w[e][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
         if constexpr (KV8) ws.vs[e] = vsc;
       }
-      if (leader) {
-        // Reserve m ring rows in tile order: after the previous tile's reservation, and
-        // once the accumulators have freed enough of the ring.
-        bool lok = i == 0 || mbar_wait(&adone[(i - 1) % kWSlots], ((i - 1) / kWSlots) & 1);
-        const int64_t issued = *s_ring_issued;
-        int64_t freed = *s_ring_freed;
-        int oldest = *s_ring_oldest;
-        // this group waited for tile i - kWSlots to be consumed before reusing its slot, so
-        // it and every older tile are done (their slots' row ends are not yet overwritten)
-        while (oldest <= i - kWSlots) {
-          freed = s_end[oldest % kWSlots];
-          ++oldest;
-        }
-        while (lok && issued + m - freed > kRing) {
-          lok = mbar_wait(&wempty[oldest % kWSlots], (oldest / kWSlots) & 1);
-          freed = s_end[oldest % kWSlots];
-          ++oldest;
-        }
-        ws.row0 = static_cast<int32_t>(issued % kRing);
-        ws.m = m;
-        s_end[slot] = issued + m;
-        *s_ring_issued = issued + m;
-        *s_ring_freed = freed;
-        *s_ring_oldest = oldest;
-        s_lead_ok[group] = lok;
-        if (lok) {
-          *s_v_issued = i + 1;
-          mbar_arrive(&adone[slot]);  // the next tile may reserve
-        }
-      }
-      __syncwarp();
-      named_bar_sync(gbar, 128);  // the reservation is published
-      if (!s_lead_ok[group]) {
+      // m rows of the group's ring, in the group's tile order.  Tiles i - 8 and older
+      // were consumed before this tile's slot was taken; wait, oldest first, for the
+      // group's later tiles until the rows in use leave room for m.
+      bool rok = true;
+      if (m1 + m2 + m3 + m > kGroupRing && i >= 6)
+        rok = mbar_wait(&wempty[(i - 6) % kWSlots], ((i - 6) / kWSlots) & 1);
+      if (rok && m1 + m2 + m > kGroupRing && i >= 4)
+        rok = mbar_wait(&wempty[(i - 4) % kWSlots], ((i - 4) / kWSlots) & 1);
+      if (rok && m1 + m > kGroupRing && i >= 2)
+        rok = mbar_wait(&wempty[(i - 2) % kWSlots], ((i - 2) / kWSlots) & 1);
+      const int row0 = issued & (kGroupRing - 1);
+      issued += m;
+      m3 = m2;
+      m2 = m1;
+      m1 = m;
+      if (!rok) {
+        // no barrier follows in this tile: the group stops together at the next one
         set_abort(s_abort, p.flags);
-        break;
+        continue;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(__popc(bal) * kRowBytes));
+      if (lane == 0) {
+        if (quarter == 0) {
+          ws.row0 = row0;
+          ws.m = m;
+        }
+        mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(__popc(bal) * kRowBytes));
+        if (quarter == 0) s_varm[slot] = s_varm[slot] + 1;
+      }
       __syncwarp();
       if (surv)
-        bulk_load(sRing + ((ws.row0 + e) & (kRing - 1)) * kRowBytes,
+        bulk_load(gring + ((row0 + e) & (kGroupRing - 1)) * kRowBytes,
                   p.v + (static_cast<int64_t>(u) * p.ncap + j) * kRowBytes, kRowBytes, &vfull[slot]);
     }
     __syncwarp();
@@ -876,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 4; ++r) {
           // rows past m are not this tile's: skip them (weight 0, value 0)
           const int e = e0 + r;
-          const uint8_t *vr = sRing + ((row0 + e) & (kRing - 1)) * kRowBytes;
+          const uint8_t *vr = sRing + ((i % kGroups) * kGroupRing + ((row0 + e) & (kGroupRing - 1))) * kRowBytes;
           if constexpr (KV8) {
             raw[r] = make_uint2(e < m ? *reinterpret_cast<const uint32_t *>(vr + lane * 4) : 0u, 0u);
             vsr[r] = e < m ? ws.vs[e] : 0.0f;
@@ -999,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     // No copy may still be landing in shared memory when the CTA leaves: wait (bounded)
     // for the last armed phase of every barrier that a copy completes.
-    const int k_issued = *s_k_issued, q_issued = *s_q_issued, v_issued = *s_v_issued;
+    const int k_issued = *s_k_issued, q_issued = *s_q_issued;
     for (int f = 0; f < 2 * kStages; ++f) {
       // tiles i < k_issued with i % kStages == f / 2 and i % 2 == f % 2
       int uses = 0;
@@ -1009,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (uses) mbar_wait(&full[f], (uses - 1) & 1);
     }
     for (int w = 0; w < kWSlots; ++w) {
-      const int uses = v_issued > w ? (v_issued - 1 - w) / kWSlots + 1 : 0;
+      const int uses = s_varm[w];
       if (uses) mbar_wait(&vfull[w], (uses - 1) & 1);
     }
     for (int q = 0; q < 2; ++q) {
