@@ -56,6 +56,8 @@ def _load():
             "oracle_sparse_decode_batch": [i, i, i, i, i64, vp, vp, vp, vp, i64, vp, d, vp],
             "oracle_window_decode_batch": [i, i, i, i, i64, i64, vp, vp, vp, d, d, vp],
             "oracle_skip_stats": [i64, vp, i64, vp, vp],
+            "oracle_prefill": [i, i, i64, i64, vp, vp, i64, vp, i64, d, d, d, vp],
+            "oracle_prefill_batch": [i, i, i, i, i64, i64, i64, vp, vp, vp, d, d, d, vp],
             "oracle_skip_stats_batch": [i, i, i64, i64, vp, i64, vp, vp],
         }
         for name, args in sig.items():
@@ -168,6 +170,29 @@ def select_topk_batch(sigma32, n, topk=1024, recent=128):
     _ok(_load().oracle_select_topk_batch(B, Hkv, n, ncap, _p(s), topk, recent, _p(idx), stride,
                                          _p(cnt)), "select_topk_batch")
     return idx, cnt
+
+
+def prefill(q, K, V, alpha=1.0, c=1.0, eps=1e-6):
+    """One unit's causal prefill: q [G, T, D] (the last T of the n keys' tokens), K and V
+    [n, D]; returns out [G, T, D]."""
+    q, K, V = f64(q), f64(K), f64(V)
+    G, T, D = q.shape
+    n = K.shape[0]
+    out = np.empty((G, T, D), dtype=np.float64)
+    _ok(_load().oracle_prefill(G, D, n, T, _p(q), _p(K), D, _p(V), D, alpha, c, eps, _p(out)),
+        "prefill")
+    return out
+
+
+def prefill_batch(q, K, V, n, alpha=1.0, c=1.0, eps=1e-6):
+    """All units: q [B, Hq, T, D], K and V [B, Hkv, ncap, D] (keys 0..n-1 valid)."""
+    q, K, V = f64(q), f64(K), f64(V)
+    B, Hq, T, D = q.shape
+    Hkv, ncap = K.shape[1], K.shape[2]
+    out = np.empty((B, Hq, T, D), dtype=np.float64)
+    _ok(_load().oracle_prefill_batch(B, Hq, Hkv, D, n, T, ncap, _p(q), _p(K), _p(V), alpha, c,
+                                     eps, _p(out)), "prefill_batch")
+    return out
 
 
 def e4m3_table() -> np.ndarray:

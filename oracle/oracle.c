@@ -258,6 +258,72 @@ int oracle_full_decode_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t n
 }
 
 /*
+ * Causal full-layer (ReLU^2) attention over a prompt, for one (batch, KV-head) unit
+ * ("The Architecture of Embla 1", section "KV bridge, KV reuse, and prefill": in prefill the
+ * early layers run on every prompt token; their full layers apply the same ReLU^2 rule as
+ * decode, and a token sees the keys up to and including its own, there being no position
+ * encoding in a full layer).  The T prompt tokens are the last T of the n keys: query t of
+ * head h sits at position p = n - T + t and attends to keys j = 0 .. p.
+ *   q   : G x T x D (head-major)
+ *   K, V: n rows with strides ldk, ldv
+ *   out : G x T x D;  out = sum_{j<=p} w v_j / (c + sum_{j<=p} w), 0 when that is 0
+ */
+int oracle_prefill(int G, int D, int64_t n, int64_t T, const double *q, const double *K,
+                   int64_t ldk, const double *V, int64_t ldv, double alpha, double c, double eps,
+                   double *out) {
+  if (G < 1 || D < 1 || T < 0 || n < T || ldk < D || ldv < D || !(eps >= 0.0)) return -1;
+  double *khat = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)D);
+  double *num = (double *)malloc(sizeof(double) * (size_t)D);
+  if (!khat || !num) { free(khat); free(num); return -1; }
+  for (int64_t j = 0; j < n; ++j) {
+    double r = rms_inverse(K + j * ldk, D, eps);
+    for (int d = 0; d < D; ++d) khat[j * D + d] = K[j * ldk + d] * r;
+  }
+  for (int h = 0; h < G; ++h) {
+    for (int64_t t = 0; t < T; ++t) {
+      const double *qt = q + ((size_t)h * T + t) * D;
+      double r = rms_inverse(qt, D, eps);
+      int64_t p = n - T + t;
+      double den = 0.0;
+      for (int d = 0; d < D; ++d) num[d] = 0.0;
+      for (int64_t j = 0; j <= p; ++j) {
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) s += qt[d] * r * khat[j * D + d];
+        s *= alpha;
+        double w = s > 0.0 ? s * s : 0.0;
+        if (w == 0.0) continue;
+        for (int d = 0; d < D; ++d) num[d] += w * V[j * ldv + d];
+        den += w;
+      }
+      double z = c + den;
+      double *o = out + ((size_t)h * T + t) * D;
+      for (int d = 0; d < D; ++d) o[d] = (z != 0.0) ? num[d] / z : 0.0;
+    }
+  }
+  free(khat);
+  free(num);
+  return 0;
+}
+
+/* Every unit: q [B, Hq, T, D], K and V [B, Hkv, ncap, D], out [B, Hq, T, D]. */
+int oracle_prefill_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t T, int64_t ncap,
+                         const double *q, const double *K, const double *V, double alpha,
+                         double c, double eps, double *out) {
+  if (B < 0 || Hkv < 1 || Hq % Hkv || ncap < n) return -1;
+  int G = Hq / Hkv;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+    int64_t b = u / Hkv, g = u % Hkv;
+    const double *qu = q + ((size_t)b * Hq + (size_t)g * G) * T * D;
+    double *ou = out + ((size_t)b * Hq + (size_t)g * G) * T * D;
+    err |= oracle_prefill(G, D, n, T, qu, K + (size_t)u * ncap * D, D, V + (size_t)u * ncap * D,
+                          D, alpha, c, eps, ou) != 0;
+  }
+  return err ? -1 : 0;
+}
+
+/*
  * V-read accounting of one unit ("The Architecture of Embla 1", section "Skipping V": a
  * value row is needed only when some head of the group gives its key a weight above zero,
  * i.e. sigma_j > 0; the page's kernel checks keys in groups of 8).
