@@ -214,6 +214,30 @@ embla_status embla_sparse_decode_e4m3(const embla_shape *shape, const void *q,
                                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Full-layer prefill — causal ReLU^2 attention over a prompt ("KV bridge, KV reuse, and
+ * prefill": the early layers run on every prompt token; "Sevren Sparse Attention learns
+ * to be sparse": the same weights as embla_full_decode).  The prompt's n_new tokens are
+ * the last n_new of the ctx_len keys already in the caches: query t of head h sits at
+ * position p = ctx_len - n_new + t and sees keys 0 .. p (a full layer has no position
+ * encoding).  out = sum_{j<=p} w v_j / (c + sum_{j<=p} w), 0 where that is 0.
+ *   n_new      0 <= n_new <= ctx_len
+ *   q          bf16 [B, Hq, n_new, D]   raw queries (normalised inside), head-major
+ *   k_cache, v_cache   bf16 [B, Hkv, cache_stride, D], rows 0 .. ctx_len-1 read
+ *   alpha, c, eps      as for embla_full_decode
+ *   out        fp32 [B, Hq, n_new, D]
+ *   workspace  the keys' norms, fp32 [B, Hkv, ctx_len rounded up to 4]
+ *              (embla_prefill_workspace_size)
+ * The scores and the value sums run on the tensor cores with fp32 accumulation; the
+ * weights enter the value product as two bf16 parts (hi + lo), about 16 bits.
+ */
+size_t embla_prefill_workspace_size(const embla_shape *shape);
+embla_status embla_prefill(const embla_shape *shape, int64_t n_new, const void *q,
+                           const void *k_cache, const void *v_cache, float alpha, float c,
+                           float eps, float *out, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
+ * Window-layer decode/*
  * Window-layer decode — "Three kinds of attention" (Sliding window).
  *   q          bf16 [B, Hq, D]   raw query; rotated here at position pos:
  *              pair (2i, 2i+1) turned by pos * rope_base^(-2i/D)

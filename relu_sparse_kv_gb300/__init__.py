@@ -88,6 +88,8 @@ def library() -> ctypes.CDLL:
                                                        vp, vp, vp, vp, sz, vp]),
             "embla_sparse_decode_e4m3": (ctypes.c_int, [P, vp, vp, vp, vp, vp, vp, i32, vp,
                                                          f32, vp, vp, sz, vp]),
+            "embla_prefill_workspace_size": (sz, [P]),
+            "embla_prefill": (ctypes.c_int, [P, i64, vp, vp, vp, f32, f32, f32, vp, vp, sz, vp]),
             "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
                                                                 vp, vp, vp, vp, vp]),
             "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
@@ -286,6 +288,28 @@ def embla_sparse_decode_e4m3(shape: Shape, q, k_codes, k_scales, v_codes, v_scal
     _call("embla_sparse_decode_e4m3", ctypes.byref(shape.c()), _ptr(q), _ptr(k_codes),
           _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(idx), idx.shape[2], _ptr(count),
           tau, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_prefill_workspace_size(shape: Shape) -> int:
+    return library().embla_prefill_workspace_size(ctypes.byref(shape.c()))
+
+
+def embla_prefill(shape: Shape, q, k_cache, v_cache, out, alpha: float = 1.0, c: float = 1.0,
+                  eps: float = 1e-6, workspace=None, stream=None):
+    """Causal full-layer attention over the prompt: q bf16 [B, Hq, T, D] holds the queries of
+    the last T of the ctx_len cached keys; out fp32 [B, Hq, T, D]."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, None, "q")
+    if q.dim() != 4 or tuple(q.shape[:2]) != (B, Hq) or q.shape[3] != D:
+        raise ValueError("q must be [B, Hq, T, D]")
+    T = q.shape[2]
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(out, torch.float32, (B, Hq, T, D), "out")
+    ws = _workspace(embla_prefill_workspace_size(shape), workspace, q.device)
+    _call("embla_prefill", ctypes.byref(shape.c()), T, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          alpha, c, eps, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
 def embla_window_decode(shape: Shape, q, k_win, v_win, pos: int, out, window: int = 128,

@@ -127,6 +127,21 @@ bool encode_scales(CUtensorMap *map, const float *base, uint64_t units, uint64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor [planes][rows][128] (256-byte rows, planes `plane_rows` rows apart),
+// boxes of {64 columns, 128 rows, 1 plane}, 128B swizzle; rows past `rows` read as zeros.
+bool encode_planes(CUtensorMap *map, const void *base, uint64_t rows, uint64_t plane_rows,
+                   uint64_t planes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), rows, planes};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2), plane_rows * kHeadDim * 2};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool finite(float x) { return x == x && x - x == 0.0f; }
@@ -386,6 +401,61 @@ embla_status embla_sparse_decode_e4m3(const embla_shape *shape, const void *q,
                                       void *workspace, size_t workspace_bytes, void *stream) {
   return sparse_decode_impl(shape, q, k_codes, k_scales, v_codes, v_scales, true, idx,
                             idx_stride, count, tau, out, workspace, workspace_bytes, stream);
+}
+
+size_t embla_prefill_workspace_size(const embla_shape *shape) {
+  int G = 0;
+  if (check_shape(shape, &G, true) != EMBLA_OK) return 0;
+  return prefill_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_kv_heads,
+                                 shape->ctx_len);
+}
+
+embla_status embla_prefill(const embla_shape *shape, int64_t n_new, const void *q,
+                           const void *k_cache, const void *v_cache, float alpha, float c,
+                           float eps, float *out, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  if (n_new < 0 || n_new > shape->ctx_len) return EMBLA_ERR_INVALID_ARG;
+  if (!(finite(alpha) && alpha > 0.0f) || !(finite(c) && c >= 0.0f) ||
+      !(finite(eps) && eps >= 0.0f))
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0 || n_new == 0) return EMBLA_OK;
+  if (!q || !k_cache || !v_cache || !out || !workspace) return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace))
+    return EMBLA_ERR_INVALID_ARG;
+  // TMA coordinates are 32-bit; one CTA per (sequence, head, 128 prompt tokens)
+  const int64_t bh = static_cast<int64_t>(shape->batch) * shape->n_q_heads;
+  if (shape->ctx_len > INT32_MAX - 256 || bh > INT32_MAX || bh * ((n_new + 127) / 128) > INT32_MAX)
+    return EMBLA_ERR_UNSUPPORTED;
+  if (workspace_bytes < prefill_workspace_bytes(units, shape->ctx_len)) return EMBLA_ERR_WORKSPACE;
+  uint32_t *flags = flags_ptr();
+  if (!flags) return EMBLA_ERR_CUDA;
+  float *rk = static_cast<float *>(workspace);
+  CUtensorMap tm_q, tm_k, tm_v, tm_rk;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return EMBLA_ERR_CUDA;
+  const cuuint64_t rdims[2] = {static_cast<cuuint64_t>(shape->ctx_len), static_cast<cuuint64_t>(units)};
+  const cuuint64_t rstrides[1] = {static_cast<cuuint64_t>(prefill_rk_stride(shape->ctx_len)) * 4};
+  const cuuint32_t rbox[2] = {128u, 1u};
+  const cuuint32_t restr[2] = {1u, 1u};
+  if (!encode_planes(&tm_q, q, static_cast<uint64_t>(n_new), static_cast<uint64_t>(n_new),
+                     static_cast<uint64_t>(bh)) ||
+      !encode_planes(&tm_k, k_cache, static_cast<uint64_t>(shape->ctx_len),
+                     static_cast<uint64_t>(shape->cache_stride), static_cast<uint64_t>(units)) ||
+      !encode_planes(&tm_v, v_cache, static_cast<uint64_t>(shape->ctx_len),
+                     static_cast<uint64_t>(shape->cache_stride), static_cast<uint64_t>(units)) ||
+      fn(&tm_rk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, rk, rdims, rstrides, rbox, restr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return EMBLA_ERR_CUDA;
+  return cuda_status(launch_prefill(tm_q, tm_k, tm_v, tm_rk, k_cache, rk, out, flags, shape->batch,
+                                    shape->n_q_heads, shape->n_kv_heads, shape->ctx_len, n_new,
+                                    shape->cache_stride, alpha, c, eps,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 size_t embla_window_decode_workspace_size(const embla_shape *shape, int32_t window) {

@@ -97,6 +97,15 @@ cudaError_t launch_skip_stats(const float *sel_scores, int64_t units, int64_t n,
                               int chunk, int32_t *keys_needed, int32_t *chunks_needed,
                               cudaStream_t stream);
 
+// Prefill (causal full-layer attention over the last T of n keys): key-norm workspace and
+// launch (a key-norm kernel, then the attention kernel).
+int64_t prefill_rk_stride(int64_t n);
+size_t prefill_workspace_bytes(int64_t units, int64_t n);
+cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_rk, const void *k_cache, float *rk, float *out,
+                           uint32_t *flags, int B, int Hq, int Hkv, int64_t n, int64_t T,
+                           int64_t ncap, float alpha, float c, float eps, cudaStream_t stream);
+
 cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const void *v_win,
                                  int64_t units, int window, int64_t pos, float rope_base,
                                  float tau, float *out, cudaStream_t stream);

@@ -1,0 +1,429 @@
+// Causal full-layer (ReLU^2) attention over a prompt: the prefill of a full layer.
+//
+// Source: "The Architecture of Embla 1", sections "KV bridge, KV reuse, and prefill" (the
+// early layers run on every prompt token) and "Sevren Sparse Attention learns to be sparse"
+// (weights ReLU(s)^2 of scores between RMS-normalised query and key, divided by a constant
+// plus the sum of weights).  A full layer has no position encoding, so the prompt token at
+// position p (the T prompt tokens are keys n-T .. n-1 of the cache) sees keys 0 .. p.
+//
+// prefill_knorm_kernel: rk[u][j] = 1 / sqrt(mean(k_j^2) + eps) for every key of every unit.
+//
+// prefill_kernel: one CTA per (sequence, query head, 128 prompt tokens), the tiles with the
+// most keys first.  Warp roles:
+//   warp 0     TMA producer: the 128 query rows once; per 128-key tile the K rows (two
+//              64-column boxes, 128-byte swizzle), the tile's 128 key norms and the V rows,
+//              each in a ring of 2.  Rows past n (and query rows past T) read as zeros.
+//   warp 1     tcgen05 issuer: S = Q K^T (M 128 queries x N 128 keys, K 16 per step, fp32
+//              in tensor memory, two S buffers), then O += P V, with P from shared memory
+//              and V read as an MN-major operand (the cached rows as they lie), in fp32 in
+//              tensor memory.  S of the next tile is issued before P V of this one, so the
+//              tensor cores work while the epilogue turns scores into weights.
+//   warps 2-9  epilogue, one thread per (query row, half of the tile's keys):
+//              s = dot * alpha rq * rk, w = max(s, 0)^2 for keys j <= p, den += w; P is
+//              written as two bf16 matrices hi = rn(w), lo = rn(w - hi), both multiplied
+//              into O, so the weights keep about 16 bits.  At the end out = O / (c + den).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace embla {
+namespace {
+
+constexpr int kPThreads = 320;
+constexpr int kBox = 128 * 128;          // one [128 rows][64 bf16] box, 16 KB
+constexpr int kTileB = 2 * kBox;         // a 128 x 128 bf16 tile
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileB;    // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileB;
+constexpr int kOffP = kOffV + 2 * kTileB;  // hi, then lo
+constexpr int kOffRK = kOffP + 2 * kTileB;  // 2 x 128 floats; the final row sums reuse it
+constexpr int kOffBar = kOffRK + 2 * 128 * 4;
+constexpr int kNBars = 20;
+constexpr int kOffMisc = kOffBar + kNBars * 8;
+constexpr int kPSmem = kOffMisc + 16 + 1024;  // + room to align the base to 1024
+static_assert(kPSmem <= 227 * 1024, "shared memory per CTA");
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
+constexpr int kColS = 0, kColO = 256, kPTmemCols = 512;
+
+struct PrefillParams {
+  float *out;      // [B, Hq, T, D]
+  uint32_t *flags;
+  int64_t n, T;
+  int32_t Hq, Hkv, BH, nqt;
+  float alpha, c, eps;
+};
+
+__device__ __forceinline__ void set_abort_p(volatile int *abort_flag, uint32_t *flags) {
+  *abort_flag = 1;
+  atomicOr(flags, kFlagWaitTimeout);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rk,
+                   const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *sQ = smem + kOffQ;
+  uint8_t *sK = smem + kOffK;
+  uint8_t *sV = smem + kOffV;
+  uint8_t *sP = smem + kOffP;
+  float *sRK = reinterpret_cast<float *>(smem + kOffRK);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *qfull = bars;
+  uint64_t *kfull = bars + 1, *kempty = bars + 3;
+  uint64_t *rkfull = bars + 5, *rkempty = bars + 7;
+  uint64_t *vfull = bars + 9, *vempty = bars + 11;
+  uint64_t *sfull = bars + 13, *sempty = bars + 15;
+  uint64_t *pfull = bars + 17, *pempty = bars + 18;
+  uint64_t *ofull = bars + 19;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+  uint32_t *s_tmem = misc;
+  volatile int *s_abort = reinterpret_cast<volatile int *>(misc + 1);
+  volatile int *s_issued = reinterpret_cast<volatile int *>(misc + 2);  // key tiles loaded
+
+  // tiles with the most keys first: the last query tile of every (sequence, head), ...
+  const int idx = static_cast<int>(blockIdx.x);
+  const int qt = p.nqt - 1 - idx / p.BH;
+  const int bh = idx % p.BH;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int u = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int64_t p0 = p.n - p.T + static_cast<int64_t>(qt) * 128;  // position of query row 0
+  const int64_t rows_here = p.T - static_cast<int64_t>(qt) * 128 < 128 ? p.T - static_cast<int64_t>(qt) * 128 : 128;
+  const int nkt = static_cast<int>((p0 + rows_here - 1) / 128) + 1;  // key tiles up to the last row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&rkfull[s], 1);
+      mbar_init(&rkempty[s], 8);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 8);
+    }
+    mbar_init(pfull, 8);
+    mbar_init(pempty, 1);
+    mbar_init(ofull, 1);
+    *s_abort = 0;
+    *s_issued = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kPTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
+  pdl_wait_primary();  // the key norms (and everything before) are complete
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_rk);
+      mbar_arrive_expect_tx(qfull, kTileB);
+      tma_load_3d(sQ, &tm_q, qfull, 0, qt * 128, bh);
+      tma_load_3d(sQ + kBox, &tm_q, qfull, 64, qt * 128, bh);
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int s = kt & 1;
+        const uint32_t ph = ((kt >> 1) - 1) & 1;
+        if (kt >= 2 && !mbar_wait(&kempty[s], ph)) {
+          set_abort_p(s_abort, p.flags);
+          break;
+        }
+        mbar_arrive_expect_tx(&kfull[s], kTileB);
+        tma_load_3d(sK + s * kTileB, &tm_k, &kfull[s], 0, kt * 128, u);
+        tma_load_3d(sK + s * kTileB + kBox, &tm_k, &kfull[s], 64, kt * 128, u);
+        if (kt >= 2 && !mbar_wait(&rkempty[s], ph)) {
+          set_abort_p(s_abort, p.flags);
+          *s_issued = 3 * kt + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&rkfull[s], 128 * 4);
+        tma_load_2d(sRK + s * 128, &tm_rk, &rkfull[s], kt * 128, u);
+        if (kt >= 2 && !mbar_wait(&vempty[s], ph)) {
+          set_abort_p(s_abort, p.flags);
+          *s_issued = 3 * kt + 2;
+          break;
+        }
+        mbar_arrive_expect_tx(&vfull[s], kTileB);
+        tma_load_3d(sV + s * kTileB, &tm_v, &vfull[s], 0, kt * 128, u);
+        tma_load_3d(sV + s * kTileB + kBox, &tm_v, &vfull[s], 64, kt * 128, u);
+        *s_issued = 3 * kt + 3;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ));
+      const uint64_t kdesc = smem_desc_sw128(smem_u32(sK));
+      const uint64_t pdesc = smem_desc_sw128(smem_u32(sP));
+      bool ok = mbar_wait(qfull, 0);
+      for (int kt = 0; ok && kt <= nkt; ++kt) {
+        if (kt < nkt) {
+          const int sb = kt & 1;
+          ok = mbar_wait(&kfull[sb], (kt >> 1) & 1) &&
+               (kt < 2 || mbar_wait(&sempty[sb], ((kt >> 1) - 1) & 1));
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // dims 16kk..16kk+15: 32 bytes into a 128-byte row; dims 64.. start the second box
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+            tc_mma_bf16(tmem + kColS + sb * 128, qdesc + off,
+                        kdesc + static_cast<uint64_t>((sb * kTileB) >> 4) + off, kIdescS,
+                        kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&sfull[sb]);
+          tc_commit(&kempty[sb]);
+        }
+        if (kt >= 1) {
+          const int t = kt - 1, vb = t & 1;
+          ok = mbar_wait(pfull, t & 1) && mbar_wait(&vfull[vb], (t >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // keys 16kk..16kk+15: P columns (K-major, as S), V rows 16kk.. (2 KB apart)
+            const uint64_t aoff = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+            const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + vb * kTileB + kk * 2048), kBox);
+            tc_mma_bf16(tmem + kColO, pdesc + aoff, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(tmem + kColO, pdesc + static_cast<uint64_t>(kTileB >> 4) + aoff, vd,
+                        kIdescPV, 1u);
+          }
+          tc_commit(pempty);
+          tc_commit(&vempty[vb]);
+        }
+      }
+      if (!ok) set_abort_p(s_abort, p.flags);
+      tc_commit(ofull);
+      // every MMA of this thread has completed before the tensor memory is released
+      mbar_wait(ofull, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;          // the tensor-memory lanes this warp may read
+    const int half = (warp - 2) >> 2;      // keys 64 half .. 64 half + 63 of each tile
+    const int r = quarter * 32 + lane;     // query row
+    const int64_t pos = p0 + r;            // its position
+    bool ok = !*s_abort && mbar_wait(qfull, 0);
+    float aq = 0.0f;
+    if (ok) {
+      float a[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(sQ + r * 128 + c * 16);
+        const uint4 x1 = *reinterpret_cast<const uint4 *>(sQ + kBox + r * 128 + c * 16);
+        sq_acc_bf16x2(x0.x, a[0], a[1]);
+        sq_acc_bf16x2(x0.y, a[2], a[3]);
+        sq_acc_bf16x2(x0.z, a[4], a[5]);
+        sq_acc_bf16x2(x0.w, a[6], a[7]);
+        sq_acc_bf16x2(x1.x, a[0], a[1]);
+        sq_acc_bf16x2(x1.y, a[2], a[3]);
+        sq_acc_bf16x2(x1.z, a[4], a[5]);
+        sq_acc_bf16x2(x1.w, a[6], a[7]);
+      }
+      const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+      aq = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+    }
+    float den = 0.0f;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    uint8_t *prow_hi = sP + half * kBox + r * 128;
+    for (int kt = 0; ok && kt < nkt; ++kt) {
+      const int sb = kt & 1;
+      ok = mbar_wait(&sfull[sb], (kt >> 1) & 1) && mbar_wait(&rkfull[sb], (kt >> 1) & 1);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t acc[64];
+      tmem_load_x32(tmem + lane_base + kColS + sb * 128 + half * 64,
+                    *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
+      tmem_load_x32(tmem + lane_base + kColS + sb * 128 + half * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+      tmem_wait_ld(acc);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sb]);
+      // key norms of this half of the tile (the same for every lane: broadcast reads)
+      float rk[64];
+#pragma unroll
+      for (int k = 0; k < 64; k += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(sRK + sb * 128 + half * 64 + k);
+        rk[k] = v.x;
+        rk[k + 1] = v.y;
+        rk[k + 2] = v.z;
+        rk[k + 3] = v.w;
+      }
+      const float used = __shfl_sync(0xffffffffu, rk[0] + rk[63], 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_after(&rkempty[sb], used);
+      // keys past this row's position weigh nothing (only tiles that reach past row 0's
+      // position need the test)
+      const int64_t j0 = static_cast<int64_t>(kt) * 128 + half * 64;
+      const bool masked = j0 + 63 > p0;
+      uint32_t hi[32], lo[32];
+#pragma unroll
+      for (int k = 0; k < 64; k += 2) {
+        float w2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float s = __uint_as_float(acc[k + e]) * aq * rk[k + e];
+          float w = s > 0.0f ? s * s : 0.0f;
+          if (masked && j0 + k + e > pos) w = 0.0f;
+          den += w;
+          w2[e] = w;
+        }
+        const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
+        hi[k >> 1] = hb;
+        lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
+      }
+      // the previous tile's P V has read P
+      if (kt >= 1 && !mbar_wait(pempty, (kt - 1) & 1)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int pc = (c ^ (r & 7)) * 16;
+        *reinterpret_cast<uint4 *>(prow_hi + pc) =
+            make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+        *reinterpret_cast<uint4 *>(prow_hi + kTileB + pc) =
+            make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+      }
+      fence_proxy_async_smem();  // P is read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
+    }
+    if (ok) ok = mbar_wait(ofull, 0) && !*s_abort;
+    if (!ok) set_abort_p(s_abort, p.flags);
+    // the two halves of each row add their weight sums (the key-norm ring is free now)
+    float *s_den = sRK;
+    s_den[r * 2 + half] = den;
+    ok = named_bar_and(1, 256, ok);
+    if (ok) {
+      tc_fence_after_sync();
+      uint32_t o[64];
+      tmem_load_x32(tmem + lane_base + kColO + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+      tmem_load_x32(tmem + lane_base + kColO + half * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+      tmem_wait_ld(o);
+      const float z = p.c + (s_den[r * 2] + s_den[r * 2 + 1]);
+      const int64_t t = static_cast<int64_t>(qt) * 128 + r;
+      if (t < p.T) {
+        float *dst = p.out + (static_cast<int64_t>(bh) * p.T + t) * kHeadDim + half * 64;
+#pragma unroll
+        for (int k = 0; k < 64; k += 4) {
+          const float4 v = z != 0.0f ? make_float4(__uint_as_float(o[k]) / z, __uint_as_float(o[k + 1]) / z,
+                                                   __uint_as_float(o[k + 2]) / z, __uint_as_float(o[k + 3]) / z)
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          *reinterpret_cast<float4 *>(dst + k) = v;
+        }
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // no copy may still be landing in shared memory when the CTA leaves
+    mbar_wait(qfull, 0);
+    const int issued = *s_issued;  // 3 per key tile: K, key norms, V
+    for (int s = 0; s < 2; ++s) {
+      const int tk = issued / 3;   // tiles whose three loads were all issued
+      int uses = tk > s ? (tk - 1 - s) / 2 + 1 : 0;
+      if (uses) mbar_wait(&vfull[s], (uses - 1) & 1);
+      const int tr = (issued + 1) / 3;  // tiles whose key-norm load was issued
+      uses = tr > s ? (tr - 1 - s) / 2 + 1 : 0;
+      if (uses) mbar_wait(&rkfull[s], (uses - 1) & 1);
+      const int tq = (issued + 2) / 3;  // tiles whose K load was issued
+      uses = tq > s ? (tq - 1 - s) / 2 + 1 : 0;
+      if (uses) mbar_wait(&kfull[s], (uses - 1) & 1);
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kPTmemCols);
+  }
+}
+
+// rk[u][j] = 1 / sqrt(mean(k_j^2) + eps), one thread per key.
+__global__ void __launch_bounds__(128) prefill_knorm_kernel(const uint8_t *K, float *rk, int64_t n,
+                                                            int64_t ncap, int64_t rk_stride,
+                                                            float eps) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int64_t u = blockIdx.y;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j >= n) return;
+  const uint4 *row = reinterpret_cast<const uint4 *>(K + (u * ncap + j) * kHeadDim * 2);
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const uint4 x0 = row[c], x1 = row[c + 1];
+    sq_acc_bf16x2(x0.x, a[0], a[1]);
+    sq_acc_bf16x2(x0.y, a[2], a[3]);
+    sq_acc_bf16x2(x0.z, a[4], a[5]);
+    sq_acc_bf16x2(x0.w, a[6], a[7]);
+    sq_acc_bf16x2(x1.x, a[0], a[1]);
+    sq_acc_bf16x2(x1.y, a[2], a[3]);
+    sq_acc_bf16x2(x1.z, a[4], a[5]);
+    sq_acc_bf16x2(x1.w, a[6], a[7]);
+  }
+  const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  rk[u * rk_stride + j] = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+}
+
+}  // namespace
+
+int64_t prefill_rk_stride(int64_t n) { return (n + 3) & ~static_cast<int64_t>(3); }
+
+size_t prefill_workspace_bytes(int64_t units, int64_t n) {
+  return (static_cast<size_t>(units) * static_cast<size_t>(prefill_rk_stride(n)) * 4 + 255) &
+         ~static_cast<size_t>(255);
+}
+
+cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_rk, const void *k_cache, float *rk, float *out,
+                           uint32_t *flags, int B, int Hq, int Hkv, int64_t n, int64_t T,
+                           int64_t ncap, float alpha, float c, float eps, cudaStream_t stream) {
+  const int64_t units = static_cast<int64_t>(B) * Hkv;
+  if (units == 0 || T == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(prefill_knorm_kernel,
+                             dim3(static_cast<unsigned>((n + 127) / 128), static_cast<unsigned>(units)),
+                             dim3(128), 0, stream, 0u, static_cast<const uint8_t *>(k_cache), rk, n,
+                             ncap, prefill_rk_stride(n), eps);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+  if (e != cudaSuccess) return e;
+  PrefillParams p;
+  p.out = out;
+  p.flags = flags;
+  p.n = n;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.BH = B * Hq;
+  p.nqt = static_cast<int32_t>((T + 127) / 128);
+  p.alpha = alpha;
+  p.c = c;
+  p.eps = eps;
+  const int64_t ctas = static_cast<int64_t>(p.BH) * p.nqt;
+  return launch_pdl(prefill_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kPThreads),
+                    static_cast<size_t>(kPSmem), stream, 0u, tm_q, tm_k, tm_v, tm_rk, p);
+}
+
+}  // namespace embla

@@ -123,6 +123,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// 3-D tiled TMA load: box at (x, y, z) into shared memory (coordinates past the tensor's
+// extent read as zeros).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Same, with an L2 cache policy (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
                                                  int32_t x, int32_t y, uint64_t policy) {
@@ -309,6 +320,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: next 8-row atom
   d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Shared-memory matrix descriptor: MN-major operand in the 128-byte swizzle layout, as TMA
+// writes a [K rows][64 MN columns] box (rows of 128 bytes, 8-row atoms of 1024 bytes);
+// further 64-column boxes follow `box_bytes` apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t box_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);          // start address >> 4
+  d |= static_cast<uint64_t>((box_bytes >> 4) & 0x3FFFu) << 16;  // next 64 MN columns
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                   // next 8 K rows
+  d |= static_cast<uint64_t>(1) << 46;                           // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                           // 128-byte swizzle
   return d;
 }
 
