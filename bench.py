@@ -29,6 +29,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode attention tokens/s and needed-byte HBM GB/s (% of roofline) at 32k–128k"
+PREFILL_METRIC = "full-layer prefill tokens/s (causal ReLU^2 attention over the prompt) and TFLOP/s (% of bf16 tensor peak)"
 ROW_BYTES = 128 * 2          # one bf16 key or value row (head_dim 128)
 ROW_BYTES_E4M3 = 128 + 4     # one 8-bit row (E4M3 codes) and its fp32 scale
 TOPK, RECENT = 1024, 128
@@ -164,10 +165,24 @@ def workload_name(cfg, batch=None, ctx=None) -> str:
     return cfg["name"] + f" (overridden: batch {batch}, ctx {ctx})"
 
 
+def prefill_flops(B: int, Hq: int, n: int, T: int) -> float:
+    """Algorithmic flops of a causal prefill: Q K^T and P V once each over the (query, key)
+    pairs with key <= query position, 2 flops per multiply-add, D = 128."""
+    pairs = T * (n - T) + T * (T + 1) / 2
+    return 4.0 * 128 * pairs * B * Hq
+
+
 def static_config(cfg_id: int, batch=None, ctx=None) -> dict:
     """The workload's description, the same on both arms."""
     import gen
     cfg = gen.CONFIGS[cfg_id]
+    if cfg.get("kind") == "prefill":
+        n = cfg["n"] if ctx is None else ctx
+        return {"workload": workload_name(cfg, batch, ctx),
+                "batch": cfg["B"] if batch is None else batch, "ctx_len": n,
+                "prompt_tokens": min(cfg["T"], n), "q_heads": cfg.get("Hq", gen.HQ),
+                "kv_heads": cfg.get("Hkv", gen.HKV), "head_dim": gen.HEAD_DIM,
+                "kv_cache": "bf16", "causal": True, "accumulate": "f32"}
     if cfg_id == 5:
         fulls = [len(gen.EMBLA_SPARSE_OF[layer]) for layer in gen.EMBLA_FULL_LAYERS]
         wins = list(gen.EMBLA_WINDOW_LAYERS)
@@ -262,6 +277,8 @@ def run_reference(args):
     import oracle
 
     cfg = gen.CONFIGS[args.config]
+    if cfg.get("kind") == "prefill":
+        return run_reference_prefill(args, cfg)
     sample_b = 1
     fls = list(gen.config_full_layers(args.config, seed=0, B=sample_b))
     wls = list(gen.config_window_layers(args.config, seed=0, B=sample_b))
@@ -302,6 +319,200 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def prefill_oracle_sample(cfg_id: int, rows: int):
+    """The oracle's prefill of the last `rows` prompt tokens of sequence 0 (every head): those
+    rows see the most keys, so their rate is the slowest the oracle runs."""
+    import gen
+    import oracle
+    q, K, V = gen.config_prefill(cfg_id, seed=0, B=1)
+    n = K.shape[2]
+    qs = oracle.f64(q[:, :, -rows:])
+    Kd, Vd = oracle.f64(K), oracle.f64(V)
+
+    def run():
+        oracle.prefill_batch(qs, Kd, Vd, n)
+    return run
+
+
+def run_reference_prefill(args, cfg):
+    import gen
+    rows = 8
+    run = prefill_oracle_sample(args.config, rows)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": static_config(args.config),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": omp_threads(),
+                         "kind": "oracle",
+                         "sample": f"the last {rows} prompt tokens of sequence 0, every head"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline_prefill(cfg_id: int, budget_s: float = 12.0):
+    rows = 8
+    run = prefill_oracle_sample(cfg_id, rows)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": rows * reps / dt, "unit": "tokens/s", "cores": omp_threads(), "kind": "oracle",
+            "sample": f"{reps} pass(es) over the last {rows} prompt tokens of sequence 0 (the rows "
+                      "with the most keys), every head", "seconds": round(dt, 2)}
+
+
+def bench_prefill(args, cfg):
+    """One step = one embla_prefill call over the whole prompt of every sequence."""
+    import numpy as np
+    import torch
+    import gen
+    import relu_sparse_kv_gb300 as E
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    q_h, K_h, V_h = gen.config_prefill(args.config, seed=rank, B=args.batch, n=args.ctx)
+    B, Hq, T, D = q_h.shape
+    Hkv, n = K_h.shape[1], K_h.shape[2]
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    step_bytes = (q_h.size + K_h.size + V_h.size) * 2 + B * Hq * T * D * 4
+    n_rep = replicas_for(step_bytes)
+    reps = [dict(q=bf(q_h), K=bf(K_h), V=bf(V_h), out=torch.empty(B, Hq, T, D, device=dev))]
+    for _ in range(n_rep - 1):
+        reps.append({k: v.clone() for k, v in reps[0].items()})
+    ws = torch.empty(max(16, E.embla_prefill_workspace_size(shape)), dtype=torch.uint8, device=dev)
+
+    def call(r):
+        E.embla_prefill(shape, r["q"], r["K"], r["V"], r["out"], alpha=1.0, c=1.0, eps=1e-6,
+                        workspace=ws)
+
+    for r in reps:
+        call(r)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(r)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_rep].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t_wall0 = time.time()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            graphs[i % n_rep].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop(t_wall0, t_wall1)
+    ms = ev[0][0].elapsed_time(ev[-1][1])
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    assert E.embla_device_check() == 0
+    ms = max_over_ranks(ms, world, dev)
+    ms_per_step = ms / args.steps
+    value = world * B * T / (ms_per_step * 1e-3)
+
+    e2e = None
+    if args.e2e_steps > 0:
+        h_q = reps[0]["q"].cpu().pin_memory()
+        h_out = torch.empty_like(reps[0]["out"], device="cpu").pin_memory()
+        h2d = h_q.numel() * h_q.element_size()
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step(k):
+            r = reps[k % n_rep]
+            r["q"].copy_(h_q, non_blocking=True)
+            call(r)
+            h_out.copy_(r["out"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for k in range(3):
+            e2e_step(k)
+        steps = max(3, min(args.e2e_steps, 20))
+        t0 = time.perf_counter()
+        for k in range(steps):
+            e2e_step(k)
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * B * T / (dt / steps), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": steps,
+               "inputs": "per-step queries from pinned host memory, outputs back to host; the "
+                         "KV caches stay resident in HBM"}
+
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("bf16_tflops_sustained")
+    peak_src = "measured bf16_tflops_sustained (MEASURED_PEAKS.json; the timed region is a long run of back-to-back calls)"
+    if not peak:
+        peak, peak_src = 1700.0, "fallback 1.7 PFLOP/s sustained"
+    flops = prefill_flops(B, Hq, n, T)
+    ach = flops / (call_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "prefill_kernel (one embla_prefill call: key-norm kernel + attention kernel)",
+                "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                "peak_source": peak_src, "traffic": None, "algorithmic_flops_per_launch": flops,
+                "launch_ms": round(call_ms, 5)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(args.config)
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {**static_config(args.config, args.batch, args.ctx),
+                   "launch": "one CUDA graph per call; events around each replay",
+                   "l2": (f"not flushed: the steps rotate through {n_rep} copies of q, K, V and out "
+                          f"({step_bytes / 1e6:.0f} MB each)" if n_rep > 1 else
+                          f"not flushed: inputs and output larger than L2 ({step_bytes / 1e6:.0f} MB)")},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
     return 0
 
 
@@ -355,6 +566,8 @@ def main():
     import gen
     import relu_sparse_kv_gb300 as E
 
+    if gen.CONFIGS[args.config].get("kind") == "prefill":
+        return bench_prefill(args, gen.CONFIGS[args.config])
     world, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)

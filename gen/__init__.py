@@ -32,6 +32,7 @@ BF16_NAN = 0x7FC0
 # stream roles
 ROLE_Q_FULL, ROLE_K, ROLE_V, ROLE_T, ROLE_Q_SPARSE = 1, 2, 3, 4, 5
 ROLE_K_WIN, ROLE_V_WIN, ROLE_Q_WIN, ROLE_IID = 6, 7, 8, 9
+ROLE_Q_PRE, ROLE_K_PRE, ROLE_V_PRE = 10, 11, 12
 
 
 def build(force: bool = False) -> str:
@@ -281,8 +282,29 @@ CONFIGS = {
     # Embla 1's own head shape: 8 query heads per KV head, K and V in 8 bits
     6: dict(name="gqa8-e4m3-full+select+3sparse-b8-n32k-f0.05", B=8, n=32768, pattern="subset",
             frac=0.05, sparse=(1, 2, 3), Hq=16, Hkv=2, kv="e4m3"),
+    # prefill of a full layer: a whole prompt of T tokens, causal (no prefix)
+    7: dict(name="prefill-b1-n8k", kind="prefill", B=1, n=8192, T=8192),
+    8: dict(name="prefill-b1-n32k", kind="prefill", B=1, n=32768, T=32768),
 }
 HQ, HKV, HEAD_DIM, WINDOW, ROPE_BASE = 16, 4, 128, 128, 10000.0
+
+
+def make_prefill(seed: int, B: int, Hq: int, Hkv: int, n: int, T: int, D: int = 128):
+    """A full layer's prompt: queries [B, Hq, T, D] of the last T of n cached keys, and the
+    caches [B, Hkv, n, D]; all N(0, 1) in bf16 (untrained statistics: about half the weights
+    are zero)."""
+    q = normal_bf16(stream(seed, ROLE_Q_PRE), (B, Hq, T, D))
+    K = normal_bf16(stream(seed, ROLE_K_PRE), (B, Hkv, n, D))
+    V = normal_bf16(stream(seed, ROLE_V_PRE), (B, Hkv, n, D))
+    return q, K, V
+
+
+def config_prefill(cfg: int, seed: int = 0, B: int | None = None, n: int | None = None):
+    c = CONFIGS[cfg]
+    B = c["B"] if B is None else B
+    n = c["n"] if n is None else n
+    T = min(c["T"], n)
+    return make_prefill(seed, B, c.get("Hq", HQ), c.get("Hkv", HKV), n, T)
 
 
 def config_full_layers(cfg: int, seed: int = 0, B: int | None = None, n: int | None = None,

@@ -6,7 +6,7 @@
 // plus the sum of weights).  A full layer has no position encoding, so the prompt token at
 // position p (the T prompt tokens are keys n-T .. n-1 of the cache) sees keys 0 .. p.
 //
-// prefill_knorm_kernel: rk[u][j] = 1 / sqrt(mean(k_j^2) + eps) for every key of every unit.
+// prefill_knorm_kernel: rk2[u][j] = 1 / (mean(k_j^2) + eps) for every key of every unit.
 //
 // prefill_kernel: one CTA per (sequence, query head, 128 prompt tokens), the tiles with the
 // most keys first.  Warp roles:
@@ -18,17 +18,27 @@
 //              and V read as an MN-major operand (the cached rows as they lie), in fp32 in
 //              tensor memory.  S of the next tile is issued before P V of this one, so the
 //              tensor cores work while the epilogue turns scores into weights.
-//   warps 2-9  epilogue, one thread per (query row, half of the tile's keys):
-//              s = dot * alpha rq * rk, w = max(s, 0)^2 for keys j <= p, den += w; P is
-//              written as two bf16 matrices hi = rn(w), lo = rn(w - hi), both multiplied
-//              into O, so the weights keep about 16 bits.  At the end out = O / (c + den).
+//   warps 2-9  epilogue, one thread per (query row, half of the tile's keys).  With
+//              s = alpha rq rk dot, w = max(s, 0)^2 = a2 * w' where a2 = alpha^2 rq^2 is the
+//              row's factor and w' = max(dot, 0)^2 * rk^2 (rq, rk > 0), so the row factor
+//              is applied once at the end: out = a2 O' / (c + a2 den'), O' = sum w' v,
+//              den' = sum w' over keys j <= p.  P = w' is written as two bf16 matrices
+//              hi = rn(w'), lo = rn(w' - hi), both multiplied into O', so the weights keep
+//              about 16 bits.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace embla {
 namespace {
 
-constexpr int kPThreads = 320;
+#ifndef EMBLA_PREFILL_EPI_WARPS
+#define EMBLA_PREFILL_EPI_WARPS 8
+#endif
+constexpr int kEpiWarps = EMBLA_PREFILL_EPI_WARPS;  // a multiple of 4 (the lane quarters)
+constexpr int kEpiParts = kEpiWarps / 4;          // threads per query row
+constexpr int kEpiCols = 128 / kEpiParts;         // keys of a tile per epilogue thread
+static_assert(kEpiWarps % 4 == 0 && kEpiCols % 32 == 0, "epilogue split");
+constexpr int kPThreads = (2 + kEpiWarps) * 32;
 constexpr int kBox = 128 * 128;          // one [128 rows][64 bf16] box, 16 KB
 constexpr int kTileB = 2 * kBox;         // a 128 x 128 bf16 tile
 constexpr int kOffQ = 0;
@@ -99,13 +109,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
       mbar_init(&rkfull[s], 1);
-      mbar_init(&rkempty[s], 8);
+      mbar_init(&rkempty[s], kEpiWarps);
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 8);
+      mbar_init(&sempty[s], kEpiWarps);
     }
-    mbar_init(pfull, 8);
+    mbar_init(pfull, kEpiWarps);
     mbar_init(pempty, 1);
     mbar_init(ofull, 1);
     *s_abort = 0;
@@ -214,19 +224,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int quarter = warp & 3;          // the tensor-memory lanes this warp may read
-    const int half = (warp - 2) >> 2;      // keys 64 half .. 64 half + 63 of each tile
+    const int cg = (warp - 2) >> 2;        // keys kEpiCols cg .. of each tile
     const int r = quarter * 32 + lane;     // query row
     const int64_t pos = p0 + r;            // its position
     bool ok = !*s_abort && mbar_wait(qfull, 0);
-    float aq = 0.0f;
+    float a2 = 0.0f;  // alpha^2 / (mean(q^2) + eps)
     if (ok) {
       float a[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) a[k] = 0.0f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 x0 = *reinterpret_cast<const uint4 *>(sQ + r * 128 + c * 16);
-        const uint4 x1 = *reinterpret_cast<const uint4 *>(sQ + kBox + r * 128 + c * 16);
+        // chunk order rotated by row: 8 neighbouring rows read 8 different bank groups
+        const int pc = (c ^ (r & 7)) * 16;
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(sQ + r * 128 + pc);
+        const uint4 x1 = *reinterpret_cast<const uint4 *>(sQ + kBox + r * 128 + pc);
         sq_acc_bf16x2(x0.x, a[0], a[1]);
         sq_acc_bf16x2(x0.y, a[2], a[3]);
         sq_acc_bf16x2(x0.z, a[4], a[5]);
@@ -237,52 +249,54 @@ __global__ void __launch_bounds__(kPThreads, 1)
         sq_acc_bf16x2(x1.w, a[6], a[7]);
       }
       const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-      aq = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+      a2 = (p.alpha * p.alpha) / (ss * (1.0f / kHeadDim) + p.eps);
     }
-    float den = 0.0f;
+    float den4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains of the row's weight sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint8_t *prow_hi = sP + half * kBox + r * 128;
+    // this thread's keys are 16-byte chunks chunk0 .. of box (cg kEpiCols) / 64 of a P row
+    uint8_t *prow = sP + ((cg * kEpiCols) >> 6) * kBox + r * 128;
+    const int chunk0 = ((cg * kEpiCols) & 63) >> 3;
     for (int kt = 0; ok && kt < nkt; ++kt) {
       const int sb = kt & 1;
       ok = mbar_wait(&sfull[sb], (kt >> 1) & 1) && mbar_wait(&rkfull[sb], (kt >> 1) & 1);
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t acc[64];
-      tmem_load_x32(tmem + lane_base + kColS + sb * 128 + half * 64,
-                    *reinterpret_cast<uint32_t(*)[32]>(&acc[0]));
-      tmem_load_x32(tmem + lane_base + kColS + sb * 128 + half * 64 + 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&acc[32]));
+      uint32_t acc[kEpiCols];
+#pragma unroll
+      for (int c = 0; c < kEpiCols; c += 32)
+        tmem_load_x32(tmem + lane_base + kColS + sb * 128 + cg * kEpiCols + c,
+                      *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
       tmem_wait_ld(acc);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-      // key norms of this half of the tile (the same for every lane: broadcast reads)
-      float rk[64];
+      // squared key norms of these keys (the same for every lane: broadcast reads)
+      float rk[kEpiCols];
 #pragma unroll
-      for (int k = 0; k < 64; k += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(sRK + sb * 128 + half * 64 + k);
+      for (int k = 0; k < kEpiCols; k += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(sRK + sb * 128 + cg * kEpiCols + k);
         rk[k] = v.x;
         rk[k + 1] = v.y;
         rk[k + 2] = v.z;
         rk[k + 3] = v.w;
       }
-      const float used = __shfl_sync(0xffffffffu, rk[0] + rk[63], 0);
+      const float used = __shfl_sync(0xffffffffu, rk[0] + rk[kEpiCols - 1], 0);
       __syncwarp();
       if (lane == 0) mbar_arrive_after(&rkempty[sb], used);
       // keys past this row's position weigh nothing (only tiles that reach past row 0's
       // position need the test)
-      const int64_t j0 = static_cast<int64_t>(kt) * 128 + half * 64;
-      const bool masked = j0 + 63 > p0;
-      uint32_t hi[32], lo[32];
+      const int64_t j0 = static_cast<int64_t>(kt) * 128 + cg * kEpiCols;
+      const bool masked = j0 + kEpiCols - 1 > p0;
+      uint32_t hi[kEpiCols / 2], lo[kEpiCols / 2];
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
+      for (int k = 0; k < kEpiCols; k += 2) {
         float w2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float s = __uint_as_float(acc[k + e]) * aq * rk[k + e];
-          float w = s > 0.0f ? s * s : 0.0f;
+          const float d = fmaxf(__uint_as_float(acc[k + e]), 0.0f);
+          float w = d * d * rk[k + e];
           if (masked && j0 + k + e > pos) w = 0.0f;
-          den += w;
+          den4[(k + e) & 3] += w;
           w2[e] = w;
         }
         const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
@@ -295,11 +309,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         break;
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int pc = (c ^ (r & 7)) * 16;
-        *reinterpret_cast<uint4 *>(prow_hi + pc) =
+      for (int c = 0; c < kEpiCols / 8; ++c) {
+        const int pc = ((chunk0 + c) ^ (r & 7)) * 16;
+        *reinterpret_cast<uint4 *>(prow + pc) =
             make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-        *reinterpret_cast<uint4 *>(prow_hi + kTileB + pc) =
+        *reinterpret_cast<uint4 *>(prow + kTileB + pc) =
             make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
       }
       fence_proxy_async_smem();  // P is read by the tensor cores
@@ -308,25 +322,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     if (ok) ok = mbar_wait(ofull, 0) && !*s_abort;
     if (!ok) set_abort_p(s_abort, p.flags);
-    // the two halves of each row add their weight sums (the key-norm ring is free now)
-    float *s_den = sRK;
-    s_den[r * 2 + half] = den;
-    ok = named_bar_and(1, 256, ok);
+    // the parts of each row add their weight sums (every MMA is done: the query tile's
+    // space is free)
+    float *s_den = reinterpret_cast<float *>(sQ);
+    s_den[r * kEpiParts + cg] = (den4[0] + den4[1]) + (den4[2] + den4[3]);
+    ok = named_bar_and(1, kEpiWarps * 32, ok);
     if (ok) {
       tc_fence_after_sync();
-      uint32_t o[64];
-      tmem_load_x32(tmem + lane_base + kColO + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-      tmem_load_x32(tmem + lane_base + kColO + half * 64 + 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+      uint32_t o[kEpiCols];
+#pragma unroll
+      for (int c = 0; c < kEpiCols; c += 32)
+        tmem_load_x32(tmem + lane_base + kColO + cg * kEpiCols + c,
+                      *reinterpret_cast<uint32_t(*)[32]>(&o[c]));
       tmem_wait_ld(o);
-      const float z = p.c + (s_den[r * 2] + s_den[r * 2 + 1]);
+      float dsum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kEpiParts; ++k) dsum += s_den[r * kEpiParts + k];
+      const float z = p.c + a2 * dsum;
       const int64_t t = static_cast<int64_t>(qt) * 128 + r;
       if (t < p.T) {
-        float *dst = p.out + (static_cast<int64_t>(bh) * p.T + t) * kHeadDim + half * 64;
+        float *dst = p.out + (static_cast<int64_t>(bh) * p.T + t) * kHeadDim + cg * kEpiCols;
 #pragma unroll
-        for (int k = 0; k < 64; k += 4) {
-          const float4 v = z != 0.0f ? make_float4(__uint_as_float(o[k]) / z, __uint_as_float(o[k + 1]) / z,
-                                                   __uint_as_float(o[k + 2]) / z, __uint_as_float(o[k + 3]) / z)
+        for (int k = 0; k < kEpiCols; k += 4) {
+          const float4 v = z != 0.0f ? make_float4(a2 * __uint_as_float(o[k]) / z, a2 * __uint_as_float(o[k + 1]) / z,
+                                                   a2 * __uint_as_float(o[k + 2]) / z, a2 * __uint_as_float(o[k + 3]) / z)
                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           *reinterpret_cast<float4 *>(dst + k) = v;
         }
@@ -358,7 +377,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
-// rk[u][j] = 1 / sqrt(mean(k_j^2) + eps), one thread per key.
+// rk2[u][j] = 1 / (mean(k_j^2) + eps), one thread per key.
 __global__ void __launch_bounds__(128) prefill_knorm_kernel(const uint8_t *K, float *rk, int64_t n,
                                                             int64_t ncap, int64_t rk_stride,
                                                             float eps) {
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(128) prefill_knorm_kernel(const uint8_t *K, fl
     sq_acc_bf16x2(x1.w, a[6], a[7]);
   }
   const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-  rk[u * rk_stride + j] = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+  rk[u * rk_stride + j] = 1.0f / (ss * (1.0f / kHeadDim) + eps);
 }
 
 }  // namespace
