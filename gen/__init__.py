@@ -33,6 +33,7 @@ BF16_NAN = 0x7FC0
 ROLE_Q_FULL, ROLE_K, ROLE_V, ROLE_T, ROLE_Q_SPARSE = 1, 2, 3, 4, 5
 ROLE_K_WIN, ROLE_V_WIN, ROLE_Q_WIN, ROLE_IID = 6, 7, 8, 9
 ROLE_Q_PRE, ROLE_K_PRE, ROLE_V_PRE = 10, 11, 12
+ROLE_MLP_X, ROLE_MLP_UP, ROLE_MLP_DOWN, ROLE_MLP_LIVE = 13, 14, 15, 16
 
 
 def build(force: bool = False) -> str:
@@ -285,6 +286,9 @@ CONFIGS = {
     # prefill of a full layer: a whole prompt of T tokens, causal (no prefix)
     7: dict(name="prefill-b1-n8k", kind="prefill", B=1, n=8192, T=8192),
     8: dict(name="prefill-b1-n32k", kind="prefill", B=1, n=32768, T=32768),
+    # a ReLU^2 MLP at batch 1 with 22 % of its neurons firing (the page reports 78 % of the
+    # down-projection bytes saved)
+    9: dict(name="relu2-mlp-b1-d2048-f8192-live0.22", kind="mlp", d=2048, f=8192, live=0.22),
 }
 HQ, HKV, HEAD_DIM, WINDOW, ROPE_BASE = 16, 4, 128, 128, 10000.0
 
@@ -305,6 +309,42 @@ def config_prefill(cfg: int, seed: int = 0, B: int | None = None, n: int | None 
     n = c["n"] if n is None else n
     T = min(c["T"], n)
     return make_prefill(seed, B, c.get("Hq", HQ), c.get("Hkv", HKV), n, T)
+
+
+def make_mlp(seed: int, d: int, f: int, live: float, margin: float = 1e-2):
+    """One token and a ReLU^2 MLP whose neurons fire for exactly round(live * f) of them:
+    x [d] ~ N(0, 1); w_up [f, d] rows ~ N(0, I/d), each moved along x so that x . w_i has
+    the chosen sign with |x . w_i| >= margin |x| after bf16 rounding; w_down [f, d] ~
+    N(0, I/f).  Returns bf16 bit patterns (x, w_up, w_down) and the live mask."""
+    x = normal_bf16(stream(seed, ROLE_MLP_X), (d,))
+    xf = bf16_to_f32(x).astype(np.float64)
+    W = bf16_to_f32(normal_bf16(stream(seed, ROLE_MLP_UP), (f, d))).astype(np.float64) / np.sqrt(d)
+    n_live = int(round(live * f))
+    perm = np.random.default_rng(stream(seed, ROLE_MLP_LIVE)).permutation(f)
+    t = -np.ones(f)
+    t[perm[:n_live]] = 1.0
+    xx = float(xf @ xf)
+    floor = margin * np.sqrt(xx)
+    Wb = None
+    for _ in range(8):
+        c = W @ xf
+        target = t * np.maximum(np.abs(c), floor)
+        W = W + np.outer((target - c) / xx, xf)
+        Wb = f32_to_bf16(W.astype(np.float32))
+        got = bf16_to_f32(Wb).astype(np.float64) @ xf
+        if np.all(got * t >= 0.5 * floor):
+            break
+        floor *= 2.0
+    else:
+        raise RuntimeError("make_mlp: sign control did not converge")
+    w_down = normal_bf16(stream(seed, ROLE_MLP_DOWN), (f, d))
+    w_down = f32_to_bf16((bf16_to_f32(w_down) / np.float32(np.sqrt(f))).astype(np.float32))
+    return x, Wb, w_down, t > 0
+
+
+def config_mlp(cfg: int, seed: int = 0):
+    c = CONFIGS[cfg]
+    return make_mlp(seed, c["d"], c["f"], c["live"])
 
 
 def config_full_layers(cfg: int, seed: int = 0, B: int | None = None, n: int | None = None,

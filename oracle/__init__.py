@@ -57,6 +57,7 @@ def _load():
             "oracle_window_decode_batch": [i, i, i, i, i64, i64, vp, vp, vp, d, d, vp],
             "oracle_skip_stats": [i64, vp, i64, vp, vp],
             "oracle_prefill": [i, i, i64, i64, vp, vp, i64, vp, i64, d, d, d, vp],
+            "oracle_relu2_mlp": [i64, i64, vp, vp, vp, vp, vp, vp],
             "oracle_prefill_batch": [i, i, i, i, i64, i64, i64, vp, vp, vp, d, d, d, vp],
             "oracle_skip_stats_batch": [i, i, i64, i64, vp, i64, vp, vp],
         }
@@ -193,6 +194,19 @@ def prefill_batch(q, K, V, n, alpha=1.0, c=1.0, eps=1e-6):
     _ok(_load().oracle_prefill_batch(B, Hq, Hkv, D, n, T, ncap, _p(q), _p(K), _p(V), alpha, c,
                                      eps, _p(out)), "prefill_batch")
     return out
+
+
+def relu2_mlp(x, w_up, w_down):
+    """One token through a ReLU^2 MLP: x [d], w_up and w_down [f, d] (row i = neuron i).
+    Returns (y [d], h [f], n_live)."""
+    x, w_up, w_down = f64(x), f64(w_up), f64(w_down)
+    f, d = w_up.shape
+    h = np.empty(f, dtype=np.float64)
+    y = np.empty(d, dtype=np.float64)
+    nl = np.zeros(1, dtype=np.int64)
+    _ok(_load().oracle_relu2_mlp(d, f, _p(x), _p(w_up), _p(w_down), _p(h), _p(y), _p(nl)),
+        "relu2_mlp")
+    return y, h, int(nl[0])
 
 
 def e4m3_table() -> np.ndarray:

@@ -324,6 +324,38 @@ int oracle_prefill_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t T, in
 }
 
 /*
+ * ReLU^2 MLP of one token ("The Architecture of Embla 1", section "ReLU^2 activation":
+ * negative pre-activations become zero and positive ones are squared; a zero neuron's row
+ * of the down projection contributes nothing, so at batch size 1 only the rows of the
+ * neurons that fired need reading).
+ *   x      : d
+ *   w_up   : f rows of d (row i = neuron i's input weights), stride d
+ *   w_down : f rows of d (row i = neuron i's output weights), stride d
+ *   h      : f (may be NULL): h_i = max(w_up_i . x, 0)^2
+ *   y      : d, y = sum_i h_i w_down_i over the neurons with h_i > 0
+ *   n_live : neurons with h_i > 0
+ */
+int oracle_relu2_mlp(int64_t d, int64_t f, const double *x, const double *w_up,
+                     const double *w_down, double *h, double *y, int64_t *n_live) {
+  if (d < 1 || f < 0 || !x || !w_up || !w_down || !y || !n_live) return -1;
+  for (int64_t c = 0; c < d; ++c) y[c] = 0.0;
+  int64_t live = 0;
+  for (int64_t i = 0; i < f; ++i) {
+    const double *wu = w_up + i * d;
+    double a = 0.0;
+    for (int64_t c = 0; c < d; ++c) a += wu[c] * x[c];
+    double hi = a > 0.0 ? a * a : 0.0;
+    if (h) h[i] = hi;
+    if (hi == 0.0) continue;
+    ++live;
+    const double *wd = w_down + i * d;
+    for (int64_t c = 0; c < d; ++c) y[c] += hi * wd[c];
+  }
+  *n_live = live;
+  return 0;
+}
+
+/*
  * V-read accounting of one unit ("The Architecture of Embla 1", section "Skipping V": a
  * value row is needed only when some head of the group gives its key a weight above zero,
  * i.e. sigma_j > 0; the page's kernel checks keys in groups of 8).
