@@ -29,6 +29,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode attention tokens/s and needed-byte HBM GB/s (% of roofline) at 32k–128k"
+MLP_METRIC = "ReLU^2 MLP batch-1 tokens/s and needed-byte HBM GB/s (% of roofline)"
 PREFILL_METRIC = "full-layer prefill tokens/s (causal ReLU^2 attention over the prompt) and TFLOP/s (% of bf16 tensor peak)"
 ROW_BYTES = 128 * 2          # one bf16 key or value row (head_dim 128)
 ROW_BYTES_E4M3 = 128 + 4     # one 8-bit row (E4M3 codes) and its fp32 scale
@@ -176,6 +177,9 @@ def static_config(cfg_id: int, batch=None, ctx=None) -> dict:
     """The workload's description, the same on both arms."""
     import gen
     cfg = gen.CONFIGS[cfg_id]
+    if cfg.get("kind") == "mlp":
+        return {"workload": cfg["name"], "batch": 1, "width": cfg["d"], "neurons": cfg["f"],
+                "live_fraction": cfg["live"], "weights": "bf16", "accumulate": "f32"}
     if cfg.get("kind") == "prefill":
         n = cfg["n"] if ctx is None else ctx
         return {"workload": workload_name(cfg, batch, ctx),
@@ -279,6 +283,8 @@ def run_reference(args):
     cfg = gen.CONFIGS[args.config]
     if cfg.get("kind") == "prefill":
         return run_reference_prefill(args, cfg)
+    if cfg.get("kind") == "mlp":
+        return run_reference_mlp(args, cfg)
     sample_b = 1
     fls = list(gen.config_full_layers(args.config, seed=0, B=sample_b))
     wls = list(gen.config_window_layers(args.config, seed=0, B=sample_b))
@@ -516,6 +522,172 @@ def bench_prefill(args, cfg):
     return 0
 
 
+def mlp_oracle_step(cfg_id: int):
+    import gen
+    import oracle
+    x, wu, wd, _ = gen.config_mlp(cfg_id, seed=0)
+    xf, wuf, wdf = oracle.f64(x), oracle.f64(wu), oracle.f64(wd)
+
+    def run():
+        oracle.relu2_mlp(xf, wuf, wdf)
+    return run
+
+
+def run_reference_mlp(args, cfg):
+    run = mlp_oracle_step(args.config)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": MLP_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": static_config(args.config),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "the whole token (one thread: the oracle's MLP is one loop)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_mlp(args, cfg):
+    """One step = one embla_relu2_mlp call: one token through the MLP."""
+    import numpy as np
+    import torch
+    import gen
+    import relu_sparse_kv_gb300 as E
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    x_h, wu_h, wd_h, mask = gen.config_mlp(args.config, seed=rank)
+    d, f = x_h.shape[0], wu_h.shape[0]
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    n_live = int(mask.sum())
+    needed = f * d * 2 + n_live * d * 2 + d * 2 + d * 4
+    n_rep = replicas_for(needed)
+    reps = [dict(x=bf(x_h), wu=bf(wu_h), wd=bf(wd_h), y=torch.empty(d, device=dev),
+                 nl=torch.empty(1, dtype=torch.int32, device=dev))]
+    for _ in range(n_rep - 1):
+        reps.append({k: v.clone() for k, v in reps[0].items()})
+    ws = torch.empty(max(16, E.embla_relu2_mlp_workspace_size(d, f)), dtype=torch.uint8, device=dev)
+
+    def call(r):
+        E.embla_relu2_mlp(r["x"], r["wu"], r["wd"], r["y"], r["nl"], workspace=ws)
+
+    for r in reps:
+        call(r)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    assert int(reps[0]["nl"].item()) == n_live
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(r)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_rep].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t_wall0 = time.time()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            graphs[i % n_rep].replay()
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop(t_wall0, t_wall1)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_per_step = ms / args.steps
+    value = world / (ms_per_step * 1e-3)
+    e2e = None
+    if args.e2e_steps > 0:
+        h_x = reps[0]["x"].cpu().pin_memory()
+        h_y = torch.empty(d, device="cpu").pin_memory()
+
+        def e2e_step(k):
+            r = reps[k % n_rep]
+            r["x"].copy_(h_x, non_blocking=True)
+            call(r)
+            h_y.copy_(r["y"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for k in range(3):
+            e2e_step(k)
+        t0 = time.perf_counter()
+        for k in range(args.e2e_steps):
+            e2e_step(k)
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * args.e2e_steps / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": d * 2, "d2h_bytes_per_step": d * 4, "steps": args.e2e_steps,
+               "inputs": "the token from pinned host memory, y back to host; weights resident"}
+    peak, peak_src = _peaks()
+    ach = needed / (call_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "relu2_mlp_kernel (one embla_relu2_mlp call: fused kernel + combine)",
+                "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+                "traffic": None, "algorithmic_bytes_per_launch": needed, "launch_ms": round(call_ms, 5)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        run = mlp_oracle_step(args.config)
+        reps_cpu, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            run()
+            reps_cpu += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps_cpu / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps_cpu} whole tokens (the oracle's MLP is one loop on one thread)",
+               "seconds": round(dt, 2)}
+    line = {
+        "metric": MLP_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {**static_config(args.config),
+                   "launch": "one CUDA graph per call; events around each replay",
+                   "l2": f"not flushed: the steps rotate through {n_rep} copies of the weights",
+                   "needed_bytes_per_step": needed,
+                   "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),
+                   "live_neurons": n_live,
+                   "down_projection_bytes_skipped": round(1.0 - n_live / f, 5)},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def cpu_baseline(cfg_id: int, budget_s: float = 12.0):
     """The oracle as it stands, on this host's cores, over the whole batch of one full layer
     step (full + selection + its sparse layers), repeated until ~budget_s of work."""
@@ -568,6 +740,8 @@ def main():
 
     if gen.CONFIGS[args.config].get("kind") == "prefill":
         return bench_prefill(args, gen.CONFIGS[args.config])
+    if gen.CONFIGS[args.config].get("kind") == "mlp":
+        return bench_mlp(args, gen.CONFIGS[args.config])
     world, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)

@@ -237,7 +237,27 @@ embla_status embla_prefill(const embla_shape *shape, int64_t n_new, const void *
                            void *stream);
 
 /*
- * Window-layer decode/*
+ * ReLU^2 MLP of one token at batch size 1 ("ReLU^2 activation": a neuron at or below zero
+ * contributes nothing, so only the down-projection rows of the neurons that fired are
+ * read).  h_i = max(w_up_i . x, 0)^2;  y = sum over i with h_i > 0 of h_i w_down_i.
+ * The pages' MLP shapes are not given; this call takes plain (non-gated) up and down
+ * projections.
+ *   d        width: 512, 1024 or 2048 (else EMBLA_ERR_UNSUPPORTED)
+ *   f        neurons, 1 <= f <= 2^30
+ *   x        bf16 [d]
+ *   w_up     bf16 [f, d]   row i = neuron i's input weights (read in full)
+ *   w_down   bf16 [f, d]   row i = neuron i's output weights (read only where h_i > 0)
+ *   y        fp32 [d]
+ *   n_live   int32 [1]     neurons with h_i > 0
+ *   workspace  fp32 partial sums (embla_relu2_mlp_workspace_size; 0 if d or f < 1)
+ * Sums are fp32 in a fixed order: the result is the same bits on every call.
+ */
+size_t embla_relu2_mlp_workspace_size(int64_t d, int64_t f);
+embla_status embla_relu2_mlp(int64_t d, int64_t f, const void *x, const void *w_up,
+                             const void *w_down, float *y, int32_t *n_live, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
  * Window-layer decode — "Three kinds of attention" (Sliding window).
  *   q          bf16 [B, Hq, D]   raw query; rotated here at position pos:
  *              pair (2i, 2i+1) turned by pos * rope_base^(-2i/D)

@@ -90,6 +90,8 @@ def library() -> ctypes.CDLL:
                                                          f32, vp, vp, sz, vp]),
             "embla_prefill_workspace_size": (sz, [P]),
             "embla_prefill": (ctypes.c_int, [P, i64, vp, vp, vp, f32, f32, f32, vp, vp, sz, vp]),
+            "embla_relu2_mlp_workspace_size": (sz, [i64, i64]),
+            "embla_relu2_mlp": (ctypes.c_int, [i64, i64, vp, vp, vp, vp, vp, vp, sz, vp]),
             "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
                                                                 vp, vp, vp, vp, vp]),
             "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
@@ -310,6 +312,29 @@ def embla_prefill(shape: Shape, q, k_cache, v_cache, out, alpha: float = 1.0, c:
     ws = _workspace(embla_prefill_workspace_size(shape), workspace, q.device)
     _call("embla_prefill", ctypes.byref(shape.c()), T, _ptr(q), _ptr(k_cache), _ptr(v_cache),
           alpha, c, eps, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_relu2_mlp_workspace_size(d: int, f: int) -> int:
+    return library().embla_relu2_mlp_workspace_size(d, f)
+
+
+def embla_relu2_mlp(x, w_up, w_down, y, n_live, workspace=None, stream=None):
+    """One token through a ReLU^2 MLP: x bf16 [d], w_up and w_down bf16 [f, d] (row i =
+    neuron i), y fp32 [d], n_live int32 [1] (neurons that fired)."""
+    _check(x, torch.bfloat16, None, "x")
+    if x.dim() != 1:
+        raise ValueError("x must be [d]")
+    d = x.shape[0]
+    _check(w_up, torch.bfloat16, None, "w_up")
+    if w_up.dim() != 2 or w_up.shape[1] != d:
+        raise ValueError("w_up must be [f, d]")
+    f = w_up.shape[0]
+    _check(w_down, torch.bfloat16, (f, d), "w_down")
+    _check(y, torch.float32, (d,), "y")
+    _check(n_live, torch.int32, (1,), "n_live")
+    ws = _workspace(embla_relu2_mlp_workspace_size(d, f), workspace, x.device)
+    _call("embla_relu2_mlp", d, f, _ptr(x), _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(n_live),
+          _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
 def embla_window_decode(shape: Shape, q, k_win, v_win, pos: int, out, window: int = 128,

@@ -458,6 +458,28 @@ embla_status embla_prefill(const embla_shape *shape, int64_t n_new, const void *
                                     static_cast<cudaStream_t>(stream)));
 }
 
+size_t embla_relu2_mlp_workspace_size(int64_t d, int64_t f) {
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0 || d < 1 || f < 1) return 0;
+  return mlp_workspace_bytes(d, f, sms);
+}
+
+embla_status embla_relu2_mlp(int64_t d, int64_t f, const void *x, const void *w_up,
+                             const void *w_down, float *y, int32_t *n_live, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  if (d != 512 && d != 1024 && d != 2048) return d < 1 ? EMBLA_ERR_INVALID_ARG : EMBLA_ERR_UNSUPPORTED;
+  if (f < 1 || f > (static_cast<int64_t>(1) << 30)) return EMBLA_ERR_INVALID_ARG;
+  if (!x || !w_up || !w_down || !y || !n_live || !workspace) return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(y) ||
+      !aligned16(n_live) || !aligned16(workspace))
+    return EMBLA_ERR_INVALID_ARG;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return EMBLA_ERR_CUDA;
+  if (workspace_bytes < mlp_workspace_bytes(d, f, sms)) return EMBLA_ERR_WORKSPACE;
+  return cuda_status(launch_relu2_mlp(x, w_up, w_down, d, f, y, n_live, workspace, sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 size_t embla_window_decode_workspace_size(const embla_shape *shape, int32_t window) {
   (void)shape;
   (void)window;

@@ -106,6 +106,15 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k, con
                            uint32_t *flags, int B, int Hq, int Hkv, int64_t n, int64_t T,
                            int64_t ncap, float alpha, float c, float eps, cudaStream_t stream);
 
+// ReLU^2 MLP of one token (d in {512, 1024, 2048}; at most kMlpMaxNeuronsPerCta neurons
+// per CTA): the fused kernel's partials and live counts in the workspace, then a combine.
+constexpr int kMlpMaxNeuronsPerCta = 1024;
+int mlp_ctas(int64_t f, int sm_count);
+size_t mlp_workspace_bytes(int64_t d, int64_t f, int sm_count);
+cudaError_t launch_relu2_mlp(const void *x, const void *w_up, const void *w_down, int64_t d,
+                             int64_t f, float *y, int32_t *n_live, void *workspace, int sm_count,
+                             cudaStream_t stream);
+
 cudaError_t launch_window_decode(int G, const void *q, const void *k_win, const void *v_win,
                                  int64_t units, int window, int64_t pos, float rope_base,
                                  float tau, float *out, cudaStream_t stream);
