@@ -214,6 +214,40 @@ embla_status embla_sparse_decode_e4m3(const embla_shape *shape, const void *q,
                                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Selection per query head — the other reading of which score the selection ranks
+ * ("Three kinds of attention", Sparse: "the 1,024 keys that layer scored highest" under
+ * grouped queries): every query head h ranks the keys by its own score s_hj and keeps its
+ * own top-1024 plus the newest 128; the sparse layer's head h then attends over its own
+ * set.  Three calls, used in this order:
+ *
+ * embla_full_decode_head_scores: the full-layer decode (out and n_surv exactly as
+ *   embla_full_decode) that writes each head's scores instead of the group's:
+ *   head_scores fp32 [B, Hq, cache_stride] (s_hj for j < n; rows >= n not written) and
+ *   head_hist uint32 [B, Hq, 2048] (the order-key histogram of each head's scores).
+ *   Workspace: embla_full_decode_workspace_size.
+ * embla_select_topk_per_head: embla_select_topk over the B*Hq units of those scores:
+ *   idx int32 [B, Hq, idx_stride], count int32 [B, Hq].
+ * embla_sparse_decode_per_head: embla_sparse_decode where query head h reads its own
+ *   idx[b, h] rows of KV head h / G (workspace: embla_sparse_decode_workspace_size).
+ */
+embla_status embla_full_decode_head_scores(const embla_shape *shape, const void *q,
+                                           const void *k_cache, const void *v_cache, float alpha,
+                                           float c, float eps, float *out, int32_t *n_surv,
+                                           float *head_scores, uint32_t *head_hist,
+                                           void *workspace, size_t workspace_bytes, void *stream);
+size_t embla_select_topk_per_head_workspace_size(const embla_shape *shape, int32_t topk,
+                                                  int32_t recent);
+embla_status embla_select_topk_per_head(const embla_shape *shape, const float *head_scores,
+                                        const uint32_t *head_hist, int32_t topk, int32_t recent,
+                                        int32_t *idx, int32_t idx_stride, int32_t *count,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+embla_status embla_sparse_decode_per_head(const embla_shape *shape, const void *q,
+                                          const void *k_cache, const void *v_cache,
+                                          const int32_t *idx, int32_t idx_stride,
+                                          const int32_t *count, float tau, float *out,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Full-layer prefill — causal ReLU^2 attention over a prompt ("KV bridge, KV reuse, and
  * prefill": the early layers run on every prompt token; "Sevren Sparse Attention learns
  * to be sparse": the same weights as embla_full_decode).  The prompt's n_new tokens are

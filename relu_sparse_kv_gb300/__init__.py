@@ -92,6 +92,13 @@ def library() -> ctypes.CDLL:
             "embla_prefill": (ctypes.c_int, [P, i64, vp, vp, vp, f32, f32, f32, vp, vp, sz, vp]),
             "embla_relu2_mlp_workspace_size": (sz, [i64, i64]),
             "embla_relu2_mlp": (ctypes.c_int, [i64, i64, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "embla_full_decode_head_scores": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32, vp, vp,
+                                                              vp, vp, vp, sz, vp]),
+            "embla_select_topk_per_head_workspace_size": (sz, [P, i32, i32]),
+            "embla_select_topk_per_head": (ctypes.c_int, [P, vp, vp, i32, i32, vp, i32, vp, vp, sz,
+                                                           vp]),
+            "embla_sparse_decode_per_head": (ctypes.c_int, [P, vp, vp, vp, vp, i32, vp, f32, vp, vp,
+                                                             sz, vp]),
             "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
                                                                 vp, vp, vp, vp, vp]),
             "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
@@ -335,6 +342,64 @@ def embla_relu2_mlp(x, w_up, w_down, y, n_live, workspace=None, stream=None):
     ws = _workspace(embla_relu2_mlp_workspace_size(d, f), workspace, x.device)
     _call("embla_relu2_mlp", d, f, _ptr(x), _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(n_live),
           _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_full_decode_head_scores(shape: Shape, q, k_cache, v_cache, out, n_surv, head_scores,
+                                  head_hist, alpha: float = 1.0, c: float = 1.0, eps: float = 1e-6,
+                                  workspace=None, stream=None):
+    """embla_full_decode writing every query head's own scores: head_scores fp32
+    [B, Hq, cache_stride], head_hist int32 [B, Hq, 2048]."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    _check(n_surv, torch.int32, (B, Hkv), "n_surv")
+    _check(head_scores, torch.float32, (B, Hq, ncap), "head_scores")
+    _check(head_hist, torch.int32, (B, Hq, HIST_BINS), "head_hist")
+    ws = _workspace(embla_full_decode_workspace_size(shape), workspace, q.device)
+    _call("embla_full_decode_head_scores", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache),
+          _ptr(v_cache), alpha, c, eps, _ptr(out), _ptr(n_surv), _ptr(head_scores),
+          _ptr(head_hist), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_select_topk_per_head(shape: Shape, head_scores, head_hist, idx, count, topk: int = 1024,
+                               recent: int = 128, workspace=None, stream=None):
+    """Each query head's own top-k + recent: idx int32 [B, Hq, stride], count int32 [B, Hq]."""
+    B, Hq, ncap = shape.batch, shape.n_q_heads, shape.cache_stride
+    _check(head_scores, torch.float32, (B, Hq, ncap), "head_scores")
+    _check(head_hist, torch.int32, (B, Hq, HIST_BINS), "head_hist")
+    _check(idx, torch.int32, None, "idx")
+    if idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hq):
+        raise ValueError("idx must be [B, Hq, idx_stride]")
+    _check(count, torch.int32, (B, Hq), "count")
+    nbytes = library().embla_select_topk_per_head_workspace_size(ctypes.byref(shape.c()), topk,
+                                                                 recent)
+    ws = _workspace(nbytes, workspace, head_scores.device)
+    _call("embla_select_topk_per_head", ctypes.byref(shape.c()), _ptr(head_scores),
+          _ptr(head_hist), topk, recent, _ptr(idx), idx.shape[2], _ptr(count), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_sparse_decode_per_head(shape: Shape, q, k_cache, v_cache, idx, count, out,
+                                 tau: float | None = None, workspace=None, stream=None):
+    """embla_sparse_decode where query head h reads its own selection idx[b, h]."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(idx, torch.int32, None, "idx")
+    if idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hq):
+        raise ValueError("idx must be [B, Hq, idx_stride]")
+    _check(count, torch.int32, (B, Hq), "count")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    tau = D ** -0.5 if tau is None else tau
+    ws = _workspace(embla_sparse_decode_workspace_size(shape, idx.shape[2]), workspace, q.device)
+    _call("embla_sparse_decode_per_head", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache),
+          _ptr(v_cache), _ptr(idx), idx.shape[2], _ptr(count), tau, _ptr(out), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
 
 
 def embla_window_decode(shape: Shape, q, k_win, v_win, pos: int, out, window: int = 128,

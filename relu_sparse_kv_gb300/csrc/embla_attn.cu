@@ -200,7 +200,8 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
                               const float *k_scales, const void *v_cache, const float *v_scales,
                               bool kv8, float alpha, float c, float eps, float *out,
                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
-                              void *workspace, size_t workspace_bytes, void *stream) {
+                              void *workspace, size_t workspace_bytes, void *stream,
+                              float *head_scores = nullptr, uint32_t *head_hist = nullptr) {
   int G = 0;
   embla_status st = check_shape(shape, &G, true);
   if (st != EMBLA_OK) return st;
@@ -215,6 +216,9 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
   if (kv8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
     return EMBLA_ERR_INVALID_ARG;
   if ((sel_scores == nullptr) != (sel_hist == nullptr)) return EMBLA_ERR_INVALID_ARG;
+  if ((head_scores == nullptr) != (head_hist == nullptr)) return EMBLA_ERR_INVALID_ARG;
+  if (head_scores && (!aligned16(head_scores) || !aligned16(head_hist)))
+    return EMBLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(workspace) || (sel_scores && (!aligned16(sel_scores) || !aligned16(sel_hist))))
     return EMBLA_ERR_INVALID_ARG;
@@ -233,6 +237,9 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
     // no keys: every output is 0, nothing survives, the histogram is empty
     if (sel_scores)
       st = cuda_status(cudaMemsetAsync(sel_hist, 0, static_cast<size_t>(units) * kHistBins * 4, s));
+    if (st == EMBLA_OK && head_scores)
+      st = cuda_status(cudaMemsetAsync(head_hist, 0,
+                                       static_cast<size_t>(shape->batch) * shape->n_q_heads * kHistBins * 4, s));
     if (st == EMBLA_OK)
       st = cuda_status(cudaMemsetAsync(out, 0, static_cast<size_t>(units) * G * kHeadDim * 4, s));
     if (st == EMBLA_OK) st = cuda_status(cudaMemsetAsync(n_surv, 0, static_cast<size_t>(units) * 4, s));
@@ -254,12 +261,16 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
               !encode_scales(&tm_vs, v_scales, static_cast<uint64_t>(units),
                              static_cast<uint64_t>(shape->cache_stride))))
     return EMBLA_ERR_CUDA;
-  return cuda_status(launch_full_decode(G, kv8, tm_k, tm_q, kv8 ? &tm_ks : nullptr,
-                                        kv8 ? &tm_vs : nullptr, v_cache, sel_scores, sel_hist,
-                                        workspace, arrivals, out, n_surv, c, flags, sp,
-                                        shape->ctx_len,
-                                        shape->cache_stride, shape->n_q_heads, shape->n_kv_heads,
-                                        alpha, eps, s));
+  st = cuda_status(launch_full_decode(G, kv8, tm_k, tm_q, kv8 ? &tm_ks : nullptr,
+                                      kv8 ? &tm_vs : nullptr, v_cache, sel_scores, head_scores,
+                                      sel_hist, workspace, arrivals, out, n_surv, c, flags, sp,
+                                      shape->ctx_len, shape->cache_stride, shape->n_q_heads,
+                                      shape->n_kv_heads, alpha, eps, s));
+  if (st == EMBLA_OK && head_scores)
+    st = cuda_status(launch_score_hist(head_scores,
+                                       static_cast<int64_t>(shape->batch) * shape->n_q_heads,
+                                       shape->ctx_len, shape->cache_stride, head_hist, s));
+  return st;
 }
 
 }  // namespace
@@ -272,6 +283,17 @@ embla_status embla_full_decode(const embla_shape *shape, const void *q, const vo
                                void *workspace, size_t workspace_bytes, void *stream) {
   return full_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, alpha, c, eps,
                           out, n_surv, sel_scores, sel_hist, workspace, workspace_bytes, stream);
+}
+
+embla_status embla_full_decode_head_scores(const embla_shape *shape, const void *q,
+                                           const void *k_cache, const void *v_cache, float alpha,
+                                           float c, float eps, float *out, int32_t *n_surv,
+                                           float *head_scores, uint32_t *head_hist,
+                                           void *workspace, size_t workspace_bytes, void *stream) {
+  if (!head_scores || !head_hist) return EMBLA_ERR_INVALID_ARG;
+  return full_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, alpha, c, eps,
+                          out, n_surv, nullptr, nullptr, workspace, workspace_bytes, stream,
+                          head_scores, head_hist);
 }
 
 embla_status embla_full_decode_e4m3(const embla_shape *shape, const void *q,
@@ -340,6 +362,42 @@ embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores
                                    workspace, flags, sms, static_cast<cudaStream_t>(stream)));
 }
 
+size_t embla_select_topk_per_head_workspace_size(const embla_shape *shape, int32_t topk,
+                                                  int32_t recent) {
+  int G = 0;
+  if (check_shape(shape, &G, true) != EMBLA_OK || topk < 0 || recent < 0) return 0;
+  return select_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_q_heads,
+                                shape->ctx_len);
+}
+
+embla_status embla_select_topk_per_head(const embla_shape *shape, const float *head_scores,
+                                        const uint32_t *head_hist, int32_t topk, int32_t recent,
+                                        int32_t *idx, int32_t idx_stride, int32_t *count,
+                                        void *workspace, size_t workspace_bytes, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, true);
+  if (st != EMBLA_OK) return st;
+  if (topk < 0 || recent < 0 || static_cast<int64_t>(topk) + recent > INT32_MAX ||
+      idx_stride < topk + recent)
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_q_heads;
+  if (units == 0) return EMBLA_OK;
+  const size_t ws_need = select_workspace_bytes(units, shape->ctx_len);
+  if (!head_scores || !head_hist || !idx || !count || (ws_need && !workspace))
+    return EMBLA_ERR_INVALID_ARG;
+  if (!aligned16(head_scores) || !aligned16(head_hist) || !aligned16(idx) || !aligned16(count) ||
+      (workspace && !aligned16(workspace)))
+    return EMBLA_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_need) return EMBLA_ERR_WORKSPACE;
+  uint32_t *flags = flags_ptr();
+  if (!flags) return EMBLA_ERR_CUDA;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return EMBLA_ERR_CUDA;
+  return cuda_status(launch_select(head_scores, head_hist, units, shape->ctx_len,
+                                   shape->cache_stride, topk, recent, idx, idx_stride, count,
+                                   workspace, flags, sms, static_cast<cudaStream_t>(stream)));
+}
+
 size_t embla_sparse_decode_workspace_size(const embla_shape *shape, int32_t idx_stride) {
   int G = 0;
   if (check_shape(shape, &G, true) != EMBLA_OK || idx_stride < 0) return 0;
@@ -355,12 +413,14 @@ embla_status sparse_decode_impl(const embla_shape *shape, const void *q, const v
                                 const float *k_scales, const void *v_cache,
                                 const float *v_scales, bool kv8, const int32_t *idx,
                                 int32_t idx_stride, const int32_t *count, float tau, float *out,
-                                void *workspace, size_t workspace_bytes, void *stream) {
+                                void *workspace, size_t workspace_bytes, void *stream,
+                                bool per_head = false) {
   int G = 0;
   embla_status st = check_shape(shape, &G, true);
   if (st != EMBLA_OK) return st;
   if (!finite(tau) || idx_stride < 0) return EMBLA_ERR_INVALID_ARG;
-  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  const int64_t units = static_cast<int64_t>(shape->batch) *
+                       (per_head ? shape->n_q_heads : shape->n_kv_heads);
   if (units == 0) return EMBLA_OK;
   if (!q || !k_cache || !v_cache || !idx || !count || !out || !workspace)
     return EMBLA_ERR_INVALID_ARG;
@@ -374,7 +434,8 @@ embla_status sparse_decode_impl(const embla_shape *shape, const void *q, const v
   if (!flags) return EMBLA_ERR_CUDA;
   const int sms = sm_count_of(current_device());
   if (sms <= 0) return EMBLA_ERR_CUDA;
-  return cuda_status(launch_sparse_decode(G, q, k_cache, v_cache, kv8 ? k_scales : nullptr,
+  return cuda_status(launch_sparse_decode(G, per_head, shape->n_q_heads, q, k_cache, v_cache,
+                                          kv8 ? k_scales : nullptr,
                                           kv8 ? v_scales : nullptr, idx, idx_stride, count,
                                           units, shape->n_kv_heads, shape->ctx_len,
                                           shape->cache_stride, tau, out, workspace, flags, sms,
@@ -391,6 +452,15 @@ embla_status embla_sparse_decode(const embla_shape *shape, const void *q, const 
                                  size_t workspace_bytes, void *stream) {
   return sparse_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, idx, idx_stride,
                             count, tau, out, workspace, workspace_bytes, stream);
+}
+
+embla_status embla_sparse_decode_per_head(const embla_shape *shape, const void *q,
+                                          const void *k_cache, const void *v_cache,
+                                          const int32_t *idx, int32_t idx_stride,
+                                          const int32_t *count, float tau, float *out,
+                                          void *workspace, size_t workspace_bytes, void *stream) {
+  return sparse_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, idx, idx_stride,
+                            count, tau, out, workspace, workspace_bytes, stream, true);
 }
 
 embla_status embla_sparse_decode_e4m3(const embla_shape *shape, const void *q,

@@ -148,6 +148,7 @@ struct FullParams {
   const uint8_t *v;  // V cache (bf16 rows or E4M3 codes)
   float *sel;        // selection scores or null
   uint32_t *hist;    // selection histogram or null
+  float *hsel;       // per-head scores [B, Hq, ncap] or null
   float *rec;        // partial records
   int32_t *arrivals; // per unit and accumulator warp: record parts published so far (zeroed by the host call)
   float *out;        // [units][G][D]
@@ -635,6 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc[h] = dot[h] * aq[h] * rk;
         sigma = fmaxf(sigma, sc[h]);
       }
+      if (p.hsel != nullptr && valid) {
+        // every head's own score, for a selection per query head
+        float *hs = p.hsel + (static_cast<int64_t>(u / p.Hkv) * p.Hq + (u % p.Hkv) * G) * p.ncap + j;
+#pragma unroll
+        for (int h = 0; h < G; ++h) hs[h * p.ncap] = sc[h];
+      }
       WSlot<G, KV8> &ws = wslots[slot];
       if (p.sel != nullptr) {
         ws.sig[row] = sigma;
@@ -1077,7 +1084,7 @@ int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count) {
 
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
-                               const void *v_cache, float *sel_scores,
+                               const void *v_cache, float *sel_scores, float *head_scores,
                                uint32_t *sel_hist, void *workspace, int32_t *arrivals,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
@@ -1088,6 +1095,7 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
   p.v = static_cast<const uint8_t *>(v_cache);
   p.sel = sel_scores;
   p.hist = sel_hist;
+  p.hsel = head_scores;
   p.rec = static_cast<float *>(workspace);
   p.arrivals = arrivals;
   p.out = out;

@@ -72,7 +72,7 @@ int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count);
 // kv8: 8-bit E4M3 caches; tm_ks / tm_vs then map the K and V scales as [units, ncap] fp32.
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
-                               const void *v_cache, float *sel_scores,
+                               const void *v_cache, float *sel_scores, float *head_scores,
                                uint32_t *sel_hist, void *workspace, int32_t *arrivals,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
@@ -80,6 +80,9 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
                                cudaStream_t stream);
 
 size_t select_workspace_bytes(int64_t units, int64_t ctx_len);
+// hist[u] = 2048-bin counts of the order keys' top 11 bits of scores[u][0..n) (every unit).
+cudaError_t launch_score_hist(const float *scores, int64_t units, int64_t n, int64_t ncap,
+                              uint32_t *hist, cudaStream_t stream);
 cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int64_t units,
                           int64_t n, int64_t ncap, int topk, int recent, int32_t *idx,
                           int idx_stride, int32_t *count, void *workspace, uint32_t *flags,
@@ -87,7 +90,10 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
 
 size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride);
 // k_scales / v_scales: per-token scales of 8-bit E4M3 caches, or both null for bf16 caches.
-cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
+// per_head: one unit per (sequence, query head) with its own selection (G then 1, the
+// cache plane of unit u is (u / Hq) * Hkv + (u % Hq) / (Hq / Hkv)).
+cudaError_t launch_sparse_decode(int G, bool per_head, int Hq, const void *q, const void *k_cache,
+                                 const void *v_cache,
                                  const float *k_scales, const float *v_scales, const int32_t *idx, int idx_stride, const int32_t *count,
                                  int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
                                  float *out, void *workspace, uint32_t *flags, int sm_count,

@@ -921,4 +921,30 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
                     stream, 0u, p);
 }
 
+namespace {
+
+// hist[u][b] = number of keys j < n of unit u whose score's order key has top 11 bits b.
+__global__ void __launch_bounds__(512) score_hist_kernel(const float *scores, int64_t n, int64_t ncap,
+                                                         uint32_t *hist) {
+  pdl_wait_primary();  // the scores are complete
+  pdl_launch_dependents();
+  __shared__ uint32_t s_h[kHistBins];
+  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) s_h[b] = 0u;
+  __syncthreads();
+  const int64_t u = blockIdx.x;
+  const float *su = scores + u * ncap;
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) atomicAdd(&s_h[order_key(su[j]) >> 21], 1u);
+  __syncthreads();
+  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) hist[u * kHistBins + b] = s_h[b];
+}
+
+}  // namespace
+
+cudaError_t launch_score_hist(const float *scores, int64_t units, int64_t n, int64_t ncap,
+                              uint32_t *hist, cudaStream_t stream) {
+  if (units == 0) return cudaSuccess;
+  return launch_pdl(score_hist_kernel, dim3(static_cast<unsigned>(units)), dim3(512), 0, stream, 0u,
+                    scores, n, ncap, hist);
+}
+
 }  // namespace embla

@@ -308,6 +308,12 @@ struct SparseParams {
   int idx_stride, rows_per_cta;
   int cl;  // CTAs per unit (the cluster size): 1, 2, 4 or 8
   float tau;
+  // cache plane of unit u: u itself, or for a selection per query head (one unit per
+  // (sequence, query head)) (u / Hq) * Hkv + (u % Hq) / Gq
+  int per_head, Hq, Hkv, Gq;
+  __device__ int64_t plane(int64_t u) const {
+    return per_head ? (u / Hq) * Hkv + (u % Hq) / Gq : u;
+  }
 };
 
 // byte offset of 16-byte piece c of staged row r
@@ -398,8 +404,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
   int cnt = p.count[u];
   cnt = cnt < 0 ? 0 : (cnt > p.idx_stride ? p.idx_stride : cnt);
   const int32_t *idx = p.idx + u * p.idx_stride;
-  const uint8_t *Ku = p.K + u * p.ncap * kRowBytes;
-  const uint8_t *Vu = p.V + u * p.ncap * kRowBytes;
+  const uint8_t *Ku = p.K + p.plane(u) * p.ncap * kRowBytes;
+  const uint8_t *Vu = p.V + p.plane(u) * p.ncap * kRowBytes;
   const float tau2 = p.tau * kLog2e;
   uint8_t *sK = smem + warp * kSpStage;
   uint8_t *sV = sK + kSpBlock * kRowBytes;
@@ -557,10 +563,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
   int cnt = p.count[u];
   cnt = cnt < 0 ? 0 : (cnt > p.idx_stride ? p.idx_stride : cnt);
   const int32_t *idx = p.idx + u * p.idx_stride;
-  const uint8_t *Ku = p.K + u * p.ncap * kSp8Row;
-  const uint8_t *Vu = p.V + u * p.ncap * kSp8Row;
-  const float *ksu = p.ks + u * p.ncap;
-  const float *vsu = p.vs + u * p.ncap;
+  const uint8_t *Ku = p.K + p.plane(u) * p.ncap * kSp8Row;
+  const uint8_t *Vu = p.V + p.plane(u) * p.ncap * kSp8Row;
+  const float *ksu = p.ks + p.plane(u) * p.ncap;
+  const float *vsu = p.vs + p.plane(u) * p.ncap;
   uint8_t *sK = smem + warp * kSp8Stage;
   uint8_t *sV = sK + kSpBlock * kSp8Row;
   float *sW = reinterpret_cast<float *>(sV + kSpBlock * kSp8Row);  // [16 rows][8 heads]
@@ -817,6 +823,14 @@ cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const Spars
 
 template <int G>
 cudaError_t launch_sparse_g(dim3 grid, const SparseParams &p, cudaStream_t stream) {
+  if constexpr (G == 1) {
+    switch (p.cl) {
+      case 8: return launch_sparse_t<false>(sparse_decode_kernel<1, 8>, grid, p, stream);
+      case 4: return launch_sparse_t<false>(sparse_decode_kernel<1, 4>, grid, p, stream);
+      case 2: return launch_sparse_t<false>(sparse_decode_kernel<1, 2>, grid, p, stream);
+      default: return launch_sparse_t<false>(sparse_decode_kernel<1, 1>, grid, p, stream);
+    }
+  }
   if (p.ks != nullptr) {
     switch (p.cl) {
       case 8: return launch_sparse_t<true>(sparse_decode_e4m3_kernel<G, 8>, grid, p, stream);
@@ -842,7 +856,8 @@ size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride) {
   return 0;
 }
 
-cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, const void *v_cache,
+cudaError_t launch_sparse_decode(int G, bool per_head, int Hq, const void *q, const void *k_cache,
+                                 const void *v_cache,
                                  const float *k_scales, const float *v_scales, const int32_t *idx, int idx_stride, const int32_t *count,
                                  int64_t units, int Hkv, int64_t n, int64_t ncap, float tau,
                                  float *out, void *workspace, uint32_t *flags, int sm_count,
@@ -869,7 +884,16 @@ cudaError_t launch_sparse_decode(int G, const void *q, const void *k_cache, cons
   p.cl = cl;
   p.rows_per_cta = ((idx_stride + cl - 1) / cl + kSpBlock - 1) / kSpBlock * kSpBlock;
   p.tau = tau;
+  p.per_head = per_head ? 1 : 0;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Gq = Hq / Hkv;
   const dim3 grid(static_cast<unsigned>(units * cl));
+  if (per_head) {
+    // one query head per unit (its own rows); 8-bit caches are not built for this variant
+    if (k_scales != nullptr) return cudaErrorInvalidValue;
+    return launch_sparse_g<1>(grid, p, stream);
+  }
   if (G == 4) return launch_sparse_g<4>(grid, p, stream);
   if (G == 8) return launch_sparse_g<8>(grid, p, stream);
   return cudaErrorInvalidValue;
