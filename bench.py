@@ -757,6 +757,7 @@ def main():
     def to_dev_raw(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
+    per_head = cfg.get("select") == "per_head"
     layers = []
     for fl in fls:
         B, Hq, D = fl.q.shape
@@ -769,15 +770,18 @@ def main():
             L = dict(fl=fl, shape=shape, q=to_dev(fl.q), K=to_dev(fl.K), V=to_dev(fl.V),
                      qs=[to_dev(x) for x in fl.sparse_q])
         L["out"] = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+        L["per_head"] = per_head
         L["n_surv"] = torch.empty(B, Hkv, dtype=torch.int32, device=dev)
         need_sel = len(fl.sparse_q) > 0
-        L["sel"] = torch.empty(B, Hkv, ncap, dtype=torch.float32, device=dev) if need_sel else None
-        L["hist"] = torch.empty(B, Hkv, E.HIST_BINS, dtype=torch.int32, device=dev) if need_sel else None
-        L["idx"] = torch.empty(B, Hkv, TOPK + RECENT, dtype=torch.int32, device=dev)
-        L["count"] = torch.empty(B, Hkv, dtype=torch.int32, device=dev)
+        Hs = Hq if per_head else Hkv  # units of the selection
+        L["sel"] = torch.empty(B, Hs, ncap, dtype=torch.float32, device=dev) if need_sel else None
+        L["hist"] = torch.empty(B, Hs, E.HIST_BINS, dtype=torch.int32, device=dev) if need_sel else None
+        L["idx"] = torch.empty(B, Hs, TOPK + RECENT, dtype=torch.int32, device=dev)
+        L["count"] = torch.empty(B, Hs, dtype=torch.int32, device=dev)
         L["souts"] = [torch.empty(B, Hq, D, dtype=torch.float32, device=dev) for _ in fl.sparse_q]
         L["ws_full"] = torch.empty(E.embla_full_decode_workspace_size(shape), dtype=torch.uint8, device=dev)
-        L["ws_sel"] = torch.empty(max(16, E.embla_select_topk_workspace_size(shape)), dtype=torch.uint8, device=dev)
+        L["ws_sel"] = torch.empty(max(16, E.embla_select_topk_workspace_size(shape) * (Hq // Hkv if per_head else 1)),
+                                  dtype=torch.uint8, device=dev)
         L["ws_sp"] = torch.empty(max(16, E.embla_sparse_decode_workspace_size(shape, TOPK + RECENT)),
                                  dtype=torch.uint8, device=dev)
         layers.append(L)
@@ -789,6 +793,11 @@ def main():
                          V=to_dev(wl.V), out=torch.empty(B, Hq, D, dtype=torch.float32, device=dev)))
 
     def full_call(L):
+        if L["per_head"]:
+            E.embla_full_decode_head_scores(L["shape"], L["q"], L["K"], L["V"], L["out"], L["n_surv"],
+                                            L["sel"], L["hist"], alpha=1.0, c=1.0, eps=1e-6,
+                                            workspace=L["ws_full"])
+            return
         if "Ks" in L:
             E.embla_full_decode_e4m3(L["shape"], L["q"], L["K"], L["Ks"], L["V"], L["Vs"], L["out"],
                                      L["n_surv"], L["sel"], L["hist"], alpha=1.0, c=1.0, eps=1e-6,
@@ -799,6 +808,13 @@ def main():
 
     def rest_calls(L):
         if not L["qs"]:
+            return
+        if L["per_head"]:
+            E.embla_select_topk_per_head(L["shape"], L["sel"], L["hist"], L["idx"], L["count"], TOPK,
+                                         RECENT, workspace=L["ws_sel"])
+            for qs, so in zip(L["qs"], L["souts"]):
+                E.embla_sparse_decode_per_head(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"],
+                                               so, workspace=L["ws_sp"])
             return
         E.embla_select_topk(L["shape"], L["sel"], L["hist"], L["idx"], L["count"], TOPK, RECENT,
                             workspace=L["ws_sel"])
@@ -920,21 +936,22 @@ def main():
     # the same V reads counted at the page's granularity (8-key chunks)
     chunk_rows = 0
     for L in layers:
-        if L["sel"] is None:
+        if L["sel"] is None or L["per_head"]:
+            # no group scores to count chunks on (per-head scores rank differently)
             chunk_rows += L["shape"].units * L["fl"].n
             continue
         kn = torch.empty(L["shape"].batch, L["shape"].n_kv_heads, dtype=torch.int32, device=dev)
         cn = torch.empty_like(kn)
         E.embla_skip_stats(L["shape"], L["sel"], kn, cn, chunk=8)
         chunk_rows += min(int(cn.sum().item()) * 8, L["shape"].units * L["fl"].n)
-    skipped_v_chunk8 = 1.0 - chunk_rows / max(1, keys_total)
+    skipped_v_chunk8 = None if per_head else 1.0 - chunk_rows / max(1, keys_total)
     batch = layers[0]["shape"].batch
     # kernels of this library per step: per full layer a zeroing kernel and the decode
     # kernel, one selection kernel and one kernel per sparse layer, one window kernel per
     # window layer
     launches_per_step = 0
     for L in layers:
-        launches_per_step += 2
+        launches_per_step += 3 if L["per_head"] else 2  # (+ the per-head score histograms)
         if L["qs"]:
             launches_per_step += 1 + len(L["qs"])
     launches_per_step += len(wins)
@@ -1062,7 +1079,8 @@ def main():
                    "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),
                    "needed_frac_of_peak": round(needed / (ms_per_step * 1e-3) / 1e9 / peak, 4),
                    "skipped_v_fraction": round(skipped_v, 5),
-                   "skipped_v_fraction_8key_chunks": round(skipped_v_chunk8, 5)},
+                   "skipped_v_fraction_8key_chunks": None if skipped_v_chunk8 is None else round(skipped_v_chunk8, 5),
+                   "selection": "per query head" if per_head else "per KV head (group max)"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clk,
     }

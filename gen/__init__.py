@@ -289,6 +289,9 @@ CONFIGS = {
     # a ReLU^2 MLP at batch 1 with 22 % of its neurons firing (the page reports 78 % of the
     # down-projection bytes saved)
     9: dict(name="relu2-mlp-b1-d2048-f8192-live0.22", kind="mlp", d=2048, f=8192, live=0.22),
+    # the benchmarked workload with a selection per query head instead of per KV head
+    10: dict(name="per-head-select-full+3sparse-b8-n32k-f0.05", B=8, n=32768, pattern="subset",
+             frac=0.05, sparse=(1, 2, 3), select="per_head"),
 }
 HQ, HKV, HEAD_DIM, WINDOW, ROPE_BASE = 16, 4, 128, 128, 10000.0
 
