@@ -5,12 +5,12 @@
 // down projection contributes nothing, so at batch size 1 a kernel reads only the rows of
 // the neurons that fired.
 //
-// relu2_mlp_kernel: one CTA per SM over a contiguous range of neurons, 8 warps.
+// relu2_mlp_kernel: one CTA per SM over a contiguous range of neurons, 16 warps.
 //   phase 1  each warp takes neurons in turn, two rows in flight: h_i = max(w_up_i . x, 0)^2
 //            with exact bf16 products summed in fp32 (the token x stays in registers);
 //   phase 2  the CTA's neurons with h_i > 0 are listed in ascending order; warp w owns
-//            columns d/8 w .. d/8 (w+1) - 1 of y and, for every listed neuron, reads its
-//            d/4 bytes of that neuron's down-projection row (eight rows in flight per lane):
+//            columns d/16 w .. d/16 (w+1) - 1 of y and, for every listed neuron, reads its
+//            d/8 bytes of that neuron's down-projection row (eight rows in flight per lane):
 //            y += h_i w_down_i in fp32; the CTA's partial y goes to the workspace.
 // relu2_mlp_combine_kernel: y = the CTAs' partials summed in CTA order (eight threads per
 //            column, then a fixed-order sum of their parts), and the live-neuron count.
@@ -20,7 +20,7 @@
 namespace embla {
 namespace {
 
-constexpr int kMlpWarps = 8;
+constexpr int kMlpWarps = 16;
 constexpr int kMlpThreads = kMlpWarps * 32;
 
 struct MlpParams {
@@ -56,8 +56,8 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// KC = d / 256: the 16-byte chunks of a row per lane in phase 1, and the columns of y per
-// lane in phase 2 (d / 8 per warp).
+// KC = d / 256: the 16-byte chunks of a row per lane in phase 1; phase 2 gives each lane
+// KC / 2 columns of y (d / 16 per warp).
 template <int KC>
 __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpParams p) {
   pdl_wait_primary();  // the token is complete
@@ -118,30 +118,27 @@ __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpPara
   __syncthreads();
   // ---- phase 2: this warp's columns of y over the listed rows
   const int nlive = s_nlive;
-  const int64_t c0 = static_cast<int64_t>(warp) * (32 * KC) + static_cast<int64_t>(lane) * KC;
-  float y[KC];
+  constexpr int NC = KC / 2;  // columns per lane
+  const int64_t c0 = static_cast<int64_t>(warp) * (32 * NC) + static_cast<int64_t>(lane) * NC;
+  float y[NC];
 #pragma unroll
-  for (int c = 0; c < KC; ++c) y[c] = 0.0f;
+  for (int c = 0; c < NC; ++c) y[c] = 0.0f;
   for (int e0 = 0; e0 < nlive; e0 += 8) {
-    uint32_t raw[8][KC / 2];
+    uint32_t raw[8][(NC + 1) / 2];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
 #pragma unroll
-      for (int k = 0; k < KC / 2; ++k) raw[r][k] = 0u;
+      for (int k = 0; k < (NC + 1) / 2; ++k) raw[r][k] = 0u;
       if (e0 + r < nlive) {
         const uint16_t *row = p.w_down + (i0 + s_idx[e0 + r]) * p.d + c0;
-        if constexpr (KC == 8) {
-          const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(row));
-          raw[r][0] = v.x;
-          raw[r][1] = v.y;
-          raw[r][2] = v.z;
-          raw[r][3] = v.w;
-        } else if constexpr (KC == 4) {
+        if constexpr (NC == 4) {
           const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(row));
           raw[r][0] = v.x;
           raw[r][1] = v.y;
-        } else {
+        } else if constexpr (NC == 2) {
           raw[r][0] = __ldcs(reinterpret_cast<const unsigned int *>(row));
+        } else {
+          raw[r][0] = __ldcs(reinterpret_cast<const unsigned short *>(row));
         }
       }
     }
@@ -149,7 +146,7 @@ __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpPara
     for (int r = 0; r < 8; ++r) {
       const float hv = e0 + r < nlive ? s_hl[e0 + r] : 0.0f;
 #pragma unroll
-      for (int c = 0; c < KC; ++c) {
+      for (int c = 0; c < NC; ++c) {
         const uint32_t wv = raw[r][c >> 1];
         const float v = (c & 1) ? bf16hi(wv) : bf16lo(wv);
         y[c] = fmaf(hv, v, y[c]);
@@ -158,7 +155,7 @@ __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpPara
   }
   float *dst = p.part + static_cast<int64_t>(blockIdx.x) * p.d + c0;
 #pragma unroll
-  for (int c = 0; c < KC; ++c) dst[c] = y[c];
+  for (int c = 0; c < NC; ++c) dst[c] = y[c];
   if (threadIdx.x == 0) p.live[blockIdx.x] = nlive;
 }
 
