@@ -12,19 +12,19 @@
 // most keys first.  Warp roles:
 //   warp 0     TMA producer: the 128 query rows once; per 128-key tile the K rows (two
 //              64-column boxes, 128-byte swizzle), the tile's 128 key norms and the V rows,
-//              each in a ring of 2.  Rows past n (and query rows past T) read as zeros.
+//              each in a ring of 3.  Rows past n (and query rows past T) read as zeros.
 //   warp 1     tcgen05 issuer: S = Q K^T (M 128 queries x N 128 keys, K 16 per step, fp32
-//              in tensor memory, two S buffers), then O += P V, with P from shared memory
-//              and V read as an MN-major operand (the cached rows as they lie), in fp32 in
-//              tensor memory.  S of the next tile is issued before P V of this one, so the
-//              tensor cores work while the epilogue turns scores into weights.
+//              in one of three tensor-memory buffers), then O += P V with P read from tensor
+//              memory (the same buffer, where the epilogue wrote it over S) and V as an
+//              MN-major operand (the cached rows as they lie), fp32 in tensor memory.  S of
+//              tile t reuses the buffer of tile t - 3, whose P V is long done.
 //   warps 2-9  epilogue, one thread per (query row, half of the tile's keys).  With
 //              s = alpha rq rk dot, w = max(s, 0)^2 = a2 * w' where a2 = alpha^2 rq^2 is the
 //              row's factor and w' = max(dot, 0)^2 * rk^2 (rq, rk > 0), so the row factor
 //              is applied once at the end: out = a2 O' / (c + a2 den'), O' = sum w' v,
-//              den' = sum w' over keys j <= p.  P = w' is written as two bf16 matrices
-//              hi = rn(w'), lo = rn(w' - hi), both multiplied into O', so the weights keep
-//              about 16 bits.
+//              den' = sum w' over keys j <= p.  P = w' is written over the thread's own S
+//              columns as two bf16 matrices hi = rn(w'), lo = rn(w' - hi), both multiplied
+//              into O', so the weights keep about 16 bits.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,23 +37,24 @@ namespace {
 constexpr int kEpiWarps = EMBLA_PREFILL_EPI_WARPS;  // a multiple of 4 (the lane quarters)
 constexpr int kEpiParts = kEpiWarps / 4;          // threads per query row
 constexpr int kEpiCols = 128 / kEpiParts;         // keys of a tile per epilogue thread
-static_assert(kEpiWarps % 4 == 0 && kEpiCols % 32 == 0, "epilogue split");
+static_assert(kEpiWarps % 4 == 0 && kEpiCols % 64 == 0, "epilogue split (hi and lo of 32 keys each)");
 constexpr int kPThreads = (2 + kEpiWarps) * 32;
+constexpr int kRing = 3;                 // K, V, key-norm stages and S/P buffers
 constexpr int kBox = 128 * 128;          // one [128 rows][64 bf16] box, 16 KB
 constexpr int kTileB = 2 * kBox;         // a 128 x 128 bf16 tile
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileB;    // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileB;
-constexpr int kOffP = kOffV + 2 * kTileB;  // hi, then lo
-constexpr int kOffRK = kOffP + 2 * kTileB;  // 2 x 128 floats; the final row sums reuse it
-constexpr int kOffBar = kOffRK + 2 * 128 * 4;
-constexpr int kNBars = 20;
+constexpr int kOffK = kOffQ + kTileB;
+constexpr int kOffV = kOffK + kRing * kTileB;
+constexpr int kOffRK = kOffV + kRing * kTileB;
+constexpr int kOffBar = kOffRK + kRing * 128 * 4;
+constexpr int kNBars = 1 + 9 * kRing + 1;
 constexpr int kOffMisc = kOffBar + kNBars * 8;
 constexpr int kPSmem = kOffMisc + 16 + 1024;  // + room to align the base to 1024
 static_assert(kPSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
-constexpr int kColS = 0, kColO = 256, kPTmemCols = 512;
+constexpr int kColO = kRing * 128, kPTmemCols = 512;
+static_assert(kColO + 128 <= kPTmemCols, "tensor memory");
 
 struct PrefillParams {
   float *out;      // [B, Hq, T, D]
@@ -77,20 +78,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint8_t *sQ = smem + kOffQ;
   uint8_t *sK = smem + kOffK;
   uint8_t *sV = smem + kOffV;
-  uint8_t *sP = smem + kOffP;
   float *sRK = reinterpret_cast<float *>(smem + kOffRK);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *qfull = bars;
-  uint64_t *kfull = bars + 1, *kempty = bars + 3;
-  uint64_t *rkfull = bars + 5, *rkempty = bars + 7;
-  uint64_t *vfull = bars + 9, *vempty = bars + 11;
-  uint64_t *sfull = bars + 13, *sempty = bars + 15;
-  uint64_t *pfull = bars + 17, *pempty = bars + 18;
-  uint64_t *ofull = bars + 19;
+  uint64_t *kfull = bars + 1, *kempty = kfull + kRing;
+  uint64_t *rkfull = kempty + kRing, *rkempty = rkfull + kRing;
+  uint64_t *vfull = rkempty + kRing, *vempty = vfull + kRing;
+  uint64_t *sfull = vempty + kRing;   // S of a tile in tensor memory
+  uint64_t *pfull = sfull + kRing;    // its P written over it
+  uint64_t *pvdone = pfull + kRing;   // its P V done: the buffer is free
+  uint64_t *ofull = pvdone + kRing;
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
   uint32_t *s_tmem = misc;
   volatile int *s_abort = reinterpret_cast<volatile int *>(misc + 1);
-  volatile int *s_issued = reinterpret_cast<volatile int *>(misc + 2);  // key tiles loaded
+  volatile int *s_issued = reinterpret_cast<volatile int *>(misc + 2);  // loads issued
 
   // tiles with the most keys first: the last query tile of every (sequence, head), ...
   const int idx = static_cast<int>(blockIdx.x);
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
       mbar_init(&rkfull[s], 1);
@@ -113,10 +114,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], kEpiWarps);
+      mbar_init(&pfull[s], kEpiWarps);
+      mbar_init(&pvdone[s], 1);
     }
-    mbar_init(pfull, kEpiWarps);
-    mbar_init(pempty, 1);
     mbar_init(ofull, 1);
     *s_abort = 0;
     *s_issued = 0;
@@ -144,23 +144,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tma_load_3d(sQ, &tm_q, qfull, 0, qt * 128, bh);
       tma_load_3d(sQ + kBox, &tm_q, qfull, 64, qt * 128, bh);
       for (int kt = 0; kt < nkt; ++kt) {
-        const int s = kt & 1;
-        const uint32_t ph = ((kt >> 1) - 1) & 1;
-        if (kt >= 2 && !mbar_wait(&kempty[s], ph)) {
+        const int s = kt % kRing;
+        const uint32_t ph = ((kt / kRing) - 1) & 1;
+        if (kt >= kRing && !mbar_wait(&kempty[s], ph)) {
           set_abort_p(s_abort, p.flags);
           break;
         }
         mbar_arrive_expect_tx(&kfull[s], kTileB);
         tma_load_3d(sK + s * kTileB, &tm_k, &kfull[s], 0, kt * 128, u);
         tma_load_3d(sK + s * kTileB + kBox, &tm_k, &kfull[s], 64, kt * 128, u);
-        if (kt >= 2 && !mbar_wait(&rkempty[s], ph)) {
+        if (kt >= kRing && !mbar_wait(&rkempty[s], ph)) {
           set_abort_p(s_abort, p.flags);
           *s_issued = 3 * kt + 1;
           break;
         }
         mbar_arrive_expect_tx(&rkfull[s], 128 * 4);
         tma_load_2d(sRK + s * 128, &tm_rk, &rkfull[s], kt * 128, u);
-        if (kt >= 2 && !mbar_wait(&vempty[s], ph)) {
+        if (kt >= kRing && !mbar_wait(&vempty[s], ph)) {
           set_abort_p(s_abort, p.flags);
           *s_issued = 3 * kt + 2;
           break;
@@ -177,20 +177,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ));
       const uint64_t kdesc = smem_desc_sw128(smem_u32(sK));
-      const uint64_t pdesc = smem_desc_sw128(smem_u32(sP));
       bool ok = mbar_wait(qfull, 0);
       for (int kt = 0; ok && kt <= nkt; ++kt) {
         if (kt < nkt) {
-          const int sb = kt & 1;
-          ok = mbar_wait(&kfull[sb], (kt >> 1) & 1) &&
-               (kt < 2 || mbar_wait(&sempty[sb], ((kt >> 1) - 1) & 1));
+          const int sb = kt % kRing;
+          ok = mbar_wait(&kfull[sb], (kt / kRing) & 1) &&
+               (kt < kRing || mbar_wait(&pvdone[sb], ((kt / kRing) - 1) & 1));
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             // dims 16kk..16kk+15: 32 bytes into a 128-byte row; dims 64.. start the second box
             const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
-            tc_mma_bf16(tmem + kColS + sb * 128, qdesc + off,
+            tc_mma_bf16(tmem + sb * 128, qdesc + off,
                         kdesc + static_cast<uint64_t>((sb * kTileB) >> 4) + off, kIdescS,
                         kk > 0 ? 1u : 0u);
           }
@@ -198,21 +197,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tc_commit(&kempty[sb]);
         }
         if (kt >= 1) {
-          const int t = kt - 1, vb = t & 1;
-          ok = mbar_wait(pfull, t & 1) && mbar_wait(&vfull[vb], (t >> 1) & 1);
+          const int t = kt - 1, pb = t % kRing;
+          ok = mbar_wait(&pfull[pb], (t / kRing) & 1) && mbar_wait(&vfull[pb], (t / kRing) & 1);
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            // keys 16kk..16kk+15: P columns (K-major, as S), V rows 16kk.. (2 KB apart)
-            const uint64_t aoff = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
-            const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + vb * kTileB + kk * 2048), kBox);
-            tc_mma_bf16(tmem + kColO, pdesc + aoff, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
-            tc_mma_bf16(tmem + kColO, pdesc + static_cast<uint64_t>(kTileB >> 4) + aoff, vd,
-                        kIdescPV, 1u);
+            // keys 16kk..16kk+15: P columns 8 (kk % 4) of the half kk / 4 (hi, then lo 32
+            // columns further); V rows 16kk.. (2 KB apart)
+            const uint32_t a_hi = tmem + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+            const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + pb * kTileB + kk * 2048), kBox);
+            tc_mma_bf16_tmem_a(tmem + kColO, a_hi, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16_tmem_a(tmem + kColO, a_hi + 32, vd, kIdescPV, 1u);
           }
-          tc_commit(pempty);
-          tc_commit(&vempty[vb]);
+          tc_commit(&pvdone[pb]);
+          tc_commit(&vempty[pb]);
         }
       }
       if (!ok) set_abort_p(s_abort, p.flags);
@@ -253,23 +252,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     float den4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains of the row's weight sum
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    // this thread's keys are 16-byte chunks chunk0 .. of box (cg kEpiCols) / 64 of a P row
-    uint8_t *prow = sP + ((cg * kEpiCols) >> 6) * kBox + r * 128;
-    const int chunk0 = ((cg * kEpiCols) & 63) >> 3;
     for (int kt = 0; ok && kt < nkt; ++kt) {
-      const int sb = kt & 1;
-      ok = mbar_wait(&sfull[sb], (kt >> 1) & 1) && mbar_wait(&rkfull[sb], (kt >> 1) & 1);
+      const int sb = kt % kRing;
+      ok = mbar_wait(&sfull[sb], (kt / kRing) & 1) && mbar_wait(&rkfull[sb], (kt / kRing) & 1);
       if (!ok) break;
       tc_fence_after_sync();
+      const uint32_t cols = tmem + lane_base + sb * 128 + cg * kEpiCols;
       uint32_t acc[kEpiCols];
 #pragma unroll
       for (int c = 0; c < kEpiCols; c += 32)
-        tmem_load_x32(tmem + lane_base + kColS + sb * 128 + cg * kEpiCols + c,
-                      *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
+        tmem_load_x32(cols + c, *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
       tmem_wait_ld(acc);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sempty[sb]);
       // squared key norms of these keys (the same for every lane: broadcast reads)
       float rk[kEpiCols];
 #pragma unroll
@@ -287,38 +280,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // position need the test)
       const int64_t j0 = static_cast<int64_t>(kt) * 128 + cg * kEpiCols;
       const bool masked = j0 + kEpiCols - 1 > p0;
-      uint32_t hi[kEpiCols / 2], lo[kEpiCols / 2];
 #pragma unroll
-      for (int k = 0; k < kEpiCols; k += 2) {
-        float w2[2];
+      for (int g = 0; g < kEpiCols; g += 64) {
+        uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float d = fmaxf(__uint_as_float(acc[k + e]), 0.0f);
-          float w = d * d * rk[k + e];
-          if (masked && j0 + k + e > pos) w = 0.0f;
-          den4[(k + e) & 3] += w;
-          w2[e] = w;
+        for (int k = 0; k < 64; k += 2) {
+          float w2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float d = fmaxf(__uint_as_float(acc[g + k + e]), 0.0f);
+            float w = d * d * rk[g + k + e];
+            if (masked && j0 + g + k + e > pos) w = 0.0f;
+            den4[(k + e) & 3] += w;
+            w2[e] = w;
+          }
+          const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
+          hi[k >> 1] = hb;
+          lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
         }
-        const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
-        hi[k >> 1] = hb;
-        lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
+        // over this thread's own S columns (already read): 64 keys = 32 columns of hi, then
+        // 32 of lo
+        tmem_store_x32(cols + g, hi);
+        tmem_store_x32(cols + g + 32, lo);
       }
-      // the previous tile's P V has read P
-      if (kt >= 1 && !mbar_wait(pempty, (kt - 1) & 1)) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int c = 0; c < kEpiCols / 8; ++c) {
-        const int pc = ((chunk0 + c) ^ (r & 7)) * 16;
-        *reinterpret_cast<uint4 *>(prow + pc) =
-            make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-        *reinterpret_cast<uint4 *>(prow + kTileB + pc) =
-            make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-      }
-      fence_proxy_async_smem();  // P is read by the tensor cores
+      tmem_wait_st();
+      tc_fence_before_sync();  // P is read by the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(pfull);
+      if (lane == 0) mbar_arrive(&pfull[sb]);
     }
     if (ok) ok = mbar_wait(ofull, 0) && !*s_abort;
     if (!ok) set_abort_p(s_abort, p.flags);
@@ -359,16 +347,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // no copy may still be landing in shared memory when the CTA leaves
     mbar_wait(qfull, 0);
     const int issued = *s_issued;  // 3 per key tile: K, key norms, V
-    for (int s = 0; s < 2; ++s) {
-      const int tk = issued / 3;   // tiles whose three loads were all issued
-      int uses = tk > s ? (tk - 1 - s) / 2 + 1 : 0;
-      if (uses) mbar_wait(&vfull[s], (uses - 1) & 1);
-      const int tr = (issued + 1) / 3;  // tiles whose key-norm load was issued
-      uses = tr > s ? (tr - 1 - s) / 2 + 1 : 0;
-      if (uses) mbar_wait(&rkfull[s], (uses - 1) & 1);
-      const int tq = (issued + 2) / 3;  // tiles whose K load was issued
-      uses = tq > s ? (tq - 1 - s) / 2 + 1 : 0;
+    const int nk = (issued + 2) / 3, nr = (issued + 1) / 3, nv = issued / 3;  // tiles of each
+    for (int s = 0; s < kRing; ++s) {
+      int uses = nk > s ? (nk - 1 - s) / kRing + 1 : 0;
       if (uses) mbar_wait(&kfull[s], (uses - 1) & 1);
+      uses = nr > s ? (nr - 1 - s) / kRing + 1 : 0;
+      if (uses) mbar_wait(&rkfull[s], (uses - 1) & 1);
+      uses = nv > s ? (nv - 1 - s) / kRing + 1 : 0;
+      if (uses) mbar_wait(&vfull[s], (uses - 1) & 1);
     }
   }
   if (warp == 1) {
