@@ -37,7 +37,7 @@ namespace {
 constexpr int kEpiWarps = EMBLA_PREFILL_EPI_WARPS;  // a multiple of 4 (the lane quarters)
 constexpr int kEpiParts = kEpiWarps / 4;          // threads per query row
 constexpr int kEpiCols = 128 / kEpiParts;         // keys of a tile per epilogue thread
-static_assert(kEpiWarps % 4 == 0 && kEpiCols % 64 == 0, "epilogue split (hi and lo of 32 keys each)");
+static_assert(kEpiWarps % 4 == 0 && (kEpiCols == 32 || kEpiCols == 64), "epilogue split");
 constexpr int kPThreads = (2 + kEpiWarps) * 32;
 constexpr int kRing = 3;                 // K, V, key-norm stages and S/P buffers
 constexpr int kBox = 128 * 128;          // one [128 rows][64 bf16] box, 16 KB
@@ -203,12 +203,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            // keys 16kk..16kk+15: P columns 8 (kk % 4) of the half kk / 4 (hi, then lo 32
-            // columns further); V rows 16kk.. (2 KB apart)
-            const uint32_t a_hi = tmem + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+            // keys 16kk..16kk+15: in the key group of kEpiCols keys holding them, hi takes
+            // the first kEpiCols / 2 columns and lo the next; V rows 16kk.. (2 KB apart)
+            const int grp = (16 * kk) / kEpiCols;
+            const uint32_t a_hi = tmem + pb * 128 + grp * kEpiCols + ((16 * kk) % kEpiCols) / 2;
             const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + pb * kTileB + kk * 2048), kBox);
             tc_mma_bf16_tmem_a(tmem + kColO, a_hi, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
-            tc_mma_bf16_tmem_a(tmem + kColO, a_hi + 32, vd, kIdescPV, 1u);
+            tc_mma_bf16_tmem_a(tmem + kColO, a_hi + kEpiCols / 2, vd, kIdescPV, 1u);
           }
           tc_commit(&pvdone[pb]);
           tc_commit(&vempty[pb]);
@@ -280,28 +281,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // position need the test)
       const int64_t j0 = static_cast<int64_t>(kt) * 128 + cg * kEpiCols;
       const bool masked = j0 + kEpiCols - 1 > p0;
+      uint32_t hi[kEpiCols / 2], lo[kEpiCols / 2];
 #pragma unroll
-      for (int g = 0; g < kEpiCols; g += 64) {
-        uint32_t hi[32], lo[32];
+      for (int k = 0; k < kEpiCols; k += 2) {
+        float w2[2];
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          float w2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float d = fmaxf(__uint_as_float(acc[g + k + e]), 0.0f);
-            float w = d * d * rk[g + k + e];
-            if (masked && j0 + g + k + e > pos) w = 0.0f;
-            den4[(k + e) & 3] += w;
-            w2[e] = w;
-          }
-          const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
-          hi[k >> 1] = hb;
-          lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
+        for (int e = 0; e < 2; ++e) {
+          const float d = fmaxf(__uint_as_float(acc[k + e]), 0.0f);
+          float w = d * d * rk[k + e];
+          if (masked && j0 + k + e > pos) w = 0.0f;
+          den4[(k + e) & 3] += w;
+          w2[e] = w;
         }
-        // over this thread's own S columns (already read): 64 keys = 32 columns of hi, then
-        // 32 of lo
-        tmem_store_x32(cols + g, hi);
-        tmem_store_x32(cols + g + 32, lo);
+        const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
+        hi[k >> 1] = hb;
+        lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
+      }
+      // over this thread's own S columns (already read): kEpiCols / 2 columns of hi, then
+      // as many of lo
+      if constexpr (kEpiCols == 64) {
+        tmem_store_x32(cols, *reinterpret_cast<const uint32_t(*)[32]>(hi));
+        tmem_store_x32(cols + 32, *reinterpret_cast<const uint32_t(*)[32]>(lo));
+      } else {
+        tmem_store_x16(cols, *reinterpret_cast<const uint32_t(*)[16]>(hi));
+        tmem_store_x16(cols + 16, *reinterpret_cast<const uint32_t(*)[16]>(lo));
       }
       tmem_wait_st();
       tc_fence_before_sync();  // P is read by the tensor cores
