@@ -677,13 +677,19 @@ __global__ void __launch_bounds__(kFThreads, 1) select_fast_kernel(const FastPar
       const bool maybe = valid && !recent && b == bstar;
       const uint32_t wsel = __ballot_sync(0xffffffffu, take);
       const uint32_t wcand = __ballot_sync(0xffffffffu, maybe);
-      if (lane == 0 && (jl >> 5) < kFWords) {
-        sh.sel[jl >> 5] = wsel;
-        sh.cand[jl >> 5] = wcand;
-        nsel += __popc(wsel);
+      // one atomic per warp for its candidates' places in the list
+      int cbase = 0;
+      if (lane == 0) {
+        if ((jl >> 5) < kFWords) {
+          sh.sel[jl >> 5] = wsel;
+          sh.cand[jl >> 5] = wcand;
+          nsel += __popc(wsel);
+        }
+        if (wcand) cbase = atomicAdd(&sh.nmine, __popc(wcand));
       }
+      cbase = __shfl_sync(0xffffffffu, cbase, 0);
       if (maybe) {
-        const int pos = atomicAdd(&sh.nmine, 1);
+        const int pos = cbase + __popc(wcand & ((1u << lane) - 1u));
         if (pos < kRankMax) sh.mine[pos] = select_key_ok(ok[r], j);
       }
     }
