@@ -137,3 +137,74 @@ def test_full_size_whole_attention_step_block():
         torch.cuda.synchronize()
         assert_close(out.cpu().numpy(), oracle.window_decode_batch(wl.q, wl.K, wl.V, wl.pos),
                      what="window output")
+
+
+@pytest.mark.parametrize("cfg", [7, 8])
+def test_full_size_prefill(cfg):
+    """The prefill workloads at full size (one sequence, a whole prompt of 8192 / 32768
+    tokens, 16 query heads): every output finite, and sampled rows of every head against the
+    oracle's single-token decode at that row's context (the prefill oracle's pinned
+    equivalent)."""
+    q, K, V = gen.config_prefill(cfg, seed=0)
+    B, Hq, T, D = q.shape
+    Hkv, n = K.shape[1], K.shape[2]
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    out = torch.full((B, Hq, T, D), float("nan"), device="cuda")
+    E.embla_prefill(shape, to_dev(q), to_dev(K), to_dev(V), out)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    out = out.cpu().numpy()
+    assert np.isfinite(out).all()
+    G = Hq // Hkv
+    rows = sorted({0, 1, 127, 128, 129, T // 3, T // 2 + 5, T - 129, T - 2, T - 1})
+    for t in rows:
+        p = n - T + t
+        for g in range(Hkv):
+            ref, _, _, _ = oracle.full_decode(q[0, g * G:(g + 1) * G, t], K[0, g, :p + 1],
+                                              V[0, g, :p + 1], alpha=1.0, c=1.0, eps=1e-6)
+            assert_close(out[0, g * G:(g + 1) * G, t], ref, what=f"prefill row {t} group {g}")
+
+
+def test_full_size_per_head_selection():
+    """The benchmarked workload with a selection per query head: per-head scores and
+    histograms of every unit, selections of sampled heads bit-exact on the scores ranked,
+    their sparse outputs against the oracle."""
+    fl = next(gen.config_full_layers(10, seed=0))
+    B, Hq, D = fl.q.shape
+    Hkv, n = fl.K.shape[1], fl.n
+    G = Hq // Hkv
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    q, K, V = to_dev(fl.q), to_dev(fl.K), to_dev(fl.V)
+    out = torch.empty(B, Hq, D, device="cuda")
+    ns = torch.empty(B, Hkv, dtype=torch.int32, device="cuda")
+    hs = torch.full((B, Hq, n), float("nan"), device="cuda")
+    hh = torch.empty(B, Hq, E.HIST_BINS, dtype=torch.int32, device="cuda")
+    E.embla_full_decode_head_scores(shape, q, K, V, out, ns, hs, hh)
+    idx = torch.full((B, Hq, TOPK + RECENT), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, Hq), -1, dtype=torch.int32, device="cuda")
+    E.embla_select_topk_per_head(shape, hs, hh, idx, cnt, TOPK, RECENT)
+    sparse = []
+    for qs in fl.sparse_q:
+        so = torch.full((B, Hq, D), float("nan"), device="cuda")
+        E.embla_sparse_decode_per_head(shape, to_dev(qs), K, V, idx, cnt, so)
+        sparse.append(so)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    assert np.array_equal(ns.cpu().numpy(), fl.n_pos)
+    hs, hh = hs.cpu().numpy(), hh.cpu().numpy().view(np.uint32)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    sparse = [so.cpu().numpy() for so in sparse]
+    assert (cnt == TOPK + RECENT).all()
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(hh[b, h], np.bincount(order_key_np(hs[b, h]) >> 21,
+                                                        minlength=E.HIST_BINS))
+    for b, h in [(0, 0), (B - 1, Hq - 1), (3, 5), (5, 10)]:
+        g = h // G
+        s = oracle.full_scores(fl.q[b, g * G:(g + 1) * G], fl.K[b, g, :n])[h - g * G]
+        assert_close(hs[b, h], s, atol=1e-4, rtol=1e-5, what=f"scores of head ({b},{h})")
+        ref_idx = oracle.select_topk(hs[b, h], TOPK, RECENT)
+        assert np.array_equal(idx[b, h], ref_idx), f"selection of head ({b},{h})"
+        for qs, so in zip(fl.sparse_q, sparse):
+            ref = oracle.sparse_decode(qs[b, h:h + 1], fl.K[b, g, :n], fl.V[b, g, :n], ref_idx)
+            assert_close(so[b, h:h + 1], ref, what=f"sparse output of head ({b},{h})")
