@@ -792,6 +792,42 @@ def main():
         wins.append(dict(wl=wl, shape=E.Shape(B, Hq, Hkv, D, 0, 0), q=to_dev(wl.q), K=to_dev(wl.K),
                          V=to_dev(wl.V), out=torch.empty(B, Hq, D, dtype=torch.float32, device=dev)))
 
+    # Every per-step input (the queries and the appended token's K/V rows) lives in one device
+    # buffer and every output in another, so a step moves its inputs with one host->device
+    # copy and its results with one device->host copy.
+    for L in layers:
+        n_last = L["fl"].n - 1
+        L["krow"] = L["K"][:, :, n_last].clone()
+        L["vrow"] = L["V"][:, :, n_last].clone()
+        if "Ks" in L:
+            L["ksrow"] = L["Ks"][:, :, n_last].clone()
+            L["vsrow"] = L["Vs"][:, :, n_last].clone()
+
+    def rehome(refs):
+        """Move each (container, key) tensor into one contiguous device buffer (256-byte
+        aligned slots) and put the view back; returns the buffer."""
+        sizes = [((c[k].numel() * c[k].element_size()) + 255) // 256 * 256 for c, k in refs]
+        arena = torch.empty(max(256, sum(sizes)), dtype=torch.uint8, device=dev)
+        off = 0
+        for (c, k), sz in zip(refs, sizes):
+            t = c[k]
+            v = arena[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            c[k] = v
+            off += sz
+        return arena
+
+    in_refs, out_refs = [], []
+    for L in layers:
+        in_refs += [(L, "q"), (L, "krow"), (L, "vrow")] + [(L["qs"], i) for i in range(len(L["qs"]))]
+        if "Ks" in L:
+            in_refs += [(L, "ksrow"), (L, "vsrow")]
+        out_refs += [(L, "out"), (L, "n_surv")] + [(L["souts"], i) for i in range(len(L["souts"]))]
+    for w in wins:
+        in_refs.append((w, "q"))
+        out_refs.append((w, "out"))
+    arena_in, arena_out = rehome(in_refs), rehome(out_refs)
+
     def full_call(L):
         if L["per_head"]:
             E.embla_full_decode_head_scores(L["shape"], L["q"], L["K"], L["V"], L["out"], L["n_surv"],
@@ -985,48 +1021,24 @@ def main():
     # end to end through the public Python API, host buffers, copies inside the timed region
     e2e = None
     if args.e2e_steps > 0:
-        L0 = layers[0]
-        pin = lambda t: t.cpu().pin_memory()
-        h_q = [pin(L["q"]) for L in layers]
-        h_qs = [[pin(x) for x in L["qs"]] for L in layers]
-        n = L0["fl"].n
-        h_krow = [pin(L["K"][:, :, n - 1, :].contiguous()) for L in layers]
-        h_vrow = [pin(L["V"][:, :, n - 1, :].contiguous()) for L in layers]
-        # 8-bit caches: the appended row's two scales as well
-        h_scales = [(pin(L["Ks"][:, :, n - 1].contiguous()), pin(L["Vs"][:, :, n - 1].contiguous()))
-                    if "Ks" in L else () for L in layers]
-        h_wq = [pin(w["q"]) for w in wins]
-        h_out = [torch.empty_like(L["out"], device="cpu").pin_memory() for L in layers]
-        h_sout = [[torch.empty_like(x, device="cpu").pin_memory() for x in L["souts"]] for L in layers]
-        h_ns = [torch.empty_like(L["n_surv"], device="cpu").pin_memory() for L in layers]
-        h_wout = [torch.empty_like(w["out"], device="cpu").pin_memory() for w in wins]
-        h2d = sum(x.numel() * x.element_size() for x in h_q + h_krow + h_vrow + h_wq) + \
-            sum(x.numel() * x.element_size() for xs in h_qs + h_scales for x in xs)
-        d2h = sum(x.numel() * x.element_size() for x in h_out + h_ns + h_wout) + \
-            sum(x.numel() * x.element_size() for xs in h_sout for x in xs)
+        n = layers[0]["fl"].n
+        h_in = torch.empty(arena_in.numel(), dtype=torch.uint8).pin_memory()
+        h_in.copy_(arena_in)
+        h_res = torch.empty(arena_out.numel(), dtype=torch.uint8).pin_memory()
+        h2d, d2h = arena_in.numel(), arena_out.numel()
 
         def e2e_body(k):
-            for li, L in enumerate(reps[k % n_rep]):
-                L["q"].copy_(h_q[li], non_blocking=True)
-                for x, hx in zip(L["qs"], h_qs[li]):
-                    x.copy_(hx, non_blocking=True)
-                L["K"][:, :, n - 1, :].copy_(h_krow[li], non_blocking=True)
-                L["V"][:, :, n - 1, :].copy_(h_vrow[li], non_blocking=True)
-                if h_scales[li]:
-                    L["Ks"][:, :, n - 1].copy_(h_scales[li][0], non_blocking=True)
-                    L["Vs"][:, :, n - 1].copy_(h_scales[li][1], non_blocking=True)
+            arena_in.copy_(h_in, non_blocking=True)  # every query and appended row: one copy
+            for L in reps[k % n_rep]:
+                L["K"][:, :, n - 1].copy_(L["krow"])
+                L["V"][:, :, n - 1].copy_(L["vrow"])
+                if "Ks" in L:
+                    L["Ks"][:, :, n - 1].copy_(L["ksrow"])
+                    L["Vs"][:, :, n - 1].copy_(L["vsrow"])
                 full_call(L)
                 rest_calls(L)
-            for wi, w in enumerate(wins):
-                w["q"].copy_(h_wq[wi], non_blocking=True)
             window_calls()
-            for li, L in enumerate(layers):
-                h_out[li].copy_(L["out"], non_blocking=True)
-                h_ns[li].copy_(L["n_surv"], non_blocking=True)
-                for hx, x in zip(h_sout[li], L["souts"]):
-                    hx.copy_(x, non_blocking=True)
-            for wi, w in enumerate(wins):
-                h_wout[wi].copy_(w["out"], non_blocking=True)
+            h_res.copy_(arena_out, non_blocking=True)  # every output: one copy
 
         def e2e_eager(k):
             e2e_body(k)
@@ -1069,8 +1081,9 @@ def main():
                "eager_value": rates["eager"],
                "eager_launch": "the public API called from Python per step, copies issued "
                                "eagerly, then a host synchronise",
-               "inputs": "per-step queries and the appended token's K/V rows from pinned host "
-                         "memory; the KV caches stay resident in HBM"}
+               "inputs": "per step, one copy of every query and the appended token's K/V rows "
+                         "from pinned host memory (then placed into the caches on the device) and "
+                         "one copy of every output back; the KV caches stay resident in HBM"}
 
     peak, peak_src = _peaks()
     wl_key = workload_name(cfg, args.batch, args.ctx).replace(" ", "_")
