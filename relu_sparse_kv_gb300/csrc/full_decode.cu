@@ -100,14 +100,21 @@ struct Cfg {
   static constexpr int mma_n = KV8 ? (3 * G <= 16 ? 16 : 32) : 16;
   static constexpr int kstep_dims = KV8 ? 32 : 16;
   static constexpr int ksteps = kHeadDim / kstep_dims;
-  // Each k-step writes its own accumulator, so a tile's MMAs do not wait on each other
-  // (and no long sum is kept inside the tensor core); the epilogue adds the partials.
-  static constexpr int acc_cols = ksteps * mma_n;                    // 128 / 64 / 128
-  static constexpr int tmem_cols = kAccBufs * acc_cols;              // 512 / 256 / 512
+  // bf16: each k-step writes its own accumulator, so a tile's MMAs do not wait on each
+  // other; the epilogue adds the partials.  8-bit: the k-steps add into one accumulator,
+  // followed by 128 columns of codes . codes^T, whose diagonal is each key's sum of squared
+  // codes (the key norms come from the tensor cores instead of the CUDA cores).
+  static constexpr int score_cols = KV8 ? mma_n : ksteps * mma_n;
+  static constexpr int diag_cols = KV8 ? kTileKeys : 0;
+  static constexpr int acc_cols = score_cols + diag_cols;            // 128 / 144 / 160
+  static constexpr int acc_bufs = KV8 ? 3 : kAccBufs;                // tiles in flight
+  static constexpr int tmem_cols = 512;
   static constexpr uint32_t idesc = KV8 ? idesc_e4m3_f32(128, mma_n) : idesc_bf16_f32(128, 16);
+  static constexpr uint32_t idesc_diag = idesc_e4m3_f32(128, kTileKeys);
   static_assert(stage_bytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(tile_bytes == (KV8 ? 1 : 2) * half_bytes, "a tile is one or two boxes");
-  static_assert(tmem_cols == 256 || tmem_cols == 512, "tensor-memory allocation size");
+  static_assert(acc_bufs <= kAccBufs && acc_bufs * acc_cols <= tmem_cols, "tensor memory");
+  static_assert(!KV8 || idesc_diag != 0u, "the codes . codes^T instruction");
 };
 
 // One tile's survivors in ascending key order: entry e has its V row in row
@@ -455,14 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qe[qb]);
           if (++tl == TU) tl = 0;
           if (++s == kStages) s = 0;
-          if (++b == kAccBufs) {
+          if (++b == C::acc_bufs) {
             b = 0;
             bphase ^= 1;
           }
           continue;
         }
         if (!mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) ||
-            (i >= kAccBufs && !mbar_wait(&acce[b], bphase ^ 1))) {
+            (i >= C::acc_bufs && !mbar_wait(&acce[b], bphase ^ 1))) {
           set_abort(s_abort, p.flags);
           break;
         }
@@ -472,10 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < C::ksteps; ++kk) {
           if constexpr (KV8) {
-            // partial scores over dims 32kk..32kk+31: D_kk[key][t*G + h] = code . t_th;
-            // k-step kk is 32 bytes into the 128-byte rows of codes and of terms
-            tc_mma_e4m3(dcol + kk * C::mma_n, adesc + ((kk * 32) >> 4), qdesc + ((kk * 32) >> 4),
-                        C::idesc, 0u);
+            // scores over dims 32kk..32kk+31 added into D[key][t*G + h] = code . t_th, and
+            // codes . codes^T into the next 128 columns; k-step kk is 32 bytes into the
+            // 128-byte rows of codes and of terms
+            const uint64_t a = adesc + ((kk * 32) >> 4);
+            tc_mma_e4m3(dcol, a, qdesc + ((kk * 32) >> 4), C::idesc, kk > 0 ? 1u : 0u);
+            tc_mma_e4m3(dcol + C::score_cols, a, a, C::idesc_diag, kk > 0 ? 1u : 0u);
           } else {
             // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is
             // 32 bytes into a 128-byte row, the second half of the dims starts a new box
@@ -490,14 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qe[qb]);
         if (++tl == TU) tl = 0;
         if (++s == kStages) s = 0;
-        if (++b == kAccBufs) {
+        if (++b == C::acc_bufs) {
           b = 0;
           bphase ^= 1;
         }
       }
       // this issuer's accumulators must be idle before the tensor memory is released
       if (issued > 0)
-        mbar_wait(&accf[(issued - 1) % kAccBufs], ((issued - 1) / kAccBufs) & 1);
+        mbar_wait(&accf[(issued - 1) % C::acc_bufs], ((issued - 1) / C::acc_bufs) & 1);
     }
     __syncwarp();
   } else if (warp < kWarpAcc) {
@@ -552,10 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&qempty[qb]);
       }
       if (static_cast<int>(i % kGroups) != group) continue;
-      const int b = static_cast<int>(i % kAccBufs);
+      const int b = static_cast<int>(i % C::acc_bufs);
       const int slot = static_cast<int>(i % kWSlots);
       const int ns = static_cast<int>(i % kNormSlots);
-      const bool ok = !*s_abort && mbar_wait(&accf[b], (i / kAccBufs) & 1) &&
+      const bool ok = !*s_abort && mbar_wait(&accf[b], (i / C::acc_bufs) & 1) &&
                       mbar_wait(&rkfull[ns], (i / kNormSlots) & 1) &&
                       (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
       if (!named_bar_and(gbar, 128, ok)) {
@@ -564,38 +573,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float dot[G];
       tc_fence_after_sync();
+      float ssq = 0.0f;  // 8-bit caches: this key's sum of squared codes
       if constexpr (KV8) {
-        // k-steps two at a time: columns t*G + h of each k-step's accumulator
+        // columns t*G + h of the score accumulator; then this warp's 32 x 32 block of
+        // codes . codes^T, whose diagonal entry for this lane is its key's sum of squares
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
-#pragma unroll
-        for (int h = 0; h < G; ++h) dot[h] = 0.0f;
-#pragma unroll
-        for (int k2 = 0; k2 < C::ksteps; k2 += 2) {
-          uint32_t r[2 * 3 * G];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint32_t a = taddr + (k2 + k) * C::mma_n;
-            if constexpr (G == 4) {
-              tmem_load_x8(a, *reinterpret_cast<uint32_t(*)[8]>(&r[k * 12]));
-              tmem_load_x4(a + 8, *reinterpret_cast<uint32_t(*)[4]>(&r[k * 12 + 8]));
-            } else {
-              tmem_load_x16(a, *reinterpret_cast<uint32_t(*)[16]>(&r[k * 24]));
-              tmem_load_x8(a + 16, *reinterpret_cast<uint32_t(*)[8]>(&r[k * 24 + 16]));
-            }
-          }
-          tmem_wait_ld(r);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const uint32_t *rk3 = &r[k * 3 * G];
-              // t1 + t2 / 16 + t3 / 256 (the scalings are exact)
-              dot[h] += (__uint_as_float(rk3[2 * G + h]) * 0.0625f + __uint_as_float(rk3[G + h])) *
-                            0.0625f +
-                        __uint_as_float(rk3[h]);
-            }
-          }
+        uint32_t r[3 * G];
+        uint32_t dg[32];
+        if constexpr (G == 4) {
+          tmem_load_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_load_x4(taddr + 8, *reinterpret_cast<uint32_t(*)[4]>(&r[8]));
+        } else {
+          tmem_load_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          tmem_load_x8(taddr + 16, *reinterpret_cast<uint32_t(*)[8]>(&r[16]));
         }
+        tmem_load_x32(taddr + C::score_cols + quarter * 32, dg);
+        tmem_wait_ld(r);
+        tmem_wait_ld(dg);
+#pragma unroll
+        for (int h = 0; h < G; ++h)  // t1 + t2 / 16 + t3 / 256 (the scalings are exact)
+          dot[h] = (__uint_as_float(r[2 * G + h]) * 0.0625f + __uint_as_float(r[G + h])) * 0.0625f +
+                   __uint_as_float(r[h]);
+        // dg[lane] by halving: keep the upper half of the candidates where this lane's bit is set
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) {
+#pragma unroll
+          for (int e = 0; e < k; ++e) dg[e] = (lane & k) ? dg[e + k] : dg[e];
+        }
+        ssq = __uint_as_float(dg[0]);
       } else {
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
         uint32_t r[C::ksteps * G];
@@ -617,10 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before_sync();
-      const float rk = s_rk[ns * kTileKeys + row];
+      // bf16: the key norm; 8-bit: the key's scale ks, whose norm follows from the sum of
+      // squared codes: ks / sqrt(ks^2 mean(code^2) + eps)
+      const float rkv = s_rk[ns * kTileKeys + row];
       const float vsc = KV8 ? s_vs[ns * kTileKeys + row] : 0.0f;
       // every lane's reads are back
-      const float rk_used = __shfl_sync(0xffffffffu, KV8 ? rk + vsc : rk, 31);
+      const float rk_used = __shfl_sync(0xffffffffu, KV8 ? rkv + vsc : rkv, 31);
+      const float rk = KV8 ? rkv * rsqrtf(rkv * rkv * (ssq * (1.0f / kHeadDim)) + p.eps) : rkv;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&acce[b]);
@@ -749,9 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kWarpNorm) {
     // ------------------------------------------------------------------ key norms
-    // One thread per key of each landed tile: 1 / sqrt(mean(k^2) + eps) (8-bit caches:
-    // ks / sqrt(ks^2 mean(code^2) + eps), with the key's V scale passed along).  The stage
-    // is released as soon as these four warps and the tile's MMAs are done with it.
+    // One thread per key of each landed tile: 1 / sqrt(mean(k^2) + eps) (8-bit caches: the
+    // key's two scales, passed along; the epilogue finishes the norm from the tensor cores'
+    // sum of squared codes).  The stage is released as soon as these four warps and the
+    // tile's MMAs are done with it.
     const int row = (warp - kWarpNorm) * 32 + lane;
     int u = u0, tl = tl0, seg = -1;
     for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
@@ -793,21 +802,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t *rowp = st + row * 128;
       float rk, vsc = 0.0f, done;
       if constexpr (KV8) {
-        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4 *>(rowp + (c ^ (row & 7)) * 16);
-          sq_acc_e4m3x4(x.x, a[0], a[1]);
-          sq_acc_e4m3x4(x.y, a[2], a[3]);
-          sq_acc_e4m3x4(x.z, a[0], a[1]);
-          sq_acc_e4m3x4(x.w, a[2], a[3]);
-        }
+        // the key's two scales go on with the tile; its sum of squared codes comes from the
+        // tensor cores (codes . codes^T)
         const float ks = reinterpret_cast<const float *>(st + C::tile_bytes)[row];
         vsc = reinterpret_cast<const float *>(st + C::tile_bytes + C::scale_bytes)[row];
-        const float ss = (a[0] + a[1]) + (a[2] + a[3]);
-        const float dep = ss + ks + vsc;  // every lane's value depends on all of its reads
+        const float dep = ks + vsc;  // every lane's value depends on its reads
         done = __shfl_sync(0xffffffffu, dep, 0) + __shfl_sync(0xffffffffu, dep, 31);
-        rk = ks * rsqrtf(ks * ks * (ss * (1.0f / kHeadDim)) + p.eps);
+        rk = ks;
+        (void)rowp;
       } else {
         float a[8];
 #pragma unroll
