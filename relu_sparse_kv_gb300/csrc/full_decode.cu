@@ -107,13 +107,18 @@ struct Cfg {
   static constexpr int score_cols = KV8 ? mma_n : ksteps * mma_n;
   static constexpr int diag_cols = KV8 ? kTileKeys : 0;
   static constexpr int acc_cols = score_cols + diag_cols;            // 128 / 144 / 160
-  static constexpr int acc_bufs = KV8 ? 3 : kAccBufs;                // tiles in flight
+  // Tiles in flight.  Tile i goes to buffer i % acc_bufs, to MMA issuer i % 2 and to
+  // epilogue group i % 2; with an even count every buffer has one issuer and one reader,
+  // which take its phases in order (with an odd count a fast group could wait for a
+  // buffer's next phase before its current one completed, and pass on the stale parity).
+  static constexpr int acc_bufs = KV8 ? kGroups : kAccBufs;
   static constexpr int tmem_cols = 512;
   static constexpr uint32_t idesc = KV8 ? idesc_e4m3_f32(128, mma_n) : idesc_bf16_f32(128, 16);
   static constexpr uint32_t idesc_diag = idesc_e4m3_f32(128, kTileKeys);
   static_assert(stage_bytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(tile_bytes == (KV8 ? 1 : 2) * half_bytes, "a tile is one or two boxes");
   static_assert(acc_bufs <= kAccBufs && acc_bufs * acc_cols <= tmem_cols, "tensor memory");
+  static_assert(acc_bufs % kGroups == 0 && acc_bufs % kMmaWarps == 0, "one issuer and one reader");
   static_assert(!KV8 || idesc_diag != 0u, "the codes . codes^T instruction");
 };
 

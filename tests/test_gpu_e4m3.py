@@ -155,6 +155,33 @@ def test_e4m3_is_repeatable():
     assert E.embla_device_check() == 0
 
 
+def test_e4m3_long_tile_streams_are_repeatable():
+    """About 108 tiles per CTA (32 sequences of 32768 keys over 2 KV heads): every
+    accumulator buffer, norm slot and survivor slot goes round many times, so a wait that
+    could pass on a stale phase would show up as a device flag or a changed output."""
+    fl = _layer(32, 16, 2, 32768, frac=0.05, seed=23, sparse=())
+    run = Run8(fl)
+    ns = run.n_surv.cpu().numpy()
+    assert np.array_equal(ns, fl.n_pos)
+    out0, sel0, hist0 = run.out.clone(), run.sel.clone(), run.hist.clone()
+    for _ in range(30):
+        E.embla_full_decode_e4m3(run.shape, run.q, run.K8, run.Ks, run.V8, run.Vs, run.out,
+                                 run.n_surv, run.sel, run.hist)
+        torch.cuda.synchronize()
+        assert E.embla_device_check() == 0
+        assert torch.equal(run.out, out0) and torch.equal(run.sel, sel0)
+        assert torch.equal(run.hist, hist0)
+    # sampled units against the oracle
+    for b, g in ((0, 0), (31, 1), (17, 0)):
+        Kd = oracle.dequant_e4m3(fl.K[b:b + 1, g:g + 1], fl.Ks[b:b + 1, g:g + 1])
+        Vd = oracle.dequant_e4m3(fl.V[b:b + 1, g:g + 1], fl.Vs[b:b + 1, g:g + 1])
+        ref_out, ref_sig, _ = oracle.full_decode_batch(fl.q[b:b + 1, 8 * g:8 * g + 8], Kd, Vd,
+                                                       fl.n)
+        assert_close(run.out[b, 8 * g:8 * g + 8].cpu().numpy(), ref_out[0])
+        assert_close(run.sel[b, g, :fl.n].cpu().numpy(), ref_sig[0, 0, :fl.n], atol=1e-4, rtol=1e-5,
+                     what="sigma")
+
+
 def test_e4m3_rejects_bad_arguments():
     fl = _layer(1, 16, 2, 256, seed=2)
     run = Run8(fl)
