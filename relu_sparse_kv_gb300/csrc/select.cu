@@ -863,6 +863,402 @@ __global__ void __launch_bounds__(kFThreads, 1) select_fast_kernel(const FastPar
   if (rank == 0 && tid == 0) p.count[u] = all;
   cluster_wait();  // the others are done reading this CTA's shared memory
 }
+
+// ----------------------------------------------------------------------------- one CTA per unit
+//
+// Contexts up to kUPasses x 32768 keys: one CTA of 1024 threads per unit and no cluster, so
+// the whole selection is a short chain of block barriers.
+//   1  a pass's 32768 scores land in shared memory by bulk copies (the 16-byte aligned
+//      middle; the few keys before and after it load directly) while the histogram, minus
+//      the recent keys, gives the boundary bin b*;
+//   2  thread t classifies keys 32t .. 32t + 31 of the pass (read in a rotated order, so a
+//      warp's reads hit 32 banks), comparing each score as a float against the edges of b*
+//      (exact for non-NaN scores): one bitmap word of keys above b* (and recent keys) and
+//      one of keys in b*, which are also listed with their 64-bit order keys;
+//   3  the listed candidates are narrowed by 8-bit digits of the 64-bit key below the bin
+//      (a digit histogram, one warp's scan, the keys above the boundary digit selected) until
+//      at most 32 are left, which one warp ranks pairwise.  A boundary bin of more than
+//      kUListMax keys is first narrowed the same way over the bitmap;
+//   4  one block scan over the words in key order places every selected index.
+
+constexpr int kUThreads = 1024;
+constexpr int kUWarps = kUThreads / 32;
+constexpr int kUPassKeys = 32 * kUThreads;    // keys per pass: 32 per thread
+#ifndef EMBLA_SEL_UNIT_PASSES
+#define EMBLA_SEL_UNIT_PASSES 2
+#endif
+constexpr int kUPasses = EMBLA_SEL_UNIT_PASSES;  // contexts up to kUPasses x 32768 keys
+constexpr int kUWords = kUPasses * kUThreads;    // bitmap words (32 keys each)
+constexpr int kUListMax = kUThreads;             // listed candidates: one per thread
+#ifndef EMBLA_SEL_BULK_PIECES
+#define EMBLA_SEL_BULK_PIECES 16
+#endif
+constexpr int kUBulkPieces = EMBLA_SEL_BULK_PIECES;
+
+// The float whose order key is k (k the key of a non-NaN float other than -0).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+struct __align__(16) UnitShared {
+  uint32_t h[kHistBins];       // recent keys per bin
+  uint32_t sel[kUWords];       // selected
+  uint32_t cand[kUWords];      // in the boundary bin, undecided
+  uint64_t list[2][kUListMax]; // listed candidates (current, next)
+  uint32_t dh[256];
+  int32_t warp_sum[2][kUWarps];
+  int32_t nnext[2];
+  int32_t bin, above, nlist, dstar, dabove, dcount;
+  uint64_t bar;
+};
+static_assert(sizeof(UnitShared) % 16 == 0, "the scores that follow start 16-byte aligned");
+
+// Exclusive scan of one int per thread over the 1024 threads (one barrier; `ws` must not be
+// reused until after the next barrier); sets *total.
+__device__ __forceinline__ int unit_scan(int v, int *total, int32_t *ws) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  const int w = ws[lane];
+  int incl = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int before = __shfl_sync(0xffffffffu, incl - w, warp);
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return before + x - v;
+}
+
+// Warp 0: the boundary digit of the 256-bin digit histogram dh (descending) for the need-th
+// key; writes dstar, dabove (keys in higher digits) and dcount (keys in it).
+__device__ __forceinline__ void unit_digit_boundary(UnitShared &sh, int need) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c[8], tot = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    c[k] = sh.dh[255 - 8 * lane - k];  // lane l: digits 255 - 8l .. 248 - 8l
+    tot += c[k];
+  }
+  uint32_t x = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  uint32_t before = x - tot;
+  const uint32_t nd = static_cast<uint32_t>(need);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (before < nd && before + c[k] >= nd) {
+      sh.dstar = 255 - 8 * lane - k;
+      sh.dabove = static_cast<int>(before);
+      sh.dcount = static_cast<int>(c[k]);
+    }
+    before += c[k];
+  }
+}
+
+// Start loading the scores of keys [0, nloc) from src into sf[k] (sf = buf + the source's
+// 16-byte phase): the aligned middle goes as kUBulkPieces bulk copies on `bar` (threads
+// 0 .. kUBulkPieces - 1 issue one each, so they are in flight together), every thread loads
+// its share of the few keys around it.  *bulk says whether a bulk copy was issued.
+__device__ __forceinline__ float *unit_pass_load(float *buf, const float *src, int nloc,
+                                                 uint64_t *bar, bool *bulk) {
+  const uint64_t gbeg = reinterpret_cast<uint64_t>(src);
+  const uint64_t gend = reinterpret_cast<uint64_t>(src + nloc);
+  const uint64_t abeg = (gbeg + 15u) & ~15ull, aend = gend & ~15ull;
+  *bulk = nloc > 0 && aend > abeg;
+  const int phase = static_cast<int>((gbeg >> 2) & 3u);
+  const int head = *bulk ? static_cast<int>((abeg - gbeg) / 4) : nloc;
+  const int mid_end = *bulk ? static_cast<int>((aend - gbeg) / 4) : nloc;
+  float *sf = buf + phase;
+  const int t = threadIdx.x;
+  if (*bulk) {
+    const uint32_t len = static_cast<uint32_t>(aend - abeg);
+    // the expected bytes may be posted after some pieces land: the phase also waits for
+    // thread 0's arrival, which comes with them
+    if (t == 0) mbar_arrive_expect_tx(bar, len);
+    const uint32_t piece = ((len + kUBulkPieces - 1) / kUBulkPieces + 15u) & ~15u;
+    const uint32_t off = static_cast<uint32_t>(t) * piece;
+    if (t < kUBulkPieces && off < len) {
+      fence_proxy_async_smem();  // earlier generic reads of the buffer come first
+      bulk_load(reinterpret_cast<uint8_t *>(sf + head) + off,
+                reinterpret_cast<const uint8_t *>(abeg) + off, min(piece, len - off), bar);
+    }
+  }
+  if (t < head) sf[t] = __ldcg(src + t);
+  if (mid_end + t < nloc) sf[mid_end + t] = __ldcg(src + mid_end + t);
+  return sf;
+}
+
+// Mask of the bits [a, b) of a 32-bit word (0 <= a, b <= 32 after clamping).
+__device__ __forceinline__ uint32_t bit_range(int a, int b) {
+  a = a < 0 ? 0 : (a > 32 ? 32 : a);
+  b = b < 0 ? 0 : (b > 32 ? 32 : b);
+  if (b <= a) return 0u;
+  const uint32_t hi = b >= 32 ? 0xFFFFFFFFu : ((1u << b) - 1u);
+  const uint32_t lo = (1u << a) - 1u;  // a < 32 here
+  return hi & ~lo;
+}
+
+__global__ void __launch_bounds__(kUThreads, 1) select_unit_kernel(const FastParams p) {
+  pdl_wait_primary();  // the scores and histogram are complete
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  UnitShared &sh = *reinterpret_cast<UnitShared *>(smem_raw);
+  float *buf = reinterpret_cast<float *>(smem_raw + sizeof(UnitShared));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t u = blockIdx.x;
+  const int n = static_cast<int>(p.n);
+  int32_t *idx = p.idx + u * p.idx_stride;
+  if (static_cast<int64_t>(n) <= static_cast<int64_t>(p.topk) + p.recent || p.topk == 0) {
+    // every key, or (no top-k) just the newest `recent`
+    const int j0 = p.topk == 0 && n > p.recent ? n - p.recent : 0;
+    for (int j = j0 + tid; j < n; j += kUThreads) idx[j - j0] = j;
+    if (tid == 0) p.count[u] = n - j0;
+    return;
+  }
+  const float *sel = p.sel + u * p.ncap;
+  const int first_recent = n - p.recent;
+  const int npass = (n + kUPassKeys - 1) / kUPassKeys;
+
+  // 1: pass 0's scores stream in while the boundary bin is found.  The histogram (thread t
+  // owns bins 2047 - 2t and 2046 - 2t, descending: one 8-byte load) and the recent keys'
+  // scores are requested first, so they do not queue behind the bulk copies.
+  const uint2 hv = __ldcg(reinterpret_cast<const uint2 *>(p.hist + u * kHistBins) + (1023 - tid));
+  const float rs = tid < p.recent ? __ldcg(sel + first_recent + tid) : 0.0f;
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_barrier_init();
+    sh.nlist = 0;
+    sh.nnext[0] = 0;
+  }
+  sh.h[2 * tid] = 0u;
+  sh.h[2 * tid + 1] = 0u;
+  if (tid < 256) sh.dh[tid] = 0u;
+  __syncthreads();
+  bool bulk;
+  float *sf = unit_pass_load(buf, sel, min(n, kUPassKeys), &sh.bar, &bulk);
+  if (tid < p.recent) atomicAdd(&sh.h[order_key(rs) >> 21], 1u);
+  for (int t = kUThreads + tid; t < p.recent; t += kUThreads)
+    atomicAdd(&sh.h[order_key(__ldcg(sel + first_recent + t)) >> 21], 1u);
+  __syncthreads();
+  {
+    const uint32_t c0 = hv.y - sh.h[kHistBins - 1 - 2 * tid];
+    const uint32_t c1 = hv.x - sh.h[kHistBins - 2 - 2 * tid];
+    int total;
+    const uint32_t before =
+        static_cast<uint32_t>(unit_scan(static_cast<int>(c0 + c1), &total, sh.warp_sum[0]));
+    const uint32_t topk = static_cast<uint32_t>(p.topk);
+    if (before < topk && before + c0 >= topk) {
+      sh.bin = kHistBins - 1 - 2 * tid;
+      sh.above = static_cast<int>(before);
+    } else if (before + c0 < topk && before + c0 + c1 >= topk) {
+      sh.bin = kHistBins - 2 - 2 * tid;
+      sh.above = static_cast<int>(before + c0);
+    }
+  }
+  __syncthreads();
+  // order keys of b* are [b* << 21, (b* + 1) << 21): a score at or above f_take is selected,
+  // one at or above f_lo and below f_take is a candidate
+  const uint32_t bstar = static_cast<uint32_t>(sh.bin);
+  const float f_lo = key_float(bstar << 21);
+  const float f_take = bstar + 1 < kHistBins ? key_float((bstar + 1) << 21) : __uint_as_float(0x7FC00000u);
+  int need = p.topk - sh.above;
+
+  // 2: classify, one pass of 32768 keys at a time
+  bool landed = true;
+  uint32_t copies = 0;  // bulk copies waited for (the barrier's phase)
+  for (int pass = 0; pass < npass; ++pass) {
+    if (pass > 0) {
+      __syncthreads();  // every thread is done with the previous pass's scores
+      if (landed)
+        sf = unit_pass_load(buf, sel + pass * kUPassKeys, min(n - pass * kUPassKeys, kUPassKeys),
+                            &sh.bar, &bulk);
+      __syncthreads();  // the keys around the bulk copies are stored
+    }
+    if (landed && bulk && !mbar_wait(&sh.bar, copies++ & 1u)) {
+      landed = false;
+      if (tid == 0) atomicOr(p.flags, kFlagWaitTimeout);
+    }
+    // step k reads key 32 tid + ((k + tid) mod 32), so bit k of the step masks belongs to key
+    // bit (k + tid) mod 32: a rotation puts them in place
+    const float *mine = sf + 32 * tid;
+    uint32_t tm = 0u, cm = 0u;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float s = mine[(k + tid) & 31];
+      tm |= (s >= f_take ? 1u : 0u) << k;
+      cm |= (s >= f_lo ? 1u : 0u) << k;
+    }
+    tm = __funnelshift_l(tm, tm, tid & 31);
+    cm = __funnelshift_l(cm, cm, tid & 31) & ~tm;
+    const int k0 = pass * kUPassKeys + 32 * tid;  // this thread's first key
+    if (k0 + 32 > first_recent || !landed) {
+      const uint32_t valid = landed ? bit_range(0, n - k0) : 0u;
+      const uint32_t recent = bit_range(first_recent - k0, n - k0);
+      tm = (tm & valid) | recent;
+      cm &= valid & ~recent;
+    }
+    sh.sel[pass * kUThreads + tid] = tm;
+    sh.cand[pass * kUThreads + tid] = cm;
+    // list the candidates (one shared atomic per warp)
+    const int c = __popc(cm);
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    int base = 0;
+    if (lane == 31 && x > 0) base = atomicAdd(&sh.nlist, x);
+    base = __shfl_sync(0xffffffffu, base, 31) + x - c;
+    while (cm) {
+      const int b = __ffs(cm) - 1;
+      cm &= cm - 1u;
+      const uint64_t key = select_key(mine[b], k0 + b);
+      atomicAdd(&sh.dh[(key >> 45) & 0xFFu], 1u);  // the first narrowing digit
+      if (base < kUListMax) sh.list[0][base] = key;
+      ++base;
+    }
+  }
+  __syncthreads();
+  int m = sh.nlist;
+  int lo = 53;  // bits [lo, 64) of the 64-bit key are decided for the candidates
+  const int nwords = npass * kUThreads;
+  bool dh_ready = true;  // dh holds every candidate's digit of bits [45, 53)
+
+  if (m > kUListMax) {
+    // 3a (crowded boundary bin): decide 8-bit digits over the candidates' bits until the
+    // list can hold them, then list them
+    while (m > kUListMax && lo > 0) {
+      const int nlo = lo >= 8 ? lo - 8 : 0;
+      const uint64_t mask = (1ull << (lo - nlo)) - 1ull;
+      if (!dh_ready) {
+        for (int k = tid; k < nwords; k += kUThreads) {
+          uint32_t cw = sh.cand[k];
+          while (cw) {
+            const int b = __ffs(cw) - 1;
+            cw &= cw - 1u;
+            const int j = 32 * k + b;
+            atomicAdd(&sh.dh[(select_key(__ldcg(sel + j), j) >> nlo) & mask], 1u);
+          }
+        }
+        __syncthreads();
+      }
+      dh_ready = false;
+      if (warp == 0) unit_digit_boundary(sh, need);
+      __syncthreads();
+      const uint64_t dstar = static_cast<uint64_t>(sh.dstar);
+      for (int k = tid; k < nwords; k += kUThreads) {
+        uint32_t cw = sh.cand[k], keep = 0u, take = 0u;
+        while (cw) {
+          const int b = __ffs(cw) - 1;
+          cw &= cw - 1u;
+          const int j = 32 * k + b;
+          const uint64_t d = (select_key(__ldcg(sel + j), j) >> nlo) & mask;
+          if (d > dstar) take |= 1u << b;
+          if (d == dstar) keep |= 1u << b;
+        }
+        sh.sel[k] |= take;
+        sh.cand[k] = keep;
+      }
+      need -= sh.dabove;
+      m = sh.dcount;
+      lo = nlo;
+      if (tid < 256) sh.dh[tid] = 0u;
+      if (tid == 0) sh.nlist = 0;
+      __syncthreads();  // dstar is read by all before the next round rewrites it
+    }
+    for (int k = tid; k < nwords; k += kUThreads) {
+      uint32_t cw = sh.cand[k];
+      while (cw) {
+        const int b = __ffs(cw) - 1;
+        cw &= cw - 1u;
+        const int j = 32 * k + b;
+        const int pos = atomicAdd(&sh.nlist, 1);
+        if (pos < kUListMax) sh.list[0][pos] = select_key(__ldcg(sel + j), j);
+      }
+    }
+    __syncthreads();
+    m = min(sh.nlist, kUListMax);
+  }
+
+  // 3: narrow the listed candidates digit by digit (one candidate per thread); dh holds the
+  // first round's digits or is zero
+  int cur = 0;
+  while (m > 32 && lo > 0) {
+    const int nlo = lo >= 8 ? lo - 8 : 0;
+    const uint64_t mask = (1ull << (lo - nlo)) - 1ull;
+    const uint64_t key = tid < m ? sh.list[cur][tid] : 0ull;
+    const uint32_t dg = static_cast<uint32_t>((key >> nlo) & mask);
+    if (tid == 0) sh.nnext[cur ^ 1] = 0;  // last used two rounds ago
+    if (!dh_ready) {
+      if (tid < m) atomicAdd(&sh.dh[dg], 1u);
+      __syncthreads();
+    }
+    dh_ready = false;
+    if (warp == 0) unit_digit_boundary(sh, need);
+    __syncthreads();
+    const uint32_t dstar = static_cast<uint32_t>(sh.dstar);
+    if (tid < m) {
+      if (dg > dstar) {
+        const int j = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+        atomicOr(&sh.sel[j >> 5], 1u << (j & 31));
+      } else if (dg == dstar) {
+        sh.list[cur ^ 1][atomicAdd(&sh.nnext[cur], 1)] = key;
+      }
+    }
+    need -= sh.dabove;
+    m = sh.dcount;
+    cur ^= 1;
+    lo = nlo;
+    if (tid < 256) sh.dh[tid] = 0u;
+    __syncthreads();  // the next list is complete; dstar is read by all
+  }
+  if (warp == 0) {
+    // at most 32 left: the need highest of them are selected
+    const uint64_t key = lane < m ? sh.list[cur][lane] : 0ull;
+    int greater = 0;
+    for (int i = 0; i < m; ++i) greater += __shfl_sync(0xffffffffu, key, i) > key ? 1 : 0;
+    if (lane < m && greater < need) {
+      const int j = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+      atomicOr(&sh.sel[j >> 5], 1u << (j & 31));
+    }
+  }
+  __syncthreads();
+
+  // 4: ascending indices; thread t takes words t*npass .. t*npass + npass - 1
+  uint32_t wv[kUPasses];
+  int mine = 0;
+#pragma unroll
+  for (int q = 0; q < kUPasses; ++q) {
+    wv[q] = q < npass ? sh.sel[tid * npass + q] : 0u;
+    mine += __popc(wv[q]);
+  }
+  int total;
+  int pos = unit_scan(mine, &total, sh.warp_sum[1]);
+#pragma unroll
+  for (int q = 0; q < kUPasses; ++q) {
+    uint32_t w = wv[q];
+    const int kbase = 32 * (tid * npass + q);
+    while (w) {
+      const int b = __ffs(w) - 1;
+      w &= w - 1u;
+      if (pos < p.idx_stride) idx[pos] = kbase + b;
+      ++pos;
+    }
+  }
+  if (tid == 0) p.count[u] = total;
+}
 }  // namespace
 
 size_t select_workspace_bytes(int64_t units, int64_t ctx_len) {
@@ -876,6 +1272,26 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
                           int idx_stride, int32_t *count, void *workspace, uint32_t *flags,
                           int sm_count, cudaStream_t stream) {
   if (units == 0) return cudaSuccess;
+  if (n <= static_cast<int64_t>(kUPasses) * kUPassKeys) {
+    FastParams f = {};
+    f.sel = sel_scores;
+    f.hist = sel_hist;
+    f.n = n;
+    f.ncap = ncap;
+    f.topk = topk;
+    f.recent = recent;
+    f.cl = 1;
+    f.chunk = n;
+    f.flags = flags;
+    f.idx = idx;
+    f.idx_stride = idx_stride;
+    f.count = count;
+    const int bytes = static_cast<int>(sizeof(UnitShared) + (kUPassKeys + 4) * sizeof(float));
+    cudaError_t e = cudaFuncSetAttribute(select_unit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_unit_kernel, dim3(static_cast<unsigned>(units)), dim3(kUThreads),
+                      static_cast<size_t>(bytes), stream, 0u, f);
+  }
   if (n <= static_cast<int64_t>(kMaxCluster) * kFKeys) {
     // about kFChunk keys per CTA, but no more CTAs than two per SM over all units (one
     // wave), and never more than kFKeys keys in one CTA
