@@ -10,19 +10,14 @@
 // 64-bit key (order_key(sigma) << 32) | (2^32 - 1 - j).  The top 11 bits were
 // histogrammed by the full-layer decode.
 //
-// Contexts up to 8 x 32768 keys (select_fast_kernel): a cluster of one to eight CTAs of
-// 1024 threads per (batch, KV head), each holding the order keys of 32768 keys and its
-// selection bitmap in shared memory:
-//   1  the scores load (coalesced, 32 per thread) while the histogram, minus the recent
-//      keys, gives the boundary bin b* and the count `above` of keys above it;
-//   2  one pass marks the keys above b* (and the recent keys) as selected and those in
-//      b* as candidates, straight from the warp ballots;
-//   3  while the unit has more than kRankMax candidates, an 8-bit digit of the 64-bit
-//      key below the bin is histogrammed over the cluster and the candidates above /
-//      below the boundary digit are decided; the last few are ranked pairwise;
-//   4  each CTA writes the indices of its words in order after those of lower ranks.
+// Contexts up to 8 x 65536 keys: a cluster of two to eight CTAs of 1024 threads per (batch,
+// KV head) (select_cluster_kernel), each holding up to 32768 scores at a time and its
+// selection bitmap in shared memory, or one such CTA (select_single_kernel) for contexts of
+// one pass or when a cluster per unit would not fit in one wave (the steps are described
+// with the kernels).
 //
-// Longer contexts (select_kernel): one cluster of 8 CTAs per (batch, KV head):
+// Longer contexts (select_kernel): one cluster of 8 CTAs per (batch, KV head), the bitmap
+// and candidate lists in the workspace:
 //   A  every CTA finds the boundary bin from the histogram minus the recent keys, while
 //      its chunk of scores is already loading;
 //   B  it classifies its chunk: bitmap words for keys above the bin (and recent keys),
@@ -108,11 +103,6 @@ struct Shared {
 
 __device__ __forceinline__ uint64_t select_key(float s, int64_t j) {
   return (static_cast<uint64_t>(order_key(s)) << 32) |
-         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(j));
-}
-
-__device__ __forceinline__ uint64_t select_key_ok(uint32_t okey, int64_t j) {
-  return (static_cast<uint64_t>(okey) << 32) |
          static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(j));
 }
 
@@ -499,36 +489,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads)
 }
 
 
-// ----------------------------------------------------------------------------- fast path
-
-constexpr int kFThreads = 512;
-constexpr int kFWarps = kFThreads / 32;
-constexpr int kFKeys = 32768;               // keys a CTA can hold
-#ifndef EMBLA_SEL_CHUNK
-#define EMBLA_SEL_CHUNK 8192
-#endif
-constexpr int kFChunk = EMBLA_SEL_CHUNK;    // keys per CTA aimed for (at most 8 CTAs a unit)
-constexpr int kFWords = kFKeys / 32;
-constexpr int kRankMax = 256;               // candidates ranked pairwise
-constexpr int kMaxCluster = 8;              // CTAs per unit: contexts up to 262144 keys
-
-// Shared memory of a CTA: this struct, then the chunk's scores (turned into order keys in
-// place), chunk + 4 entries, sized at launch.
-struct __align__(16) FastShared {
-  uint32_t sel[kFWords];      // selected
-  uint32_t cand[kFWords];     // still undecided (in the boundary bin)
-  uint32_t h[kHistBins];
-  uint64_t list[kRankMax];    // every candidate of the unit (ranking step)
-  uint64_t mine[kRankMax];    // this CTA's candidates
-  uint32_t dh[256];           // digit histogram of this CTA's candidates
-  int32_t warp_sum[kFWarps];
-  int32_t picked[kMaxCluster];  // candidates chosen per CTA of the cluster
-  int32_t info_mine[kMaxCluster], info_sel[kMaxCluster], info_off[kMaxCluster + 1];
-  int32_t bin, above, ncand, nmine, nsel, dstar, dabove, overflow;
-  uint64_t bar;
-};
-static_assert(sizeof(FastShared) % 16 == 0, "the scores that follow start 16-byte aligned");
-
+// Parameters of the cluster path (below).
 struct FastParams {
   const float *sel;
   const uint32_t *hist;
@@ -540,346 +501,25 @@ struct FastParams {
   uint32_t *flags;
 };
 
-__device__ __forceinline__ int fast_scan(int v, int *total, int32_t *warp_sum) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sum[warp] = x;
-  __syncthreads();
-  const int ws = lane < kFWarps ? warp_sum[lane] : 0;
-  int incl = ws;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const int before = __shfl_sync(0xffffffffu, incl - ws, warp);
-  *total = __shfl_sync(0xffffffffu, incl, kFWarps - 1);
-  __syncthreads();
-  return before + x - v;
-}
-
-__global__ void __launch_bounds__(kFThreads, 1) select_fast_kernel(const FastParams p) {
-  pdl_wait_primary();  // the scores and histogram are complete
-  pdl_launch_dependents();
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  FastShared &sh = *reinterpret_cast<FastShared *>(smem_raw);
-  cg::cluster_group cluster = cg::this_cluster();
-  const int cl = p.cl;
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int64_t u = blockIdx.x / cl;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int64_t n = p.n;
-  const int64_t j0 = rank * p.chunk;
-  const int64_t j1 = min(n, j0 + p.chunk);
-  const int nloc = j1 > j0 ? static_cast<int>(j1 - j0) : 0;  // keys of this CTA
-  const int nwords = (nloc + 31) >> 5;
-  int32_t *idx = p.idx + u * p.idx_stride;
-
-  if (n <= static_cast<int64_t>(p.topk) + p.recent) {
-    for (int64_t j = j0 + tid; j < j1; j += kFThreads) idx[j] = static_cast<int32_t>(j);
-    if (rank == 0 && tid == 0) p.count[u] = static_cast<int32_t>(n);
-    return;
-  }
-  const float *sel = p.sel + u * p.ncap;
-  const int64_t first_recent = n - p.recent;
-
-  // 1: this CTA's scores stream in with one bulk copy (the 16-byte aligned middle; the
-  // few keys before and after it load directly) while the histogram, minus the recent
-  // keys, gives the boundary bin.  Key k of the chunk sits at entry phase + k, so the
-  // copied middle starts on a 16-byte boundary of shared memory as it does in global.
-  const uint64_t gbeg = reinterpret_cast<uint64_t>(sel + j0);
-  const uint64_t gend = reinterpret_cast<uint64_t>(sel + j1);
-  const uint64_t abeg = (gbeg + 15u) & ~15ull, aend = gend & ~15ull;
-  const bool bulk = nloc > 0 && aend > abeg;
-  const int phase = static_cast<int>((gbeg >> 2) & 3u);
-  const int head = bulk ? static_cast<int>((abeg - gbeg) / 4) : nloc;   // keys before it
-  const int mid_end = bulk ? static_cast<int>((aend - gbeg) / 4) : nloc;
-  uint32_t *okey = reinterpret_cast<uint32_t *>(smem_raw + sizeof(FastShared)) + phase;
-  float *sf = reinterpret_cast<float *>(okey);
-  if (tid == 0) {
-    mbar_init(&sh.bar, 1);
-    fence_barrier_init();
-    if (bulk) {
-      mbar_arrive_expect_tx(&sh.bar, static_cast<uint32_t>(aend - abeg));
-      // the shared destination keeps the same 16-byte phase as the source
-      bulk_load(sf + head, reinterpret_cast<const void *>(abeg), static_cast<uint32_t>(aend - abeg), &sh.bar);
-    }
-    sh.ncand = 0;
-    sh.nmine = 0;
-    sh.nsel = 0;
-    sh.overflow = 0;
-    sh.bin = kHistBins;  // topk == 0: no bin holds a selected key
-    sh.above = 0;
-  }
-  for (int k = tid; k < head; k += kFThreads) sf[k] = sel[j0 + k];
-  for (int k = mid_end + tid; k < nloc; k += kFThreads) sf[k] = sel[j0 + k];
-  // the recent keys' scores load together with the histogram (one round trip)
-  const bool has_recent = tid < p.recent;
-  const float rsig = has_recent ? sel[first_recent + tid] : 0.0f;
-  for (int b = tid; b < kHistBins; b += kFThreads) sh.h[b] = p.hist[u * kHistBins + b];
-  if (tid < 256) sh.dh[tid] = 0u;
-  if (tid < kMaxCluster) sh.picked[tid] = 0;
-  __syncthreads();
-  if (has_recent) atomicSub(&sh.h[order_key(rsig) >> 21], 1u);
-  for (int64_t j = first_recent + kFThreads + tid; j < n; j += kFThreads)
-    atomicSub(&sh.h[order_key(sel[j]) >> 21], 1u);
-  __syncthreads();
-  {
-    // thread t owns bins 2047 - 4t .. 2044 - 4t (descending)
-    uint32_t c[4], tot = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      c[k] = sh.h[kHistBins - 1 - 4 * tid - k];
-      tot += c[k];
-    }
-    int total;
-    uint32_t before = static_cast<uint32_t>(fast_scan(static_cast<int>(tot), &total, sh.warp_sum));
-    const uint32_t topk = static_cast<uint32_t>(p.topk);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (before < topk && before + c[k] >= topk) {
-        sh.bin = kHistBins - 1 - 4 * tid - k;
-        sh.above = static_cast<int>(before);
-      }
-      before += c[k];
-    }
-  }
-  const bool landed = !bulk || mbar_wait(&sh.bar, 0);
-  if (!landed && tid == 0) atomicOr(p.flags, kFlagWaitTimeout);
-  __syncthreads();
-  const uint32_t bstar = static_cast<uint32_t>(sh.bin);
-  int need = p.topk - sh.above;
-
-  // 2: classify, four steps of kFThreads keys at a time; the ballot of warp w in step i
-  // is bitmap word 16 i + w
-  int nsel = 0;
-  for (int base = 0; base < nwords * 32; base += 4 * kFThreads) {
-    uint32_t ok[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int jl = base + r * kFThreads + tid;
-      ok[r] = jl < nloc ? order_key(sf[jl]) : 0u;
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int jl = base + r * kFThreads + tid;
-      const int64_t j = j0 + jl;
-      const bool valid = jl < nloc && landed;
-      if (jl < nloc) okey[jl] = ok[r];  // in place: the same thread read this entry
-      const bool recent = valid && j >= first_recent;
-      const uint32_t b = ok[r] >> 21;
-      const bool take = recent || (valid && b > bstar);
-      const bool maybe = valid && !recent && b == bstar;
-      const uint32_t wsel = __ballot_sync(0xffffffffu, take);
-      const uint32_t wcand = __ballot_sync(0xffffffffu, maybe);
-      // one atomic per warp for its candidates' places in the list
-      int cbase = 0;
-      if (lane == 0) {
-        if ((jl >> 5) < kFWords) {
-          sh.sel[jl >> 5] = wsel;
-          sh.cand[jl >> 5] = wcand;
-          nsel += __popc(wsel);
-        }
-        if (wcand) cbase = atomicAdd(&sh.nmine, __popc(wcand));
-      }
-      cbase = __shfl_sync(0xffffffffu, cbase, 0);
-      if (maybe) {
-        const int pos = cbase + __popc(wcand & ((1u << lane) - 1u));
-        if (pos < kRankMax) sh.mine[pos] = select_key_ok(ok[r], j);
-      }
-    }
-  }
-  if (lane == 0 && nsel) atomicAdd(&sh.nsel, nsel);
-  __syncthreads();
-  if (tid == 0) {
-    sh.ncand = sh.nmine;
-    sh.overflow = sh.nmine > kRankMax;
-  }
-  cluster.sync();
-  int m = 0;
-  bool overflow = false;
-  for (int c = 0; c < cl; ++c) {
-    const FastShared *o = cluster.map_shared_rank(&sh, c);
-    m += o->ncand;
-    overflow |= o->overflow != 0;
-  }
-
-  if (m > kRankMax || overflow) {
-    // 3a (crowded boundary bin): decide the candidates digit by digit until few are left
-    int lo = 53;  // 64-bit key bits [lo, 64) are decided
-    while (m > kRankMax && lo > 0) {
-      const int nlo = lo >= 8 ? lo - 8 : 0;
-      const uint64_t mask = (1ull << (lo - nlo)) - 1ull;
-      for (int w = tid; w < nwords; w += kFThreads) {
-        uint32_t cw = sh.cand[w];
-        while (cw) {
-          const int bb = __ffs(cw) - 1;
-          cw &= cw - 1u;
-          const int jl = 32 * w + bb;
-          atomicAdd(&sh.dh[(select_key_ok(okey[jl], j0 + jl) >> nlo) & mask], 1u);
-        }
-      }
-      cluster.sync();
-      {
-        // thread t < 256: digit 255 - t summed over the cluster; a descending scan finds
-        // the digit holding the need-th candidate
-        const int d = 255 - tid;
-        int v = 0;
-        if (tid < 256)
-          for (int c = 0; c < cl; ++c) v += static_cast<int>(cluster.map_shared_rank(sh.dh, c)[d]);
-        int total;
-        const int above = fast_scan(v, &total, sh.warp_sum);
-        if (tid < 256 && above < need && above + v >= need) {
-          sh.dstar = d;
-          sh.dabove = above;
-          sh.ncand = v;
-        }
-      }
-      cluster.sync();  // every CTA has read the others' digit counts
-      const uint64_t dstar = static_cast<uint64_t>(sh.dstar);
-      for (int w = tid; w < nwords; w += kFThreads) {
-        uint32_t cw = sh.cand[w], keep = 0u, take = 0u;
-        while (cw) {
-          const int bb = __ffs(cw) - 1;
-          cw &= cw - 1u;
-          const int jl = 32 * w + bb;
-          const uint64_t d = (select_key_ok(okey[jl], j0 + jl) >> nlo) & mask;
-          if (d > dstar) take |= 1u << bb;
-          if (d == dstar) keep |= 1u << bb;
-        }
-        sh.sel[w] |= take;
-        sh.cand[w] = keep;
-      }
-      if (tid < 256) sh.dh[tid] = 0u;
-      need -= sh.dabove;
-      m = sh.ncand;
-      lo = nlo;
-      __syncthreads();
-    }
-    // the selected counts changed: recount, then list the remaining candidates
-    int cnt = 0;
-    for (int w = tid; w < nwords; w += kFThreads) cnt += __popc(sh.sel[w]);
-    int total;
-    fast_scan(cnt, &total, sh.warp_sum);
-    if (tid == 0) {
-      sh.nsel = total;
-      sh.nmine = 0;
-    }
-    __syncthreads();
-    for (int w = tid; w < nwords; w += kFThreads) {
-      uint32_t cw = sh.cand[w];
-      while (cw) {
-        const int bb = __ffs(cw) - 1;
-        cw &= cw - 1u;
-        const int jl = 32 * w + bb;
-        const int pos = atomicAdd(&sh.nmine, 1);
-        if (pos < kRankMax) sh.mine[pos] = select_key_ok(okey[jl], j0 + jl);
-      }
-    }
-    cluster.sync();
-  }
-
-  // 3: every CTA ranks all of the unit's candidates (so it also knows how many of each
-  // CTA's are chosen) and marks its own chosen keys.  Remote reads are issued together:
-  // thread c reads CTA c's counts, then every thread fetches its share of the lists.
-  if (tid < cl) {
-    const FastShared *o = cluster.map_shared_rank(&sh, tid);
-    sh.info_mine[tid] = min(o->nmine, kRankMax);
-    sh.info_sel[tid] = o->nsel;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int c = 0; c < cl; ++c) {
-      sh.info_off[c] = acc;
-      acc += sh.info_mine[c];
-    }
-    sh.info_off[cl] = acc;
-  }
-  __syncthreads();
-  const int ml = min(sh.info_off[cl], kRankMax);
-  for (int i = tid; i < ml; i += kFThreads) {
-    int c = 0;
-    while (i >= sh.info_off[c + 1]) ++c;
-    sh.list[i] = cluster.map_shared_rank(sh.mine, c)[i - sh.info_off[c]];
-  }
-  __syncthreads();
-  cluster_arrive();  // no more reads of the other CTAs' shared memory
-  // T consecutive threads share a key, each comparing it with every T-th entry
-  int T = 1;
-  while (T < 32 && T * 2 * ml <= kFThreads) T *= 2;
-  const int sub = tid & (T - 1);
-  const int per_round = kFThreads / T;
-  const int rounds = (ml + per_round - 1) / per_round;
-  for (int r = 0; r < rounds; ++r) {
-    const int k = r * per_round + tid / T;
-    const bool real = k < ml;
-    const uint64_t key = real ? sh.list[k] : 0ull;
-    int greater = 0;
-#pragma unroll 4
-    for (int i = sub; i < ml; i += T) greater += sh.list[i] > key ? 1 : 0;
-    for (int o = 1; o < T; o <<= 1) greater += __shfl_xor_sync(0xffffffffu, greater, o);
-    if (real && sub == 0 && greater < need) {
-      const int64_t j = 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull);
-      const int owner = static_cast<int>(j / p.chunk);
-      atomicAdd(&sh.picked[owner], 1);
-      if (owner == rank) {
-        const int jl = static_cast<int>(j - j0);
-        atomicOr(&sh.sel[jl >> 5], 1u << (jl & 31));
-      }
-    }
-  }
-  __syncthreads();
-
-  // 4: ascending indices, after the lower ranks' keys
-  int before = 0, all = 0;
-  for (int c = 0; c < cl; ++c) {
-    const int t = sh.info_sel[c] + sh.picked[c];
-    before += c < rank ? t : 0;
-    all += t;
-  }
-  // thread t owns words 2t and 2t + 1
-  const uint32_t w0 = 2 * tid < nwords ? sh.sel[2 * tid] : 0u;
-  const uint32_t w1 = 2 * tid + 1 < nwords ? sh.sel[2 * tid + 1] : 0u;
-  int total;
-  const int pre = fast_scan(__popc(w0) + __popc(w1), &total, sh.warp_sum);
-  int64_t pos = before + pre;
-  uint32_t w = w0;
-  for (int half = 0; half < 2; ++half) {
-    const int64_t kbase = j0 + 32 * (2 * tid + half);
-    while (w) {
-      const int bb = __ffs(w) - 1;
-      w &= w - 1u;
-      if (pos < p.idx_stride) idx[pos] = static_cast<int32_t>(kbase + bb);
-      ++pos;
-    }
-    w = w1;
-  }
-  if (rank == 0 && tid == 0) p.count[u] = all;
-  cluster_wait();  // the others are done reading this CTA's shared memory
-}
-
-// ----------------------------------------------------------------------------- one CTA per unit
+// ----------------------------------------------------------------------------- cluster path
 //
-// Contexts up to kUPasses x 32768 keys: one CTA of 1024 threads per unit and no cluster, so
-// the whole selection is a short chain of block barriers.
-//   1  a pass's 32768 scores land in shared memory by bulk copies (the 16-byte aligned
-//      middle; the few keys before and after it load directly) while the histogram, minus
-//      the recent keys, gives the boundary bin b*;
+// Contexts up to 8 x kUPasses x 32768 keys: a cluster of C (1, 2, 4 or 8) CTAs of 1024
+// threads per unit, CTA r owning keys [r chunk, (r + 1) chunk), chunk a multiple of 32.
+//   1  a pass's (up to 32768) scores land in shared memory by bulk copies (the 16-byte
+//      aligned middle; the few keys before and after it load directly) while the
+//      histogram, minus the recent keys, gives the boundary bin b* (every CTA finds it);
 //   2  thread t classifies keys 32t .. 32t + 31 of the pass (read in a rotated order, so a
 //      warp's reads hit 32 banks), comparing each score as a float against the edges of b*
 //      (exact for non-NaN scores): one bitmap word of keys above b* (and recent keys) and
-//      one of keys in b*, which are also listed with their 64-bit order keys;
-//   3  the listed candidates are narrowed by 8-bit digits of the 64-bit key below the bin
-//      (a digit histogram, one warp's scan, the keys above the boundary digit selected) until
-//      at most 32 are left, which one warp ranks pairwise.  A boundary bin of more than
-//      kUListMax keys is first narrowed the same way over the bitmap;
-//   4  one block scan over the words in key order places every selected index.
+//      one of keys in b*, which are also listed with their 64-bit order keys and counted
+//      by their next 8-bit digit;
+//   3  after one cluster barrier every CTA reads all CTAs' candidate lists, digit counts
+//      and selected counts (distributed shared memory) and narrows the candidates by 8-bit
+//      digits of the 64-bit key below the bin until at most 32 are left, which one warp
+//      ranks pairwise.  Every CTA reaches the same winners, so each knows how many keys
+//      every CTA keeps without a second barrier.  More than kUListMax candidates in b*
+//      are first narrowed over the bitmaps, a cluster barrier per digit;
+//   4  each CTA writes its keys' indices after those of lower ranks.
 
 constexpr int kUThreads = 1024;
 constexpr int kUWarps = kUThreads / 32;
@@ -900,15 +540,25 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+constexpr int kUMaxCluster = 8;
+#ifndef EMBLA_SEL_CHUNK_TARGET
+#define EMBLA_SEL_CHUNK_TARGET 8192
+#endif
+constexpr int kUChunkTarget = EMBLA_SEL_CHUNK_TARGET;  // keys per CTA aimed for
+
 struct __align__(16) UnitShared {
   uint32_t h[kHistBins];       // recent keys per bin
-  uint32_t sel[kUWords];       // selected
-  uint32_t cand[kUWords];      // in the boundary bin, undecided
-  uint64_t list[2][kUListMax]; // listed candidates (current, next)
-  uint32_t dh[256];
+  uint32_t sel[kUWords];       // selected (this CTA's keys)
+  uint32_t cand[kUWords];      // in the boundary bin, undecided (this CTA's keys)
+  uint64_t mine[kUListMax];    // this CTA's candidates
+  uint64_t list[2][kUListMax]; // the unit's candidates (current, next)
+  uint32_t dh[256];            // this CTA's candidates per digit
+  uint32_t gdh[256];           // the unit's candidates per digit
   int32_t warp_sum[2][kUWarps];
+  int32_t off[kUMaxCluster + 1];  // list offsets of the CTAs' candidates
+  int32_t kept[kUMaxCluster];     // keys each CTA keeps (selected + winners)
   int32_t nnext[2];
-  int32_t bin, above, nlist, dstar, dabove, dcount;
+  int32_t bin, above, nlist, nsure, dstar, dabove, dcount, pad_;
   uint64_t bar;
 };
 static_assert(sizeof(UnitShared) % 16 == 0, "the scores that follow start 16-byte aligned");
@@ -937,14 +587,14 @@ __device__ __forceinline__ int unit_scan(int v, int *total, int32_t *ws) {
   return before + x - v;
 }
 
-// Warp 0: the boundary digit of the 256-bin digit histogram dh (descending) for the need-th
+// One warp: the boundary digit of the 256-bin digit histogram dh (descending) for the need-th
 // key; writes dstar, dabove (keys in higher digits) and dcount (keys in it).
-__device__ __forceinline__ void unit_digit_boundary(UnitShared &sh, int need) {
+__device__ __forceinline__ void unit_digit_boundary(UnitShared &sh, const uint32_t *dh, int need) {
   const int lane = threadIdx.x & 31;
   uint32_t c[8], tot = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    c[k] = sh.dh[255 - 8 * lane - k];  // lane l: digits 255 - 8l .. 248 - 8l
+    c[k] = dh[255 - 8 * lane - k];  // lane l: digits 255 - 8l .. 248 - 8l
     tot += c[k];
   }
   uint32_t x = tot;
@@ -1009,7 +659,49 @@ __device__ __forceinline__ uint32_t bit_range(int a, int b) {
   return hi & ~lo;
 }
 
-__global__ void __launch_bounds__(kUThreads, 1) select_unit_kernel(const FastParams p) {
+// Thread t classifies KP = 32 / S keys of bitmap word w = t / S of a pass (part t % S of it):
+// keys 32w + KP part + i, read in an order rotated by w so that a warp's reads hit 32 banks.
+// Every lane of the word's S lanes ends with the word's masks: scores at or above f_take
+// (tm) and those at or above f_lo (cm).
+template <int KP>
+__device__ __forceinline__ void unit_classify(const float *sf, float f_take, float f_lo,
+                                              uint32_t &tm, uint32_t &cm) {
+  constexpr int S = 32 / KP;
+  const int w = threadIdx.x / S, part = threadIdx.x % S;
+  const float *mine = sf + 32 * w + KP * part;
+  const int rot = w & (KP - 1);
+  uint32_t a = 0u, c = 0u;
+#pragma unroll
+  for (int k = 0; k < KP; ++k) {
+    const float s = mine[(k + rot) & (KP - 1)];
+    a |= (s >= f_take ? 1u : 0u) << k;
+    c |= (s >= f_lo ? 1u : 0u) << k;
+  }
+  // bit k belongs to key (k + rot) mod KP
+  if constexpr (KP == 32) {
+    a = __funnelshift_l(a, a, rot);
+    c = __funnelshift_l(c, c, rot);
+  } else {
+    constexpr uint32_t full = (1u << KP) - 1u;
+    a = ((a << rot) | (a >> (KP - rot))) & full;
+    c = ((c << rot) | (c >> (KP - rot))) & full;
+  }
+  a <<= KP * part;
+  c <<= KP * part;
+#pragma unroll
+  for (int o = 1; o < S; o <<= 1) {
+    a |= __shfl_xor_sync(0xffffffffu, a, o);
+    c |= __shfl_xor_sync(0xffffffffu, c, o);
+  }
+  tm = a;
+  cm = c;
+}
+
+// One CTA per unit (contexts up to kUPasses x 32768 keys when a cluster would not fit in
+// one wave, and every context of one pass): the steps of the cluster path with every
+// exchange a block barrier, the candidates listed and counted by digit straight into the
+// unit's list.
+__global__ void __launch_bounds__(kUThreads, 1) select_single_kernel(const FastParams p) {
   pdl_wait_primary();  // the scores and histogram are complete
   pdl_launch_dependents();
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -1155,7 +847,7 @@ __global__ void __launch_bounds__(kUThreads, 1) select_unit_kernel(const FastPar
         __syncthreads();
       }
       dh_ready = false;
-      if (warp == 0) unit_digit_boundary(sh, need);
+      if (warp == 0) unit_digit_boundary(sh, sh.dh, need);
       __syncthreads();
       const uint64_t dstar = static_cast<uint64_t>(sh.dstar);
       for (int k = tid; k < nwords; k += kUThreads) {
@@ -1206,7 +898,7 @@ __global__ void __launch_bounds__(kUThreads, 1) select_unit_kernel(const FastPar
       __syncthreads();
     }
     dh_ready = false;
-    if (warp == 0) unit_digit_boundary(sh, need);
+    if (warp == 0) unit_digit_boundary(sh, sh.dh, need);
     __syncthreads();
     const uint32_t dstar = static_cast<uint32_t>(sh.dstar);
     if (tid < m) {
@@ -1259,11 +951,356 @@ __global__ void __launch_bounds__(kUThreads, 1) select_unit_kernel(const FastPar
   }
   if (tid == 0) p.count[u] = total;
 }
+__global__ void __launch_bounds__(kUThreads, 1) select_cluster_kernel(const FastParams p) {
+  pdl_wait_primary();  // the scores and histogram are complete
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  UnitShared &sh = *reinterpret_cast<UnitShared *>(smem_raw);
+  float *buf = reinterpret_cast<float *>(smem_raw + sizeof(UnitShared));
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = p.cl;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t u = blockIdx.x / C;
+  const int n = static_cast<int>(p.n);
+  const int chunk = static_cast<int>(p.chunk);
+  const int j0 = min(n, rank * chunk), j1 = min(n, j0 + chunk);  // this CTA's keys
+  const int nloc = j1 - j0;
+  int32_t *idx = p.idx + u * p.idx_stride;
+  if (static_cast<int64_t>(n) <= static_cast<int64_t>(p.topk) + p.recent || p.topk == 0) {
+    // every key, or (no top-k) just the newest `recent`
+    const int start = p.topk == 0 && n > p.recent ? n - p.recent : 0;
+    for (int j = max(start, j0) + tid; j < j1; j += kUThreads) idx[j - start] = j;
+    if (rank == 0 && tid == 0) p.count[u] = n - start;
+    return;
+  }
+  const float *sel = p.sel + u * p.ncap;
+  const int first_recent = n - p.recent;
+  // keys per thread: 8, 16 or 32 (passes of 8192, 16384 or 32768 keys)
+  const int kp = nloc <= kUPassKeys / 4 ? 8 : (nloc <= kUPassKeys / 2 ? 16 : 32);
+  const int npass = (nloc + kUPassKeys - 1) / kUPassKeys;  // one unless kp is 32
+  const int nwords = (nloc + 31) / 32;                   // bitmap words of this CTA
+  const int spt = 32 / kp;                               // threads per word
+
+  // 1: pass 0's scores stream in while the boundary bin is found.  The histogram (thread t
+  // owns bins 2047 - 2t and 2046 - 2t, descending: one 8-byte load) and the recent keys'
+  // scores are requested first, so they do not queue behind the bulk copies.
+  const uint2 hv = __ldcg(reinterpret_cast<const uint2 *>(p.hist + u * kHistBins) + (1023 - tid));
+  const float rs = tid < p.recent ? __ldcg(sel + first_recent + tid) : 0.0f;
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_barrier_init();
+    sh.nlist = 0;
+    sh.nsure = 0;
+    sh.nnext[0] = 0;
+  }
+  sh.h[2 * tid] = 0u;
+  sh.h[2 * tid + 1] = 0u;
+  if (tid < 256) {
+    sh.dh[tid] = 0u;
+    sh.gdh[tid] = 0u;
+  }
+  if (tid < kUMaxCluster) sh.kept[tid] = 0;
+
+  __syncthreads();
+  bool bulk;
+  float *sf = unit_pass_load(buf, sel + j0, min(nloc, kUPassKeys), &sh.bar, &bulk);
+  if (tid < p.recent) atomicAdd(&sh.h[order_key(rs) >> 21], 1u);
+  for (int t = kUThreads + tid; t < p.recent; t += kUThreads)
+    atomicAdd(&sh.h[order_key(__ldcg(sel + first_recent + t)) >> 21], 1u);
+  __syncthreads();
+  {
+    const uint32_t c0 = hv.y - sh.h[kHistBins - 1 - 2 * tid];
+    const uint32_t c1 = hv.x - sh.h[kHistBins - 2 - 2 * tid];
+    int total;
+    const uint32_t before =
+        static_cast<uint32_t>(unit_scan(static_cast<int>(c0 + c1), &total, sh.warp_sum[0]));
+    const uint32_t topk = static_cast<uint32_t>(p.topk);
+    if (before < topk && before + c0 >= topk) {
+      sh.bin = kHistBins - 1 - 2 * tid;
+      sh.above = static_cast<int>(before);
+    } else if (before + c0 < topk && before + c0 + c1 >= topk) {
+      sh.bin = kHistBins - 2 - 2 * tid;
+      sh.above = static_cast<int>(before + c0);
+    }
+  }
+  __syncthreads();
+  // order keys of b* are [b* << 21, (b* + 1) << 21): a score at or above f_take is selected,
+  // one at or above f_lo and below f_take is a candidate
+  const uint32_t bstar = static_cast<uint32_t>(sh.bin);
+  const float f_lo = key_float(bstar << 21);
+  const float f_take = bstar + 1 < kHistBins ? key_float((bstar + 1) << 21) : __uint_as_float(0x7FC00000u);
+  int need = p.topk - sh.above;
+
+  // 2: classify, one pass of 32768 keys at a time
+  bool landed = true;
+  uint32_t copies = 0;  // bulk copies waited for (the barrier's phase)
+  int sure = 0;         // keys this thread selected
+  for (int pass = 0; pass < npass; ++pass) {
+    if (pass > 0) {
+      __syncthreads();  // every thread is done with the previous pass's scores
+      if (landed)
+        sf = unit_pass_load(buf, sel + j0 + pass * kUPassKeys, min(nloc - pass * kUPassKeys, kUPassKeys),
+                            &sh.bar, &bulk);
+      __syncthreads();  // the keys around the bulk copies are stored
+    }
+    if (landed && bulk && !mbar_wait(&sh.bar, copies++ & 1u)) {
+      landed = false;
+      if (tid == 0) atomicOr(p.flags, kFlagWaitTimeout);
+    }
+    uint32_t tm, cm;
+    if (kp == 8)
+      unit_classify<8>(sf, f_take, f_lo, tm, cm);
+    else if (kp == 16)
+      unit_classify<16>(sf, f_take, f_lo, tm, cm);
+    else
+      unit_classify<32>(sf, f_take, f_lo, tm, cm);
+    cm &= ~tm;
+    const int wp = tid / spt;                           // the word within the pass
+    const int wk = pass * (kUPassKeys / 32) + wp;       // and within this CTA
+    const int k0 = j0 + 32 * wk;                        // its first key
+    if (k0 + 32 > first_recent || k0 + 32 > j1 || !landed) {
+      const uint32_t valid = landed ? bit_range(0, j1 - k0) : 0u;
+      const uint32_t recent = bit_range(first_recent - k0, j1 - k0);
+      tm = (tm & valid) | recent;
+      cm &= valid & ~recent;
+    }
+    if (tid % spt != 0) tm = cm = 0u;  // one lane of the word keeps it
+    if (tid % spt == 0 && wk < nwords) {
+      sh.sel[wk] = tm;
+      sh.cand[wk] = cm;
+    }
+    sure += __popc(tm);
+    // list the candidates (one shared atomic per warp) and count their next digit
+    const int c = __popc(cm);
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    int base = 0;
+    if (lane == 31 && x > 0) base = atomicAdd(&sh.nlist, x);
+    base = __shfl_sync(0xffffffffu, base, 31) + x - c;
+    while (cm) {
+      const int b = __ffs(cm) - 1;
+      cm &= cm - 1u;
+      const uint64_t key = select_key(sf[32 * wp + b], k0 + b);
+      atomicAdd(&sh.dh[(key >> 45) & 0xFFu], 1u);  // the first narrowing digit
+      if (base < kUListMax) sh.mine[base] = key;
+      ++base;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sure += __shfl_xor_sync(0xffffffffu, sure, o);
+  if (lane == 0 && sure) atomicAdd(&sh.nsure, sure);
+  cluster.sync();  // every CTA's candidates, digit counts and selected counts
+
+  // 3: every CTA's candidate and selected counts, and the unit's first-digit counts
+  if (tid < C) {
+    const UnitShared *o = cluster.map_shared_rank(&sh, tid);
+    sh.off[tid] = o->nlist;
+    sh.kept[tid] = o->nsure;
+  }
+  if (tid < 256) {
+    uint32_t v = 0u;
+#pragma unroll
+    for (int c = 0; c < kUMaxCluster; ++c)
+      if (c < C) v += cluster.map_shared_rank(sh.dh, c)[tid];
+    sh.gdh[tid] = v;
+  }
+  __syncthreads();
+  int m = 0;
+#pragma unroll
+  for (int c = 0; c < kUMaxCluster; ++c) m += c < C ? sh.off[c] : 0;
+  int lo = 53;            // bits [lo, 64) of the 64-bit key are decided for the candidates
+  bool gdh_ready = true;  // gdh counts the unit's candidates by their digit of bits [45, 53)
+
+  if (m > kUListMax) {
+    // 3a (crowded boundary bin): decide 8-bit digits over the CTAs' bitmaps, a cluster
+    // barrier per digit, until the list can hold the unit's candidates
+    while (m > kUListMax && lo > 0) {
+      const int nlo = lo >= 8 ? lo - 8 : 0;
+      const uint64_t mask = (1ull << (lo - nlo)) - 1ull;
+      if (!gdh_ready) {
+        for (int k = tid; k < nwords; k += kUThreads) {
+          uint32_t cw = sh.cand[k];
+          while (cw) {
+            const int b = __ffs(cw) - 1;
+            cw &= cw - 1u;
+            const int j = j0 + 32 * k + b;
+            atomicAdd(&sh.dh[(select_key(__ldcg(sel + j), j) >> nlo) & mask], 1u);
+          }
+        }
+        cluster.sync();
+        if (tid < 256) {
+          uint32_t v = 0u;
+#pragma unroll
+          for (int c = 0; c < kUMaxCluster; ++c)
+            if (c < C) v += cluster.map_shared_rank(sh.dh, c)[tid];
+          sh.gdh[tid] = v;
+        }
+        __syncthreads();
+      }
+      gdh_ready = false;
+      if (warp == 0) unit_digit_boundary(sh, sh.gdh, need);
+      __syncthreads();
+      const uint64_t dstar = static_cast<uint64_t>(sh.dstar);
+      for (int k = tid; k < nwords; k += kUThreads) {
+        uint32_t cw = sh.cand[k], keep = 0u, take = 0u;
+        while (cw) {
+          const int b = __ffs(cw) - 1;
+          cw &= cw - 1u;
+          const int j = j0 + 32 * k + b;
+          const uint64_t d = (select_key(__ldcg(sel + j), j) >> nlo) & mask;
+          if (d > dstar) take |= 1u << b;
+          if (d == dstar) keep |= 1u << b;
+        }
+        sh.sel[k] |= take;
+        sh.cand[k] = keep;
+      }
+      need -= sh.dabove;
+      m = sh.dcount;
+      lo = nlo;
+      cluster.sync();  // every CTA has read the others' digit counts
+      if (tid < 256) sh.dh[tid] = 0u;
+      __syncthreads();
+    }
+    // list what is left of this CTA's candidates; count its selected keys again
+    if (tid == 0) {
+      sh.nlist = 0;
+      sh.nsure = 0;
+    }
+    __syncthreads();
+    int cnt = 0;
+    for (int k = tid; k < nwords; k += kUThreads) {
+      cnt += __popc(sh.sel[k]);
+      uint32_t cw = sh.cand[k];
+      while (cw) {
+        const int b = __ffs(cw) - 1;
+        cw &= cw - 1u;
+        const int j = j0 + 32 * k + b;
+        const int pos = atomicAdd(&sh.nlist, 1);
+        if (pos < kUListMax) sh.mine[pos] = select_key(__ldcg(sel + j), j);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0 && cnt) atomicAdd(&sh.nsure, cnt);
+    cluster.sync();
+    if (tid < C) {
+      const UnitShared *o = cluster.map_shared_rank(&sh, tid);
+      sh.off[tid] = o->nlist;
+      sh.kept[tid] = o->nsure;
+    }
+    if (tid < 256) sh.gdh[tid] = 0u;
+    __syncthreads();
+  }
+
+  // gather the unit's candidates
+  int start[kUMaxCluster + 1];
+  start[0] = 0;
+#pragma unroll
+  for (int c = 0; c < kUMaxCluster; ++c) start[c + 1] = start[c] + (c < C ? min(sh.off[c], kUListMax) : 0);
+  m = min(start[kUMaxCluster], kUListMax);
+  for (int i = tid; i < m; i += kUThreads) {
+    int c = 0, sc = 0;
+#pragma unroll
+    for (int cc = 1; cc < kUMaxCluster; ++cc)
+      if (cc < C && i >= start[cc]) {
+        c = cc;
+        sc = start[cc];
+      }
+    sh.list[0][i] = cluster.map_shared_rank(sh.mine, c)[i - sc];
+  }
+  __syncthreads();
+  cluster_arrive();  // no more reads of the other CTAs' shared memory
+
+  // 3b: narrow the unit's candidates digit by digit (one candidate per thread; every CTA the
+  // same); gdh holds the first round's digits or is zero.  A winner is counted for the CTA
+  // that owns it and, if that is this one, marked.
+  auto win = [&](uint64_t key) {
+    const int j = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+    const int owner = j / chunk;
+    atomicAdd(&sh.kept[owner], 1);
+    if (owner == rank) atomicOr(&sh.sel[(j - j0) >> 5], 1u << ((j - j0) & 31));
+  };
+  int cur = 0;
+  while (m > 32 && lo > 0) {
+    const int nlo = lo >= 8 ? lo - 8 : 0;
+    const uint64_t mask = (1ull << (lo - nlo)) - 1ull;
+    const uint64_t key = tid < m ? sh.list[cur][tid] : 0ull;
+    const uint32_t dg = static_cast<uint32_t>((key >> nlo) & mask);
+    if (tid == 0) sh.nnext[cur ^ 1] = 0;  // last used two rounds ago
+    if (!gdh_ready) {
+      if (tid < m) atomicAdd(&sh.gdh[dg], 1u);
+      __syncthreads();
+    }
+    gdh_ready = false;
+    if (warp == 0) unit_digit_boundary(sh, sh.gdh, need);
+    __syncthreads();
+    const uint32_t dstar = static_cast<uint32_t>(sh.dstar);
+    if (tid < m) {
+      if (dg > dstar)
+        win(key);
+      else if (dg == dstar)
+        sh.list[cur ^ 1][atomicAdd(&sh.nnext[cur], 1)] = key;
+    }
+    need -= sh.dabove;
+    m = sh.dcount;
+    cur ^= 1;
+    lo = nlo;
+    if (tid < 256) sh.gdh[tid] = 0u;
+    __syncthreads();  // the next list is complete; dstar is read by all
+  }
+  if (warp == 0) {
+    // at most 32 left: the need highest of them are selected
+    const uint64_t key = lane < m ? sh.list[cur][lane] : 0ull;
+    int greater = 0;
+    for (int i = 0; i < m; ++i) greater += __shfl_sync(0xffffffffu, key, i) > key ? 1 : 0;
+    if (lane < m && greater < need) win(key);
+  }
+  __syncthreads();
+
+  // 4: ascending indices after the lower ranks' keys; thread t takes this CTA's words
+  // t*wpt .. t*wpt + wpt - 1
+  int before = 0, all = 0;
+#pragma unroll
+  for (int c = 0; c < kUMaxCluster; ++c) {
+    const int k = c < C ? sh.kept[c] : 0;
+    before += c < rank ? k : 0;
+    all += k;
+  }
+  const int wpt = (nwords + kUThreads - 1) / kUThreads;  // at most kUPasses
+  uint32_t wv[kUPasses];
+  int cnt = 0;
+#pragma unroll
+  for (int q = 0; q < kUPasses; ++q) {
+    wv[q] = q < wpt && tid * wpt + q < nwords ? sh.sel[tid * wpt + q] : 0u;
+    cnt += __popc(wv[q]);
+  }
+  int total;
+  int pos = before + unit_scan(cnt, &total, sh.warp_sum[1]);
+#pragma unroll
+  for (int q = 0; q < kUPasses; ++q) {
+    uint32_t w = wv[q];
+    const int kbase = j0 + 32 * (tid * wpt + q);
+    while (w) {
+      const int b = __ffs(w) - 1;
+      w &= w - 1u;
+      if (pos < p.idx_stride) idx[pos] = kbase + b;
+      ++pos;
+    }
+  }
+  if (rank == 0 && tid == 0) p.count[u] = all;
+  cluster_wait();  // the other CTAs are done reading this one's shared memory
+}
+
 }  // namespace
 
 size_t select_workspace_bytes(int64_t units, int64_t ctx_len) {
   // contexts the shared-memory path handles need no workspace
-  if (ctx_len <= static_cast<int64_t>(kMaxCluster) * kFKeys) return 0;
+  if (ctx_len <= static_cast<int64_t>(kUMaxCluster) * kUPasses * kUPassKeys) return 0;
   return sel_layout(units, ctx_len).total;
 }
 
@@ -1272,7 +1309,17 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
                           int idx_stride, int32_t *count, void *workspace, uint32_t *flags,
                           int sm_count, cudaStream_t stream) {
   if (units == 0) return cudaSuccess;
-  if (n <= static_cast<int64_t>(kUPasses) * kUPassKeys) {
+  if (n <= static_cast<int64_t>(kUMaxCluster) * kUPasses * kUPassKeys) {
+    // about kUChunkTarget keys per CTA, but no more CTAs over all units than SMs (one CTA
+    // per SM, one wave), and never more than kUPasses x 32768 keys in one CTA
+    // (one pass of one CTA is faster than any cluster: its exchanges cost more than they save)
+    int64_t want = n <= kUPassKeys ? 1 : (n + kUChunkTarget - 1) / kUChunkTarget;
+    const int64_t wave = units > 0 ? static_cast<int64_t>(sm_count) / units : 1;
+    if (want > wave) want = wave;
+    const int64_t least = (n + kUPasses * kUPassKeys - 1) / (kUPasses * kUPassKeys);
+    if (want < least) want = least;
+    int cl = 1;
+    while (cl < kUMaxCluster && cl < want) cl <<= 1;
     FastParams f = {};
     f.sel = sel_scores;
     f.hist = sel_hist;
@@ -1280,46 +1327,18 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
     f.ncap = ncap;
     f.topk = topk;
     f.recent = recent;
-    f.cl = 1;
-    f.chunk = n;
-    f.flags = flags;
-    f.idx = idx;
-    f.idx_stride = idx_stride;
-    f.count = count;
-    const int bytes = static_cast<int>(sizeof(UnitShared) + (kUPassKeys + 4) * sizeof(float));
-    cudaError_t e = cudaFuncSetAttribute(select_unit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(select_unit_kernel, dim3(static_cast<unsigned>(units)), dim3(kUThreads),
-                      static_cast<size_t>(bytes), stream, 0u, f);
-  }
-  if (n <= static_cast<int64_t>(kMaxCluster) * kFKeys) {
-    // about kFChunk keys per CTA, but no more CTAs than two per SM over all units (one
-    // wave), and never more than kFKeys keys in one CTA
-    int64_t cl = (n + kFChunk - 1) / kFChunk;
-    const int64_t wave = units > 0 ? (2 * static_cast<int64_t>(sm_count)) / units : 1;
-    if (cl > wave) cl = wave;
-    const int64_t least = (n + kFKeys - 1) / kFKeys;
-    if (cl < least) cl = least;
-    cl = cl < 1 ? 1 : (cl > kMaxCluster ? kMaxCluster : cl);
-    FastParams f;
-    f.sel = sel_scores;
-    f.hist = sel_hist;
-    f.n = n;
-    f.ncap = ncap;
-    f.topk = topk;
-    f.recent = recent;
-    f.cl = static_cast<int>(cl);
+    f.cl = cl;
     f.chunk = ((n + cl - 1) / cl + 31) / 32 * 32;
     f.flags = flags;
     f.idx = idx;
     f.idx_stride = idx_stride;
     f.count = count;
-    const int bytes = static_cast<int>(sizeof(FastShared) + (f.chunk + 4) * sizeof(uint32_t));
-    cudaError_t e = cudaFuncSetAttribute(select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(FastShared) + (kFKeys + 4) * sizeof(uint32_t)));
+    const int bytes = static_cast<int>(sizeof(UnitShared) + (kUPassKeys + 4) * sizeof(float));
+    auto kernel = cl > 1 ? select_cluster_kernel : select_single_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_fast_kernel, dim3(static_cast<unsigned>(units * f.cl)), dim3(kFThreads),
-                      static_cast<size_t>(bytes), stream, static_cast<unsigned>(f.cl), f);
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(units * cl)), dim3(kUThreads),
+                      static_cast<size_t>(bytes), stream, cl > 1 ? static_cast<unsigned>(cl) : 0u, f);
   }
   const SelLayout L = sel_layout(units, n);
   uint8_t *ws = static_cast<uint8_t *>(workspace);

@@ -171,11 +171,13 @@ def _select_case(sig, n, ncap):
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
 
 
-@pytest.mark.parametrize("n,ncap", [(262144, 262144), (300000, 300000), (50001, 50003),
-                                    (4097, 4098), (1153, 1157)])
+@pytest.mark.parametrize("n,ncap", [(524288, 524288), (524289, 524291), (300000, 300000),
+                                    (262144, 262144), (50001, 50003), (4097, 4098),
+                                    (1153, 1157)])
 def test_select_long_and_unaligned_rows(n, ncap):
     # the largest context one cluster holds in shared memory, one past it (the streaming
-    # kernel), and row strides that start every unit's scores at a different 4-byte phase
+    # kernel), two passes per CTA, and row strides that start every unit's scores at a
+    # different 4-byte phase
     rng = np.random.default_rng(n)
     B, Hkv = 2, 4
     sig = rng.standard_normal((B, Hkv, ncap)).astype(np.float32)
