@@ -168,6 +168,8 @@ embla_status embla_full_decode_static_scratch(const embla_shape *shape, const vo
  *              selected key indices in ascending order; entries at and past
  *              count[b, g] are not written
  *   count      int32 [B, Hkv] = min(n, topk + recent)
+ *   workspace  embla_select_topk_workspace_size bytes (0 for contexts up to
+ *              524,288 keys, which shared memory holds), 16-byte aligned
  */
 size_t embla_select_topk_workspace_size(const embla_shape *shape, int32_t topk, int32_t recent);
 embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores,

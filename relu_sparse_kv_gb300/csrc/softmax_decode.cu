@@ -284,15 +284,19 @@ struct DotsF32 {
 //   O^T += V^T . P^T  as MMAs with M = dims (8 tiles of 16), N = heads, K = the 16 rows.
 // P is rounded to bf16 for the second product; l sums the unrounded fp32 values.
 
-constexpr int kSpWarps = 9;                 // 9 x 16 = 144 rows: a cluster of 8 covers 1152
+// 9 warps x 16 rows = 144 rows: a cluster of 8 covers 1152 (two CTAs to an SM); the wide
+// variant, 18 warps and a cluster of 4 (one CTA to an SM), takes over when 8 CTAs per unit
+// would put two on some SMs but 4 fit one each
+constexpr int kSpWarps = 9;
+constexpr int kSpWideWarps = 18;
 constexpr int kSpThreads = kSpWarps * 32;
 constexpr int kSpBlock = 16;                // rows per warp step
 constexpr int kSpStage = 2 * kSpBlock * kRowBytes;  // K and V rows of one step: 8 KB
 
-template <int G>
+template <int G, int W = kSpWarps>
 struct SpMerge {
-  float m[kSpWarps][G], l[kSpWarps][G];
-  float acc[kSpWarps][G][kHeadDim];
+  float m[W][G], l[W][G];
+  float acc[W][G][kHeadDim];
   float cm[G], cl[G];
   float ca[G][kHeadDim];
 };
@@ -306,7 +310,8 @@ struct SparseParams {
   uint32_t *flags;
   int64_t n, ncap;
   int idx_stride, rows_per_cta;
-  int cl;  // CTAs per unit (the cluster size): 1, 2, 4 or 8
+  int cl;    // CTAs per unit (the cluster size): 1, 2, 4 or 8
+  int wide;  // the 18-warp variant (cluster of 4)
   float tau;
   // cache plane of unit u: u itself, or for a selection per query head (one unit per
   // (sequence, query head)) (u / Hq) * Hkv + (u % Hq) / Gq
@@ -324,19 +329,20 @@ __device__ __forceinline__ uint32_t sp_piece(int r, int c) {
 // After every warp has written its running max, sum and unnormalised output into mg:
 // combine the warps, then the cluster's CTAs (through distributed shared memory), and
 // write this CTA's share of the unit's G x 128 outputs.
-template <int G, int CL>
-__device__ __forceinline__ void sp_combine(SpMerge<G> &mg, int rank, int64_t u, float *out_base) {
+template <int G, int CL, int W = kSpWarps>
+__device__ __forceinline__ void sp_combine(SpMerge<G, W> &mg, int rank, int64_t u, float *out_base) {
+  constexpr int kT = W * 32;
   cg::cluster_group cluster = cg::this_cluster();
   __syncthreads();
-  for (int i = threadIdx.x; i < G * kHeadDim; i += kSpThreads) {
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kT) {
     const int h = i / kHeadDim, d = i % kHeadDim;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kSpWarps; ++w) M = fmaxf(M, mg.m[w][h]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mg.m[w][h]);
     float L = 0.0f, A = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kSpWarps; ++w) {
+      for (int w = 0; w < W; ++w) {
         const float f = exp2f(mg.m[w][h] - M);
         L = fmaf(mg.l[w][h], f, L);
         A = fmaf(mg.acc[w][h][d], f, A);
@@ -351,12 +357,12 @@ __device__ __forceinline__ void sp_combine(SpMerge<G> &mg, int rank, int64_t u, 
   // the cluster's CTAs each finish their share of the outputs from all the CTAs' states
   cluster.sync();
   constexpr int per = G * kHeadDim / CL;  // outputs of this CTA (at most 4 per thread)
-  static_assert(per <= 4 * kSpThreads, "at most 4 outputs per thread");
+  static_assert(per <= 4 * kT, "at most 4 outputs per thread");
   float res[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     res[k] = 0.0f;
-    const int li = threadIdx.x + k * kSpThreads;
+    const int li = threadIdx.x + k * kT;
     if (li < per) {
       const int i = rank * per + li;
       const int h = i / kHeadDim, d = i % kHeadDim;
@@ -371,7 +377,7 @@ __device__ __forceinline__ void sp_combine(SpMerge<G> &mg, int rank, int64_t u, 
       if (M != -INFINITY) {
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-          const SpMerge<G> *o2 = cluster.map_shared_rank(&mg, c);
+          const SpMerge<G, W> *o2 = cluster.map_shared_rank(&mg, c);
           const float f = exp2f(cmv[c] - M);
           L = fmaf(o2->cl[h], f, L);
           A = fmaf(o2->ca[h][d], f, A);
@@ -383,19 +389,19 @@ __device__ __forceinline__ void sp_combine(SpMerge<G> &mg, int rank, int64_t u, 
   cluster_arrive();  // done reading the other CTAs' shared memory
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int li = threadIdx.x + k * kSpThreads;
+    const int li = threadIdx.x + k * kT;
     if (li < per) out_base[u * G * kHeadDim + rank * per + li] = res[k];
   }
   cluster_wait();  // and they are done reading this one's
 }
 
-template <int G, int CL>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
+template <int G, int CL, int W = kSpWarps>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(W * 32, W <= kSpWarps ? 2 : 1)
     sparse_decode_kernel(const SparseParams p) {
   pdl_wait_primary();  // the selection and the query are complete
   pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];  // staged rows, then the merge state
-  SpMerge<G> &mg = *reinterpret_cast<SpMerge<G> *>(smem);
+  SpMerge<G, W> &mg = *reinterpret_cast<SpMerge<G, W> *>(smem);
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int64_t u = blockIdx.x / CL;
@@ -428,7 +434,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
 
   const int r0 = rank * p.rows_per_cta;
   const int r1 = min(cnt, r0 + p.rows_per_cta);
-  for (int b0 = r0 + warp * kSpBlock; b0 < r1; b0 += kSpWarps * kSpBlock) {
+  for (int b0 = r0 + warp * kSpBlock; b0 < r1; b0 += W * kSpBlock) {
     // stage: lane r < 16 looks up row r (absent past the count, or for an index outside
     // [0, n), which is flagged); then each copy instruction moves two whole rows, lanes
     // 0-15 the 16 pieces of one and lanes 16-31 those of the next; absent rows are zeros
@@ -528,7 +534,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSpThreads, 2)
       mg.acc[warp][2 * t + 1][16 * i + g + 8] = o[i][3];
     }
   }
-  sp_combine<G, CL>(mg, rank, u, p.out);
+  sp_combine<G, CL, W>(mg, rank, u, p.out);
 }
 
 // 8-bit caches: E4M3 codes (128-byte rows) with one fp32 scale per token.  Per block of 16
@@ -811,18 +817,24 @@ cudaError_t launch_staged(void (*kernel)(Params), dim3 grid, const Params &p, cu
   return launch_pdl(kernel, grid, dim3(kThreads), kStageBytes, stream, 0u, p);
 }
 
-template <bool KV8>
+template <bool KV8, int W = kSpWarps>
 cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const SparseParams &p,
                             cudaStream_t stream) {
-  constexpr int stage = kSpWarps * (KV8 ? kSp8Stage : kSpStage);
-  constexpr int bytes = stage > static_cast<int>(sizeof(SpMerge<8>)) ? stage : static_cast<int>(sizeof(SpMerge<8>));
+  constexpr int stage = W * (KV8 ? kSp8Stage : kSpStage);
+  constexpr int merge = static_cast<int>(sizeof(SpMerge<8, W>));
+  constexpr int bytes = stage > merge ? stage : merge;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, grid, dim3(kSpThreads), bytes, stream, 0u, p);
+  return launch_pdl(kernel, grid, dim3(W * 32), bytes, stream, 0u, p);
 }
 
 template <int G>
 cudaError_t launch_sparse_g(dim3 grid, const SparseParams &p, cudaStream_t stream) {
+  if (p.wide) {
+    // the wide variant (bf16 caches, cluster of 4)
+    if (p.ks != nullptr || p.cl != 4) return cudaErrorInvalidValue;
+    return launch_sparse_t<false, kSpWideWarps>(sparse_decode_kernel<G, 4, kSpWideWarps>, grid, p, stream);
+  }
   if constexpr (G == 1) {
     switch (p.cl) {
       case 8: return launch_sparse_t<false>(sparse_decode_kernel<1, 8>, grid, p, stream);
@@ -878,8 +890,16 @@ cudaError_t launch_sparse_decode(int G, bool per_head, int Hq, const void *q, co
   p.n = n;
   p.ncap = ncap;
   p.idx_stride = idx_stride;
-  // 8 CTAs per unit, fewer when that would take more than one wave (two CTAs per SM)
+  // 8 CTAs per unit, one to an SM if they fit; else 4 wide CTAs (18 warps) per unit if those
+  // fit one to an SM (bf16 caches); else 8 CTAs, two to an SM, or fewer CTAs so that the
+  // launch stays one wave
   int cl = kMaxCluster;
+  p.wide = 0;
+  if (units * kMaxCluster > static_cast<int64_t>(sm_count) && units * 4 <= static_cast<int64_t>(sm_count) &&
+      k_scales == nullptr) {
+    cl = 4;
+    p.wide = 1;
+  }
   while (cl > 1 && units * cl > 2 * static_cast<int64_t>(sm_count)) cl >>= 1;
   p.cl = cl;
   p.rows_per_cta = ((idx_stride + cl - 1) / cl + kSpBlock - 1) / kSpBlock * kSpBlock;

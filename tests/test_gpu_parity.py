@@ -253,10 +253,12 @@ def test_sparse_decode_with_arbitrary_indices_and_counts():
     assert_close(got, ref)
 
 
-@pytest.mark.parametrize("B,Hq,Hkv", [(10, 16, 4), (20, 16, 4), (40, 16, 4), (80, 16, 4),
+@pytest.mark.parametrize("B,Hq,Hkv", [(8, 16, 4), (9, 16, 4), (16, 16, 2), (19, 16, 2),
+                                      (10, 16, 4), (20, 16, 4), (40, 16, 4), (80, 16, 4),
                                       (40, 16, 2), (90, 16, 2)])
 def test_sparse_decode_cluster_sizes(B, Hq, Hkv):
-    # 40 .. 320 units: the launch spreads a unit over 8, 4, 2 or 1 CTAs to stay one wave
+    # 32 .. 320 units: the launch spreads a unit over 8, 4, 2 or 1 CTAs to stay one wave
+    # (32 .. 38 units on 152 SMs: four 18-warp CTAs per unit)
     n, stride = 1400, 1152
     rng = np.random.default_rng(B * 7 + Hkv)
     q = gen.normal_bf16(21, (B, Hq, D))
