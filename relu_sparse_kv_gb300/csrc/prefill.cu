@@ -24,7 +24,10 @@
 //              is applied once at the end: out = a2 O' / (c + a2 den'), O' = sum w' v,
 //              den' = sum w' over keys j <= p.  P = w' is written over the thread's own S
 //              columns as two bf16 matrices hi = rn(w'), lo = rn(w' - hi), both multiplied
-//              into O', so the weights keep about 16 bits.
+//              into O', so the weights keep about 16 bits, in the first key tile; as hi
+//              alone (den' then sums hi) in the tiles after it.
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -35,6 +38,14 @@ namespace {
 #define EMBLA_PREFILL_EPI_WARPS 8
 #endif
 constexpr int kEpiWarps = EMBLA_PREFILL_EPI_WARPS;  // a multiple of 4 (the lane quarters)
+// P goes to the tensor cores as bf16 hi + lo for the first kLoTiles key tiles of a row
+// block and as hi alone after them.  A row that reaches past the first tile has at least 128
+// keys behind it, over which the rounding errors of hi (2^-9 of each weight, either sign)
+// average out; the first tile's rows can have a handful of keys, where they would not.
+#ifndef EMBLA_PREFILL_LO_TILES
+#define EMBLA_PREFILL_LO_TILES 1
+#endif
+constexpr int kLoTiles = EMBLA_PREFILL_LO_TILES;
 constexpr int kEpiParts = kEpiWarps / 4;          // threads per query row
 constexpr int kEpiCols = 128 / kEpiParts;         // keys of a tile per epilogue thread
 static_assert(kEpiWarps % 4 == 0 && (kEpiCols == 32 || kEpiCols == 64), "epilogue split");
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t a_hi = tmem + pb * 128 + grp * kEpiCols + ((16 * kk) % kEpiCols) / 2;
             const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + pb * kTileB + kk * 2048), kBox);
             tc_mma_bf16_tmem_a(tmem + kColO, a_hi, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
-            tc_mma_bf16_tmem_a(tmem + kColO, a_hi + kEpiCols / 2, vd, kIdescPV, 1u);
+            if (t < kLoTiles) tc_mma_bf16_tmem_a(tmem + kColO, a_hi + kEpiCols / 2, vd, kIdescPV, 1u);
           }
           tc_commit(&pvdone[pb]);
           tc_commit(&vempty[pb]);
@@ -281,31 +292,46 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // position need the test)
       const int64_t j0 = static_cast<int64_t>(kt) * 128 + cg * kEpiCols;
       const bool masked = j0 + kEpiCols - 1 > p0;
-      uint32_t hi[kEpiCols / 2], lo[kEpiCols / 2];
+      // P over this thread's own S columns (already read): kEpiCols / 2 columns of hi, then
+      // (in the first kLoTiles tiles) as many of lo.  One code path per case keeps the
+      // registers of each to what it needs.
+      auto write_p = [&](auto with_lo) {
+        constexpr bool kLo = decltype(with_lo)::value;
+        uint32_t hi[kEpiCols / 2], lo[kLo ? kEpiCols / 2 : 1];
 #pragma unroll
-      for (int k = 0; k < kEpiCols; k += 2) {
-        float w2[2];
+        for (int k = 0; k < kEpiCols; k += 2) {
+          float w2[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float d = fmaxf(__uint_as_float(acc[k + e]), 0.0f);
-          float w = d * d * rk[k + e];
-          if (masked && j0 + k + e > pos) w = 0.0f;
-          den4[(k + e) & 3] += w;
-          w2[e] = w;
+          for (int e = 0; e < 2; ++e) {
+            const float d = fmaxf(__uint_as_float(acc[k + e]), 0.0f);
+            float w = d * d * rk[k + e];
+            if (masked && j0 + k + e > pos) w = 0.0f;
+            w2[e] = w;
+          }
+          const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
+          hi[k >> 1] = hb;
+          if constexpr (kLo) {
+            lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
+            den4[k & 3] += w2[0];
+            den4[(k + 1) & 3] += w2[1];
+          } else {
+            // the denominator sums the weights the numerator multiplies
+            den4[k & 3] += bf16lo(hb);
+            den4[(k + 1) & 3] += bf16hi(hb);
+          }
         }
-        const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
-        hi[k >> 1] = hb;
-        lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
-      }
-      // over this thread's own S columns (already read): kEpiCols / 2 columns of hi, then
-      // as many of lo
-      if constexpr (kEpiCols == 64) {
-        tmem_store_x32(cols, *reinterpret_cast<const uint32_t(*)[32]>(hi));
-        tmem_store_x32(cols + 32, *reinterpret_cast<const uint32_t(*)[32]>(lo));
-      } else {
-        tmem_store_x16(cols, *reinterpret_cast<const uint32_t(*)[16]>(hi));
-        tmem_store_x16(cols + 16, *reinterpret_cast<const uint32_t(*)[16]>(lo));
-      }
+        if constexpr (kEpiCols == 64) {
+          tmem_store_x32(cols, *reinterpret_cast<const uint32_t(*)[32]>(hi));
+          if constexpr (kLo) tmem_store_x32(cols + 32, *reinterpret_cast<const uint32_t(*)[32]>(lo));
+        } else {
+          tmem_store_x16(cols, *reinterpret_cast<const uint32_t(*)[16]>(hi));
+          if constexpr (kLo) tmem_store_x16(cols + 16, *reinterpret_cast<const uint32_t(*)[16]>(lo));
+        }
+      };
+      if (kt < kLoTiles)
+        write_p(std::true_type{});
+      else
+        write_p(std::false_type{});
       tmem_wait_st();
       tc_fence_before_sync();  // P is read by the tensor cores
       __syncwarp();
