@@ -831,9 +831,13 @@ cudaError_t launch_sparse_t(void (*kernel)(SparseParams), dim3 grid, const Spars
 template <int G>
 cudaError_t launch_sparse_g(dim3 grid, const SparseParams &p, cudaStream_t stream) {
   if (p.wide) {
-    // the wide variant (bf16 caches, cluster of 4)
-    if (p.ks != nullptr || p.cl != 4) return cudaErrorInvalidValue;
-    return launch_sparse_t<false, kSpWideWarps>(sparse_decode_kernel<G, 4, kSpWideWarps>, grid, p, stream);
+    // the wide variant (bf16 caches, clusters of up to 4)
+    if (p.ks != nullptr) return cudaErrorInvalidValue;
+    if (p.cl == 4)
+      return launch_sparse_t<false, kSpWideWarps>(sparse_decode_kernel<G, 4, kSpWideWarps>, grid, p, stream);
+    if (p.cl == 2)
+      return launch_sparse_t<false, kSpWideWarps>(sparse_decode_kernel<G, 2, kSpWideWarps>, grid, p, stream);
+    return cudaErrorInvalidValue;
   }
   if constexpr (G == 1) {
     switch (p.cl) {
@@ -890,17 +894,22 @@ cudaError_t launch_sparse_decode(int G, bool per_head, int Hq, const void *q, co
   p.n = n;
   p.ncap = ncap;
   p.idx_stride = idx_stride;
-  // 8 CTAs per unit, one to an SM if they fit; else 4 wide CTAs (18 warps) per unit if those
-  // fit one to an SM (bf16 caches); else 8 CTAs, two to an SM, or fewer CTAs so that the
-  // launch stays one wave
+  // 8 CTAs per unit, one to an SM if they fit; else wide CTAs (18 warps), 4 or 2 per unit,
+  // if they fit one to an SM (bf16 caches); else 8 CTAs, two to an SM, or fewer CTAs so that
+  // the launch stays one wave.  (One wide CTA per unit measured no faster than two narrow
+  // ones sharing an SM.)
   int cl = kMaxCluster;
   p.wide = 0;
-  if (units * kMaxCluster > static_cast<int64_t>(sm_count) && units * 4 <= static_cast<int64_t>(sm_count) &&
-      k_scales == nullptr) {
-    cl = 4;
-    p.wide = 1;
+  if (units * kMaxCluster > static_cast<int64_t>(sm_count) && k_scales == nullptr) {
+    int w = 4;
+    while (w > 2 && units * w > static_cast<int64_t>(sm_count)) w >>= 1;
+    if (units * w <= static_cast<int64_t>(sm_count)) {
+      cl = w;
+      p.wide = 1;
+    }
   }
-  while (cl > 1 && units * cl > 2 * static_cast<int64_t>(sm_count)) cl >>= 1;
+  if (!p.wide)
+    while (cl > 1 && units * cl > 2 * static_cast<int64_t>(sm_count)) cl >>= 1;
   p.cl = cl;
   p.rows_per_cta = ((idx_stride + cl - 1) / cl + kSpBlock - 1) / kSpBlock * kSpBlock;
   p.tau = tau;

@@ -258,7 +258,7 @@ def test_sparse_decode_with_arbitrary_indices_and_counts():
                                       (40, 16, 2), (90, 16, 2)])
 def test_sparse_decode_cluster_sizes(B, Hq, Hkv):
     # 32 .. 320 units: the launch spreads a unit over 8, 4, 2 or 1 CTAs to stay one wave
-    # (32 .. 38 units on 152 SMs: four 18-warp CTAs per unit)
+    # (on 152 SMs: 32 .. 38 units take four 18-warp CTAs per unit, 40 .. 76 two)
     n, stride = 1400, 1152
     rng = np.random.default_rng(B * 7 + Hkv)
     q = gen.normal_bf16(21, (B, Hq, D))
