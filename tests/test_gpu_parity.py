@@ -186,6 +186,33 @@ def test_select_long_and_unaligned_rows(n, ncap):
     _select_case(sig, n, ncap)
 
 
+@pytest.mark.parametrize("topk,recent", [(0, 128), (1024, 0), (1, 1), (300, 2000), (5000, 50)])
+@pytest.mark.parametrize("n", [20000, 100000])
+def test_select_other_topk_and_recent(topk, recent, n):
+    # sizes other than 1024 + 128: no top-k, no recent keys, more recent keys than threads,
+    # more candidates than one list holds; one CTA per unit (20000) and clusters (100000)
+    rng = np.random.default_rng(topk + 7 * recent + n)
+    B, Hkv = 2, 4
+    sig = rng.standard_normal((B, Hkv, n)).astype(np.float32)
+    sig[1, 2] = np.round(sig[1, 2] * 2) / 2  # many exact ties
+    shape = E.Shape(B, 16, Hkv, D, n, n)
+    hist = np.stack([[np.bincount(order_key_np(sig[b, g]) >> 21, minlength=E.HIST_BINS)
+                      for g in range(Hkv)] for b in range(B)]).astype(np.int32)
+    stride = max(topk + recent, 1)
+    idx = torch.full((B, Hkv, stride), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(B, Hkv, dtype=torch.int32, device="cuda")
+    E.embla_select_topk(shape, torch.from_numpy(sig).cuda(), torch.from_numpy(hist).cuda(), idx, cnt,
+                        topk, recent)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            ref = oracle.select_topk(sig[b, g], topk, recent)
+            assert cnt[b, g] == len(ref)
+            assert np.array_equal(idx[b, g, :cnt[b, g]], ref)
+
+
 @pytest.mark.parametrize("chunk", [1, 2, 8, 32, 64, 1024])
 @pytest.mark.parametrize("n,ncap", [(5000, 5000), (4099, 4103), (33, 40), (1, 1)])
 def test_skip_stats(chunk, n, ncap):
