@@ -67,6 +67,27 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) M
 constexpr int kColO = kRing * 128, kPTmemCols = 512;
 static_assert(kColO + 128 <= kPTmemCols, "tensor memory");
 
+// Two fp32 lanes at once (Blackwell's paired fp32 pipe): a *= b, a += b, each lane rounded
+// as the scalar operation would be.
+__device__ __forceinline__ void mul_f32x2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %3};\n\t"
+      "mul.rn.f32x2 x, x, y;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add_f32x2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 x, x, y;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 struct PrefillParams {
   float *out;      // [B, Hq, T, D]
   uint32_t *flags;
@@ -300,24 +321,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         uint32_t hi[kEpiCols / 2], lo[kLo ? kEpiCols / 2 : 1];
 #pragma unroll
         for (int k = 0; k < kEpiCols; k += 2) {
-          float w2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float d = fmaxf(__uint_as_float(acc[k + e]), 0.0f);
-            float w = d * d * rk[k + e];
-            if (masked && j0 + k + e > pos) w = 0.0f;
-            w2[e] = w;
+          // w = max(dot, 0)^2 * rk for keys k and k + 1, two lanes per instruction
+          float w2[2] = {fmaxf(__uint_as_float(acc[k]), 0.0f), fmaxf(__uint_as_float(acc[k + 1]), 0.0f)};
+          mul_f32x2(w2[0], w2[1], w2[0], w2[1]);
+          mul_f32x2(w2[0], w2[1], rk[k], rk[k + 1]);
+          if (masked) {
+            if (j0 + k > pos) w2[0] = 0.0f;
+            if (j0 + k + 1 > pos) w2[1] = 0.0f;
           }
           const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
           hi[k >> 1] = hb;
           if constexpr (kLo) {
             lo[k >> 1] = pack_bf16x2(w2[0] - bf16lo(hb), w2[1] - bf16hi(hb));
-            den4[k & 3] += w2[0];
-            den4[(k + 1) & 3] += w2[1];
+            add_f32x2(den4[k & 3], den4[(k + 1) & 3], w2[0], w2[1]);
           } else {
             // the denominator sums the weights the numerator multiplies
-            den4[k & 3] += bf16lo(hb);
-            den4[(k + 1) & 3] += bf16hi(hb);
+            add_f32x2(den4[k & 3], den4[(k + 1) & 3], bf16lo(hb), bf16hi(hb));
           }
         }
         if constexpr (kEpiCols == 64) {
