@@ -697,6 +697,48 @@ __device__ __forceinline__ void unit_classify(const float *sf, float f_take, flo
   cm = c;
 }
 
+// The same masks read four scores per load when the scores start 16-byte aligned in shared
+// memory: the thread's KP / 4 chunks in an order rotated by w (a quarter-warp's loads hit
+// 32 different banks), each chunk's four compares making a nibble at its place.
+template <int KP>
+__device__ __forceinline__ void unit_classify4(const float *sf, float f_take, float f_lo,
+                                               uint32_t &tm, uint32_t &cm) {
+  constexpr int S = 32 / KP, NC = KP / 4;
+  const int w = threadIdx.x / S, part = threadIdx.x % S;
+  const float4 *mine = reinterpret_cast<const float4 *>(sf + 32 * w + KP * part);
+  uint32_t a = 0u, c = 0u;
+#pragma unroll
+  for (int k = 0; k < NC; ++k) {
+    const int ch = (k + w) & (NC - 1);
+    const float4 v = mine[ch];
+    const uint32_t na = (v.x >= f_take ? 1u : 0u) | (v.y >= f_take ? 2u : 0u) |
+                        (v.z >= f_take ? 4u : 0u) | (v.w >= f_take ? 8u : 0u);
+    const uint32_t nc = (v.x >= f_lo ? 1u : 0u) | (v.y >= f_lo ? 2u : 0u) |
+                        (v.z >= f_lo ? 4u : 0u) | (v.w >= f_lo ? 8u : 0u);
+    a |= na << (4 * ch);
+    c |= nc << (4 * ch);
+  }
+  a <<= KP * part;
+  c <<= KP * part;
+#pragma unroll
+  for (int o = 1; o < S; o <<= 1) {
+    a |= __shfl_xor_sync(0xffffffffu, a, o);
+    c |= __shfl_xor_sync(0xffffffffu, c, o);
+  }
+  tm = a;
+  cm = c;
+}
+
+// Either form, for KP keys per thread.
+template <int KP>
+__device__ __forceinline__ void unit_classify_any(const float *sf, float f_take, float f_lo,
+                                                  uint32_t &tm, uint32_t &cm) {
+  if ((reinterpret_cast<uintptr_t>(sf) & 15u) == 0u)
+    unit_classify4<KP>(sf, f_take, f_lo, tm, cm);
+  else
+    unit_classify<KP>(sf, f_take, f_lo, tm, cm);
+}
+
 // One CTA per unit (contexts up to kUPasses x 32768 keys when a cluster would not fit in
 // one wave, and every context of one pass): the steps of the cluster path with every
 // exchange a block barrier, the candidates listed and counted by digit straight into the
@@ -781,18 +823,10 @@ __global__ void __launch_bounds__(kUThreads, 1) select_single_kernel(const FastP
       landed = false;
       if (tid == 0) atomicOr(p.flags, kFlagWaitTimeout);
     }
-    // step k reads key 32 tid + ((k + tid) mod 32), so bit k of the step masks belongs to key
-    // bit (k + tid) mod 32: a rotation puts them in place
     const float *mine = sf + 32 * tid;
-    uint32_t tm = 0u, cm = 0u;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const float s = mine[(k + tid) & 31];
-      tm |= (s >= f_take ? 1u : 0u) << k;
-      cm |= (s >= f_lo ? 1u : 0u) << k;
-    }
-    tm = __funnelshift_l(tm, tm, tid & 31);
-    cm = __funnelshift_l(cm, cm, tid & 31) & ~tm;
+    uint32_t tm, cm;
+    unit_classify_any<32>(sf, f_take, f_lo, tm, cm);
+    cm &= ~tm;
     const int k0 = pass * kUPassKeys + 32 * tid;  // this thread's first key
     if (k0 + 32 > first_recent || !landed) {
       const uint32_t valid = landed ? bit_range(0, n - k0) : 0u;
@@ -1050,11 +1084,11 @@ __global__ void __launch_bounds__(kUThreads, 1) select_cluster_kernel(const Fast
     }
     uint32_t tm, cm;
     if (kp == 8)
-      unit_classify<8>(sf, f_take, f_lo, tm, cm);
+      unit_classify_any<8>(sf, f_take, f_lo, tm, cm);
     else if (kp == 16)
-      unit_classify<16>(sf, f_take, f_lo, tm, cm);
+      unit_classify_any<16>(sf, f_take, f_lo, tm, cm);
     else
-      unit_classify<32>(sf, f_take, f_lo, tm, cm);
+      unit_classify_any<32>(sf, f_take, f_lo, tm, cm);
     cm &= ~tm;
     const int wp = tid / spt;                           // the word within the pass
     const int wk = pass * (kUPassKeys / 32) + wp;       // and within this CTA
