@@ -109,7 +109,8 @@ def signed_keys(strm: int, q_group: np.ndarray, t: np.ndarray, n_cand: int, topk
 
     margin: every head satisfies t*D*cos(q_h, k) >= margin after bf16 rounding.
     gap:    when n_cand > topk, the topk-th and (topk+1)-th largest values of
-            max_h D*cos(q_h, k_j) over j < n_cand differ by at least gap.
+            max_h D*cos(q_h, k_j) over j < n_cand differ by at least gap, and so do
+            those of every head's own D*cos(q_h, k_j).
     """
     q_group = np.ascontiguousarray(q_group, dtype=np.uint16)
     G, D = q_group.shape
@@ -264,7 +265,7 @@ def iid_unit(seed: int, G: int, D: int, n: int, unit: int = 0):
     return q, K, V
 
 
-# The five workloads (batch, context, heads, structure); see the design doc for the recipe.
+# The workloads: batch, context, heads and the survivor structure each one is built with.
 EMBLA_FULL_LAYERS = (7, 16, 20, 24, 28)
 EMBLA_SPARSE_OF = {7: (), 16: (17, 18, 19), 20: (21, 22, 23), 24: (25, 26, 27), 28: (29, 30, 31)}
 EMBLA_WINDOW_LAYERS = tuple(l for l in range(16) if l != 7)

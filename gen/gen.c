@@ -22,8 +22,10 @@
  * moved inside span(Q) to k = z + Q^T (Q Q^T)^-1 (t|c| - c), so every head of
  * the group scores it with sign t and the natural Gaussian magnitude.  After
  * rounding to bf16 each key is checked against a margin on D*cos(q_h, k) and
- * redrawn if it misses; the candidate at the top-k boundary is redrawn until
- * the boundary gap on max_h D*cos(q_h, k) is at least the requested gap.
+ * redrawn if it misses; a candidate at a top-k boundary is redrawn until the
+ * boundary gap is at least the requested gap both on max_h D*cos(q_h, k) (the
+ * group's score) and on every head's own D*cos(q_h, k), so that a selection by
+ * either score has a unique answer.
  *
  * Build: gcc -O2 -fPIC -shared -fopenmp -ffp-contract=off gen.c -lm
  */
@@ -257,8 +259,9 @@ static void store_key(const signer *s, int64_t j, const double *v) {
   }
 }
 
-/* max_h D*cos(q_h, k) over the group, in double, from key j as stored. */
-static double proxy_max(const signer *s, int64_t j) {
+/* D*cos(q_h, k) of every head of the group (vals[0..G)) and their maximum (vals[G]),
+ * in double, from key j as stored. */
+static void proxy_values(const signer *s, int64_t j, double *vals) {
   double kk = 0.0;
   double kd[MAXD];
   key_values(s, j, kd);
@@ -268,9 +271,10 @@ static double proxy_max(const signer *s, int64_t j) {
     double dot = 0.0;
     for (int d = 0; d < s->D; ++d) dot += s->q[h * s->D + d] * kd[d];
     double v = (kn > 0.0 && s->qnorm[h] > 0.0) ? (double)s->D * dot / (s->qnorm[h] * kn) : 0.0;
+    vals[h] = v;
     if (v > best) best = v;
   }
-  return best;
+  vals[s->G] = best;
 }
 
 /* Draw key j (attempt a) with target sign t; returns 1 when it meets the margin. */
@@ -343,7 +347,8 @@ static void select_desc(double *v, int64_t *id, int64_t n, int64_t k) {
  *   t      : n target signs
  *   n_cand : keys [0, n_cand) compete for the top-`topk` selection; when
  *            n_cand > topk the gap between the topk-th and (topk+1)-th
- *            largest max_h D*cos(q_h, k) is made >= gap
+ *            largest max_h D*cos(q_h, k), and the same gap for every head's
+ *            own D*cos(q_h, k), is made >= gap
  *   K      : n x D bf16 bits out (row stride D)
  * Returns the number of redraws (>= 0), or a negative error code:
  *   -1 bad arguments, -2 singular query group, -3 margin not met after
@@ -387,29 +392,47 @@ static int64_t signed_keys(uint64_t stream, int G, int D, int64_t n, const uint1
   if (failed) { free(attempt); free(s); return -3; }
 
   if (n_cand > topk && topk > 0) {
-    double *v = (double *)malloc(sizeof(double) * (size_t)n_cand);
+    /* The top-k boundary must be clear both for the group's score (the maximum over its
+     * heads) and for every head's own score: column a of v holds, for a < G, head a's
+     * D*cos and, for a = G, their maximum.  A pass checks every column; a key at a
+     * boundary that is too narrow is redrawn and the pass starts again. */
+    const int A = G + 1;
+    double *v = (double *)malloc(sizeof(double) * (size_t)n_cand * (size_t)A);
     double *w = (double *)malloc(sizeof(double) * (size_t)n_cand);
     int64_t *id = (int64_t *)malloc(sizeof(int64_t) * (size_t)n_cand);
 #pragma omp parallel for schedule(static)
-    for (int64_t j = 0; j < n_cand; ++j) v[j] = proxy_max(s, j);
+    for (int64_t j = 0; j < n_cand; ++j) {
+      double vals[MAXG + 1];
+      proxy_values(s, j, vals);
+      for (int a = 0; a < A; ++a) v[(size_t)a * n_cand + j] = vals[a];
+    }
     int64_t iters = 0;
-    for (;;) {
-      for (int64_t j = 0; j < n_cand; ++j) { w[j] = v[j]; id[j] = j; }
+    int a = 0, clean = 0;
+    while (clean < A) {
+      const double *va = v + (size_t)a * n_cand;
+      for (int64_t j = 0; j < n_cand; ++j) { w[j] = va[j]; id[j] = j; }
       select_desc(w, id, n_cand, topk);
       /* w[topk] is the (topk+1)-th largest; the topk-th is the min of w[0..topk) */
       double lo_in = INFINITY;
       for (int64_t i = 0; i < topk; ++i) if (w[i] < lo_in) lo_in = w[i];
-      if (lo_in - w[topk] >= gap) break;
+      if (lo_in - w[topk] >= gap) {
+        ++clean;
+        a = (a + 1) % A;
+        continue;
+      }
       if (++iters > max_gap_iters) { failed = 1; break; }
       int64_t j = id[topk];
-      int64_t a = attempt[j];
+      int64_t at = attempt[j];
       do {
-        if (++a >= attempt[j] + max_attempts) { failed = 1; break; }
-      } while (!draw_key(s, j, a, t[j] > 0 ? 1 : -1));
+        if (++at >= attempt[j] + max_attempts) { failed = 1; break; }
+      } while (!draw_key(s, j, at, t[j] > 0 ? 1 : -1));
       if (failed) break;
-      redraws += a - attempt[j];
-      attempt[j] = a;
-      v[j] = proxy_max(s, j);
+      redraws += at - attempt[j];
+      attempt[j] = at;
+      double vals[MAXG + 1];
+      proxy_values(s, j, vals);
+      for (int b = 0; b < A; ++b) v[(size_t)b * n_cand + j] = vals[b];
+      clean = 0;
     }
     free(v); free(w); free(id);
     if (failed) { free(attempt); free(s); return -4; }

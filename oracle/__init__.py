@@ -60,13 +60,21 @@ def _load():
             "oracle_relu2_mlp": [i64, i64, vp, vp, vp, vp, vp, vp],
             "oracle_prefill_batch": [i, i, i, i, i64, i64, i64, vp, vp, vp, d, d, d, vp],
             "oracle_skip_stats_batch": [i, i, i64, i64, vp, i64, vp, vp],
+            "oracle_head_scores_batch": [i, i, i, i, i64, i64, vp, vp, d, d, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = args
+        lib.oracle_set_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads the batched functions use from now on; returns the previous count."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def f64(a) -> np.ndarray:
@@ -159,6 +167,17 @@ def full_decode_batch(q, K, V, n, alpha=1.0, c=1.0, eps=1e-6, want_sigma=True):
     _ok(_load().oracle_full_decode_batch(B, Hq, Hkv, D, n, ncap, _p(q), _p(K), _p(V), alpha, c,
                                          eps, _p(out), _p(sigma), _p(ns)), "full_decode_batch")
     return out, sigma, ns
+
+
+def head_scores_batch(q, K, n, alpha=1.0, eps=1e-6):
+    """Every query head's own scores s_hj rounded to fp32: [B, Hq, ncap] (NaN at j >= n)."""
+    q, K = f64(q), f64(K)
+    B, Hq, D = q.shape
+    Hkv, ncap = K.shape[1], K.shape[2]
+    s = np.full((B, Hq, ncap), np.nan, dtype=np.float32)
+    _ok(_load().oracle_head_scores_batch(B, Hq, Hkv, D, n, ncap, _p(q), _p(K), alpha, eps, _p(s)),
+        "head_scores_batch")
+    return s
 
 
 def select_topk_batch(sigma32, n, topk=1024, recent=128):

@@ -34,6 +34,22 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the batched functions below spread their units over (n >= 1); returns the
+ * number they used before.  Only timing code changes it: results do not depend on it. */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+  int before = omp_get_max_threads();
+  if (n >= 1) omp_set_num_threads(n);
+  return before;
+#else
+  (void)n;
+  return 1;
+#endif
+}
 
 /* 1 / sqrt(mean(x^2) + eps) */
 static double rms_inverse(const double *x, int D, double eps) {
@@ -253,6 +269,38 @@ int oracle_full_decode_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t n
     double *ou = out + ((size_t)b * Hq + (size_t)g * G) * D;
     float *su = sigma32 ? sigma32 + (size_t)u * ncap : NULL;
     err |= oracle_full_decode(G, D, n, qu, Ku, D, Vu, D, alpha, c, eps, ou, su, n_surv + u, NULL) != 0;
+  }
+  return err ? -1 : 0;
+}
+
+/*
+ * Every query head's own full-layer scores, rounded to fp32: s32[b][h][j] = (float)
+ * s_hj for j < n (rows j >= n of each head are not written).  These are the scores the
+ * per-query-head reading of the selection ranks ("The Architecture of Embla 1", section
+ * "Three kinds of attention", Sparse: the keys that layer scored highest, here each head's
+ * own), rounded to the precision the CUDA kernels rank in.
+ */
+int oracle_head_scores_batch(int B, int Hq, int Hkv, int D, int64_t n, int64_t ncap,
+                             const double *q, const double *K, double alpha, double eps,
+                             float *s32) {
+  if (B < 0 || Hkv < 1 || Hq % Hkv || ncap < n || n < 0) return -1;
+  int G = Hq / Hkv;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+    int64_t b = u / Hkv, g = u % Hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)G * (size_t)(n > 0 ? n : 1));
+    if (!s) { err |= 1; continue; }
+    const double *qu = q + ((size_t)b * Hq + (size_t)g * G) * D;
+    if (oracle_full_scores(G, D, n, qu, K + (size_t)u * ncap * D, D, alpha, eps, s) != 0) {
+      err |= 1;
+    } else {
+      for (int h = 0; h < G; ++h) {
+        float *o = s32 + ((size_t)b * Hq + (size_t)g * G + h) * ncap;
+        for (int64_t j = 0; j < n; ++j) o[j] = (float)s[(int64_t)h * n + j];
+      }
+    }
+    free(s);
   }
   return err ? -1 : 0;
 }

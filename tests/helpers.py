@@ -6,6 +6,10 @@ import relu_sparse_kv_gb300 as E
 
 ATOL, RTOL = 2e-3, 1e-2
 
+# Worst share of the tolerance used per comparison kind: max |gpu - ref| / (atol + rtol |ref|)
+# (1.0 is the limit).  Filled by assert_close, printed at the end of the run.
+MARGINS = {}
+
 
 def to_dev(a, dev="cuda"):
     """bf16 bit patterns (uint16 numpy) -> torch bf16 on the device."""
@@ -17,7 +21,12 @@ def assert_close(gpu, ref, atol=ATOL, rtol=RTOL, what="output"):
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
     err = np.abs(gpu - ref)
-    bad = ~(err <= atol + rtol * np.abs(ref))
+    lim = atol + rtol * np.abs(ref)
+    if err.size:
+        use = float(np.nanmax(np.where(np.isnan(err), np.inf, err / lim)))
+        key = what.split(" unit")[0].split(" of head")[0].split(" row")[0]
+        MARGINS[key] = max(MARGINS.get(key, 0.0), use)
+    bad = ~(err <= lim)
     assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} out of tolerance; "
                            f"max abs err {np.nanmax(err):.3e}")
 

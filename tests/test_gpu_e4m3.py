@@ -81,7 +81,7 @@ def _check(fl, run, alpha=1.0, c=1.0, eps=1e-6):
     ns = run.n_surv.cpu().numpy()
     assert np.array_equal(ns, ref_ns), (ns, ref_ns)
     assert np.array_equal(ns, fl.n_pos)
-    assert_close(run.out.cpu().numpy(), ref_out)
+    assert_close(run.out.cpu().numpy(), ref_out, what="8-bit full output, small")
     if run.sel is None:
         return ref_sig
     sel = run.sel.cpu().numpy()[:, :, :fl.n]
@@ -177,7 +177,7 @@ def test_e4m3_long_tile_streams_are_repeatable():
         Vd = oracle.dequant_e4m3(fl.V[b:b + 1, g:g + 1], fl.Vs[b:b + 1, g:g + 1])
         ref_out, ref_sig, _ = oracle.full_decode_batch(fl.q[b:b + 1, 8 * g:8 * g + 8], Kd, Vd,
                                                        fl.n)
-        assert_close(run.out[b, 8 * g:8 * g + 8].cpu().numpy(), ref_out[0])
+        assert_close(run.out[b, 8 * g:8 * g + 8].cpu().numpy(), ref_out[0], what="8-bit full output, long tile streams")
         assert_close(run.sel[b, g, :fl.n].cpu().numpy(), ref_sig[0, 0, :fl.n], atol=1e-4, rtol=1e-5,
                      what="sigma")
 
@@ -195,15 +195,15 @@ def test_e4m3_rejects_bad_arguments():
 
 def test_e4m3_full_size_workload():
     """The GQA-8 8-bit workload at full size (8 sequences, 32768 keys, 16 query and 2 KV
-    heads): every unit's survivor count, signs and histogram; the selection of every unit
-    against the properties of a top-k; sampled units against the oracle one by one."""
+    heads): every unit's survivor count, signs and histogram, and every unit's outputs,
+    scores, selection (ranked on the oracle's own scores) and sparse outputs against the
+    oracle on the decoded rows."""
     fl = next(gen.config_full_layers(6, seed=0))
     run = Run8(fl)
     B, Hkv, n = fl.q.shape[0], fl.K.shape[1], fl.n
     assert np.array_equal(run.n_surv.cpu().numpy(), fl.n_pos)
     sel = run.sel.cpu().numpy()[:, :, :n]
     assert np.array_equal(sel > 0, fl.targets > 0)
-    assert np.isfinite(run.out.cpu().numpy()).all()
     hist = run.hist.cpu().numpy().view(np.uint32)
     for b in range(B):
         for g in range(Hkv):
@@ -211,34 +211,19 @@ def test_e4m3_full_size_workload():
                                                           minlength=E.HIST_BINS))
     topk, recent = 1024, 128
     idx, cnt = run.select(topk, recent)
-    assert (cnt == topk + recent).all()
-    for b in range(B):
-        for g in range(Hkv):
-            ix = idx[b, g]
-            assert (np.diff(ix) > 0).all() and ix[0] >= 0 and ix[-1] < n
-            assert np.array_equal(ix[-recent:], np.arange(n - recent, n))
-            cand = sel[b, g, :n - recent]
-            chosen = np.zeros(n - recent, dtype=bool)
-            chosen[ix[:-recent]] = True
-            assert cand[chosen].min() > cand[~chosen].max()
     sparse = [run.sparse(qs) for qs in fl.sparse_q]
-    for so in sparse:
-        assert np.isfinite(so).all()
-    out = run.out.cpu().numpy()
-    G = fl.q.shape[1] // Hkv
-    for b, g in sorted({(0, 0), (B - 1, Hkv - 1), (B // 2, 1), (3, 0)}):
-        hs = slice(g * G, (g + 1) * G)
-        Kd = oracle.dequant_e4m3(fl.K[b, g, :n], fl.Ks[b, g, :n])
-        Vd = oracle.dequant_e4m3(fl.V[b, g, :n], fl.Vs[b, g, :n])
-        o, sig, ns, _ = oracle.full_decode(fl.q[b, hs], Kd, Vd, alpha=1.0, c=1.0, eps=1e-6)
-        assert run.n_surv.cpu().numpy()[b, g] == ns
-        assert_close(out[b, hs], o, what=f"full output unit ({b},{g})")
-        assert_close(sel[b, g], sig, atol=1e-4, rtol=1e-5, what=f"sigma ({b},{g})")
-        ref_idx = oracle.select_topk(sig, topk, recent)
-        assert np.array_equal(idx[b, g], ref_idx)
-        for qs, so in zip(fl.sparse_q, sparse):
-            assert_close(so[b, hs], oracle.sparse_decode(qs[b, hs], Kd, Vd, ref_idx),
-                         what=f"sparse output unit ({b},{g})")
+    Kd = oracle.dequant_e4m3(fl.K[:, :, :n], fl.Ks[:, :, :n])
+    Vd = oracle.dequant_e4m3(fl.V[:, :, :n], fl.Vs[:, :, :n])
+    o, sig, ns = oracle.full_decode_batch(fl.q, Kd, Vd, n, alpha=1.0, c=1.0, eps=1e-6)
+    assert np.array_equal(run.n_surv.cpu().numpy(), ns)
+    assert_close(run.out.cpu().numpy(), o, what="8-bit full output")
+    assert_close(sel, sig, atol=1e-4, rtol=1e-5, what="8-bit sigma")
+    ref_idx, ref_cnt = oracle.select_topk_batch(sig, n, topk, recent)
+    assert np.array_equal(cnt, ref_cnt) and (cnt == topk + recent).all()
+    assert np.array_equal(idx, ref_idx)
+    for qs, so in zip(fl.sparse_q, sparse):
+        assert_close(so, oracle.sparse_decode_batch(qs, Kd, Vd, ref_idx, ref_cnt),
+                     what="8-bit sparse output")
 
 
 @pytest.mark.parametrize("cnt_fill", ["short", "zero", "bad_index"])

@@ -28,7 +28,7 @@ def _check_full(fl, run, alpha=1.0, c=1.0, eps=1e-6):
     ns = run.n_surv.cpu().numpy()
     assert np.array_equal(ns, ref_ns), (ns, ref_ns)
     assert np.array_equal(ns, fl.n_pos)
-    assert_close(run.out.cpu().numpy(), ref_out)
+    assert_close(run.out.cpu().numpy(), ref_out, what="full output, small")
     sel = run.sel.cpu().numpy()[:, :, :fl.n]
     assert_close(sel, ref_sig[:, :, :fl.n], atol=1e-4 * max(alpha, 1e-3), rtol=1e-5, what="sigma")
     assert np.array_equal(sel > 0, ref_sig[:, :, :fl.n] > 0)
@@ -54,7 +54,7 @@ def test_full_and_select_small_contexts(n):
         for g in range(4):
             assert np.array_equal(idx[b, g, :cnt[b, g]], ref_idx[b, g, :ref_cnt[b, g]])
     ref_sp = oracle.sparse_decode_batch(fl.sparse_q[0], fl.K, fl.V, ref_idx, ref_cnt)
-    assert_close(run.sparse(fl.sparse_q[0]), ref_sp)
+    assert_close(run.sparse(fl.sparse_q[0]), ref_sp, what="sparse output, small contexts")
 
 
 @pytest.mark.parametrize("G", [4, 8])
@@ -130,7 +130,8 @@ def test_spill_below_zero_and_dense_selection():
     assert np.array_equal(run.count.cpu().numpy(), ref_cnt)
     assert np.array_equal(run.idx.cpu().numpy(), ref_idx)
     assert_close(run.sparse(fl.sparse_q[0]),
-                 oracle.sparse_decode_batch(fl.sparse_q[0], fl.K, fl.V, ref_idx, ref_cnt))
+                 oracle.sparse_decode_batch(fl.sparse_q[0], fl.K, fl.V, ref_idx, ref_cnt),
+                 what="sparse output, spill below zero")
 
 
 def test_select_handles_a_crowded_boundary_bin():
@@ -253,7 +254,7 @@ def test_window_decode(pos, G):
     out = torch.full((3, G * Hkv, D), float("nan"), device="cuda")
     E.embla_window_decode(shape, to_dev(wl.q), to_dev(wl.K), to_dev(wl.V), pos, out)
     torch.cuda.synchronize()
-    assert_close(out.cpu().numpy(), oracle.window_decode_batch(wl.q, wl.K, wl.V, pos))
+    assert_close(out.cpu().numpy(), oracle.window_decode_batch(wl.q, wl.K, wl.V, pos), what="window output, small")
 
 
 def test_sparse_decode_with_arbitrary_indices_and_counts():
@@ -277,7 +278,7 @@ def test_sparse_decode_with_arbitrary_indices_and_counts():
     ref = oracle.sparse_decode_batch(q, K, V, idx, cnt, tau=0.1)
     got = out.cpu().numpy()
     assert np.all(got[0, 0:4] == 0.0)  # count 0: zero output
-    assert_close(got, ref)
+    assert_close(got, ref, what="sparse output, arbitrary indices tau 0.1")
 
 
 @pytest.mark.parametrize("B,Hq,Hkv", [(8, 16, 4), (9, 16, 4), (16, 16, 2), (19, 16, 2),
@@ -302,7 +303,7 @@ def test_sparse_decode_cluster_sizes(B, Hq, Hkv):
                           torch.from_numpy(cnt.astype(np.int32)).cuda(), out)
     torch.cuda.synchronize()
     assert E.embla_device_check() == 0
-    assert_close(out.cpu().numpy(), oracle.sparse_decode_batch(q, K, V, idx, cnt))
+    assert_close(out.cpu().numpy(), oracle.sparse_decode_batch(q, K, V, idx, cnt), what="sparse output, cluster shapes")
 
 
 def test_out_of_range_index_is_skipped_and_flagged():
@@ -322,4 +323,4 @@ def test_out_of_range_index_is_skipped_and_flagged():
     assert E.embla_device_check(clear=True) == 0
     good = np.array([0, 1, 2, 4, 5, 6, 7], dtype=np.int32)
     ref = oracle.sparse_decode(q[0, 8:12], K[0, 2], V[0, 2], good)
-    assert_close(out.cpu().numpy()[0, 8:12], ref)
+    assert_close(out.cpu().numpy()[0, 8:12], ref, what="sparse output, out-of-range index skipped")

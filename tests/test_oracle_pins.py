@@ -246,6 +246,44 @@ def test_survivor_count_matches_the_generators_construction(pattern, frac):
     assert np.array_equal(sigma > 0, fl.targets > 0)
 
 
+@pytest.mark.parametrize("G,pattern,frac", [(4, "subset", 0.05), (4, "subset", 0.01),
+                                            (8, "subset", 0.2), (4, "runs", 0.05)])
+def test_generator_keeps_a_gap_at_every_top_k_boundary(G, pattern, frac):
+    # Both readings of the selection (the group's score and each head's own) need a clear
+    # boundary between the 1024th and 1025th candidate, or fp32 rounding could pick either.
+    # Checked here with plain numpy cosines of the stored bf16 keys, not the oracle.
+    n, gap = 4096, 2e-3
+    fl = gen.make_full_layer(seed=31 + G, layer=0, B=2, Hq=16, Hkv=16 // G, D=D, n=n,
+                             pattern=pattern, frac=frac, gap=gap)
+    for b in range(2):
+        for g in range(16 // G):
+            q = gen.bf16_to_f32(fl.q[b, g * G:(g + 1) * G]).astype(np.float64)
+            K = gen.bf16_to_f32(fl.K[b, g, :n - 128]).astype(np.float64)
+            cos = (q @ K.T) / np.outer(np.linalg.norm(q, axis=1), np.linalg.norm(K, axis=1))
+            for row in list(D * cos) + [D * cos.max(axis=0)]:
+                top = np.sort(row)[::-1]
+                assert top[1023] - top[1024] >= gap
+
+
+def test_head_scores_batch_is_each_heads_score_and_their_max_is_sigma():
+    # Per-head scores (the per-query-head reading of the selection): with eps 0 each is
+    # alpha * D * cos(q_h, k_j) (numpy cosines), rounded to fp32; the maximum over a
+    # group's heads is the group's selection score, bit for bit (rounding is monotone).
+    fl = gen.make_full_layer(seed=5, layer=0, B=2, Hq=16, Hkv=4, D=D, n=700, pattern="bernoulli",
+                             frac=0.3, n_cap=703)
+    hs = oracle.head_scores_batch(fl.q, fl.K, fl.n, alpha=0.5, eps=0.0)
+    assert np.isnan(hs[..., fl.n:]).all()
+    _, sigma, _ = oracle.full_decode_batch(fl.q, fl.K, fl.V, fl.n, alpha=0.5, eps=0.0)
+    for b in range(2):
+        for h in range(16):
+            q = gen.bf16_to_f32(fl.q[b, h]).astype(np.float64)
+            K = gen.bf16_to_f32(fl.K[b, h // 4, :fl.n]).astype(np.float64)
+            cos = K @ q / (np.linalg.norm(K, axis=1) * np.linalg.norm(q))
+            np.testing.assert_allclose(hs[b, h, :fl.n], 0.5 * D * cos, rtol=1e-6, atol=1e-6)
+        grp = hs[b, :, :fl.n].reshape(4, 4, fl.n).max(axis=1)
+        assert np.array_equal(grp, sigma[b, :, :fl.n])
+
+
 # ----------------------------------------------------------------------------- selection
 # "Three kinds of attention", Sparse: top 1,024 keys by the full layer's score (whether or
 # not they survived ReLU^2), together with the newest 128 keys.

@@ -1,8 +1,11 @@
 """embla_full_decode_static_scratch: the full-layer decode on the library's fixed device
 scratch, called through the C ABI, against embla_full_decode with a caller workspace.
 
-The file name sorts last so that the first use of the scratch can come after every
-other test in one process; it also passes on its own in a fresh process."""
+The file name sorts last, so a run that stops at its first failure has run every other
+test before this one.  Nothing here depends on that order: the first call on a device looks
+up the scratch's device address, and every call in this file is a plain call outside any
+stream capture (no test in the suite captures a graph), so the look-up works whichever test
+makes it, alone in a fresh process or after the rest of the suite."""
 import gc
 
 import pytest
