@@ -83,17 +83,18 @@ def _peaks():
 
 
 def _traffic_from_profile(workload_key: str, src_digest: str):
-    """DRAM bytes per launch of the full-layer kernel from a committed ncu summary, if the
-    summary was taken on the current kernel source (same digest) and workload."""
-    path = os.path.join(ROOT, "profiles", "full_decode_traffic.md")
+    """DRAM bytes per launch of the full-layer kernel, as an ncu capture measured them
+    (profiles/full_decode_traffic.json: one record per workload with the digest of the
+    kernel source it was taken on).  None when no record matches the current source."""
+    path = os.path.join(ROOT, "profiles", "full_decode_traffic.json")
     try:
-        for line in open(path):
-            if line.startswith("traffic:"):
-                kv = dict(tok.split("=", 1) for tok in line.split()[1:])
-                if kv.get("workload") == workload_key and kv.get("src") == src_digest:
-                    return float(kv["bytes_per_launch"])
-    except OSError:
-        pass
+        with open(path) as f:
+            records = json.load(f)["records"]
+    except (OSError, ValueError, KeyError):
+        return None
+    for rec in records:
+        if rec.get("workload") == workload_key and rec.get("src") == src_digest:
+            return float(rec["bytes_per_launch"])
     return None
 
 
@@ -285,23 +286,29 @@ def run_reference(args):
         return run_reference_prefill(args, cfg)
     if cfg.get("kind") == "mlp":
         return run_reference_mlp(args, cfg)
-    sample_b = 1
-    fls = list(gen.config_full_layers(args.config, seed=0, B=sample_b))
-    wls = list(gen.config_window_layers(args.config, seed=0, B=sample_b))
-    # widen to fp64 once, outside the timed region
-    prep = []
-    for fl in fls:
-        K, V = _oracle_kv(oracle, fl)
-        prep.append((oracle.f64(fl.q), K, V, [oracle.f64(qs) for qs in fl.sparse_q], fl.n))
-    wprep = [(oracle.f64(w.q), oracle.f64(w.K), oracle.f64(w.V), w.pos) for w in wls]
+    cores = omp_threads()
+    oracle.set_threads(cores)
+    if args.config == 5:
+        # the whole-model step: every layer of the step for one of its sixteen sequences
+        sample_b = 1
+        fls = list(gen.config_full_layers(args.config, seed=0, B=sample_b))
+        wls = list(gen.config_window_layers(args.config, seed=0, B=sample_b))
+        prep = []
+        for fl in fls:
+            K, V = _oracle_kv(oracle, fl)
+            prep.append((oracle.f64(fl.q), K, V, [oracle.f64(qs) for qs in fl.sparse_q], fl.n))
+        wprep = [(oracle.f64(w.q), oracle.f64(w.K), oracle.f64(w.V), w.pos) for w in wls]
+        sample = f"{sample_b} of {cfg['B']} sequences, every layer of the step"
+    else:
+        # the same work as the GPU step: the whole batch, every layer of the step
+        sample_b = cfg["B"]
+        prep = [_oracle_step_inputs(args.config, sample_b)]
+        wprep = []
+        sample = f"all {sample_b} sequences, every layer of the step"
 
     def step():
-        for q, K, V, qss, n in prep:
-            _, sig, _ = oracle.full_decode_batch(q, K, V, n)
-            if qss:
-                idx, cnt = oracle.select_topk_batch(sig, n)
-                for qs in qss:
-                    oracle.sparse_decode_batch(qs, K, V, idx, cnt)
+        for p in prep:
+            _oracle_layer_step(*p)
         for q, K, V, pos in wprep:
             oracle.window_decode_batch(q, K, V, pos)
 
@@ -312,7 +319,6 @@ def run_reference(args):
         step()
     dt = time.perf_counter() - t0
     value = sample_b * args.steps / dt
-    cores = omp_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -320,7 +326,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": static_config(args.config),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{sample_b} of {cfg['B']} sequences, every layer of the step"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -688,33 +694,59 @@ def bench_mlp(args, cfg):
     return 0
 
 
-def cpu_baseline(cfg_id: int, budget_s: float = 12.0):
+def _oracle_step_inputs(cfg_id: int, B: int):
+    """One full layer of a workload (the first of config 5) widened for the oracle once:
+    (q, K, V, sparse queries, n)."""
+    import gen
+    import oracle
+    fl = next(gen.config_full_layers(cfg_id, seed=0, B=B))
+    K, V = _oracle_kv(oracle, fl)
+    return oracle.f64(fl.q), K, V, [oracle.f64(x) for x in fl.sparse_q], fl.n
+
+
+def _oracle_layer_step(q, K, V, qss, n):
+    """The oracle as it stands over one full layer of the batch: full layer, selection and
+    the sparse layers that reuse it."""
+    import oracle
+    _, sig, _ = oracle.full_decode_batch(q, K, V, n)
+    if qss:
+        idx, cnt = oracle.select_topk_batch(sig, n)
+        for qs in qss:
+            oracle.sparse_decode_batch(qs, K, V, idx, cnt)
+
+
+def _time_passes(fn, budget_s: float):
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return reps, time.perf_counter() - t0
+
+
+def cpu_baseline(cfg_id: int, budget_s: float = 8.0):
     """The oracle as it stands, on this host's cores, over the whole batch of one full layer
-    step (full + selection + its sparse layers), repeated until ~budget_s of work."""
+    step (full + selection + its sparse layers), repeated for ~budget_s: once with every
+    core (OpenMP over the (sequence, KV head) units) and once on a single thread."""
     import gen
     import oracle
 
     cfg = gen.CONFIGS[cfg_id]
     B = cfg["B"] if cfg_id != 5 else 1
-    fl = next(gen.config_full_layers(cfg_id, seed=0, B=B))
-    q = oracle.f64(fl.q)
-    K, V = _oracle_kv(oracle, fl)
-    qss = [oracle.f64(x) for x in fl.sparse_q]
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
-        _, sig, _ = oracle.full_decode_batch(q, K, V, fl.n)
-        idx, cnt = oracle.select_topk_batch(sig, fl.n)
-        for qs in qss:
-            oracle.sparse_decode_batch(qs, K, V, idx, cnt)
-        reps += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    sample = (f"{reps} pass(es) over {B} sequence(s): full layer + selection + "
-              f"{len(qss)} sparse layer(s)" + (" (one of the five full-layer blocks)" if cfg_id == 5 else ""))
-    return {"value": B * reps / dt, "unit": "tokens/s", "cores": omp_threads(),
-            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+    inp = _oracle_step_inputs(cfg_id, B)
+    cores = omp_threads()
+    oracle.set_threads(cores)
+    reps, dt = _time_passes(lambda: _oracle_layer_step(*inp), budget_s)
+    prev = oracle.set_threads(1)
+    reps1, dt1 = _time_passes(lambda: _oracle_layer_step(*inp), budget_s)
+    oracle.set_threads(prev)
+    what = (f"full layer + selection + {len(inp[3])} sparse layer(s) over {B} sequence(s)"
+            + (" (one of the five full-layer blocks)" if cfg_id == 5 else ""))
+    return {"value": B * reps / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} pass(es) of {what}", "seconds": round(dt, 2),
+            "single_thread": {"value": B * reps1 / dt1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{reps1} pass(es) of the same", "seconds": round(dt1, 2)}}
 
 
 def main():
@@ -962,11 +994,15 @@ def main():
     sel_tot = [int(L["count"].sum().item()) if L["qs"] else 0 for L in layers]
     full_bytes = [full_layer_needed_bytes(L["shape"].units, L["fl"].n, s, L["fl"].kv)
                   for L, s in zip(layers, n_surv_tot)]
-    sparse_bytes = sum(len(L["qs"]) * sparse_layer_needed_bytes(s, L["fl"].kv)
-                       for L, s in zip(layers, sel_tot))
+    # a block's first sparse layer reads its selected rows from HBM; the block's later sparse
+    # layers read the same rows right after it, from L2, so they are counted apart
+    sparse_first = sum(sparse_layer_needed_bytes(s, L["fl"].kv)
+                       for L, s in zip(layers, sel_tot) if L["qs"])
+    sparse_rereads = sum((len(L["qs"]) - 1) * sparse_layer_needed_bytes(s, L["fl"].kv)
+                         for L, s in zip(layers, sel_tot) if L["qs"])
     win_bytes = sum(window_layer_needed_bytes(w["shape"].units, min(w["wl"].pos + 1, w["wl"].K.shape[2]))
                     for w in wins)
-    needed = sum(full_bytes) + sparse_bytes + win_bytes
+    needed = sum(full_bytes) + sparse_first + win_bytes
     keys_total = sum(L["shape"].units * L["fl"].n for L in layers)
     skipped_v = 1.0 - sum(n_surv_tot) / max(1, keys_total)
     # the same V reads counted at the page's granularity (8-key chunks)
@@ -1085,6 +1121,48 @@ def main():
                          "from pinned host memory (then placed into the caches on the device) and "
                          "one copy of every output back; the KV caches stay resident in HBM"}
 
+    # one sparse layer (the first of the first block) timed alone: after a write of twice the
+    # L2 size (its rows come from HBM), and again right after itself (its rows in L2)
+    sparse_alone = None
+    Lsp = next((L for L in layers if L["qs"]), None)
+    if Lsp is not None:
+        def sparse_one(L=Lsp):
+            qs, so = L["qs"][0], L["souts"][0]
+            if L["per_head"]:
+                E.embla_sparse_decode_per_head(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"],
+                                               so, workspace=L["ws_sp"])
+            elif "Ks" in L:
+                E.embla_sparse_decode_e4m3(L["shape"], qs, L["K"], L["Ks"], L["V"], L["Vs"],
+                                           L["idx"], L["count"], so, workspace=L["ws_sp"])
+            else:
+                E.embla_sparse_decode(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"], so,
+                                      workspace=L["ws_sp"])
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        cold, warm = [], []
+        with torch.cuda.stream(stream):
+            for r in range(12):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                flush.fill_(float(r))
+                e[0].record(stream)
+                sparse_one()
+                e[1].record(stream)
+                e[2].record(stream)
+                sparse_one()
+                e[3].record(stream)
+                torch.cuda.synchronize()
+                if r >= 2:
+                    cold.append(e[0].elapsed_time(e[1]))
+                    warm.append(e[2].elapsed_time(e[3]))
+        del flush
+        sp_bytes = sparse_layer_needed_bytes(sel_tot[layers.index(Lsp)], Lsp["fl"].kv)
+        cold_ms, warm_ms = statistics.mean(cold), statistics.mean(warm)
+        sparse_alone = {"bytes": sp_bytes,
+                        "cold_l2_us": round(cold_ms * 1e3, 2),
+                        "cold_l2_gbs": round(sp_bytes / (cold_ms * 1e-3) / 1e9, 1),
+                        "warm_l2_us": round(warm_ms * 1e3, 2),
+                        "how": "one sparse-layer call alone with CUDA events: after writing "
+                               "twice the L2 size (cold), and right after the same call (warm)"}
+
     peak, peak_src = _peaks()
     wl_key = workload_name(cfg, args.batch, args.ctx).replace(" ", "_")
     achieved = [fb / (fm * 1e-3) / 1e9 for fb, fm in zip(full_bytes, full_ms)]
@@ -1117,8 +1195,16 @@ def main():
                           f"step's rows were last read {(n_rep - 1) * step_read / 1e6:.0f} MB of "
                           "other reads earlier"),
                    "needed_bytes_per_step": needed,
+                   "needed_bytes": "HBM: every full layer's K rows and surviving V rows, each "
+                                   "block's first sparse layer's selected K and V rows, the "
+                                   "window rows",
                    "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),
                    "needed_frac_of_peak": round(needed / (ms_per_step * 1e-3) / 1e9 / peak, 4),
+                   "sparse_reread_bytes_per_step": sparse_rereads,
+                   "sparse_reread": "the same selected rows read again by a block's later "
+                                    "sparse layers right after its first (from L2; not in "
+                                    "needed_bytes_per_step)",
+                   "sparse_layer_alone": sparse_alone,
                    "skipped_v_fraction": round(skipped_v, 5),
                    "skipped_v_fraction_8key_chunks": None if skipped_v_chunk8 is None else round(skipped_v_chunk8, 5),
                    "selection": "per query head" if per_head else "per KV head (group max)"},

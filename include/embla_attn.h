@@ -38,6 +38,10 @@
  *     current device (NULL when that size is 0).  Its contents need not be initialised and are not
  *     meaningful after the call.  Calls that share a workspace must be
  *     ordered on one stream.
+ *   - A *_workspace_size call returns 0 both when the shape needs no
+ *     workspace and when its arguments are invalid (the size functions have
+ *     no error channel); the matching call checks the same arguments itself
+ *     and returns the error status.
  */
 #ifndef EMBLA_ATTN_H
 #define EMBLA_ATTN_H

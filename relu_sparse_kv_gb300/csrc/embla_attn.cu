@@ -1,6 +1,7 @@
 // C ABI of the library: host-side argument checks, workspace sizing, TMA descriptor
 // encoding and the launches of the kernels in this directory.  Declarations and the
 // meaning of every argument are in include/embla_attn.h.
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -27,44 +28,42 @@ int current_device() {
   return dev;
 }
 
+// Per-device values looked up once and kept.  Every slot is an atomic, filled at most
+// once per device (a look-up that fails leaves the slot empty, so the next call retries);
+// two host threads making their first call on a device at the same time may both look the
+// value up, and both store the same value.
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<void *> g_flags_addr[kMaxDevices];
+std::atomic<void *> g_scratch_addr[kMaxDevices];
+
 int sm_count_of(int dev) {
-  static int cache[kMaxDevices] = {0};
   if (dev < 0 || dev >= kMaxDevices) return 0;
-  if (cache[dev] == 0) {
-    int v = 0;
+  int v = g_sm_count[dev].load(std::memory_order_acquire);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cache[dev] = v;
+    g_sm_count[dev].store(v, std::memory_order_release);
   }
-  return cache[dev];
+  return v;
 }
 
-uint32_t *flags_ptr() {
-  static uint32_t *cache[kMaxDevices] = {nullptr};
+// Device address of a __device__ symbol on the current device, cached in `slot`.
+template <typename T>
+void *symbol_address(std::atomic<void *> (&slot)[kMaxDevices], const T &symbol) {
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (cache[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_check_flags) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<uint32_t *>(p);
+  void *p = slot[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+    slot[dev].store(p, std::memory_order_release);
   }
-  return cache[dev];
+  return p;
 }
+
+uint32_t *flags_ptr() { return static_cast<uint32_t *>(symbol_address(g_flags_addr, g_check_flags)); }
 
 // Device address of g_full_scratch on the current device, looked up on the first
 // call for that device and kept; nullptr if the look-up fails.
-void *full_scratch_ptr() {
-  static std::mutex mu;
-  static void *cache[kMaxDevices] = {nullptr};
-  const int dev = current_device();
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_full_scratch) != cudaSuccess) return nullptr;
-    cache[dev] = p;
-  }
-  return cache[dev];
-}
+void *full_scratch_ptr() { return symbol_address(g_scratch_addr, g_full_scratch); }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
