@@ -1121,8 +1121,8 @@ def main():
                          "from pinned host memory (then placed into the caches on the device) and "
                          "one copy of every output back; the KV caches stay resident in HBM"}
 
-    # one sparse layer (the first of the first block) timed alone: after a write of twice the
-    # L2 size (its rows come from HBM), and again right after itself (its rows in L2)
+    # one sparse layer (the first of the first block): its marginal cost after a write of twice
+    # the L2 size (its rows come from HBM), and right after itself (its rows in L2)
     sparse_alone = None
     Lsp = next((L for L in layers if L["qs"]), None)
     if Lsp is not None:
@@ -1138,30 +1138,33 @@ def main():
                 E.embla_sparse_decode(L["shape"], qs, L["K"], L["V"], L["idx"], L["count"], so,
                                       workspace=L["ws_sp"])
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-        cold, warm = [], []
-        with torch.cuda.stream(stream):
-            for r in range(12):
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-                flush.fill_(float(r))
-                e[0].record(stream)
-                sparse_one()
-                e[1].record(stream)
-                e[2].record(stream)
-                sparse_one()
-                e[3].record(stream)
-                torch.cuda.synchronize()
-                if r >= 2:
-                    cold.append(e[0].elapsed_time(e[1]))
-                    warm.append(e[2].elapsed_time(e[3]))
+
+        def graph_ms(body, reps=30):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    body()
+                g.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        # marginal cost in a graph: (flush, call) - (flush) and (call, call) - (call)
+        cold_ms = graph_ms(lambda: (flush.fill_(1.0), sparse_one())) - graph_ms(lambda: flush.fill_(1.0))
+        warm_ms = graph_ms(lambda: (sparse_one(), sparse_one())) - graph_ms(sparse_one)
         del flush
         sp_bytes = sparse_layer_needed_bytes(sel_tot[layers.index(Lsp)], Lsp["fl"].kv)
-        cold_ms, warm_ms = statistics.mean(cold), statistics.mean(warm)
         sparse_alone = {"bytes": sp_bytes,
                         "cold_l2_us": round(cold_ms * 1e3, 2),
                         "cold_l2_gbs": round(sp_bytes / (cold_ms * 1e-3) / 1e9, 1),
                         "warm_l2_us": round(warm_ms * 1e3, 2),
-                        "how": "one sparse-layer call alone with CUDA events: after writing "
-                               "twice the L2 size (cold), and right after the same call (warm)"}
+                        "how": "marginal cost of one sparse-layer call in a CUDA graph: after a "
+                               "write of twice the L2 size (cold: graph of the write and the call "
+                               "minus graph of the write) and right after the same call (warm)"}
 
     peak, peak_src = _peaks()
     wl_key = workload_name(cfg, args.batch, args.ctx).replace(" ", "_")

@@ -10,8 +10,8 @@
 //   warp 0     TMA producer: 32 KB K tiles (two 64-column boxes, 128-byte swizzle) into
 //              a 3-stage ring; the unit's G query rows when the unit changes.
 //   warps 1, 18  tcgen05 issuers taking alternate tiles: D[128 keys x 16] = K . Q^T
-//              (raw bf16 operands, fp32 in tensor memory), one independent MMA per
-//              16-dim k-step; four tiles in flight use all 512 columns.
+//              (raw bf16 operands, fp32 in tensor memory), the eight 16-dim k-steps added
+//              into one accumulator of 16 columns; four tiles in flight.
 //   warps 14-17  key norms, one thread per key as soon as a tile lands:
 //              rk = 1/sqrt(mean(k^2) + eps), handed to the epilogue through a small
 //              shared-memory ring; the K stage is free once these and the MMAs are done.
@@ -24,23 +24,28 @@
 //   warp 19    selection scores (when requested): writes each tile's sigma to global
 //              memory and counts it into a shared histogram, flushed when a unit's
 //              stretch ends.
-//   warps 10-13  V accumulators (heads split over warps): num_h += w_h v, den_h += w_h
-//              in tile order; at the end of each stretch of a unit they write a partial
-//              record, and the last warp to publish a unit's record sums its records and
-//              writes out = num / (c + den) and the survivor count.
+//   warps 10-13  V accumulators: O^T += V^T W as m16n8k16 bf16 MMAs over 16 survivors at
+//              a time (dims split over warps, heads as the N columns, the weights as bf16
+//              hi + lo), the denominators in fp32, in tile order; at the end of each
+//              stretch of a unit they write a partial record, and the last CTA to publish
+//              a unit's record sums its records and writes out = num / (c + den) and the
+//              survivor count.
 //
 // 8-bit caches (E4M3 codes with one fp32 scale per token and KV head; same roles):
 //   - a stage is the 16 KB code tile (one 128-column box, 128-byte swizzle) plus the
 //     tile's 512-byte K-scale and V-scale runs; 6 stages.
-//   - the key-norm warps also build, once per unit, the query as three E4M3 terms with
-//     t1 + t2 / 16 + t3 / 256 = q / 2^e (2^e a power of two per head, so |q / 2^e| < 256),
-//     laid out as MMA rows term * G + h; the sum is within 2^-25 of the head's largest
-//     |q| of every element, and exact for every element at least 2^-14 of it.
-//   - the tensor cores take the codes and the terms directly (kind::f8f6f4, K = 32), one
-//     accumulator per k-step; the epilogue sums the terms and k-steps in fp32 and folds
-//     2^e into the query factor, and the key scale into rk:
+//   - the key-norm warps pass on the keys' scales and build, once per unit, the query as
+//     three E4M3 terms with t1 + t2 / 16 + t3 / 256 = q / 2^e (2^e a power of two per head,
+//     so |q / 2^e| < 256), laid out as MMA rows term * G + h; the sum is within 2^-25 of
+//     the head's largest |q| of every element, and exact for every element at least 2^-14
+//     of it.
+//   - the tensor cores take the codes and the terms directly (kind::f8f6f4, K = 32), the
+//     k-steps into one accumulator, followed by 128 columns of codes . codes^T whose
+//     diagonal is each key's sum of squared codes; two tiles in flight.  The epilogue sums
+//     the terms in fp32 and folds 2^e into the query factor, and the key scale into rk:
 //     rk = ks / sqrt(ks^2 * mean(code^2) + eps).
-//   - 128-byte V rows; the accumulators decode the codes and weight them by w * vs.
+//   - 128-byte V rows; the accumulators widen each step's code rows to bf16 (exactly) and
+//     weight them by w * vs.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -67,6 +72,9 @@ constexpr int kNormSlots = 8;                      // per-tile key-norm arrays i
 constexpr int kQBufBytes = 4096;                   // 16 rows x 128 dims of bf16 (MMA N = 16)
 constexpr int kQHalfBytes = kQBufBytes / 2;
 constexpr int kQ8BufBytes = 4096;                  // up to 32 rows x 128 dims of E4M3
+constexpr int kAccStep = 16;                       // survivors per V-accumulation MMA step
+constexpr int kAccPitch = 2 * 128 + 16;            // bytes per bf16 row read by ldmatrix
+constexpr uint32_t kAccBar = 3;                    // named barrier of the accumulator warps
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
 constexpr int kWarpAcc = kWarpEpi + 4 * kGroups;
 constexpr int kWarpNorm = kWarpAcc + 4;
@@ -92,6 +100,10 @@ struct Cfg {
   // every full_period tiles.
   static constexpr int full_period = stages % 2 == 0 ? stages : 2 * stages;
   static constexpr int row_bytes = KV8 ? kHeadDim : 2 * kHeadDim;  // one cached K or V row
+  // V-ring row pitch: bf16 rows are read by ldmatrix straight from the ring, so they are
+  // padded by 16 bytes (eight rows in a row then fall in eight different bank groups);
+  // 8-bit rows are first widened to bf16 rows in a small staging area of that pitch.
+  static constexpr int ring_pitch = KV8 ? kHeadDim : 2 * kHeadDim + 16;
   static constexpr int tile_bytes = kTileKeys * row_bytes;           // 32 KB / 16 KB
   static constexpr int half_bytes = kTileKeys * 128;                 // one 128-byte-wide box
   static constexpr int scale_bytes = KV8 ? kTileKeys * 4 : 0;        // K (then V) scales
@@ -100,18 +112,17 @@ struct Cfg {
   static constexpr int mma_n = KV8 ? (3 * G <= 16 ? 16 : 32) : 16;
   static constexpr int kstep_dims = KV8 ? 32 : 16;
   static constexpr int ksteps = kHeadDim / kstep_dims;
-  // bf16: each k-step writes its own accumulator, so a tile's MMAs do not wait on each
-  // other; the epilogue adds the partials.  8-bit: the k-steps add into one accumulator,
-  // followed by 128 columns of codes . codes^T, whose diagonal is each key's sum of squared
-  // codes (the key norms come from the tensor cores instead of the CUDA cores).
-  static constexpr int score_cols = KV8 ? mma_n : ksteps * mma_n;
+  // The k-steps add into one score accumulator.  8-bit: it is followed by 128 columns of
+  // codes . codes^T, whose diagonal is each key's sum of squared codes (those key norms come
+  // from the tensor cores; bf16 key norms come from the key-norm warps).
+  static constexpr int score_cols = mma_n;
   static constexpr int diag_cols = KV8 ? kTileKeys : 0;
-  static constexpr int acc_cols = score_cols + diag_cols;            // 128 / 144 / 160
+  static constexpr int acc_cols = score_cols + diag_cols;            // 16 / 144 / 160
   // Tiles in flight.  Tile i goes to buffer i % acc_bufs, to MMA issuer i % 2 and to
   // epilogue group i % 2; with an even count every buffer has one issuer and one reader,
   // which take its phases in order (with an odd count a fast group could wait for a
   // buffer's next phase before its current one completed, and pass on the stale parity).
-  static constexpr int acc_bufs = KV8 ? kGroups : kAccBufs;
+  static constexpr int acc_bufs = KV8 ? kGroups : kAccBufs;  // bf16: 4 x 16 columns
   static constexpr int tmem_cols = 512;
   static constexpr uint32_t idesc = KV8 ? idesc_e4m3_f32(128, mma_n) : idesc_bf16_f32(128, 16);
   static constexpr uint32_t idesc_diag = idesc_e4m3_f32(128, kTileKeys);
@@ -144,7 +155,11 @@ struct Smem {
   static constexpr int q_off = k_off + C::stages * C::stage_bytes;
   static constexpr int q8_off = q_off + 2 * kQBufBytes;
   static constexpr int ring_off = q8_off + (KV8 ? 2 * kQ8BufBytes : 0);
-  static constexpr int wslot_off = ring_off + kRing * C::row_bytes;
+  // bf16: the ring, then one zero row; 8-bit: the ring, then two staging blocks of
+  // kAccStep widened rows and one zero row (the rows an MMA step reads past a tile's list)
+  static constexpr int zero_off = ring_off + kRing * C::ring_pitch;
+  static constexpr int stage_off = KV8 ? zero_off + kAccPitch : zero_off;
+  static constexpr int wslot_off = (KV8 ? stage_off + 2 * kAccStep * kAccPitch : zero_off + kAccPitch);
   static constexpr int hist_off = wslot_off + kWSlots * static_cast<int>(sizeof(WSlot<G, KV8>));
   static constexpr int rk_off = hist_off + kHistBins * 4;
   static constexpr int vs_off = rk_off + kNormSlots * kTileKeys * 4;  // V scales beside rk
@@ -371,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < 2 * kQ8BufBytes / 16; i += kThreads)
       reinterpret_cast<uint4 *>(sQ8)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0u;
+  for (int i = threadIdx.x; i < kAccPitch / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + L::zero_off)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
     tmem_alloc(s_tmem, C::tmem_cols);
@@ -493,9 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is
             // 32 bytes into a 128-byte row, the second half of the dims starts a new box
-            tc_mma_bf16(dcol + kk * C::mma_n,
+            tc_mma_bf16(dcol,
                         adesc + (((kk >> 2) * C::half_bytes + (kk & 3) * 32) >> 4),
-                        qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), C::idesc, 0u);
+                        qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), C::idesc,
+                        kk > 0 ? 1u : 0u);
           }
         }
         tc_commit(&accf[b]);
@@ -529,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The group's own V ring: rows reserved so far, and the survivor counts of its last
     // three tiles (i - 2, i - 4, i - 6), whose rows may still be in use.  Every warp of the
     // group keeps the same copy (they all see every count), so no warp waits for another.
-    uint8_t *gring = sRing + group * kGroupRing * kRowBytes;
+    uint8_t *gring = sRing + group * kGroupRing * C::ring_pitch;
     int issued = 0, m1 = 0, m2 = 0, m3 = 0;
     int u = u0, tl = tl0;
     int seg = -1;
@@ -608,23 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ssq = __uint_as_float(dg[0]);
       } else {
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
-        uint32_t r[C::ksteps * G];
-#pragma unroll
-        for (int kk = 0; kk < C::ksteps; ++kk) {
-          if constexpr (G == 4)
-            tmem_load_x4(taddr + kk * C::mma_n, *reinterpret_cast<uint32_t(*)[4]>(&r[kk * G]));
-          else
-            tmem_load_x8(taddr + kk * C::mma_n, *reinterpret_cast<uint32_t(*)[8]>(&r[kk * G]));
-        }
+        uint32_t r[G];
+        if constexpr (G == 4)
+          tmem_load_x4(taddr, *reinterpret_cast<uint32_t(*)[4]>(&r[0]));
+        else
+          tmem_load_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
         tmem_wait_ld(r);
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float p0 = __uint_as_float(r[0 * G + h]) + __uint_as_float(r[1 * G + h]);
-          const float p1 = __uint_as_float(r[2 * G + h]) + __uint_as_float(r[3 * G + h]);
-          const float p2 = __uint_as_float(r[4 * G + h]) + __uint_as_float(r[5 * G + h]);
-          const float p3 = __uint_as_float(r[6 * G + h]) + __uint_as_float(r[7 * G + h]);
-          dot[h] = (p0 + p1) + (p2 + p3);
-        }
+        for (int h = 0; h < G; ++h) dot[h] = __uint_as_float(r[h]);
       }
       tc_fence_before_sync();
       // bf16: the key norm; 8-bit: the key's scale ks, whose norm follows from the sum of
@@ -710,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (surv)
-        bulk_load(gring + ((row0 + e) & (kGroupRing - 1)) * kRowBytes,
+        bulk_load(gring + ((row0 + e) & (kGroupRing - 1)) * C::ring_pitch,
                   p.v + (static_cast<int64_t>(u) * p.ncap + j) * kRowBytes, kRowBytes, &vfull[slot]);
     }
     __syncwarp();
@@ -848,100 +857,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ V accumulators
-    constexpr int HPW = G / 4;  // heads per warp
+    // O^T[d][h] += sum_e V[e][d] w_h[e] on the tensor cores (m16n8k16 bf16 MMAs), kAccStep
+    // survivors per step: warp aw owns dims 32aw .. 32aw+31 (two 16-dim M tiles), the N = 8
+    // columns are the heads (G = 4 leaves four of them zero).  The A operand is read from
+    // the ring by ldmatrix (rows past the tile's list read a zero row); the weights enter
+    // as two bf16 parts (hi + lo, about 16 bits), and the denominators sum the fp32
+    // weights.  8-bit caches: each step first widens its code rows (exactly) to bf16 rows
+    // in a staging block, a quarter of the rows per warp, and the weights carry the V
+    // scales.  The four warps take every decision to stop together (bar.red.and), so none
+    // is left at a barrier the others have abandoned.
     const int aw = warp - kWarpAcc;
-    const int d0 = lane * 4;
-    float acc[HPW][4];
-    float den[HPW];
+    const int g = lane >> 2, t = lane & 3;
+    const int mat = lane >> 3, mr = lane & 7;
+    const uint32_t zero_u32 = smem_u32(smem + L::zero_off);
+    const uint32_t ring_u32 = smem_u32(sRing);
+    uint8_t *stage = smem + L::stage_off;
+    float o[2][4];
 #pragma unroll
-    for (int hh = 0; hh < HPW; ++hh) {
-      den[hh] = 0.0f;
-#pragma unroll
-      for (int d = 0; d < 4; ++d) acc[hh][d] = 0.0f;
-    }
-    int seg_surv = 0;
+    for (int mt = 0; mt < 2; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+    float den = 0.0f;  // lane (g, t): head g's weights of rows 2t, 2t+1, 2t+8, 2t+9 of each step
+    int seg_surv = 0, step = 0;
     int u = u0, tl = tl0;
     for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-      if (__any_sync(0xffffffffu, *s_abort)) break;
       const int slot = static_cast<int>(i % kWSlots);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&vfull[slot], (i / kWSlots) & 1));
-      if (!ok) {
+      const bool ok = !*s_abort && mbar_wait(&vfull[slot], (i / kWSlots) & 1);
+      if (!named_bar_and(kAccBar, 128, ok)) {
         set_abort(s_abort, p.flags);
         break;
       }
       const WSlot<G, KV8> &ws = wslots[slot];
       const int row0 = ws.row0, m = ws.m;
-      for (int e0 = 0; e0 < m; e0 += 4) {
-        uint2 raw[4];
-        float wv[4][HPW];
-        float vsr[4];
+      const uint32_t gring_u32 = ring_u32 + (i % kGroups) * kGroupRing * C::ring_pitch;
+      for (int e0 = 0; e0 < m; e0 += kAccStep, ++step) {
+        uint32_t base_u32;  // row 0 of this step's A operand
+        if constexpr (KV8) {
+          // widen rows e0 + 4aw .. +3 (lane: codes 4 lane .. 4 lane + 3) into the staging block
+          uint8_t *sb = stage + (step & 1) * kAccStep * kAccPitch;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          // rows past m are not this tile's: skip them (weight 0, value 0)
-          const int e = e0 + r;
-          const uint8_t *vr = sRing + ((i % kGroups) * kGroupRing + ((row0 + e) & (kGroupRing - 1))) * kRowBytes;
-          if constexpr (KV8) {
-            raw[r] = make_uint2(e < m ? *reinterpret_cast<const uint32_t *>(vr + lane * 4) : 0u, 0u);
-            vsr[r] = e < m ? ws.vs[e] : 0.0f;
-          } else {
-            raw[r] = e < m ? *reinterpret_cast<const uint2 *>(vr + lane * 8) : make_uint2(0u, 0u);
+          for (int k = 0; k < kAccStep / 4; ++k) {
+            const int e = e0 + aw * (kAccStep / 4) + k;
+            if (e < m) {
+              const uint32_t c4 = *reinterpret_cast<const uint32_t *>(
+                  sRing + (i % kGroups) * kGroupRing * C::ring_pitch +
+                  ((row0 + e) & (kGroupRing - 1)) * C::ring_pitch + lane * 4);
+              float v0, v1, v2, v3;
+              e4m3x4_to_f32(c4, v0, v1, v2, v3);
+              *reinterpret_cast<uint2 *>(sb + (e - e0) * kAccPitch + lane * 8) =
+                  make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+            }
           }
-#pragma unroll
-          for (int hh = 0; hh < HPW; ++hh) wv[r][hh] = e < m ? ws.w[e][aw + 4 * hh] : 0.0f;
+          named_bar_sync(kAccBar, 128);  // the step's rows are widened
+          base_u32 = smem_u32(sb);
         }
+        // A: this lane's matrix row r of the step (matrices: rows 0-7 / 8-15 x dims +0 / +8)
+        const int r = (mat >> 1) * 8 + mr;
+        uint32_t raddr;
+        if constexpr (KV8)
+          raddr = e0 + r < m ? base_u32 + r * kAccPitch : zero_u32;
+        else
+          raddr = e0 + r < m ? gring_u32 + ((row0 + e0 + r) & (kGroupRing - 1)) * C::ring_pitch
+                             : zero_u32;
+        uint32_t a[2][4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float v0, v1, v2, v3;
-          if constexpr (KV8) {
-            e4m3x4_to_f32(raw[r].x, v0, v1, v2, v3);
-          } else {
-            v0 = bf16lo(raw[r].x);
-            v1 = bf16hi(raw[r].x);
-            v2 = bf16lo(raw[r].y);
-            v3 = bf16hi(raw[r].y);
-          }
+        for (int mt = 0; mt < 2; ++mt)
+          ldmatrix_x4_trans(a[mt], raddr + (2 * (2 * aw + mt) + (mat & 1)) * 16);
+        // B: head g's weights of rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1)
+        float w[4], wq[4];
 #pragma unroll
-          for (int hh = 0; hh < HPW; ++hh) {
-            const float w = wv[r][hh];
-            const float wq = KV8 ? w * vsr[r] : w;  // the weight of the decoded codes
-            acc[hh][0] = fmaf(wq, v0, acc[hh][0]);
-            acc[hh][1] = fmaf(wq, v1, acc[hh][1]);
-            acc[hh][2] = fmaf(wq, v2, acc[hh][2]);
-            acc[hh][3] = fmaf(wq, v3, acc[hh][3]);
-            den[hh] += w;
-          }
+        for (int k = 0; k < 4; ++k) {
+          const int e = e0 + 2 * t + (k & 1) + (k >> 1) * 8;
+          const bool have = e < m && g < G;
+          w[k] = have ? ws.w[e][g < G ? g : 0] : 0.0f;
+          wq[k] = w[k];
+          if constexpr (KV8) wq[k] = have ? w[k] * ws.vs[e] : 0.0f;
+        }
+        den += (w[0] + w[1]) + (w[2] + w[3]);
+        const uint32_t h0 = pack_bf16x2(wq[0], wq[1]), h1 = pack_bf16x2(wq[2], wq[3]);
+        const uint32_t l0 = pack_bf16x2(wq[0] - bf16lo(h0), wq[1] - bf16hi(h0));
+        const uint32_t l1 = pack_bf16x2(wq[2] - bf16lo(h1), wq[3] - bf16hi(h1));
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma_16816_bf16(o[mt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], h0, h1);
+          mma_16816_bf16(o[mt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], l0, l1);
         }
       }
       seg_surv += m;
       // the running sums depend on every ring row and weight this lane read
-      float used = 0.0f;
-#pragma unroll
-      for (int hh = 0; hh < HPW; ++hh)
-        used += den[hh] + ((acc[hh][0] + acc[hh][1]) + (acc[hh][2] + acc[hh][3]));
+      float used = den + ((o[0][0] + o[0][1]) + (o[0][2] + o[0][3])) +
+                   ((o[1][0] + o[1][1]) + (o[1][2] + o[1][3]));
       used = __shfl_sync(0xffffffffu, used, 31) + used;
       __syncwarp();
       if (lane == 0) mbar_arrive_after(&wempty[slot], used);
       if (i + 1 == ntiles || tl + 1 == TU) {
         float *r = p.rec + (cta + u) * p.rec_stride;
+        // this warp's dims of every head
 #pragma unroll
-        for (int hh = 0; hh < HPW; ++hh) {
-          const int h = aw + 4 * hh;
-          *reinterpret_cast<float4 *>(r + h * kHeadDim + d0) =
-              make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-          if (lane == 0) r[G * kHeadDim + h] = den[hh];
-          den[hh] = 0.0f;
-          acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.0f;
+        for (int mt = 0; mt < 2; ++mt) {
+          const int d = 32 * aw + 16 * mt + g;
+          if (2 * t < G) {
+            r[(2 * t) * kHeadDim + d] = o[mt][0];
+            r[(2 * t) * kHeadDim + d + 8] = o[mt][2];
+          }
+          if (2 * t + 1 < G) {
+            r[(2 * t + 1) * kHeadDim + d] = o[mt][1];
+            r[(2 * t + 1) * kHeadDim + d + 8] = o[mt][3];
+          }
+          o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
         }
+        // every warp sees the same weights: warp 0 writes the denominators
+        float dh = den + __shfl_xor_sync(0xffffffffu, den, 1);
+        dh += __shfl_xor_sync(0xffffffffu, dh, 2);
+        den = 0.0f;
+        if (aw == 0 && t == 0 && g < G) r[G * kHeadDim + g] = dh;
         if (aw == 0 && lane == 0) reinterpret_cast<int32_t *>(r)[G * kHeadDim + G] = seg_surv;
         seg_surv = 0;
-        // Every CTA that worked on unit u publishes its part of the record; for each
-        // accumulator warp (head group) the last CTA to count itself in sums that head
-        // group over the unit's records, in CTA order, and writes its outputs.
+        // Every CTA that worked on unit u publishes its record; once the four warps have
+        // written their parts, each counts itself in for its head group, and for each head
+        // group the last CTA to count itself in sums that group over the unit's records, in
+        // CTA order, and writes its outputs.
         const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
         const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
         const int parts = static_cast<int>(c1 - c0 + 1);
         __threadfence();  // each lane's part of the record is visible before the count
-        __syncwarp();
+        named_bar_sync(kAccBar, 128);  // the whole record is written
         pdl_wait_primary();  // the arrival counters have been zeroed
         int last = 0;
         if (lane == 0) last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4 + aw], 1) == parts - 1;
@@ -949,8 +987,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           // records of CTAs c0..c1 (other SMs wrote them: read through L2), loaded eight
           // at a time so the loads overlap, summed in CTA order
+          constexpr int HPW = G / 4;  // heads per warp in the combine
+          const int d0 = lane * 4;
           const float *rr = p.rec + (c0 + u) * p.rec_stride;
-          float *o = p.out + static_cast<int64_t>(u) * G * kHeadDim;
+          float *out = p.out + static_cast<int64_t>(u) * G * kHeadDim;
 #pragma unroll
           for (int hh = 0; hh < HPW; ++hh) {
             const int h = aw + 4 * hh;
@@ -964,9 +1004,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 dd[k] = 0.0f;
                 if (k0 + k < parts) {
-                  const float *r = rr + static_cast<int64_t>(k0 + k) * p.rec_stride;
-                  x[k] = __ldcg(reinterpret_cast<const float4 *>(r + h * kHeadDim + d0));
-                  dd[k] = __ldcg(r + G * kHeadDim + h);
+                  const float *rk = rr + static_cast<int64_t>(k0 + k) * p.rec_stride;
+                  x[k] = __ldcg(reinterpret_cast<const float4 *>(rk + h * kHeadDim + d0));
+                  dd[k] = __ldcg(rk + G * kHeadDim + h);
                 }
               }
 #pragma unroll
@@ -979,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             const float z = p.c + dsum;
-            *reinterpret_cast<float4 *>(o + h * kHeadDim + d0) =
+            *reinterpret_cast<float4 *>(out + h * kHeadDim + d0) =
                 z != 0.0f ? make_float4(num.x / z, num.y / z, num.z / z, num.w / z)
                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           }
