@@ -244,7 +244,7 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
     if (st == EMBLA_OK) st = cuda_status(cudaMemsetAsync(n_surv, 0, static_cast<size_t>(units) * 4, s));
     return st;
   }
-  // the launch zeroes the histogram and the arrival counters itself
+  // the launch zeroes the histogram, the arrival counters and the survivor counts itself
   int32_t *arrivals = full_arrivals(workspace, units, G, sms);
   const uint64_t rows = static_cast<uint64_t>(units * shape->cache_stride);
   CUtensorMap tm_k, tm_q, tm_ks, tm_vs;

@@ -164,7 +164,7 @@ struct Smem {
   static constexpr int rk_off = hist_off + kHistBins * 4;
   static constexpr int vs_off = rk_off + kNormSlots * kTileKeys * 4;  // V scales beside rk
   static constexpr int misc_off = vs_off + (KV8 ? kNormSlots * kTileKeys * 4 : 0);
-  static constexpr int bar_off = misc_off + 64;
+  static constexpr int bar_off = misc_off + 128;
   static constexpr int n_bars = 3 * C::stages + 2 * kAccBufs + 8 + 3 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
@@ -289,6 +289,77 @@ __device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
   }
 }
 
+// Sums the partial records of unit u (CTAs c0 .. c0 + parts - 1, each G*128 numerators and
+// G denominators) and writes out = num / (c + den), with NT threads (t = 0 .. NT-1).  Each 4-dim column of a head is split into kSl
+// slices: slice sl sums records sl, sl + kSl, ... in order, eight loads at a time, and the
+// slices (consecutive lanes) are added by a fixed shuffle tree.  The order depends only on G,
+// not on NT, so the whole CTA (after its last stretch) and the four accumulator warps
+// (mid-run) give the same bits.
+template <int G>
+struct CombineShape {
+  static constexpr int cols = G * kHeadDim / 4;    // float4 columns of the numerators
+  static constexpr int slices = G == 4 ? 4 : 2;    // cols * slices <= the CTA's threads
+};
+
+template <int G, int NT>
+__device__ __forceinline__ void combine_unit(const FullParams &p, int u, int64_t c0, int parts,
+                                             int t) {
+  constexpr int kCols = CombineShape<G>::cols;
+  constexpr int kSl = CombineShape<G>::slices;
+  constexpr int kPer = NT / kSl;  // columns per pass
+  static_assert(NT % kSl == 0 && 32 % kSl == 0 && kCols * kSl <= kThreads, "combine shape");
+  const float *rr = p.rec + (c0 + u) * p.rec_stride;
+  float *out = p.out + static_cast<int64_t>(u) * G * kHeadDim;
+  const int sl = t % kSl;
+  for (int col0 = 0; col0 < kCols; col0 += kPer) {
+    // every thread runs each pass, so the shuffles below see whole warps
+    const int col = col0 + t / kSl;
+    const bool have = col < kCols;
+    const int h = have ? col / (kHeadDim / 4) : 0;
+    float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float den = 0.0f;
+    if (have) {
+      for (int k0 = sl; k0 < parts; k0 += 8 * kSl) {
+        float4 x[8];
+        float dd[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int kk = k0 + k * kSl;
+          x[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          dd[k] = 0.0f;
+          if (kk < parts) {
+            const float *r = rr + static_cast<int64_t>(kk) * p.rec_stride;
+            x[k] = __ldcg(reinterpret_cast<const float4 *>(r) + col);
+            dd[k] = __ldcg(r + G * kHeadDim + h);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          num.x += x[k].x;
+          num.y += x[k].y;
+          num.z += x[k].z;
+          num.w += x[k].w;
+          den += dd[k];
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < kSl; o <<= 1) {
+      num.x += __shfl_down_sync(0xffffffffu, num.x, o);
+      num.y += __shfl_down_sync(0xffffffffu, num.y, o);
+      num.z += __shfl_down_sync(0xffffffffu, num.z, o);
+      num.w += __shfl_down_sync(0xffffffffu, num.w, o);
+      den += __shfl_down_sync(0xffffffffu, den, o);
+    }
+    if (have && sl == 0) {
+      const float z = p.c + den;
+      reinterpret_cast<float4 *>(out)[col] =
+          z != 0.0f ? make_float4(num.x / z, num.y / z, num.z / z, num.w / z)
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  }
+}
+
 template <int G, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     full_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -316,7 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_abort = misc + 1;
   volatile int *s_k_issued = misc + 2;
   volatile int *s_q_issued = misc + 3;
-  volatile int *s_varm = misc + 4;       // [W slot]: V-copy phases armed on its barrier
+  volatile int *s_final_unit = misc + 4;  // unit whose outputs the whole CTA sums at the end
+  volatile int *s_final_hist = misc + 5;  // unit whose histogram the whole CTA flushes at the end
+  volatile int *s_last = misc + 6;        // the accumulators' arrival: was this CTA the last?
+  volatile int *s_varm = misc + 7;        // [W slot]: V-copy phases armed on its barrier
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
   uint64_t *full = bars;                 // K tile landed: [stage][tile parity]
   uint64_t *empty = full + 2 * kStages;  // K tile consumed (MMA and key norms)
@@ -344,6 +418,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = static_cast<int>(te - tb);
   const int TU = static_cast<int>(p.TU);
   const int u0 = static_cast<int>(tb / p.TU), tl0 = static_cast<int>(tb - tb / p.TU * p.TU);
+
+  // TMA producer state (thread 0): it issues the first stages during the set-up below and
+  // carries on from there as warp 0's role.
+  int pr_i = 0, pr_u = u0, pr_tl = tl0, pr_seg = -1, pr_s = 0, pr_sphase = 0;
+  uint64_t pr_policy = 0;
+  // Issue K tiles (and each new unit's query rows) until tile `limit`; with `setup` set it
+  // stops before any load that would have to wait for a buffer to be handed back.
+  auto produce = [&](int limit, bool setup) {
+    for (; pr_i < ntiles && pr_i < limit; ++pr_i, next_tile(pr_tl, pr_u, TU)) {
+      if (*s_abort) break;
+      if (pr_i == 0 || pr_tl == 0) {
+        const int qb = (pr_seg + 1) & 1;
+        if (pr_seg + 1 >= 2) {
+          if (setup) break;
+          if (!mbar_wait(&qempty[qb], (((pr_seg + 1) >> 1) - 1) & 1)) {
+            set_abort(s_abort, p.flags);
+            break;
+          }
+        }
+        ++pr_seg;
+        mbar_arrive_expect_tx(&qfull[qb], 2 * G * 128);
+        const int32_t qrow = static_cast<int32_t>((pr_u / p.Hkv) * p.Hq + (pr_u % p.Hkv) * G);
+        tma_load_2d(sQ + qb * kQBufBytes, &tm_q, &qfull[qb], 0, qrow);
+        tma_load_2d(sQ + qb * kQBufBytes + kQHalfBytes, &tm_q, &qfull[qb], 64, qrow);
+        *s_q_issued = pr_seg + 1;
+      }
+      if (pr_i >= kStages) {
+        if (setup) break;
+        if (!mbar_wait(&empty[pr_s], pr_sphase ^ 1)) {
+          set_abort(s_abort, p.flags);
+          break;
+        }
+      }
+      uint64_t *fb = &full[2 * pr_s + (pr_i & 1)];
+      mbar_arrive_expect_tx(fb, C::stage_bytes);
+      const int32_t row = static_cast<int32_t>(static_cast<int64_t>(pr_u) * p.ncap) + pr_tl * kTileKeys;
+      uint8_t *st = sK + pr_s * C::stage_bytes;
+      tma_load_2d_hint(st, &tm_k, fb, 0, row, pr_policy);
+      if constexpr (KV8) {
+        // the tile's K and V scales: 128 floats each from row u of the [units, ncap] arrays
+        tma_load_2d_hint(st + C::tile_bytes, &tm_ks, fb, pr_tl * kTileKeys, pr_u, pr_policy);
+        tma_load_2d_hint(st + C::tile_bytes + C::scale_bytes, &tm_vs, fb, pr_tl * kTileKeys, pr_u,
+                         pr_policy);
+      } else {
+        tma_load_2d_hint(st + C::half_bytes, &tm_k, fb, 64, row, pr_policy);
+      }
+      *s_k_issued = pr_i + 1;
+      if (++pr_s == kStages) {
+        pr_s = 0;
+        pr_sphase ^= 1;
+      }
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -375,13 +502,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0;
     *s_k_issued = 0;
     *s_q_issued = 0;
+    *s_final_unit = -1;
+    *s_final_hist = -1;
     for (int w = 0; w < kWSlots; ++w) s_varm[w] = 0;
     fence_barrier_init();
+    // the first K stages and query rows go out now, while the CTA sets up: the stages are
+    // empty, the query buffers free, and nothing below writes where these copies land
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_q);
+    if constexpr (KV8) {
+      tma_prefetch_desc(&tm_ks);
+      tma_prefetch_desc(&tm_vs);
+    }
+    pr_policy = policy_evict_first();
+    produce(kStages, true);
   }
   // Rows G..15 of the query operand feed only MMA columns that are never read; zero
-  // them anyway so no stale bits reach the tensor core.
-  for (int i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+  // them anyway so no stale bits reach the tensor core (rows 0..G-1 are being loaded).
+  for (int i = threadIdx.x; i < 2 * 2 * (16 - G) * 8; i += kThreads) {
+    const int box = i / ((16 - G) * 8), rem = i - box * ((16 - G) * 8);
+    reinterpret_cast<uint4 *>(sQ + box * kQHalfBytes + G * 128)[rem] = make_uint4(0u, 0u, 0u, 0u);
+  }
   if constexpr (KV8)
     for (int i = threadIdx.x; i < 2 * kQ8BufBytes / 16; i += kThreads)
       reinterpret_cast<uint4 *>(sQ8)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -400,56 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_q);
-      if constexpr (KV8) {
-        tma_prefetch_desc(&tm_ks);
-        tma_prefetch_desc(&tm_vs);
-      }
-      const uint64_t policy = policy_evict_first();
-      int u = u0, tl = tl0;
-      int seg = -1;
-      int s = 0, sphase = 0;
-      for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-        if (*s_abort) break;
-        if (i == 0 || tl == 0) {
-          ++seg;
-          const int qb = seg & 1;
-          if (seg >= 2 && !mbar_wait(&qempty[qb], ((seg >> 1) - 1) & 1)) {
-            set_abort(s_abort, p.flags);
-            break;
-          }
-          mbar_arrive_expect_tx(&qfull[qb], 2 * G * 128);
-          const int32_t qrow = static_cast<int32_t>((u / p.Hkv) * p.Hq + (u % p.Hkv) * G);
-          tma_load_2d(sQ + qb * kQBufBytes, &tm_q, &qfull[qb], 0, qrow);
-          tma_load_2d(sQ + qb * kQBufBytes + kQHalfBytes, &tm_q, &qfull[qb], 64, qrow);
-          *s_q_issued = seg + 1;
-        }
-        if (i >= kStages && !mbar_wait(&empty[s], sphase ^ 1)) {
-          set_abort(s_abort, p.flags);
-          break;
-        }
-        uint64_t *fb = &full[2 * s + (i & 1)];
-        mbar_arrive_expect_tx(fb, C::stage_bytes);
-        const int32_t row = static_cast<int32_t>(static_cast<int64_t>(u) * p.ncap) + tl * kTileKeys;
-        uint8_t *st = sK + s * C::stage_bytes;
-        tma_load_2d_hint(st, &tm_k, fb, 0, row, policy);
-        if constexpr (KV8) {
-          // the tile's K and V scales: 128 floats each from row u of the [units, ncap] arrays
-          tma_load_2d_hint(st + C::tile_bytes, &tm_ks, fb, tl * kTileKeys, u, policy);
-          tma_load_2d_hint(st + C::tile_bytes + C::scale_bytes, &tm_vs, fb, tl * kTileKeys, u,
-                           policy);
-        } else {
-          tma_load_2d_hint(st + C::half_bytes, &tm_k, fb, 64, row, policy);
-        }
-        *s_k_issued = i + 1;
-        if (++s == kStages) {
-          s = 0;
-          sphase ^= 1;
-        }
-      }
-    }
+    if (lane == 0) produce(ntiles, false);
     __syncwarp();
   } else if (warp == kWarpMma || warp == kWarpMma2) {
     // ------------------------------------------------------------------ MMA issuers
@@ -754,7 +846,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicAdd(&s_hist[order_key(sg[r]) >> 21], 1u);
           }
         }
-        if (i + 1 == ntiles || tl + 1 == TU) {
+        if (i + 1 == ntiles) {
+          // the CTA's last stretch: the whole CTA flushes it once every role is done
+          __syncwarp();
+          if (lane == 0) *s_final_hist = u;
+        } else if (tl + 1 == TU) {
           __syncwarp();
           pdl_wait_primary();  // the global histogram has been zeroed
           for (int bin = lane; bin < kHistBins; bin += 32) {
@@ -969,75 +1065,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         dh += __shfl_xor_sync(0xffffffffu, dh, 2);
         den = 0.0f;
         if (aw == 0 && t == 0 && g < G) r[G * kHeadDim + g] = dh;
-        if (aw == 0 && lane == 0) reinterpret_cast<int32_t *>(r)[G * kHeadDim + G] = seg_surv;
-        seg_surv = 0;
-        // Every CTA that worked on unit u publishes its record; once the four warps have
-        // written their parts, each counts itself in for its head group, and for each head
-        // group the last CTA to count itself in sums that group over the unit's records, in
-        // CTA order, and writes its outputs.
+
+        // Every CTA that worked on unit u publishes its record and counts itself in once the
+        // four warps have written their parts; the last CTA to count itself in sums the
+        // unit's records, in CTA order, and writes the outputs: the four accumulator warps
+        // (a head group each) when the stretch ends mid-run, the whole CTA after its last
+        // stretch.
         const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
         const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
         const int parts = static_cast<int>(c1 - c0 + 1);
         __threadfence();  // each lane's part of the record is visible before the count
         named_bar_sync(kAccBar, 128);  // the whole record is written
-        pdl_wait_primary();  // the arrival counters have been zeroed
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4 + aw], 1) == parts - 1;
-        if (__shfl_sync(0xffffffffu, last, 0)) {
-          __threadfence();
-          // records of CTAs c0..c1 (other SMs wrote them: read through L2), loaded eight
-          // at a time so the loads overlap, summed in CTA order
-          constexpr int HPW = G / 4;  // heads per warp in the combine
-          const int d0 = lane * 4;
-          const float *rr = p.rec + (c0 + u) * p.rec_stride;
-          float *out = p.out + static_cast<int64_t>(u) * G * kHeadDim;
-#pragma unroll
-          for (int hh = 0; hh < HPW; ++hh) {
-            const int h = aw + 4 * hh;
-            float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            float dsum = 0.0f;
-            for (int k0 = 0; k0 < parts; k0 += 8) {
-              float4 x[8];
-              float dd[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                x[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                dd[k] = 0.0f;
-                if (k0 + k < parts) {
-                  const float *rk = rr + static_cast<int64_t>(k0 + k) * p.rec_stride;
-                  x[k] = __ldcg(reinterpret_cast<const float4 *>(rk + h * kHeadDim + d0));
-                  dd[k] = __ldcg(rk + G * kHeadDim + h);
-                }
-              }
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                num.x += x[k].x;
-                num.y += x[k].y;
-                num.z += x[k].z;
-                num.w += x[k].w;
-                dsum += dd[k];
-              }
-            }
-            const float z = p.c + dsum;
-            *reinterpret_cast<float4 *>(out + h * kHeadDim + d0) =
-                z != 0.0f ? make_float4(num.x / z, num.y / z, num.z / z, num.w / z)
-                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (aw == 0) {
+          pdl_wait_primary();  // the arrival counters have been zeroed
+          int last = 0;
+          if (lane == 0) {
+            atomicAdd(&p.n_surv[u], seg_surv);  // integer sums: the same in any order
+            last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4], 1) == parts - 1;
+            // the last to count itself in sees every record: its fence orders the record
+            // reads that follow (by any thread of the CTA, after a barrier) after the count
+            if (last) __threadfence();
+            *s_last = last;
           }
-          if (aw == 0) {
-            int32_t tot = 0;
-            for (int k = lane; k < parts; k += 32)
-              tot += __ldcg(reinterpret_cast<const int32_t *>(rr + static_cast<int64_t>(k) * p.rec_stride) +
-                            G * kHeadDim + G);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o2);
-            if (lane == 0) p.n_surv[u] = tot;
-          }
+          __syncwarp();
+        }
+        named_bar_sync(kAccBar, 128);  // the count is in
+        seg_surv = 0;
+        const bool last = *s_last != 0;
+        if (last && i + 1 == ntiles) {
+          if (aw == 0 && lane == 0) *s_final_unit = u;
+        } else if (last) {
+          combine_unit<G, 4 * 32>(p, u, c0, parts, aw * 32 + lane);
         }
       }
     }
     __syncwarp();
   }
 
+  __syncthreads();
+  // The CTA's last stretch: if it was the unit's last CTA to publish, the unit's outputs, and
+  // its histogram, with every thread of the CTA.
+  if (*s_final_unit >= 0) {
+    const int u = *s_final_unit;
+    const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
+    const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
+    combine_unit<G, kThreads>(p, u, c0, static_cast<int>(c1 - c0 + 1), threadIdx.x);
+  }
+  if (*s_final_hist >= 0) {
+    pdl_wait_primary();  // the global histogram has been zeroed
+    const int64_t hu = *s_final_hist;
+    for (int bin = threadIdx.x; bin < kHistBins; bin += kThreads) {
+      const uint32_t cnt = s_hist[bin];
+      if (cnt) atomicAdd(&p.hist[hu * kHistBins + bin], cnt);
+    }
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     // No copy may still be landing in shared memory when the CTA leaves: wait (bounded)
@@ -1066,18 +1147,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Zeroes what the decode accumulates into with atomics: the selection histogram (if any)
-// and the per-unit arrival counters.  Once the kernel before it has finished it lets the
+// Zeroes what the decode accumulates into with atomics: the selection histogram (if any),
+// the per-unit arrival counters and the survivor counts.  Once the kernel before it has finished it lets the
 // decode kernel launch; the decode waits for the zeroing only before its first histogram
 // flush and its first arrival.
 __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t hist_vecs,
-                                                        int32_t *arrivals, int64_t n_arrivals) {
+                                                        int32_t *arrivals, int64_t n_arrivals,
+                                                        int32_t *n_surv, int64_t units) {
   pdl_wait_primary();
   pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t i = t; i < hist_vecs; i += stride) hist[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int64_t i = t; i < n_arrivals; i += stride) arrivals[i] = 0;
+  for (int64_t i = t; i < units; i += stride) n_surv[i] = 0;
 }
 
 template <int G, bool KV8>
@@ -1093,7 +1176,7 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
   const int64_t zblocks = (work + 255) / 256;
   e = launch_pdl(full_zero_kernel, dim3(static_cast<unsigned>(zblocks < 1024 ? zblocks : 1024)),
                  dim3(256), 0, stream, 0u, reinterpret_cast<uint4 *>(p.hist), hist_vecs,
-                 p.arrivals, 4 * units);
+                 p.arrivals, 4 * units, p.n_surv, units);
   if (e != cudaSuccess) return e;
   return launch_pdl(full_decode_kernel<G, KV8>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
                     static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, tm_ks, tm_vs, p);

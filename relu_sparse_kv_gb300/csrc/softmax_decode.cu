@@ -282,7 +282,7 @@ struct DotsF32 {
 //        S holds, per lane, head lane/4 and rows 2(lane%4), +1 of each 8-row tile, which
 //        is exactly the B operand layout the next product needs);
 //   O^T += V^T . P^T  as MMAs with M = dims (8 tiles of 16), N = heads, K = the 16 rows.
-// P is rounded to bf16 for the second product; l sums the unrounded fp32 values.
+// P enters the second product as two bf16 parts (hi + lo); l sums the fp32 values.
 
 // 9 warps x 16 rows = 144 rows: a cluster of 8 covers 1152 (two CTAs to an SM); the wide
 // variant, 18 warps and a cluster of 4 (one CTA to an SM), takes over when 8 CTAs per unit
@@ -497,7 +497,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(W * 32, W <= kSpWar
     // rescale O^T: this lane holds heads 2t and 2t + 1, whose factors live in lanes 8t, 8t + 4
     const float sc_a = __shfl_sync(0xffffffffu, sc, 8 * t);
     const float sc_b = __shfl_sync(0xffffffffu, sc, 8 * t + 4);
-    const uint32_t pb0 = pack_bf16x2(pz[0], pz[1]), pb1 = pack_bf16x2(pz[2], pz[3]);
+    // P enters the product as two bf16 parts (hi + lo, about 16 bits), so the weights the
+    // values are summed with are the ones l sums
+    const uint32_t ph0 = pack_bf16x2(pz[0], pz[1]), ph1 = pack_bf16x2(pz[2], pz[3]);
+    const uint32_t pl0 = pack_bf16x2(pz[0] - bf16lo(ph0), pz[1] - bf16hi(ph0));
+    const uint32_t pl1 = pack_bf16x2(pz[2] - bf16lo(ph1), pz[3] - bf16hi(ph1));
     {
       const int mat = lane >> 3, mr = lane & 7;
       const int row = (mat >> 1) * 8 + mr;  // matrices: rows 0-7 / 8-15 x dims +0 / +8
@@ -511,7 +515,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(W * 32, W <= kSpWar
         o[i][3] *= sc_b;
         // A = V^T tile: a0 rows(dims) g / k rows 0-7, a1 dims g+8 / rows 0-7,
         // a2 dims g / rows 8-15, a3 dims g+8 / rows 8-15
-        mma_16816_bf16(o[i], av[0], av[1], av[2], av[3], pb0, pb1);
+        mma_16816_bf16(o[i], av[0], av[1], av[2], av[3], ph0, ph1);
+        mma_16816_bf16(o[i], av[0], av[1], av[2], av[3], pl0, pl1);
       }
     }
     __syncwarp();  // the stage is read before the next block's copies land in it
