@@ -13,12 +13,14 @@
 //   warp 0     TMA producer: the 128 query rows once; per 128-key tile the K rows (two
 //              64-column boxes, 128-byte swizzle), the tile's 128 key norms and the V rows,
 //              each in a ring of 3.  Rows past n (and query rows past T) read as zeros.
-//   warp 1     tcgen05 issuer: S = Q K^T (M 128 queries x N 128 keys, K 16 per step, fp32
-//              in one of three tensor-memory buffers), then O += P V with P read from tensor
-//              memory (the same buffer, where the epilogue wrote it over S) and V as an
-//              MN-major operand (the cached rows as they lie), fp32 in tensor memory.  S of
-//              tile t reuses the buffer of tile t - 3, whose P V is long done.
-//   warps 2-9  epilogue, one thread per (query row, half of the tile's keys).  With
+//   warp 1     tcgen05 issuer of S = Q K^T (M 128 queries x N 128 keys, K 16 per step, fp32
+//              in one of three tensor-memory buffers); S of tile t reuses the buffer of tile
+//              t - 3 once its P V is done.
+//   last warp  tcgen05 issuer of O += P V with P read from tensor memory (the same buffer,
+//              where the epilogue wrote it over S) and V as an MN-major operand (the cached
+//              rows as they lie), fp32 in tensor memory.  Two issuers, one commit per tile
+//              each: S runs ahead of P V, and every commit costs the tensor pipe time.
+//   warps 2..  epilogue, one thread per (query row, half of the tile's keys).  With
 //              s = alpha rq rk dot, w = max(s, 0)^2 = a2 * w' where a2 = alpha^2 rq^2 is the
 //              row's factor and w' = max(dot, 0)^2 * rk^2 (rq, rk > 0), so the row factor
 //              is applied once at the end: out = a2 O' / (c + a2 den'), O' = sum w' v,
@@ -49,7 +51,8 @@ constexpr int kLoTiles = EMBLA_PREFILL_LO_TILES;
 constexpr int kEpiParts = kEpiWarps / 4;          // threads per query row
 constexpr int kEpiCols = 128 / kEpiParts;         // keys of a tile per epilogue thread
 static_assert(kEpiWarps % 4 == 0 && (kEpiCols == 32 || kEpiCols == 64), "epilogue split");
-constexpr int kPThreads = (2 + kEpiWarps) * 32;
+constexpr int kWarpPV = 2 + kEpiWarps;           // the P V issuer (after the epilogue warps)
+constexpr int kPThreads = (3 + kEpiWarps) * 32;
 constexpr int kRing = 3;                 // K, V, key-norm stages and S/P buffers
 constexpr int kBox = 128 * 128;          // one [128 rows][64 bf16] box, 16 KB
 constexpr int kTileB = 2 * kBox;         // a 128 x 128 bf16 tile
@@ -58,7 +61,7 @@ constexpr int kOffK = kOffQ + kTileB;
 constexpr int kOffV = kOffK + kRing * kTileB;
 constexpr int kOffRK = kOffV + kRing * kTileB;
 constexpr int kOffBar = kOffRK + kRing * 128 * 4;
-constexpr int kNBars = 1 + 9 * kRing + 1;
+constexpr int kNBars = 1 + 7 * kRing + 1;
 constexpr int kOffMisc = kOffBar + kNBars * 8;
 constexpr int kPSmem = kOffMisc + 16 + 1024;  // + room to align the base to 1024
 static_assert(kPSmem <= 227 * 1024, "shared memory per CTA");
@@ -113,12 +116,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   float *sRK = reinterpret_cast<float *>(smem + kOffRK);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *qfull = bars;
-  uint64_t *kfull = bars + 1, *kempty = kfull + kRing;
-  uint64_t *rkfull = kempty + kRing, *rkempty = rkfull + kRing;
-  uint64_t *vfull = rkempty + kRing, *vempty = vfull + kRing;
-  uint64_t *sfull = vempty + kRing;   // S of a tile in tensor memory
+  // A K stage is free once its tile's S is done (sfull), a V stage once its P V is done
+  // (pvdone): each MMA issuer commits once per tile.
+  uint64_t *kfull = bars + 1;
+  uint64_t *rkfull = kfull + kRing, *rkempty = rkfull + kRing;
+  uint64_t *vfull = rkempty + kRing;
+  uint64_t *sfull = vfull + kRing;    // S of a tile in tensor memory; its K stage free
   uint64_t *pfull = sfull + kRing;    // its P written over it
-  uint64_t *pvdone = pfull + kRing;   // its P V done: the buffer is free
+  uint64_t *pvdone = pfull + kRing;   // its P V done: the S/P buffer and the V stage are free
   uint64_t *ofull = pvdone + kRing;
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
   uint32_t *s_tmem = misc;
@@ -140,11 +145,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     mbar_init(qfull, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&kfull[s], 1);
-      mbar_init(&kempty[s], 1);
       mbar_init(&rkfull[s], 1);
       mbar_init(&rkempty[s], kEpiWarps);
       mbar_init(&vfull[s], 1);
-      mbar_init(&vempty[s], 1);
       mbar_init(&sfull[s], 1);
       mbar_init(&pfull[s], kEpiWarps);
       mbar_init(&pvdone[s], 1);
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int kt = 0; kt < nkt; ++kt) {
         const int s = kt % kRing;
         const uint32_t ph = ((kt / kRing) - 1) & 1;
-        if (kt >= kRing && !mbar_wait(&kempty[s], ph)) {
+        if (kt >= kRing && !mbar_wait(&sfull[s], ph)) {
           set_abort_p(s_abort, p.flags);
           break;
         }
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         mbar_arrive_expect_tx(&rkfull[s], 128 * 4);
         tma_load_2d(sRK + s * 128, &tm_rk, &rkfull[s], kt * 128, u);
-        if (kt >= kRing && !mbar_wait(&vempty[s], ph)) {
+        if (kt >= kRing && !mbar_wait(&pvdone[s], ph)) {
           set_abort_p(s_abort, p.flags);
           *s_issued = 3 * kt + 2;
           break;
@@ -205,47 +208,54 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S issuer
+    // S = Q K^T of every tile, as soon as its K stage has landed and its S/P buffer is free
+    // (the P V of the tile three back is done); one commit per tile.
     if (lane == 0) {
       const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ));
       const uint64_t kdesc = smem_desc_sw128(smem_u32(sK));
       bool ok = mbar_wait(qfull, 0);
-      for (int kt = 0; ok && kt <= nkt; ++kt) {
-        if (kt < nkt) {
-          const int sb = kt % kRing;
-          ok = mbar_wait(&kfull[sb], (kt / kRing) & 1) &&
-               (kt < kRing || mbar_wait(&pvdone[sb], ((kt / kRing) - 1) & 1));
-          if (!ok) break;
-          tc_fence_after_sync();
+      for (int kt = 0; ok && kt < nkt; ++kt) {
+        const int sb = kt % kRing;
+        ok = mbar_wait(&kfull[sb], (kt / kRing) & 1) &&
+             (kt < kRing || mbar_wait(&pvdone[sb], ((kt / kRing) - 1) & 1));
+        if (!ok) break;
+        tc_fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // dims 16kk..16kk+15: 32 bytes into a 128-byte row; dims 64.. start the second box
-            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
-            tc_mma_bf16(tmem + sb * 128, qdesc + off,
-                        kdesc + static_cast<uint64_t>((sb * kTileB) >> 4) + off, kIdescS,
-                        kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&sfull[sb]);
-          tc_commit(&kempty[sb]);
+        for (int kk = 0; kk < 8; ++kk) {
+          // dims 16kk..16kk+15: 32 bytes into a 128-byte row; dims 64.. start the second box
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+          tc_mma_bf16(tmem + sb * 128, qdesc + off,
+                      kdesc + static_cast<uint64_t>((sb * kTileB) >> 4) + off, kIdescS,
+                      kk > 0 ? 1u : 0u);
         }
-        if (kt >= 1) {
-          const int t = kt - 1, pb = t % kRing;
-          ok = mbar_wait(&pfull[pb], (t / kRing) & 1) && mbar_wait(&vfull[pb], (t / kRing) & 1);
-          if (!ok) break;
-          tc_fence_after_sync();
+        tc_commit(&sfull[sb]);
+      }
+      if (!ok) set_abort_p(s_abort, p.flags);
+    }
+    __syncwarp();
+  } else if (warp == kWarpPV) {
+    // ------------------------------------------------------------------ P V issuer
+    // O += P V of every tile once its P is written and its V stage has landed; one commit
+    // per tile; at the end one more, on which every MMA of this thread has completed.
+    if (lane == 0) {
+      bool ok = true;
+      for (int t = 0; ok && t < nkt; ++t) {
+        const int pb = t % kRing;
+        ok = mbar_wait(&pfull[pb], (t / kRing) & 1) && mbar_wait(&vfull[pb], (t / kRing) & 1);
+        if (!ok) break;
+        tc_fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // keys 16kk..16kk+15: in the key group of kEpiCols keys holding them, hi takes
-            // the first kEpiCols / 2 columns and lo the next; V rows 16kk.. (2 KB apart)
-            const int grp = (16 * kk) / kEpiCols;
-            const uint32_t a_hi = tmem + pb * 128 + grp * kEpiCols + ((16 * kk) % kEpiCols) / 2;
-            const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + pb * kTileB + kk * 2048), kBox);
-            tc_mma_bf16_tmem_a(tmem + kColO, a_hi, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
-            if (t < kLoTiles) tc_mma_bf16_tmem_a(tmem + kColO, a_hi + kEpiCols / 2, vd, kIdescPV, 1u);
-          }
-          tc_commit(&pvdone[pb]);
-          tc_commit(&vempty[pb]);
+        for (int kk = 0; kk < 8; ++kk) {
+          // keys 16kk..16kk+15: in the key group of kEpiCols keys holding them, hi takes
+          // the first kEpiCols / 2 columns and lo the next; V rows 16kk.. (2 KB apart)
+          const int grp = (16 * kk) / kEpiCols;
+          const uint32_t a_hi = tmem + pb * 128 + grp * kEpiCols + ((16 * kk) % kEpiCols) / 2;
+          const uint64_t vd = smem_desc_sw128_mn(smem_u32(sV + pb * kTileB + kk * 2048), kBox);
+          tc_mma_bf16_tmem_a(tmem + kColO, a_hi, vd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          if (t < kLoTiles) tc_mma_bf16_tmem_a(tmem + kColO, a_hi + kEpiCols / 2, vd, kIdescPV, 1u);
         }
+        tc_commit(&pvdone[pb]);
       }
       if (!ok) set_abort_p(s_abort, p.flags);
       tc_commit(ofull);
@@ -310,14 +320,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_after(&rkempty[sb], used);
       // keys past this row's position weigh nothing (only tiles that reach past row 0's
-      // position need the test)
+      // position need the test): key j0 + k is masked when k > lim
       const int64_t j0 = static_cast<int64_t>(kt) * 128 + cg * kEpiCols;
       const bool masked = j0 + kEpiCols - 1 > p0;
+      const int lim = masked ? static_cast<int>(pos - j0 < kEpiCols ? pos - j0 : kEpiCols) : kEpiCols;
       // P over this thread's own S columns (already read): kEpiCols / 2 columns of hi, then
       // (in the first kLoTiles tiles) as many of lo.  One code path per case keeps the
       // registers of each to what it needs.
-      auto write_p = [&](auto with_lo) {
+      auto write_p = [&](auto with_lo, auto with_mask) {
         constexpr bool kLo = decltype(with_lo)::value;
+        constexpr bool kMask = decltype(with_mask)::value;
         uint32_t hi[kEpiCols / 2], lo[kLo ? kEpiCols / 2 : 1];
 #pragma unroll
         for (int k = 0; k < kEpiCols; k += 2) {
@@ -325,9 +337,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           float w2[2] = {fmaxf(__uint_as_float(acc[k]), 0.0f), fmaxf(__uint_as_float(acc[k + 1]), 0.0f)};
           mul_f32x2(w2[0], w2[1], w2[0], w2[1]);
           mul_f32x2(w2[0], w2[1], rk[k], rk[k + 1]);
-          if (masked) {
-            if (j0 + k > pos) w2[0] = 0.0f;
-            if (j0 + k + 1 > pos) w2[1] = 0.0f;
+          if constexpr (kMask) {
+            if (k > lim) w2[0] = 0.0f;
+            if (k + 1 > lim) w2[1] = 0.0f;
           }
           const uint32_t hb = pack_bf16x2(w2[0], w2[1]);
           hi[k >> 1] = hb;
@@ -347,10 +359,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if constexpr (kLo) tmem_store_x16(cols + 16, *reinterpret_cast<const uint32_t(*)[16]>(lo));
         }
       };
-      if (kt < kLoTiles)
-        write_p(std::true_type{});
-      else
-        write_p(std::false_type{});
+      // one code path per case (the first tile's lo, the causal mask), so the common one,
+      // hi alone and no mask, carries neither
+      if (kt < kLoTiles) {
+        if (masked)
+          write_p(std::true_type{}, std::true_type{});
+        else
+          write_p(std::true_type{}, std::false_type{});
+      } else if (masked) {
+        write_p(std::false_type{}, std::true_type{});
+      } else {
+        write_p(std::false_type{}, std::false_type{});
+      }
       tmem_wait_st();
       tc_fence_before_sync();  // P is read by the tensor cores
       __syncwarp();
