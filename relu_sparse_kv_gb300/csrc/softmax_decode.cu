@@ -297,6 +297,7 @@ template <int G, int W = kSpWarps>
 struct SpMerge {
   float m[W][G], l[W][G];
   float acc[W][G][kHeadDim];
+  float f[W][G];  // exp2(m[w][h] - the CTA's max for head h)
   float cm[G], cl[G];
   float ca[G][kHeadDim];
 };
@@ -334,25 +335,30 @@ __device__ __forceinline__ void sp_combine(SpMerge<G, W> &mg, int rank, int64_t 
   constexpr int kT = W * 32;
   cg::cluster_group cluster = cg::this_cluster();
   __syncthreads();
-  for (int i = threadIdx.x; i < G * kHeadDim; i += kT) {
-    const int h = i / kHeadDim, d = i % kHeadDim;
+  // per head: the CTA's running max and sum, and each warp's rescaling factor (once, not
+  // once per output element)
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) M = fmaxf(M, mg.m[w][h]);
-    float L = 0.0f, A = 0.0f;
-    if (M != -INFINITY) {
+    float L = 0.0f;
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float f = exp2f(mg.m[w][h] - M);
-        L = fmaf(mg.l[w][h], f, L);
-        A = fmaf(mg.acc[w][h][d], f, A);
-      }
+    for (int w = 0; w < W; ++w) {
+      const float f = M != -INFINITY ? exp2f(mg.m[w][h] - M) : 0.0f;
+      mg.f[w][h] = f;
+      L = fmaf(mg.l[w][h], f, L);
     }
+    mg.cm[h] = M;
+    mg.cl[h] = L;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kT) {
+    const int h = i / kHeadDim, d = i % kHeadDim;
+    float A = 0.0f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) A = fmaf(mg.acc[w][h][d], mg.f[w][h], A);
     mg.ca[h][d] = A;
-    if (d == 0) {
-      mg.cm[h] = M;
-      mg.cl[h] = L;
-    }
   }
   // the cluster's CTAs each finish their share of the outputs from all the CTAs' states
   cluster.sync();
@@ -407,9 +413,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(W * 32, W <= kSpWar
   const int64_t u = blockIdx.x / CL;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  const int32_t *idx = p.idx + u * p.idx_stride;
+  const int r0 = rank * p.rows_per_cta;
+  // the first block's indices are requested together with the count, not after it (entries
+  // past the count are read but not used)
+  int32_t jfirst = -1;
+  {
+    const int b = r0 + warp * kSpBlock + lane;
+    if (lane < kSpBlock && b < p.idx_stride && b < r0 + p.rows_per_cta) jfirst = idx[b];
+  }
   int cnt = p.count[u];
   cnt = cnt < 0 ? 0 : (cnt > p.idx_stride ? p.idx_stride : cnt);
-  const int32_t *idx = p.idx + u * p.idx_stride;
   const uint8_t *Ku = p.K + p.plane(u) * p.ncap * kRowBytes;
   const uint8_t *Vu = p.V + p.plane(u) * p.ncap * kRowBytes;
   const float tau2 = p.tau * kLog2e;
@@ -432,7 +446,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(W * 32, W <= kSpWar
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
 
-  const int r0 = rank * p.rows_per_cta;
   const int r1 = min(cnt, r0 + p.rows_per_cta);
   for (int b0 = r0 + warp * kSpBlock; b0 < r1; b0 += W * kSpBlock) {
     // stage: lane r < 16 looks up row r (absent past the count, or for an index outside
@@ -440,7 +453,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(W * 32, W <= kSpWar
     // 0-15 the 16 pieces of one and lanes 16-31 those of the next; absent rows are zeros
     int64_t j = -1;
     if (lane < kSpBlock && b0 + lane < r1) {
-      const int32_t jj = idx[b0 + lane];
+      const int32_t jj = b0 == r0 + warp * kSpBlock ? jfirst : idx[b0 + lane];
       if (jj < 0 || static_cast<int64_t>(jj) >= p.n)
         atomicOr(p.flags, kFlagIndexRange);
       else
