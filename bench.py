@@ -514,7 +514,11 @@ def bench_prefill(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {**static_config(args.config, args.batch, args.ctx),
-                   "launch": "one CUDA graph per call; events around each replay",
+                   "launch": f"CUDA graphs of {MLP_LAYERS} consecutive calls (one per layer of a decoder "
+                             f"step), events around the timed region; ms_per_step = its time / steps",
+                   "one_call_graph_us": round(one_call_us, 2),
+                   "one_call_graph": "median time of one call in a CUDA graph of its own (events around "
+                                     "each replay): mostly the graph's launch",
                    "l2": (f"not flushed: the steps rotate through {n_rep} copies of q, K, V and out "
                           f"({step_bytes / 1e6:.0f} MB each)" if n_rep > 1 else
                           f"not flushed: inputs and output larger than L2 ({step_bytes / 1e6:.0f} MB)")},
@@ -563,8 +567,14 @@ def run_reference_mlp(args, cfg):
     return 0
 
 
+MLP_LAYERS = 32  # calls per CUDA graph: the MLPs of a 32-layer decoder, one after another
+
+
 def bench_mlp(args, cfg):
-    """One step = one embla_relu2_mlp call: one token through the MLP."""
+    """One step = one embla_relu2_mlp call: one token through one MLP.  The calls run in CUDA
+    graphs of MLP_LAYERS consecutive calls (one per layer of a decoder step, each on its own
+    copy of the weights in turn), as a model's decode step launches them; the time of a call
+    in a graph of its own is reported beside it."""
     import numpy as np
     import torch
     import gen
@@ -600,39 +610,56 @@ def bench_mlp(args, cfg):
     assert E.embla_device_check() == 0
     assert int(reps[0]["nl"].item()) == n_live
     stream = torch.cuda.Stream(device=dev)
-    graphs = []
+
+    def capture(ncalls, first):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(ncalls):
+                call(reps[(first + i) % n_rep])
+        return g
+
+    # the timed steps: K // MLP_LAYERS replays of a graph of MLP_LAYERS calls, then one graph
+    # of the K % MLP_LAYERS calls left; a graph of a single call for comparison
+    full_n, rem_n = divmod(args.steps, MLP_LAYERS)
     with torch.cuda.stream(stream):
-        for r in reps:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                call(r)
-            graphs.append(g)
+        g_layers = capture(MLP_LAYERS, 0)
+        g_rem = capture(rem_n, MLP_LAYERS) if rem_n else None
+        g_one = [capture(1, k) for k in range(n_rep)]
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     clocks = ClockSampler(local)
     with torch.cuda.stream(stream):
+        for i in range(max(1, args.warmup // MLP_LAYERS)):
+            g_layers.replay()
         for i in range(args.warmup):
-            graphs[i % n_rep].replay()
+            g_one[i % n_rep].replay()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         t_wall0 = time.time()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            graphs[i % n_rep].replay()
-            ev[i][1].record(stream)
+        for i in range(full_n):
+            g_layers.replay()
+        if g_rem is not None:
+            g_rem.replay()
         end.record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.time()
+        one = []
+        for i in range(2 * n_rep):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g_one[i % n_rep].replay()
+            b.record(stream)
+            one.append((a, b))
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop(t_wall0, t_wall1)
     ms = max_over_ranks(start.elapsed_time(end), world, dev)
-    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     ms_per_step = ms / args.steps
+    call_ms = ms_per_step
+    one_call_us = statistics.median(a.elapsed_time(b) for a, b in one) * 1e3
     value = world / (ms_per_step * 1e-3)
     e2e = None
     if args.e2e_steps > 0:
@@ -651,13 +678,38 @@ def bench_mlp(args, cfg):
         t0 = time.perf_counter()
         for k in range(args.e2e_steps):
             e2e_step(k)
-        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        dt_eager = max_over_ranks(time.perf_counter() - t0, world, dev)
+        # the same step as one CUDA graph (copy in, call, copy out), then a host synchronise
+        e2e_graphs = []
+        with torch.cuda.stream(stream):
+            for k in range(n_rep):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    r = reps[k]
+                    r["x"].copy_(h_x, non_blocking=True)
+                    call(r)
+                    h_y.copy_(r["y"], non_blocking=True)
+                e2e_graphs.append(g)
+            for k in range(3):
+                e2e_graphs[k % n_rep].replay()
+                stream.synchronize()
+            t0 = time.perf_counter()
+            for k in range(args.e2e_steps):
+                e2e_graphs[k % n_rep].replay()
+                stream.synchronize()
+            dt = max_over_ranks(time.perf_counter() - t0, world, dev)
         e2e = {"value": world * args.e2e_steps / dt, "unit": "tokens/s",
                "h2d_bytes_per_step": d * 2, "d2h_bytes_per_step": d * 4, "steps": args.e2e_steps,
+               "launch": "per step one CUDA graph of the copy in, the public API call and the copy "
+                         "out, then a host synchronise",
+               "eager_value": world * args.e2e_steps / dt_eager,
+               "eager_launch": "the public API called from Python per step, copies issued eagerly, "
+                               "then a host synchronise",
                "inputs": "the token from pinned host memory, y back to host; weights resident"}
     peak, peak_src = _peaks()
     ach = needed / (call_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "relu2_mlp_kernel (one embla_relu2_mlp call: fused kernel + combine)",
+    roofline = {"bound": "hbm", "kernel": "relu2_mlp_kernel (one embla_relu2_mlp call: fused kernel + combine, "
+                                          "the average call of the timed graphs)",
                 "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                 "traffic": None, "algorithmic_bytes_per_launch": needed, "launch_ms": round(call_ms, 5)}
@@ -678,7 +730,11 @@ def bench_mlp(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {**static_config(args.config),
-                   "launch": "one CUDA graph per call; events around each replay",
+                   "launch": f"CUDA graphs of {MLP_LAYERS} consecutive calls (one per layer of a decoder "
+                             f"step), events around the timed region; ms_per_step = its time / steps",
+                   "one_call_graph_us": round(one_call_us, 2),
+                   "one_call_graph": "median time of one call in a CUDA graph of its own (events around "
+                                     "each replay): mostly the graph's launch",
                    "l2": f"not flushed: the steps rotate through {n_rep} copies of the weights",
                    "needed_bytes_per_step": needed,
                    "needed_gbs": round(needed / (ms_per_step * 1e-3) / 1e9, 1),

@@ -7,13 +7,15 @@
 //
 // relu2_mlp_kernel: one CTA per SM over a contiguous range of neurons, 16 warps.
 //   phase 1  each warp takes neurons in turn, two rows in flight: h_i = max(w_up_i . x, 0)^2
-//            with exact bf16 products summed in fp32 (the token x stays in registers);
-//   phase 2  the CTA's neurons with h_i > 0 are listed in ascending order; warp w owns
-//            columns d/16 w .. d/16 (w+1) - 1 of y and, for every listed neuron, reads its
-//            d/8 bytes of that neuron's down-projection row (eight rows in flight per lane):
-//            y += h_i w_down_i in fp32; the CTA's partial y goes to the workspace.
-// relu2_mlp_combine_kernel: y = the CTAs' partials summed in CTA order (eight threads per
-//            column, then a fixed-order sum of their parts), and the live-neuron count.
+//            with exact bf16 products summed in fp32 (the token x in shared memory);
+//   phase 2  the CTA's neurons with h_i > 0 are listed in ascending order; each thread owns
+//            8 columns of y and a class of listed rows (every listed row is read once, 16
+//            bytes to a thread, all of a thread's rows in flight together): y += h_i w_down_i
+//            in fp32, the classes' sums added in class order; the CTA's partial y goes to
+//            the workspace.  Every up-projection row of the CTA is prefetched into L2 when
+//            the CTA starts, and a neuron's down-projection row as soon as it fires.
+// relu2_mlp_combine_kernel: y = the CTAs' partials summed in a fixed order (8 threads per
+//            column, then their sums in order), and the live-neuron count.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -60,8 +62,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 // KC / 2 columns of y (d / 16 per warp).
 template <int KC>
 __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpParams p) {
-  pdl_wait_primary();  // the token is complete
-  pdl_launch_dependents();
   __shared__ float s_h[kMlpMaxNeuronsPerCta];
   __shared__ int32_t s_idx[kMlpMaxNeuronsPerCta];
   __shared__ float s_hl[kMlpMaxNeuronsPerCta];
@@ -70,11 +70,18 @@ __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpPara
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * p.per_cta;
   const int64_t i1 = i0 + p.per_cta < p.f ? i0 + p.per_cta : p.f;
   const int nn = i1 > i0 ? static_cast<int>(i1 - i0) : 0;
+  // The CTA's up-projection rows start moving into L2 before the wait for the kernel before
+  // this one (a prefetch reads nothing into the SM, so it is safe whatever that kernel does);
+  // the loads after the wait then find them there.
+  const uint32_t row_bytes = static_cast<uint32_t>(p.d * 2);
+  for (int a = threadIdx.x; a < nn; a += kMlpThreads) prefetch_l2_bulk(p.w_up + (i0 + a) * p.d, row_bytes);
+  pdl_wait_primary();  // the token is complete
+  pdl_launch_dependents();
 
-  // ---- phase 1: pre-activations of this CTA's neurons
-  uint4 xr[KC];
-#pragma unroll
-  for (int k = 0; k < KC; ++k) xr[k] = reinterpret_cast<const uint4 *>(p.x)[lane + 32 * k];
+  // ---- phase 1: pre-activations of this CTA's neurons (the token in shared memory)
+  __shared__ uint4 s_x[KC * 32];
+  for (int k = threadIdx.x; k < KC * 32; k += kMlpThreads) s_x[k] = reinterpret_cast<const uint4 *>(p.x)[k];
+  __syncthreads();
   for (int a = warp; a < nn; a += 2 * kMlpWarps) {
     const int b = a + kMlpWarps;  // a second row in flight
     const uint4 *ra = reinterpret_cast<const uint4 *>(p.w_up + (i0 + a) * p.d);
@@ -88,14 +95,18 @@ __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpPara
     float sa = 0.0f, sb = 0.0f;
 #pragma unroll
     for (int k = 0; k < KC; ++k) {
-      sa = dot_chunk(wa[k], xr[k], sa);
-      sb = dot_chunk(wb[k], xr[k], sb);
+      const uint4 xk = s_x[lane + 32 * k];
+      sa = dot_chunk(wa[k], xk, sa);
+      sb = dot_chunk(wb[k], xk, sb);
     }
     sa = warp_sum(sa);
     sb = warp_sum(sb);
     if (lane == 0) {
       s_h[a] = sa > 0.0f ? sa * sa : 0.0f;
       if (b < nn) s_h[b] = sb > 0.0f ? sb * sb : 0.0f;
+      // a neuron that fired: its down-projection row starts moving into L2 now
+      if (sa > 0.0f) prefetch_l2_bulk(p.w_down + (i0 + a) * p.d, row_bytes);
+      if (b < nn && sb > 0.0f) prefetch_l2_bulk(p.w_down + (i0 + b) * p.d, row_bytes);
     }
   }
   __syncthreads();
@@ -116,79 +127,95 @@ __global__ void __launch_bounds__(kMlpThreads, 1) relu2_mlp_kernel(const MlpPara
     if (lane == 0) s_nlive = cnt;
   }
   __syncthreads();
-  // ---- phase 2: this warp's columns of y over the listed rows
+  // ---- phase 2: y over the listed rows.  Thread t owns the 8 columns of 16-byte piece
+  // t % (d / 8) of a row and every listed row e with e % R == t / (d / 8), R = 512 / (d / 8)
+  // row classes; all of its rows' pieces are requested before any is used (up to 8 in
+  // flight, then the next 8), and the R class sums are added in class order.
   const int nlive = s_nlive;
-  constexpr int NC = KC / 2;  // columns per lane
-  const int64_t c0 = static_cast<int64_t>(warp) * (32 * NC) + static_cast<int64_t>(lane) * NC;
-  float y[NC];
+  constexpr int kPieces = KC * 32;          // 16-byte pieces of a row: d / 8
+  constexpr int kClasses = kMlpThreads / kPieces;
+  const int piece = threadIdx.x % kPieces, cls = threadIdx.x / kPieces;
+  float y[8];
 #pragma unroll
-  for (int c = 0; c < NC; ++c) y[c] = 0.0f;
-  for (int e0 = 0; e0 < nlive; e0 += 8) {
-    uint32_t raw[8][(NC + 1) / 2];
+  for (int c = 0; c < 8; ++c) y[c] = 0.0f;
+  for (int e0 = cls; e0 < nlive; e0 += 8 * kClasses) {
+    uint4 raw[8];
+    float hv[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-#pragma unroll
-      for (int k = 0; k < (NC + 1) / 2; ++k) raw[r][k] = 0u;
-      if (e0 + r < nlive) {
-        const uint16_t *row = p.w_down + (i0 + s_idx[e0 + r]) * p.d + c0;
-        if constexpr (NC == 4) {
-          const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(row));
-          raw[r][0] = v.x;
-          raw[r][1] = v.y;
-        } else if constexpr (NC == 2) {
-          raw[r][0] = __ldcs(reinterpret_cast<const unsigned int *>(row));
-        } else {
-          raw[r][0] = __ldcs(reinterpret_cast<const unsigned short *>(row));
-        }
+      const int e = e0 + r * kClasses;
+      raw[r] = make_uint4(0u, 0u, 0u, 0u);
+      hv[r] = 0.0f;
+      if (e < nlive) {
+        raw[r] = __ldcs(reinterpret_cast<const uint4 *>(p.w_down + (i0 + s_idx[e]) * p.d) + piece);
+        hv[r] = s_hl[e];
       }
     }
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const float hv = e0 + r < nlive ? s_hl[e0 + r] : 0.0f;
+      const uint32_t w4[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const uint32_t wv = raw[r][c >> 1];
-        const float v = (c & 1) ? bf16hi(wv) : bf16lo(wv);
-        y[c] = fmaf(hv, v, y[c]);
+      for (int c = 0; c < 4; ++c) {
+        y[2 * c] = fmaf(hv[r], bf16lo(w4[c]), y[2 * c]);
+        y[2 * c + 1] = fmaf(hv[r], bf16hi(w4[c]), y[2 * c + 1]);
       }
     }
   }
-  float *dst = p.part + static_cast<int64_t>(blockIdx.x) * p.d + c0;
+  // the class sums, added in class order
+  __shared__ float s_y[(kClasses - 1) * kPieces * 8 + 1];
+  if (cls > 0) {
 #pragma unroll
-  for (int c = 0; c < NC; ++c) dst[c] = y[c];
+    for (int c = 0; c < 8; ++c) s_y[(cls - 1) * kPieces * 8 + piece * 8 + c] = y[c];
+  }
+  __syncthreads();
+  if (cls == 0) {
+#pragma unroll
+    for (int k = 1; k < kClasses; ++k) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] += s_y[(k - 1) * kPieces * 8 + piece * 8 + c];
+    }
+    float4 *dst = reinterpret_cast<float4 *>(p.part + static_cast<int64_t>(blockIdx.x) * p.d + piece * 8);
+    dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+    dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+  }
   if (threadIdx.x == 0) p.live[blockIdx.x] = nlive;
 }
 
-// y[col] = sum over CTAs in order of part[cta][col]: thread (s, c) sums CTAs s, s + 8, ...
-// of column c, then the eight parts are added in order of s.
-__global__ void __launch_bounds__(256) relu2_mlp_combine_kernel(const float *part, const int32_t *live,
-                                                                int ctas, int64_t d, float *y,
-                                                                int32_t *n_live) {
+// y[col] = the CTAs' partials of column col summed in a fixed order: thread (s, c) of a CTA
+// (32 columns x 8 slices) sums CTAs s, s + 8, ... of column c (all of its loads in flight
+// together), then the 8 slice sums are added in slice order.  256 threads of few registers,
+// so a CTA fits beside one of the next call's relu2_mlp_kernel on an SM.
+constexpr int kCombSlices = 8;
+constexpr int kCombLoads = 20;  // loads in flight per thread: 160 CTAs per pass
+__global__ void __launch_bounds__(32 * kCombSlices) relu2_mlp_combine_kernel(const float *part,
+                                                                             const int32_t *live,
+                                                                             int ctas, int64_t d, float *y,
+                                                                             int32_t *n_live) {
   pdl_wait_primary();  // every partial is written
   pdl_launch_dependents();
-  __shared__ float s_part[8][33];
+  __shared__ float s_part[kCombSlices][33];
   const int c = threadIdx.x & 31, s = threadIdx.x >> 5;
   const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + c;
   float acc = 0.0f;
   if (col < d) {
-    for (int k0 = s; k0 < ctas; k0 += 64) {
-      float v[8];
+    for (int k0 = s; k0 < ctas; k0 += kCombSlices * kCombLoads) {
+      float v[kCombLoads];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int k = k0 + 8 * t;
+      for (int t = 0; t < kCombLoads; ++t) {
+        const int k = k0 + kCombSlices * t;
         v[t] = k < ctas ? part[static_cast<int64_t>(k) * d + col] : 0.0f;
       }
 #pragma unroll
-      for (int t = 0; t < 8; ++t) acc += v[t];
+      for (int t = 0; t < kCombLoads; ++t) acc += v[t];
     }
   }
   s_part[s][c] = acc;
   __syncthreads();
   if (s == 0 && col < d) {
-    float t = 0.0f;
+    float v = s_part[0][c];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t += s_part[k][c];
-    y[col] = t;
+    for (int k = 1; k < kCombSlices; ++k) v += s_part[k][c];
+    y[col] = v;
   }
   if (blockIdx.x == 0 && s == 1) {
     int32_t tot = 0;
@@ -237,7 +264,7 @@ cudaError_t launch_relu2_mlp(const void *x, const void *w_up, const void *w_down
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch_pdl(relu2_mlp_combine_kernel, dim3(static_cast<unsigned>((d + 31) / 32)), dim3(256),
+  return launch_pdl(relu2_mlp_combine_kernel, dim3(static_cast<unsigned>((d + 31) / 32)), dim3(32 * kCombSlices),
                     0, stream, 0u, static_cast<const float *>(p.part),
                     static_cast<const int32_t *>(p.live), ctas, d, y, n_live);
 }
