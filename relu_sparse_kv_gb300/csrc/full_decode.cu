@@ -620,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // this issuer's accumulators must be idle before the tensor memory is released
-      if (issued > 0)
-        mbar_wait(&accf[(issued - 1) % C::acc_bufs], ((issued - 1) / C::acc_bufs) & 1);
+      if (issued > 0 && !mbar_wait(&accf[(issued - 1) % C::acc_bufs], ((issued - 1) / C::acc_bufs) & 1))
+        set_abort(s_abort, p.flags);
     }
     __syncwarp();
   } else if (warp < kWarpAcc) {
@@ -1120,8 +1120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // No copy may still be landing in shared memory when the CTA leaves: wait (bounded)
+  if (threadIdx.x == 0 && *s_abort) {
+    // No copy may still be landing in shared memory when the CTA leaves.  Without an abort
+    // every copy issued was waited for by the role that used it; after one, wait (bounded)
     // for the last armed phase of every barrier that a copy completes.
     const int k_issued = *s_k_issued, q_issued = *s_q_issued;
     for (int f = 0; f < 2 * kStages; ++f) {
