@@ -406,8 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *q8full = rkempty + kNormSlots;  // E4M3 query terms written
   uint64_t *q8empty = q8full + 2;           // E4M3 query terms no longer needed
 
-  // the zeroing kernel before this one waited for everything earlier, so the selection
-  // kernel after this one may launch now (it waits for this kernel to finish)
+  // The zeroing kernel lets this kernel launch before the kernels ahead of it have finished:
+  // the set-up below touches no global memory, and thread 0 waits for them (through the
+  // zeroing kernel) before its first load; every other global access follows that load.
+  // The kernel after this one may launch now (it waits for this kernel to finish).
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -515,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_vs);
     }
     pr_policy = policy_evict_first();
+    pdl_wait_primary();  // the query, and the caches' newest rows, are written
     produce(kStages, true);
   }
   // Rows G..15 of the query operand feed only MMA columns that are never read; zero
@@ -1074,17 +1077,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
         const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
         const int parts = static_cast<int>(c1 - c0 + 1);
-        __threadfence();  // each lane's part of the record is visible before the count
         named_bar_sync(kAccBar, 128);  // the whole record is written
         if (aw == 0) {
           pdl_wait_primary();  // the arrival counters have been zeroed
           int last = 0;
           if (lane == 0) {
             atomicAdd(&p.n_surv[u], seg_surv);  // integer sums: the same in any order
+            // release: the four warps' record writes (ordered before this thread by the
+            // barrier) are visible before the count
+            fence_acq_rel_gpu();
             last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4], 1) == parts - 1;
-            // the last to count itself in sees every record: its fence orders the record
-            // reads that follow (by any thread of the CTA, after a barrier) after the count
-            if (last) __threadfence();
+            // acquire: the last to count itself in sees every record; its fence orders the
+            // record reads that follow (by any thread of the CTA, after a barrier) after it
+            if (last) fence_acq_rel_gpu();
             *s_last = last;
           }
           __syncwarp();
@@ -1149,14 +1154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Zeroes what the decode accumulates into with atomics: the selection histogram (if any),
-// the per-unit arrival counters and the survivor counts.  Once the kernel before it has finished it lets the
-// decode kernel launch; the decode waits for the zeroing only before its first histogram
-// flush and its first arrival.
+// the per-unit arrival counters and the survivor counts, once the kernel before it has
+// finished.  It lets the decode kernel launch at once, which sets up and then waits for it
+// before its first load.
 __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t hist_vecs,
                                                         int32_t *arrivals, int64_t n_arrivals,
                                                         int32_t *n_surv, int64_t units) {
-  pdl_wait_primary();
-  pdl_launch_dependents();
+  pdl_launch_dependents();  // the decode kernel sets up meanwhile; it waits for this one
+  pdl_wait_primary();       // what the earlier kernels read here is no longer needed
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t i = t; i < hist_vecs; i += stride) hist[i] = make_uint4(0u, 0u, 0u, 0u);

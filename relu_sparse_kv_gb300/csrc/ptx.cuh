@@ -234,6 +234,11 @@ __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Acquire-release fence at GPU scope: with a barrier before it, it publishes the writes of
+// every thread that reached the barrier before this thread's next atomic (release), or
+// orders this thread's later reads after an atomic it observed (acquire).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
