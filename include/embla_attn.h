@@ -346,6 +346,18 @@ embla_status embla_skip_stats(const embla_shape *shape, const float *sel_scores,
  */
 embla_status embla_device_check(uint32_t *flags, int clear, void *stream);
 
+/*
+ * Exercises the timed-out-wait path on the device without touching any kernel's
+ * data: one thread waits, through the same bounded wait the pipelined kernels
+ * use, on a shared-memory barrier that nothing arrives at, gives up after
+ * limit_us microseconds (1 .. 1,000,000, else EMBLA_ERR_INVALID_ARG) and sets
+ * bit 1 of the check word, as a kernel's timed-out wait does; the context stays
+ * usable.  With `arrive` non-zero the thread arrives first, the wait succeeds
+ * at once and nothing is set.  Asynchronous on `stream`; read the result with
+ * embla_device_check.
+ */
+embla_status embla_self_test_wait_limit(uint32_t limit_us, int arrive, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -112,6 +112,7 @@ def library() -> ctypes.CDLL:
             "embla_skip_stats": (ctypes.c_int, [P, vp, i32, vp, vp, vp]),
             "embla_device_check": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
                                                   vp]),
+            "embla_self_test_wait_limit": (ctypes.c_int, [ctypes.c_uint32, ctypes.c_int, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -424,6 +425,12 @@ def embla_skip_stats(shape: Shape, sel_scores, keys_needed, chunks_needed, chunk
     _check(chunks_needed, torch.int32, (B, Hkv), "chunks_needed")
     _call("embla_skip_stats", ctypes.byref(shape.c()), _ptr(sel_scores), chunk, _ptr(keys_needed),
           _ptr(chunks_needed), _stream(stream))
+
+
+def embla_self_test_wait_limit(limit_us: int, arrive: bool = False, stream=None):
+    """Run the bounded-wait error path on the device (see the header): a wait that nothing
+    completes gives up after limit_us and sets bit 1 of the check word."""
+    _call("embla_self_test_wait_limit", limit_us, 1 if arrive else 0, _stream(stream))
 
 
 def embla_device_check(clear: bool = True, stream=None) -> int:

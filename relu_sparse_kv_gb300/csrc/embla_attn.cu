@@ -61,6 +61,19 @@ void *symbol_address(std::atomic<void *> (&slot)[kMaxDevices], const T &symbol) 
 
 uint32_t *flags_ptr() { return static_cast<uint32_t *>(symbol_address(g_flags_addr, g_check_flags)); }
 
+// One thread waits, through the kernels' bounded wait, on a shared-memory barrier that
+// nothing arrives at; when the limit runs out it records a timed-out wait in the check
+// word, as a kernel's pipeline wait does, and returns.  If `arrive` is set the thread
+// arrives first, so the wait succeeds at once and nothing is recorded.
+__global__ void wait_limit_kernel(uint32_t *flags, uint64_t limit_ns, int arrive) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (arrive) mbar_arrive(&bar);
+  if (!mbar_wait(&bar, 0u, limit_ns)) atomicOr(flags, kFlagWaitTimeout);
+}
+
 // Device address of g_full_scratch on the current device, looked up on the first
 // call for that device and kept; nullptr if the look-up fails.
 void *full_scratch_ptr() { return symbol_address(g_scratch_addr, g_full_scratch); }
@@ -590,6 +603,15 @@ embla_status embla_skip_stats(const embla_shape *shape, const float *sel_scores,
   return cuda_status(launch_skip_stats(sel_scores, units, shape->ctx_len, shape->cache_stride,
                                        chunk, keys_needed, chunks_needed,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+embla_status embla_self_test_wait_limit(uint32_t limit_us, int arrive, void *stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return EMBLA_ERR_INVALID_ARG;
+  uint32_t *d = flags_ptr();
+  if (!d) return EMBLA_ERR_CUDA;
+  wait_limit_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      d, static_cast<uint64_t>(limit_us) * 1000ull, arrive);
+  return cuda_status(cudaGetLastError());
 }
 
 embla_status embla_device_check(uint32_t *flags, int clear, void *stream) {

@@ -414,12 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
-  const int64_t tb = split_first_tile(cta, p.T, p.P);
-  const int64_t te = split_first_tile(cta + 1, p.T, p.P);
-  // tile counts fit 32 bits: the host limits units * cache_stride to 2^31 rows
+  // the CTA's tiles [tb, te) (split_first_tile, in 32-bit arithmetic when T * P fits it:
+  // the host limits units * cache_stride to 2^31 rows, so tile numbers fit 32 bits)
+  int64_t tb, te;
+  if (((p.T * p.P) >> 32) == 0) {
+    const uint32_t T32 = static_cast<uint32_t>(p.T), P32 = static_cast<uint32_t>(p.P);
+    tb = static_cast<uint32_t>(cta) * T32 / P32;
+    te = (static_cast<uint32_t>(cta) + 1u) * T32 / P32;
+  } else {
+    tb = split_first_tile(cta, p.T, p.P);
+    te = split_first_tile(cta + 1, p.T, p.P);
+  }
   const int ntiles = static_cast<int>(te - tb);
   const int TU = static_cast<int>(p.TU);
-  const int u0 = static_cast<int>(tb / p.TU), tl0 = static_cast<int>(tb - tb / p.TU * p.TU);
+  const int u0 = static_cast<int>(static_cast<uint32_t>(tb) / static_cast<uint32_t>(TU));
+  const int tl0 = static_cast<int>(tb) - u0 * TU;
 
   // TMA producer state (thread 0): it issues the first stages during the set-up below and
   // carries on from there as warp 0's role.
@@ -475,41 +484,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[2 * s], 1);
-      mbar_init(&full[2 * s + 1], 1);
-      mbar_init(&empty[s], 5);  // MMA commit + the four norm warps
-    }
-    for (int b = 0; b < kAccBufs; ++b) {
-      mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
-    }
-    for (int q = 0; q < 2; ++q) {
-      mbar_init(&qfull[q], 1);
-      // readers of the bf16 query rows: the epilogue warps, and the MMA issuers (bf16
-      // caches) or the norm warps building the E4M3 terms (8-bit caches)
-      mbar_init(&qempty[q], 4 * kGroups + (KV8 ? 4 : kMmaWarps));
-      mbar_init(&q8full[q], 4);
-      mbar_init(&q8empty[q], kMmaWarps);
-    }
-    for (int w = 0; w < kWSlots; ++w) {
-      mbar_init(&wempty[w], p.sel != nullptr ? 5 : 4);  // accumulators (+ histogram warp)
-      mbar_init(&vfull[w], 4);
-      mbar_init(&sfull[w], 4);
-    }
-    for (int r = 0; r < kNormSlots; ++r) {
-      mbar_init(&rkfull[r], 4);
-      mbar_init(&rkempty[r], 4);
-    }
+    // The first K stages and query rows go out before anything else is set up: their
+    // barriers first, then the copies (the stages are empty, the query buffers free, and
+    // nothing below writes where these copies land).
+    for (int f = 0; f < 2 * kStages; ++f) mbar_init(&full[f], 1);
+    mbar_init(&qfull[0], 1);
+    mbar_init(&qfull[1], 1);
+    fence_barrier_init();
     *s_abort = 0;
     *s_k_issued = 0;
     *s_q_issued = 0;
-    *s_final_unit = -1;
-    *s_final_hist = -1;
-    for (int w = 0; w < kWSlots; ++w) s_varm[w] = 0;
-    fence_barrier_init();
-    // the first K stages and query rows go out now, while the CTA sets up: the stages are
-    // empty, the query buffers free, and nothing below writes where these copies land
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_q);
     if constexpr (KV8) {
@@ -519,6 +503,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     pr_policy = policy_evict_first();
     pdl_wait_primary();  // the query, and the caches' newest rows, are written
     produce(kStages, true);
+  }
+  if (warp == kWarpEpi) {
+    // the other barriers, by the lanes of another warp side by side (each lane at most one
+    // of each kind)
+    static_assert(kStages <= 32 && kAccBufs <= 32 && kWSlots <= 32 && kNormSlots <= 32,
+                  "one barrier of each kind per lane");
+    if (lane < kStages) mbar_init(&empty[lane], 5);  // MMA commit + the four norm warps
+    if (lane < kAccBufs) {
+      mbar_init(&accf[lane], 1);
+      mbar_init(&acce[lane], 4);
+    }
+    if (lane < 2) {
+      // readers of the bf16 query rows: the epilogue warps, and the MMA issuers (bf16
+      // caches) or the norm warps building the E4M3 terms (8-bit caches)
+      mbar_init(&qempty[lane], 4 * kGroups + (KV8 ? 4 : kMmaWarps));
+      mbar_init(&q8full[lane], 4);
+      mbar_init(&q8empty[lane], kMmaWarps);
+    }
+    if (lane < kWSlots) {
+      mbar_init(&wempty[lane], p.sel != nullptr ? 5 : 4);  // accumulators (+ histogram warp)
+      mbar_init(&vfull[lane], 4);
+      mbar_init(&sfull[lane], 4);
+    }
+    if (lane < kNormSlots) {
+      mbar_init(&rkfull[lane], 4);
+      mbar_init(&rkempty[lane], 4);
+    }
+    if (lane == 0) {
+      *s_final_unit = -1;
+      *s_final_hist = -1;
+    }
+    if (lane < kWSlots) s_varm[lane] = 0;
+    fence_barrier_init();
   }
   // Rows G..15 of the query operand feed only MMA columns that are never read; zero
   // them anyway so no stale bits reach the tensor core (rows 0..G-1 are being loaded).

@@ -82,6 +82,9 @@ def test_scalar_and_pointer_validation_without_gpu(lib):
     assert w(ctypes.byref(s), None, None, None, 0, 5, 10000.0, 0.1, None, None, 0, None) == 1
     assert w(ctypes.byref(s), None, None, None, 128, -1, 10000.0, 0.1, None, None, 0, None) == 1
     assert w(ctypes.byref(s), None, None, None, 128, 5, 0.0, 0.1, None, None, 0, None) == 1
+    st = lib.embla_self_test_wait_limit
+    assert st(0, 0, None) == 1  # a limit of 0 or above one second is refused before any launch
+    assert st(1000001, 0, None) == 1
 
 
 def test_empty_batch_is_a_no_op(lib):

@@ -324,3 +324,27 @@ def test_out_of_range_index_is_skipped_and_flagged():
     good = np.array([0, 1, 2, 4, 5, 6, 7], dtype=np.int32)
     ref = oracle.sparse_decode(q[0, 8:12], K[0, 2], V[0, 2], good)
     assert_close(out.cpu().numpy()[0, 8:12], ref, what="sparse output, out-of-range index skipped")
+
+
+def test_timed_out_wait_is_flagged_and_the_context_stays_usable():
+    """The bounded-wait error path: a wait that nothing completes gives up after its limit,
+    sets bit 1 of the check word and returns; the next calls run normally.  A wait that is
+    completed sets nothing."""
+    import time
+    E.embla_device_check(clear=True)
+    E.embla_self_test_wait_limit(1000, arrive=True)
+    assert E.embla_device_check(clear=True) == 0
+    t0 = time.perf_counter()
+    E.embla_self_test_wait_limit(2000)
+    flags = E.embla_device_check(clear=True)
+    waited = time.perf_counter() - t0
+    assert flags == 2
+    assert 0.002 <= waited < 5.0
+    assert E.embla_device_check(clear=True) == 0
+    # the context is intact: a full layer and its selection still match the oracle
+    fl = _layer(1, 16, 4, 3000, pattern="bernoulli", frac=0.3)
+    run = FullRun(fl)
+    ref_sig = _check_full(fl, run)
+    ref_idx, ref_cnt = oracle.select_topk_batch(ref_sig, fl.n)
+    assert np.array_equal(run.count.cpu().numpy(), ref_cnt)
+    assert E.embla_device_check(clear=True) == 0
