@@ -514,11 +514,7 @@ def bench_prefill(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {**static_config(args.config, args.batch, args.ctx),
-                   "launch": f"CUDA graphs of {MLP_LAYERS} consecutive calls (one per layer of a decoder "
-                             f"step), events around the timed region; ms_per_step = its time / steps",
-                   "one_call_graph_us": round(one_call_us, 2),
-                   "one_call_graph": "median time of one call in a CUDA graph of its own (events around "
-                                     "each replay): mostly the graph's launch",
+                   "launch": "one CUDA graph per call; events around each replay",
                    "l2": (f"not flushed: the steps rotate through {n_rep} copies of q, K, V and out "
                           f"({step_bytes / 1e6:.0f} MB each)" if n_rep > 1 else
                           f"not flushed: inputs and output larger than L2 ({step_bytes / 1e6:.0f} MB)")},
