@@ -1075,7 +1075,8 @@ def main():
     # window layer
     launches_per_step = 0
     for L in layers:
-        launches_per_step += 3 if L["per_head"] else 2  # (+ the per-head score histograms)
+        # zeroing, decode and combining kernels (+ the per-head score histograms)
+        launches_per_step += 4 if L["per_head"] else 3
         if L["qs"]:
             launches_per_step += 1 + len(L["qs"])
     launches_per_step += len(wins)
@@ -1222,7 +1223,7 @@ def main():
     wl_key = workload_name(cfg, args.batch, args.ctx).replace(" ", "_")
     achieved = [fb / (fm * 1e-3) / 1e9 for fb, fm in zip(full_bytes, full_ms)]
     ach = statistics.mean(achieved)
-    roofline = {"bound": "hbm", "kernel": "full_decode_kernel (one embla_full_decode call: zeroing kernel + decode kernel)",
+    roofline = {"bound": "hbm", "kernel": "full_decode_kernel (one embla_full_decode call: zeroing, decode and combining kernels)",
                 "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                 "traffic": _traffic_from_profile(wl_key, _kernel_digest()),

@@ -140,15 +140,14 @@ embla_status embla_full_decode_e4m3(const embla_shape *shape, const void *q,
  * device memory, one per device.
  *   Limit: when embla_full_decode_workspace_size(shape) exceeds
  *     EMBLA_FULL_DECODE_SCRATCH_BYTES the call returns EMBLA_ERR_WORKSPACE and
- *     launches nothing.  On a 152-SM device that is above about 1850 (b, g)
- *     units at G = 4 and about 850 at G = 8.
+ *     launches nothing.  On a 152-SM device that is above about 1860 (b, g)
+ *     units at G = 4 and about 860 at G = 8.
  *   Set-up: the first call on a device, made with that device current, looks
  *     up the array's device address and keeps it for later calls (a failed
  *     look-up returns EMBLA_ERR_CUDA).  Make that first call before beginning
  *     any stream capture.
- *   Zeroing: the per-unit arrival counters in the scratch must start at zero;
- *     every call zeroes them on `stream` before its decode kernel uses them.  The rest of the
- *     scratch is written before it is read and needs no initial value.
+ *   Zeroing: none needed; the scratch (the per-CTA partial records) is written
+ *     before it is read.
  *   Concurrency: all calls on one device share the one array.  Two calls that
  *     may run at the same time on the device (different streams or host
  *     threads with no ordering between them) race on it and give wrong

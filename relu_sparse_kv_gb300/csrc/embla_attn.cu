@@ -257,8 +257,7 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
     if (st == EMBLA_OK) st = cuda_status(cudaMemsetAsync(n_surv, 0, static_cast<size_t>(units) * 4, s));
     return st;
   }
-  // the launch zeroes the histogram, the arrival counters and the survivor counts itself
-  int32_t *arrivals = full_arrivals(workspace, units, G, sms);
+  // the launch zeroes the histogram and the survivor counts itself
   const uint64_t rows = static_cast<uint64_t>(units * shape->cache_stride);
   CUtensorMap tm_k, tm_q, tm_ks, tm_vs;
   const bool kmap = kv8 ? encode_rows_e4m3(&tm_k, k_cache, rows, kTileKeys)
@@ -275,7 +274,7 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
     return EMBLA_ERR_CUDA;
   st = cuda_status(launch_full_decode(G, kv8, tm_k, tm_q, kv8 ? &tm_ks : nullptr,
                                       kv8 ? &tm_vs : nullptr, v_cache, sel_scores, head_scores,
-                                      sel_hist, workspace, arrivals, out, n_surv, c, flags, sp,
+                                      sel_hist, workspace, out, n_surv, c, flags, sp,
                                       shape->ctx_len, shape->cache_stride, shape->n_q_heads,
                                       shape->n_kv_heads, alpha, eps, s));
   if (st == EMBLA_OK && head_scores)
@@ -333,8 +332,6 @@ embla_status embla_full_decode_static_scratch(const embla_shape *shape, const vo
   if (need > EMBLA_FULL_DECODE_SCRATCH_BYTES) return EMBLA_ERR_WORKSPACE;
   void *scratch = full_scratch_ptr();
   if (!scratch) return EMBLA_ERR_CUDA;
-  // The workspace call zeroes the arrival counters inside the scratch on `stream`
-  // before its decode kernel uses them.
   return embla_full_decode(shape, q, k_cache, v_cache, alpha, c, eps, out, n_surv, sel_scores,
                            sel_hist, scratch, need, stream);
 }

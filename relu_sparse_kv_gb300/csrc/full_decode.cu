@@ -27,9 +27,12 @@
 //   warps 10-13  V accumulators: O^T += V^T W as m16n8k16 bf16 MMAs over 16 survivors at
 //              a time (dims split over warps, heads as the N columns, the weights as bf16
 //              hi + lo), the denominators in fp32, in tile order; at the end of each
-//              stretch of a unit they write a partial record, and the last CTA to publish
-//              a unit's record sums its records and writes out = num / (c + den) and the
-//              survivor count.
+//              stretch of a unit they write a partial record and count the stretch's
+//              survivors into the unit's total.
+//
+// full_combine_kernel, launched after it, sums each unit's records in CTA order and writes
+// out = num / (c + den): spread over one CTA per (unit, head), so that no SM reads a whole
+// unit's records alone, and with no counting-in or fence in the decode kernel.
 //
 // 8-bit caches (E4M3 codes with one fp32 scale per token and KV head; same roles):
 //   - a stage is the 16 KB code tile (one 128-column box, 128-byte swizzle) plus the
@@ -176,8 +179,7 @@ struct FullParams {
   float *sel;        // selection scores or null
   uint32_t *hist;    // selection histogram or null
   float *hsel;       // per-head scores [B, Hq, ncap] or null
-  float *rec;        // partial records
-  int32_t *arrivals; // per unit and accumulator warp: record parts published so far (zeroed by the host call)
+  float *rec;        // partial records: one per (CTA, unit) stretch, at index cta + unit
   float *out;        // [units][G][D]
   int32_t *n_surv;   // [units]
   float c;           // normaliser constant
@@ -289,77 +291,6 @@ __device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
   }
 }
 
-// Sums the partial records of unit u (CTAs c0 .. c0 + parts - 1, each G*128 numerators and
-// G denominators) and writes out = num / (c + den), with NT threads (t = 0 .. NT-1).  Each 4-dim column of a head is split into kSl
-// slices: slice sl sums records sl, sl + kSl, ... in order, eight loads at a time, and the
-// slices (consecutive lanes) are added by a fixed shuffle tree.  The order depends only on G,
-// not on NT, so the whole CTA (after its last stretch) and the four accumulator warps
-// (mid-run) give the same bits.
-template <int G>
-struct CombineShape {
-  static constexpr int cols = G * kHeadDim / 4;    // float4 columns of the numerators
-  static constexpr int slices = G == 4 ? 4 : 2;    // cols * slices <= the CTA's threads
-};
-
-template <int G, int NT>
-__device__ __forceinline__ void combine_unit(const FullParams &p, int u, int64_t c0, int parts,
-                                             int t) {
-  constexpr int kCols = CombineShape<G>::cols;
-  constexpr int kSl = CombineShape<G>::slices;
-  constexpr int kPer = NT / kSl;  // columns per pass
-  static_assert(NT % kSl == 0 && 32 % kSl == 0 && kCols * kSl <= kThreads, "combine shape");
-  const float *rr = p.rec + (c0 + u) * p.rec_stride;
-  float *out = p.out + static_cast<int64_t>(u) * G * kHeadDim;
-  const int sl = t % kSl;
-  for (int col0 = 0; col0 < kCols; col0 += kPer) {
-    // every thread runs each pass, so the shuffles below see whole warps
-    const int col = col0 + t / kSl;
-    const bool have = col < kCols;
-    const int h = have ? col / (kHeadDim / 4) : 0;
-    float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    float den = 0.0f;
-    if (have) {
-      for (int k0 = sl; k0 < parts; k0 += 8 * kSl) {
-        float4 x[8];
-        float dd[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int kk = k0 + k * kSl;
-          x[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          dd[k] = 0.0f;
-          if (kk < parts) {
-            const float *r = rr + static_cast<int64_t>(kk) * p.rec_stride;
-            x[k] = __ldcg(reinterpret_cast<const float4 *>(r) + col);
-            dd[k] = __ldcg(r + G * kHeadDim + h);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          num.x += x[k].x;
-          num.y += x[k].y;
-          num.z += x[k].z;
-          num.w += x[k].w;
-          den += dd[k];
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 1; o < kSl; o <<= 1) {
-      num.x += __shfl_down_sync(0xffffffffu, num.x, o);
-      num.y += __shfl_down_sync(0xffffffffu, num.y, o);
-      num.z += __shfl_down_sync(0xffffffffu, num.z, o);
-      num.w += __shfl_down_sync(0xffffffffu, num.w, o);
-      den += __shfl_down_sync(0xffffffffu, den, o);
-    }
-    if (have && sl == 0) {
-      const float z = p.c + den;
-      reinterpret_cast<float4 *>(out)[col] =
-          z != 0.0f ? make_float4(num.x / z, num.y / z, num.z / z, num.w / z)
-                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
-  }
-}
-
 template <int G, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     full_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -387,9 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_abort = misc + 1;
   volatile int *s_k_issued = misc + 2;
   volatile int *s_q_issued = misc + 3;
-  volatile int *s_final_unit = misc + 4;  // unit whose outputs the whole CTA sums at the end
   volatile int *s_final_hist = misc + 5;  // unit whose histogram the whole CTA flushes at the end
-  volatile int *s_last = misc + 6;        // the accumulators' arrival: was this CTA the last?
   volatile int *s_varm = misc + 7;        // [W slot]: V-copy phases armed on its barrier
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
   uint64_t *full = bars;                 // K tile landed: [stage][tile parity]
@@ -530,10 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&rkfull[lane], 4);
       mbar_init(&rkempty[lane], 4);
     }
-    if (lane == 0) {
-      *s_final_unit = -1;
-      *s_final_hist = -1;
-    }
+    if (lane == 0) *s_final_hist = -1;
     if (lane < kWSlots) s_varm[lane] = 0;
     fence_barrier_init();
   }
@@ -1086,53 +1012,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         den = 0.0f;
         if (aw == 0 && t == 0 && g < G) r[G * kHeadDim + g] = dh;
 
-        // Every CTA that worked on unit u publishes its record and counts itself in once the
-        // four warps have written their parts; the last CTA to count itself in sums the
-        // unit's records, in CTA order, and writes the outputs: the four accumulator warps
-        // (a head group each) when the stretch ends mid-run, the whole CTA after its last
-        // stretch.
-        const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
-        const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
-        const int parts = static_cast<int>(c1 - c0 + 1);
-        named_bar_sync(kAccBar, 128);  // the whole record is written
-        if (aw == 0) {
-          pdl_wait_primary();  // the arrival counters have been zeroed
-          int last = 0;
-          if (lane == 0) {
-            atomicAdd(&p.n_surv[u], seg_surv);  // integer sums: the same in any order
-            // release: the four warps' record writes (ordered before this thread by the
-            // barrier) are visible before the count
-            fence_acq_rel_gpu();
-            last = atomicAdd(&p.arrivals[static_cast<int64_t>(u) * 4], 1) == parts - 1;
-            // acquire: the last to count itself in sees every record; its fence orders the
-            // record reads that follow (by any thread of the CTA, after a barrier) after it
-            if (last) fence_acq_rel_gpu();
-            *s_last = last;
-          }
-          __syncwarp();
+        // the stretch's survivors are counted in (integer sums: the same in any order); the
+        // records are summed by full_combine_kernel, which follows this kernel
+        if (aw == 0 && lane == 0) {
+          pdl_wait_primary();  // the survivor counts have been zeroed
+          atomicAdd(&p.n_surv[u], seg_surv);
         }
-        named_bar_sync(kAccBar, 128);  // the count is in
         seg_surv = 0;
-        const bool last = *s_last != 0;
-        if (last && i + 1 == ntiles) {
-          if (aw == 0 && lane == 0) *s_final_unit = u;
-        } else if (last) {
-          combine_unit<G, 4 * 32>(p, u, c0, parts, aw * 32 + lane);
-        }
       }
     }
     __syncwarp();
   }
 
   __syncthreads();
-  // The CTA's last stretch: if it was the unit's last CTA to publish, the unit's outputs, and
-  // its histogram, with every thread of the CTA.
-  if (*s_final_unit >= 0) {
-    const int u = *s_final_unit;
-    const int64_t c0 = split_cta_of_tile(static_cast<int64_t>(u) * TU, p.T, p.P);
-    const int64_t c1 = split_cta_of_tile(static_cast<int64_t>(u) * TU + TU - 1, p.T, p.P);
-    combine_unit<G, kThreads>(p, u, c0, static_cast<int>(c1 - c0 + 1), threadIdx.x);
-  }
+  // The histogram of the CTA's last stretch, with every thread of the CTA.
   if (*s_final_hist >= 0) {
     pdl_wait_primary();  // the global histogram has been zeroed
     const int64_t hu = *s_final_hist;
@@ -1170,20 +1063,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Zeroes what the decode accumulates into with atomics: the selection histogram (if any),
-// the per-unit arrival counters and the survivor counts, once the kernel before it has
-// finished.  It lets the decode kernel launch at once, which sets up and then waits for it
-// before its first load.
+// Zeroes what the decode accumulates into with atomics: the selection histogram (if any)
+// and the survivor counts, once the kernel before it has finished.  It lets the decode
+// kernel launch at once, which sets up and then waits for it before its first load.
 __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t hist_vecs,
-                                                        int32_t *arrivals, int64_t n_arrivals,
                                                         int32_t *n_surv, int64_t units) {
   pdl_launch_dependents();  // the decode kernel sets up meanwhile; it waits for this one
   pdl_wait_primary();       // what the earlier kernels read here is no longer needed
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t i = t; i < hist_vecs; i += stride) hist[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int64_t i = t; i < n_arrivals; i += stride) arrivals[i] = 0;
   for (int64_t i = t; i < units; i += stride) n_surv[i] = 0;
+}
+
+// out[u][h][d] = num / (c + den), num and den the sums of unit u's records (the stretches of
+// the CTAs c0 .. c1 that worked on it, records c0 + u .. c1 + u), in a fixed order.  One CTA
+// of dc x S threads per dc dims of a (unit, head) (dc = 128, 64 or 32, so that there are
+// about as many CTAs as SMs), S = the slices (a power of two, at most 8, from the records per
+// unit): thread (s, d) sums records s, s + S, s + 2S, ... of its dim (up to eight loads in
+// flight), and the S slices are added in slice order; each slice's first warp sums the
+// head's denominators the same way.
+constexpr int kCombMaxSlices = 8;
+constexpr int kCombLoads = 8;
+template <int G>
+__global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel(const FullParams p,
+                                                                                 int dc) {
+  pdl_wait_primary();  // every record is written
+  pdl_launch_dependents();
+  __shared__ float s_num[kCombMaxSlices][kHeadDim];
+  __shared__ float s_den[kCombMaxSlices];
+  const int S = static_cast<int>(blockDim.x) / dc;
+  const int per_head = kHeadDim / dc;
+  const int64_t u = blockIdx.x / (G * per_head);
+  const int h = static_cast<int>(blockIdx.x / per_head % G);
+  const int dl = static_cast<int>(threadIdx.x) % dc, sl = static_cast<int>(threadIdx.x) / dc;
+  const int d = static_cast<int>(blockIdx.x % per_head) * dc + dl;
+  const int64_t c0 = split_cta_of_tile(u * p.TU, p.T, p.P);
+  const int64_t c1 = split_cta_of_tile(u * p.TU + p.TU - 1, p.T, p.P);
+  const int parts = static_cast<int>(c1 - c0 + 1);
+  const float *rr = p.rec + (c0 + u) * p.rec_stride;
+  const int col = h * kHeadDim + d;
+  float num = 0.0f, den = 0.0f;
+  for (int k0 = sl; k0 < parts; k0 += S * kCombLoads) {
+    float x[kCombLoads], y[kCombLoads];
+#pragma unroll
+    for (int k = 0; k < kCombLoads; ++k) {
+      const int kk = k0 + k * S;
+      x[k] = kk < parts ? rr[static_cast<int64_t>(kk) * p.rec_stride + col] : 0.0f;
+      y[k] = kk < parts && dl < 32 ? rr[static_cast<int64_t>(kk) * p.rec_stride + G * kHeadDim + h] : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < kCombLoads; ++k) {
+      num += x[k];
+      den += y[k];
+    }
+  }
+  s_num[sl][dl] = num;
+  if (dl == 0) s_den[sl] = den;
+  __syncthreads();
+  if (sl == 0) {
+    float n = s_num[0][dl], z = s_den[0];
+    for (int k = 1; k < S; ++k) {
+      n += s_num[k][dl];
+      z += s_den[k];
+    }
+    z += p.c;
+    p.out[u * G * kHeadDim + col] = z != 0.0f ? n / z : 0.0f;
+  }
 }
 
 template <int G, bool KV8>
@@ -1195,14 +1141,24 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t hist_vecs = p.hist ? units * kHistBins / 4 : 0;
-  const int64_t work = hist_vecs > 4 * units ? hist_vecs : 4 * units;
+  const int64_t work = hist_vecs > units ? hist_vecs : units;
   const int64_t zblocks = (work + 255) / 256;
   e = launch_pdl(full_zero_kernel, dim3(static_cast<unsigned>(zblocks < 1024 ? zblocks : 1024)),
                  dim3(256), 0, stream, 0u, reinterpret_cast<uint4 *>(p.hist), hist_vecs,
-                 p.arrivals, 4 * units, p.n_surv, units);
+                 p.n_surv, units);
   if (e != cudaSuccess) return e;
-  return launch_pdl(full_decode_kernel<G, KV8>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
-                    static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, tm_ks, tm_vs, p);
+  e = launch_pdl(full_decode_kernel<G, KV8>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
+                 static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, tm_ks, tm_vs, p);
+  if (e != cudaSuccess) return e;
+  // slices: the records of the unit with the most, rounded up to a power of two (at most 8)
+  const int64_t most = (p.TU * p.P + p.T - 1) / p.T + 1;
+  int slices = 1;
+  while (slices < kCombMaxSlices && slices < most) slices <<= 1;
+  // dims per CTA: 128, halved (to 32 at least) while there are fewer CTAs than SMs
+  int dc = kHeadDim;
+  while (dc > 32 && units * G * (kHeadDim / dc) < p.P) dc >>= 1;
+  return launch_pdl(full_combine_kernel<G>, dim3(static_cast<unsigned>(units * G * (kHeadDim / dc))),
+                    dim3(dc * slices), 0, stream, 0u, p, dc);
 }
 
 }  // namespace
@@ -1227,18 +1183,13 @@ static size_t full_records_bytes(int64_t units, int G, int sm_count) {
 }
 
 size_t full_workspace_bytes(int64_t units, int G, int sm_count) {
-  return full_records_bytes(units, G, sm_count) + static_cast<size_t>(units) * 4 * sizeof(int32_t);
-}
-
-int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count) {
-  return reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
-                                     full_records_bytes(units, G, sm_count));
+  return full_records_bytes(units, G, sm_count);
 }
 
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
                                const void *v_cache, float *sel_scores, float *head_scores,
-                               uint32_t *sel_hist, void *workspace, int32_t *arrivals,
+                               uint32_t *sel_hist, void *workspace,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
@@ -1250,7 +1201,6 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
   p.hist = sel_hist;
   p.hsel = head_scores;
   p.rec = static_cast<float *>(workspace);
-  p.arrivals = arrivals;
   p.out = out;
   p.n_surv = n_surv;
   p.c = c;

@@ -66,14 +66,11 @@ FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count);
 int full_record_floats(int G);
 size_t full_workspace_bytes(int64_t units, int G, int sm_count);
 
-// The arrival counters (4 per unit) at the end of the full-decode workspace (zeroed per call).
-int32_t *full_arrivals(void *workspace, int64_t units, int G, int sm_count);
-
 // kv8: 8-bit E4M3 caches; tm_ks / tm_vs then map the K and V scales as [units, ncap] fp32.
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
                                const void *v_cache, float *sel_scores, float *head_scores,
-                               uint32_t *sel_hist, void *workspace, int32_t *arrivals,
+                               uint32_t *sel_hist, void *workspace,
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,

@@ -58,7 +58,7 @@ def _compare(shape, q, K, V, with_sel, alpha=1.0, c=1.0):
 
 
 @pytest.mark.parametrize("B,Hq,n,with_sel", [
-    (4, 16, 5000, True),     # units split over several CTAs: the arrival counters matter
+    (4, 16, 5000, True),     # units split over several CTAs: their records are combined
     (2, 32, 1153, True),     # G = 8, ragged last tile
     (8, 16, 300, False),     # without the selection outputs
     (1, 16, 70001, True),    # one unit over every CTA
