@@ -335,30 +335,34 @@ __device__ __forceinline__ void sp_combine(SpMerge<G, W> &mg, int rank, int64_t 
   constexpr int kT = W * 32;
   cg::cluster_group cluster = cg::this_cluster();
   __syncthreads();
-  // per head: the CTA's running max and sum, and each warp's rescaling factor (once, not
-  // once per output element)
-  if (threadIdx.x < G) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
+  // per head (warp h, lane w for the CTA's warp w): the CTA's running max and sum, and each
+  // warp's rescaling factor (once, not once per output element); the sum by a fixed
+  // shuffle tree
+  static_assert(W <= 32 && G <= W, "a lane per warp, a warp per head");
+  if (static_cast<int>(threadIdx.x >> 5) < G) {
+    const int h = threadIdx.x >> 5, w = threadIdx.x & 31;
+    const float mw = w < W ? mg.m[w][h] : -INFINITY;
+    float M = mw;
 #pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, mg.m[w][h]);
-    float L = 0.0f;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = w < W && M != -INFINITY ? exp2f(mw - M) : 0.0f;
+    if (w < W) mg.f[w][h] = f;
+    float L = w < W ? mg.l[w][h] * f : 0.0f;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float f = M != -INFINITY ? exp2f(mg.m[w][h] - M) : 0.0f;
-      mg.f[w][h] = f;
-      L = fmaf(mg.l[w][h], f, L);
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (w == 0) {
+      mg.cm[h] = M;
+      mg.cl[h] = L;
     }
-    mg.cm[h] = M;
-    mg.cl[h] = L;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < G * kHeadDim; i += kT) {
     const int h = i / kHeadDim, d = i % kHeadDim;
-    float A = 0.0f;
+    // four chains (warps w = c mod 4), added in a fixed order
+    float A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int w = 0; w < W; ++w) A = fmaf(mg.acc[w][h][d], mg.f[w][h], A);
-    mg.ca[h][d] = A;
+    for (int w = 0; w < W; ++w) A[w & 3] = fmaf(mg.acc[w][h][d], mg.f[w][h], A[w & 3]);
+    mg.ca[h][d] = (A[0] + A[1]) + (A[2] + A[3]);
   }
   // the cluster's CTAs each finish their share of the outputs from all the CTAs' states
   cluster.sync();
