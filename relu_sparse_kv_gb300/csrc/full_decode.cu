@@ -1098,8 +1098,17 @@ __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel
   const int h = static_cast<int>(blockIdx.x / per_head % G);
   const int dl = static_cast<int>(threadIdx.x) % dc, sl = static_cast<int>(threadIdx.x) / dc;
   const int d = static_cast<int>(blockIdx.x % per_head) * dc + dl;
-  const int64_t c0 = split_cta_of_tile(u * p.TU, p.T, p.P);
-  const int64_t c1 = split_cta_of_tile(u * p.TU + p.TU - 1, p.T, p.P);
+  // the unit's first and last CTA (split_cta_of_tile, in 32-bit arithmetic when T * P fits)
+  int64_t c0, c1;
+  if (((p.T * p.P) >> 32) == 0) {
+    const uint32_t T32 = static_cast<uint32_t>(p.T), P32 = static_cast<uint32_t>(p.P);
+    const uint32_t t0 = static_cast<uint32_t>(u * p.TU), t1 = t0 + static_cast<uint32_t>(p.TU) - 1u;
+    c0 = ((t0 + 1u) * P32 - 1u) / T32;
+    c1 = ((t1 + 1u) * P32 - 1u) / T32;
+  } else {
+    c0 = split_cta_of_tile(u * p.TU, p.T, p.P);
+    c1 = split_cta_of_tile(u * p.TU + p.TU - 1, p.T, p.P);
+  }
   const int parts = static_cast<int>(c1 - c0 + 1);
   const float *rr = p.rec + (c0 + u) * p.rec_stride;
   const int col = h * kHeadDim + d;
