@@ -141,20 +141,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int nkt = static_cast<int>((p0 + rows_here - 1) / 128) + 1;  // key tiles up to the last row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) {
-    mbar_init(qfull, 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&kfull[s], 1);
-      mbar_init(&rkfull[s], 1);
-      mbar_init(&rkempty[s], kEpiWarps);
-      mbar_init(&vfull[s], 1);
-      mbar_init(&sfull[s], 1);
-      mbar_init(&pfull[s], kEpiWarps);
-      mbar_init(&pvdone[s], 1);
+  if (warp == 0) {
+    // the barriers, by the warp's lanes side by side
+    static_assert(kRing <= 32, "one stage per lane");
+    if (lane < kRing) {
+      mbar_init(&kfull[lane], 1);
+      mbar_init(&rkfull[lane], 1);
+      mbar_init(&rkempty[lane], kEpiWarps);
+      mbar_init(&vfull[lane], 1);
+      mbar_init(&sfull[lane], 1);
+      mbar_init(&pfull[lane], kEpiWarps);
+      mbar_init(&pvdone[lane], 1);
     }
-    mbar_init(ofull, 1);
-    *s_abort = 0;
-    *s_issued = 0;
+    if (lane == 0) {
+      mbar_init(qfull, 1);
+      mbar_init(ofull, 1);
+      *s_abort = 0;
+      *s_issued = 0;
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -411,8 +415,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // no copy may still be landing in shared memory when the CTA leaves
+  if (threadIdx.x == 0 && *s_abort) {
+    // No copy may still be landing in shared memory when the CTA leaves.  Without an abort
+    // every copy issued was waited for by the role that used it; after one, wait (bounded)
+    // for the last armed phase of every barrier that a copy completes.
     mbar_wait(qfull, 0);
     const int issued = *s_issued;  // 3 per key tile: K, key norms, V
     const int nk = (issued + 2) / 3, nr = (issued + 1) / 3, nv = issued / 3;  // tiles of each
