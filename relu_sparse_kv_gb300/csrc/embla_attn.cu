@@ -531,9 +531,11 @@ embla_status embla_prefill(const embla_shape *shape, int64_t n_new, const void *
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return EMBLA_ERR_CUDA;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return EMBLA_ERR_CUDA;
   return cuda_status(launch_prefill(tm_q, tm_k, tm_v, tm_rk, k_cache, rk, out, flags, shape->batch,
                                     shape->n_q_heads, shape->n_kv_heads, shape->ctx_len, n_new,
-                                    shape->cache_stride, alpha, c, eps,
+                                    shape->cache_stride, alpha, c, eps, sms,
                                     static_cast<cudaStream_t>(stream)));
 }
 

@@ -107,7 +107,8 @@ size_t prefill_workspace_bytes(int64_t units, int64_t n);
 cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            const CUtensorMap &tm_rk, const void *k_cache, float *rk, float *out,
                            uint32_t *flags, int B, int Hq, int Hkv, int64_t n, int64_t T,
-                           int64_t ncap, float alpha, float c, float eps, cudaStream_t stream);
+                           int64_t ncap, float alpha, float c, float eps, int sm_count,
+                           cudaStream_t stream);
 
 // ReLU^2 MLP of one token (d in {512, 1024, 2048}; at most kMlpMaxNeuronsPerCta neurons
 // per CTA): the fused kernel's partials and live counts in the workspace, then a combine.

@@ -438,6 +438,16 @@ __device__ __forceinline__ void tmem_store_x16(uint32_t taddr, const uint32_t (&
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_store_x1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+
+__device__ __forceinline__ uint32_t tmem_load_x1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return r;
+}
+
 // Wait for this thread's tcgen05.st stores to be done.
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
