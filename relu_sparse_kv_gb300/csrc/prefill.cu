@@ -478,15 +478,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(ofree);  // the next block's P V may overwrite O
+      // out = a2 O' / (c + a2 den'): one division per row, then a multiply per output
       const float z = p.c + a2 * dsum;
+      const float f = z != 0.0f ? a2 / z : 0.0f;
       const int64_t t = static_cast<int64_t>(rb.qt) * 128 + r;
       if (t < p.T) {
         float *dst = p.out + (static_cast<int64_t>(rb.bh) * p.T + t) * kHeadDim + cg * kEpiCols;
 #pragma unroll
         for (int c = 0; c < kEpiCols; c += 4) {
-          const float4 v = z != 0.0f ? make_float4(a2 * __uint_as_float(o[c]) / z, a2 * __uint_as_float(o[c + 1]) / z,
-                                                   a2 * __uint_as_float(o[c + 2]) / z, a2 * __uint_as_float(o[c + 3]) / z)
-                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          const float4 v = make_float4(__uint_as_float(o[c]) * f, __uint_as_float(o[c + 1]) * f,
+                                       __uint_as_float(o[c + 2]) * f, __uint_as_float(o[c + 3]) * f);
           *reinterpret_cast<float4 *>(dst + c) = v;
         }
       }
