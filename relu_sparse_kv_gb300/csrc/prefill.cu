@@ -96,6 +96,7 @@ struct PrefillParams {
   uint32_t *flags;
   int64_t n, T;
   int32_t Hq, Hkv, BH, nqt, items;  // items = BH * nqt row blocks
+  int32_t out32;                     // out is 32-byte aligned (32-byte stores)
   float alpha, c, eps;
 };
 
@@ -484,11 +485,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int64_t t = static_cast<int64_t>(rb.qt) * 128 + r;
       if (t < p.T) {
         float *dst = p.out + (static_cast<int64_t>(rb.bh) * p.T + t) * kHeadDim + cg * kEpiCols;
+        // each store instruction writes one row piece per lane: 32-byte pieces fill whole
+        // sectors, with half the instructions of 16-byte ones
+        if (p.out32) {
 #pragma unroll
-        for (int c = 0; c < kEpiCols; c += 4) {
-          const float4 v = make_float4(__uint_as_float(o[c]) * f, __uint_as_float(o[c + 1]) * f,
-                                       __uint_as_float(o[c + 2]) * f, __uint_as_float(o[c + 3]) * f);
-          *reinterpret_cast<float4 *>(dst + c) = v;
+          for (int c = 0; c < kEpiCols; c += 8)
+            st_global_v8(dst + c, __uint_as_float(o[c]) * f, __uint_as_float(o[c + 1]) * f,
+                         __uint_as_float(o[c + 2]) * f, __uint_as_float(o[c + 3]) * f,
+                         __uint_as_float(o[c + 4]) * f, __uint_as_float(o[c + 5]) * f,
+                         __uint_as_float(o[c + 6]) * f, __uint_as_float(o[c + 7]) * f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kEpiCols; c += 4) {
+            const float4 v = make_float4(__uint_as_float(o[c]) * f, __uint_as_float(o[c + 1]) * f,
+                                         __uint_as_float(o[c + 2]) * f, __uint_as_float(o[c + 3]) * f);
+            *reinterpret_cast<float4 *>(dst + c) = v;
+          }
         }
       }
     }
@@ -581,6 +593,7 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k, con
   p.BH = B * Hq;
   p.nqt = static_cast<int32_t>((T + 127) / 128);
   p.items = p.BH * p.nqt;
+  p.out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.alpha = alpha;
   p.c = c;
   p.eps = eps;

@@ -438,6 +438,14 @@ __device__ __forceinline__ void tmem_store_x16(uint32_t taddr, const uint32_t (&
       : "memory");
 }
 
+// 32 bytes to global memory in one store (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float *dst, float a0, float a1, float a2, float a3,
+                                             float a4, float a5, float a6, float a7) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(a0),
+               "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_store_x1(uint32_t taddr, uint32_t r) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
 }

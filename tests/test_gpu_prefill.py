@@ -54,6 +54,23 @@ def test_prefill_matches_oracle(B, Hq, Hkv, n, T):
     assert_close(out, ref, what="prefill output")
 
 
+def test_prefill_output_only_16_byte_aligned():
+    """An output base that is 16- but not 32-byte aligned takes the 16-byte stores; the
+    results are the same and nothing is written outside the output."""
+    B, Hq, Hkv, n, T = 1, 16, 4, 700, 300
+    q, K, V = _case(5, B, Hq, Hkv, n, T)
+    shape = E.Shape(B, Hq, Hkv, D, n, n)
+    size = B * Hq * T * D
+    buf = torch.full((size + 16,), 7.0, device="cuda")
+    out = buf[4:4 + size].view(B, Hq, T, D)  # base 16 bytes past a 32-byte boundary
+    assert out.data_ptr() % 32 == 16
+    E.embla_prefill(shape, to_dev(q), to_dev(K), to_dev(V), out)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    assert (buf[:4] == 7.0).all() and (buf[4 + size:] == 7.0).all()
+    assert_close(out.cpu().numpy(), oracle.prefill_batch(q, K, V, n), what="prefill output")
+
+
 @pytest.mark.parametrize("alpha,c", [(1.0 / 128, 0.0), (0.5, 2.0), (3.0, 0.0)])
 def test_prefill_scalars(alpha, c):
     q, K, V = _case(3, 1, 16, 4, 700, 400)
