@@ -1088,8 +1088,6 @@ constexpr int kCombLoads = 8;
 template <int G>
 __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel(const FullParams p,
                                                                                  int dc) {
-  pdl_wait_primary();  // every record is written
-  pdl_launch_dependents();
   __shared__ float s_num[kCombMaxSlices][kHeadDim];
   __shared__ float s_den[kCombMaxSlices];
   const int S = static_cast<int>(blockDim.x) / dc;
@@ -1112,6 +1110,12 @@ __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel
   const int parts = static_cast<int>(c1 - c0 + 1);
   const float *rr = p.rec + (c0 + u) * p.rec_stride;
   const int col = h * kHeadDim + d;
+  // The CTA is launched while the decode kernel runs; its first record lines go to L2 (with
+  // their address translations) before the wait: a prefetch reads nothing into the SM.
+  if (sl < parts)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(rr + static_cast<int64_t>(sl) * p.rec_stride + col));
+  pdl_wait_primary();  // every record is written
+  pdl_launch_dependents();
   float num = 0.0f, den = 0.0f;
   for (int k0 = sl; k0 < parts; k0 += S * kCombLoads) {
     float x[kCombLoads], y[kCombLoads];

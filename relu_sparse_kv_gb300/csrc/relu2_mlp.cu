@@ -191,11 +191,16 @@ __global__ void __launch_bounds__(32 * kCombSlices) relu2_mlp_combine_kernel(con
                                                                              const int32_t *live,
                                                                              int ctas, int64_t d, float *y,
                                                                              int32_t *n_live) {
-  pdl_wait_primary();  // every partial is written
-  pdl_launch_dependents();
   __shared__ float s_part[kCombSlices][33];
   const int c = threadIdx.x & 31, s = threadIdx.x >> 5;
   const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + c;
+  // The CTA is launched while the main kernel runs; its partials' lines go to L2 (with their
+  // address translations) before the wait: a prefetch reads nothing into the SM.
+  if (col < d && c == 0)
+    for (int k = s; k < ctas; k += kCombSlices)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(part + static_cast<int64_t>(k) * d + col));
+  pdl_wait_primary();  // every partial is written
+  pdl_launch_dependents();
   float acc = 0.0f;
   if (col < d) {
     for (int k0 = s; k0 < ctas; k0 += kCombSlices * kCombLoads) {
