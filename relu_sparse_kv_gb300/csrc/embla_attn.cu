@@ -199,7 +199,8 @@ size_t embla_full_decode_workspace_size(const embla_shape *shape) {
   if (check_shape(shape, &G, true) != EMBLA_OK) return 0;
   const int sms = sm_count_of(current_device());
   if (sms <= 0) return 0;
-  return full_workspace_bytes(static_cast<int64_t>(shape->batch) * shape->n_kv_heads, G, sms);
+  return full_workspace_bytes(
+      full_split(static_cast<int64_t>(shape->batch) * shape->n_kv_heads, shape->ctx_len, sms), G);
 }
 
 }  // extern "C"
@@ -213,7 +214,8 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
                               bool kv8, float alpha, float c, float eps, float *out,
                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
                               void *workspace, size_t workspace_bytes, void *stream,
-                              float *head_scores = nullptr, uint32_t *head_hist = nullptr) {
+                              float *head_scores = nullptr, uint32_t *head_hist = nullptr,
+                              int max_pieces = kMaxPiecesPerCta) {
   int G = 0;
   embla_status st = check_shape(shape, &G, true);
   if (st != EMBLA_OK) return st;
@@ -239,12 +241,12 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
   const int dev = current_device();
   const int sms = sm_count_of(dev);
   if (sms <= 0) return EMBLA_ERR_CUDA;
-  if (workspace_bytes < full_workspace_bytes(units, G, sms)) return EMBLA_ERR_WORKSPACE;
+  const FullSplit sp = full_split(units, shape->ctx_len, sms, max_pieces);
+  if (workspace_bytes < full_workspace_bytes(sp, G)) return EMBLA_ERR_WORKSPACE;
   uint32_t *flags = flags_ptr();
   if (!flags) return EMBLA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  const FullSplit sp = full_split(units, shape->ctx_len, sms);
   if (sp.tiles == 0) {
     // no keys: every output is 0, nothing survives, the histogram is empty
     if (sel_scores)
@@ -328,12 +330,19 @@ embla_status embla_full_decode_static_scratch(const embla_shape *shape, const vo
   const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
   const int sms = sm_count_of(current_device());
   if (sms <= 0) return EMBLA_ERR_CUDA;
-  const size_t need = full_workspace_bytes(units, G, sms);
+  // fewer pieces per CTA (fewer records) where the usual split's records do not fit
+  int max_pieces = kMaxPiecesPerCta;
+  size_t need = full_workspace_bytes(full_split(units, shape->ctx_len, sms, max_pieces), G);
+  while (need > EMBLA_FULL_DECODE_SCRATCH_BYTES && max_pieces > 1) {
+    max_pieces -= 2;
+    need = full_workspace_bytes(full_split(units, shape->ctx_len, sms, max_pieces), G);
+  }
   if (need > EMBLA_FULL_DECODE_SCRATCH_BYTES) return EMBLA_ERR_WORKSPACE;
   void *scratch = full_scratch_ptr();
   if (!scratch) return EMBLA_ERR_CUDA;
-  return embla_full_decode(shape, q, k_cache, v_cache, alpha, c, eps, out, n_surv, sel_scores,
-                           sel_hist, scratch, need, stream);
+  return full_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, alpha, c, eps, out,
+                          n_surv, sel_scores, sel_hist, scratch, need, stream, nullptr, nullptr,
+                          max_pieces);
 }
 
 size_t embla_select_topk_workspace_size(const embla_shape *shape, int32_t topk, int32_t recent) {

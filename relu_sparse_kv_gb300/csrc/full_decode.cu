@@ -5,10 +5,13 @@
 // divided by a constant plus the sum of weights) and "Skipping V" (a value row is
 // read only when some query head of the KV group gives its key a weight above zero).
 //
-// One persistent CTA per SM walks a contiguous run of 128-key tiles of the flattened
-// (unit, tile) sequence, unit = (batch, KV head).  Warp roles:
+// One persistent CTA per SM walks its pieces of the flattened (unit, tile) sequence of
+// 128-key tiles, unit = (batch, KV head): the sequence is cut into K pieces per CTA and CTA
+// c takes pieces c, c + P, c + 2P, ... (K = 1 while a CTA's share is short), so that units
+// with many survivors are shared out.  A stretch is the part of a piece inside one unit: it
+// has its own query rows, partial record and histogram flush.  Warp roles:
 //   warp 0     TMA producer: 32 KB K tiles (two 64-column boxes, 128-byte swizzle) into
-//              a 3-stage ring; the unit's G query rows when the unit changes.
+//              a 3-stage ring; the unit's G query rows when a stretch starts.
 //   warps 1, 18  tcgen05 issuers taking alternate tiles: D[128 keys x 16] = K . Q^T
 //              (raw bf16 operands, fp32 in tensor memory), the eight 16-dim k-steps added
 //              into one accumulator of 16 columns; four tiles in flight.
@@ -30,7 +33,7 @@
 //              stretch of a unit they write a partial record and count the stretch's
 //              survivors into the unit's total.
 //
-// full_combine_kernel, launched after it, sums each unit's records in CTA order and writes
+// full_combine_kernel, launched after it, sums each unit's records in piece order and writes
 // out = num / (c + den): spread over one CTA per (unit, head), so that no SM reads a whole
 // unit's records alone, and with no counting-in or fence in the decode kernel.
 //
@@ -167,11 +170,12 @@ struct Smem {
   static constexpr int rk_off = hist_off + kHistBins * 4;
   static constexpr int vs_off = rk_off + kNormSlots * kTileKeys * 4;  // V scales beside rk
   static constexpr int misc_off = vs_off + (KV8 ? kNormSlots * kTileKeys * 4 : 0);
-  static constexpr int bar_off = misc_off + 128;
+  static constexpr int bar_off = misc_off + 128 + 16 * kMaxPiecesPerCta;
   static constexpr int n_bars = 3 * C::stages + 2 * kAccBufs + 8 + 3 * kWSlots + 2 * kNormSlots;
   static constexpr int total = bar_off + n_bars * 8;
   static constexpr int alloc = total + 1024;  // room to align the base to 1024
   static_assert(alloc <= 227 * 1024, "shared memory per CTA");
+  static_assert(misc_off % 16 == 0 && 7 + kWSlots <= 32, "misc words, then the piece table");
 };
 
 struct FullParams {
@@ -179,13 +183,13 @@ struct FullParams {
   float *sel;        // selection scores or null
   uint32_t *hist;    // selection histogram or null
   float *hsel;       // per-head scores [B, Hq, ncap] or null
-  float *rec;        // partial records: one per (CTA, unit) stretch, at index cta + unit
+  float *rec;        // partial records: one per (piece, unit) stretch, at index piece + unit
   float *out;        // [units][G][D]
   int32_t *n_surv;   // [units]
   float c;           // normaliser constant
   uint32_t *flags;
   int64_t T, TU, n, ncap;
-  int32_t P, Hq, Hkv, rec_stride;
+  int32_t P, Q, K, Hq, Hkv, rec_stride;  // CTAs, pieces (K per CTA)
   float alpha, eps;
 };
 
@@ -283,6 +287,26 @@ __device__ __forceinline__ void set_abort(volatile int *abort_flag, uint32_t *fl
   atomicOr(flags, kFlagWaitTimeout);
 }
 
+// Piece j = 0 .. K-1 of a CTA is piece q = j*P + cta of the Q = K*P, tiles
+// [floor(qT/Q), floor((q+1)T/Q)) (split_piece_start): {unit, tile in unit, tiles, q}.
+__device__ __forceinline__ int4 piece_entry(const FullParams &p, int j, int cta) {
+  const int q = j * p.P + cta;
+  int64_t b, e;
+  if (((p.T * p.Q) >> 32) == 0) {
+    // 32-bit arithmetic (the host limits units * cache_stride to 2^31 rows, so tile numbers
+    // fit 32 bits)
+    const uint32_t T32 = static_cast<uint32_t>(p.T), Q32 = static_cast<uint32_t>(p.Q);
+    b = static_cast<uint32_t>(q) * T32 / Q32;
+    e = (static_cast<uint32_t>(q) + 1u) * T32 / Q32;
+  } else {
+    b = split_piece_start(q, p.T, p.Q);
+    e = split_piece_start(q + 1, p.T, p.Q);
+  }
+  const int TU = static_cast<int>(p.TU);
+  const int u = static_cast<int>(static_cast<uint32_t>(b) / static_cast<uint32_t>(TU));
+  return make_int4(u, static_cast<int>(b) - u * TU, static_cast<int>(e - b), q);
+}
+
 // Advance (tile-in-unit, unit) to the next tile of the flattened sequence.
 __device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
   if (++tl == TU) {
@@ -291,7 +315,9 @@ __device__ __forceinline__ void next_tile(int &tl, int &u, int TU) {
   }
 }
 
-template <int G, bool KV8>
+// PIECES: K > 1 pieces per CTA (without it the walk is compiled for one piece, a CTA's
+// contiguous share).
+template <int G, bool KV8, bool PIECES>
 __global__ void __launch_bounds__(kThreads, 1)
     full_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_q,
@@ -320,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *s_q_issued = misc + 3;
   volatile int *s_final_hist = misc + 5;  // unit whose histogram the whole CTA flushes at the end
   volatile int *s_varm = misc + 7;        // [W slot]: V-copy phases armed on its barrier
+  int4 *s_piece = reinterpret_cast<int4 *>(misc + 32);  // [j]: the CTA's pieces
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
   uint64_t *full = bars;                 // K tile landed: [stage][tile parity]
   uint64_t *empty = full + 2 * kStages;  // K tile consumed (MMA and key norms)
@@ -342,33 +369,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t cta = blockIdx.x;
-  // the CTA's tiles [tb, te) (split_first_tile, in 32-bit arithmetic when T * P fits it:
-  // the host limits units * cache_stride to 2^31 rows, so tile numbers fit 32 bits)
-  int64_t tb, te;
-  if (((p.T * p.P) >> 32) == 0) {
-    const uint32_t T32 = static_cast<uint32_t>(p.T), P32 = static_cast<uint32_t>(p.P);
-    tb = static_cast<uint32_t>(cta) * T32 / P32;
-    te = (static_cast<uint32_t>(cta) + 1u) * T32 / P32;
-  } else {
-    tb = split_first_tile(cta, p.T, p.P);
-    te = split_first_tile(cta + 1, p.T, p.P);
-  }
-  const int ntiles = static_cast<int>(te - tb);
+  const int cta = static_cast<int>(blockIdx.x);
   const int TU = static_cast<int>(p.TU);
-  const int u0 = static_cast<int>(static_cast<uint32_t>(tb) / static_cast<uint32_t>(TU));
-  const int tl0 = static_cast<int>(tb) - u0 * TU;
+  const int K = PIECES ? p.K : 1;
+  // the CTA's pieces, one lane of warp 0 each, before thread 0 starts the loads
+  if (warp == kWarpProducer) {
+    if (lane < K) s_piece[lane] = piece_entry(p, lane, cta);
+    __syncwarp();
+  }
 
   // TMA producer state (thread 0): it issues the first stages during the set-up below and
   // carries on from there as warp 0's role.
-  int pr_i = 0, pr_u = u0, pr_tl = tl0, pr_seg = -1, pr_s = 0, pr_sphase = 0;
+  int pr_i = 0, pr_j = -1, pr_ib = 0, pr_ie = 0, pr_u = 0, pr_tl = 0;
+  int pr_seg = -1, pr_s = 0, pr_sphase = 0;
   uint64_t pr_policy = 0;
-  // Issue K tiles (and each new unit's query rows) until tile `limit`; with `setup` set it
+  // Issue K tiles (and each new stretch's query rows) until tile `limit`; with `setup` set it
   // stops before any load that would have to wait for a buffer to be handed back.
   auto produce = [&](int limit, bool setup) {
-    for (; pr_i < ntiles && pr_i < limit; ++pr_i, next_tile(pr_tl, pr_u, TU)) {
+    for (; pr_i < limit; ++pr_i, next_tile(pr_tl, pr_u, TU)) {
+      if (pr_i == pr_ie) {
+        // the next piece, if any
+        if (pr_j + 1 == K) break;
+        const int4 pe = s_piece[++pr_j];
+        pr_u = pe.x;
+        pr_tl = pe.y;
+        pr_ib = pr_i;
+        pr_ie = pr_i + pe.z;
+      }
       if (*s_abort) break;
-      if (pr_i == 0 || pr_tl == 0) {
+      if (pr_i == pr_ib || pr_tl == 0) {
         const int qb = (pr_seg + 1) & 1;
         if (pr_seg + 1 >= 2) {
           if (setup) break;
@@ -487,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) produce(ntiles, false);
+    if (lane == 0) produce(INT32_MAX, false);
     __syncwarp();
   } else if (warp == kWarpMma || warp == kWarpMma2) {
     // ------------------------------------------------------------------ MMA issuers
@@ -504,66 +533,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(sK));
       const uint64_t qdesc0 = smem_desc_sw128(smem_u32(KV8 ? sQ8 : sQ));
       uint64_t qdesc = qdesc0;
-      int tl = tl0, seg = -1, qb = 0, issued = 0;
+      int seg = -1, qb = 0, issued = 0;
       int s = 0, b = 0, bphase = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        if (*s_abort) break;
-        if (i == 0 || tl == 0) {
-          ++seg;
-          qb = seg & 1;
-          qdesc = qdesc0 + static_cast<uint64_t>((qb * qbuf_bytes) >> 4);
-          if (!mbar_wait(&qf[qb], (seg >> 1) & 1)) {
+      int i = 0;
+      for (int pc = 0; pc < K; ++pc) {
+        const int4 pe = s_piece[pc];
+        int tl = pe.y;
+        const int ib = i, ie = i + pe.z;
+        for (; i < ie; ++i) {
+          if (*s_abort) break;
+          if (i == ib || tl == 0) {
+            ++seg;
+            qb = seg & 1;
+            qdesc = qdesc0 + static_cast<uint64_t>((qb * qbuf_bytes) >> 4);
+            if (!mbar_wait(&qf[qb], (seg >> 1) & 1)) {
+              set_abort(s_abort, p.flags);
+              break;
+            }
+          }
+          if ((i & 1) != mw) {
+            // not this issuer's tile; it still hands back the query buffer at a stretch's end
+            if (i + 1 == ie || tl + 1 == TU) tc_commit(&qe[qb]);
+            if (++tl == TU) tl = 0;
+            if (++s == kStages) s = 0;
+            if (++b == C::acc_bufs) {
+              b = 0;
+              bphase ^= 1;
+            }
+            continue;
+          }
+          if (!mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) ||
+              (i >= C::acc_bufs && !mbar_wait(&acce[b], bphase ^ 1))) {
             set_abort(s_abort, p.flags);
             break;
           }
-        }
-        if ((i & 1) != mw) {
-          // not this issuer's tile; it still hands back the query buffer at a unit's end
-          if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qe[qb]);
+          tc_fence_after_sync();
+          const uint64_t adesc = kdesc0 + static_cast<uint64_t>((s * C::stage_bytes) >> 4);
+          const uint32_t dcol = tmem + b * C::acc_cols;
+  #pragma unroll
+          for (int kk = 0; kk < C::ksteps; ++kk) {
+            if constexpr (KV8) {
+              // scores over dims 32kk..32kk+31 added into D[key][t*G + h] = code . t_th, and
+              // codes . codes^T into the next 128 columns; k-step kk is 32 bytes into the
+              // 128-byte rows of codes and of terms
+              const uint64_t a = adesc + ((kk * 32) >> 4);
+              tc_mma_e4m3(dcol, a, qdesc + ((kk * 32) >> 4), C::idesc, kk > 0 ? 1u : 0u);
+              tc_mma_e4m3(dcol + C::score_cols, a, a, C::idesc_diag, kk > 0 ? 1u : 0u);
+            } else {
+              // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is
+              // 32 bytes into a 128-byte row, the second half of the dims starts a new box
+              tc_mma_bf16(dcol,
+                          adesc + (((kk >> 2) * C::half_bytes + (kk & 3) * 32) >> 4),
+                          qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), C::idesc,
+                          kk > 0 ? 1u : 0u);
+            }
+          }
+          tc_commit(&accf[b]);
+          tc_commit(&empty[s]);
+          issued = i + 1;
+          if (i + 1 == ie || tl + 1 == TU) tc_commit(&qe[qb]);
           if (++tl == TU) tl = 0;
           if (++s == kStages) s = 0;
           if (++b == C::acc_bufs) {
             b = 0;
             bphase ^= 1;
           }
-          continue;
         }
-        if (!mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) ||
-            (i >= C::acc_bufs && !mbar_wait(&acce[b], bphase ^ 1))) {
-          set_abort(s_abort, p.flags);
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t adesc = kdesc0 + static_cast<uint64_t>((s * C::stage_bytes) >> 4);
-        const uint32_t dcol = tmem + b * C::acc_cols;
-#pragma unroll
-        for (int kk = 0; kk < C::ksteps; ++kk) {
-          if constexpr (KV8) {
-            // scores over dims 32kk..32kk+31 added into D[key][t*G + h] = code . t_th, and
-            // codes . codes^T into the next 128 columns; k-step kk is 32 bytes into the
-            // 128-byte rows of codes and of terms
-            const uint64_t a = adesc + ((kk * 32) >> 4);
-            tc_mma_e4m3(dcol, a, qdesc + ((kk * 32) >> 4), C::idesc, kk > 0 ? 1u : 0u);
-            tc_mma_e4m3(dcol + C::score_cols, a, a, C::idesc_diag, kk > 0 ? 1u : 0u);
-          } else {
-            // partial scores over dims 16kk..16kk+15: D_kk[key][h] = k . q_h; k-step kk is
-            // 32 bytes into a 128-byte row, the second half of the dims starts a new box
-            tc_mma_bf16(dcol,
-                        adesc + (((kk >> 2) * C::half_bytes + (kk & 3) * 32) >> 4),
-                        qdesc + (((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4), C::idesc,
-                        kk > 0 ? 1u : 0u);
-          }
-        }
-        tc_commit(&accf[b]);
-        tc_commit(&empty[s]);
-        issued = i + 1;
-        if (i + 1 == ntiles || tl + 1 == TU) tc_commit(&qe[qb]);
-        if (++tl == TU) tl = 0;
-        if (++s == kStages) s = 0;
-        if (++b == C::acc_bufs) {
-          b = 0;
-          bphase ^= 1;
-        }
+        if (i < ie) break;  // stopped early
       }
       // this issuer's accumulators must be idle before the tensor memory is released
       if (issued > 0 && !mbar_wait(&accf[(issued - 1) % C::acc_bufs], ((issued - 1) / C::acc_bufs) & 1))
@@ -587,178 +623,192 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group keeps the same copy (they all see every count), so no warp waits for another.
     uint8_t *gring = sRing + group * kGroupRing * C::ring_pitch;
     int issued = 0, m1 = 0, m2 = 0, m3 = 0;
-    int u = u0, tl = tl0;
     int seg = -1;
-    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-      if (i == 0 || tl == 0) {
-        // every epilogue warp takes the new unit's query norms, whichever tiles it owns
-        ++seg;
-        const int qb = seg & 1;
-        const bool ok = !*s_abort && mbar_wait(&qfull[qb], (seg >> 1) & 1);
+    int i = 0;
+    for (int pc = 0; pc < K; ++pc) {
+      const int4 pe = s_piece[pc];
+      int u = pe.x, tl = pe.y;
+      const int ib = i, ie = i + pe.z;
+      for (; i < ie; ++i, next_tile(tl, u, TU)) {
+        if (i == ib || tl == 0) {
+          // every epilogue warp takes the new stretch's query norms, whichever tiles it owns
+          ++seg;
+          const int qb = seg & 1;
+          const bool ok = !*s_abort && mbar_wait(&qfull[qb], (seg >> 1) & 1);
+          if (!named_bar_and(gbar, 128, ok)) {
+            set_abort(s_abort, p.flags);
+            break;
+          }
+          {
+            // alpha / sqrt(mean(q_h^2) + eps): 32 / G neighbouring lanes per head, each summing
+            // 16-byte chunks of the head's row (the swizzle only permutes chunks within a
+            // 128-byte row, which a sum does not see), then every lane takes every head's
+            constexpr int kLanesPerHead = 32 / G, kChunks = 16 / kLanesPerHead;
+            static_assert(32 % G == 0 && kChunks * kLanesPerHead == 16, "chunks per lane");
+            const int hq = lane / kLanesPerHead, sub = lane % kLanesPerHead;
+            float ss = 0.0f, mx = 0.0f;
+  #pragma unroll
+            for (int k = 0; k < kChunks; ++k) {
+              const int c = sub * kChunks + k;
+              const uint4 x = *reinterpret_cast<const uint4 *>(sQ + qb * kQBufBytes + (c >> 3) * kQHalfBytes +
+                                                               hq * 128 + (c & 7) * 16);
+              ss += sumsq8(x);
+              if constexpr (KV8) mx = fmaxf(mx, maxabs8(x));
+            }
+  #pragma unroll
+            for (int o = kLanesPerHead / 2; o > 0; o >>= 1) {
+              ss += __shfl_xor_sync(0xffffffffu, ss, o);
+              if constexpr (KV8) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            float a = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            // the E4M3 terms hold q / 2^e: put the 2^e back here
+            if constexpr (KV8) a *= pow2f(q8_exponent(mx));
+  #pragma unroll
+            for (int h = 0; h < G; ++h) aq[h] = __shfl_sync(0xffffffffu, a, h * kLanesPerHead);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qempty[qb]);
+        }
+        if (static_cast<int>(i % kGroups) != group) continue;
+        const int b = static_cast<int>(i % C::acc_bufs);
+        const int slot = static_cast<int>(i % kWSlots);
+        const int ns = static_cast<int>(i % kNormSlots);
+        const bool ok = !*s_abort && mbar_wait(&accf[b], (i / C::acc_bufs) & 1) &&
+                        mbar_wait(&rkfull[ns], (i / kNormSlots) & 1) &&
+                        (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
         if (!named_bar_and(gbar, 128, ok)) {
           set_abort(s_abort, p.flags);
           break;
         }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float ss = 0.0f, mx = 0.0f;
-          if (lane < 16) {
-            const uint4 x = *reinterpret_cast<const uint4 *>(sQ + qb * kQBufBytes +
-                                                             (lane >> 3) * kQHalfBytes + h * 128 +
-                                                             (lane & 7) * 16);
-            ss = sumsq8(x);
-            if constexpr (KV8) mx = maxabs8(x);
+        float dot[G];
+        tc_fence_after_sync();
+        float ssq = 0.0f;  // 8-bit caches: this key's sum of squared codes
+        if constexpr (KV8) {
+          // columns t*G + h of the score accumulator; then this warp's 32 x 32 block of
+          // codes . codes^T, whose diagonal entry for this lane is its key's sum of squares
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
+          uint32_t r[3 * G];
+          uint32_t dg[32];
+          if constexpr (G == 4) {
+            tmem_load_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+            tmem_load_x4(taddr + 8, *reinterpret_cast<uint32_t(*)[4]>(&r[8]));
+          } else {
+            tmem_load_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+            tmem_load_x8(taddr + 16, *reinterpret_cast<uint32_t(*)[8]>(&r[16]));
           }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if constexpr (KV8) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          tmem_load_x32(taddr + C::score_cols + quarter * 32, dg);
+          tmem_wait_ld(r);
+          tmem_wait_ld(dg);
+  #pragma unroll
+          for (int h = 0; h < G; ++h)  // t1 + t2 / 16 + t3 / 256 (the scalings are exact)
+            dot[h] = (__uint_as_float(r[2 * G + h]) * 0.0625f + __uint_as_float(r[G + h])) * 0.0625f +
+                     __uint_as_float(r[h]);
+          // dg[lane] by halving: keep the upper half of the candidates where this lane's bit is set
+  #pragma unroll
+          for (int k = 16; k >= 1; k >>= 1) {
+  #pragma unroll
+            for (int e = 0; e < k; ++e) dg[e] = (lane & k) ? dg[e + k] : dg[e];
           }
-          aq[h] = p.alpha * rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-          // the E4M3 terms hold q / 2^e: put the 2^e back here
-          if constexpr (KV8) aq[h] *= pow2f(q8_exponent(mx));
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[qb]);
-      }
-      if (static_cast<int>(i % kGroups) != group) continue;
-      const int b = static_cast<int>(i % C::acc_bufs);
-      const int slot = static_cast<int>(i % kWSlots);
-      const int ns = static_cast<int>(i % kNormSlots);
-      const bool ok = !*s_abort && mbar_wait(&accf[b], (i / C::acc_bufs) & 1) &&
-                      mbar_wait(&rkfull[ns], (i / kNormSlots) & 1) &&
-                      (i < kWSlots || mbar_wait(&wempty[slot], ((i / kWSlots) - 1) & 1));
-      if (!named_bar_and(gbar, 128, ok)) {
-        set_abort(s_abort, p.flags);
-        break;
-      }
-      float dot[G];
-      tc_fence_after_sync();
-      float ssq = 0.0f;  // 8-bit caches: this key's sum of squared codes
-      if constexpr (KV8) {
-        // columns t*G + h of the score accumulator; then this warp's 32 x 32 block of
-        // codes . codes^T, whose diagonal entry for this lane is its key's sum of squares
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
-        uint32_t r[3 * G];
-        uint32_t dg[32];
-        if constexpr (G == 4) {
-          tmem_load_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
-          tmem_load_x4(taddr + 8, *reinterpret_cast<uint32_t(*)[4]>(&r[8]));
+          ssq = __uint_as_float(dg[0]);
         } else {
-          tmem_load_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-          tmem_load_x8(taddr + 16, *reinterpret_cast<uint32_t(*)[8]>(&r[16]));
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
+          uint32_t r[G];
+          if constexpr (G == 4)
+            tmem_load_x4(taddr, *reinterpret_cast<uint32_t(*)[4]>(&r[0]));
+          else
+            tmem_load_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_wait_ld(r);
+  #pragma unroll
+          for (int h = 0; h < G; ++h) dot[h] = __uint_as_float(r[h]);
         }
-        tmem_load_x32(taddr + C::score_cols + quarter * 32, dg);
-        tmem_wait_ld(r);
-        tmem_wait_ld(dg);
-#pragma unroll
-        for (int h = 0; h < G; ++h)  // t1 + t2 / 16 + t3 / 256 (the scalings are exact)
-          dot[h] = (__uint_as_float(r[2 * G + h]) * 0.0625f + __uint_as_float(r[G + h])) * 0.0625f +
-                   __uint_as_float(r[h]);
-        // dg[lane] by halving: keep the upper half of the candidates where this lane's bit is set
-#pragma unroll
-        for (int k = 16; k >= 1; k >>= 1) {
-#pragma unroll
-          for (int e = 0; e < k; ++e) dg[e] = (lane & k) ? dg[e + k] : dg[e];
-        }
-        ssq = __uint_as_float(dg[0]);
-      } else {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * C::acc_cols;
-        uint32_t r[G];
-        if constexpr (G == 4)
-          tmem_load_x4(taddr, *reinterpret_cast<uint32_t(*)[4]>(&r[0]));
-        else
-          tmem_load_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
-        tmem_wait_ld(r);
-#pragma unroll
-        for (int h = 0; h < G; ++h) dot[h] = __uint_as_float(r[h]);
-      }
-      tc_fence_before_sync();
-      // bf16: the key norm; 8-bit: the key's scale ks, whose norm follows from the sum of
-      // squared codes: ks / sqrt(ks^2 mean(code^2) + eps)
-      const float rkv = s_rk[ns * kTileKeys + row];
-      const float vsc = KV8 ? s_vs[ns * kTileKeys + row] : 0.0f;
-      // every lane's reads are back
-      const float rk_used = __shfl_sync(0xffffffffu, KV8 ? rkv + vsc : rkv, 31);
-      const float rk = KV8 ? rkv * rsqrtf(rkv * rkv * (ssq * (1.0f / kHeadDim)) + p.eps) : rkv;
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&acce[b]);
-        mbar_arrive_after(&rkempty[ns], rk_used);
-      }
-
-      const int j = tl * kTileKeys + row;
-      const bool valid = j < p.n;
-      float sc[G];
-      float sigma = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        sc[h] = dot[h] * aq[h] * rk;
-        sigma = fmaxf(sigma, sc[h]);
-      }
-      if (p.hsel != nullptr && valid) {
-        // every head's own score, for a selection per query head
-        float *hs = p.hsel + (static_cast<int64_t>(u / p.Hkv) * p.Hq + (u % p.Hkv) * G) * p.ncap + j;
-#pragma unroll
-        for (int h = 0; h < G; ++h) hs[h * p.ncap] = sc[h];
-      }
-      WSlot<G, KV8> &ws = wslots[slot];
-      if (p.sel != nullptr) {
-        ws.sig[row] = sigma;
+        tc_fence_before_sync();
+        // bf16: the key norm; 8-bit: the key's scale ks, whose norm follows from the sum of
+        // squared codes: ks / sqrt(ks^2 mean(code^2) + eps)
+        const float rkv = s_rk[ns * kTileKeys + row];
+        const float vsc = KV8 ? s_vs[ns * kTileKeys + row] : 0.0f;
+        // every lane's reads are back
+        const float rk_used = __shfl_sync(0xffffffffu, KV8 ? rkv + vsc : rkv, 31);
+        const float rk = KV8 ? rkv * rsqrtf(rkv * rkv * (ssq * (1.0f / kHeadDim)) + p.eps) : rkv;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sfull[slot]);
-      }
-      const bool surv = valid && sigma > 0.0f;
-      const uint32_t bal = __ballot_sync(0xffffffffu, surv);
-      if (lane == 0) ws.cnt[quarter] = __popc(bal);
-      __syncwarp();
-      named_bar_sync(gbar, 128);  // the four counts are in
-      int off = 0, m = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = ws.cnt[q];
-        m += c;
-        off += q < quarter ? c : 0;
-      }
-      const int e = off + __popc(bal & lanemask_lt);  // this key's place in the tile's list
-      if (surv) {
-        ws.key[e] = j;
-#pragma unroll
-        for (int h = 0; h < G; ++h) ws.w[e][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
-        if constexpr (KV8) ws.vs[e] = vsc;
-      }
-      // m rows of the group's ring, in the group's tile order.  Tiles i - 8 and older
-      // were consumed before this tile's slot was taken; wait, oldest first, for the
-      // group's later tiles until the rows in use leave room for m.
-      bool rok = true;
-      if (m1 + m2 + m3 + m > kGroupRing && i >= 6)
-        rok = mbar_wait(&wempty[(i - 6) % kWSlots], ((i - 6) / kWSlots) & 1);
-      if (rok && m1 + m2 + m > kGroupRing && i >= 4)
-        rok = mbar_wait(&wempty[(i - 4) % kWSlots], ((i - 4) / kWSlots) & 1);
-      if (rok && m1 + m > kGroupRing && i >= 2)
-        rok = mbar_wait(&wempty[(i - 2) % kWSlots], ((i - 2) / kWSlots) & 1);
-      const int row0 = issued & (kGroupRing - 1);
-      issued += m;
-      m3 = m2;
-      m2 = m1;
-      m1 = m;
-      if (!rok) {
-        // no barrier follows in this tile: the group stops together at the next one
-        set_abort(s_abort, p.flags);
-        continue;
-      }
-      if (lane == 0) {
-        if (quarter == 0) {
-          ws.row0 = row0;
-          ws.m = m;
+        if (lane == 0) {
+          mbar_arrive(&acce[b]);
+          mbar_arrive_after(&rkempty[ns], rk_used);
         }
-        mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(__popc(bal) * kRowBytes));
-        if (quarter == 0) s_varm[slot] = s_varm[slot] + 1;
+
+        const int j = tl * kTileKeys + row;
+        const bool valid = j < p.n;
+        float sc[G];
+        float sigma = -INFINITY;
+  #pragma unroll
+        for (int h = 0; h < G; ++h) {
+          sc[h] = dot[h] * aq[h] * rk;
+          sigma = fmaxf(sigma, sc[h]);
+        }
+        if (p.hsel != nullptr && valid) {
+          // every head's own score, for a selection per query head
+          float *hs = p.hsel + (static_cast<int64_t>(u / p.Hkv) * p.Hq + (u % p.Hkv) * G) * p.ncap + j;
+  #pragma unroll
+          for (int h = 0; h < G; ++h) hs[h * p.ncap] = sc[h];
+        }
+        WSlot<G, KV8> &ws = wslots[slot];
+        if (p.sel != nullptr) {
+          ws.sig[row] = sigma;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfull[slot]);
+        }
+        const bool surv = valid && sigma > 0.0f;
+        const uint32_t bal = __ballot_sync(0xffffffffu, surv);
+        if (lane == 0) ws.cnt[quarter] = __popc(bal);
+        __syncwarp();
+        named_bar_sync(gbar, 128);  // the four counts are in
+        int off = 0, m = 0;
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = ws.cnt[q];
+          m += c;
+          off += q < quarter ? c : 0;
+        }
+        const int e = off + __popc(bal & lanemask_lt);  // this key's place in the tile's list
+        if (surv) {
+          ws.key[e] = j;
+  #pragma unroll
+          for (int h = 0; h < G; ++h) ws.w[e][h] = sc[h] > 0.0f ? sc[h] * sc[h] : 0.0f;
+          if constexpr (KV8) ws.vs[e] = vsc;
+        }
+        // m rows of the group's ring, in the group's tile order.  Tiles i - 8 and older
+        // were consumed before this tile's slot was taken; wait, oldest first, for the
+        // group's later tiles until the rows in use leave room for m.
+        bool rok = true;
+        if (m1 + m2 + m3 + m > kGroupRing && i >= 6)
+          rok = mbar_wait(&wempty[(i - 6) % kWSlots], ((i - 6) / kWSlots) & 1);
+        if (rok && m1 + m2 + m > kGroupRing && i >= 4)
+          rok = mbar_wait(&wempty[(i - 4) % kWSlots], ((i - 4) / kWSlots) & 1);
+        if (rok && m1 + m > kGroupRing && i >= 2)
+          rok = mbar_wait(&wempty[(i - 2) % kWSlots], ((i - 2) / kWSlots) & 1);
+        const int row0 = issued & (kGroupRing - 1);
+        issued += m;
+        m3 = m2;
+        m2 = m1;
+        m1 = m;
+        if (!rok) {
+          // no barrier follows in this tile: the group stops together at the next one
+          set_abort(s_abort, p.flags);
+          continue;
+        }
+        if (lane == 0) {
+          if (quarter == 0) {
+            ws.row0 = row0;
+            ws.m = m;
+          }
+          mbar_arrive_expect_tx(&vfull[slot], static_cast<uint32_t>(__popc(bal) * kRowBytes));
+          if (quarter == 0) s_varm[slot] = s_varm[slot] + 1;
+        }
+        __syncwarp();
+        if (surv)
+          bulk_load(gring + ((row0 + e) & (kGroupRing - 1)) * C::ring_pitch,
+                    p.v + (static_cast<int64_t>(u) * p.ncap + j) * kRowBytes, kRowBytes, &vfull[slot]);
       }
-      __syncwarp();
-      if (surv)
-        bulk_load(gring + ((row0 + e) & (kGroupRing - 1)) * C::ring_pitch,
-                  p.v + (static_cast<int64_t>(u) * p.ncap + j) * kRowBytes, kRowBytes, &vfull[slot]);
+      if (i < ie) break;  // stopped early
     }
     __syncwarp();
   } else if (warp == kWarpHist) {
@@ -767,47 +817,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the histogram of the order key's top 11 bits; at the end of each stretch of a unit
     // the histogram is added to the unit's global one and cleared.
     if (p.sel != nullptr) {
-      int u = u0, tl = tl0;
-      for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-        const int slot = static_cast<int>(i % kWSlots);
-        const bool ok = __all_sync(0xffffffffu, !*s_abort && mbar_wait(&sfull[slot], (i / kWSlots) & 1));
-        if (!ok) {
-          set_abort(s_abort, p.flags);
-          break;
-        }
-        const WSlot<G, KV8> &ws = wslots[slot];
-        float sg[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) sg[r] = ws.sig[lane + 32 * r];
-        float used = (sg[0] + sg[1]) + (sg[2] + sg[3]);
-        used = __shfl_sync(0xffffffffu, used, 31) + used;  // the whole warp takes part
-        __syncwarp();
-        if (lane == 0) mbar_arrive_after(&wempty[slot], used);
-        float *dst = p.sel + static_cast<int64_t>(u) * p.ncap + tl * kTileKeys;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = lane + 32 * r;
-          if (tl * kTileKeys + row < p.n) {
-            dst[row] = sg[r];
-            atomicAdd(&s_hist[order_key(sg[r]) >> 21], 1u);
+      int i = 0;
+      for (int pc = 0; pc < K; ++pc) {
+        const int4 pe = s_piece[pc];
+        int u = pe.x, tl = pe.y;
+        const int ie = i + pe.z;
+        for (; i < ie; ++i, next_tile(tl, u, TU)) {
+          const int slot = static_cast<int>(i % kWSlots);
+          const bool ok = __all_sync(0xffffffffu, !*s_abort && mbar_wait(&sfull[slot], (i / kWSlots) & 1));
+          if (!ok) {
+            set_abort(s_abort, p.flags);
+            break;
           }
-        }
-        if (i + 1 == ntiles) {
-          // the CTA's last stretch: the whole CTA flushes it once every role is done
+          const WSlot<G, KV8> &ws = wslots[slot];
+          float sg[4];
+  #pragma unroll
+          for (int r = 0; r < 4; ++r) sg[r] = ws.sig[lane + 32 * r];
+          float used = (sg[0] + sg[1]) + (sg[2] + sg[3]);
+          used = __shfl_sync(0xffffffffu, used, 31) + used;  // the whole warp takes part
           __syncwarp();
-          if (lane == 0) *s_final_hist = u;
-        } else if (tl + 1 == TU) {
-          __syncwarp();
-          pdl_wait_primary();  // the global histogram has been zeroed
-          for (int bin = lane; bin < kHistBins; bin += 32) {
-            const uint32_t cnt = s_hist[bin];
-            if (cnt) {
-              atomicAdd(&p.hist[static_cast<int64_t>(u) * kHistBins + bin], cnt);
-              s_hist[bin] = 0u;
+          if (lane == 0) mbar_arrive_after(&wempty[slot], used);
+          float *dst = p.sel + static_cast<int64_t>(u) * p.ncap + tl * kTileKeys;
+  #pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = lane + 32 * r;
+            if (tl * kTileKeys + row < p.n) {
+              dst[row] = sg[r];
+              atomicAdd(&s_hist[order_key(sg[r]) >> 21], 1u);
             }
           }
-          __syncwarp();
+          if (i + 1 == ie && pc + 1 == K) {
+            // the CTA's last stretch: the whole CTA flushes it once every role is done
+            __syncwarp();
+            if (lane == 0) *s_final_hist = u;
+          } else if (i + 1 == ie || tl + 1 == TU) {
+            __syncwarp();
+            pdl_wait_primary();  // the global histogram has been zeroed
+            for (int bin = lane; bin < kHistBins; bin += 32) {
+              const uint32_t cnt = s_hist[bin];
+              if (cnt) {
+                atomicAdd(&p.hist[static_cast<int64_t>(u) * kHistBins + bin], cnt);
+                s_hist[bin] = 0u;
+              }
+            }
+            __syncwarp();
+          }
         }
+        if (i < ie) break;  // stopped early
       }
     }
     __syncwarp();
@@ -818,83 +874,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sum of squared codes).  The stage is released as soon as these four warps and the
     // tile's MMAs are done with it.
     const int row = (warp - kWarpNorm) * 32 + lane;
-    int u = u0, tl = tl0, seg = -1;
-    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-      if (__any_sync(0xffffffffu, *s_abort)) break;
-      if constexpr (KV8) {
-        if (i == 0 || tl == 0) {
-          // the unit's query as E4M3 terms for the tensor cores
-          ++seg;
-          const int qb = seg & 1;
-          const bool qok = __all_sync(0xffffffffu,
-                                      mbar_wait(&qfull[qb], (seg >> 1) & 1) &&
-                                          (seg < 2 || mbar_wait(&q8empty[qb], ((seg >> 1) - 1) & 1)));
-          if (!qok) {
-            set_abort(s_abort, p.flags);
-            break;
-          }
-          build_q8_terms<G>(sQ + qb * kQBufBytes, sQ8 + qb * kQ8BufBytes, row);
-          fence_proxy_async_smem();  // the terms are read by the tensor cores
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&q8full[qb]);
-            mbar_arrive(&qempty[qb]);
+    int seg = -1;
+    int i = 0;
+    for (int pc = 0; pc < K; ++pc) {
+      const int4 pe = s_piece[pc];
+      int u = pe.x, tl = pe.y;
+      const int ib = i, ie = i + pe.z;
+      (void)ib;  // the stretch starts matter to the 8-bit caches only
+      for (; i < ie; ++i, next_tile(tl, u, TU)) {
+        if (__any_sync(0xffffffffu, *s_abort)) break;
+        if constexpr (KV8) {
+          if (i == ib || tl == 0) {
+            // the stretch's query as E4M3 terms for the tensor cores
+            ++seg;
+            const int qb = seg & 1;
+            const bool qok = __all_sync(0xffffffffu,
+                                        mbar_wait(&qfull[qb], (seg >> 1) & 1) &&
+                                            (seg < 2 || mbar_wait(&q8empty[qb], ((seg >> 1) - 1) & 1)));
+            if (!qok) {
+              set_abort(s_abort, p.flags);
+              break;
+            }
+            build_q8_terms<G>(sQ + qb * kQBufBytes, sQ8 + qb * kQ8BufBytes, row);
+            fence_proxy_async_smem();  // the terms are read by the tensor cores
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&q8full[qb]);
+              mbar_arrive(&qempty[qb]);
+            }
           }
         }
-      }
-      const int s = static_cast<int>(i % kStages);
-      const int ns = static_cast<int>(i % kNormSlots);
-      const bool ok = __all_sync(0xffffffffu,
-                                 mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) &&
-                                     (i < kNormSlots ||
-                                      mbar_wait(&rkempty[ns], ((i / kNormSlots) - 1) & 1)));
-      if (!ok) {
-        set_abort(s_abort, p.flags);
-        break;
-      }
-      // chunk order rotated by row so 8 neighbouring rows hit 8 different bank groups
-      // (the swizzle permutes 16-byte chunks within a row; the order does not matter)
-      const uint8_t *st = sK + s * C::stage_bytes;
-      const uint8_t *rowp = st + row * 128;
-      float rk, vsc = 0.0f, done;
-      if constexpr (KV8) {
-        // the key's two scales go on with the tile; its sum of squared codes comes from the
-        // tensor cores (codes . codes^T)
-        const float ks = reinterpret_cast<const float *>(st + C::tile_bytes)[row];
-        vsc = reinterpret_cast<const float *>(st + C::tile_bytes + C::scale_bytes)[row];
-        const float dep = ks + vsc;  // every lane's value depends on its reads
-        done = __shfl_sync(0xffffffffu, dep, 0) + __shfl_sync(0xffffffffu, dep, 31);
-        rk = ks;
-        (void)rowp;
-      } else {
-        float a[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) a[c] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int pc = (c ^ (row & 7)) * 16;
-          const uint4 x0 = *reinterpret_cast<const uint4 *>(rowp + pc);
-          const uint4 x1 = *reinterpret_cast<const uint4 *>(rowp + C::half_bytes + pc);
-          sq_acc_bf16x2(x0.x, a[0], a[1]);
-          sq_acc_bf16x2(x0.y, a[2], a[3]);
-          sq_acc_bf16x2(x0.z, a[4], a[5]);
-          sq_acc_bf16x2(x0.w, a[6], a[7]);
-          sq_acc_bf16x2(x1.x, a[0], a[1]);
-          sq_acc_bf16x2(x1.y, a[2], a[3]);
-          sq_acc_bf16x2(x1.z, a[4], a[5]);
-          sq_acc_bf16x2(x1.w, a[6], a[7]);
+        const int s = static_cast<int>(i % kStages);
+        const int ns = static_cast<int>(i % kNormSlots);
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait(&full[2 * s + (i & 1)], (i / kFullPeriod) & 1) &&
+                                       (i < kNormSlots ||
+                                        mbar_wait(&rkempty[ns], ((i / kNormSlots) - 1) & 1)));
+        if (!ok) {
+          set_abort(s_abort, p.flags);
+          break;
         }
-        // every lane's sum depends on all of its reads of the stage
-        const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-        done = __shfl_sync(0xffffffffu, ss, 0) + __shfl_sync(0xffffffffu, ss, 31);
-        rk = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+        // chunk order rotated by row so 8 neighbouring rows hit 8 different bank groups
+        // (the swizzle permutes 16-byte chunks within a row; the order does not matter)
+        const uint8_t *st = sK + s * C::stage_bytes;
+        const uint8_t *rowp = st + row * 128;
+        float rk, vsc = 0.0f, done;
+        if constexpr (KV8) {
+          // the key's two scales go on with the tile; its sum of squared codes comes from the
+          // tensor cores (codes . codes^T)
+          const float ks = reinterpret_cast<const float *>(st + C::tile_bytes)[row];
+          vsc = reinterpret_cast<const float *>(st + C::tile_bytes + C::scale_bytes)[row];
+          const float dep = ks + vsc;  // every lane's value depends on its reads
+          done = __shfl_sync(0xffffffffu, dep, 0) + __shfl_sync(0xffffffffu, dep, 31);
+          rk = ks;
+          (void)rowp;
+        } else {
+          float a[8];
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) a[c] = 0.0f;
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int pc = (c ^ (row & 7)) * 16;
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(rowp + pc);
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(rowp + C::half_bytes + pc);
+            sq_acc_bf16x2(x0.x, a[0], a[1]);
+            sq_acc_bf16x2(x0.y, a[2], a[3]);
+            sq_acc_bf16x2(x0.z, a[4], a[5]);
+            sq_acc_bf16x2(x0.w, a[6], a[7]);
+            sq_acc_bf16x2(x1.x, a[0], a[1]);
+            sq_acc_bf16x2(x1.y, a[2], a[3]);
+            sq_acc_bf16x2(x1.z, a[4], a[5]);
+            sq_acc_bf16x2(x1.w, a[6], a[7]);
+          }
+          // every lane's sum depends on all of its reads of the stage
+          const float ss = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+          done = __shfl_sync(0xffffffffu, ss, 0) + __shfl_sync(0xffffffffu, ss, 31);
+          rk = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_after(&empty[s], done);
+        s_rk[ns * kTileKeys + row] = rk;
+        if constexpr (KV8) s_vs[ns * kTileKeys + row] = vsc;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rkfull[ns]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_after(&empty[s], done);
-      s_rk[ns * kTileKeys + row] = rk;
-      if constexpr (KV8) s_vs[ns * kTileKeys + row] = vsc;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&rkfull[ns]);
+      if (i < ie) break;  // stopped early
     }
     __syncwarp();
   } else {
@@ -919,107 +983,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int mt = 0; mt < 2; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
     float den = 0.0f;  // lane (g, t): head g's weights of rows 2t, 2t+1, 2t+8, 2t+9 of each step
     int seg_surv = 0, step = 0;
-    int u = u0, tl = tl0;
-    for (int i = 0; i < ntiles; ++i, next_tile(tl, u, TU)) {
-      const int slot = static_cast<int>(i % kWSlots);
-      const bool ok = !*s_abort && mbar_wait(&vfull[slot], (i / kWSlots) & 1);
-      if (!named_bar_and(kAccBar, 128, ok)) {
-        set_abort(s_abort, p.flags);
-        break;
-      }
-      const WSlot<G, KV8> &ws = wslots[slot];
-      const int row0 = ws.row0, m = ws.m;
-      const uint32_t gring_u32 = ring_u32 + (i % kGroups) * kGroupRing * C::ring_pitch;
-      for (int e0 = 0; e0 < m; e0 += kAccStep, ++step) {
-        uint32_t base_u32;  // row 0 of this step's A operand
-        if constexpr (KV8) {
-          // widen rows e0 + 4aw .. +3 (lane: codes 4 lane .. 4 lane + 3) into the staging block
-          uint8_t *sb = stage + (step & 1) * kAccStep * kAccPitch;
-#pragma unroll
-          for (int k = 0; k < kAccStep / 4; ++k) {
-            const int e = e0 + aw * (kAccStep / 4) + k;
-            if (e < m) {
-              const uint32_t c4 = *reinterpret_cast<const uint32_t *>(
-                  sRing + (i % kGroups) * kGroupRing * C::ring_pitch +
-                  ((row0 + e) & (kGroupRing - 1)) * C::ring_pitch + lane * 4);
-              float v0, v1, v2, v3;
-              e4m3x4_to_f32(c4, v0, v1, v2, v3);
-              *reinterpret_cast<uint2 *>(sb + (e - e0) * kAccPitch + lane * 8) =
-                  make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+    int i = 0;
+    for (int pc = 0; pc < K; ++pc) {
+      const int4 pe = s_piece[pc];
+      int u = pe.x, tl = pe.y;
+      const int ie = i + pe.z;
+      const int q = pe.w;
+      for (; i < ie; ++i, next_tile(tl, u, TU)) {
+        const int slot = static_cast<int>(i % kWSlots);
+        const bool ok = !*s_abort && mbar_wait(&vfull[slot], (i / kWSlots) & 1);
+        if (!named_bar_and(kAccBar, 128, ok)) {
+          set_abort(s_abort, p.flags);
+          break;
+        }
+        const WSlot<G, KV8> &ws = wslots[slot];
+        const int row0 = ws.row0, m = ws.m;
+        const uint32_t gring_u32 = ring_u32 + (i % kGroups) * kGroupRing * C::ring_pitch;
+        for (int e0 = 0; e0 < m; e0 += kAccStep, ++step) {
+          uint32_t base_u32;  // row 0 of this step's A operand
+          if constexpr (KV8) {
+            // widen rows e0 + 4aw .. +3 (lane: codes 4 lane .. 4 lane + 3) into the staging block
+            uint8_t *sb = stage + (step & 1) * kAccStep * kAccPitch;
+  #pragma unroll
+            for (int k = 0; k < kAccStep / 4; ++k) {
+              const int e = e0 + aw * (kAccStep / 4) + k;
+              if (e < m) {
+                const uint32_t c4 = *reinterpret_cast<const uint32_t *>(
+                    sRing + (i % kGroups) * kGroupRing * C::ring_pitch +
+                    ((row0 + e) & (kGroupRing - 1)) * C::ring_pitch + lane * 4);
+                float v0, v1, v2, v3;
+                e4m3x4_to_f32(c4, v0, v1, v2, v3);
+                *reinterpret_cast<uint2 *>(sb + (e - e0) * kAccPitch + lane * 8) =
+                    make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+              }
             }
+            named_bar_sync(kAccBar, 128);  // the step's rows are widened
+            base_u32 = smem_u32(sb);
           }
-          named_bar_sync(kAccBar, 128);  // the step's rows are widened
-          base_u32 = smem_u32(sb);
-        }
-        // A: this lane's matrix row r of the step (matrices: rows 0-7 / 8-15 x dims +0 / +8)
-        const int r = (mat >> 1) * 8 + mr;
-        uint32_t raddr;
-        if constexpr (KV8)
-          raddr = e0 + r < m ? base_u32 + r * kAccPitch : zero_u32;
-        else
-          raddr = e0 + r < m ? gring_u32 + ((row0 + e0 + r) & (kGroupRing - 1)) * C::ring_pitch
-                             : zero_u32;
-        uint32_t a[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-          ldmatrix_x4_trans(a[mt], raddr + (2 * (2 * aw + mt) + (mat & 1)) * 16);
-        // B: head g's weights of rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1)
-        float w[4], wq[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int e = e0 + 2 * t + (k & 1) + (k >> 1) * 8;
-          const bool have = e < m && g < G;
-          w[k] = have ? ws.w[e][g < G ? g : 0] : 0.0f;
-          wq[k] = w[k];
-          if constexpr (KV8) wq[k] = have ? w[k] * ws.vs[e] : 0.0f;
-        }
-        den += (w[0] + w[1]) + (w[2] + w[3]);
-        const uint32_t h0 = pack_bf16x2(wq[0], wq[1]), h1 = pack_bf16x2(wq[2], wq[3]);
-        const uint32_t l0 = pack_bf16x2(wq[0] - bf16lo(h0), wq[1] - bf16hi(h0));
-        const uint32_t l1 = pack_bf16x2(wq[2] - bf16lo(h1), wq[3] - bf16hi(h1));
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          mma_16816_bf16(o[mt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], h0, h1);
-          mma_16816_bf16(o[mt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], l0, l1);
-        }
-      }
-      seg_surv += m;
-      // the running sums depend on every ring row and weight this lane read
-      float used = den + ((o[0][0] + o[0][1]) + (o[0][2] + o[0][3])) +
-                   ((o[1][0] + o[1][1]) + (o[1][2] + o[1][3]));
-      used = __shfl_sync(0xffffffffu, used, 31) + used;
-      __syncwarp();
-      if (lane == 0) mbar_arrive_after(&wempty[slot], used);
-      if (i + 1 == ntiles || tl + 1 == TU) {
-        float *r = p.rec + (cta + u) * p.rec_stride;
-        // this warp's dims of every head
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const int d = 32 * aw + 16 * mt + g;
-          if (2 * t < G) {
-            r[(2 * t) * kHeadDim + d] = o[mt][0];
-            r[(2 * t) * kHeadDim + d + 8] = o[mt][2];
+          // A: this lane's matrix row r of the step (matrices: rows 0-7 / 8-15 x dims +0 / +8)
+          const int r = (mat >> 1) * 8 + mr;
+          uint32_t raddr;
+          if constexpr (KV8)
+            raddr = e0 + r < m ? base_u32 + r * kAccPitch : zero_u32;
+          else
+            raddr = e0 + r < m ? gring_u32 + ((row0 + e0 + r) & (kGroupRing - 1)) * C::ring_pitch
+                               : zero_u32;
+          uint32_t a[2][4];
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+            ldmatrix_x4_trans(a[mt], raddr + (2 * (2 * aw + mt) + (mat & 1)) * 16);
+          // B: head g's weights of rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1)
+          float w[4], wq[4];
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = e0 + 2 * t + (k & 1) + (k >> 1) * 8;
+            const bool have = e < m && g < G;
+            w[k] = have ? ws.w[e][g < G ? g : 0] : 0.0f;
+            wq[k] = w[k];
+            if constexpr (KV8) wq[k] = have ? w[k] * ws.vs[e] : 0.0f;
           }
-          if (2 * t + 1 < G) {
-            r[(2 * t + 1) * kHeadDim + d] = o[mt][1];
-            r[(2 * t + 1) * kHeadDim + d + 8] = o[mt][3];
+          den += (w[0] + w[1]) + (w[2] + w[3]);
+          const uint32_t h0 = pack_bf16x2(wq[0], wq[1]), h1 = pack_bf16x2(wq[2], wq[3]);
+          const uint32_t l0 = pack_bf16x2(wq[0] - bf16lo(h0), wq[1] - bf16hi(h0));
+          const uint32_t l1 = pack_bf16x2(wq[2] - bf16lo(h1), wq[3] - bf16hi(h1));
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            mma_16816_bf16(o[mt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], h0, h1);
+            mma_16816_bf16(o[mt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], l0, l1);
           }
-          o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
         }
-        // every warp sees the same weights: warp 0 writes the denominators
-        float dh = den + __shfl_xor_sync(0xffffffffu, den, 1);
-        dh += __shfl_xor_sync(0xffffffffu, dh, 2);
-        den = 0.0f;
-        if (aw == 0 && t == 0 && g < G) r[G * kHeadDim + g] = dh;
+        seg_surv += m;
+        // the running sums depend on every ring row and weight this lane read
+        float used = den + ((o[0][0] + o[0][1]) + (o[0][2] + o[0][3])) +
+                     ((o[1][0] + o[1][1]) + (o[1][2] + o[1][3]));
+        used = __shfl_sync(0xffffffffu, used, 31) + used;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_after(&wempty[slot], used);
+        if (i + 1 == ie || tl + 1 == TU) {
+          float *r = p.rec + static_cast<int64_t>(q + u) * p.rec_stride;
+          // this warp's dims of every head
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const int d = 32 * aw + 16 * mt + g;
+            if (2 * t < G) {
+              r[(2 * t) * kHeadDim + d] = o[mt][0];
+              r[(2 * t) * kHeadDim + d + 8] = o[mt][2];
+            }
+            if (2 * t + 1 < G) {
+              r[(2 * t + 1) * kHeadDim + d] = o[mt][1];
+              r[(2 * t + 1) * kHeadDim + d + 8] = o[mt][3];
+            }
+            o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+          }
+          // every warp sees the same weights: warp 0 writes the denominators
+          float dh = den + __shfl_xor_sync(0xffffffffu, den, 1);
+          dh += __shfl_xor_sync(0xffffffffu, dh, 2);
+          den = 0.0f;
+          if (aw == 0 && t == 0 && g < G) r[G * kHeadDim + g] = dh;
 
-        // the stretch's survivors are counted in (integer sums: the same in any order); the
-        // records are summed by full_combine_kernel, which follows this kernel
-        if (aw == 0 && lane == 0) {
-          pdl_wait_primary();  // the survivor counts have been zeroed
-          atomicAdd(&p.n_surv[u], seg_surv);
+          // the stretch's survivors are counted in (integer sums: the same in any order); the
+          // records are summed by full_combine_kernel, which follows this kernel
+          if (aw == 0 && lane == 0) {
+            pdl_wait_primary();  // the survivor counts have been zeroed
+            atomicAdd(&p.n_surv[u], seg_surv);
+          }
+          seg_surv = 0;
         }
-        seg_surv = 0;
       }
+      if (i < ie) break;  // stopped early
     }
     __syncwarp();
   }
@@ -1076,8 +1147,8 @@ __global__ void __launch_bounds__(256) full_zero_kernel(uint4 *hist, int64_t his
   for (int64_t i = t; i < units; i += stride) n_surv[i] = 0;
 }
 
-// out[u][h][d] = num / (c + den), num and den the sums of unit u's records (the stretches of
-// the CTAs c0 .. c1 that worked on it, records c0 + u .. c1 + u), in a fixed order.  One CTA
+// out[u][h][d] = num / (c + den), num and den the sums of unit u's records (its stretches in
+// the pieces c0 .. c1 that hold its tiles, records c0 + u .. c1 + u), in a fixed order.  One CTA
 // of dc x S threads per dc dims of a (unit, head) (dc = 128, 64 or 32, so that there are
 // about as many CTAs as SMs), S = the slices (a power of two, at most 8, from the records per
 // unit): thread (s, d) sums records s, s + S, s + 2S, ... of its dim (up to eight loads in
@@ -1096,16 +1167,16 @@ __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel
   const int h = static_cast<int>(blockIdx.x / per_head % G);
   const int dl = static_cast<int>(threadIdx.x) % dc, sl = static_cast<int>(threadIdx.x) / dc;
   const int d = static_cast<int>(blockIdx.x % per_head) * dc + dl;
-  // the unit's first and last CTA (split_cta_of_tile, in 32-bit arithmetic when T * P fits)
+  // the unit's first and last piece (split_piece_of_tile, in 32-bit arithmetic when T * Q fits)
   int64_t c0, c1;
-  if (((p.T * p.P) >> 32) == 0) {
-    const uint32_t T32 = static_cast<uint32_t>(p.T), P32 = static_cast<uint32_t>(p.P);
+  if (((p.T * p.Q) >> 32) == 0) {
+    const uint32_t T32 = static_cast<uint32_t>(p.T), Q32 = static_cast<uint32_t>(p.Q);
     const uint32_t t0 = static_cast<uint32_t>(u * p.TU), t1 = t0 + static_cast<uint32_t>(p.TU) - 1u;
-    c0 = ((t0 + 1u) * P32 - 1u) / T32;
-    c1 = ((t1 + 1u) * P32 - 1u) / T32;
+    c0 = ((t0 + 1u) * Q32 - 1u) / T32;
+    c1 = ((t1 + 1u) * Q32 - 1u) / T32;
   } else {
-    c0 = split_cta_of_tile(u * p.TU, p.T, p.P);
-    c1 = split_cta_of_tile(u * p.TU + p.TU - 1, p.T, p.P);
+    c0 = split_piece_of_tile(u * p.TU, p.T, p.Q);
+    c1 = split_piece_of_tile(u * p.TU + p.TU - 1, p.T, p.Q);
   }
   const int parts = static_cast<int>(c1 - c0 + 1);
   const float *rr = p.rec + (c0 + u) * p.rec_stride;
@@ -1150,8 +1221,8 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
                                  const CUtensorMap &tm_ks, const CUtensorMap &tm_vs,
                                  const FullParams &p, int64_t units, cudaStream_t stream) {
   const int smem = Smem<G, KV8>::alloc;
-  cudaError_t e = cudaFuncSetAttribute(full_decode_kernel<G, KV8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kernel = p.K > 1 ? full_decode_kernel<G, KV8, true> : full_decode_kernel<G, KV8, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t hist_vecs = p.hist ? units * kHistBins / 4 : 0;
   const int64_t work = hist_vecs > units ? hist_vecs : units;
@@ -1160,11 +1231,11 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
                  dim3(256), 0, stream, 0u, reinterpret_cast<uint4 *>(p.hist), hist_vecs,
                  p.n_surv, units);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(full_decode_kernel<G, KV8>, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
+  e = launch_pdl(kernel, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
                  static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, tm_ks, tm_vs, p);
   if (e != cudaSuccess) return e;
   // slices: the records of the unit with the most, rounded up to a power of two (at most 8)
-  const int64_t most = (p.TU * p.P + p.T - 1) / p.T + 1;
+  const int64_t most = (p.TU * p.Q + p.T - 1) / p.T + 1;
   int slices = 1;
   while (slices < kCombMaxSlices && slices < most) slices <<= 1;
   // dims per CTA: 128, halved (to 32 at least) while there are fewer CTAs than SMs
@@ -1176,12 +1247,19 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
 
 }  // namespace
 
-FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count) {
+FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count, int max_pieces) {
   FullSplit sp;
   sp.units = units;
   sp.tiles_per_unit = (ctx_len + kTileKeys - 1) / kTileKeys;
   sp.tiles = units * sp.tiles_per_unit;
   sp.ctas = static_cast<int32_t>(sp.tiles < sm_count ? sp.tiles : sm_count);
+  // K: as many pieces of kMinPieceTiles tiles or more as a CTA's share holds, odd, at most
+  // max_pieces; every piece then holds at least one tile (Q <= T)
+  int64_t k = sp.ctas > 0 ? sp.tiles / sp.ctas / kMinPieceTiles : 1;
+  if (k > max_pieces) k = max_pieces;
+  if (k < 1) k = 1;
+  if (k % 2 == 0) --k;
+  sp.pieces = static_cast<int32_t>(k * sp.ctas);
   return sp;
 }
 
@@ -1190,13 +1268,10 @@ int full_record_floats(int G) {
   return (f + 3) & ~3;
 }
 
-static size_t full_records_bytes(int64_t units, int G, int sm_count) {
-  return (static_cast<size_t>(units + sm_count) * full_record_floats(G) * sizeof(float) + 255) &
+size_t full_workspace_bytes(const FullSplit &sp, int G) {
+  // the records: one slot per (piece, unit) stretch, slots q + u < Q + units
+  return (static_cast<size_t>(sp.units + sp.pieces) * full_record_floats(G) * sizeof(float) + 255) &
          ~static_cast<size_t>(255);
-}
-
-size_t full_workspace_bytes(int64_t units, int G, int sm_count) {
-  return full_records_bytes(units, G, sm_count);
 }
 
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
@@ -1223,6 +1298,8 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
   p.n = n;
   p.ncap = ncap;
   p.P = sp.ctas;
+  p.Q = sp.pieces;
+  p.K = sp.pieces / sp.ctas;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.rec_stride = full_record_floats(G);

@@ -44,27 +44,38 @@ constexpr int kHeadDim = 128;
 constexpr int kTileKeys = 128;     // keys per full-decode tile (the MMA's M)
 constexpr int kHistBins = 2048;    // selection histogram: top 11 bits of the order key
 
-// Work split of the full-layer decode: T tiles (TU per unit) over P persistent CTAs,
-// CTA c owning tiles [floor(c*T/P), floor((c+1)*T/P)).  The partial record of the
-// stretch of unit u that CTA c handles lives in slot c + u.
+// Work split of the full-layer decode: the T tiles (TU per unit, units one after another)
+// are cut into Q = K * P pieces, piece q holding tiles [floor(q*T/Q), floor((q+1)*T/Q)), and
+// persistent CTA c of P takes pieces c, c + P, ..., c + (K-1)P in that order.  With K > 1 a
+// CTA's tiles come from K places spread over the batch, so sequences whose keys survive
+// more often (more V rows to fetch) do not all land on the same CTAs; K is odd, so a
+// power-of-two period in the batch (sequences x heads) does not line a CTA's pieces up with
+// it.  The partial record of the stretch of unit u inside piece q lives in slot q + u.
 struct FullSplit {
   int64_t units;      // B * Hkv
   int64_t tiles_per_unit;
   int64_t tiles;      // units * tiles_per_unit
   int32_t ctas;       // P
+  int32_t pieces;     // Q = K * P
 };
 
-__host__ __device__ inline int64_t split_first_tile(int64_t c, int64_t T, int64_t P) {
-  return (c * T) / P;
+constexpr int kMaxPiecesPerCta = 5;
+static_assert(kMaxPiecesPerCta % 2 == 1, "K is odd");
+constexpr int kMinPieceTiles = 20;  // a CTA's share is cut into pieces of at least this many
+
+__host__ __device__ inline int64_t split_piece_start(int64_t q, int64_t T, int64_t Q) {
+  return (q * T) / Q;
 }
-// The CTA whose range holds tile t.
-__host__ __device__ inline int64_t split_cta_of_tile(int64_t t, int64_t T, int64_t P) {
-  return ((t + 1) * P - 1) / T;
+// The piece that holds tile t.
+__host__ __device__ inline int64_t split_piece_of_tile(int64_t t, int64_t T, int64_t Q) {
+  return ((t + 1) * Q - 1) / T;
 }
 
-FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count);
+// max_pieces (odd, >= 1) caps K.
+FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count,
+                     int max_pieces = kMaxPiecesPerCta);
 int full_record_floats(int G);
-size_t full_workspace_bytes(int64_t units, int G, int sm_count);
+size_t full_workspace_bytes(const FullSplit &sp, int G);
 
 // kv8: 8-bit E4M3 caches; tm_ks / tm_vs then map the K and V scales as [units, ncap] fp32.
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,

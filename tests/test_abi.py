@@ -100,42 +100,50 @@ HARNESS = r"""
 #include "internal.h"
 using namespace embla;
 int main() {
-  // every tile belongs to exactly one CTA; the stretch of unit u held by CTA c uses
-  // slot c+u, which no other (CTA, unit) pair uses; the combine's [c0, c1] range
-  // lists exactly the CTAs that touched u
-  for (int sms = 1; sms <= 20; ++sms)
-    for (long units = 1; units <= 9; ++units)
-      for (long n = 0; n <= 1300; n += 97) {
-        FullSplit sp = full_split(units, n, sms);
-        long T = sp.tiles, P = sp.ctas;
-        if (T == 0) { if (P != 0) return 1; continue; }
-        if (P < 1 || P > T || P > sms) return 2;
-        static int owner[100000];
-        static int slot_user[200];
-        for (int i = 0; i < 200; ++i) slot_user[i] = -1;
-        for (long c = 0; c < P; ++c) {
-          long b = split_first_tile(c, T, P), e = split_first_tile(c + 1, T, P);
-          if (e <= b) return 3;
-          for (long t = b; t < e; ++t) {
-            owner[t] = (int)c;
-            if (split_cta_of_tile(t, T, P) != c) return 4;
-            long u = t / sp.tiles_per_unit, slot = c + u;
-            if (slot >= P + units) return 5;
-            if (slot_user[slot] != -1 && slot_user[slot] != (int)(c * 1000 + u)) return 6;
-            slot_user[slot] = (int)(c * 1000 + u);
+  // every tile belongs to exactly one piece; CTA c takes pieces c, c + P, ...; the stretch
+  // of unit u inside piece q uses slot q+u, which no other (piece, unit) pair uses; the
+  // combine's [q0, q1] range lists exactly the pieces that touch u
+  static int slot_user[400];
+  for (int mp = 1; mp <= 5; mp += 2)
+    for (int sms = 1; sms <= 20; ++sms)
+      for (long units = 1; units <= 9; ++units)
+        for (long n = 0; n <= 2600; n += 97) {
+          FullSplit sp = full_split(units, n, sms, mp);
+          long T = sp.tiles, P = sp.ctas, Q = sp.pieces, TU = sp.tiles_per_unit;
+          if (T == 0) { if (P != 0) return 1; continue; }
+          if (P < 1 || P > T || P > sms) return 2;
+          if (Q % P != 0) return 9;
+          long K = Q / P;
+          if (K < 1 || K > mp || K % 2 == 0 || Q > T) return 10;
+          if (K > 1 && T / P / K < kMinPieceTiles) return 12;
+          for (int i = 0; i < 400; ++i) slot_user[i] = -1;
+          for (long q = 0; q < Q; ++q) {
+            long b = split_piece_start(q, T, Q), e = split_piece_start(q + 1, T, Q);
+            if (e <= b) return 3;
+            for (long t = b; t < e; ++t) {
+              if (split_piece_of_tile(t, T, Q) != q) return 4;
+              long u = t / TU, slot = q + u;
+              if (slot >= Q + units) return 5;
+              if (slot_user[slot] != -1 && slot_user[slot] != (int)(q * 1000 + u)) return 6;
+              slot_user[slot] = (int)(q * 1000 + u);
+            }
+          }
+          if (split_piece_start(0, T, Q) != 0 || split_piece_start(Q, T, Q) != T) return 7;
+          for (long u = 0; u < units; ++u) {
+            long q0 = split_piece_of_tile(u * TU, T, Q);
+            long q1 = split_piece_of_tile(u * TU + TU - 1, T, Q);
+            if (q1 - q0 + 1 > (TU * Q + T - 1) / T + 1) return 11;
+            for (long q = 0; q < Q; ++q) {
+              long b = split_piece_start(q, T, Q), e = split_piece_start(q + 1, T, Q);
+              bool touches = b < (u + 1) * TU && e > u * TU;
+              if (touches != (q >= q0 && q <= q1)) return 8;
+            }
           }
         }
-        if (split_first_tile(P, T, P) != T) return 7;
-        for (long u = 0; u < units; ++u) {
-          long c0 = split_cta_of_tile(u * sp.tiles_per_unit, T, P);
-          long c1 = split_cta_of_tile(u * sp.tiles_per_unit + sp.tiles_per_unit - 1, T, P);
-          for (long c = 0; c < P; ++c) {
-            long b = split_first_tile(c, T, P), e = split_first_tile(c + 1, T, P);
-            bool touches = b < (u + 1) * sp.tiles_per_unit && e > u * sp.tiles_per_unit;
-            if (touches != (c >= c0 && c <= c1)) return 8;
-          }
-        }
-      }
+  // the decode workloads' splits on 152 SMs: B 8 x 4 KV heads at 32k keys keeps one piece
+  // per CTA; B 32 x 4 at 16k keys (108 tiles a CTA) takes five
+  if (full_split(32, 32768, 152).pieces != 152) return 13;
+  if (full_split(128, 16384, 152).pieces != 5 * 152) return 14;
   std::puts("ok");
   return 0;
 }

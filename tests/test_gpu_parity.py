@@ -84,7 +84,20 @@ def test_full_many_units_and_split_boundaries(B, n):
     _check_full(fl, run)
 
 
-@pytest.mark.parametrize("B,n,frac", [(8, 32768, 0.05), (16, 8192, 0.5)])
+@pytest.mark.parametrize("tiles_per_cta,n_short", [(70, 77), (110, 50)])
+def test_full_pieces_over_units_of_mixed_survival(tiles_per_cta, n_short):
+    # shares long enough that each CTA takes three or five pieces spread over the batch;
+    # sequences whose keys survive at 50 / 20 / 5 / 1 %, ragged last tiles
+    B, Hkv = 5, 4
+    tu = -(-tiles_per_cta * E.embla_device_sm_count() // (B * Hkv))
+    fl = _layer(B, 16, Hkv, tu * 128 - n_short, pattern="subset", frac=[0.5, 0.2, 0.05, 0.01],
+                seed=23)
+    run = FullRun(fl)
+    _check_full(fl, run)
+
+
+@pytest.mark.parametrize("B,n,frac", [(8, 32768, 0.05), (16, 8192, 0.5),
+                                      (32, 16384, [0.5, 0.2, 0.05, 0.01])])
 def test_full_decode_is_repeatable(B, n, frac):
     # pipeline races show up as a tile scored from the wrong buffer now and then: every
     # call must give the same bits (the combine sums in a fixed order)
