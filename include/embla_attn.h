@@ -138,16 +138,19 @@ embla_status embla_full_decode_e4m3(const embla_shape *shape, const void *q,
  * allocator of its own.  Nothing is allocated, here or inside: the scratch is
  * one fixed array of EMBLA_FULL_DECODE_SCRATCH_BYTES (4 MiB) in the library's
  * device memory, one per device.
- *   Limit: when embla_full_decode_workspace_size(shape) exceeds
- *     EMBLA_FULL_DECODE_SCRATCH_BYTES the call returns EMBLA_ERR_WORKSPACE and
- *     launches nothing.  On a 152-SM device that is above about 1860 (b, g)
- *     units at G = 4 and about 860 at G = 8.
+ *   Limit: the scratch holds the partial records of the work split.  Where
+ *     embla_full_decode would cut each CTA's share of a long batch into several
+ *     pieces and their records do not fit, this call takes fewer pieces (its
+ *     partial sums are then grouped differently, so results can differ from
+ *     embla_full_decode's in rounding); when even one piece per CTA does not fit, it returns
+ *     EMBLA_ERR_WORKSPACE and launches nothing.  On a 152-SM device that is
+ *     above about 1860 (b, g) units at G = 4 and about 860 at G = 8.
  *   Set-up: the first call on a device, made with that device current, looks
  *     up the array's device address and keeps it for later calls (a failed
  *     look-up returns EMBLA_ERR_CUDA).  Make that first call before beginning
  *     any stream capture.
- *   Zeroing: none needed; the scratch (the per-CTA partial records) is written
- *     before it is read.
+ *   Zeroing: none needed; the scratch (the partial records) is written before
+ *     it is read.
  *   Concurrency: all calls on one device share the one array.  Two calls that
  *     may run at the same time on the device (different streams or host
  *     threads with no ordering between them) race on it and give wrong
@@ -179,6 +182,36 @@ embla_status embla_select_topk(const embla_shape *shape, const float *sel_scores
                                const uint32_t *sel_hist, int32_t topk, int32_t recent,
                                int32_t *idx, int32_t idx_stride, int32_t *count, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/*
+ * Full-layer decode followed by the sparse layers' selection, in one call —
+ * "Three kinds of attention": the full layer's scores choose the keys its
+ * block's sparse layers read.  The results are exactly those of
+ * embla_full_decode (or embla_full_decode_e4m3) with sel_scores and sel_hist,
+ * then embla_select_topk on them: out, n_surv, sel_scores, sel_hist, idx and
+ * count as documented there (sel_scores and sel_hist are required).  The
+ * selection starts as soon as the scores are complete; the full layer's
+ * output is finished beside it, so the pair takes less time than the two
+ * calls.  Everything is ordered on `stream` as for the two calls.
+ *   workspace  embla_full_decode_select_workspace_size(shape, topk, recent)
+ *              bytes, 16-byte aligned
+ */
+size_t embla_full_decode_select_workspace_size(const embla_shape *shape, int32_t topk,
+                                               int32_t recent);
+embla_status embla_full_decode_select(const embla_shape *shape, const void *q, const void *k_cache,
+                                      const void *v_cache, float alpha, float c, float eps,
+                                      float *out, int32_t *n_surv, float *sel_scores,
+                                      uint32_t *sel_hist, int32_t topk, int32_t recent,
+                                      int32_t *idx, int32_t idx_stride, int32_t *count,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+embla_status embla_full_decode_e4m3_select(const embla_shape *shape, const void *q,
+                                           const uint8_t *k_codes, const float *k_scales,
+                                           const uint8_t *v_codes, const float *v_scales,
+                                           float alpha, float c, float eps, float *out,
+                                           int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
+                                           int32_t topk, int32_t recent, int32_t *idx,
+                                           int32_t idx_stride, int32_t *count, void *workspace,
+                                           size_t workspace_bytes, void *stream);
 
 /*
  * Sparse-layer decode — "Three kinds of attention" (Sparse): for every query

@@ -101,6 +101,12 @@ def library() -> ctypes.CDLL:
                                                              sz, vp]),
             "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
                                                                 vp, vp, vp, vp, vp]),
+            "embla_full_decode_select_workspace_size": (sz, [P, i32, i32]),
+            "embla_full_decode_select": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32, vp, vp, vp,
+                                                        vp, i32, i32, vp, i32, vp, vp, sz, vp]),
+            "embla_full_decode_e4m3_select": (ctypes.c_int, [P, vp, vp, vp, vp, vp, f32, f32, f32,
+                                                             vp, vp, vp, vp, i32, i32, vp, i32,
+                                                             vp, vp, sz, vp]),
             "embla_select_topk_workspace_size": (sz, [P, i32, i32]),
             "embla_select_topk": (ctypes.c_int, [P, vp, vp, i32, i32, vp, i32, vp, vp, sz, vp]),
             "embla_sparse_decode_workspace_size": (sz, [P, i32]),
@@ -257,6 +263,66 @@ def embla_select_topk(shape: Shape, sel_scores, sel_hist, idx, count, topk: int 
     _call("embla_select_topk", ctypes.byref(shape.c()), _ptr(sel_scores), _ptr(sel_hist), topk,
           recent, _ptr(idx), idx.shape[2], _ptr(count), _ptr(ws), ws.numel() * ws.element_size(),
           _stream(stream))
+
+
+def embla_full_decode_select_workspace_size(shape: Shape, topk: int = 1024, recent: int = 128) -> int:
+    return library().embla_full_decode_select_workspace_size(ctypes.byref(shape.c()), topk, recent)
+
+
+def _check_select_outputs(shape: Shape, idx, count):
+    B, Hkv = shape.batch, shape.n_kv_heads
+    _check(idx, torch.int32, None, "idx")
+    if idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hkv):
+        raise ValueError("idx must be [B, Hkv, idx_stride]")
+    _check(count, torch.int32, (B, Hkv), "count")
+
+
+def embla_full_decode_select(shape: Shape, q, k_cache, v_cache, out, n_surv, sel_scores, sel_hist,
+                             idx, count, topk: int = 1024, recent: int = 128, alpha: float = 1.0,
+                             c: float = 1.0, eps: float = 1e-6, workspace=None, stream=None):
+    """embla_full_decode with sel_scores and sel_hist, then embla_select_topk on them, in one
+    call (the selection starts as soon as the scores are complete)."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    _check(n_surv, torch.int32, (B, Hkv), "n_surv")
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores")
+    _check(sel_hist, torch.int32, (B, Hkv, HIST_BINS), "sel_hist")
+    _check_select_outputs(shape, idx, count)
+    ws = _workspace(embla_full_decode_select_workspace_size(shape, topk, recent), workspace,
+                    q.device)
+    _call("embla_full_decode_select", ctypes.byref(shape.c()), _ptr(q), _ptr(k_cache),
+          _ptr(v_cache), alpha, c, eps, _ptr(out), _ptr(n_surv), _ptr(sel_scores),
+          _ptr(sel_hist), topk, recent, _ptr(idx), idx.shape[2], _ptr(count), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def embla_full_decode_e4m3_select(shape: Shape, q, k_codes, k_scales, v_codes, v_scales, out,
+                                  n_surv, sel_scores, sel_hist, idx, count, topk: int = 1024,
+                                  recent: int = 128, alpha: float = 1.0, c: float = 1.0,
+                                  eps: float = 1e-6, workspace=None, stream=None):
+    """embla_full_decode_e4m3 with its selection, as embla_full_decode_select."""
+    B, Hq, Hkv, D, ncap = shape.batch, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, \
+        shape.cache_stride
+    _check(q, torch.bfloat16, (B, Hq, D), "q")
+    _check(k_codes, torch.uint8, (B, Hkv, ncap, D), "k_codes")
+    _check(k_scales, torch.float32, (B, Hkv, ncap), "k_scales")
+    _check(v_codes, torch.uint8, (B, Hkv, ncap, D), "v_codes")
+    _check(v_scales, torch.float32, (B, Hkv, ncap), "v_scales")
+    _check(out, torch.float32, (B, Hq, D), "out")
+    _check(n_surv, torch.int32, (B, Hkv), "n_surv")
+    _check(sel_scores, torch.float32, (B, Hkv, ncap), "sel_scores")
+    _check(sel_hist, torch.int32, (B, Hkv, HIST_BINS), "sel_hist")
+    _check_select_outputs(shape, idx, count)
+    ws = _workspace(embla_full_decode_select_workspace_size(shape, topk, recent), workspace,
+                    q.device)
+    _call("embla_full_decode_e4m3_select", ctypes.byref(shape.c()), _ptr(q), _ptr(k_codes),
+          _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), alpha, c, eps, _ptr(out), _ptr(n_surv),
+          _ptr(sel_scores), _ptr(sel_hist), topk, recent, _ptr(idx), idx.shape[2], _ptr(count),
+          _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
 def embla_sparse_decode(shape: Shape, q, k_cache, v_cache, idx, count, out, tau: float | None = None,

@@ -207,15 +207,25 @@ size_t embla_full_decode_workspace_size(const embla_shape *shape) {
 
 namespace {
 
+// The selection requested together with a full-layer decode.
+struct SelectArgs {
+  int32_t topk, recent;
+  int32_t *idx;
+  int32_t idx_stride;
+  int32_t *count;
+};
+
 // The full-layer decode for bf16 caches (k_scales and v_scales null) or 8-bit E4M3 caches
-// with per-token scales.
+// with per-token scales; with sa, followed by the selection over its scores (the workspace
+// then holds the decode's records, then the selection's workspace).
 embla_status full_decode_impl(const embla_shape *shape, const void *q, const void *k_cache,
                               const float *k_scales, const void *v_cache, const float *v_scales,
                               bool kv8, float alpha, float c, float eps, float *out,
                               int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
                               void *workspace, size_t workspace_bytes, void *stream,
                               float *head_scores = nullptr, uint32_t *head_hist = nullptr,
-                              int max_pieces = kMaxPiecesPerCta) {
+                              int max_pieces = kMaxPiecesPerCta,
+                              const SelectArgs *sa = nullptr) {
   int G = 0;
   embla_status st = check_shape(shape, &G, true);
   if (st != EMBLA_OK) return st;
@@ -230,6 +240,11 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
   if (kv8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
     return EMBLA_ERR_INVALID_ARG;
   if ((sel_scores == nullptr) != (sel_hist == nullptr)) return EMBLA_ERR_INVALID_ARG;
+  if (sa && (!sel_scores || sa->topk < 0 || sa->recent < 0 ||
+             static_cast<int64_t>(sa->topk) + sa->recent > INT32_MAX ||
+             sa->idx_stride < sa->topk + sa->recent || !sa->idx || !sa->count ||
+             !aligned16(sa->idx) || !aligned16(sa->count)))
+    return EMBLA_ERR_INVALID_ARG;
   if ((head_scores == nullptr) != (head_hist == nullptr)) return EMBLA_ERR_INVALID_ARG;
   if (head_scores && (!aligned16(head_scores) || !aligned16(head_hist)))
     return EMBLA_ERR_INVALID_ARG;
@@ -242,7 +257,9 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
   const int sms = sm_count_of(dev);
   if (sms <= 0) return EMBLA_ERR_CUDA;
   const FullSplit sp = full_split(units, shape->ctx_len, sms, max_pieces);
-  if (workspace_bytes < full_workspace_bytes(sp, G)) return EMBLA_ERR_WORKSPACE;
+  const size_t rec_bytes = full_workspace_bytes(sp, G);
+  const size_t sel_bytes = sa ? select_workspace_bytes(units, shape->ctx_len) : 0;
+  if (workspace_bytes < rec_bytes + sel_bytes) return EMBLA_ERR_WORKSPACE;
   uint32_t *flags = flags_ptr();
   if (!flags) return EMBLA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -257,6 +274,8 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
     if (st == EMBLA_OK)
       st = cuda_status(cudaMemsetAsync(out, 0, static_cast<size_t>(units) * G * kHeadDim * 4, s));
     if (st == EMBLA_OK) st = cuda_status(cudaMemsetAsync(n_surv, 0, static_cast<size_t>(units) * 4, s));
+    if (st == EMBLA_OK && sa)  // no keys to select
+      st = cuda_status(cudaMemsetAsync(sa->count, 0, static_cast<size_t>(units) * 4, s));
     return st;
   }
   // the launch zeroes the histogram and the survivor counts itself
@@ -274,11 +293,21 @@ embla_status full_decode_impl(const embla_shape *shape, const void *q, const voi
               !encode_scales(&tm_vs, v_scales, static_cast<uint64_t>(units),
                              static_cast<uint64_t>(shape->cache_stride))))
     return EMBLA_ERR_CUDA;
+  SelectJob sj = {};
+  if (sa) {
+    sj.topk = sa->topk;
+    sj.recent = sa->recent;
+    sj.idx = sa->idx;
+    sj.idx_stride = sa->idx_stride;
+    sj.count = sa->count;
+    sj.workspace = sel_bytes ? static_cast<uint8_t *>(workspace) + rec_bytes : nullptr;
+    sj.sm_count = sms;
+  }
   st = cuda_status(launch_full_decode(G, kv8, tm_k, tm_q, kv8 ? &tm_ks : nullptr,
                                       kv8 ? &tm_vs : nullptr, v_cache, sel_scores, head_scores,
                                       sel_hist, workspace, out, n_surv, c, flags, sp,
                                       shape->ctx_len, shape->cache_stride, shape->n_q_heads,
-                                      shape->n_kv_heads, alpha, eps, s));
+                                      shape->n_kv_heads, alpha, eps, s, sa ? &sj : nullptr));
   if (st == EMBLA_OK && head_scores)
     st = cuda_status(launch_score_hist(head_scores,
                                        static_cast<int64_t>(shape->batch) * shape->n_q_heads,
@@ -317,6 +346,43 @@ embla_status embla_full_decode_e4m3(const embla_shape *shape, const void *q,
                                     size_t workspace_bytes, void *stream) {
   return full_decode_impl(shape, q, k_codes, k_scales, v_codes, v_scales, true, alpha, c, eps,
                           out, n_surv, sel_scores, sel_hist, workspace, workspace_bytes, stream);
+}
+
+size_t embla_full_decode_select_workspace_size(const embla_shape *shape, int32_t topk,
+                                               int32_t recent) {
+  int G = 0;
+  if (check_shape(shape, &G, true) != EMBLA_OK || topk < 0 || recent < 0) return 0;
+  const int sms = sm_count_of(current_device());
+  if (sms <= 0) return 0;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  return full_workspace_bytes(full_split(units, shape->ctx_len, sms), G) +
+         select_workspace_bytes(units, shape->ctx_len);
+}
+
+embla_status embla_full_decode_select(const embla_shape *shape, const void *q, const void *k_cache,
+                                      const void *v_cache, float alpha, float c, float eps,
+                                      float *out, int32_t *n_surv, float *sel_scores,
+                                      uint32_t *sel_hist, int32_t topk, int32_t recent,
+                                      int32_t *idx, int32_t idx_stride, int32_t *count,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+  const SelectArgs sa = {topk, recent, idx, idx_stride, count};
+  return full_decode_impl(shape, q, k_cache, nullptr, v_cache, nullptr, false, alpha, c, eps, out,
+                          n_surv, sel_scores, sel_hist, workspace, workspace_bytes, stream, nullptr,
+                          nullptr, kMaxPiecesPerCta, &sa);
+}
+
+embla_status embla_full_decode_e4m3_select(const embla_shape *shape, const void *q,
+                                           const uint8_t *k_codes, const float *k_scales,
+                                           const uint8_t *v_codes, const float *v_scales,
+                                           float alpha, float c, float eps, float *out,
+                                           int32_t *n_surv, float *sel_scores, uint32_t *sel_hist,
+                                           int32_t topk, int32_t recent, int32_t *idx,
+                                           int32_t idx_stride, int32_t *count, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+  const SelectArgs sa = {topk, recent, idx, idx_stride, count};
+  return full_decode_impl(shape, q, k_codes, k_scales, v_codes, v_scales, true, alpha, c, eps, out,
+                          n_surv, sel_scores, sel_hist, workspace, workspace_bytes, stream, nullptr,
+                          nullptr, kMaxPiecesPerCta, &sa);
 }
 
 embla_status embla_full_decode_static_scratch(const embla_shape *shape, const void *q,

@@ -1158,7 +1158,8 @@ constexpr int kCombMaxSlices = 8;
 constexpr int kCombLoads = 8;
 template <int G>
 __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel(const FullParams p,
-                                                                                 int dc) {
+                                                                                 int dc,
+                                                                                 int after_select) {
   __shared__ float s_num[kCombMaxSlices][kHeadDim];
   __shared__ float s_den[kCombMaxSlices];
   const int S = static_cast<int>(blockDim.x) / dc;
@@ -1181,11 +1182,17 @@ __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel
   const int parts = static_cast<int>(c1 - c0 + 1);
   const float *rr = p.rec + (c0 + u) * p.rec_stride;
   const int col = h * kHeadDim + d;
-  // The CTA is launched while the decode kernel runs; its first record lines go to L2 (with
-  // their address translations) before the wait: a prefetch reads nothing into the SM.
-  if (sl < parts)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(rr + static_cast<int64_t>(sl) * p.rec_stride + col));
-  pdl_wait_primary();  // every record is written
+  // Right after the decode kernel, the CTA is launched while that kernel runs: its first
+  // record lines go to L2 (with their address translations) before the wait (a prefetch
+  // reads nothing into the SM).  After a selection kernel, the CTA starts only once every
+  // selection CTA has passed its own wait for the decode kernel, so every record is
+  // written already; it runs beside the selection and waits for it only at the end, so
+  // that the kernels after it see the selection finished.  The records are read from L2.
+  if (!after_select) {
+    if (sl < parts)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rr + static_cast<int64_t>(sl) * p.rec_stride + col));
+    pdl_wait_primary();  // every record is written
+  }
   pdl_launch_dependents();
   float num = 0.0f, den = 0.0f;
   for (int k0 = sl; k0 < parts; k0 += S * kCombLoads) {
@@ -1193,8 +1200,9 @@ __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel
 #pragma unroll
     for (int k = 0; k < kCombLoads; ++k) {
       const int kk = k0 + k * S;
-      x[k] = kk < parts ? rr[static_cast<int64_t>(kk) * p.rec_stride + col] : 0.0f;
-      y[k] = kk < parts && dl < 32 ? rr[static_cast<int64_t>(kk) * p.rec_stride + G * kHeadDim + h] : 0.0f;
+      x[k] = kk < parts ? __ldcg(rr + static_cast<int64_t>(kk) * p.rec_stride + col) : 0.0f;
+      y[k] = kk < parts && dl < 32 ? __ldcg(rr + static_cast<int64_t>(kk) * p.rec_stride + G * kHeadDim + h)
+                                   : 0.0f;
     }
 #pragma unroll
     for (int k = 0; k < kCombLoads; ++k) {
@@ -1214,12 +1222,14 @@ __global__ void __launch_bounds__(kHeadDim * kCombMaxSlices) full_combine_kernel
     z += p.c;
     p.out[u * G * kHeadDim + col] = z != 0.0f ? n / z : 0.0f;
   }
+  if (after_select) pdl_wait_primary();  // the selection has finished
 }
 
 template <int G, bool KV8>
 cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_ks, const CUtensorMap &tm_vs,
-                                 const FullParams &p, int64_t units, cudaStream_t stream) {
+                                 const FullParams &p, int64_t units, cudaStream_t stream,
+                                 const SelectJob *sj) {
   const int smem = Smem<G, KV8>::alloc;
   auto kernel = p.K > 1 ? full_decode_kernel<G, KV8, true> : full_decode_kernel<G, KV8, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1234,6 +1244,11 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
   e = launch_pdl(kernel, dim3(static_cast<unsigned>(p.P)), dim3(kThreads),
                  static_cast<size_t>(smem), stream, 0u, tm_k, tm_q, tm_ks, tm_vs, p);
   if (e != cudaSuccess) return e;
+  if (sj) {
+    e = launch_select(p.sel, p.hist, units, p.n, p.ncap, sj->topk, sj->recent, sj->idx,
+                      sj->idx_stride, sj->count, sj->workspace, p.flags, sj->sm_count, stream);
+    if (e != cudaSuccess) return e;
+  }
   // slices: the records of the unit with the most, rounded up to a power of two (at most 8)
   const int64_t most = (p.TU * p.Q + p.T - 1) / p.T + 1;
   int slices = 1;
@@ -1242,7 +1257,7 @@ cudaError_t launch_full_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_
   int dc = kHeadDim;
   while (dc > 32 && units * G * (kHeadDim / dc) < p.P) dc >>= 1;
   return launch_pdl(full_combine_kernel<G>, dim3(static_cast<unsigned>(units * G * (kHeadDim / dc))),
-                    dim3(dc * slices), 0, stream, 0u, p, dc);
+                    dim3(dc * slices), 0, stream, 0u, p, dc, sj ? 1 : 0);
 }
 
 }  // namespace
@@ -1281,8 +1296,9 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const SelectJob *sj) {
   if (sp.tiles == 0) return cudaSuccess;
+  if (sj && (!sel_scores || !sel_hist)) return cudaErrorInvalidValue;
   FullParams p;
   p.v = static_cast<const uint8_t *>(v_cache);
   p.sel = sel_scores;
@@ -1307,13 +1323,13 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
   p.eps = eps;
   if (kv8) {
     if (!tm_ks || !tm_vs) return cudaErrorInvalidValue;
-    if (G == 4) return launch_full_decode_t<4, true>(tm_k, tm_q, *tm_ks, *tm_vs, p, sp.units, stream);
-    if (G == 8) return launch_full_decode_t<8, true>(tm_k, tm_q, *tm_ks, *tm_vs, p, sp.units, stream);
+    if (G == 4) return launch_full_decode_t<4, true>(tm_k, tm_q, *tm_ks, *tm_vs, p, sp.units, stream, sj);
+    if (G == 8) return launch_full_decode_t<8, true>(tm_k, tm_q, *tm_ks, *tm_vs, p, sp.units, stream, sj);
     return cudaErrorInvalidValue;
   }
   // the bf16 kernel does not read the scale maps
-  if (G == 4) return launch_full_decode_t<4, false>(tm_k, tm_q, tm_k, tm_k, p, sp.units, stream);
-  if (G == 8) return launch_full_decode_t<8, false>(tm_k, tm_q, tm_k, tm_k, p, sp.units, stream);
+  if (G == 4) return launch_full_decode_t<4, false>(tm_k, tm_q, tm_k, tm_k, p, sp.units, stream, sj);
+  if (G == 8) return launch_full_decode_t<8, false>(tm_k, tm_q, tm_k, tm_k, p, sp.units, stream, sj);
   return cudaErrorInvalidValue;
 }
 

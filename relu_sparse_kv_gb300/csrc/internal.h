@@ -77,7 +77,19 @@ FullSplit full_split(int64_t units, int64_t ctx_len, int sm_count,
 int full_record_floats(int G);
 size_t full_workspace_bytes(const FullSplit &sp, int G);
 
+// The selection launched between the decode and its combining kernel (launch_select's
+// arguments beyond the scores and histogram): the combining kernel then runs beside it.
+struct SelectJob {
+  int topk, recent;
+  int32_t *idx;
+  int idx_stride;
+  int32_t *count;
+  void *workspace;
+  int sm_count;
+};
+
 // kv8: 8-bit E4M3 caches; tm_ks / tm_vs then map the K and V scales as [units, ncap] fp32.
+// sj (needs sel_scores): also select each unit's keys from the decode's scores.
 cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                const CUtensorMap *tm_ks, const CUtensorMap *tm_vs,
                                const void *v_cache, float *sel_scores, float *head_scores,
@@ -85,7 +97,7 @@ cudaError_t launch_full_decode(int G, bool kv8, const CUtensorMap &tm_k, const C
                                float *out, int32_t *n_surv, float c, uint32_t *flags,
                                const FullSplit &sp, int64_t n,
                                int64_t ncap, int Hq, int Hkv, float alpha, float eps,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const SelectJob *sj = nullptr);
 
 size_t select_workspace_bytes(int64_t units, int64_t ctx_len);
 // hist[u] = 2048-bin counts of the order keys' top 11 bits of scores[u][0..n) (every unit).

@@ -82,6 +82,16 @@ def test_scalar_and_pointer_validation_without_gpu(lib):
     assert w(ctypes.byref(s), None, None, None, 0, 5, 10000.0, 0.1, None, None, 0, None) == 1
     assert w(ctypes.byref(s), None, None, None, 128, -1, 10000.0, 0.1, None, None, 0, None) == 1
     assert w(ctypes.byref(s), None, None, None, 128, 5, 0.0, 0.1, None, None, 0, None) == 1
+    # the decode with its selection: the selection's arguments are checked with the rest
+    fs = lib.embla_full_decode_select
+    a = [ctypes.c_void_p(256 * (k + 1)) for k in range(8)]  # aligned, never dereferenced
+    base = [ctypes.byref(s), a[0], a[1], a[2], 1.0, 1.0, 1e-6, a[3], a[4], a[5], a[6]]
+    assert fs(*base, 1024, 128, a[7], 1000, a[7], a[7], 1 << 20, None) == 1   # stride < topk + recent
+    assert fs(*base, -1, 128, a[7], 1152, a[7], a[7], 1 << 20, None) == 1
+    assert fs(*base, 1024, 128, None, 1152, a[7], a[7], 1 << 20, None) == 1    # no idx
+    assert fs(*base, 1024, 128, a[7], 1152, ctypes.c_void_p(260), a[7], 1 << 20, None) == 1  # count unaligned
+    nosel = base[:9] + [None, None]
+    assert fs(*nosel, 1024, 128, a[7], 1152, a[7], a[7], 1 << 20, None) == 1  # scores required
     st = lib.embla_self_test_wait_limit
     assert st(0, 0, None) == 1  # a limit of 0 or above one second is refused before any launch
     assert st(1000001, 0, None) == 1
@@ -93,6 +103,9 @@ def test_empty_batch_is_a_no_op(lib):
                                  None, None, None, 0, None) == 0
     assert lib.embla_sparse_decode(ctypes.byref(s), None, None, None, None, 1152, None, 0.1,
                                    None, None, 0, None) == 0
+    assert lib.embla_full_decode_select(ctypes.byref(s), None, None, None, 1.0, 1.0, 1e-6, None,
+                                        None, None, None, 1024, 128, None, 1152, None, None, 0,
+                                        None) == 0
 
 
 HARNESS = r"""
@@ -156,7 +169,8 @@ def test_full_decode_work_split_host_logic(tmp_path):
     exe = tmp_path / "split"
     cuda_inc = "/usr/local/cuda/include"
     r = subprocess.run(["g++", "-std=c++17", "-O1", "-I" + B.CSRC, "-I" + cuda_inc, str(src),
-                        os.path.join(B.BUILD, "full_decode.o"), "-o", str(exe),
+                        os.path.join(B.BUILD, "full_decode.o"), os.path.join(B.BUILD, "select.o"),
+                        "-o", str(exe),
                         "-L/usr/local/cuda/lib64", "-lcudart_static", "-ldl", "-lpthread",
                         "-lrt"], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-2000:]

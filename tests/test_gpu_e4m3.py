@@ -136,6 +136,31 @@ def test_e4m3_full_many_units_and_split_boundaries(B, n):
     _check(fl, Run8(fl))
 
 
+@pytest.mark.parametrize("B,n", [(2, 3000), (8, 32768)])
+def test_e4m3_full_decode_select_matches_the_two_calls(B, n):
+    fl = _layer(B, 16, 2, n, frac=0.05, seed=41, sparse=())
+    run = Run8(fl)
+    idx, cnt = run.select()
+    Hq, Hkv, ncap = 16, 2, fl.K.shape[2]
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    ns = torch.full((B, Hkv), -1, dtype=torch.int32, device="cuda")
+    sel = torch.full((B, Hkv, ncap), float("nan"), device="cuda")
+    hist = torch.full((B, Hkv, E.HIST_BINS), -1, dtype=torch.int32, device="cuda")
+    idx2 = torch.full((B, Hkv, 1152), -7, dtype=torch.int32, device="cuda")
+    cnt2 = torch.full((B, Hkv), -1, dtype=torch.int32, device="cuda")
+    E.embla_full_decode_e4m3_select(run.shape, run.q, run.K8, run.Ks, run.V8, run.Vs, out, ns, sel,
+                                    hist, idx2, cnt2)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    assert torch.equal(out, run.out) and torch.equal(ns, run.n_surv)
+    assert torch.equal(sel[..., :fl.n], run.sel[..., :fl.n]) and torch.equal(hist, run.hist)
+    assert np.array_equal(cnt2.cpu().numpy(), cnt)
+    i2 = idx2.cpu().numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            assert np.array_equal(i2[b, g, :cnt[b, g]], idx[b, g, :cnt[b, g]])
+
+
 def test_e4m3_without_selection_outputs():
     fl = _layer(4, 32, 4, 2000, frac=0.1, seed=9)
     run = Run8(fl, with_sel=False)

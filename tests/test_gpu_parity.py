@@ -96,6 +96,61 @@ def test_full_pieces_over_units_of_mixed_survival(tiles_per_cta, n_short):
     _check_full(fl, run)
 
 
+def _fused(run, topk=1024, recent=128):
+    """The decode with its selection in one call, on the inputs of a FullRun."""
+    r = dict(out=torch.full_like(run.out, float("nan")), n_surv=torch.full_like(run.n_surv, -1),
+             sel=torch.full_like(run.sel, float("nan")), hist=torch.full_like(run.hist, -1),
+             idx=torch.full_like(run.idx, -7), count=torch.full_like(run.count, -1))
+    E.embla_full_decode_select(run.shape, run.q, run.K, run.V, r["out"], r["n_surv"], r["sel"],
+                               r["hist"], r["idx"], r["count"], topk=topk, recent=recent)
+    torch.cuda.synchronize()
+    assert E.embla_device_check() == 0
+    return r
+
+
+def _assert_same_as_two_calls(run, r, n):
+    assert torch.equal(r["out"], run.out) and torch.equal(r["n_surv"], run.n_surv)
+    assert torch.equal(r["sel"][..., :n], run.sel[..., :n]) and torch.equal(r["hist"], run.hist)
+    assert torch.equal(r["count"], run.count)
+    cnt = run.count.cpu().numpy()
+    idx_a, idx_b = r["idx"].cpu().numpy(), run.idx.cpu().numpy()
+    for b in range(cnt.shape[0]):
+        for g in range(cnt.shape[1]):
+            assert np.array_equal(idx_a[b, g, :cnt[b, g]], idx_b[b, g, :cnt[b, g]])
+
+
+@pytest.mark.parametrize("B,Hkv,n,frac", [
+    (2, 4, 3000, 0.2),                         # one selection CTA per unit
+    (1, 4, 70001, 0.05),                       # clusters of selection CTAs per unit
+    (5, 4, 532 * 128 - 77, [0.5, 0.2, 0.05, 0.01]),  # several pieces per decode CTA
+    (1, 1, 600001, 0.05),                      # the long-context selection (workspace)
+    (2, 4, 700, 0.3),                          # every key selected
+])
+def test_full_decode_select_matches_the_two_calls(B, Hkv, n, frac):
+    fl = _layer(B, 4 * Hkv, Hkv, n, pattern="subset", frac=frac, seed=31, sparse=())
+    run = FullRun(fl)
+    _assert_same_as_two_calls(run, _fused(run), fl.n)
+
+
+def test_full_decode_select_then_sparse_layers_are_repeatable():
+    # the output is finished beside the selection: the sparse layer after the call must see
+    # the finished selection every time
+    fl = _layer(8, 16, 4, 32768, pattern="subset", frac=0.05, seed=37, sparse=(1,))
+    run = FullRun(fl)
+    ref_sp = run.sparse(fl.sparse_q[0])
+    qs = to_dev(fl.sparse_q[0])
+    r = _fused(run)
+    sp_out = torch.empty_like(run.out)
+    for _ in range(20):
+        E.embla_full_decode_select(run.shape, run.q, run.K, run.V, r["out"], r["n_surv"], r["sel"],
+                                   r["hist"], r["idx"], r["count"])
+        E.embla_sparse_decode(run.shape, qs, run.K, run.V, r["idx"], r["count"], sp_out)
+        torch.cuda.synchronize()
+        assert np.array_equal(sp_out.cpu().numpy(), ref_sp)
+    _assert_same_as_two_calls(run, r, fl.n)
+    assert E.embla_device_check() == 0
+
+
 @pytest.mark.parametrize("B,n,frac", [(8, 32768, 0.05), (16, 8192, 0.5),
                                       (32, 16384, [0.5, 0.2, 0.05, 0.01])])
 def test_full_decode_is_repeatable(B, n, frac):
