@@ -997,12 +997,16 @@ def main():
         side = torch.cuda.Stream(device=dev)
 
         def step_body(i):
-            # the event after a full-layer call is recorded on a side branch of the graph,
-            # so the call's kernel and the next one stay directly chained
+            # the events around a full-layer call are recorded on a side branch of the graph
+            # (it forks after the work before the call, and after the call), so every kernel
+            # stays directly chained to the one before it: the start event fires when the
+            # work before the call has finished, the end event when the call has, and their
+            # difference is the call's share of the step
             def body():
                 for li, L in enumerate(reps[(i or 0) % n_rep]):
                     if i is not None:
-                        ev[i * nl + li][0].record(stream)
+                        side.wait_stream(stream)
+                        ev[i * nl + li][0].record(side)
                     full_call(L)
                     if i is not None:
                         side.wait_stream(stream)
@@ -1239,8 +1243,9 @@ def main():
         "dtype": "e4m3" if layers[0]["fl"].kv == "e4m3" else "bf16",
         "data": "synthetic",
         "config": {**static_config(args.config, args.batch, args.ctx),
-                   "launch": ("one CUDA graph per step; events inside it around each full-layer call "
-                              "(the closing one on a side branch)"
+                   "launch": ("one CUDA graph per step; events inside it around each full-layer call, "
+                              "on a side branch that forks before and after the call (the kernels stay "
+                              "chained): the call's share of the step"
                               if in_graph_events else
                               "two CUDA graphs per full layer (its call, then the rest); events between them"),
                    "l2": ("not flushed: inputs larger than L2 (each full layer's K cache is "
