@@ -69,6 +69,19 @@ def test_static_scratch_matches_workspace_call(B, Hq, n, with_sel):
     _compare(shape, to_dev(fl.q), to_dev(fl.K), to_dev(fl.V), with_sel, alpha=0.7, c=0.5)
 
 
+def test_static_scratch_takes_fewer_pieces_when_the_records_do_not_fit():
+    """1300 units of 12 tiles: on 152 SMs the usual split cuts each CTA's 102 tiles into five
+    pieces, whose records need more than the fixed scratch; the static call takes three
+    pieces instead (its partial sums are grouped differently: the output agrees to within
+    rounding, the counts, scores and histogram exactly)."""
+    B, Hq, n = 325, 16, 1536
+    fl = _layer(29, B, Hq, n, pattern="subset")
+    shape = E.Shape(B, Hq, 4, 128, fl.n, fl.K.shape[2])
+    if E.embla_device_sm_count() == 152:
+        assert E.embla_full_decode_workspace_size(shape) > E.FULL_DECODE_SCRATCH_BYTES
+    _compare(shape, to_dev(fl.q), to_dev(fl.K), to_dev(fl.V), True)
+
+
 def test_static_scratch_size_limit():
     """The largest batch whose workspace fits the fixed scratch runs and matches; one more
     sequence is refused with 'workspace too small' and leaves the outputs untouched."""
