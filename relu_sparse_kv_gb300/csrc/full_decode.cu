@@ -643,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // alpha / sqrt(mean(q_h^2) + eps): 32 / G neighbouring lanes per head, each summing
             // 16-byte chunks of the head's row (the swizzle only permutes chunks within a
             // 128-byte row, which a sum does not see), then every lane takes every head's
+            // factor from that head's first lane
             constexpr int kLanesPerHead = 32 / G, kChunks = 16 / kLanesPerHead;
             static_assert(32 % G == 0 && kChunks * kLanesPerHead == 16, "chunks per lane");
             const int hq = lane / kLanesPerHead, sub = lane % kLanesPerHead;
