@@ -1123,11 +1123,12 @@ def main():
         def e2e_body(k):
             arena_in.copy_(h_in, non_blocking=True)  # every query and appended row: one copy
             for L in reps[k % n_rep]:
-                L["K"][:, :, n - 1].copy_(L["krow"])
-                L["V"][:, :, n - 1].copy_(L["vrow"])
+                # the appended token's rows into the caches (a kernel of the library's)
                 if "Ks" in L:
-                    L["Ks"][:, :, n - 1].copy_(L["ksrow"])
-                    L["Vs"][:, :, n - 1].copy_(L["vsrow"])
+                    E.embla_append_kv_e4m3(L["shape"], n - 1, L["krow"], L["ksrow"], L["vrow"],
+                                           L["vsrow"], L["K"], L["Ks"], L["V"], L["Vs"])
+                else:
+                    E.embla_append_kv(L["shape"], n - 1, L["krow"], L["vrow"], L["K"], L["V"])
                 full_call(L)
                 rest_calls(L)
             window_calls()
@@ -1175,7 +1176,7 @@ def main():
                "eager_launch": "the public API called from Python per step, copies issued "
                                "eagerly, then a host synchronise",
                "inputs": "per step, one copy of every query and the appended token's K/V rows "
-                         "from pinned host memory (then placed into the caches on the device) and "
+                         "from pinned host memory (then written into the caches by embla_append_kv) and "
                          "one copy of every output back; the KV caches stay resident in HBM"}
 
     # one sparse layer (the first of the first block): its marginal cost after a write of twice

@@ -351,6 +351,28 @@ embla_status embla_window_decode(const embla_shape *shape, const void *q, const 
                                  void *stream);
 
 /*
+ * Cache append — the decode step's token written into the caches the calls above
+ * read ("Three kinds of attention": a full layer keeps every token's K and V).
+ * Row `pos` of every (b, g) plane is copied from a packed array of one row per plane:
+ *   k_rows, v_rows     bf16 [B, Hkv, D]   the token's K and V (device memory)
+ *   k_cache, v_cache   bf16 [B, Hkv, cache_stride, D], as for embla_full_decode
+ *   pos                0 <= pos < cache_stride (the token's position, ctx_len - 1 of
+ *                      the decode call that follows); shape->ctx_len is not used
+ * 8-bit caches: the codes and the per-token scales of K and V:
+ *   k_code_rows, v_code_rows   uint8 [B, Hkv, D];   k_codes, v_codes   uint8 [B, Hkv, cache_stride, D]
+ *   k_scale_rows, v_scale_rows fp32 [B, Hkv];       k_scales, v_scales fp32 [B, Hkv, cache_stride]
+ * One kernel per call, launched like every kernel of this library: the call after it may
+ * begin its launch while it runs, and reads nothing before it has finished.  Any
+ * alignment works; 16-byte aligned rows are copied 16 bytes at a time.
+ */
+embla_status embla_append_kv(const embla_shape *shape, int64_t pos, const void *k_rows,
+                             const void *v_rows, void *k_cache, void *v_cache, void *stream);
+embla_status embla_append_kv_e4m3(const embla_shape *shape, int64_t pos, const uint8_t *k_code_rows,
+                                  const float *k_scale_rows, const uint8_t *v_code_rows,
+                                  const float *v_scale_rows, uint8_t *k_codes, float *k_scales,
+                                  uint8_t *v_codes, float *v_scales, void *stream);
+
+/*
  * V-read accounting — "The Architecture of Embla 1", "Skipping V": a value row
  * is read only when some query head of the group gives its key a weight above
  * zero, i.e. when sigma_j > 0; the page's own kernel decides this for groups of

@@ -101,6 +101,8 @@ def library() -> ctypes.CDLL:
                                                              sz, vp]),
             "embla_full_decode_static_scratch": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32,
                                                                 vp, vp, vp, vp, vp]),
+            "embla_append_kv": (ctypes.c_int, [P, i64, vp, vp, vp, vp, vp]),
+            "embla_append_kv_e4m3": (ctypes.c_int, [P, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "embla_full_decode_select_workspace_size": (sz, [P, i32, i32]),
             "embla_full_decode_select": (ctypes.c_int, [P, vp, vp, vp, f32, f32, f32, vp, vp, vp,
                                                         vp, i32, i32, vp, i32, vp, vp, sz, vp]),
@@ -263,6 +265,36 @@ def embla_select_topk(shape: Shape, sel_scores, sel_hist, idx, count, topk: int 
     _call("embla_select_topk", ctypes.byref(shape.c()), _ptr(sel_scores), _ptr(sel_hist), topk,
           recent, _ptr(idx), idx.shape[2], _ptr(count), _ptr(ws), ws.numel() * ws.element_size(),
           _stream(stream))
+
+
+def embla_append_kv(shape: Shape, pos: int, k_rows, v_rows, k_cache, v_cache, stream=None):
+    """Write one token's K and V rows (bf16 [B, Hkv, D]) into row `pos` of every plane of the
+    caches (bf16 [B, Hkv, cache_stride, D])."""
+    B, Hkv, D, ncap = shape.batch, shape.n_kv_heads, shape.head_dim, shape.cache_stride
+    _check(k_rows, torch.bfloat16, (B, Hkv, D), "k_rows")
+    _check(v_rows, torch.bfloat16, (B, Hkv, D), "v_rows")
+    _check(k_cache, torch.bfloat16, (B, Hkv, ncap, D), "k_cache")
+    _check(v_cache, torch.bfloat16, (B, Hkv, ncap, D), "v_cache")
+    _call("embla_append_kv", ctypes.byref(shape.c()), pos, _ptr(k_rows), _ptr(v_rows),
+          _ptr(k_cache), _ptr(v_cache), _stream(stream))
+
+
+def embla_append_kv_e4m3(shape: Shape, pos: int, k_code_rows, k_scale_rows, v_code_rows,
+                         v_scale_rows, k_codes, k_scales, v_codes, v_scales, stream=None):
+    """embla_append_kv for 8-bit caches: the token's E4M3 codes (uint8 [B, Hkv, D]) and scales
+    (float32 [B, Hkv]) into row `pos` of the codes and scale arrays."""
+    B, Hkv, D, ncap = shape.batch, shape.n_kv_heads, shape.head_dim, shape.cache_stride
+    _check(k_code_rows, torch.uint8, (B, Hkv, D), "k_code_rows")
+    _check(v_code_rows, torch.uint8, (B, Hkv, D), "v_code_rows")
+    _check(k_scale_rows, torch.float32, (B, Hkv), "k_scale_rows")
+    _check(v_scale_rows, torch.float32, (B, Hkv), "v_scale_rows")
+    _check(k_codes, torch.uint8, (B, Hkv, ncap, D), "k_codes")
+    _check(v_codes, torch.uint8, (B, Hkv, ncap, D), "v_codes")
+    _check(k_scales, torch.float32, (B, Hkv, ncap), "k_scales")
+    _check(v_scales, torch.float32, (B, Hkv, ncap), "v_scales")
+    _call("embla_append_kv_e4m3", ctypes.byref(shape.c()), pos, _ptr(k_code_rows),
+          _ptr(k_scale_rows), _ptr(v_code_rows), _ptr(v_scale_rows), _ptr(k_codes),
+          _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _stream(stream))
 
 
 def embla_full_decode_select_workspace_size(shape: Shape, topk: int = 1024, recent: int = 128) -> int:

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libembla_attn.so")
 SOURCES = ["embla_attn.cu", "full_decode.cu", "select.cu", "softmax_decode.cu", "skip_stats.cu",
-           "prefill.cu", "relu2_mlp.cu"]
+           "prefill.cu", "relu2_mlp.cu", "append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

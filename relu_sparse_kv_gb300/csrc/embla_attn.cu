@@ -679,6 +679,46 @@ embla_status embla_skip_stats(const embla_shape *shape, const float *sel_scores,
                                        static_cast<cudaStream_t>(stream)));
 }
 
+embla_status embla_append_kv(const embla_shape *shape, int64_t pos, const void *k_rows,
+                             const void *v_rows, void *k_cache, void *v_cache, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, false);
+  if (st != EMBLA_OK) return st;
+  if (shape->cache_stride < 1 || pos < 0 || pos >= shape->cache_stride)
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!k_rows || !v_rows || !k_cache || !v_cache) return EMBLA_ERR_INVALID_ARG;
+  const int64_t rb = 2 * kHeadDim;
+  const AppendJob jobs[2] = {
+      {static_cast<const uint8_t *>(k_rows), static_cast<uint8_t *>(k_cache), rb, shape->cache_stride, 0},
+      {static_cast<const uint8_t *>(v_rows), static_cast<uint8_t *>(v_cache), rb, shape->cache_stride, 0}};
+  return cuda_status(launch_append_rows(jobs, 2, units, pos, static_cast<cudaStream_t>(stream)));
+}
+
+embla_status embla_append_kv_e4m3(const embla_shape *shape, int64_t pos, const uint8_t *k_code_rows,
+                                  const float *k_scale_rows, const uint8_t *v_code_rows,
+                                  const float *v_scale_rows, uint8_t *k_codes, float *k_scales,
+                                  uint8_t *v_codes, float *v_scales, void *stream) {
+  int G = 0;
+  embla_status st = check_shape(shape, &G, false);
+  if (st != EMBLA_OK) return st;
+  if (shape->cache_stride < 1 || pos < 0 || pos >= shape->cache_stride)
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t units = static_cast<int64_t>(shape->batch) * shape->n_kv_heads;
+  if (units == 0) return EMBLA_OK;
+  if (!k_code_rows || !k_scale_rows || !v_code_rows || !v_scale_rows || !k_codes || !k_scales ||
+      !v_codes || !v_scales)
+    return EMBLA_ERR_INVALID_ARG;
+  const int64_t ncap = shape->cache_stride;
+  const AppendJob jobs[4] = {
+      {k_code_rows, k_codes, kHeadDim, ncap, 0},
+      {v_code_rows, v_codes, kHeadDim, ncap, 0},
+      {reinterpret_cast<const uint8_t *>(k_scale_rows), reinterpret_cast<uint8_t *>(k_scales), 4, ncap, 0},
+      {reinterpret_cast<const uint8_t *>(v_scale_rows), reinterpret_cast<uint8_t *>(v_scales), 4, ncap, 0}};
+  return cuda_status(launch_append_rows(jobs, 4, units, pos, static_cast<cudaStream_t>(stream)));
+}
+
 embla_status embla_self_test_wait_limit(uint32_t limit_us, int arrive, void *stream) {
   if (limit_us == 0 || limit_us > 1000000u) return EMBLA_ERR_INVALID_ARG;
   uint32_t *d = flags_ptr();

@@ -108,6 +108,25 @@ cudaError_t launch_select(const float *sel_scores, const uint32_t *sel_hist, int
                           int idx_stride, int32_t *count, void *workspace, uint32_t *flags,
                           int sm_count, cudaStream_t stream);
 
+// Appending a token's rows: for each plane u < units, row_bytes bytes from
+// src + u * row_bytes to dst + (u * cache_stride + pos) * row_bytes.  vec (the copy width,
+// 16, 4 or 1 bytes) is set by the launcher.
+struct AppendJob {
+  const uint8_t *src;
+  uint8_t *dst;
+  int64_t row_bytes;
+  int64_t cache_stride;
+  int vec;
+};
+constexpr int kAppendMaxJobs = 4;
+struct AppendParams {
+  AppendJob job[kAppendMaxJobs];
+  int njobs;
+  int64_t units, pos;
+};
+cudaError_t launch_append_rows(const AppendJob *jobs, int njobs, int64_t units, int64_t pos,
+                               cudaStream_t stream);
+
 size_t sparse_workspace_bytes(int64_t units, int G, int idx_stride);
 // k_scales / v_scales: per-token scales of 8-bit E4M3 caches, or both null for bf16 caches.
 // per_head: one unit per (sequence, query head) with its own selection (G then 1, the

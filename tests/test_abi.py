@@ -92,6 +92,20 @@ def test_scalar_and_pointer_validation_without_gpu(lib):
     assert fs(*base, 1024, 128, a[7], 1152, ctypes.c_void_p(260), a[7], 1 << 20, None) == 1  # count unaligned
     nosel = base[:9] + [None, None]
     assert fs(*nosel, 1024, 128, a[7], 1152, a[7], a[7], 1 << 20, None) == 1  # scores required
+    # the token's rows into the caches: the position must lie inside the cache
+    ap = lib.embla_append_kv
+    assert ap(ctypes.byref(s), -1, a[0], a[1], a[2], a[3], None) == 1
+    assert ap(ctypes.byref(s), 4096, a[0], a[1], a[2], a[3], None) == 1  # pos == cache_stride
+    assert ap(ctypes.byref(s), 5, None, a[1], a[2], a[3], None) == 1
+    assert lib.embla_append_kv_e4m3(ctypes.byref(s), 5, a[0], a[1], a[2], a[3], a[4], a[5],
+                                    a[6], None, None) == 1
+    # the token's rows into the caches: the position must lie inside the cache
+    ap = lib.embla_append_kv
+    assert ap(ctypes.byref(s), -1, a[0], a[1], a[2], a[3], None) == 1
+    assert ap(ctypes.byref(s), 4096, a[0], a[1], a[2], a[3], None) == 1  # pos == cache_stride
+    assert ap(ctypes.byref(s), 5, None, a[1], a[2], a[3], None) == 1
+    assert lib.embla_append_kv_e4m3(ctypes.byref(s), 5, a[0], a[1], a[2], a[3], a[4], a[5],
+                                    a[6], None, None) == 1
     st = lib.embla_self_test_wait_limit
     assert st(0, 0, None) == 1  # a limit of 0 or above one second is refused before any launch
     assert st(1000001, 0, None) == 1
@@ -103,6 +117,8 @@ def test_empty_batch_is_a_no_op(lib):
                                  None, None, None, 0, None) == 0
     assert lib.embla_sparse_decode(ctypes.byref(s), None, None, None, None, 1152, None, 0.1,
                                    None, None, 0, None) == 0
+    assert lib.embla_append_kv(ctypes.byref(s), 0, None, None, None, None, None) == 0
+    assert lib.embla_append_kv(ctypes.byref(s), 0, None, None, None, None, None) == 0
     assert lib.embla_full_decode_select(ctypes.byref(s), None, None, None, 1.0, 1.0, 1e-6, None,
                                         None, None, None, 1024, 128, None, 1152, None, None, 0,
                                         None) == 0
