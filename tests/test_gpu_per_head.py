@@ -21,7 +21,8 @@ D, TOPK, RECENT = 128, 1024, 128
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,n", [(2, 16, 4, 1000), (2, 16, 4, 3000), (1, 16, 2, 40000),
-                                        (3, 32, 4, 5000)])
+                                        (3, 32, 4, 5000),
+                                        (5, 16, 4, 532 * 128 - 77)])  # several pieces per CTA
 def test_per_head_selection_and_sparse(B, Hq, Hkv, n):
     fl = gen.make_full_layer(seed=n + B, layer=0, B=B, Hq=Hq, Hkv=Hkv, D=D, n=n, pattern="subset",
                              frac=0.1, sparse_layers=(1,))
